@@ -1,0 +1,367 @@
+"""Throughput of the RLT hot path on one B300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic
+sequences: state init (H_0), token-parallel encode with memory projection,
+and the batched recurrent decoder over all T positions with teacher-forced
+scoring of every next token (tempered top-k log-probabilities for the replay
+workload).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload small]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Multi-GPU: sequences are sharded by index (each rank its own B sequences,
+weak scaling); there is no collective on the data path, only a barrier and
+a max-over-ranks reduction of the timings.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import rlt_inputs as ri  # noqa: E402
+
+METRIC = "decoder tokens/s (B seqs x steps/s) on 1 B300; % of per-step HBM/TC roofline"
+UNIT = "tokens/s"
+L2_BYTES = 126 * 2 ** 20
+
+
+# ---------------------------------------------------------------------------
+# roofline arithmetic (algorithmic bytes / flops of the decoder)
+
+def decoder_weight_bytes(c) -> int:
+    es = 2 if c.dtype == "bf16" else 4
+    d, f, L, V = c.d, c.d_ffn, c.n_layers, c.vocab
+    return es * (L * (6 * d * d + 3 * d * f) + 2 * d * d + V * d)
+
+
+def xattn_bytes(c, B, t) -> int:
+    """Memory K and V of positions 1..t read by one layer's cross-attention (per step)."""
+    es = 2 if c.dtype == "bf16" else 4
+    return es * B * t * 2 * c.d
+
+
+def step_bytes(c, B, t) -> int:
+    es = 2 if c.dtype == "bf16" else 4
+    n_win = min(c.window, t)
+    swa = es * B * c.n_layers * (n_win - 1 + 1) * 2 * c.d
+    mem = c.n_layers * xattn_bytes(c, B, t)
+    io = B * c.d * 4 * 2 + B * c.d * es + B * 4 * 3
+    return decoder_weight_bytes(c) + swa + mem + io
+
+
+def step_flops(c, B, t) -> int:
+    d, f, L, V = c.d, c.d_ffn, c.n_layers, c.vocab
+    gemm = 2 * B * (L * (6 * d * d + 3 * d * f) + 2 * d * d + V * d)
+    attn = 4 * B * d * L * (min(c.window, t) + t)
+    return gemm + attn
+
+
+def decode_roofline_s(c, B, T, bw, peak) -> float:
+    return sum(max(step_bytes(c, B, t) / bw, step_flops(c, B, t) / peak) for t in range(1, T + 1))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return j["hbm_gbs"] * 1e9, j["bf16_tflops"] * 1e12, "measured"
+    return 6.4e12, 1.8e15, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampling during the timed region
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from recurrent_looped_transformer_rlt_b300 import runner
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = ri.preset(args.workload)
+    c = wl.cfg
+    B, T = wl.B, wl.T
+    # weights: seeded numpy draws (identical on every rank); tokens: this rank's sequences
+    W = ri.make_weights(c, wl.seed)
+    tok = ri.make_tokens(wl, seed=wl.seed + 7919 * rank)
+    prompt = ri.make_splits(wl, seed=wl.seed + 7919 * rank)
+    acts = ri.teacher_actions(tok, 0, T, None if wl.score_prompt else prompt)
+    model = rlt.Model(c, W, device=dev)
+    stream = torch.cuda.current_stream()
+    buf = runner.alloc_buffers(model, B, T)
+    tok_d = torch.from_numpy(tok).to(dev)
+    acts_d = torch.from_numpy(acts).to(dev)
+    out = runner.StepOutputs(torch.empty(B, T, device=dev), torch.empty(B, T, device=dev),
+                             torch.empty(B, T, dtype=torch.int32, device=dev), None)
+    st = rlt.State(model, B)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(tok_dev, act_dev):
+        rlt.rlt_state_init(model.handle, st.c, stream)
+        rlt.rlt_encode(model.handle, tok_dev, B, T, buf.e, buf.mem, buf.ws, buf.ws.numel(), stream)
+        ev_mid.record(stream)
+        rlt.rlt_decode_steps(model.handle, st.c, buf.e, buf.mem, T, T, act_dev, wl.temperature, wl.top_k,
+                             out.logp, out.logp_full, out.argmax, (), None, buf.ws, buf.ws.numel(), stream)
+
+    ev0, ev_mid, ev1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    for _ in range(args.warmup):
+        step(tok_d, acts_d)
+    torch.cuda.synchronize()
+    if rlt.rlt_status(buf.ws, stream) != 0:
+        raise RuntimeError("device status flag set during warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # timed region: K steps, inputs resident in HBM, L2 flushed before each step
+    times, enc_times = [], []
+    launches0 = rlt.rlt_launch_count()
+    timer_on = model.timer_arm(args.kernel_class, 1 << 15) if args.kernel_class else False
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            ev0.record(stream)
+            step(tok_d, acts_d)
+            ev1.record(stream)
+            ev1.synchronize()
+            times.append(ev0.elapsed_time(ev1) / 1e3)
+            enc_times.append(ev0.elapsed_time(ev_mid) / 1e3)
+        torch.cuda.synchronize()
+        barrier()
+    launches = rlt.rlt_launch_count() - launches0
+    kernel_ms = model.timer_read() if timer_on else []
+    if rlt.rlt_status(buf.ws, stream) != 0:
+        raise RuntimeError("device status flag set in the timed region")
+    lp = out.logp.cpu().numpy()
+    assert np.isfinite(lp[acts >= 0]).sum() > 0
+
+    # end to end through the public API: host tokens/actions in, host log-probs out
+    tok_h = torch.from_numpy(tok).pin_memory()
+    acts_h = torch.from_numpy(acts).pin_memory()
+    lp_h = torch.empty(B, T, dtype=torch.float32).pin_memory()
+    tok_e = torch.empty_like(tok_d)
+    acts_e = torch.empty_like(acts_d)
+    e2e = []
+    barrier()
+    for _ in range(args.steps):
+        flush.fill_(1.0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tok_e.copy_(tok_h, non_blocking=True)
+        acts_e.copy_(acts_h, non_blocking=True)
+        step(tok_e, acts_e)
+        lp_h.copy_(out.logp, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e.append(time.perf_counter() - t0)
+    barrier()
+
+    t_step = float(np.mean(times))
+    t_enc = float(np.mean(enc_times))
+    t_e2e = float(np.mean(e2e))
+    if world > 1:
+        v = torch.tensor([t_step, t_enc, t_e2e], device=dev, dtype=torch.float64)
+        dist.all_reduce(v, op=dist.ReduceOp.MAX)
+        t_step, t_enc, t_e2e = v.tolist()
+    res = dict(t_step=t_step, t_enc=t_enc, t_e2e=t_e2e, launches=launches // max(args.steps, 1),
+               clocks=clk.summary(), kernel_ms=kernel_ms, B=B, T=T, wl=wl,
+               h2d=tok.nbytes + acts.nbytes, d2h=B * T * 4)
+    model.close()
+    return res
+
+
+def kernel_roofline(wl, kernel_ms, kernel_class, bw, peak, src):
+    """Roofline object of the timed kernel class from its per-launch CUDA-event durations."""
+    if not kernel_ms:
+        return None
+    c, B, T = wl.cfg, wl.B, wl.T
+    L = c.n_layers
+    if kernel_class == "xattn":
+        # launch j of the timed region: step t = j // L + 1 (steps cycle 1..T per pass)
+        byts = [xattn_bytes(c, B, (j // L) % T + 1) + B * c.d * 4 + B * c.d * 2 for j in range(len(kernel_ms))]
+    else:
+        return None
+    ach = sum(byts) / (sum(kernel_ms) / 1e3)
+    return {"bound": "hbm", "achieved": round(ach / 1e9, 1), "peak": round(bw / 1e9, 1), "unit": "GB/s",
+            "frac": round(ach / bw, 4), "traffic": None, "kernel": "dec_xattn (partial + combine)",
+            "launches": len(kernel_ms), "avg_us": round(1e3 * float(np.mean(kernel_ms)), 2),
+            "peak_source": src}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline / reference arm)
+
+def oracle_sample(wl, budget_s=20.0):
+    """Time the oracle on a bounded sample of the workload: B_sub sequences, full T
+    (or a prefix for the largest configurations).  Returns tokens/s and the sample."""
+    from oracle import rlt_oracle as O
+    c = O.Cfg.of(wl.cfg)
+    B_sub = {"tiny": wl.B, "small": 2, "medium": 1, "refdep": 1, "rlreplay": 1}[wl.name]
+    T_sub = {"tiny": wl.T, "small": wl.T, "medium": 256, "refdep": 32, "rlreplay": wl.T}[wl.name]
+    W = ri.make_weights(wl.cfg, wl.seed)
+    tok = ri.make_tokens(wl, B=B_sub, T=T_sub)
+    acts = ri.teacher_actions(tok, 0, T_sub)
+    t0 = time.perf_counter()
+    O.run_sequence(c, W, tok, acts, wl.temperature, wl.top_k)
+    dt = time.perf_counter() - t0
+    return B_sub * T_sub / dt, f"{B_sub} seq x {T_sub} positions (encode + decode + scoring), float64 numpy", dt
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, rank):
+    wl = ri.preset(args.workload)
+    if rank != 0:
+        return
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        pass
+    vals, dts = [], []
+    sample = ""
+    for _ in range(max(args.steps, 1)):
+        v, sample, dt = oracle_sample(wl)
+        vals.append(v)
+        dts.append(dt)
+    v = float(np.mean(vals))
+    line = {"metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(dts)), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": f"{wl.name}: d={wl.cfg.d} L={wl.cfg.n_layers} B={wl.B} T={wl.T}"},
+            "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="rlt", choices=["rlt", "reference"])
+    ap.add_argument("--workload", default="small", choices=sorted(ri.PRESETS))
+    ap.add_argument("--kernel-class", default="xattn", choices=["xattn", ""])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    r = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        wl, B, T = r["wl"], r["B"], r["T"]
+        bw, peak, src = load_peaks()
+        n_tok = B * T * world
+        value = n_tok / r["t_step"]
+        roof_s = decode_roofline_s(wl.cfg, B, T, bw, peak)
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * r["t_step"], 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.cfg.dtype, "data": "synthetic",
+            "config": {"workload": f"{wl.name}: d={wl.cfg.d} L_E=L_D={wl.cfg.n_layers} H={wl.cfg.n_heads}"
+                                   f"x{wl.cfg.head_dim} f={wl.cfg.d_ffn} W={wl.cfg.window} G={wl.cfg.mem_groups}"
+                                   f" V={wl.cfg.vocab}",
+                       "B_per_gpu": B, "T": T, "global_batch": B * world, "parallelism": f"replicas{world}",
+                       "l2": "flushed before every timed step (256 MB write)"},
+            "decode_ms": round(1e3 * (r["t_step"] - r["t_enc"]), 3),
+            "encode_ms": round(1e3 * r["t_enc"], 3),
+            "decode_roofline_ms": round(1e3 * roof_s, 3),
+            "decode_roofline_frac": round(roof_s / (r["t_step"] - r["t_enc"]), 4),
+            "roofline": kernel_roofline(wl, r["kernel_ms"], args.kernel_class, bw, peak, src),
+            "e2e": {"value": round(n_tok / r["t_e2e"], 1), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": int(r["launches"]),
+            "clocks": r["clocks"],
+        }
+        if not args.no_cpu_baseline:
+            v, sample, _ = oracle_sample(wl)
+            line["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                                    "sample": sample}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

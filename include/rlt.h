@@ -1,0 +1,207 @@
+/*
+ * rlt.h -- C ABI of the B300 implementation of the Recurrent Looped
+ * Transformer (RLT) hot path: the causal encoder with memory projection (the
+ * producer) and the batched recurrent decoder transition with its scoring head.
+ *
+ * Sources (page title, section):
+ *  - "Understanding and Applying the Recurrent Looped Transformer
+ *    Architecture", "How the Architecture Works": H_t = (s_t, C_t^D),
+ *    H_0 = (s_*, empty), (s_t, C_t^D) = D_phi(Merge(e_t, s_{t-1}), M_<=t,
+ *    C_{t-1}^D, t), p(x_{t+1} | x_{1:t}) = softmax(W_o RMSNorm_o(s_t));
+ *    "Three forms of context" (window W includes the current token,
+ *    cross-attention reads memory through the current position);
+ *    "Basic Usage" (prompt prefill = parallel encode, then recur through every
+ *    prompt token); "Current-Policy Reinforcement Learning Replay" (score an
+ *    action before consuming it; temperature and truncation in the behaviour
+ *    log-probability; caches are stale after a weight update).
+ *  - "Princeton Researcher Proposes Recurrent Looped Transformer to Carry
+ *    Decoder State Across Tokens", architecture and design-principle
+ *    paragraphs (token-parallel encoder and memory projection in G groups,
+ *    tied encoder/decoder weights, decoder sequential in t and batched across
+ *    independent sequences, Proposition 3.1: the prompt/response split does
+ *    not change the state).
+ *
+ * Conventions
+ *  - All tensors are caller-owned device memory (PyTorch allocates them); the
+ *    library borrows the pointers for the duration of a call and allocates no
+ *    device memory.  Every call is asynchronous on the given CUDA stream.
+ *  - Matrices are row-major W[out][in] (y = x W^T).  "dtype" below is float32
+ *    when config.dtype == RLT_F32 and bfloat16 when RLT_BF16; norm gains, the
+ *    gate bias and s_* are always float32.  Pointers must be 16-byte aligned.
+ *  - Per-layer tensors are stacked on a leading layer axis L = n_layers
+ *    (L_E = L_D; encoder layer l and decoder layer l share W_qkv, W_O, W_1,
+ *    W_3, W_2).
+ *  - Return values: RLT_OK (0) or a negative RLT_E* code.  The library never
+ *    aborts, traps or exits.  Device-side conditions (a bounded wait that gave
+ *    up, an out-of-range token id) are recorded in a flag inside the workspace
+ *    and read with rlt_status().
+ */
+#ifndef RLT_H_
+#define RLT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(RLT_BUILD)
+#define RLT_API __attribute__((visibility("default")))
+#else
+#define RLT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* rlt_stream_t;   /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+  RLT_OK = 0,
+  RLT_EINVAL = -1,      /* bad argument: null pointer, shape, alignment, config */
+  RLT_ESTALE = -2,      /* state.version differs from the model's version */
+  RLT_ERANGE = -3,      /* state.pos + n exceeds the encoded length T_mem */
+  RLT_ECUDA = -4,       /* a CUDA runtime call or launch failed */
+  RLT_ETIMEOUT = -5,    /* device flag: a bounded wait gave up */
+  RLT_EBOUNDS = -6,     /* device flag: an index (token or action id) was out of range */
+  RLT_EWORKSPACE = -7,  /* workspace smaller than rlt_workspace_size() */
+  RLT_EUNSUPPORTED = -8 /* shape outside what the kernels are built for */
+};
+
+enum { RLT_F32 = 0, RLT_BF16 = 1 };
+enum { RLT_GATE_LEARNED = 0, RLT_GATE_DISCARD_S = 1 };
+
+/* Model shape.  d_model = n_heads * head_dim; head_dim even and <= 128;
+ * mem_groups is 1 (memory shared by all decoder layers) or n_layers (one
+ * group per layer).  gate_mode RLT_GATE_DISCARD_S forces the merge gate z to
+ * 0 (u_t = e_t) and exists for the equivalence checks; RLT_GATE_LEARNED is
+ * z = sigmoid(W_g [e_t; s_{t-1}] + b_g), u_t = z * s_{t-1} + (1 - z) * e_t. */
+typedef struct rlt_config {
+  int32_t d_model, n_layers, n_heads, head_dim, d_ffn, window, mem_groups, vocab;
+  int32_t dtype;          /* RLT_F32 or RLT_BF16 */
+  float rms_eps;          /* RMSNorm: x / sqrt(mean(x^2) + eps) * g */
+  float rope_theta;       /* rotate-half RoPE base on encoder and decoder self-attention */
+  int32_t gate_mode;
+} rlt_config;
+
+/* Weights: device pointers, borrowed for the model's lifetime (the caller
+ * keeps them alive and calls rlt_model_set_version after changing them). */
+typedef struct rlt_weights {
+  const void* tok_emb;          /* [V][d]        dtype   token embedding */
+  const float* s_star;          /* [d]           f32     learned start state s_* */
+  const void* W_g;              /* [d][2d]       dtype   merge gate, input [e_t; s_{t-1}] */
+  const float* b_g;             /* [d]           f32     merge gate bias */
+  const void* W_qkv;            /* [L][3d][d]    dtype   rows [q; k; v], head-major (tied) */
+  const void* W_O;              /* [L][d][d]     dtype   self-attention output (tied) */
+  const void* W_1;              /* [L][f][d]     dtype   SwiGLU gate branch (tied) */
+  const void* W_3;              /* [L][f][d]     dtype   SwiGLU linear branch (tied) */
+  const void* W_2;              /* [L][d][f]     dtype   SwiGLU down projection (tied) */
+  const void* W_Qx;             /* [L][d][d]     dtype   cross-attention query (decoder only) */
+  const void* W_Ox;             /* [L][d][d]     dtype   cross-attention output (decoder only) */
+  const void* W_K;              /* [G][d][d]     dtype   memory key projection per group */
+  const void* W_V;              /* [G][d][d]     dtype   memory value projection per group */
+  const void* W_o;              /* [V][d]        dtype   output head */
+  const float* enc_attn_norm;   /* [L][d] */
+  const float* enc_ffn_norm;    /* [L][d] */
+  const float* enc_norm;        /* [d]   final encoder norm producing e */
+  const float* dec_attn_norm;   /* [L][d] */
+  const float* dec_xattn_norm;  /* [L][d] */
+  const float* dec_ffn_norm;    /* [L][d] */
+  const float* head_norm;       /* [d]   RMSNorm_o */
+} rlt_weights;
+
+/* Recurrent state H_t = (s_t, C_t^D) of B sequences advancing in lockstep.
+ * All device buffers are caller-owned.  ring_k/ring_v hold the per-layer SWA
+ * cache as a ring of W slots: entry of position p (0-based) lives in slot
+ * p mod W, after RoPE for keys.  pos and version are host-side fields the
+ * library reads and updates. */
+typedef struct rlt_state {
+  int32_t batch;          /* B */
+  int32_t pos;            /* tokens consumed so far (t of s_t) */
+  uint64_t version;       /* model version the state was built under */
+  float* s;               /* [B][d]              f32    s_t */
+  void* ring_k;           /* [L][B][H][W][hd]    dtype  keys after RoPE */
+  void* ring_v;           /* [L][B][H][W][hd]    dtype  values */
+} rlt_state;
+
+typedef struct rlt_model rlt_model;   /* opaque host object */
+
+/* Validates the config and weight pointers and keeps them.  Creates host-side
+ * resources only (a capture stream, graph cache); no device allocation. */
+RLT_API int rlt_model_create(const rlt_config* cfg, const rlt_weights* w, uint64_t version,
+                     rlt_model** out);
+/* Declares that the weights changed: every state built earlier becomes stale
+ * (rlt_decode_steps then returns RLT_ESTALE). */
+RLT_API int rlt_model_set_version(rlt_model* m, uint64_t version);
+RLT_API void rlt_model_destroy(rlt_model* m);
+
+/* Bytes of workspace rlt_encode / rlt_decode_steps need for B sequences of up
+ * to T_max positions.  The workspace also holds the device status flag.  A
+ * workspace serves one call at a time (calls that share it must be ordered
+ * on one stream). */
+RLT_API int rlt_workspace_size(const rlt_model* m, int32_t B, int32_t T_max, size_t* bytes);
+/* Clears the device status flag of a fresh workspace (call once after
+ * allocating it, before the first rlt_encode / rlt_decode_steps). */
+RLT_API int rlt_workspace_init(void* ws, size_t ws_bytes, rlt_stream_t stream);
+/* Byte sizes of the state buffers (s, each of ring_k / ring_v) for B sequences. */
+RLT_API int rlt_state_sizes(const rlt_model* m, int32_t B, size_t* s_bytes, size_t* ring_bytes);
+
+/* H_0: s = s_* for every sequence, ring slots filled with NaN (never read
+ * before written), pos = 0, version = model version. */
+RLT_API int rlt_state_init(const rlt_model* m, rlt_state* st, rlt_stream_t stream);
+
+/* Token-parallel causal encoder and memory projection over positions 0..T-1:
+ *   tokens [B][T] int32 (device), e [B][T][d] dtype,
+ *   mem [G][2][B][H][T][hd] dtype (index 0 keys, 1 values; no RoPE).
+ * Memory depends only on the tokens. */
+RLT_API int rlt_encode(const rlt_model* m, const int32_t* tokens, int32_t B, int32_t T,
+               void* e, void* mem, void* ws, size_t ws_bytes, rlt_stream_t stream);
+
+/* Advances every sequence of st by n tokens: for i in 0..n-1 the token at
+ * position p = st->pos + i is consumed (step t = p + 1, reading e[:, p] and
+ * memory positions 0..p), then the head scores actions[b][i], the token that
+ * follows, before it is consumed:
+ *   logp[b][i]      = l_a/T - LSE_topk(l/T)   (-inf if a is outside the top-k;
+ *                     top_k = 0 means no truncation)
+ *   logp_full[b][i] = l_a/T - LSE(l/T)
+ *   argmax[b][i]    = argmax_v l_v (lowest id on ties)
+ * where l = W_o RMSNorm_o(s_t) and T = temperature.  An action < 0 gives NaN.
+ * Any output pointer may be NULL.  emit_steps (HOST array, n_emit entries,
+ * each in [0, n)) selects steps whose logits are written to
+ * logits[n_emit][B][V] (f32).  e is [B][T_mem][d], mem [G][2][B][H][T_mem][hd].
+ * Requires st->pos + n <= T_mem and st->version == model version.  Splitting
+ * n across calls gives bit-identical results (Proposition 3.1). */
+RLT_API int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, const void* mem,
+                     int32_t T_mem, int32_t n, const int32_t* actions, float temperature,
+                     int32_t top_k, float* logp, float* logp_full, int32_t* argmax,
+                     const int32_t* emit_steps, int32_t n_emit, float* logits,
+                     void* ws, size_t ws_bytes, rlt_stream_t stream);
+
+/* Synchronises the stream, returns the device status recorded in the workspace
+ * (RLT_OK, RLT_ETIMEOUT or RLT_EBOUNDS) and clears it. */
+RLT_API int rlt_status(void* ws, rlt_stream_t stream);
+
+RLT_API const char* rlt_strerror(int code);
+
+/* Per-launch timing of one kernel class inside rlt_decode_steps, with CUDA
+ * events recorded on the launching stream (event-record nodes of the captured
+ * step, re-pointed to fresh events on every replay).  rlt_timer_arm enables it
+ * for up to max_launches launches; rlt_timer_read synchronises the device,
+ * writes the per-launch durations in milliseconds (in launch order) and
+ * disarms.  Classes: RLT_TIMER_XATTN (cross-attention, partial + combine),
+ * RLT_TIMER_SWA, RLT_TIMER_GEMM (every decoder GEMM), RLT_TIMER_HEAD (norm,
+ * head GEMM and log-softmax reduction), RLT_TIMER_STEP (a whole step). */
+enum { RLT_TIMER_OFF = 0, RLT_TIMER_XATTN = 1, RLT_TIMER_SWA = 2, RLT_TIMER_GEMM = 3,
+       RLT_TIMER_HEAD = 4, RLT_TIMER_STEP = 5 };
+RLT_API int rlt_timer_arm(rlt_model* m, int32_t kernel_class, int32_t max_launches);
+RLT_API int rlt_timer_read(rlt_model* m, float* ms, int32_t cap, int32_t* n_out);
+
+/* Number of kernels this library has enqueued in this process (graph nodes
+ * count once per graph launch). */
+RLT_API uint64_t rlt_launch_count(void);
+
+/* ABI version of this header (major * 100 + minor). */
+RLT_API int rlt_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RLT_H_ */

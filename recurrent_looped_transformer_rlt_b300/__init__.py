@@ -1,0 +1,288 @@
+"""Python binding of librlt.so, the B300 implementation of the RLT hot path.
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels.  The functions keep the C names (rlt_model_create, rlt_state_init,
+rlt_encode, rlt_decode_steps, ...) and take torch tensors or raw pointers.
+PyTorch provides the device memory and the stream.  There is no CPU path:
+if the library is missing, importing this package raises.
+
+Helpers ``Model`` and ``State`` hold the torch tensors behind the C structs
+so that their pointers stay valid.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librlt.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"librlt.so not built at {LIB_PATH}: run "
+                      "`python recurrent_looped_transformer_rlt_b300/build.py` (needs nvcc)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+RLT_OK, RLT_EINVAL, RLT_ESTALE, RLT_ERANGE, RLT_ECUDA = 0, -1, -2, -3, -4
+RLT_ETIMEOUT, RLT_EBOUNDS, RLT_EWORKSPACE, RLT_EUNSUPPORTED = -5, -6, -7, -8
+RLT_F32, RLT_BF16 = 0, 1
+RLT_GATE_LEARNED, RLT_GATE_DISCARD_S = 0, 1
+
+_p = ctypes.c_void_p
+_i32 = ctypes.c_int32
+
+
+class rlt_config(ctypes.Structure):
+    _fields_ = [("d_model", _i32), ("n_layers", _i32), ("n_heads", _i32), ("head_dim", _i32),
+                ("d_ffn", _i32), ("window", _i32), ("mem_groups", _i32), ("vocab", _i32),
+                ("dtype", _i32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+                ("gate_mode", _i32)]
+
+
+WEIGHT_FIELDS = ["tok_emb", "s_star", "W_g", "b_g", "W_qkv", "W_O", "W_1", "W_3", "W_2", "W_Qx",
+                 "W_Ox", "W_K", "W_V", "W_o", "enc_attn_norm", "enc_ffn_norm", "enc_norm",
+                 "dec_attn_norm", "dec_xattn_norm", "dec_ffn_norm", "head_norm"]
+
+
+class rlt_weights(ctypes.Structure):
+    _fields_ = [(n, _p) for n in WEIGHT_FIELDS]
+
+
+class rlt_state(ctypes.Structure):
+    _fields_ = [("batch", _i32), ("pos", _i32), ("version", ctypes.c_uint64), ("s", _p),
+                ("ring_k", _p), ("ring_v", _p)]
+
+
+def _sig(name, res, args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = args
+    return f
+
+
+_model_create = _sig("rlt_model_create", ctypes.c_int,
+                     [ctypes.POINTER(rlt_config), ctypes.POINTER(rlt_weights), ctypes.c_uint64,
+                      ctypes.POINTER(_p)])
+_model_set_version = _sig("rlt_model_set_version", ctypes.c_int, [_p, ctypes.c_uint64])
+_model_destroy = _sig("rlt_model_destroy", None, [_p])
+_workspace_size = _sig("rlt_workspace_size", ctypes.c_int, [_p, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)])
+_workspace_init = _sig("rlt_workspace_init", ctypes.c_int, [_p, ctypes.c_size_t, _p])
+_state_sizes = _sig("rlt_state_sizes", ctypes.c_int,
+                    [_p, _i32, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)])
+_state_init = _sig("rlt_state_init", ctypes.c_int, [_p, ctypes.POINTER(rlt_state), _p])
+_encode = _sig("rlt_encode", ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _p, ctypes.c_size_t, _p])
+_decode_steps = _sig("rlt_decode_steps", ctypes.c_int,
+                     [_p, ctypes.POINTER(rlt_state), _p, _p, _i32, _i32, _p, ctypes.c_float, _i32, _p, _p,
+                      _p, ctypes.POINTER(_i32), _i32, _p, _p, ctypes.c_size_t, _p])
+_status = _sig("rlt_status", ctypes.c_int, [_p, _p])
+_timer_arm = _sig("rlt_timer_arm", ctypes.c_int, [_p, _i32, _i32])
+_timer_read = _sig("rlt_timer_read", ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_float), _i32, ctypes.POINTER(_i32)])
+_strerror = _sig("rlt_strerror", ctypes.c_char_p, [ctypes.c_int])
+_launch_count = _sig("rlt_launch_count", ctypes.c_uint64, [])
+_abi_version = _sig("rlt_abi_version", ctypes.c_int, [])
+
+EXPORTED = ["rlt_model_create", "rlt_model_set_version", "rlt_model_destroy", "rlt_workspace_size",
+            "rlt_workspace_init", "rlt_state_sizes", "rlt_state_init", "rlt_encode", "rlt_decode_steps",
+            "rlt_status", "rlt_strerror", "rlt_launch_count", "rlt_abi_version", "rlt_timer_arm",
+            "rlt_timer_read"]
+RLT_TIMER_CLASSES = {"off": 0, "xattn": 1, "swa": 2, "gemm": 3, "head": 4, "step": 5}
+
+
+class RLTError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {rlt_strerror(code)} ({code})")
+        self.code = code
+
+
+def _check(rc: int, where: str):
+    if rc != RLT_OK:
+        raise RLTError(rc, where)
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def rlt_strerror(code: int) -> str:
+    return _strerror(code).decode()
+
+
+def rlt_launch_count() -> int:
+    return int(_launch_count())
+
+
+def rlt_abi_version() -> int:
+    return int(_abi_version())
+
+
+# ---------------------------------------------------------------------------
+# thin wrappers with the C names
+
+def rlt_model_create(cfg: rlt_config, weights: rlt_weights, version: int = 0) -> int:
+    h = _p()
+    _check(_model_create(ctypes.byref(cfg), ctypes.byref(weights), version, ctypes.byref(h)), "rlt_model_create")
+    return h.value
+
+
+def rlt_model_set_version(model: int, version: int):
+    _check(_model_set_version(model, version), "rlt_model_set_version")
+
+
+def rlt_model_destroy(model: int):
+    _model_destroy(model)
+
+
+def rlt_workspace_size(model: int, B: int, T_max: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_workspace_size(model, B, T_max, ctypes.byref(n)), "rlt_workspace_size")
+    return n.value
+
+
+def rlt_workspace_init(ws, nbytes: int, stream=None):
+    _check(_workspace_init(_ptr(ws), nbytes, _stream_ptr(stream)), "rlt_workspace_init")
+
+
+def rlt_state_sizes(model: int, B: int):
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(_state_sizes(model, B, ctypes.byref(a), ctypes.byref(b)), "rlt_state_sizes")
+    return a.value, b.value
+
+
+def rlt_state_init(model: int, st: rlt_state, stream=None):
+    _check(_state_init(model, ctypes.byref(st), _stream_ptr(stream)), "rlt_state_init")
+
+
+def rlt_encode(model: int, tokens, B: int, T: int, e, mem, ws, ws_bytes: int, stream=None):
+    _check(_encode(model, _ptr(tokens), B, T, _ptr(e), _ptr(mem), _ptr(ws), ws_bytes, _stream_ptr(stream)),
+           "rlt_encode")
+
+
+def rlt_decode_steps(model: int, st: rlt_state, e, mem, T_mem: int, n: int, actions=None,
+                     temperature: float = 1.0, top_k: int = 0, logp=None, logp_full=None, argmax=None,
+                     emit_steps: Sequence[int] = (), logits=None, ws=None, ws_bytes: int = 0, stream=None,
+                     check: bool = True) -> int:
+    ne = len(emit_steps)
+    arr = (_i32 * max(ne, 1))(*emit_steps)
+    rc = _decode_steps(model, ctypes.byref(st), _ptr(e), _ptr(mem), T_mem, n, _ptr(actions), float(temperature),
+                       top_k, _ptr(logp), _ptr(logp_full), _ptr(argmax), arr if ne else None, ne, _ptr(logits),
+                       _ptr(ws), ws_bytes, _stream_ptr(stream))
+    if check:
+        _check(rc, "rlt_decode_steps")
+    return rc
+
+
+def rlt_status(ws, stream=None) -> int:
+    return int(_status(_ptr(ws), _stream_ptr(stream)))
+
+
+def rlt_timer_arm(model: int, kernel_class: int, max_launches: int):
+    _check(_timer_arm(model, kernel_class, max_launches), "rlt_timer_arm")
+
+
+def rlt_timer_read(model: int, cap: int):
+    buf = (ctypes.c_float * max(cap, 1))()
+    n = _i32()
+    _check(_timer_read(model, buf, cap, ctypes.byref(n)), "rlt_timer_read")
+    return [float(buf[i]) for i in range(min(n.value, cap))]
+
+
+# ---------------------------------------------------------------------------
+# torch-side holders
+
+def make_config(c, gate_mode: Optional[int] = None) -> rlt_config:
+    """rlt_config from any object with the fields of rlt_inputs.RLTConfig."""
+    return rlt_config(c.d, c.n_layers, c.n_heads, c.head_dim, c.d_ffn, c.window, c.mem_groups, c.vocab,
+                      RLT_BF16 if c.dtype == "bf16" else RLT_F32, c.rms_eps, c.rope_theta,
+                      c.gate_mode if gate_mode is None else gate_mode)
+
+
+class Model:
+    """Device weights (torch tensors) plus the library's model handle."""
+
+    MATRICES = {"tok_emb", "W_g", "W_qkv", "W_O", "W_1", "W_3", "W_2", "W_Qx", "W_Ox", "W_K", "W_V", "W_o"}
+
+    def __init__(self, cfg, weights: Dict[str, object], device="cuda", version: int = 1):
+        import torch
+        self.cfg = cfg
+        self.dtype = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+        self.t = {}
+        for name in WEIGHT_FIELDS:
+            w = weights[name]
+            if not isinstance(w, torch.Tensor):
+                w = torch.from_numpy(w)
+            dt = self.dtype if name in self.MATRICES else torch.float32
+            self.t[name] = w.to(device=device, dtype=dt).contiguous()
+        self.cstruct = rlt_weights(*[self.t[n].data_ptr() for n in WEIGHT_FIELDS])
+        self.ccfg = make_config(cfg)
+        self.handle = rlt_model_create(self.ccfg, self.cstruct, version)
+        self.version = version
+
+    def set_version(self, v: int):
+        rlt_model_set_version(self.handle, v)
+        self.version = v
+
+    def timer_arm(self, kernel_class: str, max_launches: int) -> bool:
+        rlt_timer_arm(self.handle, RLT_TIMER_CLASSES[kernel_class], max_launches)
+        self._timer_cap = max_launches
+        return True
+
+    def timer_read(self):
+        return rlt_timer_read(self.handle, self._timer_cap)
+
+    def workspace(self, B: int, T_max: int, stream=None):
+        import torch
+        n = rlt_workspace_size(self.handle, B, T_max)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        rlt_workspace_init(ws, n, stream)
+        return ws
+
+    def close(self):
+        if self.handle:
+            rlt_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class State:
+    """Caller-owned state tensors of B sequences plus the C struct over them."""
+
+    def __init__(self, model: Model, B: int):
+        import torch
+        c = model.cfg
+        self.s = torch.empty(B, c.d, dtype=torch.float32, device="cuda")
+        shape = (c.n_layers, B, c.n_heads, c.window, c.head_dim)
+        self.ring_k = torch.empty(shape, dtype=model.dtype, device="cuda")
+        self.ring_v = torch.empty(shape, dtype=model.dtype, device="cuda")
+        self.c = rlt_state(B, 0, 0, self.s.data_ptr(), self.ring_k.data_ptr(), self.ring_v.data_ptr())
+
+    @property
+    def pos(self) -> int:
+        return self.c.pos
+
+    def clone(self) -> "State":
+        other = State.__new__(State)
+        other.s = self.s.clone()
+        other.ring_k = self.ring_k.clone()
+        other.ring_v = self.ring_v.clone()
+        other.c = rlt_state(self.c.batch, self.c.pos, self.c.version, other.s.data_ptr(),
+                            other.ring_k.data_ptr(), other.ring_v.data_ptr())
+        return other

@@ -1,0 +1,55 @@
+// Common device helpers for the RLT kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace rlt {
+
+using bf16 = __nv_bfloat16;
+
+// Storage-type conversions.  bf16 rounding is round-to-nearest-even
+// (__float2bfloat16_rn), the only rounding the bf16 configurations use.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+// Round an fp32 value through the storage type (identity for fp32).
+template <typename T> __device__ __forceinline__ float round_st(float x) { return to_f32(from_f32<T>(x)); }
+
+template <typename T> __device__ __forceinline__ T nan_of();
+template <> __device__ __forceinline__ float nan_of<float>() { return __int_as_float(0x7fc00000); }
+template <> __device__ __forceinline__ bf16 nan_of<bf16>() { return __ushort_as_bfloat16((unsigned short)0x7fc0); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Device status flag (first word of the workspace).  The first error wins.
+__device__ __forceinline__ void set_error(int* flag, int code) { atomicCAS(flag, 0, code); }
+
+// Status codes mirrored from rlt.h for device code.
+constexpr int kErrTimeout = -5;
+constexpr int kErrBounds = -6;
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+// Step context read by the per-step kernels so that one captured step can be
+// replayed: pos = position consumed by this step (0-based), step = index of
+// the step inside the current call.
+struct StepCtx {
+  int pos;
+  int step;
+};
+
+}  // namespace rlt

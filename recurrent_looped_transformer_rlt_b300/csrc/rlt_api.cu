@@ -1,0 +1,694 @@
+// C ABI of the RLT hot path (declared in include/rlt.h).
+//
+// Host side: argument validation, workspace layout, the token-parallel
+// encoder pass, and the decoder step, which is captured once per call as a
+// CUDA graph and replayed n times (every per-step kernel reads the position
+// and step index from a small context in the workspace).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "../../include/rlt.h"
+#include "common.cuh"
+#include "gemm_simple.cuh"
+#include "kernels.cuh"
+
+using namespace rlt;
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+#define RLT_CUDA_TRY(x)                         \
+  do {                                          \
+    cudaError_t e_ = (x);                       \
+    if (e_ != cudaSuccess) return RLT_ECUDA;    \
+  } while (0)
+
+inline int launch_ok() { return cudaGetLastError() == cudaSuccess ? RLT_OK : RLT_ECUDA; }
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline unsigned cdiv(size_t a, size_t b) { return (unsigned)((a + b - 1) / b); }
+
+}  // namespace
+
+// Per-launch timing of one kernel class (see rlt_timer_arm).
+struct KernelTimer {
+  int cls = RLT_TIMER_OFF;
+  int cap = 0;                       // event pairs available
+  int used = 0;                      // pairs recorded so far
+  std::vector<cudaEvent_t> ev;       // [2 * cap]: start, stop, start, stop, ...
+  std::vector<cudaEvent_t> ph;       // placeholders bound at capture time
+  std::vector<cudaGraphNode_t> nodes;  // captured event-record nodes of the current step graph
+};
+
+struct rlt_model {
+  rlt_config cfg;
+  rlt_weights w;
+  uint64_t version;
+  cudaStream_t cap_stream;
+  size_t esz;  // bytes per stored element
+  KernelTimer* timer;
+};
+
+// ---------------------------------------------------------------------------
+// workspace layout
+
+namespace {
+
+struct WsLayout {
+  size_t status, ctx, emit, rope;       // header
+  // decoder
+  size_t d_h, d_x, d_c, d_o, d_part;
+  // encoder
+  size_t e_h, e_a, e_c, e_q, e_k, e_v, e_o;
+  size_t total;
+  int n_chunks;
+};
+
+WsLayout layout(const rlt_model* m, int B, int T) {
+  const rlt_config& c = m->cfg;
+  const size_t d = c.d_model, f = c.d_ffn, V = c.vocab, H = c.n_heads, hd = c.head_dim;
+  const size_t es = m->esz;
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.status = take(sizeof(int) * 4);
+  L.ctx = take(sizeof(StepCtx));
+  L.emit = take(sizeof(int) * (size_t)T);
+  L.rope = take(sizeof(float2) * (size_t)T * (hd / 2));
+  const size_t common_end = off;
+  // decoder region
+  L.n_chunks = (int)cdiv(T, kXChunk);
+  size_t cmax = std::max(std::max(3 * d, 2 * f), std::max(V, 2 * d));
+  L.d_h = take(4 * (size_t)B * d);
+  L.d_x = take(es * (size_t)B * std::max(2 * d, f));
+  L.d_c = take(4 * (size_t)B * cmax);
+  L.d_o = take(es * (size_t)B * d);
+  L.d_part = take(4 * (size_t)B * H * L.n_chunks * (hd + 2));
+  const size_t dec_end = off;
+  // encoder region overlaps the decoder region (one call at a time per workspace)
+  off = common_end;
+  const size_t R = (size_t)B * T;
+  L.e_h = take(4 * R * d);
+  L.e_a = take(es * R * std::max(d, f));
+  L.e_c = take(4 * R * std::max(3 * d, 2 * f));
+  L.e_q = take(es * R * d);
+  L.e_k = take(es * R * d);
+  L.e_v = take(es * R * d);
+  L.e_o = take(es * R * d);
+  const size_t enc_end = off;
+  L.total = std::max(dec_end, enc_end);
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ---------------------------------------------------------------------------
+// launch helpers
+
+template <typename T_, class Epi>
+int gemm(cudaStream_t st, const T_* A, int lda, GemmB gb, int M, int N, int K, Epi epi) {
+  if (M <= 0 || N <= 0) return RLT_OK;
+  if constexpr (std::is_same<T_, bf16>::value) {
+    dim3 grid(cdiv(N, mma_v0::BN), cdiv(M, mma_v0::BM));
+    mma_v0::gemm_bf16_kernel<Epi><<<grid, mma_v0::THREADS, mma_v0::smem_bytes(), st>>>(A, lda, gb, M, N, K, epi);
+  } else {
+    dim3 grid(cdiv(N, simt_v0::BN), cdiv(M, simt_v0::BM));
+    simt_v0::gemm_f32_kernel<Epi><<<grid, simt_v0::THREADS, 0, st>>>(A, lda, gb, M, N, K, epi);
+  }
+  g_launches++;
+  return launch_ok();
+}
+
+template <typename T_>
+int rmsnorm(cudaStream_t st, const float* x, const float* g, T_* y, int rows, int d, int ldy, float eps) {
+  rmsnorm_kernel<T_><<<cdiv((size_t)rows * 32, 256), 256, 0, st>>>(x, g, y, rows, d, ldy, eps);
+  g_launches++;
+  return launch_ok();
+}
+
+template <typename T_>
+const T_* wl(const void* base, int l, size_t per_layer) {
+  return static_cast<const T_*>(base) + (size_t)l * per_layer;
+}
+
+bool g_attr_done = false;
+std::mutex g_attr_mu;
+
+template <typename T_>
+void set_attrs() {
+  cudaFuncSetAttribute(mma_v0::gemm_bf16_kernel<EpiStoreF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)mma_v0::smem_bytes());
+  cudaFuncSetAttribute(mma_v0::gemm_bf16_kernel<EpiAddF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)mma_v0::smem_bytes());
+  cudaFuncSetAttribute(mma_v0::gemm_bf16_kernel<EpiMemScatter<bf16>>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)mma_v0::smem_bytes());
+  cudaFuncSetAttribute(enc_attn_simt_kernel<T_>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+  cudaFuncSetAttribute(head_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+}
+void ensure_attrs() {
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (g_attr_done) return;
+  set_attrs<float>();
+  set_attrs<bf16>();
+  g_attr_done = true;
+}
+
+// ---------------------------------------------------------------------------
+// encoder
+
+template <typename T_>
+int encode_impl(const rlt_model* m, const int32_t* tok, int B, int T, T_* e, T_* mem, void* ws, cudaStream_t st) {
+  const rlt_config& c = m->cfg;
+  const rlt_weights& w = m->w;
+  const int d = c.d_model, f = c.d_ffn, H = c.n_heads, hd = c.head_dim, L = c.n_layers, G = c.mem_groups;
+  const int R = B * T;
+  WsLayout Lw = layout(m, B, T);
+  int* status = at<int>(ws, Lw.status);
+  float2* tab = at<float2>(ws, Lw.rope);
+  float* h = at<float>(ws, Lw.e_h);
+  T_* a = at<T_>(ws, Lw.e_a);
+  float* C = at<float>(ws, Lw.e_c);
+  T_* q = at<T_>(ws, Lw.e_q);
+  T_* k = at<T_>(ws, Lw.e_k);
+  T_* v = at<T_>(ws, Lw.e_v);
+  T_* o = at<T_>(ws, Lw.e_o);
+  int rc;
+  rope_table_kernel<<<cdiv((size_t)T * (hd / 2), 256), 256, 0, st>>>(tab, 0, T, hd / 2, (double)c.rope_theta);
+  g_launches++;
+  embed_kernel<T_><<<R, 128, 0, st>>>(tok, static_cast<const T_*>(w.tok_emb), h, R, d, c.vocab, status);
+  g_launches++;
+  if ((rc = launch_ok())) return rc;
+  const float scale = 1.0f / sqrtf((float)hd);
+  const size_t att_smem = sizeof(float) * (32 * hd + 32 * (hd + 1) + 32 * hd);
+  for (int l = 0; l < L; ++l) {
+    if ((rc = rmsnorm<T_>(st, h, w.enc_attn_norm + (size_t)l * d, a, R, d, d, c.rms_eps))) return rc;
+    const T_* Wqkv = wl<T_>(w.W_qkv, l, (size_t)3 * d * d);
+    if ((rc = gemm<T_>(st, a, d, GemmB{Wqkv, Wqkv, 3 * d, d}, R, 3 * d, d, EpiStoreF32{C, 3 * d}))) return rc;
+    rope_split_kernel<T_><<<cdiv((size_t)R * H * (hd / 2), 256), 256, 0, st>>>(C, q, k, v, tab, B, T, H, hd);
+    g_launches++;
+    enc_attn_simt_kernel<T_><<<dim3(cdiv(T, 32), H, B), 256, att_smem, st>>>(q, k, v, o, T, H, hd, scale);
+    g_launches++;
+    if ((rc = launch_ok())) return rc;
+    const T_* WO = wl<T_>(w.W_O, l, (size_t)d * d);
+    if ((rc = gemm<T_>(st, o, d, GemmB{WO, WO, d, d}, R, d, d, EpiAddF32{h, d}))) return rc;
+    if ((rc = rmsnorm<T_>(st, h, w.enc_ffn_norm + (size_t)l * d, a, R, d, d, c.rms_eps))) return rc;
+    const T_* W1 = wl<T_>(w.W_1, l, (size_t)f * d);
+    const T_* W3 = wl<T_>(w.W_3, l, (size_t)f * d);
+    if ((rc = gemm<T_>(st, a, d, GemmB{W1, W3, f, d}, R, 2 * f, d, EpiStoreF32{C, 2 * f}))) return rc;
+    swiglu_kernel<T_><<<cdiv((size_t)R * f, 256), 256, 0, st>>>(C, a, R, f);
+    g_launches++;
+    const T_* W2 = wl<T_>(w.W_2, l, (size_t)d * f);
+    if ((rc = gemm<T_>(st, a, f, GemmB{W2, W2, d, f}, R, d, f, EpiAddF32{h, d}))) return rc;
+  }
+  if ((rc = rmsnorm<T_>(st, h, w.enc_norm, e, R, d, d, c.rms_eps))) return rc;
+  const size_t plane = (size_t)B * H * T * hd;
+  for (int g = 0; g < G; ++g) {
+    const T_* WK = wl<T_>(w.W_K, g, (size_t)d * d);
+    const T_* WV = wl<T_>(w.W_V, g, (size_t)d * d);
+    if ((rc = gemm<T_>(st, e, d, GemmB{WK, WK, d, d}, R, d, d, EpiMemScatter<T_>{mem + (2 * g) * plane, T, H, hd})))
+      return rc;
+    if ((rc = gemm<T_>(st, e, d, GemmB{WV, WV, d, d}, R, d, d,
+                       EpiMemScatter<T_>{mem + (2 * g + 1) * plane, T, H, hd})))
+      return rc;
+  }
+  return RLT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// decoder: the kernels of one step (enqueued during graph capture)
+
+struct DecodeArgs {
+  const void* e;
+  const void* mem;
+  int T_mem, n;
+  const int32_t* actions;
+  float inv_temp;
+  int top_k;
+  float *logp, *logp_full;
+  int32_t* argmax;
+  float* logits;
+  int n_emit;
+};
+
+template <typename T_>
+int enqueue_step(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* ws, const WsLayout& Lw,
+                 cudaStream_t st, int* n_kernels) {
+  const rlt_config& c = m->cfg;
+  const rlt_weights& w = m->w;
+  const int B = sst->batch;
+  const int d = c.d_model, f = c.d_ffn, H = c.n_heads, hd = c.head_dim, L = c.n_layers, Wn = c.window;
+  const int V = c.vocab;
+  StepCtx* ctx = at<StepCtx>(ws, Lw.ctx);
+  int* status = at<int>(ws, Lw.status);
+  const float2* tab = at<float2>(ws, Lw.rope);
+  float* h = at<float>(ws, Lw.d_h);
+  T_* x = at<T_>(ws, Lw.d_x);
+  float* C = at<float>(ws, Lw.d_c);
+  T_* o = at<T_>(ws, Lw.d_o);
+  float* part = at<float>(ws, Lw.d_part);
+  const T_* e = static_cast<const T_*>(A.e);
+  const T_* mem = static_cast<const T_*>(A.mem);
+  const float scale = 1.0f / sqrtf((float)hd);
+  int rc, nk = 0;
+  auto post = [&]() {
+    g_launches++;
+    nk++;
+    return launch_ok();
+  };
+  // event-record node around launches of the timed class
+  KernelTimer* tm = m->timer;
+  auto mark = [&](int cls) -> int {
+    if (!tm || tm->cls != cls) return RLT_OK;
+    size_t j = tm->nodes.size();
+    if (j >= tm->ph.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return RLT_ECUDA;
+      tm->ph.push_back(e);
+    }
+    if (cudaEventRecordWithFlags(tm->ph[j], st, cudaEventRecordExternal) != cudaSuccess) return RLT_ECUDA;
+    cudaStreamCaptureStatus cst;
+    const cudaGraphNode_t* deps = nullptr;
+    size_t nd = 0;
+    if (cudaStreamGetCaptureInfo(st, &cst, nullptr, nullptr, &deps, nullptr, &nd) != cudaSuccess || nd != 1)
+      return RLT_ECUDA;
+    tm->nodes.push_back(deps[0]);
+    return RLT_OK;
+  };
+  if (tm) tm->nodes.clear();
+  if ((rc = mark(RLT_TIMER_STEP))) return rc;
+  // merge
+  const int bd = B * d;
+  if (c.gate_mode == RLT_GATE_LEARNED) {
+    merge_prep_kernel<T_><<<cdiv(bd, 256), 256, 0, st>>>(e, sst->s, x, B, A.T_mem, d, ctx);
+    if ((rc = post())) return rc;
+    const T_* Wg = static_cast<const T_*>(w.W_g);
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm<T_>(st, x, 2 * d, GemmB{Wg, Wg, d, 2 * d}, B, d, 2 * d, EpiStoreF32{C, d}))) return rc;
+    nk++;
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+  }
+  merge_blend_kernel<T_><<<cdiv(bd, 256), 256, 0, st>>>(C, w.b_g, e, sst->s, h, B, A.T_mem, d,
+                                                        c.gate_mode == RLT_GATE_DISCARD_S, ctx);
+  if ((rc = post())) return rc;
+  const size_t ring_layer = (size_t)B * H * Wn * hd;
+  const size_t plane = (size_t)B * H * A.T_mem * hd;
+  T_* rk = static_cast<T_*>(sst->ring_k);
+  T_* rv = static_cast<T_*>(sst->ring_v);
+  const size_t swa_smem = sizeof(float) * (hd + Wn);
+  const size_t xa_smem = sizeof(float) * (hd + kXChunk + 128);
+  const int n_chunks = (int)cdiv(A.T_mem, kXChunk);
+  for (int l = 0; l < L; ++l) {
+    // self-attention over the window
+    if ((rc = rmsnorm<T_>(st, h, w.dec_attn_norm + (size_t)l * d, x, B, d, d, c.rms_eps))) return rc;
+    nk++;
+    const T_* Wqkv = wl<T_>(w.W_qkv, l, (size_t)3 * d * d);
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm<T_>(st, x, d, GemmB{Wqkv, Wqkv, 3 * d, d}, B, 3 * d, d, EpiStoreF32{C, 3 * d}))) return rc;
+    nk++;
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = mark(RLT_TIMER_SWA))) return rc;
+    dec_swa_kernel<T_><<<dim3(H, B), 128, swa_smem, st>>>(C, rk + l * ring_layer, rv + l * ring_layer, o, tab, H, hd,
+                                                          Wn, scale, ctx);
+    if ((rc = post())) return rc;
+    if ((rc = mark(RLT_TIMER_SWA))) return rc;
+    const T_* WO = wl<T_>(w.W_O, l, (size_t)d * d);
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm<T_>(st, o, d, GemmB{WO, WO, d, d}, B, d, d, EpiAddF32{h, d}))) return rc;
+    nk++;
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    // cross-attention to memory positions 0..p
+    if ((rc = rmsnorm<T_>(st, h, w.dec_xattn_norm + (size_t)l * d, x, B, d, d, c.rms_eps))) return rc;
+    nk++;
+    const T_* WQx = wl<T_>(w.W_Qx, l, (size_t)d * d);
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm<T_>(st, x, d, GemmB{WQx, WQx, d, d}, B, d, d, EpiStoreF32{C, d}))) return rc;
+    nk++;
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    const int g = (c.mem_groups == 1) ? 0 : l;
+    if ((rc = mark(RLT_TIMER_XATTN))) return rc;
+    dec_xattn_part_kernel<T_><<<dim3(n_chunks, H, B), 128, xa_smem, st>>>(
+        C, mem + (2 * g) * plane, mem + (2 * g + 1) * plane, part, H, hd, A.T_mem, n_chunks, scale, ctx);
+    if ((rc = post())) return rc;
+    dec_xattn_combine_kernel<T_><<<dim3(H, B), 128, 0, st>>>(part, o, H, hd, n_chunks, ctx);
+    if ((rc = post())) return rc;
+    if ((rc = mark(RLT_TIMER_XATTN))) return rc;
+    const T_* WOx = wl<T_>(w.W_Ox, l, (size_t)d * d);
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm<T_>(st, o, d, GemmB{WOx, WOx, d, d}, B, d, d, EpiAddF32{h, d}))) return rc;
+    nk++;
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    // SwiGLU FFN
+    if ((rc = rmsnorm<T_>(st, h, w.dec_ffn_norm + (size_t)l * d, x, B, d, d, c.rms_eps))) return rc;
+    nk++;
+    const T_* W1 = wl<T_>(w.W_1, l, (size_t)f * d);
+    const T_* W3 = wl<T_>(w.W_3, l, (size_t)f * d);
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm<T_>(st, x, d, GemmB{W1, W3, f, d}, B, 2 * f, d, EpiStoreF32{C, 2 * f}))) return rc;
+    nk++;
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    swiglu_kernel<T_><<<cdiv((size_t)B * f, 256), 256, 0, st>>>(C, x, B, f);
+    if ((rc = post())) return rc;
+    const T_* W2 = wl<T_>(w.W_2, l, (size_t)d * f);
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm<T_>(st, x, f, GemmB{W2, W2, d, f}, B, d, f, EpiAddF32{h, d}))) return rc;
+    nk++;
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+  }
+  // head
+  if ((rc = mark(RLT_TIMER_HEAD))) return rc;
+  head_prep_kernel<T_><<<cdiv((size_t)B * 32, 256), 256, 0, st>>>(h, sst->s, w.head_norm, x, B, d, c.rms_eps);
+  if ((rc = post())) return rc;
+  const T_* Wo = static_cast<const T_*>(w.W_o);
+  if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+  if ((rc = gemm<T_>(st, x, d, GemmB{Wo, Wo, V, d}, B, V, d, EpiStoreF32{C, V}))) return rc;
+  nk++;
+  if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+  HeadArgs ha;
+  ha.logits = C;
+  ha.actions = A.actions;
+  ha.logp = A.logp;
+  ha.logp_full = A.logp_full;
+  ha.argmax = A.argmax;
+  ha.emit_map = at<int>(ws, Lw.emit);
+  ha.logits_out = (A.n_emit > 0) ? A.logits : nullptr;
+  ha.B = B;
+  ha.V = V;
+  ha.n = A.n;
+  ha.top_k = A.top_k;
+  ha.inv_temp = A.inv_temp;
+  ha.status = status;
+  head_reduce_kernel<<<B, 1024, sizeof(float) * V, st>>>(ha, ctx);
+  if ((rc = post())) return rc;
+  if ((rc = mark(RLT_TIMER_HEAD))) return rc;
+  advance_kernel<<<1, 1, 0, st>>>(ctx);
+  if ((rc = post())) return rc;
+  if ((rc = mark(RLT_TIMER_STEP))) return rc;
+  *n_kernels = nk;
+  return RLT_OK;
+}
+
+template <typename T_>
+int decode_impl(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const int32_t* emit_steps, void* ws,
+                cudaStream_t st) {
+  const rlt_config& c = m->cfg;
+  const int B = sst->batch;
+  WsLayout Lw = layout(m, B, A.T_mem);
+  const int p0 = sst->pos;
+  int rc;
+  // per-call setup (not captured): context, emit map, RoPE rows p0..p0+n-1
+  set_ctx_kernel<<<1, 1, 0, st>>>(at<StepCtx>(ws, Lw.ctx), p0);
+  g_launches++;
+  std::vector<int> emap(A.n, -1);
+  for (int j = 0; j < A.n_emit; ++j) emap[emit_steps[j]] = j;
+  RLT_CUDA_TRY(cudaMemcpyAsync(at<int>(ws, Lw.emit), emap.data(), sizeof(int) * A.n, cudaMemcpyHostToDevice, st));
+  const int half = c.head_dim / 2;
+  rope_table_kernel<<<cdiv((size_t)A.n * half, 256), 256, 0, st>>>(at<float2>(ws, Lw.rope), p0, A.n, half,
+                                                                   (double)c.rope_theta);
+  g_launches++;
+  if ((rc = launch_ok())) return rc;
+  // capture one step and replay it n times
+  cudaStream_t cs = m->cap_stream;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  RLT_CUDA_TRY(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal));
+  int nk = 0;
+  const uint64_t before = g_launches.load();
+  rc = enqueue_step<T_>(m, sst, A, ws, Lw, cs, &nk);
+  cudaError_t ce = cudaStreamEndCapture(cs, &graph);
+  g_launches.store(before);  // captured launches are counted when the graph runs
+  if (rc) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (ce != cudaSuccess) return RLT_ECUDA;
+  ce = cudaGraphInstantiate(&exec, graph, 0);
+  if (ce != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return RLT_ECUDA;
+  }
+  KernelTimer* tm = m->timer;
+  const int pairs = (tm && tm->cls != RLT_TIMER_OFF) ? (int)tm->nodes.size() / 2 : 0;
+  bool parked = false;
+  for (int i = 0; i < A.n; ++i) {
+    if (pairs > 0) {
+      if (tm->used + pairs <= tm->cap) {
+        for (int j = 0; j < pairs; ++j) {
+          cudaGraphExecEventRecordNodeSetEvent(exec, tm->nodes[2 * j], tm->ev[2 * (tm->used + j)]);
+          cudaGraphExecEventRecordNodeSetEvent(exec, tm->nodes[2 * j + 1], tm->ev[2 * (tm->used + j) + 1]);
+        }
+        tm->used += pairs;
+      } else if (!parked) {  // pool exhausted: point the nodes back at the placeholders
+        for (size_t j = 0; j < tm->nodes.size(); ++j)
+          cudaGraphExecEventRecordNodeSetEvent(exec, tm->nodes[j], tm->ph[j]);
+        parked = true;
+      }
+    }
+    ce = cudaGraphLaunch(exec, st);
+    if (ce != cudaSuccess) break;
+    g_launches += (uint64_t)nk;
+  }
+  cudaGraphDestroy(graph);
+  // destroying an executable graph with launches in flight is allowed; its
+  // resources are released once they complete
+  cudaGraphExecDestroy(exec);
+  if (ce != cudaSuccess) return RLT_ECUDA;
+  sst->pos += A.n;
+  return RLT_OK;
+}
+
+int validate_cfg(const rlt_config* c) {
+  if (!c) return RLT_EINVAL;
+  if (c->d_model <= 0 || c->n_layers <= 0 || c->n_heads <= 0 || c->head_dim <= 0 || c->d_ffn <= 0 ||
+      c->window <= 0 || c->vocab <= 0)
+    return RLT_EINVAL;
+  if (c->d_model != c->n_heads * c->head_dim) return RLT_EINVAL;
+  if (c->mem_groups != 1 && c->mem_groups != c->n_layers) return RLT_EINVAL;
+  if (c->dtype != RLT_F32 && c->dtype != RLT_BF16) return RLT_EINVAL;
+  if (c->gate_mode != RLT_GATE_LEARNED && c->gate_mode != RLT_GATE_DISCARD_S) return RLT_EINVAL;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return RLT_EINVAL;
+  // kernel limits
+  if (c->head_dim % 8 != 0 || 128 % c->head_dim != 0) return RLT_EUNSUPPORTED;
+  // bf16 rows are moved in 16-byte pieces
+  if (c->dtype == RLT_BF16 && (c->d_model % 8 != 0 || c->d_ffn % 8 != 0)) return RLT_EUNSUPPORTED;
+  if (c->vocab > 49152) return RLT_EUNSUPPORTED;
+  if (c->window > 4096) return RLT_EUNSUPPORTED;
+  return RLT_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// extern "C" entry points
+
+extern "C" {
+
+int rlt_abi_version(void) { return 100; }
+
+uint64_t rlt_launch_count(void) { return g_launches.load(); }
+
+const char* rlt_strerror(int code) {
+  switch (code) {
+    case RLT_OK: return "ok";
+    case RLT_EINVAL: return "invalid argument";
+    case RLT_ESTALE: return "state built under another model version";
+    case RLT_ERANGE: return "position range exceeds the encoded length";
+    case RLT_ECUDA: return "CUDA error";
+    case RLT_ETIMEOUT: return "device wait timed out";
+    case RLT_EBOUNDS: return "index out of range on the device";
+    case RLT_EWORKSPACE: return "workspace too small";
+    case RLT_EUNSUPPORTED: return "shape not supported by the kernels";
+    default: return "unknown error";
+  }
+}
+
+int rlt_model_create(const rlt_config* cfg, const rlt_weights* w, uint64_t version, rlt_model** out) {
+  if (!out) return RLT_EINVAL;
+  *out = nullptr;
+  int rc = validate_cfg(cfg);
+  if (rc) return rc;
+  if (!w) return RLT_EINVAL;
+  const void* ptrs[] = {w->tok_emb, w->s_star, w->W_g, w->b_g, w->W_qkv, w->W_O, w->W_1, w->W_3,
+                        w->W_2, w->W_Qx, w->W_Ox, w->W_K, w->W_V, w->W_o, w->enc_attn_norm,
+                        w->enc_ffn_norm, w->enc_norm, w->dec_attn_norm, w->dec_xattn_norm, w->dec_ffn_norm,
+                        w->head_norm};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return RLT_EINVAL;
+  rlt_model* m = new rlt_model();
+  m->cfg = *cfg;
+  m->w = *w;
+  m->version = version;
+  m->esz = (cfg->dtype == RLT_BF16) ? 2 : 4;
+  m->timer = nullptr;
+  if (cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    delete m;
+    return RLT_ECUDA;
+  }
+  ensure_attrs();
+  *out = m;
+  return RLT_OK;
+}
+
+int rlt_model_set_version(rlt_model* m, uint64_t version) {
+  if (!m) return RLT_EINVAL;
+  m->version = version;
+  return RLT_OK;
+}
+
+void rlt_model_destroy(rlt_model* m) {
+  if (!m) return;
+  cudaStreamSynchronize(m->cap_stream);
+  cudaStreamDestroy(m->cap_stream);
+  if (m->timer) {
+    cudaDeviceSynchronize();
+    for (cudaEvent_t e : m->timer->ev) cudaEventDestroy(e);
+    for (cudaEvent_t e : m->timer->ph) cudaEventDestroy(e);
+    delete m->timer;
+  }
+  delete m;
+}
+
+int rlt_timer_arm(rlt_model* m, int32_t kernel_class, int32_t max_launches) {
+  if (!m || kernel_class < RLT_TIMER_OFF || kernel_class > RLT_TIMER_STEP || max_launches < 0) return RLT_EINVAL;
+  if (!m->timer) m->timer = new KernelTimer();
+  KernelTimer* t = m->timer;
+  while ((int)t->ev.size() < 2 * max_launches) {
+    cudaEvent_t e;
+    RLT_CUDA_TRY(cudaEventCreate(&e));
+    t->ev.push_back(e);
+  }
+  t->cap = max_launches;
+  t->used = 0;
+  t->cls = kernel_class;
+  t->nodes.clear();
+  return RLT_OK;
+}
+
+int rlt_timer_read(rlt_model* m, float* ms, int32_t cap, int32_t* n_out) {
+  if (!m || !n_out || (cap > 0 && !ms)) return RLT_EINVAL;
+  *n_out = 0;
+  KernelTimer* t = m->timer;
+  if (!t) return RLT_OK;
+  RLT_CUDA_TRY(cudaDeviceSynchronize());
+  int n = std::min(t->used, cap);
+  for (int i = 0; i < n; ++i) RLT_CUDA_TRY(cudaEventElapsedTime(&ms[i], t->ev[2 * i], t->ev[2 * i + 1]));
+  *n_out = t->used;
+  t->cls = RLT_TIMER_OFF;
+  t->used = 0;
+  t->nodes.clear();
+  return RLT_OK;
+}
+
+int rlt_workspace_size(const rlt_model* m, int32_t B, int32_t T_max, size_t* bytes) {
+  if (!m || !bytes || B <= 0 || T_max <= 0) return RLT_EINVAL;
+  *bytes = layout(m, B, T_max).total;
+  return RLT_OK;
+}
+
+int rlt_workspace_init(void* ws, size_t ws_bytes, rlt_stream_t stream) {
+  if (!ws || ws_bytes < 256 || !aligned16(ws)) return RLT_EINVAL;
+  RLT_CUDA_TRY(cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream)));
+  return RLT_OK;
+}
+
+int rlt_state_sizes(const rlt_model* m, int32_t B, size_t* s_bytes, size_t* ring_bytes) {
+  if (!m || B <= 0) return RLT_EINVAL;
+  const rlt_config& c = m->cfg;
+  if (s_bytes) *s_bytes = (size_t)B * c.d_model * 4;
+  if (ring_bytes) *ring_bytes = (size_t)c.n_layers * B * c.n_heads * c.window * c.head_dim * m->esz;
+  return RLT_OK;
+}
+
+int rlt_state_init(const rlt_model* m, rlt_state* st, rlt_stream_t stream) {
+  if (!m || !st || st->batch <= 0 || !st->s || !st->ring_k || !st->ring_v) return RLT_EINVAL;
+  if (!aligned16(st->s) || !aligned16(st->ring_k) || !aligned16(st->ring_v)) return RLT_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const rlt_config& c = m->cfg;
+  const int d = c.d_model;
+  bcast_rows_kernel<<<cdiv((size_t)st->batch * d, 256), 256, 0, s>>>(st->s, m->w.s_star, st->batch, d);
+  g_launches++;
+  size_t ring_el = (size_t)c.n_layers * st->batch * c.n_heads * c.window * c.head_dim;
+  if (m->cfg.dtype == RLT_BF16) {
+    fill_nan_kernel<bf16><<<1184, 256, 0, s>>>(static_cast<bf16*>(st->ring_k), ring_el);
+    fill_nan_kernel<bf16><<<1184, 256, 0, s>>>(static_cast<bf16*>(st->ring_v), ring_el);
+  } else {
+    fill_nan_kernel<float><<<1184, 256, 0, s>>>(static_cast<float*>(st->ring_k), ring_el);
+    fill_nan_kernel<float><<<1184, 256, 0, s>>>(static_cast<float*>(st->ring_v), ring_el);
+  }
+  g_launches += 2;
+  if (launch_ok()) return RLT_ECUDA;
+  st->pos = 0;
+  st->version = m->version;
+  return RLT_OK;
+}
+
+int rlt_encode(const rlt_model* m, const int32_t* tokens, int32_t B, int32_t T, void* e, void* mem, void* ws,
+               size_t ws_bytes, rlt_stream_t stream) {
+  if (!m || !tokens || !e || !mem || !ws || B <= 0 || T <= 0) return RLT_EINVAL;
+  if (!aligned16(e) || !aligned16(mem) || !aligned16(ws) || !aligned16(tokens)) return RLT_EINVAL;
+  if (ws_bytes < layout(m, B, T).total) return RLT_EWORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (m->cfg.dtype == RLT_BF16)
+    return encode_impl<bf16>(m, tokens, B, T, static_cast<bf16*>(e), static_cast<bf16*>(mem), ws, s);
+  return encode_impl<float>(m, tokens, B, T, static_cast<float*>(e), static_cast<float*>(mem), ws, s);
+}
+
+int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, const void* mem, int32_t T_mem, int32_t n,
+                     const int32_t* actions, float temperature, int32_t top_k, float* logp, float* logp_full,
+                     int32_t* argmax, const int32_t* emit_steps, int32_t n_emit, float* logits, void* ws,
+                     size_t ws_bytes, rlt_stream_t stream) {
+  if (!m || !st || !e || !mem || !ws || T_mem <= 0 || n < 0 || st->batch <= 0) return RLT_EINVAL;
+  if (!st->s || !st->ring_k || !st->ring_v) return RLT_EINVAL;
+  if (!(temperature > 0.f) || top_k < 0 || n_emit < 0) return RLT_EINVAL;
+  if (n_emit > 0 && (!emit_steps || !logits)) return RLT_EINVAL;
+  for (int j = 0; j < n_emit; ++j)
+    if (emit_steps[j] < 0 || emit_steps[j] >= n) return RLT_EINVAL;
+  if (st->version != m->version) return RLT_ESTALE;
+  if (st->pos < 0 || (int64_t)st->pos + n > T_mem) return RLT_ERANGE;
+  if (ws_bytes < layout(m, st->batch, T_mem).total) return RLT_EWORKSPACE;
+  if (n == 0) return RLT_OK;
+  DecodeArgs A;
+  A.e = e;
+  A.mem = mem;
+  A.T_mem = T_mem;
+  A.n = n;
+  A.actions = actions;
+  A.inv_temp = 1.0f / temperature;
+  A.top_k = top_k;
+  A.logp = logp;
+  A.logp_full = logp_full;
+  A.argmax = argmax;
+  A.logits = logits;
+  A.n_emit = n_emit;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (m->cfg.dtype == RLT_BF16) return decode_impl<bf16>(m, st, A, emit_steps, ws, s);
+  return decode_impl<float>(m, st, A, emit_steps, ws, s);
+}
+
+int rlt_status(void* ws, rlt_stream_t stream) {
+  if (!ws) return RLT_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RLT_ECUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return RLT_ECUDA;
+  if (v != 0) {
+    int z = 0;
+    if (cudaMemcpy(ws, &z, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return RLT_ECUDA;
+  }
+  return v;
+}
+
+}  // extern "C"

@@ -1,0 +1,194 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle."""
+import numpy as np
+import pytest
+
+import rlt_inputs as ri
+from oracle import rlt_oracle as O
+from tests.gpu_common import (BF16_ARGMAX_AGREE, BF16_REL_LOGIT, F32_ABS, check_argmax, gpu_run, oracle_ring,
+                              oracle_run, rel_logit_err)
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(name, B=None, T=None, jitter=0.1, seed=None, **over):
+    wl = ri.preset(name, **over)
+    W = ri.make_weights(wl.cfg, wl.seed if seed is None else seed, norm_jitter=jitter)
+    tok = ri.make_tokens(wl, B=B, T=T)
+    acts = ri.teacher_actions(tok, 0, tok.shape[1])
+    return wl, W, tok, acts
+
+
+# ---------------------------------------------------------------------------
+# fp32 tiny model: absolute tolerance 1e-4 on s, logits and log-probs
+
+@pytest.mark.parametrize("B,T", [(8, 64), (3, 7), (1, 1)])
+def test_tiny_f32_parity(B, T):
+    wl, W, tok, acts = _inputs("tiny", B=B, T=T)
+    emit = list(range(T))
+    g = gpu_run(wl, W, tok, acts, emit=emit)
+    o = oracle_run(wl, W, tok, acts, emit=emit)
+    assert g["status"] == 0 and g["pos"] == T
+    assert np.abs(g["e"] - o["e"]).max() <= F32_ABS
+    assert np.abs(g["mem"] - o["mem"]).max() <= F32_ABS
+    assert np.abs(g["s"] - o["s"]).max() <= F32_ABS
+    for i in emit:
+        assert np.abs(g["logits"][i] - o["logits"][i]).max() <= F32_ABS
+    m = ~np.isnan(o["logp"])
+    assert np.array_equal(np.isnan(g["logp"]), ~m)
+    if m.any():
+        assert np.abs(g["logp"][m] - o["logp"][m]).max() <= F32_ABS
+        assert np.abs(g["logp_full"][m] - o["logp_full"][m]).max() <= F32_ABS
+    # argmax: decided in each side's own precision (see check_argmax)
+    G = np.concatenate([g["logits"][i] for i in range(T)])
+    Ol = np.concatenate([o["logits"][i] for i in range(T)])
+    ga = np.concatenate([g["argmax"][:, i] for i in range(T)])
+    check_argmax(ga, G, Ol, tol_rel=F32_ABS, agree=1.0)
+    # retained SWA entries equal the oracle's cache
+    c = O.Cfg.of(wl.cfg)
+    ring = oracle_ring(c, o["cache"], T)
+    for (l, slot), (k, v) in ring.items():
+        assert np.abs(g["ring_k"][l, :, :, slot] - k).max() <= F32_ABS
+        assert np.abs(g["ring_v"][l, :, :, slot] - v).max() <= F32_ABS
+
+
+@pytest.mark.parametrize("window", [1, 2, 3, 64])
+def test_tiny_window_variants(window):
+    wl, W, tok, acts = _inputs("tiny", B=4, T=20, window=window)
+    g = gpu_run(wl, W, tok, acts, emit=[19])
+    o = oracle_run(wl, W, tok, acts, emit=[19])
+    assert np.abs(g["s"] - o["s"]).max() <= F32_ABS
+    assert np.abs(g["logits"][19] - o["logits"][19]).max() <= F32_ABS
+
+
+def test_tiny_gate_discard_window_one_equals_parallel_pass():
+    """z forced to 0 and W = 1: the recurrence equals a token-parallel decoder pass."""
+    from tests import _torch_ref as TR
+    wl, W, tok, acts = _inputs("tiny", B=4, T=16, window=1, gate_mode=1)
+    g = gpu_run(wl, W, tok, acts, emit=list(range(16)))
+    c = O.Cfg.of(wl.cfg)
+    e, mem = O.encode(c, W, tok)
+    H = TR.parallel_decoder(c, W, e, mem, 1)
+    assert np.abs(g["s"] - H[:, -1]).max() <= F32_ABS
+    lg = TR.head_logits(c, W, H)
+    for i in range(16):
+        assert np.abs(g["logits"][i] - lg[:, i]).max() <= F32_ABS
+
+
+def test_tiny_learned_gate_differs_from_parallel_pass():
+    from tests import _torch_ref as TR
+    wl, W, tok, acts = _inputs("tiny", B=4, T=16, window=1)
+    g = gpu_run(wl, W, tok, acts)
+    c = O.Cfg.of(wl.cfg)
+    e, mem = O.encode(c, W, tok)
+    H = TR.parallel_decoder(c, W, e, mem, 1)
+    assert np.abs(g["s"] - H[:, -1]).max() > 100 * F32_ABS
+
+
+# ---------------------------------------------------------------------------
+# bf16 small model against the bf16-emulating oracle
+
+def _check_bf16(g, o, emit):
+    rel = np.concatenate([rel_logit_err(g["logits"][i], o["logits"][i]) for i in emit])
+    assert rel.max() <= BF16_REL_LOGIT, rel.max()
+    G = np.concatenate([g["logits"][i] for i in emit])
+    Ol = np.concatenate([o["logits"][i] for i in emit])
+    ga = np.concatenate([g["argmax"][:, i] for i in emit])
+    raw = check_argmax(ga, G, Ol)
+    assert raw >= 0.99, raw
+    srel = np.abs(g["s"] - o["s"]).max() / np.abs(o["s"]).max()
+    assert srel <= BF16_REL_LOGIT, srel
+    m = ~np.isnan(o["logp"])
+    assert np.array_equal(np.isnan(g["logp"]), ~m)
+    # log-probabilities: absolute error bounded by twice the logit error
+    lim = 2 * BF16_REL_LOGIT * max(np.abs(o["logits"][i]).max() for i in emit) + 1e-3
+    assert np.abs(g["logp"][m] - o["logp"][m]).max() <= lim
+    erel = np.abs(g["e"] - o["e"]).max() / np.abs(o["e"]).max()
+    assert erel <= BF16_REL_LOGIT, erel
+    mrel = np.abs(g["mem"] - o["mem"]).max() / np.abs(o["mem"]).max()
+    assert mrel <= BF16_REL_LOGIT, mrel
+
+
+@pytest.mark.parametrize("B,T", [(8, 160), (3, 37)])
+def test_small_bf16_parity(B, T):
+    wl, W, tok, acts = _inputs("small", B=B, T=T)
+    emit = list(range(T))
+    g = gpu_run(wl, W, tok, acts, emit=emit)
+    o = oracle_run(wl, W, tok, acts, emit=emit)
+    assert g["status"] == 0
+    _check_bf16(g, o, emit)
+
+
+def test_small_bf16_full_size_sampled_rows():
+    """Full small workload (B=64, T=512) on the GPU; sequences 0, 21, 42, 63 against the oracle."""
+    wl, W, tok, acts = _inputs("small", jitter=0.0)
+    T = wl.T
+    emit = [0, 1, 15, 16, 17, 127, 128, 255, 256, 300, 511]
+    g = gpu_run(wl, W, tok, acts, emit=emit)
+    rows = [0, 21, 42, 63]
+    o = oracle_run(wl, W, tok[rows], acts[rows], emit=emit)
+    gs = dict(e=g["e"][rows], mem=g["mem"][:, :, rows], s=g["s"][rows], logp=g["logp"][rows],
+              logp_full=g["logp_full"][rows], argmax=g["argmax"][rows],
+              logits={i: g["logits"][i][rows] for i in emit})
+    _check_bf16(gs, o, emit)
+    assert np.isfinite(g["s"]).all() and np.isfinite(g["logp"][~np.isnan(g["logp"])]).all()
+
+
+# ---------------------------------------------------------------------------
+# invariants on the GPU
+
+@pytest.mark.parametrize("name,B,T,cuts", [("tiny", 8, 64, [1, 32, 33]), ("small", 16, 96, [5, 17, 64])])
+def test_split_invariance_bitwise(name, B, T, cuts):
+    """Proposition 3.1: any split of decode_steps gives bit-identical states and outputs."""
+    wl, W, tok, acts = _inputs(name, B=B, T=T)
+    a = gpu_run(wl, W, tok, acts, emit=[T - 1])
+    b = gpu_run(wl, W, tok, acts, n_split=cuts, emit=[T - 1])
+    for k in ("s", "ring_k", "ring_v", "argmax"):
+        assert np.array_equal(a[k], b[k], equal_nan=True), k
+    assert np.array_equal(a["logp"], b["logp"], equal_nan=True)
+    assert np.array_equal(a["logits"][T - 1], b["logits"][T - 1])
+
+
+def test_ring_unused_slots_stay_poisoned_and_outputs_finite():
+    wl, W, tok, acts = _inputs("small", B=4, T=9)    # W = 16 > T: slots 9..15 never written
+    g = gpu_run(wl, W, tok, acts)
+    assert np.isnan(g["ring_k"][:, :, :, 9:]).all() and np.isnan(g["ring_v"][:, :, :, 9:]).all()
+    assert np.isfinite(g["s"]).all() and np.isfinite(g["logp"][:, :-1]).all()
+
+
+def test_memory_prefix_invariant_on_gpu():
+    """Memory depends only on tokens: M[:, :t] is bit-identical when later tokens change."""
+    wl, W, tok, acts = _inputs("small", B=4, T=64)
+    tok2 = tok.copy()
+    tok2[:, 40:] = (tok2[:, 40:] + 1) % 5
+    a = gpu_run(wl, W, tok, acts)
+    b = gpu_run(wl, W, tok2, acts)
+    assert np.array_equal(a["mem"][..., :40, :], b["mem"][..., :40, :])
+    assert np.array_equal(a["e"][:, :40], b["e"][:, :40])
+
+
+def test_stale_state_rejected_and_bounds_flag():
+    import torch
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from recurrent_looped_transformer_rlt_b300 import runner
+    wl, W, tok, acts = _inputs("tiny", B=2, T=8)
+    model = rlt.Model(wl.cfg, W)
+    buf = runner.alloc_buffers(model, 2, 8)
+    bad = tok.copy()
+    bad[0, 3] = 7   # vocabulary is {0, 1}
+    runner.encode(model, torch.from_numpy(bad).cuda(), buf)
+    assert runner.status(buf) == rlt.RLT_EBOUNDS
+    assert runner.status(buf) == 0      # cleared after reading
+    runner.encode(model, torch.from_numpy(tok).cuda(), buf)
+    st = runner.new_state(model, 2)
+    runner.decode(model, st, buf, 4)
+    model.set_version(2)
+    with pytest.raises(rlt.RLTError) as ei:
+        runner.decode(model, st, buf, 1)
+    assert ei.value.code == rlt.RLT_ESTALE
+    st2 = runner.new_state(model, 2)
+    runner.decode(model, st2, buf, 8)
+    with pytest.raises(rlt.RLTError) as ei:
+        runner.decode(model, st2, buf, 1)
+    assert ei.value.code == rlt.RLT_ERANGE
+    assert runner.status(buf) == 0
+    model.close()
