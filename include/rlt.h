@@ -175,6 +175,19 @@ RLT_API int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, c
                      const int32_t* emit_steps, int32_t n_emit, float* logits,
                      void* ws, size_t ws_bytes, rlt_stream_t stream);
 
+/* Cross-attention of one decoder layer (the step that reads encoder memory),
+ * as a standalone call: for every sequence b and head h,
+ *   out[b][h*hd + i] = sum_{j < t} softmax_j(q[b][h] . K[b][h][j] / sqrt(hd)) V[b][h][j][i]
+ * i.e. attention to memory positions 1..t (the current position included).
+ *   q     [B][d] f32 (the projected query, no RoPE)
+ *   mem_k [B][H][T_mem][hd] dtype, mem_v same layout (one group's plane of the
+ *         memory written by rlt_encode)
+ *   out   [B][d] dtype;  1 <= t <= T_mem.
+ * Partial results go to the workspace (rlt_workspace_size(m, B, T_mem)). */
+RLT_API int rlt_cross_attention(const rlt_model* m, const float* q, const void* mem_k, const void* mem_v,
+                                int32_t B, int32_t T_mem, int32_t t, void* out, void* ws, size_t ws_bytes,
+                                rlt_stream_t stream);
+
 /* Synchronises the stream, returns the device status recorded in the workspace
  * (RLT_OK, RLT_ETIMEOUT or RLT_EBOUNDS) and clears it. */
 RLT_API int rlt_status(void* ws, rlt_stream_t stream);

@@ -678,6 +678,36 @@ int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, const voi
   return decode_impl<float>(m, st, A, emit_steps, ws, s);
 }
 
+int rlt_cross_attention(const rlt_model* m, const float* q, const void* mem_k, const void* mem_v, int32_t B,
+                        int32_t T_mem, int32_t t, void* out, void* ws, size_t ws_bytes, rlt_stream_t stream) {
+  if (!m || !q || !mem_k || !mem_v || !out || !ws || B <= 0 || T_mem <= 0 || t < 1 || t > T_mem)
+    return RLT_EINVAL;
+  if (!aligned16(q) || !aligned16(mem_k) || !aligned16(mem_v) || !aligned16(out) || !aligned16(ws)) return RLT_EINVAL;
+  WsLayout Lw = layout(m, B, T_mem);
+  if (ws_bytes < Lw.total) return RLT_EWORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const rlt_config& c = m->cfg;
+  const int H = c.n_heads, hd = c.head_dim;
+  StepCtx* ctx = at<StepCtx>(ws, Lw.ctx);
+  float* part = at<float>(ws, Lw.d_part);
+  const int n_chunks = (int)cdiv(T_mem, kXChunk);
+  const float scale = 1.0f / sqrtf((float)hd);
+  const size_t xa_smem = sizeof(float) * (hd + kXChunk + 128);
+  set_ctx_kernel<<<1, 1, 0, s>>>(ctx, t - 1);
+  if (c.dtype == RLT_BF16) {
+    dec_xattn_part_kernel<bf16><<<dim3(n_chunks, H, B), 128, xa_smem, s>>>(
+        q, static_cast<const bf16*>(mem_k), static_cast<const bf16*>(mem_v), part, H, hd, T_mem, n_chunks, scale, ctx);
+    dec_xattn_combine_kernel<bf16><<<dim3(H, B), 128, 0, s>>>(part, static_cast<bf16*>(out), H, hd, n_chunks, ctx);
+  } else {
+    dec_xattn_part_kernel<float><<<dim3(n_chunks, H, B), 128, xa_smem, s>>>(
+        q, static_cast<const float*>(mem_k), static_cast<const float*>(mem_v), part, H, hd, T_mem, n_chunks, scale,
+        ctx);
+    dec_xattn_combine_kernel<float><<<dim3(H, B), 128, 0, s>>>(part, static_cast<float*>(out), H, hd, n_chunks, ctx);
+  }
+  g_launches += 3;
+  return launch_ok();
+}
+
 int rlt_status(void* ws, rlt_stream_t stream) {
   if (!ws) return RLT_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

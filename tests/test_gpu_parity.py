@@ -192,3 +192,40 @@ def test_stale_state_rejected_and_bounds_flag():
     assert ei.value.code == rlt.RLT_ERANGE
     assert runner.status(buf) == 0
     model.close()
+
+
+# ---------------------------------------------------------------------------
+# the cross-attention step on its own
+
+@pytest.mark.parametrize("name,B,T_mem,ts", [("small", 5, 300, [1, 2, 127, 128, 129, 300]),
+                                              ("tiny", 3, 64, [1, 17, 64])])
+def test_cross_attention_entry_point(name, B, T_mem, ts):
+    import torch
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    wl = ri.preset(name)
+    c = wl.cfg
+    W = ri.make_weights(c, wl.seed)
+    model = rlt.Model(c, W)
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((B, c.d)).astype(np.float32)
+    km = rng.standard_normal((B, c.n_heads, T_mem, c.head_dim)).astype(np.float32)
+    vm = rng.standard_normal((B, c.n_heads, T_mem, c.head_dim)).astype(np.float32)
+    if c.dtype == "bf16":
+        km, vm = O.bf16(km).astype(np.float32), O.bf16(vm).astype(np.float32)
+    dt = model.dtype
+    qd = torch.from_numpy(q).cuda()
+    kd = torch.from_numpy(km).to("cuda", dt)
+    vd = torch.from_numpy(vm).to("cuda", dt)
+    out = torch.empty(B, c.d, dtype=dt, device="cuda")
+    ws = model.workspace(B, T_mem)
+    for t in ts:
+        rlt.rlt_cross_attention(model.handle, qd, kd, vd, B, T_mem, t, out, ws, ws.numel())
+        ref = O.swa_attend(q.reshape(B, c.n_heads, c.head_dim).astype(np.float64), km[:, :, :t], vm[:, :, :t],
+                           c.head_dim).reshape(B, c.d)
+        got = out.float().cpu().numpy()
+        if c.dtype == "bf16":
+            assert np.abs(got - ref).max() <= BF16_REL_LOGIT * np.abs(ref).max()
+            assert np.abs(got - O.bf16(ref)).max() <= 2 ** -7 * np.abs(ref).max()
+        else:
+            assert np.abs(got - ref).max() <= F32_ABS
+    model.close()
