@@ -188,6 +188,22 @@ RLT_API int rlt_cross_attention(const rlt_model* m, const float* q, const void* 
                                 int32_t B, int32_t T_mem, int32_t t, void* out, void* ws, size_t ws_bytes,
                                 rlt_stream_t stream);
 
+/* Allocation-free variant of rlt_cross_attention, for callers that cannot
+ * allocate device memory (no cudaMalloc, no torch allocator): same result,
+ * same q / mem_k / mem_v / out layouts, but the partial results live in a
+ * fixed 16 MiB array inside the library, so no workspace is passed and the
+ * shape comes as plain sizes (n_heads, head_dim, dtype = RLT_F32/RLT_BF16).
+ * The pages have no counterpart: this is an integration convenience.
+ *  - Limit: B * n_heads * ceil(T_mem / 128) * (head_dim + 2) * 4 bytes must fit
+ *    in 16 MiB - 256 B; larger requests return RLT_EUNSUPPORTED.
+ *  - The first call on a device looks up the array's device address (set-up);
+ *    make that first call before any stream capture.
+ *  - Every call shares the array: calls that overlap on the GPU race.
+ *  - Allocates nothing; its launches are not included in rlt_launch_count(). */
+RLT_API int rlt_cross_attention_noalloc(const float* q, const void* mem_k, const void* mem_v, int32_t B,
+                                        int32_t n_heads, int32_t head_dim, int32_t dtype, int32_t T_mem,
+                                        int32_t t, void* out, rlt_stream_t stream);
+
 /* Synchronises the stream, returns the device status recorded in the workspace
  * (RLT_OK, RLT_ETIMEOUT or RLT_EBOUNDS) and clears it. */
 RLT_API int rlt_status(void* ws, rlt_stream_t stream);

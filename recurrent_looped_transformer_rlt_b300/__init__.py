@@ -78,6 +78,8 @@ _decode_steps = _sig("rlt_decode_steps", ctypes.c_int,
 _status = _sig("rlt_status", ctypes.c_int, [_p, _p])
 _cross_attention = _sig("rlt_cross_attention", ctypes.c_int, [_p, _p, _p, _p, _i32, _i32, _i32, _p, _p,
                                                               ctypes.c_size_t, _p])
+_cross_attention_noalloc = _sig("rlt_cross_attention_noalloc", ctypes.c_int,
+                                [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p])
 _timer_arm = _sig("rlt_timer_arm", ctypes.c_int, [_p, _i32, _i32])
 _timer_read = _sig("rlt_timer_read", ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_float), _i32, ctypes.POINTER(_i32)])
 _strerror = _sig("rlt_strerror", ctypes.c_char_p, [ctypes.c_int])
@@ -87,7 +89,7 @@ _abi_version = _sig("rlt_abi_version", ctypes.c_int, [])
 EXPORTED = ["rlt_model_create", "rlt_model_set_version", "rlt_model_destroy", "rlt_workspace_size",
             "rlt_workspace_init", "rlt_state_sizes", "rlt_state_init", "rlt_encode", "rlt_decode_steps",
             "rlt_status", "rlt_strerror", "rlt_launch_count", "rlt_abi_version", "rlt_timer_arm",
-            "rlt_timer_read", "rlt_cross_attention"]
+            "rlt_timer_read", "rlt_cross_attention", "rlt_cross_attention_noalloc"]
 RLT_TIMER_CLASSES = {"off": 0, "xattn": 1, "swa": 2, "gemm": 3, "head": 4, "step": 5}
 
 
@@ -195,6 +197,16 @@ def rlt_cross_attention(model: int, q, mem_k, mem_v, B: int, T_mem: int, t: int,
                         stream=None):
     _check(_cross_attention(model, _ptr(q), _ptr(mem_k), _ptr(mem_v), B, T_mem, t, _ptr(out), _ptr(ws), ws_bytes,
                             _stream_ptr(stream)), "rlt_cross_attention")
+
+
+def rlt_cross_attention_noalloc(q, mem_k, mem_v, B: int, n_heads: int, head_dim: int, dtype: int, T_mem: int,
+                                t: int, out, stream=None, check: bool = True) -> int:
+    """Same as rlt_cross_attention without a workspace (fixed scratch inside the library)."""
+    rc = _cross_attention_noalloc(_ptr(q), _ptr(mem_k), _ptr(mem_v), B, n_heads, head_dim, dtype, T_mem, t,
+                                  _ptr(out), _stream_ptr(stream))
+    if check:
+        _check(rc, "rlt_cross_attention_noalloc")
+    return rc
 
 
 def rlt_timer_arm(model: int, kernel_class: int, max_launches: int):
