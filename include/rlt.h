@@ -183,10 +183,25 @@ RLT_API int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, c
  *   mem_k [B][H][T_mem][hd] dtype, mem_v same layout (one group's plane of the
  *         memory written by rlt_encode)
  *   out   [B][d] dtype;  1 <= t <= T_mem.
- * Partial results go to the workspace (rlt_workspace_size(m, B, T_mem)). */
+ * Partial results and per-(b, h) arrival counters go to the workspace
+ * (rlt_workspace_size(m, B, T_mem)). */
 RLT_API int rlt_cross_attention(const rlt_model* m, const float* q, const void* mem_k, const void* mem_v,
                                 int32_t B, int32_t T_mem, int32_t t, void* out, void* ws, size_t ws_bytes,
                                 rlt_stream_t stream);
+
+/* Dense projection on the tensor cores: the kernel behind every projection of
+ * the encoder and of the decoder step of bf16 models, exposed so that it can
+ * be tested and timed on its own.
+ *   W3 == NULL:  C[m][n] = sum_k A[m][k] W[n][k]                       (n < N)
+ *   W3 != NULL:  C[m][j] = silu(sum_k A[m][k] W[j][k]) * sum_k A[m][k] W3[j][k]
+ *                (the SwiGLU pair W_1, W_3 of one FFN layer; j < N)
+ * A [M][lda] bf16, W and W3 [N][ldw] bf16 (row pitches multiples of 8
+ * elements), C [M][ldc] f32.  K may be any positive size (zero padded).  The
+ * model must be a bf16 model; the workspace must hold
+ * rlt_workspace_size(m, 1, 1) bytes (split-K partials and counters). */
+RLT_API int rlt_linear(const rlt_model* m, const void* A, int32_t lda, int32_t M, int32_t K, const void* W,
+                       const void* W3, int32_t ldw, int32_t N, float* C, int32_t ldc, void* ws, size_t ws_bytes,
+                       rlt_stream_t stream);
 
 /* Allocation-free variant of rlt_cross_attention, for callers that cannot
  * allocate device memory (no cudaMalloc, no torch allocator): same result,
@@ -194,8 +209,10 @@ RLT_API int rlt_cross_attention(const rlt_model* m, const float* q, const void* 
  * fixed 16 MiB array inside the library, so no workspace is passed and the
  * shape comes as plain sizes (n_heads, head_dim, dtype = RLT_F32/RLT_BF16).
  * The pages have no counterpart: this is an integration convenience.
- *  - Limit: B * n_heads * ceil(T_mem / 128) * (head_dim + 2) * 4 bytes must fit
- *    in 16 MiB - 256 B; larger requests return RLT_EUNSUPPORTED.
+ *  - Limit: with CH = 16384 / (head_dim * element bytes) positions per chunk,
+ *    round_up(4 * B * n_heads, 256) + B * n_heads * ceil(T_mem / CH) *
+ *    (head_dim + 2) * 4 bytes must fit in 16 MiB - 256 B; larger requests
+ *    return RLT_EUNSUPPORTED.
  *  - The first call on a device looks up the array's device address (set-up);
  *    make that first call before any stream capture.
  *  - Every call shares the array: calls that overlap on the GPU race.

@@ -80,6 +80,8 @@ _cross_attention = _sig("rlt_cross_attention", ctypes.c_int, [_p, _p, _p, _p, _i
                                                               ctypes.c_size_t, _p])
 _cross_attention_noalloc = _sig("rlt_cross_attention_noalloc", ctypes.c_int,
                                 [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p])
+_linear = _sig("rlt_linear", ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _i32, _i32, _p, _i32, _p,
+                                          ctypes.c_size_t, _p])
 _timer_arm = _sig("rlt_timer_arm", ctypes.c_int, [_p, _i32, _i32])
 _timer_read = _sig("rlt_timer_read", ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_float), _i32, ctypes.POINTER(_i32)])
 _strerror = _sig("rlt_strerror", ctypes.c_char_p, [ctypes.c_int])
@@ -89,7 +91,7 @@ _abi_version = _sig("rlt_abi_version", ctypes.c_int, [])
 EXPORTED = ["rlt_model_create", "rlt_model_set_version", "rlt_model_destroy", "rlt_workspace_size",
             "rlt_workspace_init", "rlt_state_sizes", "rlt_state_init", "rlt_encode", "rlt_decode_steps",
             "rlt_status", "rlt_strerror", "rlt_launch_count", "rlt_abi_version", "rlt_timer_arm",
-            "rlt_timer_read", "rlt_cross_attention", "rlt_cross_attention_noalloc"]
+            "rlt_timer_read", "rlt_cross_attention", "rlt_cross_attention_noalloc", "rlt_linear"]
 RLT_TIMER_CLASSES = {"off": 0, "xattn": 1, "swa": 2, "gemm": 3, "head": 4, "step": 5}
 
 
@@ -206,6 +208,15 @@ def rlt_cross_attention_noalloc(q, mem_k, mem_v, B: int, n_heads: int, head_dim:
                                   _ptr(out), _stream_ptr(stream))
     if check:
         _check(rc, "rlt_cross_attention_noalloc")
+    return rc
+
+
+def rlt_linear(model: int, A, lda: int, M: int, K: int, W, W3, ldw: int, N: int, C, ldc: int, ws, ws_bytes: int,
+               stream=None, check: bool = True) -> int:
+    rc = _linear(model, _ptr(A), lda, M, K, _ptr(W), _ptr(W3), ldw, N, _ptr(C), ldc, _ptr(ws), ws_bytes,
+                 _stream_ptr(stream))
+    if check:
+        _check(rc, "rlt_linear")
     return rc
 
 

@@ -19,6 +19,12 @@ struct EpiStoreF32 {
   int ldc;
   __device__ __forceinline__ void operator()(int m, int n, float v) const { C[(size_t)m * ldc + n] = v; }
 };
+template <typename T>
+struct EpiStoreT {  // store rounded to the storage type
+  T* C;
+  int ldc;
+  __device__ __forceinline__ void operator()(int m, int n, float v) const { C[(size_t)m * ldc + n] = from_f32<T>(v); }
+};
 struct EpiAddF32 {  // residual stream update h += acc
   float* C;
   int ldc;
@@ -34,6 +40,41 @@ struct EpiMemScatter {
     int b = m / T_len, t = m - b * T_len;
     int h = n / hd, i = n - h * hd;
     dst[(((size_t)b * H + h) * T_len + t) * hd + i] = from_f32<T>(v);
+  }
+};
+
+// Decoder QKV projection with RoPE, in pairs (i, i + hd/2) of one head:
+// q (after RoPE, fp32) to q[b][d]; k (after RoPE) and v rounded to storage and
+// written to ring slot pos mod W of this layer's ring [B][H][W][hd].
+template <typename T>
+struct EpiQKVRope {
+  static constexpr bool kPair = true;
+  float* q;
+  T* ring_k;
+  T* ring_v;
+  const float2* tab;  // [position][hd/2] (cos, sin)
+  const StepCtx* ctx;
+  int d, H, hd, W;
+  __device__ __forceinline__ void pair(int b, int n, float x1, float x2) const {
+    const int which = n / d, r = n - which * d;
+    const int head = r / hd, i = r - head * hd, half = hd >> 1;
+    const int p = ctx->pos;
+    if (which == 2) {
+      const size_t o = (((size_t)b * H + head) * W + p % W) * hd + i;
+      ring_v[o] = from_f32<T>(x1);
+      ring_v[o + half] = from_f32<T>(x2);
+      return;
+    }
+    const float2 cs = tab[(size_t)p * half + i];
+    const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
+    if (which == 0) {
+      q[(size_t)b * d + head * hd + i] = y1;
+      q[(size_t)b * d + head * hd + i + half] = y2;
+    } else {
+      const size_t o = (((size_t)b * H + head) * W + p % W) * hd + i;
+      ring_k[o] = from_f32<T>(y1);
+      ring_k[o + half] = from_f32<T>(y2);
+    }
   }
 };
 

@@ -1,0 +1,355 @@
+// Tensor-core GEMM for sm_103a: C = A[M,K] * B[N,K]^T, bf16 operands, fp32
+// accumulation in tensor memory (TMEM), operands staged in shared memory by
+// the TMA engine (tiled tensor maps, 128-byte swizzle), MMAs issued with
+// tcgen05.mma by one thread, results read back with tcgen05.ld and handed to
+// an element-wise epilogue functor.
+//
+// Roles inside a CTA (192 threads):
+//   warp 0  - TMA producer: fills a STAGES-deep ring of (A, B) k-blocks;
+//   warp 1  - allocates the TMEM accumulator and issues the MMAs (one lane);
+//   warps 2-5 - epilogue: TMEM -> registers -> functor (warp w reads TMEM
+//             lanes 32*(w%4) .. 32*(w%4)+31, i.e. tile rows).
+// Grid: (N tiles, M tiles, K splits).  When K is split over S CTAs, the S
+// CTAs of a tile form a thread-block cluster (1, 1, S): each stages its
+// partial tile in shared memory, and after a cluster barrier CTA z sums rows
+// [z*rows/S, (z+1)*rows/S) of all S tiles through distributed shared memory,
+// in split order (deterministic), and runs the epilogue on them.
+//
+// A is always the activation matrix (rows = tokens or sequences) and B a
+// weight matrix [N][K], so one kernel serves the token-parallel encoder
+// (M = B*T) and the decoder's weight-streaming projections (M = the batch of
+// sequences: the A tile is mostly zero-filled rows, the CTAs split K to spread
+// the weight stream over every SM).
+#pragma once
+
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace rlt {
+namespace tc {
+
+constexpr int BM = 128;  // UMMA M (tile rows of A)
+constexpr int BK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int UK = 16;   // K of one tcgen05.mma kind::f16
+constexpr int THREADS = 192;
+
+template <int BN, int STAGES>
+struct Cfg {
+  static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN");
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = BN;  // fp32 accumulator: one column per output column
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::
+          "r"(smem_u32(dst)),
+      "l"(tm), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(tm) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, int ncols) {  // whole warp
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, int ncols) {  // whole warp
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major operand with 128-byte swizzle:
+// rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset),
+// descriptor version 1, layout type 2 (SWIZZLE_128B).
+__device__ __forceinline__ uint64_t sdesc_k_sw128(const void* p) {
+  const uint64_t addr = smem_u32(p);
+  uint64_t d = 0;
+  d |= (addr >> 4) & 0x3FFFull;            // start address
+  d |= (uint64_t)1 << 16;                  // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset
+  d |= (uint64_t)1 << 46;                  // version
+  d |= (uint64_t)2 << 61;                  // SWIZZLE_128B
+  return d;
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, int accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` when every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+
+// Epilogues that consume column pairs (i, i + hd/2) of each head block of hd
+// columns (RoPE) declare kPair, a member hd and pair(m, n, x_n, x_{n+hd/2});
+// tiles then start on head boundaries (BN a multiple of hd).
+template <class E, class = void>
+struct IsPairEpi : std::false_type {};
+template <class E>
+struct IsPairEpi<E, std::void_t<decltype(E::kPair)>> : std::true_type {};
+
+struct SplitK {
+  int splits;        // CTAs along K (= cluster size along z when > 1)
+  int kb_per_split;  // k-blocks per CTA
+};
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// float4 at the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ float4 ld_dsmem_f4(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
+}
+
+// B operand: one weight matrix [N][K], or (glu) the pair W_1, W_3 [N][K]
+// whose tile j holds rows j*BN/2 .. of W_1 in its first half and the same
+// rows of W_3 in its second half, so that the epilogue sees gate and linear
+// values of one output column in the same thread and writes
+// silu(gate) * linear.
+template <int BN, int STAGES, bool GLU, class Epi>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmB3, int M, int N, int K, SplitK sk, Epi epi, int* status) {
+  using C = Cfg<BN, STAGES>;
+  constexpr int NOUT = GLU ? BN / 2 : BN;  // output columns per tile
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accum = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  __shared__ int s_last;
+  __shared__ int s_fail;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, z = blockIdx.z;
+  const int nb0 = blockIdx.x * (GLU ? BN / 2 : BN);  // first B row of the tile (per matrix)
+  const int kb_total = (K + BK - 1) / BK;
+  const int kb0 = z * sk.kb_per_split;
+  const int nkb = max(0, min(kb_total, kb0 + sk.kb_per_split) - kb0);
+  int issued = 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    s_fail = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (GLU) tma_prefetch_desc(&tmB3);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, kWaitBudget)) {
+          atomicExch(&s_fail, 1);
+          break;
+        }
+        unsigned char* sa = smem + s * C::STAGE_BYTES;
+        const int kx = (kb0 + i) * BK;
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        tma_load_2d(sa, &tmA, kx, m0, &full[s]);
+        if (GLU) {
+          tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[s]);
+          tma_load_2d(sa + C::A_BYTES + C::B_BYTES / 2, &tmB3, kx, nb0, &full[s]);
+        } else {
+          tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[s]);
+        }
+        issued = i + 1;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait(&full[s], (i / STAGES) & 1, kWaitBudget)) {
+          atomicExch(&s_fail, 1);
+          break;
+        }
+        tc_fence_after();
+        const unsigned char* sa = smem + s * C::STAGE_BYTES;
+        const uint64_t da = sdesc_k_sw128(sa), db = sdesc_k_sw128(sa + C::A_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / UK; ++k)  // advance 16 elements = 32 bytes (2 in descriptor units)
+          mma_bf16(tmem, da + 2 * k, db + 2 * k, idesc, (i > 0 || k > 0) ? 1 : 0);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(accum);  // arrives once every issued MMA has completed (at once if none)
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue warps (128 threads)
+    // 1. TMEM -> shared staging tile [BM][BN + 4] fp32 (thread <-> tile row,
+    //    i.e. TMEM lane); the stage ring is free once every MMA has completed.
+    const int q = warp & 3;
+    const int rl = q * 32 + lane;
+    const int et = threadIdx.x - 64;
+    const bool ok = mbar_wait(accum, 0, kWaitBudget) && (nkb > 0);
+    if (!ok) atomicExch(&s_fail, 1);
+    tc_fence_after();
+    constexpr int LDT = BN + 4;
+    float* stile = reinterpret_cast<float*>(smem);
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      float v[16];
+      tmem_ld16(tq + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; j += 4)
+        *reinterpret_cast<float4*>(stile + rl * LDT + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    }
+    epi_bar();
+  }
+  // ---- all threads: split-K reduction through distributed shared memory
+  const int rows = min(BM, M - m0);
+  int r0 = 0, r1 = rows;
+  if (sk.splits > 1) {
+    cluster_sync_all();  // every split's tile is staged
+    r0 = (int)(((long long)rows * z) / sk.splits);
+    r1 = (int)(((long long)rows * (z + 1)) / sk.splits);
+    if (warp >= 2) {
+      const int et = threadIdx.x - 64;
+      constexpr int LDT = BN + 4, V4 = BN / 4;
+      float* stile = reinterpret_cast<float*>(smem);
+      float4 acc[4];
+      const int nv = (r1 - r0) * V4;
+      // sums land in this CTA's own rows [r0, r1): no peer reads those rows
+      for (int i0 = et; i0 < nv; i0 += 4 * 128) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int zz = 0; zz < sk.splits; ++zz)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * 128;
+            if (i < nv) {
+              const int r = r0 + i / V4, c4 = i - (i / V4) * V4;
+              const float4 f = ld_dsmem_f4(stile + r * LDT + c4 * 4, (uint32_t)zz);
+              acc[u].x += f.x;
+              acc[u].y += f.y;
+              acc[u].z += f.z;
+              acc[u].w += f.w;
+            }
+          }
+        // the sums go back to rows [r0, r1) of this CTA's own tile: every
+        // element is read and written by the same thread, and the other CTAs
+        // of the cluster read only their own (disjoint) row ranges
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * 128;
+          if (i < nv) {
+            const int r = r0 + i / V4, c4 = i - (i / V4) * V4;
+            *reinterpret_cast<float4*>(stile + r * LDT + c4 * 4) = acc[u];
+          }
+        }
+      }
+    }
+  }
+  if (warp >= 2) {
+    // ---- epilogue functor on rows [r0, r1); consecutive threads take
+    //      consecutive columns
+    const int et = threadIdx.x - 64;
+    constexpr int LDT = BN + 4;
+    const float* stile = reinterpret_cast<const float*>(smem);
+    epi_bar();
+    if (!s_fail) {
+      if constexpr (GLU) {
+        constexpr int HB = BN / 2;
+        const int n = (r1 - r0) * HB;
+#pragma unroll 4
+        for (int i = et; i < n; i += 128) {
+          const int r = r0 + i / HB, j = i % HB;
+          if (nb0 + j < N) epi(m0 + r, nb0 + j, silu_f(stile[r * LDT + j]) * stile[r * LDT + j + HB]);
+        }
+      } else if constexpr (IsPairEpi<Epi>::value) {
+        const int half = epi.hd >> 1;
+        constexpr int HB = BN / 2;  // pairs per tile row
+        const int n = (r1 - r0) * HB;
+#pragma unroll 4
+        for (int i = et; i < n; i += 128) {
+          const int r = r0 + i / HB, pi = i % HB;
+          const int hb = pi / half, ii = pi - hb * half;
+          const int c = hb * 2 * half + ii;
+          if (nb0 + c < N) epi.pair(m0 + r, nb0 + c, stile[r * LDT + c], stile[r * LDT + c + half]);
+        }
+      } else {
+        const int n = (r1 - r0) * BN;
+#pragma unroll 4
+        for (int i = et; i < n; i += 128) {
+          const int r = r0 + i / BN, c = i % BN;
+          if (nb0 + c < N) epi(m0 + r, nb0 + c, stile[r * LDT + c]);
+        }
+      }
+    }
+  }
+  if (sk.splits > 1) cluster_sync_all();  // peers are done reading this CTA's tile
+  tc_fence_before();
+  __syncthreads();
+  if (s_fail && threadIdx.x == 0) {
+    set_error(status, kErrTimeout);
+    // give the copies still in flight a bounded time to land before leaving
+    for (int i = max(0, issued - STAGES); i < issued; ++i) mbar_wait(&full[i % STAGES], (i / STAGES) & 1, kWaitBudget);
+  }
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace tc
+}  // namespace rlt

@@ -3,61 +3,70 @@
 // Some callers cannot call cudaMalloc at all: code running inside another
 // framework's allocator regime, embedders that forbid allocation after start-up,
 // or hosts that only hand out input and output buffers.  rlt_cross_attention
-// needs a caller-provided workspace for its per-chunk partial results; this
-// variant keeps those partials (and its small step context) in one fixed array
-// compiled into the library instead, so the caller passes only q, the memory
-// planes and the output.
+// needs a caller-provided workspace for its per-chunk partial results and
+// arrival counters; this variant keeps those (and its small step context) in
+// one fixed array compiled into the library instead, so the caller passes only
+// q, the memory planes and the output.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds its kNoAllocScratchBytes until the process exits.  In host
 // code the array's name only stands for the symbol; its device address is
 // obtained once per device with cudaGetSymbolAddress (with that device
 // current) on the first call made on that device, which is why that first call
-// should come before any stream capture.  All calls share the array and
-// nothing in it needs to start at zero (every partial that is read was written
-// by the same call); calls that overlap on the GPU race on it.
+// should come before any stream capture.  All calls share the array; each call
+// clears the arrival counters it uses (the partials need no clearing: every
+// partial that is read was written by the same call); calls that overlap on the
+// GPU race on it.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "../../include/rlt.h"
 #include "common.cuh"
+#include "ptx.cuh"
 
 // This translation unit compiles its own copy of the kernels, in a private
 // namespace, so that its kernel symbols do not collide with the library's.
 namespace rlt_noalloc {
 using namespace ::rlt;
 #include "kernels.cuh"
+#include "xattn.cuh"
 }  // namespace rlt_noalloc
 
 using namespace ::rlt;
-using rlt_noalloc::rlt::dec_xattn_combine_kernel;
-using rlt_noalloc::rlt::dec_xattn_part_kernel;
-using rlt_noalloc::rlt::kXChunk;
+using rlt_noalloc::rlt::kXChunkBytes;
+using rlt_noalloc::rlt::launch_xattn;
 using rlt_noalloc::rlt::set_ctx_kernel;
+using rlt_noalloc::rlt::XattnArgs;
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
-constexpr size_t kCtxBytes = 256;                    // step context at the start of the array
+constexpr size_t kCtxBytes = 256;                    // step context + status word at the start of the array
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 128;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+int g_n_sm[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device (set-up on the
 // first call per device).
-int scratch_on_current_device(void** out) {
+int scratch_on_current_device(void** out, int* n_sm) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RLT_ECUDA;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return RLT_ECUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      return RLT_ECUDA;
+    g_n_sm[dev] = sms;
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];
+  *n_sm = g_n_sm[dev];
   return RLT_OK;
 }
 
@@ -75,31 +84,43 @@ int rlt_cross_attention_noalloc(const float* q, const void* mem_k, const void* m
   if (dtype != RLT_F32 && dtype != RLT_BF16) return RLT_EINVAL;
   if (head_dim < 8 || head_dim % 8 != 0 || 128 % head_dim != 0) return RLT_EUNSUPPORTED;
   if (!aligned16(q) || !aligned16(mem_k) || !aligned16(mem_v) || !aligned16(out)) return RLT_EINVAL;
-  const int n_chunks = (T_mem + kXChunk - 1) / kXChunk;
-  const size_t part_bytes = sizeof(float) * (size_t)B * n_heads * n_chunks * (head_dim + 2);
-  if (part_bytes > kNoAllocScratchBytes - kCtxBytes) return RLT_EUNSUPPORTED;  // beyond the built-in scratch
+  const int es = (dtype == RLT_BF16) ? 2 : 4;
+  const size_t chunk = (size_t)kXChunkBytes / ((size_t)head_dim * es);
+  const size_t n_chunks = ((size_t)T_mem + chunk - 1) / chunk;
+  const size_t pairs = (size_t)B * n_heads;
+  const size_t cnt_bytes = (sizeof(int) * pairs + 255) / 256 * 256;
+  const size_t part_bytes = sizeof(float) * pairs * n_chunks * (head_dim + 2);
+  if (cnt_bytes + part_bytes > kNoAllocScratchBytes - kCtxBytes) return RLT_EUNSUPPORTED;  // beyond the built-in scratch
   void* base = nullptr;
-  int rc = scratch_on_current_device(&base);
+  int n_sm = 0;
+  int rc = scratch_on_current_device(&base, &n_sm);
   if (rc) return rc;
-  StepCtx* ctx = static_cast<StepCtx*>(base);
-  float* part = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kCtxBytes);
+  unsigned char* sb = static_cast<unsigned char*>(base);
+  StepCtx* ctx = reinterpret_cast<StepCtx*>(sb);
+  int* status = reinterpret_cast<int*>(sb + 128);
+  int* cnt = reinterpret_cast<int*>(sb + kCtxBytes);
+  float* part = reinterpret_cast<float*>(sb + kCtxBytes + cnt_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const float scale = 1.0f / sqrtf((float)head_dim);
-  const size_t smem = sizeof(float) * (head_dim + kXChunk + 128);
+  XattnArgs xa{};
+  xa.q = q;
+  xa.mk = mem_k;
+  xa.mv = mem_v;
+  xa.part = part;
+  xa.cnt = cnt;
+  xa.out = out;
+  xa.B = B;
+  xa.H = n_heads;
+  xa.T_mem = T_mem;
+  xa.t_cap = T_mem;
+  xa.max_chunks = (int)n_chunks;
+  xa.scale = 1.0f / sqrtf((float)head_dim);
+  xa.ctx = ctx;
+  xa.status = status;
   set_ctx_kernel<<<1, 1, 0, s>>>(ctx, t - 1);
-  if (dtype == RLT_BF16) {
-    dec_xattn_part_kernel<bf16><<<dim3(n_chunks, n_heads, B), 128, smem, s>>>(
-        q, static_cast<const bf16*>(mem_k), static_cast<const bf16*>(mem_v), part, n_heads, head_dim, T_mem, n_chunks,
-        scale, ctx);
-    dec_xattn_combine_kernel<bf16><<<dim3(n_heads, B), 128, 0, s>>>(part, static_cast<bf16*>(out), n_heads,
-                                                                    head_dim, n_chunks, ctx);
-  } else {
-    dec_xattn_part_kernel<float><<<dim3(n_chunks, n_heads, B), 128, smem, s>>>(
-        q, static_cast<const float*>(mem_k), static_cast<const float*>(mem_v), part, n_heads, head_dim, T_mem,
-        n_chunks, scale, ctx);
-    dec_xattn_combine_kernel<float><<<dim3(n_heads, B), 128, 0, s>>>(part, static_cast<float*>(out), n_heads,
-                                                                     head_dim, n_chunks, ctx);
-  }
+  if (cudaMemsetAsync(cnt, 0, sizeof(int) * pairs, s) != cudaSuccess) return RLT_ECUDA;
+  cudaError_t ce = (dtype == RLT_BF16) ? launch_xattn<bf16>(xa, head_dim, n_sm, s)
+                                       : launch_xattn<float>(xa, head_dim, n_sm, s);
+  if (ce != cudaSuccess) return RLT_ECUDA;
   return cudaGetLastError() == cudaSuccess ? RLT_OK : RLT_ECUDA;
 }
 

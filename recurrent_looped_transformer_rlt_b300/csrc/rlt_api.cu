@@ -4,6 +4,8 @@
 // encoder pass, and the decoder step, which is captured once per call as a
 // CUDA graph and replayed n times (every per-step kernel reads the position
 // and step index from a small context in the workspace).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -16,7 +18,9 @@
 #include "../../include/rlt.h"
 #include "common.cuh"
 #include "gemm_simple.cuh"
+#include "gemm_tc.cuh"
 #include "kernels.cuh"
+#include "xattn.cuh"
 
 using namespace rlt;
 
@@ -53,6 +57,7 @@ struct rlt_model {
   uint64_t version;
   cudaStream_t cap_stream;
   size_t esz;  // bytes per stored element
+  int n_sm;    // SMs of the device the model was created on
   KernelTimer* timer;
 };
 
@@ -62,14 +67,18 @@ struct rlt_model {
 namespace {
 
 struct WsLayout {
-  size_t status, ctx, emit, rope;       // header
+  size_t status, ctx, emit, rope;  // header
   // decoder
-  size_t d_h, d_x, d_c, d_o, d_part;
+  size_t d_h, d_x, d_m, d_c, d_o, d_part, d_cnt;
   // encoder
-  size_t e_h, e_a, e_c, e_q, e_k, e_v, e_o;
+  size_t e_h, e_a, e_m, e_c, e_q, e_k, e_v, e_o;
   size_t total;
   int n_chunks;
 };
+
+// the status word: the part of the workspace that must start at zero
+// (cleared by rlt_workspace_init)
+constexpr size_t kWsHeaderBytes = 256;
 
 WsLayout layout(const rlt_model* m, int B, int T) {
   const rlt_config& c = m->cfg;
@@ -88,19 +97,22 @@ WsLayout layout(const rlt_model* m, int B, int T) {
   L.rope = take(sizeof(float2) * (size_t)T * (hd / 2));
   const size_t common_end = off;
   // decoder region
-  L.n_chunks = (int)cdiv(T, kXChunk);
+  L.n_chunks = (int)cdiv(std::max((size_t)T, (size_t)c.window), (size_t)kXChunkBytes / (hd * es));
   size_t cmax = std::max(std::max(3 * d, 2 * f), std::max(V, 2 * d));
   L.d_h = take(4 * (size_t)B * d);
   L.d_x = take(es * (size_t)B * std::max(2 * d, f));
+  L.d_m = take(es * (size_t)B * f);
   L.d_c = take(4 * (size_t)B * cmax);
   L.d_o = take(es * (size_t)B * d);
   L.d_part = take(4 * (size_t)B * H * L.n_chunks * (hd + 2));
+  L.d_cnt = take(sizeof(int) * (size_t)B * H);
   const size_t dec_end = off;
   // encoder region overlaps the decoder region (one call at a time per workspace)
   off = common_end;
   const size_t R = (size_t)B * T;
   L.e_h = take(4 * R * d);
-  L.e_a = take(es * R * std::max(d, f));
+  L.e_a = take(es * R * d);
+  L.e_m = take(es * R * f);
   L.e_c = take(4 * R * std::max(3 * d, 2 * f));
   L.e_q = take(es * R * d);
   L.e_k = take(es * R * d);
@@ -131,6 +143,125 @@ int gemm(cudaStream_t st, const T_* A, int lda, GemmB gb, int M, int N, int K, E
   }
   g_launches++;
   return launch_ok();
+}
+
+// ---------------------------------------------------------------------------
+// tensor-core GEMM launcher (bf16 models)
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tiled map of a row-major bf16 matrix [rows][cols] (row pitch ld elements),
+// box = 64 columns (128 bytes, swizzled) x box_rows rows; reads outside the
+// matrix return zeros.
+int tmap_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows) {
+  auto fn = tmap_encoder();
+  if (!fn) return RLT_ECUDA;
+  if (((uintptr_t)base & 15u) || (ld * 2) % 16) return RLT_EINVAL;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)tc::BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RLT_OK : RLT_ECUDA;
+}
+
+// Launch context of the tensor-core GEMMs.
+struct TcScratch {
+  int n_sm;
+  int* status;
+};
+
+template <int BN, int STAGES, bool GLU, class Epi>
+int gemm_tc_launch(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* B, const bf16* B3, int ldb,
+                   int N, Epi epi, const TcScratch& sc) {
+  using C = tc::Cfg<BN, STAGES>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, STAGES, GLU, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM) != cudaSuccess)
+      return RLT_ECUDA;
+    attr = true;
+  }
+  const int nout = GLU ? BN / 2 : BN;
+  const int tiles_n = (N + nout - 1) / nout, tiles_m = (M + tc::BM - 1) / tc::BM;
+  const int kb = (K + tc::BK - 1) / tc::BK;
+  // split K (a cluster of up to 8 CTAs per tile) until the grid covers the SMs
+  const int tiles = tiles_n * tiles_m;
+  int splits = 1;
+  if (tiles < sc.n_sm) splits = std::min(std::min(kb, 8), std::max(1, sc.n_sm / tiles));
+  const int kbps = (kb + splits - 1) / splits;
+  splits = (kb + kbps - 1) / kbps;
+  CUtensorMap ta, tb, tb3;
+  int rc;
+  if ((rc = tmap_bf16(&ta, A, M, K, lda, tc::BM))) return rc;
+  if ((rc = tmap_bf16(&tb, B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
+  if ((rc = tmap_bf16(&tb3, GLU ? B3 : B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
+  tc::SplitK sk{splits, kbps};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles_n, tiles_m, splits);
+  cfg.blockDim = dim3(tc::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = splits;
+  cfg.attrs = at;
+  cfg.numAttrs = splits > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi>, ta, tb, tb3, M, N, K, sk, epi, sc.status) !=
+      cudaSuccess)
+    return RLT_ECUDA;
+  g_launches++;
+  return launch_ok();
+}
+
+// C = A[M,K] B[N,K]^T with the epilogue functor; tiles sized for the shape.
+template <class Epi>
+int gemm_bf16_tc(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* B, int ldb, int N, Epi epi,
+                 const TcScratch& sc) {
+  if (M <= 0 || N <= 0) return RLT_OK;
+  if (M <= tc::BM) return gemm_tc_launch<128, 6, false>(st, A, lda, M, K, B, nullptr, ldb, N, epi, sc);
+  return gemm_tc_launch<256, 4, false>(st, A, lda, M, K, B, nullptr, ldb, N, epi, sc);
+}
+// out[m][j] = silu(A W_1^T)[m][j] * (A W_3^T)[m][j], j < N (= d_ffn).
+template <class Epi>
+int gemm_bf16_tc_glu(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* W1, const bf16* W3, int ldb,
+                     int N, Epi epi, const TcScratch& sc) {
+  if (M <= 0 || N <= 0) return RLT_OK;
+  if (M <= tc::BM) return gemm_tc_launch<128, 6, true>(st, A, lda, M, K, W1, W3, ldb, N, epi, sc);
+  return gemm_tc_launch<256, 4, true>(st, A, lda, M, K, W1, W3, ldb, N, epi, sc);
+}
+
+TcScratch tc_scratch(const rlt_model* m, void* ws, const WsLayout& Lw) {
+  TcScratch sc;
+  sc.n_sm = m->n_sm;
+  sc.status = at<int>(ws, Lw.status);
+  return sc;
+}
+
+// y = A W^T with the epilogue: tensor cores for bf16 models, FFMA for fp32.
+template <typename T_, class Epi>
+int proj(cudaStream_t st, const T_* A, int lda, int M, int K, const void* W, int ldw, int N, Epi epi,
+         const TcScratch& sc) {
+  if constexpr (std::is_same<T_, bf16>::value)
+    return gemm_bf16_tc(st, A, lda, M, K, static_cast<const bf16*>(W), ldw, N, epi, sc);
+  else
+    return gemm<T_>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, epi);
 }
 
 template <typename T_>
@@ -170,6 +301,22 @@ void ensure_attrs() {
 // ---------------------------------------------------------------------------
 // encoder
 
+// out[m][j] = silu(A W_1^T)[m][j] * (A W_3^T)[m][j] in storage precision (j < f);
+// fp32 models go through an fp32 buffer C [M][2f] and a separate kernel.
+template <typename T_>
+int swiglu_proj(cudaStream_t st, const T_* A, int lda, int M, int K, const T_* W1, const T_* W3, int f, T_* out,
+                float* C, const TcScratch& sc) {
+  if constexpr (std::is_same<T_, bf16>::value) {
+    return gemm_bf16_tc_glu(st, A, lda, M, K, W1, W3, K, f, EpiStoreT<bf16>{out, f}, sc);
+  } else {
+    int rc = gemm<T_>(st, A, lda, GemmB{W1, W3, f, K}, M, 2 * f, K, EpiStoreF32{C, 2 * f});
+    if (rc) return rc;
+    swiglu_kernel<T_><<<cdiv((size_t)M * f, 256), 256, 0, st>>>(C, out, M, f);
+    g_launches++;
+    return launch_ok();
+  }
+}
+
 template <typename T_>
 int encode_impl(const rlt_model* m, const int32_t* tok, int B, int T, T_* e, T_* mem, void* ws, cudaStream_t st) {
   const rlt_config& c = m->cfg;
@@ -181,11 +328,13 @@ int encode_impl(const rlt_model* m, const int32_t* tok, int B, int T, T_* e, T_*
   float2* tab = at<float2>(ws, Lw.rope);
   float* h = at<float>(ws, Lw.e_h);
   T_* a = at<T_>(ws, Lw.e_a);
+  T_* am = at<T_>(ws, Lw.e_m);
   float* C = at<float>(ws, Lw.e_c);
   T_* q = at<T_>(ws, Lw.e_q);
   T_* k = at<T_>(ws, Lw.e_k);
   T_* v = at<T_>(ws, Lw.e_v);
   T_* o = at<T_>(ws, Lw.e_o);
+  const TcScratch sc = tc_scratch(m, ws, Lw);
   int rc;
   rope_table_kernel<<<cdiv((size_t)T * (hd / 2), 256), 256, 0, st>>>(tab, 0, T, hd / 2, (double)c.rope_theta);
   g_launches++;
@@ -197,32 +346,28 @@ int encode_impl(const rlt_model* m, const int32_t* tok, int B, int T, T_* e, T_*
   for (int l = 0; l < L; ++l) {
     if ((rc = rmsnorm<T_>(st, h, w.enc_attn_norm + (size_t)l * d, a, R, d, d, c.rms_eps))) return rc;
     const T_* Wqkv = wl<T_>(w.W_qkv, l, (size_t)3 * d * d);
-    if ((rc = gemm<T_>(st, a, d, GemmB{Wqkv, Wqkv, 3 * d, d}, R, 3 * d, d, EpiStoreF32{C, 3 * d}))) return rc;
+    if ((rc = proj<T_>(st, a, d, R, d, Wqkv, d, 3 * d, EpiStoreF32{C, 3 * d}, sc))) return rc;
     rope_split_kernel<T_><<<cdiv((size_t)R * H * (hd / 2), 256), 256, 0, st>>>(C, q, k, v, tab, B, T, H, hd);
     g_launches++;
     enc_attn_simt_kernel<T_><<<dim3(cdiv(T, 32), H, B), 256, att_smem, st>>>(q, k, v, o, T, H, hd, scale);
     g_launches++;
     if ((rc = launch_ok())) return rc;
     const T_* WO = wl<T_>(w.W_O, l, (size_t)d * d);
-    if ((rc = gemm<T_>(st, o, d, GemmB{WO, WO, d, d}, R, d, d, EpiAddF32{h, d}))) return rc;
+    if ((rc = proj<T_>(st, o, d, R, d, WO, d, d, EpiAddF32{h, d}, sc))) return rc;
     if ((rc = rmsnorm<T_>(st, h, w.enc_ffn_norm + (size_t)l * d, a, R, d, d, c.rms_eps))) return rc;
     const T_* W1 = wl<T_>(w.W_1, l, (size_t)f * d);
     const T_* W3 = wl<T_>(w.W_3, l, (size_t)f * d);
-    if ((rc = gemm<T_>(st, a, d, GemmB{W1, W3, f, d}, R, 2 * f, d, EpiStoreF32{C, 2 * f}))) return rc;
-    swiglu_kernel<T_><<<cdiv((size_t)R * f, 256), 256, 0, st>>>(C, a, R, f);
-    g_launches++;
+    if ((rc = swiglu_proj<T_>(st, a, d, R, d, W1, W3, f, am, C, sc))) return rc;
     const T_* W2 = wl<T_>(w.W_2, l, (size_t)d * f);
-    if ((rc = gemm<T_>(st, a, f, GemmB{W2, W2, d, f}, R, d, f, EpiAddF32{h, d}))) return rc;
+    if ((rc = proj<T_>(st, am, f, R, f, W2, f, d, EpiAddF32{h, d}, sc))) return rc;
   }
   if ((rc = rmsnorm<T_>(st, h, w.enc_norm, e, R, d, d, c.rms_eps))) return rc;
   const size_t plane = (size_t)B * H * T * hd;
   for (int g = 0; g < G; ++g) {
     const T_* WK = wl<T_>(w.W_K, g, (size_t)d * d);
     const T_* WV = wl<T_>(w.W_V, g, (size_t)d * d);
-    if ((rc = gemm<T_>(st, e, d, GemmB{WK, WK, d, d}, R, d, d, EpiMemScatter<T_>{mem + (2 * g) * plane, T, H, hd})))
-      return rc;
-    if ((rc = gemm<T_>(st, e, d, GemmB{WV, WV, d, d}, R, d, d,
-                       EpiMemScatter<T_>{mem + (2 * g + 1) * plane, T, H, hd})))
+    if ((rc = proj<T_>(st, e, d, R, d, WK, d, d, EpiMemScatter<T_>{mem + (2 * g) * plane, T, H, hd}, sc))) return rc;
+    if ((rc = proj<T_>(st, e, d, R, d, WV, d, d, EpiMemScatter<T_>{mem + (2 * g + 1) * plane, T, H, hd}, sc)))
       return rc;
   }
   return RLT_OK;
@@ -257,7 +402,9 @@ int enqueue_step(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* 
   const float2* tab = at<float2>(ws, Lw.rope);
   float* h = at<float>(ws, Lw.d_h);
   T_* x = at<T_>(ws, Lw.d_x);
+  T_* xm = at<T_>(ws, Lw.d_m);
   float* C = at<float>(ws, Lw.d_c);
+  const TcScratch sc = tc_scratch(m, ws, Lw);
   T_* o = at<T_>(ws, Lw.d_o);
   float* part = at<float>(ws, Lw.d_part);
   const T_* e = static_cast<const T_*>(A.e);
@@ -297,7 +444,7 @@ int enqueue_step(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* 
     if ((rc = post())) return rc;
     const T_* Wg = static_cast<const T_*>(w.W_g);
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm<T_>(st, x, 2 * d, GemmB{Wg, Wg, d, 2 * d}, B, d, 2 * d, EpiStoreF32{C, d}))) return rc;
+    if ((rc = proj<T_>(st, x, 2 * d, B, 2 * d, Wg, 2 * d, d, EpiStoreF32{C, d}, sc))) return rc;
     nk++;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
   }
@@ -309,25 +456,56 @@ int enqueue_step(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* 
   T_* rk = static_cast<T_*>(sst->ring_k);
   T_* rv = static_cast<T_*>(sst->ring_v);
   const size_t swa_smem = sizeof(float) * (hd + Wn);
-  const size_t xa_smem = sizeof(float) * (hd + kXChunk + 128);
-  const int n_chunks = (int)cdiv(A.T_mem, kXChunk);
+  XattnArgs xa{};
+  xa.part = part;
+  xa.cnt = at<int>(ws, Lw.d_cnt);
+  xa.out = o;
+  xa.q = C;
+  xa.B = B;
+  xa.H = H;
+  xa.T_mem = A.T_mem;
+  xa.t_cap = A.T_mem;
+  xa.max_chunks = Lw.n_chunks;
+  xa.scale = scale;
+  xa.ctx = ctx;
+  xa.status = status;
   for (int l = 0; l < L; ++l) {
     // self-attention over the window
     if ((rc = rmsnorm<T_>(st, h, w.dec_attn_norm + (size_t)l * d, x, B, d, d, c.rms_eps))) return rc;
     nk++;
     const T_* Wqkv = wl<T_>(w.W_qkv, l, (size_t)3 * d * d);
-    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm<T_>(st, x, d, GemmB{Wqkv, Wqkv, 3 * d, d}, B, 3 * d, d, EpiStoreF32{C, 3 * d}))) return rc;
-    nk++;
-    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = mark(RLT_TIMER_SWA))) return rc;
-    dec_swa_kernel<T_><<<dim3(H, B), 128, swa_smem, st>>>(C, rk + l * ring_layer, rv + l * ring_layer, o, tab, H, hd,
-                                                          Wn, scale, ctx);
-    if ((rc = post())) return rc;
-    if ((rc = mark(RLT_TIMER_SWA))) return rc;
+    if constexpr (std::is_same<T_, bf16>::value) {
+      // QKV on the tensor cores; the epilogue applies RoPE, keeps q in C and
+      // writes k, v to ring slot p mod W; then attention over the ring
+      if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+      EpiQKVRope<T_> eq{C, rk + l * ring_layer, rv + l * ring_layer, tab, ctx, d, H, hd, Wn};
+      if ((rc = gemm_bf16_tc(st, x, d, B, d, Wqkv, d, 3 * d, eq, sc))) return rc;
+      nk++;
+      if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+      if ((rc = mark(RLT_TIMER_SWA))) return rc;
+      XattnArgs sa = xa;
+      sa.q = C;
+      sa.mk = rk + l * ring_layer;
+      sa.mv = rv + l * ring_layer;
+      sa.T_mem = Wn;
+      sa.t_cap = Wn;
+      if (launch_xattn<T_>(sa, hd, m->n_sm, st) != cudaSuccess) return RLT_ECUDA;
+      if ((rc = post())) return rc;
+      if ((rc = mark(RLT_TIMER_SWA))) return rc;
+    } else {
+      if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+      if ((rc = proj<T_>(st, x, d, B, d, Wqkv, d, 3 * d, EpiStoreF32{C, 3 * d}, sc))) return rc;
+      nk++;
+      if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+      if ((rc = mark(RLT_TIMER_SWA))) return rc;
+      dec_swa_kernel<T_><<<dim3(H, B), 128, swa_smem, st>>>(C, rk + l * ring_layer, rv + l * ring_layer, o, tab, H,
+                                                            hd, Wn, scale, ctx);
+      if ((rc = post())) return rc;
+      if ((rc = mark(RLT_TIMER_SWA))) return rc;
+    }
     const T_* WO = wl<T_>(w.W_O, l, (size_t)d * d);
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm<T_>(st, o, d, GemmB{WO, WO, d, d}, B, d, d, EpiAddF32{h, d}))) return rc;
+    if ((rc = proj<T_>(st, o, d, B, d, WO, d, d, EpiAddF32{h, d}, sc))) return rc;
     nk++;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     // cross-attention to memory positions 0..p
@@ -335,20 +513,19 @@ int enqueue_step(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* 
     nk++;
     const T_* WQx = wl<T_>(w.W_Qx, l, (size_t)d * d);
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm<T_>(st, x, d, GemmB{WQx, WQx, d, d}, B, d, d, EpiStoreF32{C, d}))) return rc;
+    if ((rc = proj<T_>(st, x, d, B, d, WQx, d, d, EpiStoreF32{C, d}, sc))) return rc;
     nk++;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     const int g = (c.mem_groups == 1) ? 0 : l;
     if ((rc = mark(RLT_TIMER_XATTN))) return rc;
-    dec_xattn_part_kernel<T_><<<dim3(n_chunks, H, B), 128, xa_smem, st>>>(
-        C, mem + (2 * g) * plane, mem + (2 * g + 1) * plane, part, H, hd, A.T_mem, n_chunks, scale, ctx);
-    if ((rc = post())) return rc;
-    dec_xattn_combine_kernel<T_><<<dim3(H, B), 128, 0, st>>>(part, o, H, hd, n_chunks, ctx);
+    xa.mk = mem + (2 * g) * plane;
+    xa.mv = mem + (2 * g + 1) * plane;
+    if (launch_xattn<T_>(xa, hd, m->n_sm, st) != cudaSuccess) return RLT_ECUDA;
     if ((rc = post())) return rc;
     if ((rc = mark(RLT_TIMER_XATTN))) return rc;
     const T_* WOx = wl<T_>(w.W_Ox, l, (size_t)d * d);
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm<T_>(st, o, d, GemmB{WOx, WOx, d, d}, B, d, d, EpiAddF32{h, d}))) return rc;
+    if ((rc = proj<T_>(st, o, d, B, d, WOx, d, d, EpiAddF32{h, d}, sc))) return rc;
     nk++;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     // SwiGLU FFN
@@ -357,14 +534,15 @@ int enqueue_step(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* 
     const T_* W1 = wl<T_>(w.W_1, l, (size_t)f * d);
     const T_* W3 = wl<T_>(w.W_3, l, (size_t)f * d);
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm<T_>(st, x, d, GemmB{W1, W3, f, d}, B, 2 * f, d, EpiStoreF32{C, 2 * f}))) return rc;
-    nk++;
+    {
+      const uint64_t l0 = g_launches.load();
+      if ((rc = swiglu_proj<T_>(st, x, d, B, d, W1, W3, f, xm, C, sc))) return rc;
+      nk += (int)(g_launches.load() - l0);
+    }
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    swiglu_kernel<T_><<<cdiv((size_t)B * f, 256), 256, 0, st>>>(C, x, B, f);
-    if ((rc = post())) return rc;
     const T_* W2 = wl<T_>(w.W_2, l, (size_t)d * f);
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm<T_>(st, x, f, GemmB{W2, W2, d, f}, B, d, f, EpiAddF32{h, d}))) return rc;
+    if ((rc = proj<T_>(st, xm, f, B, f, W2, f, d, EpiAddF32{h, d}, sc))) return rc;
     nk++;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
   }
@@ -374,7 +552,7 @@ int enqueue_step(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* 
   if ((rc = post())) return rc;
   const T_* Wo = static_cast<const T_*>(w.W_o);
   if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-  if ((rc = gemm<T_>(st, x, d, GemmB{Wo, Wo, V, d}, B, V, d, EpiStoreF32{C, V}))) return rc;
+  if ((rc = proj<T_>(st, x, d, B, d, Wo, d, V, EpiStoreF32{C, V}, sc))) return rc;
   nk++;
   if ((rc = mark(RLT_TIMER_GEMM))) return rc;
   HeadArgs ha;
@@ -420,6 +598,7 @@ int decode_impl(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const i
                                                                    (double)c.rope_theta);
   g_launches++;
   if ((rc = launch_ok())) return rc;
+  RLT_CUDA_TRY(cudaMemsetAsync(at<int>(ws, Lw.d_cnt), 0, sizeof(int) * (size_t)B * c.n_heads, st));
   // capture one step and replay it n times
   cudaStream_t cs = m->cap_stream;
   cudaGraph_t graph = nullptr;
@@ -533,6 +712,14 @@ int rlt_model_create(const rlt_config* cfg, const rlt_weights* w, uint64_t versi
   m->version = version;
   m->esz = (cfg->dtype == RLT_BF16) ? 2 : 4;
   m->timer = nullptr;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&m->n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || m->n_sm < 1) {
+      delete m;
+      return RLT_ECUDA;
+    }
+  }
   if (cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
     delete m;
     return RLT_ECUDA;
@@ -599,8 +786,8 @@ int rlt_workspace_size(const rlt_model* m, int32_t B, int32_t T_max, size_t* byt
 }
 
 int rlt_workspace_init(void* ws, size_t ws_bytes, rlt_stream_t stream) {
-  if (!ws || ws_bytes < 256 || !aligned16(ws)) return RLT_EINVAL;
-  RLT_CUDA_TRY(cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream)));
+  if (!ws || ws_bytes < kWsHeaderBytes || !aligned16(ws)) return RLT_EINVAL;
+  RLT_CUDA_TRY(cudaMemsetAsync(ws, 0, kWsHeaderBytes, reinterpret_cast<cudaStream_t>(stream)));
   return RLT_OK;
 }
 
@@ -690,22 +877,43 @@ int rlt_cross_attention(const rlt_model* m, const float* q, const void* mem_k, c
   const int H = c.n_heads, hd = c.head_dim;
   StepCtx* ctx = at<StepCtx>(ws, Lw.ctx);
   float* part = at<float>(ws, Lw.d_part);
-  const int n_chunks = (int)cdiv(T_mem, kXChunk);
-  const float scale = 1.0f / sqrtf((float)hd);
-  const size_t xa_smem = sizeof(float) * (hd + kXChunk + 128);
+  XattnArgs xa{};
+  xa.q = q;
+  xa.mk = mem_k;
+  xa.mv = mem_v;
+  xa.part = part;
+  xa.cnt = at<int>(ws, Lw.d_cnt);
+  xa.out = out;
+  xa.B = B;
+  xa.H = H;
+  xa.T_mem = T_mem;
+  xa.t_cap = T_mem;
+  xa.max_chunks = Lw.n_chunks;
+  xa.scale = 1.0f / sqrtf((float)hd);
+  xa.ctx = ctx;
+  xa.status = at<int>(ws, Lw.status);
   set_ctx_kernel<<<1, 1, 0, s>>>(ctx, t - 1);
-  if (c.dtype == RLT_BF16) {
-    dec_xattn_part_kernel<bf16><<<dim3(n_chunks, H, B), 128, xa_smem, s>>>(
-        q, static_cast<const bf16*>(mem_k), static_cast<const bf16*>(mem_v), part, H, hd, T_mem, n_chunks, scale, ctx);
-    dec_xattn_combine_kernel<bf16><<<dim3(H, B), 128, 0, s>>>(part, static_cast<bf16*>(out), H, hd, n_chunks, ctx);
-  } else {
-    dec_xattn_part_kernel<float><<<dim3(n_chunks, H, B), 128, xa_smem, s>>>(
-        q, static_cast<const float*>(mem_k), static_cast<const float*>(mem_v), part, H, hd, T_mem, n_chunks, scale,
-        ctx);
-    dec_xattn_combine_kernel<float><<<dim3(H, B), 128, 0, s>>>(part, static_cast<float*>(out), H, hd, n_chunks, ctx);
-  }
-  g_launches += 3;
+  RLT_CUDA_TRY(cudaMemsetAsync(xa.cnt, 0, sizeof(int) * (size_t)B * H, s));
+  cudaError_t ce = (c.dtype == RLT_BF16) ? launch_xattn<bf16>(xa, hd, m->n_sm, s) : launch_xattn<float>(xa, hd, m->n_sm, s);
+  if (ce != cudaSuccess) return RLT_ECUDA;
+  g_launches += 2;
   return launch_ok();
+}
+
+int rlt_linear(const rlt_model* m, const void* A, int32_t lda, int32_t M, int32_t K, const void* W, const void* W3,
+               int32_t ldw, int32_t N, float* C, int32_t ldc, void* ws, size_t ws_bytes, rlt_stream_t stream) {
+  if (!m || !A || !W || !C || !ws || M <= 0 || K <= 0 || N <= 0 || lda < K || ldw < K || ldc < N) return RLT_EINVAL;
+  if (m->cfg.dtype != RLT_BF16) return RLT_EUNSUPPORTED;
+  if (!aligned16(A) || !aligned16(W) || (W3 && !aligned16(W3)) || !aligned16(ws) || lda % 8 || ldw % 8)
+    return RLT_EINVAL;
+  WsLayout Lw = layout(m, 1, 1);
+  if (ws_bytes < Lw.total) return RLT_EWORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const TcScratch sc = tc_scratch(m, ws, Lw);
+  const bf16* a = static_cast<const bf16*>(A);
+  const bf16* w = static_cast<const bf16*>(W);
+  if (W3) return gemm_bf16_tc_glu(s, a, lda, M, K, w, static_cast<const bf16*>(W3), ldw, N, EpiStoreF32{C, ldc}, sc);
+  return gemm_bf16_tc(s, a, lda, M, K, w, ldw, N, EpiStoreF32{C, ldc}, sc);
 }
 
 int rlt_status(void* ws, rlt_stream_t stream) {
