@@ -209,10 +209,10 @@ RLT_API int rlt_linear(const rlt_model* m, const void* A, int32_t lda, int32_t M
  * fixed 16 MiB array inside the library, so no workspace is passed and the
  * shape comes as plain sizes (n_heads, head_dim, dtype = RLT_F32/RLT_BF16).
  * The pages have no counterpart: this is an integration convenience.
- *  - Limit: with CH = 16384 / (head_dim * element bytes) positions per chunk,
- *    round_up(4 * B * n_heads, 256) + B * n_heads * ceil(T_mem / CH) *
- *    (head_dim + 2) * 4 bytes must fit in 16 MiB - 256 B; larger requests
- *    return RLT_EUNSUPPORTED.
+ *  - Limit: round_up(4 * B * n_heads, 256) + B * n_heads * 32 * (head_dim + 2)
+ *    * 4 bytes (arrival counters and up to 32 partial results per (b, h)) must
+ *    fit in 16 MiB - 256 B, i.e. B * n_heads <= 1007 at head_dim 128; larger
+ *    requests return RLT_EUNSUPPORTED.
  *  - The first call on a device looks up the array's device address (set-up);
  *    make that first call before any stream capture.
  *  - Every call shares the array: calls that overlap on the GPU race.

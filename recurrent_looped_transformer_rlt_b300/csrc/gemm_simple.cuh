@@ -14,7 +14,10 @@ namespace rlt {
 // ---------------------------------------------------------------------------
 // epilogues: operator()(m, n, acc) is called once per in-range element.
 
+// kStore4 / kAdd4: the tensor-core kernel writes (or adds into) C four
+// columns at a time with 16-byte accesses (needs ldc % 4 == 0).
 struct EpiStoreF32 {
+  static constexpr bool kStore4 = true;
   float* C;
   int ldc;
   __device__ __forceinline__ void operator()(int m, int n, float v) const { C[(size_t)m * ldc + n] = v; }
@@ -26,6 +29,7 @@ struct EpiStoreT {  // store rounded to the storage type
   __device__ __forceinline__ void operator()(int m, int n, float v) const { C[(size_t)m * ldc + n] = from_f32<T>(v); }
 };
 struct EpiAddF32 {  // residual stream update h += acc
+  static constexpr bool kAdd4 = true;
   float* C;
   int ldc;
   __device__ __forceinline__ void operator()(int m, int n, float v) const { C[(size_t)m * ldc + n] += v; }
@@ -75,6 +79,96 @@ struct EpiQKVRope {
       ring_k[o] = from_f32<T>(y1);
       ring_k[o + half] = from_f32<T>(y2);
     }
+  }
+};
+
+// Encoder QKV projection with RoPE, in pairs (i, i + hd/2) of one head: row
+// m = b*T + t; q and k rotated at position t, v plain; all three rounded to
+// storage and written head-major [B][H][T][hd].
+template <typename T>
+struct EpiEncQKVRope {
+  static constexpr bool kPair = true;
+  T* q;
+  T* k;
+  T* v;
+  const float2* tab;  // [position][hd/2]
+  int d, H, hd, T_len;
+  __device__ __forceinline__ void pair(int m, int n, float x1, float x2) const {
+    const int which = n / d, r = n - which * d;
+    const int head = r / hd, i = r - head * hd, half = hd >> 1;
+    const int b = m / T_len, t = m - b * T_len;
+    const size_t o = (((size_t)b * H + head) * T_len + t) * hd + i;
+    if (which == 2) {
+      v[o] = from_f32<T>(x1);
+      v[o + half] = from_f32<T>(x2);
+      return;
+    }
+    const float2 cs = tab[(size_t)t * half + i];
+    T* dst = (which == 0) ? q : k;
+    dst[o] = from_f32<T>(x1 * cs.x - x2 * cs.y);
+    dst[o + half] = from_f32<T>(x2 * cs.x + x1 * cs.y);
+  }
+};
+
+// Epilogues that produce the residual stream h (fp32 [M][ldh]) declare kHOut,
+// load(m, n) of what they combine with and combine(aux, acc4, n) -> the new
+// h[m][n..n+3].  The kernel then writes h, x = bf16(h * g) (the A operand of
+// the next projection: gain of the next RMSNorm applied, its row scale
+// deferred to that projection), optional copies s (fp32) and s16 (bf16), and
+// per row and 128-column block the sum of squares ss[n / 128][m].
+struct HOut {
+  float* h;
+  int ldh;
+  bf16* x;
+  const float* g;
+  float* s;
+  bf16* s16;
+  float* ss;
+  int M;
+};
+// h += acc (a residual update).
+struct EpiResidual {
+  static constexpr bool kHOut = true;
+  HOut o;
+  struct Aux {
+    float4 old;
+  };
+  __device__ __forceinline__ Aux load(int m, int n) const {
+    return Aux{*reinterpret_cast<const float4*>(o.h + (size_t)m * o.ldh + n)};
+  }
+  __device__ __forceinline__ float4 combine(const Aux& a, float4 v, int) const {
+    return make_float4(a.old.x + v.x, a.old.y + v.y, a.old.z + v.z, a.old.w + v.w);
+  }
+};
+// The gated merge h = z * s_{t-1} + (1 - z) * e_t with z = sigmoid(acc + b_g)
+// (acc = W_g [e_t; s_{t-1}]); with discard, h = e_t.
+struct EpiMerge {
+  static constexpr bool kHOut = true;
+  HOut o;
+  const bf16* e;       // [B][T][d], row of sequence m at position ctx->pos
+  size_t e_seq_stride;  // T * d
+  const float* s_prev;  // [B][d]
+  const float* bg;      // [d]
+  const StepCtx* ctx;
+  int discard;
+  struct Aux {
+    float4 e, s;
+  };
+  __device__ __forceinline__ Aux load(int m, int n) const {
+    const bf16* ep = e + (size_t)m * e_seq_stride + (size_t)ctx->pos * o.ldh + n;
+    const uint2 u = *reinterpret_cast<const uint2*>(ep);
+    const float2 e01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 e23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return Aux{make_float4(e01.x, e01.y, e23.x, e23.y),
+               *reinterpret_cast<const float4*>(s_prev + (size_t)m * o.ldh + n)};
+  }
+  __device__ __forceinline__ float4 combine(const Aux& a, float4 v, int n) const {
+    if (discard) return a.e;
+    const float4 b = *reinterpret_cast<const float4*>(bg + n);
+    const float z0 = sigmoid_f(v.x + b.x), z1 = sigmoid_f(v.y + b.y), z2 = sigmoid_f(v.z + b.z),
+                z3 = sigmoid_f(v.w + b.w);
+    return make_float4(z0 * a.s.x + (1.f - z0) * a.e.x, z1 * a.s.y + (1.f - z1) * a.e.y,
+                       z2 * a.s.z + (1.f - z2) * a.e.z, z3 * a.s.w + (1.f - z3) * a.e.w);
   }
 };
 

@@ -57,6 +57,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
       "l"(tm), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::
+          "r"(smem_u32(dst)),
+      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(tm) : "memory");
 }
@@ -124,6 +131,38 @@ template <class E, class = void>
 struct IsPairEpi : std::false_type {};
 template <class E>
 struct IsPairEpi<E, std::void_t<decltype(E::kPair)>> : std::true_type {};
+template <class E, class = void>
+struct IsStore4Epi : std::false_type {};
+template <class E>
+struct IsStore4Epi<E, std::void_t<decltype(E::kStore4)>> : std::true_type {};
+template <class E, class = void>
+struct IsHOutEpi : std::false_type {};
+template <class E>
+struct IsHOutEpi<E, std::void_t<decltype(E::kHOut)>> : std::true_type {};
+template <class E, class = void>
+struct IsAdd4Epi : std::false_type {};
+template <class E>
+struct IsAdd4Epi<E, std::void_t<decltype(E::kAdd4)>> : std::true_type {};
+
+// Where the A tiles come from.  k-blocks below split_kb are read through tmA
+// (a 2-D map [M][K], or with pos3d a 3-D map [M][T][K] at position
+// ctx->pos: one row of each sequence), the rest through tmA2 (a 2-D map whose
+// column 0 is k = split_kb * BK).
+struct AOperand {
+  int split_kb;
+  int pos3d;
+  const StepCtx* ctx;
+};
+
+// Deferred RMSNorm: when ss != nullptr, output row m is multiplied by
+// rsqrt(sum_{p < parts} ss[p * M + m] * inv_d + eps), the row's RMS scale; the
+// A operand then holds x * g (the gain applied, the scale not), and since the
+// scale is one number per row it factors out of the contraction.
+struct RowScale {
+  const float* ss;
+  int parts;
+  float inv_d, eps;
+};
 
 struct SplitK {
   int splits;        // CTAs along K (= cluster size along z when > 1)
@@ -152,8 +191,9 @@ __device__ __forceinline__ float4 ld_dsmem_f4(const void* local, uint32_t rank) 
 // silu(gate) * linear.
 template <int BN, int STAGES, bool GLU, class Epi>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmB3, int M, int N, int K, SplitK sk, Epi epi, int* status) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3, int M, int N,
+                   int K, AOperand ao, RowScale rsc, SplitK sk, Epi epi, int* status) {
   using C = Cfg<BN, STAGES>;
   constexpr int NOUT = GLU ? BN / 2 : BN;  // output columns per tile
   extern __shared__ unsigned char smem_raw[];
@@ -185,6 +225,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmA2);
     tma_prefetch_desc(&tmB);
     if (GLU) tma_prefetch_desc(&tmB3);
   }
@@ -196,6 +237,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      const int pos = ao.pos3d ? ao.ctx->pos : 0;
       for (int i = 0; i < nkb; ++i) {
         const int s = i % STAGES;
         if (i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, kWaitBudget)) {
@@ -205,7 +247,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         unsigned char* sa = smem + s * C::STAGE_BYTES;
         const int kx = (kb0 + i) * BK;
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-        tma_load_2d(sa, &tmA, kx, m0, &full[s]);
+        if (kb0 + i < ao.split_kb) {
+          if (ao.pos3d)
+            tma_load_3d(sa, &tmA, kx, pos, m0, &full[s]);
+          else
+            tma_load_2d(sa, &tmA, kx, m0, &full[s]);
+        } else {
+          tma_load_2d(sa, &tmA2, kx - ao.split_kb * BK, m0, &full[s]);
+        }
         if (GLU) {
           tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[s]);
           tma_load_2d(sa + C::A_BYTES + C::B_BYTES / 2, &tmB3, kx, nb0, &full[s]);
@@ -249,13 +298,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int LDT = BN + 4;
     float* stile = reinterpret_cast<float*>(smem);
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    float rs = 1.f;
+    if (rsc.ss && m0 + rl < M) {
+      float acc = 0.f;
+      for (int p = 0; p < rsc.parts; ++p) acc += rsc.ss[(size_t)p * M + m0 + rl];
+      rs = rsqrtf(acc * rsc.inv_d + rsc.eps);
+    }
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
       float v[16];
       tmem_ld16(tq + c0, v);
 #pragma unroll
       for (int j = 0; j < 16; j += 4)
-        *reinterpret_cast<float4*>(stile + rl * LDT + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        *reinterpret_cast<float4*>(stile + rl * LDT + c0 + j) =
+            make_float4(v[j] * rs, v[j + 1] * rs, v[j + 2] * rs, v[j + 3] * rs);
     }
     epi_bar();
   }
@@ -329,6 +385,87 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int hb = pi / half, ii = pi - hb * half;
           const int c = hb * 2 * half + ii;
           if (nb0 + c < N) epi.pair(m0 + r, nb0 + c, stile[r * LDT + c], stile[r * LDT + c + half]);
+        }
+      } else if constexpr (IsHOutEpi<Epi>::value) {
+        // the residual stream: N a multiple of BN and rows 16-byte aligned
+        // (checked by the host); a warp covers 128 consecutive columns of one row
+        constexpr int V4 = BN / 4;
+        const int n = (r1 - r0) * V4;
+        const HOut& o = epi.o;
+        for (int i0 = et; i0 < n; i0 += 4 * 128) {
+          typename Epi::Aux aux[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * 128;
+            if (i < n) aux[u] = epi.load(m0 + r0 + i / V4, nb0 + (i % V4) * 4);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * 128;
+            if (i >= n) continue;  // warp-uniform: n is a multiple of 32
+            const int r = r0 + i / V4, c = (i % V4) * 4;
+            const int m = m0 + r, col = nb0 + c;
+            const float4 hv = epi.combine(aux[u], *reinterpret_cast<const float4*>(stile + r * LDT + c), col);
+            const size_t off = (size_t)m * o.ldh + col;
+            *reinterpret_cast<float4*>(o.h + off) = hv;
+            if (o.s) *reinterpret_cast<float4*>(o.s + off) = hv;
+            const float4 gg = *reinterpret_cast<const float4*>(o.g + col);
+            __nv_bfloat162 x01 = __floats2bfloat162_rn(hv.x * gg.x, hv.y * gg.y);
+            __nv_bfloat162 x23 = __floats2bfloat162_rn(hv.z * gg.z, hv.w * gg.w);
+            uint2 xp;
+            xp.x = *reinterpret_cast<unsigned*>(&x01);
+            xp.y = *reinterpret_cast<unsigned*>(&x23);
+            *reinterpret_cast<uint2*>(o.x + off) = xp;
+            if (o.s16) {
+              __nv_bfloat162 s01 = __floats2bfloat162_rn(hv.x, hv.y);
+              __nv_bfloat162 s23 = __floats2bfloat162_rn(hv.z, hv.w);
+              uint2 sp;
+              sp.x = *reinterpret_cast<unsigned*>(&s01);
+              sp.y = *reinterpret_cast<unsigned*>(&s23);
+              *reinterpret_cast<uint2*>(o.s16 + off) = sp;
+            }
+            const float q2 = warp_sum(hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w);
+            if ((et & 31) == 0) o.ss[(size_t)(col >> 7) * o.M + m] = q2;
+          }
+        }
+      } else if constexpr (IsStore4Epi<Epi>::value || IsAdd4Epi<Epi>::value) {
+        // 16-byte accesses, four per thread in flight (reads of the residual
+        // first, then the stores); full 4-column groups only, the rest below.
+        // An output whose rows are not 16-byte aligned takes the scalar path.
+        constexpr int V4 = BN / 4;
+        const bool vec = (epi.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(epi.C) & 15u) == 0);
+        const int nq = vec ? min(V4, (N - nb0) / 4) : 0;  // whole float4 columns inside N
+        const int n = vec ? (r1 - r0) * V4 : 0;
+        for (int i0 = et; i0 < n; i0 += 4 * 128) {
+          float4 v[4], o[4];
+          float* dst[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * 128;
+            const int r = r0 + i / V4, c4 = i % V4;
+            dst[u] = (i < n && c4 < nq) ? epi.C + (size_t)(m0 + r) * epi.ldc + nb0 + c4 * 4 : nullptr;
+            v[u] = dst[u] ? *reinterpret_cast<const float4*>(stile + r * LDT + c4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (IsAdd4Epi<Epi>::value)
+              o[u] = dst[u] ? *reinterpret_cast<const float4*>(dst[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (!dst[u]) continue;
+            if constexpr (IsAdd4Epi<Epi>::value) {
+              v[u].x += o[u].x;
+              v[u].y += o[u].y;
+              v[u].z += o[u].z;
+              v[u].w += o[u].w;
+            }
+            *reinterpret_cast<float4*>(dst[u]) = v[u];
+          }
+        }
+        if (nb0 + 4 * nq < N && nq < V4) {  // ragged last columns of N (all of them without vec)
+          const int c_beg = 4 * nq, w = min(BN, N - nb0) - c_beg;
+          for (int i = et; i < (r1 - r0) * w; i += 128) {
+            const int r = r0 + i / w, c = c_beg + i % w;
+            epi(m0 + r, nb0 + c, stile[r * LDT + c]);
+          }
         }
       } else {
         const int n = (r1 - r0) * BN;

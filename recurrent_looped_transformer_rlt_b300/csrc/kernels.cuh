@@ -41,6 +41,43 @@ __global__ void embed_kernel(const int* __restrict__ tok, const T_* __restrict__
   for (int j = threadIdx.x; j < d; j += blockDim.x) h[(size_t)r * d + j] = to_f32(emb[(size_t)x * d + j]);
 }
 
+// Token embedding of bf16 models, with the first RMSNorm deferred: h[r] =
+// tok_emb[tok[r]] (fp32), x[r] = bf16(h[r] * g) and per 128-column block j the
+// sum of squares ss[j][r] (the consumer applies the row scale).  Block = one
+// row, d/4 threads, 4 columns each (warp w covers columns 128w .. 128w+127).
+__global__ void embed_norm_kernel(const int* __restrict__ tok, const bf16* __restrict__ emb, float* __restrict__ h,
+                                  bf16* __restrict__ xo, const float* __restrict__ g, float* __restrict__ ss,
+                                  int rows, int d, int V, int* status) {
+  const int r = blockIdx.x, c = threadIdx.x * 4;
+  if (r >= rows) return;
+  int t = tok[r];
+  const bool bad = (t < 0 || t >= V);
+  if (bad && threadIdx.x == 0) set_error(status, kErrBounds);
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!bad) {
+    const uint2 u = *reinterpret_cast<const uint2*>(emb + (size_t)t * d + c);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    v = make_float4(a.x, a.y, b.x, b.y);
+  }
+  *reinterpret_cast<float4*>(h + (size_t)r * d + c) = v;
+  const float4 gg = *reinterpret_cast<const float4*>(g + c);
+  __nv_bfloat162 x01 = __floats2bfloat162_rn(v.x * gg.x, v.y * gg.y);
+  __nv_bfloat162 x23 = __floats2bfloat162_rn(v.z * gg.z, v.w * gg.w);
+  uint2 xp;
+  xp.x = *reinterpret_cast<unsigned*>(&x01);
+  xp.y = *reinterpret_cast<unsigned*>(&x23);
+  *reinterpret_cast<uint2*>(xo + (size_t)r * d + c) = xp;
+  const float q = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+  if ((threadIdx.x & 31) == 0) ss[(size_t)(c >> 7) * rows + r] = q;
+}
+
+// o = bf16(s), element-wise.
+__global__ void to_bf16_kernel(const float* __restrict__ s, bf16* __restrict__ o, size_t n) {
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) o[i] = __float2bfloat16_rn(s[i]);
+}
+
 // ---------------------------------------------------------------------------
 // RMSNorm, one warp per row: y = x / sqrt(mean(x^2) + eps) * g.
 template <typename T_>

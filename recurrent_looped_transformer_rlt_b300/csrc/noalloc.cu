@@ -34,7 +34,7 @@ using namespace ::rlt;
 }  // namespace rlt_noalloc
 
 using namespace ::rlt;
-using rlt_noalloc::rlt::kXChunkBytes;
+using rlt_noalloc::rlt::kXMaxSplits;
 using rlt_noalloc::rlt::launch_xattn;
 using rlt_noalloc::rlt::set_ctx_kernel;
 using rlt_noalloc::rlt::XattnArgs;
@@ -84,12 +84,9 @@ int rlt_cross_attention_noalloc(const float* q, const void* mem_k, const void* m
   if (dtype != RLT_F32 && dtype != RLT_BF16) return RLT_EINVAL;
   if (head_dim < 8 || head_dim % 8 != 0 || 128 % head_dim != 0) return RLT_EUNSUPPORTED;
   if (!aligned16(q) || !aligned16(mem_k) || !aligned16(mem_v) || !aligned16(out)) return RLT_EINVAL;
-  const int es = (dtype == RLT_BF16) ? 2 : 4;
-  const size_t chunk = (size_t)kXChunkBytes / ((size_t)head_dim * es);
-  const size_t n_chunks = ((size_t)T_mem + chunk - 1) / chunk;
   const size_t pairs = (size_t)B * n_heads;
   const size_t cnt_bytes = (sizeof(int) * pairs + 255) / 256 * 256;
-  const size_t part_bytes = sizeof(float) * pairs * n_chunks * (head_dim + 2);
+  const size_t part_bytes = sizeof(float) * pairs * kXMaxSplits * (head_dim + 2);
   if (cnt_bytes + part_bytes > kNoAllocScratchBytes - kCtxBytes) return RLT_EUNSUPPORTED;  // beyond the built-in scratch
   void* base = nullptr;
   int n_sm = 0;
@@ -112,7 +109,6 @@ int rlt_cross_attention_noalloc(const float* q, const void* mem_k, const void* m
   xa.H = n_heads;
   xa.T_mem = T_mem;
   xa.t_cap = T_mem;
-  xa.max_chunks = (int)n_chunks;
   xa.scale = 1.0f / sqrtf((float)head_dim);
   xa.ctx = ctx;
   xa.status = status;

@@ -69,11 +69,10 @@ namespace {
 struct WsLayout {
   size_t status, ctx, emit, rope;  // header
   // decoder
-  size_t d_h, d_x, d_m, d_c, d_o, d_part, d_cnt;
+  size_t d_h, d_x, d_m, d_c, d_o, d_part, d_cnt, d_ss, d_s16;
   // encoder
-  size_t e_h, e_a, e_m, e_c, e_q, e_k, e_v, e_o;
+  size_t e_h, e_a, e_m, e_c, e_q, e_k, e_v, e_o, e_ss;
   size_t total;
-  int n_chunks;
 };
 
 // the status word: the part of the workspace that must start at zero
@@ -97,15 +96,16 @@ WsLayout layout(const rlt_model* m, int B, int T) {
   L.rope = take(sizeof(float2) * (size_t)T * (hd / 2));
   const size_t common_end = off;
   // decoder region
-  L.n_chunks = (int)cdiv(std::max((size_t)T, (size_t)c.window), (size_t)kXChunkBytes / (hd * es));
   size_t cmax = std::max(std::max(3 * d, 2 * f), std::max(V, 2 * d));
   L.d_h = take(4 * (size_t)B * d);
   L.d_x = take(es * (size_t)B * std::max(2 * d, f));
   L.d_m = take(es * (size_t)B * f);
   L.d_c = take(4 * (size_t)B * cmax);
   L.d_o = take(es * (size_t)B * d);
-  L.d_part = take(4 * (size_t)B * H * L.n_chunks * (hd + 2));
+  L.d_part = take(4 * (size_t)B * H * kXMaxSplits * (hd + 2));
   L.d_cnt = take(sizeof(int) * (size_t)B * H);
+  L.d_ss = take(4 * (size_t)B * ((d + 127) / 128));
+  L.d_s16 = take(es * (size_t)B * d);
   const size_t dec_end = off;
   // encoder region overlaps the decoder region (one call at a time per workspace)
   off = common_end;
@@ -118,6 +118,7 @@ WsLayout layout(const rlt_model* m, int B, int T) {
   L.e_k = take(es * R * d);
   L.e_v = take(es * R * d);
   L.e_o = take(es * R * d);
+  L.e_ss = take(4 * R * ((d + 127) / 128));
   const size_t enc_end = off;
   L.total = std::max(dec_end, enc_end);
   return L;
@@ -178,6 +179,21 @@ int tmap_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, u
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? RLT_OK : RLT_ECUDA;
 }
+// 3-D map of a bf16 tensor [rows][T][cols] (rows of T positions), box = 64
+// columns x 1 position x box_rows rows: one position of every row.
+int tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t T, uint64_t cols, uint32_t box_rows) {
+  auto fn = tmap_encoder();
+  if (!fn) return RLT_ECUDA;
+  if (((uintptr_t)base & 15u) || (cols * 2) % 16) return RLT_EINVAL;
+  cuuint64_t dims[3] = {cols, T, rows};
+  cuuint64_t strides[2] = {cols * 2, T * cols * 2};
+  cuuint32_t box[3] = {(cuuint32_t)tc::BK, 1, box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RLT_OK : RLT_ECUDA;
+}
 
 // Launch context of the tensor-core GEMMs.
 struct TcScratch {
@@ -185,9 +201,22 @@ struct TcScratch {
   int* status;
 };
 
+// The A operand of a projection: A [M][lda] for k < split (all of K when
+// A2 == nullptr), A2 [M][lda2] for k >= split (column 0 = k split); with T3 > 0
+// the first part is a [M][T3][lda] tensor read at the step's position ctx->pos.
+struct AArg {
+  const bf16* A;
+  int lda;
+  const bf16* A2 = nullptr;
+  int lda2 = 0;
+  int split = 0;
+  int T3 = 0;
+  const StepCtx* ctx = nullptr;
+};
+
 template <int BN, int STAGES, bool GLU, class Epi>
-int gemm_tc_launch(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* B, const bf16* B3, int ldb,
-                   int N, Epi epi, const TcScratch& sc) {
+int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, const bf16* B3, int ldb, int N,
+                   Epi epi, const TcScratch& sc, tc::RowScale rsc) {
   using C = tc::Cfg<BN, STAGES>;
   static bool attr = false;
   if (!attr) {
@@ -205,11 +234,19 @@ int gemm_tc_launch(cudaStream_t st, const bf16* A, int lda, int M, int K, const 
   if (tiles < sc.n_sm) splits = std::min(std::min(kb, 8), std::max(1, sc.n_sm / tiles));
   const int kbps = (kb + splits - 1) / splits;
   splits = (kb + kbps - 1) / kbps;
-  CUtensorMap ta, tb, tb3;
+  if (a.A2 && (a.split % tc::BK)) return RLT_EINVAL;
+  CUtensorMap ta, ta2, tb, tb3;
   int rc;
-  if ((rc = tmap_bf16(&ta, A, M, K, lda, tc::BM))) return rc;
+  const int k1 = a.A2 ? a.split : K;
+  if (a.T3 > 0) {
+    if ((rc = tmap_bf16_3d(&ta, a.A, M, a.T3, a.lda, tc::BM))) return rc;
+  } else if ((rc = tmap_bf16(&ta, a.A, M, k1, a.lda, tc::BM))) {
+    return rc;
+  }
+  if ((rc = tmap_bf16(&ta2, a.A2 ? a.A2 : a.A, M, a.A2 ? K - a.split : k1, a.A2 ? a.lda2 : a.lda, tc::BM))) return rc;
   if ((rc = tmap_bf16(&tb, B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
   if ((rc = tmap_bf16(&tb3, GLU ? B3 : B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
+  tc::AOperand ao{a.A2 ? a.split / tc::BK : kb, a.T3 > 0 ? 1 : 0, a.ctx};
   tc::SplitK sk{splits, kbps};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_m, splits);
@@ -223,8 +260,8 @@ int gemm_tc_launch(cudaStream_t st, const bf16* A, int lda, int M, int K, const 
   at[0].val.clusterDim.z = splits;
   cfg.attrs = at;
   cfg.numAttrs = splits > 1 ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi>, ta, tb, tb3, M, N, K, sk, epi, sc.status) !=
-      cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi>, ta, ta2, tb, tb3, M, N, K, ao, rsc, sk, epi,
+                         sc.status) != cudaSuccess)
     return RLT_ECUDA;
   g_launches++;
   return launch_ok();
@@ -232,19 +269,30 @@ int gemm_tc_launch(cudaStream_t st, const bf16* A, int lda, int M, int K, const 
 
 // C = A[M,K] B[N,K]^T with the epilogue functor; tiles sized for the shape.
 template <class Epi>
-int gemm_bf16_tc(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* B, int ldb, int N, Epi epi,
-                 const TcScratch& sc) {
+int gemm_bf16_tc(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, int ldb, int N, Epi epi,
+                 const TcScratch& sc, tc::RowScale rsc = tc::RowScale{nullptr, 0, 0.f, 0.f}) {
   if (M <= 0 || N <= 0) return RLT_OK;
-  if (M <= tc::BM) return gemm_tc_launch<128, 6, false>(st, A, lda, M, K, B, nullptr, ldb, N, epi, sc);
-  return gemm_tc_launch<256, 4, false>(st, A, lda, M, K, B, nullptr, ldb, N, epi, sc);
+  if (M <= tc::BM) return gemm_tc_launch<128, 6, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc, rsc);
+  return gemm_tc_launch<256, 4, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc, rsc);
+}
+template <class Epi>
+int gemm_bf16_tc(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* B, int ldb, int N, Epi epi,
+                 const TcScratch& sc, tc::RowScale rsc = tc::RowScale{nullptr, 0, 0.f, 0.f}) {
+  AArg a;
+  a.A = A;
+  a.lda = lda;
+  return gemm_bf16_tc(st, a, M, K, B, ldb, N, epi, sc, rsc);
 }
 // out[m][j] = silu(A W_1^T)[m][j] * (A W_3^T)[m][j], j < N (= d_ffn).
 template <class Epi>
 int gemm_bf16_tc_glu(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* W1, const bf16* W3, int ldb,
-                     int N, Epi epi, const TcScratch& sc) {
+                     int N, Epi epi, const TcScratch& sc, tc::RowScale rsc = tc::RowScale{nullptr, 0, 0.f, 0.f}) {
   if (M <= 0 || N <= 0) return RLT_OK;
-  if (M <= tc::BM) return gemm_tc_launch<128, 6, true>(st, A, lda, M, K, W1, W3, ldb, N, epi, sc);
-  return gemm_tc_launch<256, 4, true>(st, A, lda, M, K, W1, W3, ldb, N, epi, sc);
+  AArg a;
+  a.A = A;
+  a.lda = lda;
+  if (M <= tc::BM) return gemm_tc_launch<128, 6, true>(st, a, M, K, W1, W3, ldb, N, epi, sc, rsc);
+  return gemm_tc_launch<256, 4, true>(st, a, M, K, W1, W3, ldb, N, epi, sc, rsc);
 }
 
 TcScratch tc_scratch(const rlt_model* m, void* ws, const WsLayout& Lw) {
@@ -315,6 +363,70 @@ int swiglu_proj(cudaStream_t st, const T_* A, int lda, int M, int K, const T_* W
     g_launches++;
     return launch_ok();
   }
+}
+
+// bf16 encoder: projections on the tensor cores with the RMSNorms deferred
+// into them (the residual producers write x = bf16(h * g_next) and row sums of
+// squares; the consumers scale their output rows), RoPE and the head-major
+// q/k/v layout in the QKV epilogue, SwiGLU in the W_1/W_3 epilogue.
+int encode_bf16(const rlt_model* m, const int32_t* tok, int B, int T, bf16* e, bf16* mem, void* ws,
+                cudaStream_t st) {
+  const rlt_config& c = m->cfg;
+  const rlt_weights& w = m->w;
+  const int d = c.d_model, f = c.d_ffn, H = c.n_heads, hd = c.head_dim, L = c.n_layers, G = c.mem_groups;
+  const int R = B * T;
+  WsLayout Lw = layout(m, B, T);
+  int* status = at<int>(ws, Lw.status);
+  float2* tab = at<float2>(ws, Lw.rope);
+  float* h = at<float>(ws, Lw.e_h);
+  bf16* x = at<bf16>(ws, Lw.e_a);
+  bf16* xm = at<bf16>(ws, Lw.e_m);
+  bf16* q = at<bf16>(ws, Lw.e_q);
+  bf16* k = at<bf16>(ws, Lw.e_k);
+  bf16* v = at<bf16>(ws, Lw.e_v);
+  bf16* o = at<bf16>(ws, Lw.e_o);
+  float* ss = at<float>(ws, Lw.e_ss);
+  const TcScratch sc = tc_scratch(m, ws, Lw);
+  const tc::RowScale rsc{ss, d / 128, 1.0f / (float)d, c.rms_eps};
+  int rc;
+  rope_table_kernel<<<cdiv((size_t)T * (hd / 2), 256), 256, 0, st>>>(tab, 0, T, hd / 2, (double)c.rope_theta);
+  g_launches++;
+  embed_norm_kernel<<<R, d / 4, 0, st>>>(tok, static_cast<const bf16*>(w.tok_emb), h, x, w.enc_attn_norm, ss, R, d,
+                                         c.vocab, status);
+  g_launches++;
+  if ((rc = launch_ok())) return rc;
+  const float scale = 1.0f / sqrtf((float)hd);
+  const size_t att_smem = sizeof(float) * (32 * hd + 32 * (hd + 1) + 32 * hd);
+  for (int l = 0; l < L; ++l) {
+    const bf16* Wqkv = wl<bf16>(w.W_qkv, l, (size_t)3 * d * d);
+    if ((rc = gemm_bf16_tc(st, x, d, R, d, Wqkv, d, 3 * d, EpiEncQKVRope<bf16>{q, k, v, tab, d, H, hd, T}, sc, rsc)))
+      return rc;
+    enc_attn_simt_kernel<bf16><<<dim3(cdiv(T, 32), H, B), 256, att_smem, st>>>(q, k, v, o, T, H, hd, scale);
+    g_launches++;
+    if ((rc = launch_ok())) return rc;
+    const bf16* WO = wl<bf16>(w.W_O, l, (size_t)d * d);
+    if ((rc = gemm_bf16_tc(st, o, d, R, d, WO, d, d,
+                           EpiResidual{HOut{h, d, x, w.enc_ffn_norm + (size_t)l * d, nullptr, nullptr, ss, R}}, sc)))
+      return rc;
+    const bf16* W1 = wl<bf16>(w.W_1, l, (size_t)f * d);
+    const bf16* W3 = wl<bf16>(w.W_3, l, (size_t)f * d);
+    if ((rc = gemm_bf16_tc_glu(st, x, d, R, d, W1, W3, d, f, EpiStoreT<bf16>{xm, f}, sc, rsc))) return rc;
+    const bf16* W2 = wl<bf16>(w.W_2, l, (size_t)d * f);
+    const float* gn = (l + 1 < L) ? w.enc_attn_norm + (size_t)(l + 1) * d : w.enc_norm;
+    if ((rc = gemm_bf16_tc(st, xm, f, R, f, W2, f, d, EpiResidual{HOut{h, d, x, gn, nullptr, nullptr, ss, R}}, sc)))
+      return rc;
+  }
+  if ((rc = rmsnorm<bf16>(st, h, w.enc_norm, e, R, d, d, c.rms_eps))) return rc;
+  const size_t plane = (size_t)B * H * T * hd;
+  for (int g = 0; g < G; ++g) {
+    const bf16* WK = wl<bf16>(w.W_K, g, (size_t)d * d);
+    const bf16* WV = wl<bf16>(w.W_V, g, (size_t)d * d);
+    if ((rc = gemm_bf16_tc(st, e, d, R, d, WK, d, d, EpiMemScatter<bf16>{mem + (2 * g) * plane, T, H, hd}, sc)))
+      return rc;
+    if ((rc = gemm_bf16_tc(st, e, d, R, d, WV, d, d, EpiMemScatter<bf16>{mem + (2 * g + 1) * plane, T, H, hd}, sc)))
+      return rc;
+  }
+  return RLT_OK;
 }
 
 template <typename T_>
@@ -465,7 +577,6 @@ int enqueue_step(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* 
   xa.H = H;
   xa.T_mem = A.T_mem;
   xa.t_cap = A.T_mem;
-  xa.max_chunks = Lw.n_chunks;
   xa.scale = scale;
   xa.ctx = ctx;
   xa.status = status;
@@ -579,6 +690,179 @@ int enqueue_step(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* 
   return RLT_OK;
 }
 
+// One decoder step of a bf16 model (enqueued during graph capture):
+//   gate GEMM [e_t; s_{t-1}] W_g^T with the merge in its epilogue -> h,
+//   per layer: QKV (RoPE, ring write) -> window attention -> O (+ residual)
+//              -> Qx -> cross-attention -> Ox (+ residual) -> W_1/W_3 (SwiGLU)
+//              -> W_2 (+ residual),
+//   head GEMM -> log-softmax reduction -> advance.
+// Every RMSNorm is deferred into the projection that consumes it (row scale
+// from the producer's sums of squares).  8 L + 4 kernels per step.
+int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, void* ws, const WsLayout& Lw,
+                      cudaStream_t st, int* n_kernels) {
+  const rlt_config& c = m->cfg;
+  const rlt_weights& w = m->w;
+  const int B = sst->batch;
+  const int d = c.d_model, f = c.d_ffn, H = c.n_heads, hd = c.head_dim, L = c.n_layers, Wn = c.window;
+  const int V = c.vocab;
+  StepCtx* ctx = at<StepCtx>(ws, Lw.ctx);
+  int* status = at<int>(ws, Lw.status);
+  const float2* tab = at<float2>(ws, Lw.rope);
+  float* h = at<float>(ws, Lw.d_h);
+  bf16* x = at<bf16>(ws, Lw.d_x);
+  bf16* xm = at<bf16>(ws, Lw.d_m);
+  float* C = at<float>(ws, Lw.d_c);
+  bf16* o = at<bf16>(ws, Lw.d_o);
+  float* ss = at<float>(ws, Lw.d_ss);
+  bf16* s16 = at<bf16>(ws, Lw.d_s16);
+  const TcScratch sc = tc_scratch(m, ws, Lw);
+  const tc::RowScale rsc{ss, d / 128, 1.0f / (float)d, c.rms_eps};
+  const bf16* e = static_cast<const bf16*>(A.e);
+  const bf16* mem = static_cast<const bf16*>(A.mem);
+  int rc, nk = 0;
+  auto post = [&]() {
+    g_launches++;
+    nk++;
+    return launch_ok();
+  };
+  KernelTimer* tm = m->timer;
+  auto mark = [&](int cls) -> int {
+    if (!tm || tm->cls != cls) return RLT_OK;
+    size_t j = tm->nodes.size();
+    if (j >= tm->ph.size()) {
+      cudaEvent_t ev;
+      if (cudaEventCreate(&ev) != cudaSuccess) return RLT_ECUDA;
+      tm->ph.push_back(ev);
+    }
+    if (cudaEventRecordWithFlags(tm->ph[j], st, cudaEventRecordExternal) != cudaSuccess) return RLT_ECUDA;
+    cudaStreamCaptureStatus cst;
+    const cudaGraphNode_t* deps = nullptr;
+    size_t nd = 0;
+    if (cudaStreamGetCaptureInfo(st, &cst, nullptr, nullptr, &deps, nullptr, &nd) != cudaSuccess || nd != 1)
+      return RLT_ECUDA;
+    tm->nodes.push_back(deps[0]);
+    return RLT_OK;
+  };
+  auto gemm_done = [&](int r) -> int {
+    if (r) return r;
+    nk++;
+    return mark(RLT_TIMER_GEMM);
+  };
+  if (tm) tm->nodes.clear();
+  if ((rc = mark(RLT_TIMER_STEP))) return rc;
+  // merge: A = [e_t ; bf16(s_{t-1})], epilogue h = z s + (1 - z) e
+  {
+    AArg a;
+    a.A = e;
+    a.lda = d;
+    a.T3 = A.T_mem;
+    a.ctx = ctx;
+    a.A2 = s16;
+    a.lda2 = d;
+    a.split = d;
+    EpiMerge em{HOut{h, d, x, w.dec_attn_norm, nullptr, nullptr, ss, B}, e, (size_t)A.T_mem * d, sst->s, w.b_g, ctx,
+                c.gate_mode == RLT_GATE_DISCARD_S ? 1 : 0};
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm_done(gemm_bf16_tc(st, a, B, 2 * d, static_cast<const bf16*>(w.W_g), 2 * d, d, em, sc)))) return rc;
+  }
+  const size_t ring_layer = (size_t)B * H * Wn * hd;
+  const size_t plane = (size_t)B * H * A.T_mem * hd;
+  bf16* rk = static_cast<bf16*>(sst->ring_k);
+  bf16* rv = static_cast<bf16*>(sst->ring_v);
+  XattnArgs xa{};
+  xa.part = at<float>(ws, Lw.d_part);
+  xa.cnt = at<int>(ws, Lw.d_cnt);
+  xa.out = o;
+  xa.q = C;
+  xa.B = B;
+  xa.H = H;
+  xa.scale = 1.0f / sqrtf((float)hd);
+  xa.ctx = ctx;
+  xa.status = status;
+  for (int l = 0; l < L; ++l) {
+    const size_t ld = (size_t)l * d;
+    // self-attention over the window
+    const bf16* Wqkv = wl<bf16>(w.W_qkv, l, (size_t)3 * d * d);
+    EpiQKVRope<bf16> eq{C, rk + l * ring_layer, rv + l * ring_layer, tab, ctx, d, H, hd, Wn};
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm_done(gemm_bf16_tc(st, x, d, B, d, Wqkv, d, 3 * d, eq, sc, rsc)))) return rc;
+    if ((rc = mark(RLT_TIMER_SWA))) return rc;
+    {
+      XattnArgs sa = xa;
+      sa.mk = rk + l * ring_layer;
+      sa.mv = rv + l * ring_layer;
+      sa.T_mem = Wn;
+      sa.t_cap = Wn;
+      if (launch_xattn<bf16>(sa, hd, m->n_sm, st) != cudaSuccess) return RLT_ECUDA;
+      if ((rc = post())) return rc;
+    }
+    if ((rc = mark(RLT_TIMER_SWA))) return rc;
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm_done(gemm_bf16_tc(st, o, d, B, d, wl<bf16>(w.W_O, l, (size_t)d * d), d, d,
+                                     EpiResidual{HOut{h, d, x, w.dec_xattn_norm + ld, nullptr, nullptr, ss, B}}, sc))))
+      return rc;
+    // cross-attention to memory positions 0..p
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm_done(gemm_bf16_tc(st, x, d, B, d, wl<bf16>(w.W_Qx, l, (size_t)d * d), d, d, EpiStoreF32{C, d}, sc,
+                                     rsc))))
+      return rc;
+    const int g = (c.mem_groups == 1) ? 0 : l;
+    if ((rc = mark(RLT_TIMER_XATTN))) return rc;
+    {
+      XattnArgs ca = xa;
+      ca.mk = mem + (2 * g) * plane;
+      ca.mv = mem + (2 * g + 1) * plane;
+      ca.T_mem = A.T_mem;
+      ca.t_cap = A.T_mem;
+      if (launch_xattn<bf16>(ca, hd, m->n_sm, st) != cudaSuccess) return RLT_ECUDA;
+      if ((rc = post())) return rc;
+    }
+    if ((rc = mark(RLT_TIMER_XATTN))) return rc;
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm_done(gemm_bf16_tc(st, o, d, B, d, wl<bf16>(w.W_Ox, l, (size_t)d * d), d, d,
+                                     EpiResidual{HOut{h, d, x, w.dec_ffn_norm + ld, nullptr, nullptr, ss, B}}, sc))))
+      return rc;
+    // SwiGLU FFN
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm_done(gemm_bf16_tc_glu(st, x, d, B, d, wl<bf16>(w.W_1, l, (size_t)f * d),
+                                         wl<bf16>(w.W_3, l, (size_t)f * d), d, f, EpiStoreT<bf16>{xm, f}, sc, rsc))))
+      return rc;
+    const bool last = (l + 1 == L);
+    HOut ho{h, d, x, last ? w.head_norm : w.dec_attn_norm + ld + d, last ? sst->s : nullptr, last ? s16 : nullptr, ss,
+            B};
+    if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+    if ((rc = gemm_done(gemm_bf16_tc(st, xm, f, B, f, wl<bf16>(w.W_2, l, (size_t)d * f), f, d, EpiResidual{ho}, sc))))
+      return rc;
+  }
+  // head: logits = W_o (x * r) with x = bf16(s_t * g_o) and r the RMS scale of s_t
+  if ((rc = mark(RLT_TIMER_HEAD))) return rc;
+  if ((rc = mark(RLT_TIMER_GEMM))) return rc;
+  if ((rc = gemm_done(gemm_bf16_tc(st, x, d, B, d, static_cast<const bf16*>(w.W_o), d, V, EpiStoreF32{C, V}, sc, rsc))))
+    return rc;
+  HeadArgs ha;
+  ha.logits = C;
+  ha.actions = A.actions;
+  ha.logp = A.logp;
+  ha.logp_full = A.logp_full;
+  ha.argmax = A.argmax;
+  ha.emit_map = at<int>(ws, Lw.emit);
+  ha.logits_out = (A.n_emit > 0) ? A.logits : nullptr;
+  ha.B = B;
+  ha.V = V;
+  ha.n = A.n;
+  ha.top_k = A.top_k;
+  ha.inv_temp = A.inv_temp;
+  ha.status = status;
+  head_reduce_kernel<<<B, 1024, sizeof(float) * V, st>>>(ha, ctx);
+  if ((rc = post())) return rc;
+  if ((rc = mark(RLT_TIMER_HEAD))) return rc;
+  advance_kernel<<<1, 1, 0, st>>>(ctx);
+  if ((rc = post())) return rc;
+  if ((rc = mark(RLT_TIMER_STEP))) return rc;
+  *n_kernels = nk;
+  return RLT_OK;
+}
+
 template <typename T_>
 int decode_impl(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const int32_t* emit_steps, void* ws,
                 cudaStream_t st) {
@@ -599,6 +883,12 @@ int decode_impl(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const i
   g_launches++;
   if ((rc = launch_ok())) return rc;
   RLT_CUDA_TRY(cudaMemsetAsync(at<int>(ws, Lw.d_cnt), 0, sizeof(int) * (size_t)B * c.n_heads, st));
+  if constexpr (std::is_same<T_, bf16>::value) {  // bf16(s_{t-1}) for the first step's gate input
+    const size_t n = (size_t)B * c.d_model;
+    to_bf16_kernel<<<cdiv(n, 256), 256, 0, st>>>(sst->s, at<bf16>(ws, Lw.d_s16), n);
+    g_launches++;
+    if ((rc = launch_ok())) return rc;
+  }
   // capture one step and replay it n times
   cudaStream_t cs = m->cap_stream;
   cudaGraph_t graph = nullptr;
@@ -606,7 +896,10 @@ int decode_impl(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const i
   RLT_CUDA_TRY(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal));
   int nk = 0;
   const uint64_t before = g_launches.load();
-  rc = enqueue_step<T_>(m, sst, A, ws, Lw, cs, &nk);
+  if constexpr (std::is_same<T_, bf16>::value)
+    rc = enqueue_step_bf16(m, sst, A, ws, Lw, cs, &nk);
+  else
+    rc = enqueue_step<T_>(m, sst, A, ws, Lw, cs, &nk);
   cudaError_t ce = cudaStreamEndCapture(cs, &graph);
   g_launches.store(before);  // captured launches are counted when the graph runs
   if (rc) {
@@ -663,6 +956,9 @@ int validate_cfg(const rlt_config* c) {
   if (c->head_dim % 8 != 0 || 128 % c->head_dim != 0) return RLT_EUNSUPPORTED;
   // bf16 rows are moved in 16-byte pieces
   if (c->dtype == RLT_BF16 && (c->d_model % 8 != 0 || c->d_ffn % 8 != 0)) return RLT_EUNSUPPORTED;
+  // bf16 models: the residual stream is produced in 256-column tiles and the
+  // deferred RMSNorm keeps one sum of squares per 128 columns
+  if (c->dtype == RLT_BF16 && c->d_model % 256 != 0) return RLT_EUNSUPPORTED;
   if (c->vocab > 49152) return RLT_EUNSUPPORTED;
   if (c->window > 4096) return RLT_EUNSUPPORTED;
   return RLT_OK;
@@ -829,7 +1125,7 @@ int rlt_encode(const rlt_model* m, const int32_t* tokens, int32_t B, int32_t T, 
   if (ws_bytes < layout(m, B, T).total) return RLT_EWORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (m->cfg.dtype == RLT_BF16)
-    return encode_impl<bf16>(m, tokens, B, T, static_cast<bf16*>(e), static_cast<bf16*>(mem), ws, s);
+    return encode_bf16(m, tokens, B, T, static_cast<bf16*>(e), static_cast<bf16*>(mem), ws, s);
   return encode_impl<float>(m, tokens, B, T, static_cast<float*>(e), static_cast<float*>(mem), ws, s);
 }
 
@@ -888,7 +1184,6 @@ int rlt_cross_attention(const rlt_model* m, const float* q, const void* mem_k, c
   xa.H = H;
   xa.T_mem = T_mem;
   xa.t_cap = T_mem;
-  xa.max_chunks = Lw.n_chunks;
   xa.scale = 1.0f / sqrtf((float)hd);
   xa.ctx = ctx;
   xa.status = at<int>(ws, Lw.status);

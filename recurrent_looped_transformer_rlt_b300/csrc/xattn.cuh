@@ -7,22 +7,26 @@
 // entries, so attending to that slot range is attending to the window.
 // Pages: "Understanding and Applying the Recurrent Looped Transformer
 // Architecture", "Three forms of context" (cross-attention reads encoder
-// memory only through the current position); "Princeton Researcher Proposes
-// Recurrent Looped Transformer ...", architecture paragraph.
+// memory only through the current position; the window includes the current
+// token); "Princeton Researcher Proposes Recurrent Looped Transformer ...",
+// architecture paragraph.
 //
-// Design (HBM streaming, ~1 flop per byte, no tensor-core shape):
-//  - work item = (pair = b*H + h, chunk of CH positions); CH*hd*es = 16 KB, so
-//    one chunk of K and one of V are each a single contiguous 16 KB span of
-//    the [B][H][T][hd] memory plane, fetched by one bulk asynchronous copy
-//    (TMA engine) into shared memory;
-//  - persistent CTAs walk the items of the current t round-robin with a
-//    two-stage copy pipeline (the next-but-one item is in flight while the
-//    current one is reduced);
-//  - inside a chunk: scores with hd/8 lanes per key row (16-byte shared loads,
-//    conflict-free), exact chunk max and sum, then P.V with the same layout;
-//  - chunks of a pair are merged by the CTA that finishes the pair's last
-//    chunk (device-scope fence + arrival counter), so no second launch is
-//    needed; a pair with a single chunk is written out directly.
+// Design (HBM streaming, ~1 flop per byte: no tensor-core shape):
+//  - the keys of one (b, h) pair are contiguous in the [B][H][T][hd] plane; a
+//    chunk is CH consecutive positions = 4 KB of K and 4 KB of V, each fetched
+//    by one bulk asynchronous copy (TMA engine) into shared memory;
+//  - work is split per warp, not per block: a task is (pair, split) = a run of
+//    chunks of one pair; every warp owns a two-stage ring of chunk buffers and
+//    their mbarriers, walks its tasks chunk by chunk with the next chunk always
+//    in flight (across task boundaries too), and keeps an online softmax
+//    (running max, sum, output) in registers: no block-wide barrier;
+//  - within a chunk hd*es/16 lanes share a key row (16-byte shared loads), so a
+//    chunk is 8 passes of the warp over its rows;
+//  - the number of splits per pair is picked on the device from t (a cost
+//    model of task rounds over all warps of the grid plus a per-task cost);
+//    the splits of a pair are merged by the warp that arrives last on the
+//    pair's counter (acquire-release atomic), and a pair with a single split
+//    is written out directly.
 #pragma once
 
 #include "common.cuh"
@@ -30,34 +34,33 @@
 
 namespace rlt {
 
-constexpr int kXThreads = 128;
-constexpr int kXChunkBytes = 16384;  // bytes of K (and of V) per chunk
-constexpr int kXStages = 2;
+constexpr int kXWarps = 4;           // warps per CTA (each independent)
+constexpr int kXThreads = 32 * kXWarps;
+constexpr int kXChunkBytes = 4096;   // bytes of K (and of V) per chunk
+constexpr int kXMaxSplits = 32;      // splits per pair at most (partials buffer)
 
 template <typename T_, int HD>
 struct XShape {
   static constexpr int ES = (int)sizeof(T_);
   static constexpr int EPL = 16 / ES;           // elements per lane (one 16-byte load)
   static constexpr int LPR = HD / EPL;          // lanes per key row
-  static constexpr int RPW = 32 / LPR;          // rows per warp and pass
-  static constexpr int NW = kXThreads / 32;
-  static constexpr int RPB = RPW * NW;          // rows per block and pass
+  static constexpr int RPW = 32 / LPR;          // rows per warp pass
   static constexpr int CH = kXChunkBytes / (HD * ES);  // positions per chunk
+  static constexpr int PASSES = CH / RPW;       // = 8
   static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "unsupported head_dim");
-  static_assert(CH % RPB == 0, "chunk must be a whole number of passes");
-  static constexpr size_t smem_bytes() {
-    return (size_t)2 * kXStages * kXChunkBytes + sizeof(float) * (CH + NW * HD) + sizeof(uint64_t) * 2 * kXStages;
-  }
+  static_assert(CH % RPW == 0, "chunk must be a whole number of passes");
+  // per warp: 2 stages x (K, V) chunk buffers, then 4 mbarriers per warp
+  static constexpr size_t smem_bytes() { return (size_t)kXWarps * 4 * kXChunkBytes + 32 * kXWarps; }
 };
 
 struct XattnArgs {
-  const float* q;     // [B][d]  projected query (fp32, no RoPE)
-  const void* mk;     // [B][H][T_mem][hd]  memory keys of one group
-  const void* mv;     // [B][H][T_mem][hd]  memory values
-  float* part;        // [B*H][max_chunks][hd + 2]  (max, sum, unnormalised o)
+  const float* q;     // [B][d]  query (fp32; RoPE already applied for the window)
+  const void* mk;     // [B][H][T_mem][hd]  keys (memory plane of one group, or a layer's ring)
+  const void* mv;     // [B][H][T_mem][hd]  values
+  float* part;        // [B*H][kXMaxSplits][hd + 2]  (max, sum, unnormalised o)
   int* cnt;           // [B*H] arrival counters, zero between launches
   void* out;          // [B][d]  storage dtype
-  int B, H, T_mem, max_chunks;
+  int B, H, T_mem;
   int t_cap;          // attend to positions 0 .. min(t_cap, ctx->pos + 1) - 1
   float scale;
   const StepCtx* ctx;
@@ -86,74 +89,125 @@ __device__ __forceinline__ void load_seg<float, 4>(const float* p, float (&v)[4]
   v[3] = f.w;
 }
 
+// Splits per pair: the S in [1, min(nch, kXMaxSplits)] (every split
+// non-empty) with the least estimated time, in chunk-times: rounds of tasks
+// over the warps of the grid times (chunks per task + the per-task cost of
+// emitting a partial and merging), ties to the smaller S.
+constexpr int kXTaskCost = 3;
+__device__ __forceinline__ int xattn_splits(int pairs, int nch, int warps) {
+  int best = 1;
+  long long best_cost = (((long long)pairs + warps - 1) / warps) * (nch + 1);
+  const int smax = min(nch, kXMaxSplits);
+  for (int s = 2; s <= smax; ++s) {
+    const int cps = (nch + s - 1) / s;
+    if ((nch + cps - 1) / cps != s) continue;
+    const long long rounds = ((long long)pairs * s + warps - 1) / warps;
+    const long long cost = rounds * (cps + kXTaskCost);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+// Arrival on a counter with release (this warp's partial) and acquire (the
+// other warps' partials) semantics at device scope; returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 template <typename T_, int HD>
 __global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
   using S = XShape<T_, HD>;
-  constexpr int CH = S::CH, EPL = S::EPL, LPR = S::LPR, RPW = S::RPW, RPB = S::RPB, NW = S::NW;
+  constexpr int CH = S::CH, EPL = S::EPL, LPR = S::LPR, RPW = S::RPW, PASSES = S::PASSES;
+  constexpr int CHE = CH * HD;  // elements per chunk buffer
   extern __shared__ __align__(128) unsigned char xsm[];
-  T_* sK = reinterpret_cast<T_*>(xsm);
-  T_* sV = reinterpret_cast<T_*>(xsm + kXStages * kXChunkBytes);
-  float* sp = reinterpret_cast<float*>(xsm + 2 * kXStages * kXChunkBytes);  // [CH]
-  float* red = sp + CH;                                                       // [NW][HD]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + NW * HD);                 // K stages, then V stages
-  __shared__ float s_max[NW], s_sum[NW];
-  __shared__ int s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T_* sbuf = reinterpret_cast<T_*>(xsm + (size_t)warp * 4 * kXChunkBytes);  // [stage][K|V][CHE]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(xsm + (size_t)kXWarps * 4 * kXChunkBytes) + warp * 4;  // K0 K1 V0 V1
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sub = lane % LPR, rg = lane / LPR;
   const int t = min(a.t_cap, a.ctx->pos + 1);
   const int nch = (t + CH - 1) / CH;
-  const int n_items = a.B * a.H * nch;
+  const int pairs = a.B * a.H;
+  const int warps = gridDim.x * kXWarps;
+  const int gw = blockIdx.x * kXWarps + warp;
+  const int ns = xattn_splits(pairs, nch, warps);
+  const int cps = (nch + ns - 1) / ns;  // chunks per split (the last split may have fewer)
+  const int tasks = pairs * ns;
+  const int my_tasks = (gw < tasks) ? (tasks - gw + warps - 1) / warps : 0;
   const int d = a.H * HD;
   const T_* mk = static_cast<const T_*>(a.mk);
   const T_* mv = static_cast<const T_*>(a.mv);
   T_* out = static_cast<T_*>(a.out);
 
-  if (tid == 0) {
-    for (int i = 0; i < 2 * kXStages; ++i) mbar_init(&bar[i], 1);
+  if (lane == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
   }
   __syncwarp();
-  __syncthreads();
 
-  auto issue = [&](int item, int stage) {  // one thread
-    const int pair = item / nch, c = item - pair * nch;
-    const int j0 = c * CH, nj = min(CH, t - j0);
-    const unsigned bytes = (unsigned)(nj * HD * S::ES);
-    const size_t off = ((size_t)pair * a.T_mem + j0) * HD;
-    mbar_arrive_expect_tx(&bar[stage], bytes);
-    bulk_g2s(sK + stage * (CH * HD), mk + off, bytes, &bar[stage]);
-    mbar_arrive_expect_tx(&bar[kXStages + stage], bytes);
-    bulk_g2s(sV + stage * (CH * HD), mv + off, bytes, &bar[kXStages + stage]);
+  // chunk iterator over this warp's work: k-th task (gw + k*warps), chunk c
+  auto n_chunks_of = [&](int task) {
+    const int sp = task % ns;
+    return min(cps, nch - sp * cps);
   };
-
-  int item = blockIdx.x;
-  if (tid == 0) {
-    if (item < n_items) issue(item, 0);
-    if (item + (int)gridDim.x < n_items) issue(item + gridDim.x, 1);
+  int ik = 0, ic = 0;  // next chunk to issue
+  auto issue_next = [&](int stage) {  // lane 0; returns nothing, advances (ik, ic)
+    if (ik >= my_tasks) return;
+    const int task = gw + ik * warps;
+    const int pair = task / ns, sp = task - pair * ns;
+    const int c0 = (sp * cps + ic) * CH;
+    const int nj = min(CH, t - c0);
+    const unsigned bytes = (unsigned)(nj * HD * S::ES);
+    const size_t off = ((size_t)pair * a.T_mem + c0) * HD;
+    mbar_arrive_expect_tx(&bar[stage], bytes);
+    bulk_g2s(sbuf + (stage * 2) * CHE, mk + off, bytes, &bar[stage]);
+    mbar_arrive_expect_tx(&bar[2 + stage], bytes);
+    bulk_g2s(sbuf + (stage * 2 + 1) * CHE, mv + off, bytes, &bar[2 + stage]);
+    if (++ic >= n_chunks_of(task)) {
+      ++ik;
+      ic = 0;
+    }
+  };
+  if (lane == 0) {
+    issue_next(0);
+    issue_next(1);
   }
-  __syncwarp();  // warps reach every block-wide barrier converged
+  __syncwarp();
+
   unsigned phase = 0;  // bit s: parity of the next completion of stage s
-  for (int it = 0; item < n_items; item += gridDim.x, ++it) {
-    const int s = it & 1;
-    const unsigned par = (phase >> s) & 1u;
-    const int pair = item / nch, c = item - pair * nch;
+  int used = 0;        // chunks consumed (stage = used & 1)
+  float acc[EPL], qr[EPL];
+  for (int k = 0; k < my_tasks; ++k) {
+    const int task = gw + k * warps;
+    const int pair = task / ns, sp = task - pair * ns;
     const int b = pair / a.H, h = pair - b * a.H;
-    const int j0 = c * CH, nj = min(CH, t - j0);
-    float qr[EPL];
+    const int nct = n_chunks_of(task);
     {
       const float* qp = a.q + (size_t)b * d + h * HD + sub * EPL;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) qr[e] = qp[e];
+      for (int e = 0; e < EPL; ++e) qr[e] = qp[e] * a.scale;
     }
-    // ---- scores over the chunk's keys
-    bool ok = mbar_wait(&bar[s], par, kWaitBudget);
-    if (__syncthreads_or(!ok)) goto fail;
-    {
-      const T_* Ks = sK + s * (CH * HD);
-      float lmax = -INFINITY;
-      for (int r0 = warp * RPW; r0 < nj; r0 += RPB) {  // warp-uniform bound
-        const int r = r0 + rg;
+    float m = -INFINITY, l = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    for (int c = 0; c < nct; ++c, ++used) {
+      const int c0 = (sp * cps + c) * CH;
+      const int nj = min(CH, t - c0);
+      const int st = used & 1;
+      const unsigned par = (phase >> st) & 1u;
+      if (!mbar_wait(&bar[st], par, kWaitBudget)) goto fail;
+      // ---- scores: pass p covers rows p*RPW + rg
+      float sc[PASSES];
+      const T_* Ks = sbuf + (st * 2) * CHE;
+      float cmax = -INFINITY;
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        const int r = p * RPW + rg;
         float dot = 0.f;
         if (r < nj) {
           float kv[EPL];
@@ -163,115 +217,102 @@ __global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
         }
 #pragma unroll
         for (int o = LPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (r < nj) {
-          dot *= a.scale;
-          if (sub == 0) sp[r] = dot;
-          lmax = fmaxf(lmax, dot);
-        }
+        sc[p] = (r < nj) ? dot : -INFINITY;
+        cmax = fmaxf(cmax, sc[p]);
       }
-      lmax = warp_max(lmax);
-      if (lane == 0) s_max[warp] = lmax;
-    }
-    __syncthreads();
-    {
-      float m = s_max[0];
 #pragma unroll
-      for (int w = 1; w < NW; ++w) m = fmaxf(m, s_max[w]);
-      float lsum = 0.f;
-      for (int j = tid; j < nj; j += kXThreads) {
-        const float p = expf(sp[j] - m);
-        sp[j] = p;
-        lsum += p;
+      for (int o = LPR; o < 32; o <<= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+      const float mn = fmaxf(m, cmax);
+      const float corr = expf(m - mn);  // 0 on the first chunk (m = -inf)
+      m = mn;
+      float ls = 0.f;
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        sc[p] = expf(sc[p] - mn);  // rows past nj: exp(-inf) = 0
+        ls += sc[p];
       }
-      lsum = warp_sum(lsum);
-      if (lane == 0) s_sum[warp] = lsum;
-      ok = mbar_wait(&bar[kXStages + s], par, kWaitBudget);
-      if (__syncthreads_or(!ok)) goto fail;
-      float l = s_sum[0];
+      l = l * corr + ls;  // this lane's row group's share
 #pragma unroll
-      for (int w = 1; w < NW; ++w) l += s_sum[w];
-      // ---- P . V
-      const T_* Vs = sV + s * (CH * HD);
-      float acc[EPL];
+      for (int e = 0; e < EPL; ++e) acc[e] *= corr;
+      if (!mbar_wait(&bar[2 + st], par, kWaitBudget)) goto fail;
+      const T_* Vs = sbuf + (st * 2 + 1) * CHE;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-      for (int r0 = warp * RPW; r0 < nj; r0 += RPB) {
-        const int r = r0 + rg;
+      for (int p = 0; p < PASSES; ++p) {
+        const int r = p * RPW + rg;
         if (r < nj) {
-          const float p = sp[r];
           float vv[EPL];
           load_seg<T_, EPL>(Vs + r * HD + sub * EPL, vv);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(p, vv[e], acc[e]);
+          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(sc[p], vv[e], acc[e]);
         }
       }
-#pragma unroll
-      for (int o = LPR; o < 32; o <<= 1)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
-      if (rg == 0)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) red[warp * HD + sub * EPL + e] = acc[e];
-      __syncthreads();  // stage s fully consumed, red complete
-      if (tid == 0 && item + 2 * (int)gridDim.x < n_items) issue(item + 2 * gridDim.x, s);
+      __syncwarp();  // every lane is done with stage st
+      phase ^= (1u << st);
+      if (lane == 0) issue_next(st);
       __syncwarp();
-      phase ^= (1u << s);
-      if (nch == 1) {
-        for (int i = tid; i < HD; i += kXThreads) {
-          float o = 0.f;
+    }
+    // ---- end of the task: sum over the row groups and emit
+    float lt = l;
 #pragma unroll
-          for (int w = 0; w < NW; ++w) o += red[w * HD + i];
-          out[(size_t)b * d + h * HD + i] = from_f32<T_>(o / l);
-        }
-        continue;
-      }
-      float* pr = a.part + ((size_t)pair * a.max_chunks + c) * (HD + 2);
-      for (int i = tid; i < HD; i += kXThreads) {
-        float o = 0.f;
+    for (int o = LPR; o < 32; o <<= 1) {
+      lt += __shfl_xor_sync(0xffffffffu, lt, o);
 #pragma unroll
-        for (int w = 0; w < NW; ++w) o += red[w * HD + i];
-        pr[2 + i] = o;
+      for (int e = 0; e < EPL; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+    }
+    if (ns == 1) {
+      if (rg == 0) {
+        const float inv = 1.f / lt;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) out[(size_t)b * d + h * HD + sub * EPL + e] = from_f32<T_>(acc[e] * inv);
       }
-      if (tid == 0) {
+      continue;
+    }
+    {
+      float* pr = a.part + ((size_t)pair * kXMaxSplits + sp) * (HD + 2);
+      if (rg == 0) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) pr[2 + sub * EPL + e] = acc[e];
+      }
+      if (lane == 0) {
         pr[0] = m;
-        pr[1] = l;
+        pr[1] = lt;
       }
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) s_last = (atomicAdd(&a.cnt[pair], 1) == nch - 1);
-      __syncwarp();
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        const float* pp = a.part + (size_t)pair * a.max_chunks * (HD + 2);
+      __syncwarp();  // the warp's partial writes are ordered before lane 0's release
+      int last = 0;
+      if (lane == 0) last = (atom_add_acq_rel(&a.cnt[pair], 1) == ns - 1);
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        const float* pp = a.part + (size_t)pair * kXMaxSplits * (HD + 2);
         float M = -INFINITY;
-        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(pp + (size_t)cc * (HD + 2)));
+        for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(pp + (size_t)s2 * (HD + 2)));
         float L = 0.f;
-        for (int cc = 0; cc < nch; ++cc)
-          L += __ldcg(pp + (size_t)cc * (HD + 2) + 1) * expf(__ldcg(pp + (size_t)cc * (HD + 2)) - M);
-        for (int i = tid; i < HD; i += kXThreads) {
+        for (int s2 = 0; s2 < ns; ++s2)
+          L += __ldcg(pp + (size_t)s2 * (HD + 2) + 1) * expf(__ldcg(pp + (size_t)s2 * (HD + 2)) - M);
+        const float inv = 1.f / L;
+        for (int i = lane; i < HD; i += 32) {
           float o = 0.f;
-          for (int cc = 0; cc < nch; ++cc)
-            o += __ldcg(pp + (size_t)cc * (HD + 2) + 2 + i) * expf(__ldcg(pp + (size_t)cc * (HD + 2)) - M);
-          out[(size_t)b * d + h * HD + i] = from_f32<T_>(o / L);
+          for (int s2 = 0; s2 < ns; ++s2)
+            o += __ldcg(pp + (size_t)s2 * (HD + 2) + 2 + i) * expf(__ldcg(pp + (size_t)s2 * (HD + 2)) - M);
+          out[(size_t)b * d + h * HD + i] = from_f32<T_>(o * inv);
         }
-        if (tid == 0) a.cnt[pair] = 0;  // ready for the next launch
+        __syncwarp();
+        if (lane == 0) a.cnt[pair] = 0;  // ready for the next launch
       }
     }
   }
   return;
 fail:
-  // a copy never completed: record it, give in-flight copies a bounded time
-  // to land (they write this CTA's shared memory), then leave
-  if (tid == 0) {
+  // a copy never completed: record it, give this warp's copies in flight a
+  // bounded time to land (they write its shared memory), then leave
+  if (lane == 0) {
     set_error(a.status, kErrTimeout);
-    for (int s2 = 0; s2 < kXStages; ++s2) {
+    for (int s2 = 0; s2 < 2; ++s2) {
       const unsigned p2 = (phase >> s2) & 1u;
       mbar_wait(&bar[s2], p2, kWaitBudget);
-      mbar_wait(&bar[kXStages + s2], p2, kWaitBudget);
+      mbar_wait(&bar[2 + s2], p2, kWaitBudget);
     }
   }
-  __syncthreads();
+  __syncwarp();
 }
 
 // Host-side launch: grid = resident CTAs on every SM (persistent).
@@ -291,11 +332,6 @@ inline cudaError_t launch_xattn_hd(const XattnArgs& a, int n_sm, cudaStream_t st
   }
   dec_xattn_kernel<T_, HD><<<n_sm * occ, kXThreads, S::smem_bytes(), st>>>(a);
   return cudaGetLastError();
-}
-
-template <typename T_>
-inline int xattn_chunk(int hd) {
-  return kXChunkBytes / (hd * (int)sizeof(T_));
 }
 
 template <typename T_>

@@ -29,6 +29,8 @@ def _model():
     (1000, 512, 100, False),
     (1024, 128, 512, True),
     (5, 64, 32000, False),     # head-like: many column tiles
+    (64, 128, 101, False),     # output rows not 16-byte aligned (scalar epilogue)
+    (200, 192, 37, False),
 ])
 def test_linear_matches_cpu_matmul(M, K, N, glu):
     import torch

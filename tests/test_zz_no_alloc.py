@@ -49,7 +49,7 @@ def test_cross_attention_noalloc_matches_workspace_entry_point(name, B, T_mem, c
 def test_cross_attention_noalloc_rejects_sizes_beyond_its_scratch():
     import torch
     import recurrent_looped_transformer_rlt_b300 as rlt
-    B, H, hd, T_mem = 64, 16, 128, 8192     # 64*16*64*130*4 bytes > 16 MiB
+    B, H, hd, T_mem = 64, 16, 128, 8192     # 64*16 pairs x 32 partials x 130 floats > 16 MiB
     q = torch.zeros(B, H * hd, device="cuda")
     km = torch.zeros(1, device="cuda", dtype=torch.bfloat16)
     out = torch.zeros(B, H * hd, device="cuda", dtype=torch.bfloat16)
