@@ -184,6 +184,123 @@ __device__ __forceinline__ float4 ld_dsmem_f4(const void* local, uint32_t rank) 
   return v;
 }
 
+// Epilogue on a staged fp32 tile stile[rows][BN + 4] (rows = output rows m0 +
+// r, columns = output columns nb0 + c): rows [r0, r1) go through the functor,
+// 128 threads (et = 0..127), consecutive threads on consecutive columns.
+template <int BN, bool GLU, class Epi>
+__device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1, int m0, int nb0, int N,
+                                              const Epi& epi, int et) {
+  constexpr int LDT = BN + 4;
+  if constexpr (GLU) {
+    constexpr int HB = BN / 2;
+    const int n = (r1 - r0) * HB;
+#pragma unroll 4
+    for (int i = et; i < n; i += 128) {
+      const int r = r0 + i / HB, j = i % HB;
+      if (nb0 + j < N) epi(m0 + r, nb0 + j, silu_f(stile[r * LDT + j]) * stile[r * LDT + j + HB]);
+    }
+  } else if constexpr (IsPairEpi<Epi>::value) {
+    const int half = epi.hd >> 1;
+    constexpr int HB = BN / 2;  // pairs per tile row
+    const int n = (r1 - r0) * HB;
+#pragma unroll 4
+    for (int i = et; i < n; i += 128) {
+      const int r = r0 + i / HB, pi = i % HB;
+      const int hb = pi / half, ii = pi - hb * half;
+      const int c = hb * 2 * half + ii;
+      if (nb0 + c < N) epi.pair(m0 + r, nb0 + c, stile[r * LDT + c], stile[r * LDT + c + half]);
+    }
+  } else if constexpr (IsHOutEpi<Epi>::value) {
+    // the residual stream: N a multiple of BN and rows 16-byte aligned
+    // (checked by the host); a warp covers 128 consecutive columns of one row
+    constexpr int V4 = BN / 4;
+    const int n = (r1 - r0) * V4;
+    const HOut& o = epi.o;
+    for (int i0 = et; i0 < n; i0 += 4 * 128) {
+      typename Epi::Aux aux[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 128;
+        if (i < n) aux[u] = epi.load(m0 + r0 + i / V4, nb0 + (i % V4) * 4);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 128;
+        if (i >= n) continue;  // warp-uniform: n is a multiple of 32
+        const int r = r0 + i / V4, c = (i % V4) * 4;
+        const int m = m0 + r, col = nb0 + c;
+        const float4 hv = epi.combine(aux[u], *reinterpret_cast<const float4*>(stile + r * LDT + c), col);
+        const size_t off = (size_t)m * o.ldh + col;
+        *reinterpret_cast<float4*>(o.h + off) = hv;
+        if (o.s) *reinterpret_cast<float4*>(o.s + off) = hv;
+        const float4 gg = *reinterpret_cast<const float4*>(o.g + col);
+        __nv_bfloat162 x01 = __floats2bfloat162_rn(hv.x * gg.x, hv.y * gg.y);
+        __nv_bfloat162 x23 = __floats2bfloat162_rn(hv.z * gg.z, hv.w * gg.w);
+        uint2 xp;
+        xp.x = *reinterpret_cast<unsigned*>(&x01);
+        xp.y = *reinterpret_cast<unsigned*>(&x23);
+        *reinterpret_cast<uint2*>(o.x + off) = xp;
+        if (o.s16) {
+          __nv_bfloat162 s01 = __floats2bfloat162_rn(hv.x, hv.y);
+          __nv_bfloat162 s23 = __floats2bfloat162_rn(hv.z, hv.w);
+          uint2 sp;
+          sp.x = *reinterpret_cast<unsigned*>(&s01);
+          sp.y = *reinterpret_cast<unsigned*>(&s23);
+          *reinterpret_cast<uint2*>(o.s16 + off) = sp;
+        }
+        const float q2 = warp_sum(hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w);
+        if ((et & 31) == 0) o.ss[(size_t)(col >> 7) * o.M + m] = q2;
+      }
+    }
+  } else if constexpr (IsStore4Epi<Epi>::value || IsAdd4Epi<Epi>::value) {
+    // 16-byte accesses, four per thread in flight (reads of the residual
+    // first, then the stores); full 4-column groups only, the rest below.
+    // An output whose rows are not 16-byte aligned takes the scalar path.
+    constexpr int V4 = BN / 4;
+    const bool vec = (epi.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(epi.C) & 15u) == 0);
+    const int nq = vec ? min(V4, (N - nb0) / 4) : 0;  // whole float4 columns inside N
+    const int n = vec ? (r1 - r0) * V4 : 0;
+    for (int i0 = et; i0 < n; i0 += 4 * 128) {
+      float4 v[4], o[4];
+      float* dst[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 128;
+        const int r = r0 + i / V4, c4 = i % V4;
+        dst[u] = (i < n && c4 < nq) ? epi.C + (size_t)(m0 + r) * epi.ldc + nb0 + c4 * 4 : nullptr;
+        v[u] = dst[u] ? *reinterpret_cast<const float4*>(stile + r * LDT + c4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (IsAdd4Epi<Epi>::value)
+          o[u] = dst[u] ? *reinterpret_cast<const float4*>(dst[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (!dst[u]) continue;
+        if constexpr (IsAdd4Epi<Epi>::value) {
+          v[u].x += o[u].x;
+          v[u].y += o[u].y;
+          v[u].z += o[u].z;
+          v[u].w += o[u].w;
+        }
+        *reinterpret_cast<float4*>(dst[u]) = v[u];
+      }
+    }
+    if (nb0 + 4 * nq < N && nq < V4) {  // ragged last columns of N (all of them without vec)
+      const int c_beg = 4 * nq, w = min(BN, N - nb0) - c_beg;
+      for (int i = et; i < (r1 - r0) * w; i += 128) {
+        const int r = r0 + i / w, c = c_beg + i % w;
+        epi(m0 + r, nb0 + c, stile[r * LDT + c]);
+      }
+    }
+  } else {
+    const int n = (r1 - r0) * BN;
+#pragma unroll 4
+    for (int i = et; i < n; i += 128) {
+      const int r = r0 + i / BN, c = i % BN;
+      if (nb0 + c < N) epi(m0 + r, nb0 + c, stile[r * LDT + c]);
+    }
+  }
+}
+
 // B operand: one weight matrix [N][K], or (glu) the pair W_1, W_3 [N][K]
 // whose tile j holds rows j*BN/2 .. of W_1 in its first half and the same
 // rows of W_3 in its second half, so that the epilogue sees gate and linear
@@ -366,116 +483,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int LDT = BN + 4;
     const float* stile = reinterpret_cast<const float*>(smem);
     epi_bar();
-    if (!s_fail) {
-      if constexpr (GLU) {
-        constexpr int HB = BN / 2;
-        const int n = (r1 - r0) * HB;
-#pragma unroll 4
-        for (int i = et; i < n; i += 128) {
-          const int r = r0 + i / HB, j = i % HB;
-          if (nb0 + j < N) epi(m0 + r, nb0 + j, silu_f(stile[r * LDT + j]) * stile[r * LDT + j + HB]);
-        }
-      } else if constexpr (IsPairEpi<Epi>::value) {
-        const int half = epi.hd >> 1;
-        constexpr int HB = BN / 2;  // pairs per tile row
-        const int n = (r1 - r0) * HB;
-#pragma unroll 4
-        for (int i = et; i < n; i += 128) {
-          const int r = r0 + i / HB, pi = i % HB;
-          const int hb = pi / half, ii = pi - hb * half;
-          const int c = hb * 2 * half + ii;
-          if (nb0 + c < N) epi.pair(m0 + r, nb0 + c, stile[r * LDT + c], stile[r * LDT + c + half]);
-        }
-      } else if constexpr (IsHOutEpi<Epi>::value) {
-        // the residual stream: N a multiple of BN and rows 16-byte aligned
-        // (checked by the host); a warp covers 128 consecutive columns of one row
-        constexpr int V4 = BN / 4;
-        const int n = (r1 - r0) * V4;
-        const HOut& o = epi.o;
-        for (int i0 = et; i0 < n; i0 += 4 * 128) {
-          typename Epi::Aux aux[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * 128;
-            if (i < n) aux[u] = epi.load(m0 + r0 + i / V4, nb0 + (i % V4) * 4);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * 128;
-            if (i >= n) continue;  // warp-uniform: n is a multiple of 32
-            const int r = r0 + i / V4, c = (i % V4) * 4;
-            const int m = m0 + r, col = nb0 + c;
-            const float4 hv = epi.combine(aux[u], *reinterpret_cast<const float4*>(stile + r * LDT + c), col);
-            const size_t off = (size_t)m * o.ldh + col;
-            *reinterpret_cast<float4*>(o.h + off) = hv;
-            if (o.s) *reinterpret_cast<float4*>(o.s + off) = hv;
-            const float4 gg = *reinterpret_cast<const float4*>(o.g + col);
-            __nv_bfloat162 x01 = __floats2bfloat162_rn(hv.x * gg.x, hv.y * gg.y);
-            __nv_bfloat162 x23 = __floats2bfloat162_rn(hv.z * gg.z, hv.w * gg.w);
-            uint2 xp;
-            xp.x = *reinterpret_cast<unsigned*>(&x01);
-            xp.y = *reinterpret_cast<unsigned*>(&x23);
-            *reinterpret_cast<uint2*>(o.x + off) = xp;
-            if (o.s16) {
-              __nv_bfloat162 s01 = __floats2bfloat162_rn(hv.x, hv.y);
-              __nv_bfloat162 s23 = __floats2bfloat162_rn(hv.z, hv.w);
-              uint2 sp;
-              sp.x = *reinterpret_cast<unsigned*>(&s01);
-              sp.y = *reinterpret_cast<unsigned*>(&s23);
-              *reinterpret_cast<uint2*>(o.s16 + off) = sp;
-            }
-            const float q2 = warp_sum(hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w);
-            if ((et & 31) == 0) o.ss[(size_t)(col >> 7) * o.M + m] = q2;
-          }
-        }
-      } else if constexpr (IsStore4Epi<Epi>::value || IsAdd4Epi<Epi>::value) {
-        // 16-byte accesses, four per thread in flight (reads of the residual
-        // first, then the stores); full 4-column groups only, the rest below.
-        // An output whose rows are not 16-byte aligned takes the scalar path.
-        constexpr int V4 = BN / 4;
-        const bool vec = (epi.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(epi.C) & 15u) == 0);
-        const int nq = vec ? min(V4, (N - nb0) / 4) : 0;  // whole float4 columns inside N
-        const int n = vec ? (r1 - r0) * V4 : 0;
-        for (int i0 = et; i0 < n; i0 += 4 * 128) {
-          float4 v[4], o[4];
-          float* dst[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * 128;
-            const int r = r0 + i / V4, c4 = i % V4;
-            dst[u] = (i < n && c4 < nq) ? epi.C + (size_t)(m0 + r) * epi.ldc + nb0 + c4 * 4 : nullptr;
-            v[u] = dst[u] ? *reinterpret_cast<const float4*>(stile + r * LDT + c4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-            if constexpr (IsAdd4Epi<Epi>::value)
-              o[u] = dst[u] ? *reinterpret_cast<const float4*>(dst[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            if (!dst[u]) continue;
-            if constexpr (IsAdd4Epi<Epi>::value) {
-              v[u].x += o[u].x;
-              v[u].y += o[u].y;
-              v[u].z += o[u].z;
-              v[u].w += o[u].w;
-            }
-            *reinterpret_cast<float4*>(dst[u]) = v[u];
-          }
-        }
-        if (nb0 + 4 * nq < N && nq < V4) {  // ragged last columns of N (all of them without vec)
-          const int c_beg = 4 * nq, w = min(BN, N - nb0) - c_beg;
-          for (int i = et; i < (r1 - r0) * w; i += 128) {
-            const int r = r0 + i / w, c = c_beg + i % w;
-            epi(m0 + r, nb0 + c, stile[r * LDT + c]);
-          }
-        }
-      } else {
-        const int n = (r1 - r0) * BN;
-#pragma unroll 4
-        for (int i = et; i < n; i += 128) {
-          const int r = r0 + i / BN, c = i % BN;
-          if (nb0 + c < N) epi(m0 + r, nb0 + c, stile[r * LDT + c]);
-        }
-      }
-    }
+    if (!s_fail) epilogue_tile<BN, GLU>(stile, r0, r1, m0, nb0, N, epi, et);
   }
   if (sk.splits > 1) cluster_sync_all();  // peers are done reading this CTA's tile
   tc_fence_before();

@@ -228,10 +228,19 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   const int nout = GLU ? BN / 2 : BN;
   const int tiles_n = (N + nout - 1) / nout, tiles_m = (M + tc::BM - 1) / tc::BM;
   const int kb = (K + tc::BK - 1) / tc::BK;
-  // split K (a cluster of up to 8 CTAs per tile) until the grid covers the SMs
+  // split K over a cluster of CTAs per tile when there are few tiles.  Sizes
+  // from measurements of the weight-streaming shapes on B300: clusters of 8
+  // fit on 120 of the 148 SMs only (15 at a time), clusters of 2 on all;
+  // about 100 CTAs already saturate HBM with 3-stage rings.
   const int tiles = tiles_n * tiles_m;
   int splits = 1;
-  if (tiles < sc.n_sm) splits = std::min(std::min(kb, 8), std::max(1, sc.n_sm / tiles));
+  if (tiles < 12)
+    splits = 8;
+  else if (tiles < 32)
+    splits = 6;
+  else if (tiles < 128)
+    splits = 2;
+  splits = std::max(1, std::min(splits, kb));
   const int kbps = (kb + splits - 1) / splits;
   splits = (kb + kbps - 1) / kbps;
   if (a.A2 && (a.split % tc::BK)) return RLT_EINVAL;
@@ -272,7 +281,7 @@ template <class Epi>
 int gemm_bf16_tc(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, int ldb, int N, Epi epi,
                  const TcScratch& sc, tc::RowScale rsc = tc::RowScale{nullptr, 0, 0.f, 0.f}) {
   if (M <= 0 || N <= 0) return RLT_OK;
-  if (M <= tc::BM) return gemm_tc_launch<128, 6, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc, rsc);
+  if (M <= tc::BM) return gemm_tc_launch<128, 3, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc, rsc);
   return gemm_tc_launch<256, 4, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc, rsc);
 }
 template <class Epi>
@@ -283,6 +292,17 @@ int gemm_bf16_tc(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf
   a.lda = lda;
   return gemm_bf16_tc(st, a, M, K, B, ldb, N, epi, sc, rsc);
 }
+// Projection of a batch of sequences (decoder step, rlt_linear): 3-stage
+// pipeline for up to 128 rows (two CTAs fit on an SM), 4 stages of 256-wide
+// tiles beyond.
+template <bool GLU, class Epi>
+int proj_bf16(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const bf16* W3, int ldw, int N, Epi epi,
+              const TcScratch& sc, tc::RowScale rsc) {
+  if (M <= 0 || N <= 0) return RLT_OK;
+  if (M <= tc::BM) return gemm_tc_launch<128, 3, GLU>(st, x, M, K, W, W3, ldw, N, epi, sc, rsc);
+  return gemm_tc_launch<256, 4, GLU>(st, x, M, K, W, W3, ldw, N, epi, sc, rsc);
+}
+
 // out[m][j] = silu(A W_1^T)[m][j] * (A W_3^T)[m][j], j < N (= d_ffn).
 template <class Epi>
 int gemm_bf16_tc_glu(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* W1, const bf16* W3, int ldb,
@@ -291,7 +311,7 @@ int gemm_bf16_tc_glu(cudaStream_t st, const bf16* A, int lda, int M, int K, cons
   AArg a;
   a.A = A;
   a.lda = lda;
-  if (M <= tc::BM) return gemm_tc_launch<128, 6, true>(st, a, M, K, W1, W3, ldb, N, epi, sc, rsc);
+  if (M <= tc::BM) return gemm_tc_launch<128, 3, true>(st, a, M, K, W1, W3, ldb, N, epi, sc, rsc);
   return gemm_tc_launch<256, 4, true>(st, a, M, K, W1, W3, ldb, N, epi, sc, rsc);
 }
 
@@ -717,6 +737,13 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
   bf16* s16 = at<bf16>(ws, Lw.d_s16);
   const TcScratch sc = tc_scratch(m, ws, Lw);
   const tc::RowScale rsc{ss, d / 128, 1.0f / (float)d, c.rms_eps};
+  const tc::RowScale none{nullptr, 0, 0.f, 0.f};
+  auto act = [](const bf16* p, int ld) {
+    AArg a;
+    a.A = p;
+    a.lda = ld;
+    return a;
+  };
   const bf16* e = static_cast<const bf16*>(A.e);
   const bf16* mem = static_cast<const bf16*>(A.mem);
   int rc, nk = 0;
@@ -763,7 +790,7 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     EpiMerge em{HOut{h, d, x, w.dec_attn_norm, nullptr, nullptr, ss, B}, e, (size_t)A.T_mem * d, sst->s, w.b_g, ctx,
                 c.gate_mode == RLT_GATE_DISCARD_S ? 1 : 0};
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(gemm_bf16_tc(st, a, B, 2 * d, static_cast<const bf16*>(w.W_g), 2 * d, d, em, sc)))) return rc;
+    if ((rc = gemm_done(proj_bf16<false>(st, a, B, 2 * d, static_cast<const bf16*>(w.W_g), nullptr, 2 * d, d, em, sc, none)))) return rc;
   }
   const size_t ring_layer = (size_t)B * H * Wn * hd;
   const size_t plane = (size_t)B * H * A.T_mem * hd;
@@ -785,7 +812,7 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     const bf16* Wqkv = wl<bf16>(w.W_qkv, l, (size_t)3 * d * d);
     EpiQKVRope<bf16> eq{C, rk + l * ring_layer, rv + l * ring_layer, tab, ctx, d, H, hd, Wn};
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(gemm_bf16_tc(st, x, d, B, d, Wqkv, d, 3 * d, eq, sc, rsc)))) return rc;
+    if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, Wqkv, nullptr, d, 3 * d, eq, sc, rsc)))) return rc;
     if ((rc = mark(RLT_TIMER_SWA))) return rc;
     {
       XattnArgs sa = xa;
@@ -798,13 +825,14 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     }
     if ((rc = mark(RLT_TIMER_SWA))) return rc;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(gemm_bf16_tc(st, o, d, B, d, wl<bf16>(w.W_O, l, (size_t)d * d), d, d,
-                                     EpiResidual{HOut{h, d, x, w.dec_xattn_norm + ld, nullptr, nullptr, ss, B}}, sc))))
+    if ((rc = gemm_done(proj_bf16<false>(st, act(o, d), B, d, wl<bf16>(w.W_O, l, (size_t)d * d), nullptr, d, d,
+                                         EpiResidual{HOut{h, d, x, w.dec_xattn_norm + ld, nullptr, nullptr, ss, B}}, sc,
+                                         none))))
       return rc;
     // cross-attention to memory positions 0..p
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(gemm_bf16_tc(st, x, d, B, d, wl<bf16>(w.W_Qx, l, (size_t)d * d), d, d, EpiStoreF32{C, d}, sc,
-                                     rsc))))
+    if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, wl<bf16>(w.W_Qx, l, (size_t)d * d), nullptr, d, d,
+                                         EpiStoreF32{C, d}, sc, rsc))))
       return rc;
     const int g = (c.mem_groups == 1) ? 0 : l;
     if ((rc = mark(RLT_TIMER_XATTN))) return rc;
@@ -819,25 +847,28 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     }
     if ((rc = mark(RLT_TIMER_XATTN))) return rc;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(gemm_bf16_tc(st, o, d, B, d, wl<bf16>(w.W_Ox, l, (size_t)d * d), d, d,
-                                     EpiResidual{HOut{h, d, x, w.dec_ffn_norm + ld, nullptr, nullptr, ss, B}}, sc))))
+    if ((rc = gemm_done(proj_bf16<false>(st, act(o, d), B, d, wl<bf16>(w.W_Ox, l, (size_t)d * d), nullptr, d, d,
+                                         EpiResidual{HOut{h, d, x, w.dec_ffn_norm + ld, nullptr, nullptr, ss, B}}, sc,
+                                         none))))
       return rc;
     // SwiGLU FFN
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(gemm_bf16_tc_glu(st, x, d, B, d, wl<bf16>(w.W_1, l, (size_t)f * d),
-                                         wl<bf16>(w.W_3, l, (size_t)f * d), d, f, EpiStoreT<bf16>{xm, f}, sc, rsc))))
+    if ((rc = gemm_done(proj_bf16<true>(st, act(x, d), B, d, wl<bf16>(w.W_1, l, (size_t)f * d),
+                                        wl<bf16>(w.W_3, l, (size_t)f * d), d, f, EpiStoreT<bf16>{xm, f}, sc, rsc))))
       return rc;
     const bool last = (l + 1 == L);
     HOut ho{h, d, x, last ? w.head_norm : w.dec_attn_norm + ld + d, last ? sst->s : nullptr, last ? s16 : nullptr, ss,
             B};
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(gemm_bf16_tc(st, xm, f, B, f, wl<bf16>(w.W_2, l, (size_t)d * f), f, d, EpiResidual{ho}, sc))))
+    if ((rc = gemm_done(proj_bf16<false>(st, act(xm, f), B, f, wl<bf16>(w.W_2, l, (size_t)d * f), nullptr, f, d, EpiResidual{ho}, sc,
+                                         none))))
       return rc;
   }
   // head: logits = W_o (x * r) with x = bf16(s_t * g_o) and r the RMS scale of s_t
   if ((rc = mark(RLT_TIMER_HEAD))) return rc;
   if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-  if ((rc = gemm_done(gemm_bf16_tc(st, x, d, B, d, static_cast<const bf16*>(w.W_o), d, V, EpiStoreF32{C, V}, sc, rsc))))
+  if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, static_cast<const bf16*>(w.W_o), nullptr, d, V, EpiStoreF32{C, V}, sc,
+                                         rsc))))
     return rc;
   HeadArgs ha;
   ha.logits = C;
@@ -1205,10 +1236,14 @@ int rlt_linear(const rlt_model* m, const void* A, int32_t lda, int32_t M, int32_
   if (ws_bytes < Lw.total) return RLT_EWORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const TcScratch sc = tc_scratch(m, ws, Lw);
-  const bf16* a = static_cast<const bf16*>(A);
+  AArg a;
+  a.A = static_cast<const bf16*>(A);
+  a.lda = lda;
   const bf16* w = static_cast<const bf16*>(W);
-  if (W3) return gemm_bf16_tc_glu(s, a, lda, M, K, w, static_cast<const bf16*>(W3), ldw, N, EpiStoreF32{C, ldc}, sc);
-  return gemm_bf16_tc(s, a, lda, M, K, w, ldw, N, EpiStoreF32{C, ldc}, sc);
+  const tc::RowScale none{nullptr, 0, 0.f, 0.f};
+  if (W3)
+    return proj_bf16<true>(s, a, M, K, w, static_cast<const bf16*>(W3), ldw, N, EpiStoreF32{C, ldc}, sc, none);
+  return proj_bf16<false>(s, a, M, K, w, nullptr, ldw, N, EpiStoreF32{C, ldc}, sc, none);
 }
 
 int rlt_status(void* ws, rlt_stream_t stream) {
