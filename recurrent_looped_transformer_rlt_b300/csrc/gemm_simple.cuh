@@ -112,15 +112,12 @@ struct EpiEncQKVRope {
 
 // Epilogues that produce the residual stream h (fp32 [M][ldh]) declare kHOut,
 // load(m, n) of what they combine with and combine(aux, acc4, n) -> the new
-// h[m][n..n+3].  The kernel then writes h, x = bf16(h * g) (the A operand of
-// the next projection: gain of the next RMSNorm applied, its row scale
-// deferred to that projection), optional copies s (fp32) and s16 (bf16), and
-// per row and 128-column block the sum of squares ss[n / 128][m].
+// h[m][n..n+3].  The kernel then writes h, optional copies s (fp32) and s16
+// (bf16), and per row and 128-column block the sum of squares ss[n / 128][m]
+// (the next RMSNorm reads these instead of reducing the row again).
 struct HOut {
   float* h;
   int ldh;
-  bf16* x;
-  const float* g;
   float* s;
   bf16* s16;
   float* ss;

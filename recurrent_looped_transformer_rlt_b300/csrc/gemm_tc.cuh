@@ -233,13 +233,6 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
         const size_t off = (size_t)m * o.ldh + col;
         *reinterpret_cast<float4*>(o.h + off) = hv;
         if (o.s) *reinterpret_cast<float4*>(o.s + off) = hv;
-        const float4 gg = *reinterpret_cast<const float4*>(o.g + col);
-        __nv_bfloat162 x01 = __floats2bfloat162_rn(hv.x * gg.x, hv.y * gg.y);
-        __nv_bfloat162 x23 = __floats2bfloat162_rn(hv.z * gg.z, hv.w * gg.w);
-        uint2 xp;
-        xp.x = *reinterpret_cast<unsigned*>(&x01);
-        xp.y = *reinterpret_cast<unsigned*>(&x23);
-        *reinterpret_cast<uint2*>(o.x + off) = xp;
         if (o.s16) {
           __nv_bfloat162 s01 = __floats2bfloat162_rn(hv.x, hv.y);
           __nv_bfloat162 s23 = __floats2bfloat162_rn(hv.z, hv.w);

@@ -41,13 +41,13 @@ __global__ void embed_kernel(const int* __restrict__ tok, const T_* __restrict__
   for (int j = threadIdx.x; j < d; j += blockDim.x) h[(size_t)r * d + j] = to_f32(emb[(size_t)x * d + j]);
 }
 
-// Token embedding of bf16 models, with the first RMSNorm deferred: h[r] =
-// tok_emb[tok[r]] (fp32), x[r] = bf16(h[r] * g) and per 128-column block j the
-// sum of squares ss[j][r] (the consumer applies the row scale).  Block = one
-// row, d/4 threads, 4 columns each (warp w covers columns 128w .. 128w+127).
+// Token embedding of bf16 models with the first RMSNorm: h[r] = tok_emb[tok[r]]
+// (fp32) and x[r] = bf16(h[r] / sqrt(mean(h[r]^2) + eps) * g).  Block = one
+// row, d/4 threads, 4 columns each (d a multiple of 128).
 __global__ void embed_norm_kernel(const int* __restrict__ tok, const bf16* __restrict__ emb, float* __restrict__ h,
-                                  bf16* __restrict__ xo, const float* __restrict__ g, float* __restrict__ ss,
-                                  int rows, int d, int V, int* status) {
+                                  bf16* __restrict__ xo, const float* __restrict__ g, int rows, int d, int V,
+                                  float eps, int* status) {
+  __shared__ float red[32];
   const int r = blockIdx.x, c = threadIdx.x * 4;
   if (r >= rows) return;
   int t = tok[r];
@@ -61,15 +61,40 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, const bf16* __res
     v = make_float4(a.x, a.y, b.x, b.y);
   }
   *reinterpret_cast<float4*>(h + (size_t)r * d + c) = v;
+  float q = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = q;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+  const float rs = rsqrtf(tot / (float)d + eps);
   const float4 gg = *reinterpret_cast<const float4*>(g + c);
-  __nv_bfloat162 x01 = __floats2bfloat162_rn(v.x * gg.x, v.y * gg.y);
-  __nv_bfloat162 x23 = __floats2bfloat162_rn(v.z * gg.z, v.w * gg.w);
+  __nv_bfloat162 x01 = __floats2bfloat162_rn(v.x * rs * gg.x, v.y * rs * gg.y);
+  __nv_bfloat162 x23 = __floats2bfloat162_rn(v.z * rs * gg.z, v.w * rs * gg.w);
   uint2 xp;
   xp.x = *reinterpret_cast<unsigned*>(&x01);
   xp.y = *reinterpret_cast<unsigned*>(&x23);
   *reinterpret_cast<uint2*>(xo + (size_t)r * d + c) = xp;
-  const float q = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
-  if ((threadIdx.x & 31) == 0) ss[(size_t)(c >> 7) * rows + r] = q;
+}
+
+// RMSNorm of bf16 models from the row sums of squares the producing GEMM
+// left per 128-column block (ss[p][r], p < d/128):
+//   x[r] = bf16(h[r] / sqrt(sum_p ss[p][r] / d + eps) * g).
+// Block = one row, d/4 threads (4 columns each).
+__global__ void norm_rows_kernel(const float* __restrict__ h, const float* __restrict__ ss, const float* __restrict__ g,
+                                 bf16* __restrict__ xo, int rows, int d, float eps) {
+  const int r = blockIdx.x, c = threadIdx.x * 4;
+  if (r >= rows) return;
+  float tot = 0.f;
+  for (int p = 0; p < d / 128; ++p) tot += ss[(size_t)p * rows + r];
+  const float rs = rsqrtf(tot / (float)d + eps);
+  const float4 v = *reinterpret_cast<const float4*>(h + (size_t)r * d + c);
+  const float4 gg = *reinterpret_cast<const float4*>(g + c);
+  __nv_bfloat162 x01 = __floats2bfloat162_rn(v.x * rs * gg.x, v.y * rs * gg.y);
+  __nv_bfloat162 x23 = __floats2bfloat162_rn(v.z * rs * gg.z, v.w * rs * gg.w);
+  uint2 xp;
+  xp.x = *reinterpret_cast<unsigned*>(&x01);
+  xp.y = *reinterpret_cast<unsigned*>(&x23);
+  *reinterpret_cast<uint2*>(xo + (size_t)r * d + c) = xp;
 }
 
 // o = bf16(s), element-wise.

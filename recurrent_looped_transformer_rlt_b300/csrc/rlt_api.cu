@@ -20,6 +20,7 @@
 #include "gemm_simple.cuh"
 #include "gemm_tc.cuh"
 #include "kernels.cuh"
+#include "attn_enc.cuh"
 #include "xattn.cuh"
 
 using namespace rlt;
@@ -385,6 +386,48 @@ int swiglu_proj(cudaStream_t st, const T_* A, int lda, int M, int K, const T_* W
   }
 }
 
+// x = bf16(RMSNorm(h) * g) for bf16 models, from the producer's per-128-column
+// sums of squares.
+int norm_rows(cudaStream_t st, const float* h, const float* ss, const float* g, bf16* x, int rows, int d, float eps) {
+  norm_rows_kernel<<<rows, d / 4, 0, st>>>(h, ss, g, x, rows, d, eps);
+  g_launches++;
+  return launch_ok();
+}
+
+// Causal self-attention of the bf16 encoder: the flash kernel on the tensor
+// cores (head_dim 16..128), the CUDA-core kernel below that.
+template <int HD>
+int enc_flash_launch(cudaStream_t st, const bf16* q, const bf16* k, const bf16* v, bf16* o, int B, int T, int H) {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(fa::enc_flash_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)fa::smem_bytes<HD>()) != cudaSuccess)
+      return RLT_ECUDA;
+    attr = true;
+  }
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  fa::enc_flash_kernel<HD><<<dim3(cdiv(T, fa::BQ), H, B), fa::THREADS, fa::smem_bytes<HD>(), st>>>(q, k, v, o, T, H,
+                                                                                                   scale_log2);
+  g_launches++;
+  return launch_ok();
+}
+int enc_attention_bf16(cudaStream_t st, const bf16* q, const bf16* k, const bf16* v, bf16* o, int B, int T, int H,
+                       int hd) {
+  switch (hd) {
+    case 16: return enc_flash_launch<16>(st, q, k, v, o, B, T, H);
+    case 32: return enc_flash_launch<32>(st, q, k, v, o, B, T, H);
+    case 64: return enc_flash_launch<64>(st, q, k, v, o, B, T, H);
+    case 128: return enc_flash_launch<128>(st, q, k, v, o, B, T, H);
+    default: {
+      const size_t att_smem = sizeof(float) * (32 * hd + 32 * (hd + 1) + 32 * hd);
+      enc_attn_simt_kernel<bf16><<<dim3(cdiv(T, 32), H, B), 256, att_smem, st>>>(q, k, v, o, T, H, hd,
+                                                                                 1.0f / sqrtf((float)hd));
+      g_launches++;
+      return launch_ok();
+    }
+  }
+}
+
 // bf16 encoder: projections on the tensor cores with the RMSNorms deferred
 // into them (the residual producers write x = bf16(h * g_next) and row sums of
 // squares; the consumers scale their output rows), RoPE and the head-major
@@ -407,36 +450,31 @@ int encode_bf16(const rlt_model* m, const int32_t* tok, int B, int T, bf16* e, b
   bf16* o = at<bf16>(ws, Lw.e_o);
   float* ss = at<float>(ws, Lw.e_ss);
   const TcScratch sc = tc_scratch(m, ws, Lw);
-  const tc::RowScale rsc{ss, d / 128, 1.0f / (float)d, c.rms_eps};
   int rc;
   rope_table_kernel<<<cdiv((size_t)T * (hd / 2), 256), 256, 0, st>>>(tab, 0, T, hd / 2, (double)c.rope_theta);
   g_launches++;
-  embed_norm_kernel<<<R, d / 4, 0, st>>>(tok, static_cast<const bf16*>(w.tok_emb), h, x, w.enc_attn_norm, ss, R, d,
-                                         c.vocab, status);
+  embed_norm_kernel<<<R, d / 4, 0, st>>>(tok, static_cast<const bf16*>(w.tok_emb), h, x, w.enc_attn_norm, R, d,
+                                         c.vocab, c.rms_eps, status);
   g_launches++;
   if ((rc = launch_ok())) return rc;
-  const float scale = 1.0f / sqrtf((float)hd);
-  const size_t att_smem = sizeof(float) * (32 * hd + 32 * (hd + 1) + 32 * hd);
   for (int l = 0; l < L; ++l) {
     const bf16* Wqkv = wl<bf16>(w.W_qkv, l, (size_t)3 * d * d);
-    if ((rc = gemm_bf16_tc(st, x, d, R, d, Wqkv, d, 3 * d, EpiEncQKVRope<bf16>{q, k, v, tab, d, H, hd, T}, sc, rsc)))
+    if ((rc = gemm_bf16_tc(st, x, d, R, d, Wqkv, d, 3 * d, EpiEncQKVRope<bf16>{q, k, v, tab, d, H, hd, T}, sc)))
       return rc;
-    enc_attn_simt_kernel<bf16><<<dim3(cdiv(T, 32), H, B), 256, att_smem, st>>>(q, k, v, o, T, H, hd, scale);
-    g_launches++;
-    if ((rc = launch_ok())) return rc;
+    if ((rc = enc_attention_bf16(st, q, k, v, o, B, T, H, hd))) return rc;
     const bf16* WO = wl<bf16>(w.W_O, l, (size_t)d * d);
-    if ((rc = gemm_bf16_tc(st, o, d, R, d, WO, d, d,
-                           EpiResidual{HOut{h, d, x, w.enc_ffn_norm + (size_t)l * d, nullptr, nullptr, ss, R}}, sc)))
-      return rc;
+    if ((rc = gemm_bf16_tc(st, o, d, R, d, WO, d, d, EpiResidual{HOut{h, d, nullptr, nullptr, ss, R}}, sc))) return rc;
+    if ((rc = norm_rows(st, h, ss, w.enc_ffn_norm + (size_t)l * d, x, R, d, c.rms_eps))) return rc;
     const bf16* W1 = wl<bf16>(w.W_1, l, (size_t)f * d);
     const bf16* W3 = wl<bf16>(w.W_3, l, (size_t)f * d);
-    if ((rc = gemm_bf16_tc_glu(st, x, d, R, d, W1, W3, d, f, EpiStoreT<bf16>{xm, f}, sc, rsc))) return rc;
+    if ((rc = gemm_bf16_tc_glu(st, x, d, R, d, W1, W3, d, f, EpiStoreT<bf16>{xm, f}, sc))) return rc;
     const bf16* W2 = wl<bf16>(w.W_2, l, (size_t)d * f);
-    const float* gn = (l + 1 < L) ? w.enc_attn_norm + (size_t)(l + 1) * d : w.enc_norm;
-    if ((rc = gemm_bf16_tc(st, xm, f, R, f, W2, f, d, EpiResidual{HOut{h, d, x, gn, nullptr, nullptr, ss, R}}, sc)))
+    if ((rc = gemm_bf16_tc(st, xm, f, R, f, W2, f, d, EpiResidual{HOut{h, d, nullptr, nullptr, ss, R}}, sc))) return rc;
+    // RMSNorm of the next layer's attention, or the final norm producing e
+    if ((rc = norm_rows(st, h, ss, (l + 1 < L) ? w.enc_attn_norm + (size_t)(l + 1) * d : w.enc_norm,
+                        (l + 1 < L) ? x : e, R, d, c.rms_eps)))
       return rc;
   }
-  if ((rc = rmsnorm<bf16>(st, h, w.enc_norm, e, R, d, d, c.rms_eps))) return rc;
   const size_t plane = (size_t)B * H * T * hd;
   for (int g = 0; g < G; ++g) {
     const bf16* WK = wl<bf16>(w.W_K, g, (size_t)d * d);
@@ -736,7 +774,6 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
   float* ss = at<float>(ws, Lw.d_ss);
   bf16* s16 = at<bf16>(ws, Lw.d_s16);
   const TcScratch sc = tc_scratch(m, ws, Lw);
-  const tc::RowScale rsc{ss, d / 128, 1.0f / (float)d, c.rms_eps};
   const tc::RowScale none{nullptr, 0, 0.f, 0.f};
   auto act = [](const bf16* p, int ld) {
     AArg a;
@@ -787,11 +824,17 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     a.A2 = s16;
     a.lda2 = d;
     a.split = d;
-    EpiMerge em{HOut{h, d, x, w.dec_attn_norm, nullptr, nullptr, ss, B}, e, (size_t)A.T_mem * d, sst->s, w.b_g, ctx,
+    EpiMerge em{HOut{h, d, nullptr, nullptr, ss, B}, e, (size_t)A.T_mem * d, sst->s, w.b_g, ctx,
                 c.gate_mode == RLT_GATE_DISCARD_S ? 1 : 0};
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, a, B, 2 * d, static_cast<const bf16*>(w.W_g), nullptr, 2 * d, d, em, sc, none)))) return rc;
   }
+  auto norm = [&](const float* g) -> int {  // x = bf16(RMSNorm(h) * g)
+    int r = norm_rows(st, h, ss, g, x, B, d, c.rms_eps);
+    nk++;
+    return r;
+  };
+  if ((rc = norm(w.dec_attn_norm))) return rc;
   const size_t ring_layer = (size_t)B * H * Wn * hd;
   const size_t plane = (size_t)B * H * A.T_mem * hd;
   bf16* rk = static_cast<bf16*>(sst->ring_k);
@@ -812,7 +855,7 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     const bf16* Wqkv = wl<bf16>(w.W_qkv, l, (size_t)3 * d * d);
     EpiQKVRope<bf16> eq{C, rk + l * ring_layer, rv + l * ring_layer, tab, ctx, d, H, hd, Wn};
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, Wqkv, nullptr, d, 3 * d, eq, sc, rsc)))) return rc;
+    if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, Wqkv, nullptr, d, 3 * d, eq, sc, none)))) return rc;
     if ((rc = mark(RLT_TIMER_SWA))) return rc;
     {
       XattnArgs sa = xa;
@@ -826,13 +869,13 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     if ((rc = mark(RLT_TIMER_SWA))) return rc;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, act(o, d), B, d, wl<bf16>(w.W_O, l, (size_t)d * d), nullptr, d, d,
-                                         EpiResidual{HOut{h, d, x, w.dec_xattn_norm + ld, nullptr, nullptr, ss, B}}, sc,
-                                         none))))
+                                         EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc, none))))
       return rc;
+    if ((rc = norm(w.dec_xattn_norm + ld))) return rc;
     // cross-attention to memory positions 0..p
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, wl<bf16>(w.W_Qx, l, (size_t)d * d), nullptr, d, d,
-                                         EpiStoreF32{C, d}, sc, rsc))))
+                                         EpiStoreF32{C, d}, sc, none))))
       return rc;
     const int g = (c.mem_groups == 1) ? 0 : l;
     if ((rc = mark(RLT_TIMER_XATTN))) return rc;
@@ -848,27 +891,27 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     if ((rc = mark(RLT_TIMER_XATTN))) return rc;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, act(o, d), B, d, wl<bf16>(w.W_Ox, l, (size_t)d * d), nullptr, d, d,
-                                         EpiResidual{HOut{h, d, x, w.dec_ffn_norm + ld, nullptr, nullptr, ss, B}}, sc,
-                                         none))))
+                                         EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc, none))))
       return rc;
+    if ((rc = norm(w.dec_ffn_norm + ld))) return rc;
     // SwiGLU FFN
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<true>(st, act(x, d), B, d, wl<bf16>(w.W_1, l, (size_t)f * d),
-                                        wl<bf16>(w.W_3, l, (size_t)f * d), d, f, EpiStoreT<bf16>{xm, f}, sc, rsc))))
+                                        wl<bf16>(w.W_3, l, (size_t)f * d), d, f, EpiStoreT<bf16>{xm, f}, sc, none))))
       return rc;
     const bool last = (l + 1 == L);
-    HOut ho{h, d, x, last ? w.head_norm : w.dec_attn_norm + ld + d, last ? sst->s : nullptr, last ? s16 : nullptr, ss,
-            B};
+    HOut ho{h, d, last ? sst->s : nullptr, last ? s16 : nullptr, ss, B};
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, act(xm, f), B, f, wl<bf16>(w.W_2, l, (size_t)d * f), nullptr, f, d, EpiResidual{ho}, sc,
                                          none))))
       return rc;
+    if ((rc = norm(last ? w.head_norm : w.dec_attn_norm + ld + d))) return rc;
   }
-  // head: logits = W_o (x * r) with x = bf16(s_t * g_o) and r the RMS scale of s_t
+  // head: logits = W_o x with x = bf16(RMSNorm_o(s_t))
   if ((rc = mark(RLT_TIMER_HEAD))) return rc;
   if ((rc = mark(RLT_TIMER_GEMM))) return rc;
   if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, static_cast<const bf16*>(w.W_o), nullptr, d, V, EpiStoreF32{C, V}, sc,
-                                         rsc))))
+                                         none))))
     return rc;
   HeadArgs ha;
   ha.logits = C;

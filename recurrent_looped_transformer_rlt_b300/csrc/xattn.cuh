@@ -89,23 +89,30 @@ __device__ __forceinline__ void load_seg<float, 4>(const float* p, float (&v)[4]
   v[3] = f.w;
 }
 
-// Splits per pair: the S in [1, min(nch, kXMaxSplits)] (every split
-// non-empty) with the least estimated time, in chunk-times: rounds of tasks
-// over the warps of the grid times (chunks per task + the per-task cost of
-// emitting a partial and merging), ties to the smaller S.
+// Splits per pair.  A warp keeps two chunks in flight, so the stream rate
+// grows with the number of busy warps: S is at least the smallest count that
+// gives every warp a task (when the pairs have that many chunks); among the
+// S from there to min(nch, kXMaxSplits) (every split non-empty) the one with
+// the least estimated time in chunk-times - rounds of tasks over the warps
+// times (chunks per task + the per-task cost of emitting a partial and
+// merging) - ties to the smaller S.
 constexpr int kXTaskCost = 3;
 __device__ __forceinline__ int xattn_splits(int pairs, int nch, int warps) {
-  int best = 1;
-  long long best_cost = (((long long)pairs + warps - 1) / warps) * (nch + 1);
   const int smax = min(nch, kXMaxSplits);
-  for (int s = 2; s <= smax; ++s) {
-    const int cps = (nch + s - 1) / s;
-    if ((nch + cps - 1) / cps != s) continue;
-    const long long rounds = ((long long)pairs * s + warps - 1) / warps;
-    const long long cost = rounds * (cps + kXTaskCost);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = s;
+  const int smin = max(1, min(smax, (9 * warps / 10 + pairs - 1) / pairs));
+  int best = 1;  // always valid
+  long long best_cost = -1;
+  for (int pass = 0; pass < 2 && best_cost < 0; ++pass) {
+    const int lo = pass == 0 ? smin : 1, hi = pass == 0 ? smax : smin - 1;
+    for (int s = lo; s <= hi; ++s) {
+      const int cps = (nch + s - 1) / s;
+      if ((nch + cps - 1) / cps != s) continue;  // some split would be empty
+      const long long rounds = ((long long)pairs * s + warps - 1) / warps;
+      const long long cost = rounds * (cps + (s > 1 ? kXTaskCost : 1));
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best = s;
+      }
     }
   }
   return best;
@@ -136,7 +143,7 @@ __global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
   const int warps = gridDim.x * kXWarps;
   const int gw = blockIdx.x * kXWarps + warp;
   const int ns = xattn_splits(pairs, nch, warps);
-  const int cps = (nch + ns - 1) / ns;  // chunks per split (the last split may have fewer)
+  const int cps = (nch + ns - 1) / ns;  // chunks per split (the last split may have fewer, never none)
   const int tasks = pairs * ns;
   const int my_tasks = (gw < tasks) ? (tasks - gw + warps - 1) / warps : 0;
   const int d = a.H * HD;

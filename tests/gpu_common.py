@@ -102,3 +102,54 @@ def oracle_ring(cfg, cache, pos):
             p = pos - n + j
             out[(l, p % W)] = (k, v)
     return out
+
+
+def gpu_transition_snapshots(wl, W, tok, acts, t0s, rows, temperature=1.0, top_k=0):
+    """Run the CUDA path over all of tok; before each step t0 + 1 (t0 in t0s) keep
+    the state of the sequences `rows` (s, the window's ring entries, position) and
+    the outputs of that step.  Returns (e, mem) of those rows and a list of dicts."""
+    import torch
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from recurrent_looped_transformer_rlt_b300 import runner
+    B, T = tok.shape
+    model = rlt.Model(wl.cfg, W)
+    buf = runner.alloc_buffers(model, B, T)
+    runner.encode(model, torch.from_numpy(tok).cuda(), buf)
+    st = runner.new_state(model, B)
+    acts_t = torch.from_numpy(acts).cuda()
+    snaps = []
+    for t0 in sorted(t0s):
+        if t0 > st.pos:
+            runner.decode(model, st, buf, t0 - st.pos, acts_t[:, st.pos:t0].contiguous(), temperature, top_k)
+        torch.cuda.synchronize()
+        snap = dict(pos=st.pos, s=st.s[rows].cpu().numpy().astype(np.float64),
+                    ring_k=st.ring_k[:, rows].float().cpu().numpy(), ring_v=st.ring_v[:, rows].float().cpu().numpy())
+        out = runner.decode(model, st, buf, 1, acts_t[:, t0:t0 + 1].contiguous(), temperature, top_k, emit_steps=[0])
+        torch.cuda.synchronize()
+        snap.update(logits=out.logits[0][rows].cpu().numpy(), logp=out.logp[rows, 0].cpu().numpy(),
+                    logp_full=out.logp_full[rows, 0].cpu().numpy(), argmax=out.argmax[rows, 0].cpu().numpy(),
+                    s_next=st.s[rows].cpu().numpy())
+        snaps.append(snap)
+    assert runner.status(buf) == 0
+    e = buf.e[rows].float().cpu().numpy().astype(np.float64)
+    mem = buf.mem[:, :, rows].float().cpu().numpy().astype(np.float64)
+    model.close()
+    return e, mem, snaps
+
+
+def oracle_transition(wl, W, e, mem, snap, acts_col, temperature=1.0, top_k=0):
+    """One oracle step from the CUDA path's state: s, the ring entries of positions
+    pos - W + 1 .. pos - 1 (oldest first), e and memory of the same run."""
+    c = O.Cfg.of(wl.cfg)
+    pos, Wn = snap["pos"], c.window
+    cache = []
+    for l in range(c.n_layers):
+        ent = []
+        for p in range(max(0, pos - (Wn - 1)), pos):
+            ent.append((snap["ring_k"][l, :, :, p % Wn].astype(np.float64),
+                        snap["ring_v"][l, :, :, p % Wn].astype(np.float64)))
+        cache.append(ent)
+    st = O.State(snap["s"].copy(), cache, pos)
+    st2, out = O.decode_steps(c, W, st, e, mem, 1, acts_col, temperature, top_k, emit=[0])
+    return dict(logits=out.logits[0], logp=out.logp[:, 0], logp_full=out.logp_full[:, 0], argmax=out.argmax[:, 0],
+                s_next=st2.s)

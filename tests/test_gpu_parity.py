@@ -4,8 +4,8 @@ import pytest
 
 import rlt_inputs as ri
 from oracle import rlt_oracle as O
-from tests.gpu_common import (BF16_ARGMAX_AGREE, BF16_REL_LOGIT, F32_ABS, check_argmax, gpu_run, oracle_ring,
-                              oracle_run, rel_logit_err)
+from tests.gpu_common import (BF16_ARGMAX_AGREE, BF16_REL_LOGIT, F32_ABS, check_argmax, gpu_run,
+                              gpu_transition_snapshots, oracle_ring, oracle_run, oracle_transition, rel_logit_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -131,6 +131,48 @@ def test_small_bf16_full_size_sampled_rows():
               logits={i: g["logits"][i][rows] for i in emit})
     _check_bf16(gs, o, emit)
     assert np.isfinite(g["s"]).all() and np.isfinite(g["logp"][~np.isnan(g["logp"])]).all()
+
+
+# The larger models' recurrences are chaotic at random init: a one-ulp change
+# in a few elements of e moves the oracle's own logits by ~13% after 70 steps
+# (medium), so two correct bf16 implementations agree only over a few steps.
+# The transition itself is therefore checked from the CUDA path's state: at
+# sampled steps the oracle takes the GPU's s, window entries, e and memory and
+# computes one step, which must match the GPU's next step within the bf16
+# tolerances; the encoder is checked on a prefix of the sequences (causal, so
+# the prefix depends on its own tokens only).
+
+@pytest.mark.parametrize("name,B,T,t0s,kw", [
+    ("medium", 4, 300, [0, 5, 127, 128, 299], {}),                          # ring of 128 wraps
+    ("rlreplay", 4, 120, [0, 63, 64, 119], dict(temperature=0.7, top_k=50)),  # G = L, tempered top-k
+])
+def test_large_configs_transition_parity(name, B, T, t0s, kw):
+    wl, W, tok, acts = _inputs(name, B=B, T=T, jitter=0.0)
+    rows = list(range(B))
+    e, mem, snaps = gpu_transition_snapshots(wl, W, tok, acts, t0s, rows, **kw)
+    for snap in snaps:
+        t0 = snap["pos"]
+        o = oracle_transition(wl, W, e, mem, snap, acts[:, t0:t0 + 1], **kw)
+        rel = rel_logit_err(snap["logits"], o["logits"])
+        assert rel.max() <= BF16_REL_LOGIT, (t0, rel.max())
+        check_argmax(snap["argmax"], snap["logits"], o["logits"])
+        srel = np.abs(snap["s_next"] - o["s_next"]).max() / np.abs(o["s_next"]).max()
+        assert srel <= BF16_REL_LOGIT, (t0, srel)
+        m = np.isfinite(o["logp"])
+        assert np.array_equal(np.isfinite(snap["logp"]), m)
+        lim = 2 * BF16_REL_LOGIT * np.abs(o["logits"]).max() + 1e-3
+        if m.any():
+            assert np.abs(snap["logp"][m] - o["logp"][m]).max() <= lim
+        mf = np.isfinite(o["logp_full"])   # the last position has no next token to score
+        assert np.array_equal(np.isfinite(snap["logp_full"]), mf)
+        if mf.any():
+            assert np.abs(snap["logp_full"][mf] - o["logp_full"][mf]).max() <= lim
+    # encoder and memory on a prefix
+    P = 24
+    c = O.Cfg.of(wl.cfg)
+    oe, omem = O.encode(c, W, tok[:, :P])
+    assert np.abs(e[:, :P] - oe).max() <= BF16_REL_LOGIT * np.abs(oe).max()
+    assert np.abs(mem[..., :P, :] - omem).max() <= BF16_REL_LOGIT * np.abs(omem).max()
 
 
 # ---------------------------------------------------------------------------
