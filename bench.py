@@ -179,7 +179,8 @@ def run_gpu(args, rank, world, local_rank):
     # timed region: K steps, inputs resident in HBM, L2 flushed before each step
     times, enc_times = [], []
     launches0 = rlt.rlt_launch_count()
-    timer_on = model.timer_arm(args.kernel_class, 1 << 15) if args.kernel_class else False
+    n_timed = min(args.steps * T * c.n_layers, 1 << 18)  # one launch per layer and step
+    timer_on = model.timer_arm(args.kernel_class, n_timed) if args.kernel_class else False
     with ClockSampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize()

@@ -114,7 +114,7 @@ WsLayout layout(const rlt_model* m, int B, int T) {
   L.e_h = take(4 * R * d);
   L.e_a = take(es * R * d);
   L.e_m = take(es * R * f);
-  L.e_c = take(4 * R * std::max(3 * d, 2 * f));
+  L.e_c = take(es == 4 ? 4 * R * std::max(3 * d, 2 * f) : 0);  // fp32 models: projection outputs
   L.e_q = take(es * R * d);
   L.e_k = take(es * R * d);
   L.e_v = take(es * R * d);
