@@ -154,21 +154,31 @@ struct AOperand {
   const StepCtx* ctx;
 };
 
-// Deferred RMSNorm: when ss != nullptr, output row m is multiplied by
-// rsqrt(sum_{p < parts} ss[p * M + m] * inv_d + eps), the row's RMS scale; the
-// A operand then holds x * g (the gain applied, the scale not), and since the
-// scale is one number per row it factors out of the contraction.
-struct RowScale {
-  const float* ss;
-  int parts;
-  float inv_d, eps;
-};
-
 struct SplitK {
   int splits;        // CTAs along K (= cluster size along z when > 1)
   int kb_per_split;  // k-blocks per CTA
 };
 
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// shared::cluster address of the same offset in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t mapa_u32(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  return ra;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
@@ -303,7 +313,7 @@ template <int BN, int STAGES, bool GLU, class Epi>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3, int M, int N,
-                   int K, AOperand ao, RowScale rsc, SplitK sk, Epi epi, int* status) {
+                   int K, AOperand ao, SplitK sk, Epi epi, int* status) {
   using C = Cfg<BN, STAGES>;
   constexpr int NOUT = GLU ? BN / 2 : BN;  // output columns per tile
   extern __shared__ unsigned char smem_raw[];
@@ -322,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int kb_total = (K + BK - 1) / BK;
   const int kb0 = z * sk.kb_per_split;
   const int nkb = max(0, min(kb_total, kb0 + sk.kb_per_split) - kb0);
-  int issued = 0;
+  int issued = 0;  // k-blocks whose copies were requested (weights of the first `pre` requested earlier)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -345,6 +355,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // weights do not depend on the previous kernel: the first stages' weight
+  // tiles are requested before waiting for it
+  const int pre = min(nkb, STAGES);
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < pre; ++i) {
+      unsigned char* sa = smem + i * C::STAGE_BYTES;
+      const int kx = (kb0 + i) * BK;
+      mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+      if (GLU) {
+        tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[i]);
+        tma_load_2d(sa + C::A_BYTES + C::B_BYTES / 2, &tmB3, kx, nb0, &full[i]);
+      } else {
+        tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[i]);
+      }
+    }
+  }
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_trigger();
+
   if (warp == 0) {
     if (lane == 0) {
       const int pos = ao.pos3d ? ao.ctx->pos : 0;
@@ -356,7 +385,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         unsigned char* sa = smem + s * C::STAGE_BYTES;
         const int kx = (kb0 + i) * BK;
-        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        if (i >= pre) mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         if (kb0 + i < ao.split_kb) {
           if (ao.pos3d)
             tma_load_3d(sa, &tmA, kx, pos, m0, &full[s]);
@@ -365,11 +394,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {
           tma_load_2d(sa, &tmA2, kx - ao.split_kb * BK, m0, &full[s]);
         }
-        if (GLU) {
-          tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[s]);
-          tma_load_2d(sa + C::A_BYTES + C::B_BYTES / 2, &tmB3, kx, nb0, &full[s]);
-        } else {
-          tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[s]);
+        if (i >= pre) {
+          if (GLU) {
+            tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[s]);
+            tma_load_2d(sa + C::A_BYTES + C::B_BYTES / 2, &tmB3, kx, nb0, &full[s]);
+          } else {
+            tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[s]);
+          }
         }
         issued = i + 1;
       }
@@ -408,20 +439,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int LDT = BN + 4;
     float* stile = reinterpret_cast<float*>(smem);
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-    float rs = 1.f;
-    if (rsc.ss && m0 + rl < M) {
-      float acc = 0.f;
-      for (int p = 0; p < rsc.parts; ++p) acc += rsc.ss[(size_t)p * M + m0 + rl];
-      rs = rsqrtf(acc * rsc.inv_d + rsc.eps);
-    }
+    if (q * 32 < M - m0) {  // warps whose 32 TMEM lanes hold at least one output row
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      float v[16];
-      tmem_ld16(tq + c0, v);
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(tq + c0, v);
 #pragma unroll
-      for (int j = 0; j < 16; j += 4)
-        *reinterpret_cast<float4*>(stile + rl * LDT + c0 + j) =
-            make_float4(v[j] * rs, v[j + 1] * rs, v[j + 2] * rs, v[j + 3] * rs);
+        for (int j = 0; j < 16; j += 4)
+          *reinterpret_cast<float4*>(stile + rl * LDT + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
     }
     epi_bar();
   }
@@ -436,38 +462,35 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int et = threadIdx.x - 64;
       constexpr int LDT = BN + 4, V4 = BN / 4;
       float* stile = reinterpret_cast<float*>(smem);
-      float4 acc[4];
+      uint32_t rbase[8];  // the staged tile in every CTA of the cluster (splits <= 8)
+#pragma unroll
+      for (int zz = 0; zz < 8; ++zz) rbase[zz] = zz < sk.splits ? mapa_u32(stile, (uint32_t)zz) : 0u;
       const int nv = (r1 - r0) * V4;
-      // sums land in this CTA's own rows [r0, r1): no peer reads those rows
-      for (int i0 = et; i0 < nv; i0 += 4 * 128) {
+      // all splits' values of an element are in flight before they are summed
+      // in split order; the sums go back to rows [r0, r1) of this CTA's own
+      // tile (each element read and written by one thread; the other CTAs of
+      // the cluster read only their own, disjoint row ranges)
+#pragma unroll 2
+      for (int i = et; i < nv; i += 128) {
+        const int r = r0 + i / V4, c4 = i % V4;
+        const uint32_t off = (uint32_t)((r * LDT + c4 * 4) * 4);
+        float4 f[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int zz = 0; zz < sk.splits; ++zz)
+        for (int zz = 0; zz < 8; ++zz)
+          if (zz < sk.splits) f[zz] = ld_cluster_f4(rbase[zz] + off);
+        float4 acc = f[0];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * 128;
-            if (i < nv) {
-              const int r = r0 + i / V4, c4 = i - (i / V4) * V4;
-              const float4 f = ld_dsmem_f4(stile + r * LDT + c4 * 4, (uint32_t)zz);
-              acc[u].x += f.x;
-              acc[u].y += f.y;
-              acc[u].z += f.z;
-              acc[u].w += f.w;
-            }
+        for (int zz = 1; zz < 8; ++zz)
+          if (zz < sk.splits) {
+            acc.x += f[zz].x;
+            acc.y += f[zz].y;
+            acc.z += f[zz].z;
+            acc.w += f[zz].w;
           }
-        // the sums go back to rows [r0, r1) of this CTA's own tile: every
-        // element is read and written by the same thread, and the other CTAs
-        // of the cluster read only their own (disjoint) row ranges
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u * 128;
-          if (i < nv) {
-            const int r = r0 + i / V4, c4 = i - (i / V4) * V4;
-            *reinterpret_cast<float4*>(stile + r * LDT + c4 * 4) = acc[u];
-          }
-        }
+        *reinterpret_cast<float4*>(stile + r * LDT + c4 * 4) = acc;
       }
     }
+    cluster_arrive();  // this CTA is done reading its peers' tiles
   }
   if (warp >= 2) {
     // ---- epilogue functor on rows [r0, r1); consecutive threads take
@@ -478,7 +501,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     epi_bar();
     if (!s_fail) epilogue_tile<BN, GLU>(stile, r0, r1, m0, nb0, N, epi, et);
   }
-  if (sk.splits > 1) cluster_sync_all();  // peers are done reading this CTA's tile
+  if (sk.splits > 1) cluster_wait();  // peers are done reading this CTA's tile before it exits
   tc_fence_before();
   __syncthreads();
   if (s_fail && threadIdx.x == 0) {

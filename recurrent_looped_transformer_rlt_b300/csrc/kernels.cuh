@@ -6,6 +6,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace rlt {
 
@@ -82,6 +83,8 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, const bf16* __res
 // Block = one row, d/4 threads (4 columns each).
 __global__ void norm_rows_kernel(const float* __restrict__ h, const float* __restrict__ ss, const float* __restrict__ g,
                                  bf16* __restrict__ xo, int rows, int d, float eps) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_trigger();
   const int r = blockIdx.x, c = threadIdx.x * 4;
   if (r >= rows) return;
   float tot = 0.f;
@@ -473,6 +476,8 @@ struct HeadArgs {
 };
 
 __global__ void __launch_bounds__(1024) head_reduce_kernel(HeadArgs a, const StepCtx* ctx) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_trigger();
   extern __shared__ float sx[];  // [V] tempered logits
   __shared__ unsigned hist[256];
   __shared__ float fred[32];
@@ -598,6 +603,8 @@ __global__ void __launch_bounds__(1024) head_reduce_kernel(HeadArgs a, const Ste
 }
 
 __global__ void advance_kernel(StepCtx* ctx) {
+  pdl_wait();
+  pdl_trigger();
   ctx->pos += 1;
   ctx->step += 1;
 }

@@ -53,6 +53,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
                : "memory");
 }
 
+// Programmatic dependent launch.  pdl_wait: block until the previous kernel of
+// the stream has completed and its memory is visible (immediately when the
+// kernel was launched without the programmatic attribute); pdl_trigger: allow
+// the next kernel to be scheduled.  Kernels here trigger only after their own
+// wait, so at most one kernel runs ahead: before its wait a kernel may read
+// only data produced two or more kernels earlier (weights, encoder memory).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 // ~1 s at the maximum SM clock: a wait that long means the copy engine never
 // delivered, which is reported as a timeout.
 constexpr long long kWaitBudget = 2000000000LL;

@@ -36,6 +36,24 @@ std::atomic<uint64_t> g_launches{0};
   } while (0)
 
 inline int launch_ok() { return cudaGetLastError() == cudaSuccess ? RLT_OK : RLT_ECUDA; }
+
+// Launch with programmatic dependent launch: the kernel may be scheduled
+// while the previous kernel of the stream is still running; it calls
+// pdl_wait() before touching anything that kernel produces.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? RLT_OK : RLT_ECUDA;
+}
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline unsigned cdiv(size_t a, size_t b) { return (unsigned)((a + b - 1) / b); }
@@ -217,7 +235,7 @@ struct AArg {
 
 template <int BN, int STAGES, bool GLU, class Epi>
 int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, const bf16* B3, int ldb, int N,
-                   Epi epi, const TcScratch& sc, tc::RowScale rsc) {
+                   Epi epi, const TcScratch& sc) {
   using C = tc::Cfg<BN, STAGES>;
   static bool attr = false;
   if (!attr) {
@@ -263,14 +281,16 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   cfg.blockDim = dim3(tc::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 1;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = splits;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = 1;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = splits;
   cfg.attrs = at;
-  cfg.numAttrs = splits > 1 ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi>, ta, ta2, tb, tb3, M, N, K, ao, rsc, sk, epi,
+  cfg.numAttrs = splits > 1 ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi>, ta, ta2, tb, tb3, M, N, K, ao, sk, epi,
                          sc.status) != cudaSuccess)
     return RLT_ECUDA;
   g_launches++;
@@ -280,40 +300,40 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
 // C = A[M,K] B[N,K]^T with the epilogue functor; tiles sized for the shape.
 template <class Epi>
 int gemm_bf16_tc(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, int ldb, int N, Epi epi,
-                 const TcScratch& sc, tc::RowScale rsc = tc::RowScale{nullptr, 0, 0.f, 0.f}) {
+                 const TcScratch& sc) {
   if (M <= 0 || N <= 0) return RLT_OK;
-  if (M <= tc::BM) return gemm_tc_launch<128, 3, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc, rsc);
-  return gemm_tc_launch<256, 4, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc, rsc);
+  if (M <= tc::BM) return gemm_tc_launch<128, 3, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc);
+  return gemm_tc_launch<256, 4, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc);
 }
 template <class Epi>
 int gemm_bf16_tc(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* B, int ldb, int N, Epi epi,
-                 const TcScratch& sc, tc::RowScale rsc = tc::RowScale{nullptr, 0, 0.f, 0.f}) {
+                 const TcScratch& sc) {
   AArg a;
   a.A = A;
   a.lda = lda;
-  return gemm_bf16_tc(st, a, M, K, B, ldb, N, epi, sc, rsc);
+  return gemm_bf16_tc(st, a, M, K, B, ldb, N, epi, sc);
 }
 // Projection of a batch of sequences (decoder step, rlt_linear): 3-stage
 // pipeline for up to 128 rows (two CTAs fit on an SM), 4 stages of 256-wide
 // tiles beyond.
 template <bool GLU, class Epi>
 int proj_bf16(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const bf16* W3, int ldw, int N, Epi epi,
-              const TcScratch& sc, tc::RowScale rsc) {
+              const TcScratch& sc) {
   if (M <= 0 || N <= 0) return RLT_OK;
-  if (M <= tc::BM) return gemm_tc_launch<128, 3, GLU>(st, x, M, K, W, W3, ldw, N, epi, sc, rsc);
-  return gemm_tc_launch<256, 4, GLU>(st, x, M, K, W, W3, ldw, N, epi, sc, rsc);
+  if (M <= tc::BM) return gemm_tc_launch<128, 3, GLU>(st, x, M, K, W, W3, ldw, N, epi, sc);
+  return gemm_tc_launch<256, 4, GLU>(st, x, M, K, W, W3, ldw, N, epi, sc);
 }
 
 // out[m][j] = silu(A W_1^T)[m][j] * (A W_3^T)[m][j], j < N (= d_ffn).
 template <class Epi>
 int gemm_bf16_tc_glu(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* W1, const bf16* W3, int ldb,
-                     int N, Epi epi, const TcScratch& sc, tc::RowScale rsc = tc::RowScale{nullptr, 0, 0.f, 0.f}) {
+                     int N, Epi epi, const TcScratch& sc) {
   if (M <= 0 || N <= 0) return RLT_OK;
   AArg a;
   a.A = A;
   a.lda = lda;
-  if (M <= tc::BM) return gemm_tc_launch<128, 3, true>(st, a, M, K, W1, W3, ldb, N, epi, sc, rsc);
-  return gemm_tc_launch<256, 4, true>(st, a, M, K, W1, W3, ldb, N, epi, sc, rsc);
+  if (M <= tc::BM) return gemm_tc_launch<128, 3, true>(st, a, M, K, W1, W3, ldb, N, epi, sc);
+  return gemm_tc_launch<256, 4, true>(st, a, M, K, W1, W3, ldb, N, epi, sc);
 }
 
 TcScratch tc_scratch(const rlt_model* m, void* ws, const WsLayout& Lw) {
@@ -389,9 +409,8 @@ int swiglu_proj(cudaStream_t st, const T_* A, int lda, int M, int K, const T_* W
 // x = bf16(RMSNorm(h) * g) for bf16 models, from the producer's per-128-column
 // sums of squares.
 int norm_rows(cudaStream_t st, const float* h, const float* ss, const float* g, bf16* x, int rows, int d, float eps) {
-  norm_rows_kernel<<<rows, d / 4, 0, st>>>(h, ss, g, x, rows, d, eps);
   g_launches++;
-  return launch_ok();
+  return launch_pdl(norm_rows_kernel, dim3(rows), dim3(d / 4), 0, st, h, ss, g, x, rows, d, eps);
 }
 
 // Causal self-attention of the bf16 encoder: the flash kernel on the tensor
@@ -774,7 +793,6 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
   float* ss = at<float>(ws, Lw.d_ss);
   bf16* s16 = at<bf16>(ws, Lw.d_s16);
   const TcScratch sc = tc_scratch(m, ws, Lw);
-  const tc::RowScale none{nullptr, 0, 0.f, 0.f};
   auto act = [](const bf16* p, int ld) {
     AArg a;
     a.A = p;
@@ -827,7 +845,7 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     EpiMerge em{HOut{h, d, nullptr, nullptr, ss, B}, e, (size_t)A.T_mem * d, sst->s, w.b_g, ctx,
                 c.gate_mode == RLT_GATE_DISCARD_S ? 1 : 0};
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(proj_bf16<false>(st, a, B, 2 * d, static_cast<const bf16*>(w.W_g), nullptr, 2 * d, d, em, sc, none)))) return rc;
+    if ((rc = gemm_done(proj_bf16<false>(st, a, B, 2 * d, static_cast<const bf16*>(w.W_g), nullptr, 2 * d, d, em, sc)))) return rc;
   }
   auto norm = [&](const float* g) -> int {  // x = bf16(RMSNorm(h) * g)
     int r = norm_rows(st, h, ss, g, x, B, d, c.rms_eps);
@@ -855,7 +873,7 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     const bf16* Wqkv = wl<bf16>(w.W_qkv, l, (size_t)3 * d * d);
     EpiQKVRope<bf16> eq{C, rk + l * ring_layer, rv + l * ring_layer, tab, ctx, d, H, hd, Wn};
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, Wqkv, nullptr, d, 3 * d, eq, sc, none)))) return rc;
+    if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, Wqkv, nullptr, d, 3 * d, eq, sc)))) return rc;
     if ((rc = mark(RLT_TIMER_SWA))) return rc;
     {
       XattnArgs sa = xa;
@@ -863,19 +881,20 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
       sa.mv = rv + l * ring_layer;
       sa.T_mem = Wn;
       sa.t_cap = Wn;
+      sa.early = 0;  // the ring entry of this step is written by the QKV projection just before
       if (launch_xattn<bf16>(sa, hd, m->n_sm, st) != cudaSuccess) return RLT_ECUDA;
       if ((rc = post())) return rc;
     }
     if ((rc = mark(RLT_TIMER_SWA))) return rc;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, act(o, d), B, d, wl<bf16>(w.W_O, l, (size_t)d * d), nullptr, d, d,
-                                         EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc, none))))
+                                         EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc))))
       return rc;
     if ((rc = norm(w.dec_xattn_norm + ld))) return rc;
     // cross-attention to memory positions 0..p
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, wl<bf16>(w.W_Qx, l, (size_t)d * d), nullptr, d, d,
-                                         EpiStoreF32{C, d}, sc, none))))
+                                         EpiStoreF32{C, d}, sc))))
       return rc;
     const int g = (c.mem_groups == 1) ? 0 : l;
     if ((rc = mark(RLT_TIMER_XATTN))) return rc;
@@ -885,33 +904,32 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
       ca.mv = mem + (2 * g + 1) * plane;
       ca.T_mem = A.T_mem;
       ca.t_cap = A.T_mem;
+      ca.early = 1;  // encoder memory: written before the decoder call
       if (launch_xattn<bf16>(ca, hd, m->n_sm, st) != cudaSuccess) return RLT_ECUDA;
       if ((rc = post())) return rc;
     }
     if ((rc = mark(RLT_TIMER_XATTN))) return rc;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, act(o, d), B, d, wl<bf16>(w.W_Ox, l, (size_t)d * d), nullptr, d, d,
-                                         EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc, none))))
+                                         EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc))))
       return rc;
     if ((rc = norm(w.dec_ffn_norm + ld))) return rc;
     // SwiGLU FFN
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<true>(st, act(x, d), B, d, wl<bf16>(w.W_1, l, (size_t)f * d),
-                                        wl<bf16>(w.W_3, l, (size_t)f * d), d, f, EpiStoreT<bf16>{xm, f}, sc, none))))
+                                        wl<bf16>(w.W_3, l, (size_t)f * d), d, f, EpiStoreT<bf16>{xm, f}, sc))))
       return rc;
     const bool last = (l + 1 == L);
     HOut ho{h, d, last ? sst->s : nullptr, last ? s16 : nullptr, ss, B};
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(proj_bf16<false>(st, act(xm, f), B, f, wl<bf16>(w.W_2, l, (size_t)d * f), nullptr, f, d, EpiResidual{ho}, sc,
-                                         none))))
+    if ((rc = gemm_done(proj_bf16<false>(st, act(xm, f), B, f, wl<bf16>(w.W_2, l, (size_t)d * f), nullptr, f, d, EpiResidual{ho}, sc))))
       return rc;
     if ((rc = norm(last ? w.head_norm : w.dec_attn_norm + ld + d))) return rc;
   }
   // head: logits = W_o x with x = bf16(RMSNorm_o(s_t))
   if ((rc = mark(RLT_TIMER_HEAD))) return rc;
   if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-  if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, static_cast<const bf16*>(w.W_o), nullptr, d, V, EpiStoreF32{C, V}, sc,
-                                         none))))
+  if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, static_cast<const bf16*>(w.W_o), nullptr, d, V, EpiStoreF32{C, V}, sc))))
     return rc;
   HeadArgs ha;
   ha.logits = C;
@@ -927,10 +945,11 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
   ha.top_k = A.top_k;
   ha.inv_temp = A.inv_temp;
   ha.status = status;
-  head_reduce_kernel<<<B, 1024, sizeof(float) * V, st>>>(ha, ctx);
+  if ((rc = launch_pdl(head_reduce_kernel, dim3(B), dim3(1024), sizeof(float) * V, st, ha, (const StepCtx*)ctx)))
+    return rc;
   if ((rc = post())) return rc;
   if ((rc = mark(RLT_TIMER_HEAD))) return rc;
-  advance_kernel<<<1, 1, 0, st>>>(ctx);
+  if ((rc = launch_pdl(advance_kernel, dim3(1), dim3(1), 0, st, ctx))) return rc;
   if ((rc = post())) return rc;
   if ((rc = mark(RLT_TIMER_STEP))) return rc;
   *n_kernels = nk;
@@ -1283,10 +1302,9 @@ int rlt_linear(const rlt_model* m, const void* A, int32_t lda, int32_t M, int32_
   a.A = static_cast<const bf16*>(A);
   a.lda = lda;
   const bf16* w = static_cast<const bf16*>(W);
-  const tc::RowScale none{nullptr, 0, 0.f, 0.f};
   if (W3)
-    return proj_bf16<true>(s, a, M, K, w, static_cast<const bf16*>(W3), ldw, N, EpiStoreF32{C, ldc}, sc, none);
-  return proj_bf16<false>(s, a, M, K, w, nullptr, ldw, N, EpiStoreF32{C, ldc}, sc, none);
+    return proj_bf16<true>(s, a, M, K, w, static_cast<const bf16*>(W3), ldw, N, EpiStoreF32{C, ldc}, sc);
+  return proj_bf16<false>(s, a, M, K, w, nullptr, ldw, N, EpiStoreF32{C, ldc}, sc);
 }
 
 int rlt_status(void* ws, rlt_stream_t stream) {

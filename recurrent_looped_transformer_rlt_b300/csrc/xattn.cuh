@@ -62,6 +62,8 @@ struct XattnArgs {
   void* out;          // [B][d]  storage dtype
   int B, H, T_mem;
   int t_cap;          // attend to positions 0 .. min(t_cap, ctx->pos + 1) - 1
+  int early;          // keys/values written two or more kernels earlier (encoder memory): the
+                      // first copies may start before waiting for the previous kernel
   float scale;
   const StepCtx* ctx;
   int* status;
@@ -180,7 +182,13 @@ __global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
       ic = 0;
     }
   };
-  if (lane == 0) {
+  if (a.early && lane == 0) {
+    issue_next(0);
+    issue_next(1);
+  }
+  pdl_wait();  // q, the ring (window) and the outputs depend on the previous kernels
+  if (threadIdx.x == 0) pdl_trigger();
+  if (!a.early && lane == 0) {
     issue_next(0);
     issue_next(1);
   }
@@ -337,8 +345,17 @@ inline cudaError_t launch_xattn_hd(const XattnArgs& a, int n_sm, cudaStream_t st
       o = 1;
     occ = o;
   }
-  dec_xattn_kernel<T_, HD><<<n_sm * occ, kXThreads, S::smem_bytes(), st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_sm * occ);
+  cfg.blockDim = dim3(kXThreads);
+  cfg.dynamicSmemBytes = S::smem_bytes();
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dec_xattn_kernel<T_, HD>, a);
 }
 
 template <typename T_>
