@@ -304,6 +304,90 @@ def run_reference(args, rank):
 
 
 # ---------------------------------------------------------------------------
+# single-kernel cases (for profiler captures): one decoder-step launch of the
+# chosen kernel at the workload's shapes, through the public entry points
+
+def run_profile_case(args):
+    """Cross-attention ("xattn", memory positions 1..T/2), window attention
+    ("swa", the ring of W entries) or a projection ("proj": W_qkv at M = B,
+    "glu": the W_1/W_3 pair) of the workload, timed over --steps launches
+    after --warmup; prints one JSON line with the algorithmic bytes per launch
+    and the achieved bandwidth."""
+    import torch
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    wl = ri.preset(args.workload)
+    c, B = wl.cfg, wl.B
+    if c.dtype != "bf16":
+        raise SystemExit("profile cases cover bf16 workloads")
+    # a one-layer model of the workload's widths (the cases do not use the other layers)
+    c1 = ri.preset(args.workload, n_layers=1, mem_groups=1, vocab=256).cfg
+    g = torch.Generator(device="cuda").manual_seed(0)
+    W = {}
+    for n_, shape, kind in ri.weight_specs(c1):
+        if kind == "mat":
+            W[n_] = (torch.randn(shape, device="cuda", generator=g) * c1.sigma).to(torch.bfloat16)
+        elif kind == "ones":
+            W[n_] = torch.ones(shape, device="cuda")
+        else:
+            W[n_] = torch.randn(shape, device="cuda", generator=g) * 0.02
+    model = rlt.Model(c1, W)
+    d, H, hd = c.d, c.n_heads, c.head_dim
+    stream = torch.cuda.current_stream()
+    bw, _, src = load_peaks()
+    case = args.profile_case
+    if case in ("xattn", "swa"):
+        T_mem = wl.T if case == "xattn" else c.window
+        t = wl.T // 2 if case == "xattn" else c.window
+        mk = torch.randn(B, H, T_mem, hd, device="cuda", generator=g).to(torch.bfloat16)
+        mv = torch.randn(B, H, T_mem, hd, device="cuda", generator=g).to(torch.bfloat16)
+        q = torch.randn(B, d, device="cuda", generator=g)
+        out = torch.empty(B, d, device="cuda", dtype=torch.bfloat16)
+        ws = model.workspace(B, T_mem)
+
+        def launch():
+            rlt.rlt_cross_attention(model.handle, q, mk, mv, B, T_mem, t, out, ws, ws.numel(), stream)
+        nbytes = 2 * B * t * 2 * d + B * d * 4 + B * d * 2
+        kernel = "dec_xattn_kernel"
+        shape = f"B={B} H={H} hd={hd} T_mem={T_mem} t={t}"
+    else:
+        M, K = B, d
+        N = 3 * d if case == "proj" else c.d_ffn
+        A = (torch.randn(M, K, device="cuda", generator=g)).to(torch.bfloat16)
+        Wm = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        W3 = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16) if case == "glu" else None
+        Cm = torch.empty(M, N, device="cuda")
+        ws = model.workspace(1, 1)
+
+        def launch():
+            rlt.rlt_linear(model.handle, A, K, M, K, Wm, W3, K, N, Cm, N, ws, ws.numel(), stream)
+        nbytes = (2 if W3 is not None else 1) * N * K * 2 + M * K * 2 + M * N * 4
+        kernel = "gemm_tc_kernel"
+        shape = f"M={M} K={K} N={N}" + (" (W_1, W_3 pair)" if W3 is not None else "")
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    if rlt.rlt_status(ws, stream) != 0:
+        raise RuntimeError("device status flag set")
+    t_avg = float(np.mean(ts))
+    print(json.dumps({"case": case, "workload": wl.name, "kernel": kernel, "shape": shape,
+                      "bytes_per_launch": nbytes, "us_per_launch": round(1e6 * t_avg, 2),
+                      "achieved_gbs": round(nbytes / t_avg / 1e9, 1), "peak_gbs": round(bw / 1e9, 1),
+                      "frac": round(nbytes / t_avg / bw, 4), "peak_source": src, "l2": "flushed before each launch"}),
+          flush=True)
+    model.close()
+
+
+# ---------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser()
@@ -314,7 +398,12 @@ def main():
     ap.add_argument("--workload", default="small", choices=sorted(ri.PRESETS))
     ap.add_argument("--kernel-class", default="xattn", choices=["xattn", ""])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default="", choices=["", "xattn", "swa", "proj", "glu"],
+                    help="time one kernel of the workload (profiler captures) instead of the bench step")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

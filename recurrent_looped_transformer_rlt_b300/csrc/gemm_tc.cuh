@@ -37,14 +37,21 @@ constexpr int BK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int UK = 16;   // K of one tcgen05.mma kind::f16
 constexpr int THREADS = 192;
 
-template <int BN, int STAGES>
+// BMA: rows of A copied per k-block (128, or 64 when M <= 64).  The MMA
+// always reads 128 rows; with BMA = 64 rows 64..127 of its A operand fall on
+// the B tile of the same stage, and the accumulator rows they produce are
+// never read.
+template <int BN, int STAGES, int BMA = BM>
 struct Cfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN");
-  static constexpr int A_BYTES = BM * BK * 2;
+  static_assert(BMA == BM || (BMA == 64 && BN >= 64), "A rows 64..127 must stay inside the stage");
+  static constexpr int A_BYTES = BMA * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = BN;  // fp32 accumulator: one column per output column
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+  // the epilogue stages up to BMA rows of fp32 results in the ring
+  static_assert((size_t)STAGES * STAGE_BYTES >= (size_t)BMA * (BN + 4) * 4, "staging tile");
 };
 
 // ---------------------------------------------------------------------------
@@ -309,13 +316,12 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
 // rows of W_3 in its second half, so that the epilogue sees gate and linear
 // values of one output column in the same thread and writes
 // silu(gate) * linear.
-template <int BN, int STAGES, bool GLU, class Epi>
+template <int BN, int STAGES, bool GLU, class Epi, int BMA = BM>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3, int M, int N,
                    int K, AOperand ao, SplitK sk, Epi epi, int* status) {
-  using C = Cfg<BN, STAGES>;
-  constexpr int NOUT = GLU ? BN / 2 : BN;  // output columns per tile
+  using C = Cfg<BN, STAGES, BMA>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -323,7 +329,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* accum = empty + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
-  __shared__ int s_last;
   __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -432,7 +437,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     //    i.e. TMEM lane); the stage ring is free once every MMA has completed.
     const int q = warp & 3;
     const int rl = q * 32 + lane;
-    const int et = threadIdx.x - 64;
     const bool ok = mbar_wait(accum, 0, kWaitBudget) && (nkb > 0);
     if (!ok) atomicExch(&s_fail, 1);
     tc_fence_after();
@@ -496,7 +500,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---- epilogue functor on rows [r0, r1); consecutive threads take
     //      consecutive columns
     const int et = threadIdx.x - 64;
-    constexpr int LDT = BN + 4;
     const float* stile = reinterpret_cast<const float*>(smem);
     epi_bar();
     if (!s_fail) epilogue_tile<BN, GLU>(stile, r0, r1, m0, nb0, N, epi, et);

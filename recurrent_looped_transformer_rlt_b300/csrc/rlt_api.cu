@@ -78,6 +78,9 @@ struct rlt_model {
   size_t esz;  // bytes per stored element
   int n_sm;    // SMs of the device the model was created on
   KernelTimer* timer;
+  // co-resident clusters of the deep projection kernels, [config][cluster
+  // size] (size 1: CTAs), measured on the device at creation
+  int gemm_maxc[4][9];
 };
 
 // ---------------------------------------------------------------------------
@@ -218,6 +221,7 @@ int tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t T, u
 struct TcScratch {
   int n_sm;
   int* status;
+  const int (*maxc)[9];  // rlt_model::gemm_maxc
 };
 
 // The A operand of a projection: A [M][lda] for k < split (all of K when
@@ -233,27 +237,31 @@ struct AArg {
   const StepCtx* ctx = nullptr;
 };
 
-template <int BN, int STAGES, bool GLU, class Epi>
+template <int BN, int STAGES, bool GLU, class Epi, int BMA = tc::BM>
 int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, const bf16* B3, int ldb, int N,
-                   Epi epi, const TcScratch& sc) {
-  using C = tc::Cfg<BN, STAGES>;
+                   Epi epi, const TcScratch& sc, int split_req = 0) {
+  using C = tc::Cfg<BN, STAGES, BMA>;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, STAGES, GLU, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
       return RLT_ECUDA;
     attr = true;
   }
+  if (M > BMA && BMA != tc::BM) return RLT_EINVAL;
   const int nout = GLU ? BN / 2 : BN;
   const int tiles_n = (N + nout - 1) / nout, tiles_m = (M + tc::BM - 1) / tc::BM;
   const int kb = (K + tc::BK - 1) / tc::BK;
-  // split K over a cluster of CTAs per tile when there are few tiles.  Sizes
-  // from measurements of the weight-streaming shapes on B300: clusters of 8
-  // fit on 120 of the 148 SMs only (15 at a time), clusters of 2 on all;
-  // about 100 CTAs already saturate HBM with 3-stage rings.
+  // split K over a cluster of CTAs per tile when there are few tiles (the
+  // caller's split when given).  Sizes from measurements of the
+  // weight-streaming shapes on B300: clusters of 8 fit on 120 of the 148 SMs
+  // only (15 at a time), clusters of 2 on all; about 100 CTAs already
+  // saturate HBM with 3-stage rings.
   const int tiles = tiles_n * tiles_m;
   int splits = 1;
-  if (tiles < 12)
+  if (split_req > 0)
+    splits = split_req;
+  else if (tiles < 12)
     splits = 8;
   else if (tiles < 32)
     splits = 6;
@@ -267,11 +275,11 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   int rc;
   const int k1 = a.A2 ? a.split : K;
   if (a.T3 > 0) {
-    if ((rc = tmap_bf16_3d(&ta, a.A, M, a.T3, a.lda, tc::BM))) return rc;
-  } else if ((rc = tmap_bf16(&ta, a.A, M, k1, a.lda, tc::BM))) {
+    if ((rc = tmap_bf16_3d(&ta, a.A, M, a.T3, a.lda, BMA))) return rc;
+  } else if ((rc = tmap_bf16(&ta, a.A, M, k1, a.lda, BMA))) {
     return rc;
   }
-  if ((rc = tmap_bf16(&ta2, a.A2 ? a.A2 : a.A, M, a.A2 ? K - a.split : k1, a.A2 ? a.lda2 : a.lda, tc::BM))) return rc;
+  if ((rc = tmap_bf16(&ta2, a.A2 ? a.A2 : a.A, M, a.A2 ? K - a.split : k1, a.A2 ? a.lda2 : a.lda, BMA))) return rc;
   if ((rc = tmap_bf16(&tb, B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
   if ((rc = tmap_bf16(&tb3, GLU ? B3 : B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
   tc::AOperand ao{a.A2 ? a.split / tc::BK : kb, a.T3 > 0 ? 1 : 0, a.ctx};
@@ -290,8 +298,8 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   at[1].val.clusterDim.z = splits;
   cfg.attrs = at;
   cfg.numAttrs = splits > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi>, ta, ta2, tb, tb3, M, N, K, ao, sk, epi,
-                         sc.status) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA>, ta, ta2, tb, tb3, M, N, K, ao, sk,
+                         epi, sc.status) != cudaSuccess)
     return RLT_ECUDA;
   g_launches++;
   return launch_ok();
@@ -313,14 +321,102 @@ int gemm_bf16_tc(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf
   a.lda = lda;
   return gemm_bf16_tc(st, a, M, K, B, ldb, N, epi, sc);
 }
-// Projection of a batch of sequences (decoder step, rlt_linear): 3-stage
-// pipeline for up to 128 rows (two CTAs fit on an SM), 4 stages of 256-wide
-// tiles beyond.
+// Weight streaming at up to 128 rows (decoder step, rlt_linear): one CTA per
+// SM whose shared memory is one deep ring of k-blocks, so that each SM keeps
+// 100-160 KB of weights in flight.  Configurations (BN, rows of A per copy):
+//   0: (128, 64)  8 stages   1: (256, 64)  5 stages
+//   2: (128, 128) 6 stages   3: (256, 128) 4 stages
+template <int BN, int BMA>
+constexpr int deep_stages() {
+  return std::min(8, (200 * 1024) / ((BMA + BN) * tc::BK * 2));
+}
+struct DeepPlan {
+  int cfg, splits;
+};
+// The tile width and K split with the most CTAs that are all resident at
+// once (one wave), fewer splits on ties; the widest tiles without a split
+// when no choice fits in one wave.
+DeepPlan deep_plan(const TcScratch& sc, int M, int N, int K, bool glu) {
+  const int base = (M <= 64) ? 0 : 2;
+  const int kb = (K + tc::BK - 1) / tc::BK;
+  DeepPlan best{base + 1, 1};
+  int best_ctas = 0, best_s = 0;
+  for (int j = 0; j < 2; ++j) {
+    const int bn = j ? 256 : 128, nout = glu ? bn / 2 : bn;
+    const long long tiles = (N + nout - 1) / nout;
+    for (int s = 1; s <= std::min(8, kb); ++s) {
+      const int kbps = (kb + s - 1) / s;
+      if ((kb + kbps - 1) / kbps != s) continue;  // every split non-empty
+      const long long ctas = tiles * s;
+      const long long cap = (long long)sc.maxc[base + j][s] * s;
+      if (ctas > cap) continue;
+      if (ctas > best_ctas || (ctas == best_ctas && s < best_s)) {
+        best = {base + j, s};
+        best_ctas = (int)ctas;
+        best_s = s;
+      }
+    }
+  }
+  return best;
+}
+template <bool GLU, class Epi>
+int proj_deep(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const bf16* W3, int ldw, int N, Epi epi,
+              const TcScratch& sc) {
+  const DeepPlan p = deep_plan(sc, M, N, K, GLU);
+  switch (p.cfg) {
+    case 0:
+      return gemm_tc_launch<128, deep_stages<128, 64>(), GLU, Epi, 64>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
+    case 1:
+      return gemm_tc_launch<256, deep_stages<256, 64>(), GLU, Epi, 64>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
+    case 2:
+      return gemm_tc_launch<128, deep_stages<128, 128>(), GLU, Epi>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
+    default:
+      return gemm_tc_launch<256, deep_stages<256, 128>(), GLU, Epi>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
+  }
+}
+// Co-resident clusters of each deep configuration for cluster sizes 1..8.
+template <int BN, int BMA>
+int deep_occupancy(int n_sm, int* maxc) {
+  using C = tc::Cfg<BN, deep_stages<BN, BMA>(), BMA>;
+  auto kern = tc::gemm_tc_kernel<BN, deep_stages<BN, BMA>(), false, EpiStoreF32, BMA>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
+    return RLT_ECUDA;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, tc::THREADS, C::SMEM) != cudaSuccess) return RLT_ECUDA;
+  maxc[0] = 0;
+  maxc[1] = nb * n_sm;
+  for (int s = 2; s <= 8; ++s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, s);
+    cfg.blockDim = dim3(tc::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) return RLT_ECUDA;
+    maxc[s] = nc;
+  }
+  return RLT_OK;
+}
+int deep_occupancy_all(rlt_model* m) {
+  int rc;
+  if ((rc = deep_occupancy<128, 64>(m->n_sm, m->gemm_maxc[0]))) return rc;
+  if ((rc = deep_occupancy<256, 64>(m->n_sm, m->gemm_maxc[1]))) return rc;
+  if ((rc = deep_occupancy<128, 128>(m->n_sm, m->gemm_maxc[2]))) return rc;
+  return deep_occupancy<256, 128>(m->n_sm, m->gemm_maxc[3]);
+}
+// Projection of a batch of sequences (decoder step, rlt_linear): the deep
+// weight-streaming kernels up to 128 rows, 4 stages of 256-wide tiles beyond.
 template <bool GLU, class Epi>
 int proj_bf16(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const bf16* W3, int ldw, int N, Epi epi,
               const TcScratch& sc) {
   if (M <= 0 || N <= 0) return RLT_OK;
-  if (M <= tc::BM) return gemm_tc_launch<128, 3, GLU>(st, x, M, K, W, W3, ldw, N, epi, sc);
+  if (M <= tc::BM) return proj_deep<GLU>(st, x, M, K, W, W3, ldw, N, epi, sc);
   return gemm_tc_launch<256, 4, GLU>(st, x, M, K, W, W3, ldw, N, epi, sc);
 }
 
@@ -339,6 +435,7 @@ int gemm_bf16_tc_glu(cudaStream_t st, const bf16* A, int lda, int M, int K, cons
 TcScratch tc_scratch(const rlt_model* m, void* ws, const WsLayout& Lw) {
   TcScratch sc;
   sc.n_sm = m->n_sm;
+  sc.maxc = m->gemm_maxc;
   sc.status = at<int>(ws, Lw.status);
   return sc;
 }
@@ -1114,6 +1211,11 @@ int rlt_model_create(const rlt_config* cfg, const rlt_weights* w, uint64_t versi
     return RLT_ECUDA;
   }
   ensure_attrs();
+  if (cfg->dtype == RLT_BF16 && deep_occupancy_all(m) != RLT_OK) {
+    cudaStreamDestroy(m->cap_stream);
+    delete m;
+    return RLT_ECUDA;
+  }
   *out = m;
   return RLT_OK;
 }
