@@ -38,6 +38,8 @@ constexpr int kXWarps = 4;           // warps per CTA (each independent)
 constexpr int kXThreads = 32 * kXWarps;
 constexpr int kXChunkBytes = 4096;   // bytes of K (and of V) per chunk
 constexpr int kXMaxSplits = 32;      // splits per pair at most (partials buffer)
+constexpr int kXBlocksPerSM = 3;     // resident CTAs per SM the kernel is built for
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <typename T_, int HD>
 struct XShape {
@@ -129,7 +131,7 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 }
 
 template <typename T_, int HD>
-__global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
+__global__ void __launch_bounds__(kXThreads, kXBlocksPerSM) dec_xattn_kernel(XattnArgs a) {
   using S = XShape<T_, HD>;
   constexpr int CH = S::CH, EPL = S::EPL, LPR = S::LPR, RPW = S::RPW, PASSES = S::PASSES;
   constexpr int CHE = CH * HD;  // elements per chunk buffer
@@ -139,6 +141,16 @@ __global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
   uint64_t* bar = reinterpret_cast<uint64_t*>(xsm + (size_t)kXWarps * 4 * kXChunkBytes) + warp * 4;  // K0 K1 V0 V1
 
   const int sub = lane % LPR, rg = lane / LPR;
+  // transposed reduction of the PASSES partial dots over the LPR lanes of a
+  // row group: LV halving steps (offsets LPR/2, LPR/4, ...) leave NV values per
+  // lane, shared by REP lanes when LPR > PASSES
+  constexpr int RL = LPR < PASSES ? LPR : PASSES;
+  constexpr int NV = PASSES / RL, REP = LPR / RL;
+  constexpr int LV = RL >= 8 ? 3 : RL >= 4 ? 2 : RL >= 2 ? 1 : 0;
+  int idx = 0;  // this lane's block of passes: idx * NV .. idx * NV + NV - 1
+#pragma unroll
+  for (int lv = 0; lv < LV; ++lv) idx = (idx << 1) | ((lane & (LPR >> (lv + 1))) ? 1 : 0);
+  const bool rep0 = (lane & (REP - 1)) == 0;
   const int t = min(a.t_cap, a.ctx->pos + 1);
   const int nch = (t + CH - 1) / CH;
   const int pairs = a.B * a.H;
@@ -205,7 +217,7 @@ __global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
     {
       const float* qp = a.q + (size_t)b * d + h * HD + sub * EPL;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) qr[e] = qp[e] * a.scale;
+      for (int e = 0; e < EPL; ++e) qr[e] = qp[e] * (a.scale * kLog2e);  // scores in log2 units
     }
     float m = -INFINITY, l = 0.f;
 #pragma unroll
@@ -216,49 +228,72 @@ __global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
       const int st = used & 1;
       const unsigned par = (phase >> st) & 1u;
       if (!mbar_wait(&bar[st], par, kWaitBudget)) goto fail;
-      // ---- scores: pass p covers rows p*RPW + rg
-      float sc[PASSES];
+      // ---- scores: pass p covers rows p*RPW + rg; partial dots of the lane's
+      //      EPL dimensions, then a transposed reduction over the row group
+      //      (LV halving steps leave NV full dots per lane: passes idx*NV + j)
       const T_* Ks = sbuf + (st * 2) * CHE;
-      float cmax = -INFINITY;
+      float v[PASSES];
 #pragma unroll
       for (int p = 0; p < PASSES; ++p) {
-        const int r = p * RPW + rg;
+        float kv[EPL];
+        load_seg<T_, EPL>(Ks + (p * RPW + rg) * HD + sub * EPL, kv);  // rows past nj: stale, masked below
         float dot = 0.f;
-        if (r < nj) {
-          float kv[EPL];
-          load_seg<T_, EPL>(Ks + r * HD + sub * EPL, kv);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) dot = fmaf(qr[e], kv[e], dot);
-        }
-#pragma unroll
-        for (int o = LPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        sc[p] = (r < nj) ? dot : -INFINITY;
-        cmax = fmaxf(cmax, sc[p]);
+        for (int e = 0; e < EPL; ++e) dot = fmaf(qr[e], kv[e], dot);
+        v[p] = dot;
       }
+#pragma unroll
+      for (int lv = 0; lv < LV; ++lv) {
+        const int o = LPR >> (lv + 1), hn = PASSES >> (lv + 1);
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < hn; ++i) {
+          const float send = up ? v[i] : v[i + hn];
+          const float keep = up ? v[i + hn] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+#pragma unroll
+      for (int o = REP >> 1; o > 0; o >>= 1)  // lanes that share a value (LPR > PASSES)
+#pragma unroll
+        for (int j = 0; j < NV; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], o);
+      float cmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        if ((idx * NV + j) * RPW + rg >= nj) v[j] = -INFINITY;
+        cmax = fmaxf(cmax, v[j]);
+      }
+#pragma unroll
+      for (int lv = 0; lv < LV; ++lv) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, LPR >> (lv + 1)));
 #pragma unroll
       for (int o = LPR; o < 32; o <<= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
       const float mn = fmaxf(m, cmax);
-      const float corr = expf(m - mn);  // 0 on the first chunk (m = -inf)
+      const float corr = exp2f(m - mn);  // 0 on the first chunk (m = -inf)
       m = mn;
       float ls = 0.f;
 #pragma unroll
-      for (int p = 0; p < PASSES; ++p) {
-        sc[p] = expf(sc[p] - mn);  // rows past nj: exp(-inf) = 0
-        ls += sc[p];
+      for (int j = 0; j < NV; ++j) {
+        v[j] = exp2f(v[j] - mn);  // masked rows: exp2(-inf) = 0
+        ls += v[j];
       }
-      l = l * corr + ls;  // this lane's row group's share
+      l = l * corr + (rep0 ? ls : 0.f);  // each row counted by one lane
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] *= corr;
       if (!mbar_wait(&bar[2 + st], par, kWaitBudget)) goto fail;
       const T_* Vs = sbuf + (st * 2 + 1) * CHE;
 #pragma unroll
       for (int p = 0; p < PASSES; ++p) {
+        // P of pass p from the lane that holds it (same row group)
+        int g = 0;
+#pragma unroll
+        for (int lv = 0; lv < LV; ++lv) g += (((p / NV) >> (LV - 1 - lv)) & 1) * (LPR >> (lv + 1));
+        const float w = __shfl_sync(0xffffffffu, v[p % NV], rg * LPR + g);
         const int r = p * RPW + rg;
         if (r < nj) {
           float vv[EPL];
           load_seg<T_, EPL>(Vs + r * HD + sub * EPL, vv);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(sc[p], vv[e], acc[e]);
+          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, vv[e], acc[e]);
         }
       }
       __syncwarp();  // every lane is done with stage st
@@ -269,8 +304,9 @@ __global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
     // ---- end of the task: sum over the row groups and emit
     float lt = l;
 #pragma unroll
+    for (int o = 1; o < 32; o <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+#pragma unroll
     for (int o = LPR; o < 32; o <<= 1) {
-      lt += __shfl_xor_sync(0xffffffffu, lt, o);
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
     }
@@ -302,12 +338,12 @@ __global__ void __launch_bounds__(kXThreads) dec_xattn_kernel(XattnArgs a) {
         for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(pp + (size_t)s2 * (HD + 2)));
         float L = 0.f;
         for (int s2 = 0; s2 < ns; ++s2)
-          L += __ldcg(pp + (size_t)s2 * (HD + 2) + 1) * expf(__ldcg(pp + (size_t)s2 * (HD + 2)) - M);
+          L += __ldcg(pp + (size_t)s2 * (HD + 2) + 1) * exp2f(__ldcg(pp + (size_t)s2 * (HD + 2)) - M);
         const float inv = 1.f / L;
         for (int i = lane; i < HD; i += 32) {
           float o = 0.f;
           for (int s2 = 0; s2 < ns; ++s2)
-            o += __ldcg(pp + (size_t)s2 * (HD + 2) + 2 + i) * expf(__ldcg(pp + (size_t)s2 * (HD + 2)) - M);
+            o += __ldcg(pp + (size_t)s2 * (HD + 2) + 2 + i) * exp2f(__ldcg(pp + (size_t)s2 * (HD + 2)) - M);
           out[(size_t)b * d + h * HD + i] = from_f32<T_>(o * inv);
         }
         __syncwarp();
