@@ -179,8 +179,6 @@ def run_gpu(args, rank, world, local_rank):
     # timed region: K steps, inputs resident in HBM, L2 flushed before each step
     times, enc_times = [], []
     launches0 = rlt.rlt_launch_count()
-    n_timed = min(args.steps * T * c.n_layers, 1 << 18)  # one launch per layer and step
-    timer_on = model.timer_arm(args.kernel_class, n_timed) if args.kernel_class else False
     with ClockSampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize()
@@ -195,9 +193,20 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
         barrier()
     launches = rlt.rlt_launch_count() - launches0
-    kernel_ms = model.timer_read() if timer_on else []
     if rlt.rlt_status(buf.ws, stream) != 0:
         raise RuntimeError("device status flag set in the timed region")
+    # per-launch durations of the roofline kernel: one more step with CUDA
+    # events around each launch of that kernel class, outside the timed steps
+    # (an event between two kernels of the step graph suspends their
+    # programmatic overlap, so the instrumented step runs slower than the
+    # timed ones)
+    kernel_ms = []
+    if args.kernel_class:
+        model.timer_arm(args.kernel_class, min(T * c.n_layers, 1 << 18))  # one launch per layer and step
+        flush.fill_(1.0)
+        step(tok_d, acts_d)
+        torch.cuda.synchronize()
+        kernel_ms = model.timer_read()  # reading disarms the timer
     lp = out.logp.cpu().numpy()
     assert np.isfinite(lp[acts >= 0]).sum() > 0
 

@@ -59,23 +59,36 @@ struct EpiQKVRope {
   const float2* tab;  // [position][hd/2] (cos, sin)
   const StepCtx* ctx;
   int d, H, hd, W;
-  __device__ __forceinline__ void pair(int b, int n, float x1, float x2) const {
-    const int which = n / d, r = n - which * d;
-    const int head = r / hd, i = r - head * hd, half = hd >> 1;
+  // what a pair of columns (n, n + hd/2) needs, the same for every row
+  struct PairCtx {
+    int which, head, i, slot;
+    float2 cs;
+  };
+  __device__ __forceinline__ PairCtx pair_ctx(int n) const {
+    PairCtx c;
+    c.which = n / d;
+    const int r = n - c.which * d;
+    c.head = r / hd;
+    c.i = r - c.head * hd;
     const int p = ctx->pos;
-    if (which == 2) {
-      const size_t o = (((size_t)b * H + head) * W + p % W) * hd + i;
+    c.slot = p % W;
+    c.cs = (c.which == 2) ? make_float2(1.f, 0.f) : tab[(size_t)p * (hd >> 1) + c.i];
+    return c;
+  }
+  __device__ __forceinline__ void pair(const PairCtx& c, int b, int, float x1, float x2) const {
+    const int half = hd >> 1;
+    if (c.which == 2) {
+      const size_t o = (((size_t)b * H + c.head) * W + c.slot) * hd + c.i;
       ring_v[o] = from_f32<T>(x1);
       ring_v[o + half] = from_f32<T>(x2);
       return;
     }
-    const float2 cs = tab[(size_t)p * half + i];
-    const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
-    if (which == 0) {
-      q[(size_t)b * d + head * hd + i] = y1;
-      q[(size_t)b * d + head * hd + i + half] = y2;
+    const float y1 = x1 * c.cs.x - x2 * c.cs.y, y2 = x2 * c.cs.x + x1 * c.cs.y;
+    if (c.which == 0) {
+      q[(size_t)b * d + c.head * hd + c.i] = y1;
+      q[(size_t)b * d + c.head * hd + c.i + half] = y2;
     } else {
-      const size_t o = (((size_t)b * H + head) * W + p % W) * hd + i;
+      const size_t o = (((size_t)b * H + c.head) * W + c.slot) * hd + c.i;
       ring_k[o] = from_f32<T>(y1);
       ring_k[o + half] = from_f32<T>(y2);
     }
@@ -93,18 +106,28 @@ struct EpiEncQKVRope {
   T* v;
   const float2* tab;  // [position][hd/2]
   int d, H, hd, T_len;
-  __device__ __forceinline__ void pair(int m, int n, float x1, float x2) const {
-    const int which = n / d, r = n - which * d;
-    const int head = r / hd, i = r - head * hd, half = hd >> 1;
+  struct PairCtx {
+    int which, head, i;
+  };
+  __device__ __forceinline__ PairCtx pair_ctx(int n) const {
+    PairCtx c;
+    c.which = n / d;
+    const int r = n - c.which * d;
+    c.head = r / hd;
+    c.i = r - c.head * hd;
+    return c;
+  }
+  __device__ __forceinline__ void pair(const PairCtx& c, int m, int, float x1, float x2) const {
+    const int half = hd >> 1;
     const int b = m / T_len, t = m - b * T_len;
-    const size_t o = (((size_t)b * H + head) * T_len + t) * hd + i;
-    if (which == 2) {
+    const size_t o = (((size_t)b * H + c.head) * T_len + t) * hd + c.i;
+    if (c.which == 2) {
       v[o] = from_f32<T>(x1);
       v[o + half] = from_f32<T>(x2);
       return;
     }
-    const float2 cs = tab[(size_t)t * half + i];
-    T* dst = (which == 0) ? q : k;
+    const float2 cs = tab[(size_t)t * half + c.i];
+    T* dst = (c.which == 0) ? q : k;
     dst[o] = from_f32<T>(x1 * cs.x - x2 * cs.y);
     dst[o + half] = from_f32<T>(x2 * cs.x + x1 * cs.y);
   }

@@ -127,8 +127,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// The same load without waiting for it: several may be in flight, then one
+// tmem_wait_ld before their registers are read.
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
-
 // ---------------------------------------------------------------------------
 
 // Epilogues that consume column pairs (i, i + hd/2) of each head block of hd
@@ -219,13 +228,26 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
   } else if constexpr (IsPairEpi<Epi>::value) {
     const int half = epi.hd >> 1;
     constexpr int HB = BN / 2;  // pairs per tile row
-    const int n = (r1 - r0) * HB;
-#pragma unroll 4
-    for (int i = et; i < n; i += 128) {
-      const int r = r0 + i / HB, pi = i % HB;
-      const int hb = pi / half, ii = pi - hb * half;
+    if constexpr (128 % HB == 0) {
+      // a thread keeps one pair of columns for all its rows: its per-column
+      // context (position, rotation) is read once
+      const int pi = et % HB, hb = pi / half, ii = pi - hb * half;
       const int c = hb * 2 * half + ii;
-      if (nb0 + c < N) epi.pair(m0 + r, nb0 + c, stile[r * LDT + c], stile[r * LDT + c + half]);
+      if (nb0 + c < N) {
+        const auto pc = epi.pair_ctx(nb0 + c);
+#pragma unroll 4
+        for (int r = r0 + et / HB; r < r1; r += 128 / HB)
+          epi.pair(pc, m0 + r, nb0 + c, stile[r * LDT + c], stile[r * LDT + c + half]);
+      }
+    } else {
+      const int n = (r1 - r0) * HB;
+#pragma unroll 4
+      for (int i = et; i < n; i += 128) {
+        const int r = r0 + i / HB, pi = i % HB;
+        const int hb = pi / half, ii = pi - hb * half;
+        const int c = hb * 2 * half + ii;
+        if (nb0 + c < N) epi.pair(epi.pair_ctx(nb0 + c), m0 + r, nb0 + c, stile[r * LDT + c], stile[r * LDT + c + half]);
+      }
     }
   } else if constexpr (IsHOutEpi<Epi>::value) {
     // the residual stream: N a multiple of BN and rows 16-byte aligned
@@ -329,6 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* accum = empty + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  constexpr int LDT = BN + 4;
   __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -440,17 +463,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool ok = mbar_wait(accum, 0, kWaitBudget) && (nkb > 0);
     if (!ok) atomicExch(&s_fail, 1);
     tc_fence_after();
-    constexpr int LDT = BN + 4;
     float* stile = reinterpret_cast<float*>(smem);
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
     if (q * 32 < M - m0) {  // warps whose 32 TMEM lanes hold at least one output row
+      constexpr int NL = BN >= 64 ? 4 : BN / 16;  // 16-column loads in flight per wait
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        tmem_ld16(tq + c0, v);
+      for (int c0 = 0; c0 < BN; c0 += 16 * NL) {
+        uint32_t v[NL][16];
 #pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          *reinterpret_cast<float4*>(stile + rl * LDT + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        for (int u = 0; u < NL; ++u) tmem_ld16_async(tq + c0 + 16 * u, v[u]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < NL; ++u)
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4*>(stile + rl * LDT + c0 + 16 * u + j) =
+                make_float4(__uint_as_float(v[u][j]), __uint_as_float(v[u][j + 1]), __uint_as_float(v[u][j + 2]),
+                            __uint_as_float(v[u][j + 3]));
       }
     }
     epi_bar();
@@ -464,34 +493,43 @@ __global__ void __launch_bounds__(THREADS, 1)
     r1 = (int)(((long long)rows * (z + 1)) / sk.splits);
     if (warp >= 2) {
       const int et = threadIdx.x - 64;
-      constexpr int LDT = BN + 4, V4 = BN / 4;
+      constexpr int V4 = BN / 4;
       float* stile = reinterpret_cast<float*>(smem);
       uint32_t rbase[8];  // the staged tile in every CTA of the cluster (splits <= 8)
 #pragma unroll
       for (int zz = 0; zz < 8; ++zz) rbase[zz] = zz < sk.splits ? mapa_u32(stile, (uint32_t)zz) : 0u;
       const int nv = (r1 - r0) * V4;
-      // all splits' values of an element are in flight before they are summed
-      // in split order; the sums go back to rows [r0, r1) of this CTA's own
-      // tile (each element read and written by one thread; the other CTAs of
-      // the cluster read only their own, disjoint row ranges)
-#pragma unroll 2
-      for (int i = et; i < nv; i += 128) {
-        const int r = r0 + i / V4, c4 = i % V4;
-        const uint32_t off = (uint32_t)((r * LDT + c4 * 4) * 4);
-        float4 f[8];
+      // the values of every split for E elements are in flight before they
+      // are summed in split order; the sums go back to rows [r0, r1) of this
+      // CTA's own tile (each element read and written by one thread; the other
+      // CTAs of the cluster read only their own, disjoint row ranges)
+      constexpr int E = 4;
+      for (int i0 = et; i0 < nv; i0 += 128 * E) {
+        float4 f[E][8];
 #pragma unroll
-        for (int zz = 0; zz < 8; ++zz)
-          if (zz < sk.splits) f[zz] = ld_cluster_f4(rbase[zz] + off);
-        float4 acc = f[0];
+        for (int u = 0; u < E; ++u) {
+          const int i = i0 + u * 128;
+          if (i >= nv) continue;
+          const uint32_t off = (uint32_t)(((r0 + i / V4) * LDT + (i % V4) * 4) * 4);
 #pragma unroll
-        for (int zz = 1; zz < 8; ++zz)
-          if (zz < sk.splits) {
-            acc.x += f[zz].x;
-            acc.y += f[zz].y;
-            acc.z += f[zz].z;
-            acc.w += f[zz].w;
-          }
-        *reinterpret_cast<float4*>(stile + r * LDT + c4 * 4) = acc;
+          for (int zz = 0; zz < 8; ++zz)
+            if (zz < sk.splits) f[u][zz] = ld_cluster_f4(rbase[zz] + off);
+        }
+#pragma unroll
+        for (int u = 0; u < E; ++u) {
+          const int i = i0 + u * 128;
+          if (i >= nv) continue;
+          float4 acc = f[u][0];
+#pragma unroll
+          for (int zz = 1; zz < 8; ++zz)
+            if (zz < sk.splits) {
+              acc.x += f[u][zz].x;
+              acc.y += f[u][zz].y;
+              acc.z += f[u][zz].z;
+              acc.w += f[u][zz].w;
+            }
+          *reinterpret_cast<float4*>(stile + (r0 + i / V4) * LDT + (i % V4) * 4) = acc;
+        }
       }
     }
     cluster_arrive();  // this CTA is done reading its peers' tiles

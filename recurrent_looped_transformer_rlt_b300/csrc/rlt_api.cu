@@ -335,7 +335,10 @@ struct DeepPlan {
 };
 // The tile width and K split with the most CTAs that are all resident at
 // once (one wave), fewer splits on ties; the widest tiles without a split
-// when no choice fits in one wave.
+// when no choice fits in one wave.  More CTAs stream more weight bytes at
+// once and share the epilogue; a split's partial sums cost a cluster barrier
+// and a pull through distributed shared memory (~2-3 us, measured), which
+// fewer, longer CTAs lose more than that to streaming and epilogue time.
 DeepPlan deep_plan(const TcScratch& sc, int M, int N, int K, bool glu) {
   const int base = (M <= 64) ? 0 : 2;
   const int kb = (K + tc::BK - 1) / tc::BK;
@@ -344,12 +347,13 @@ DeepPlan deep_plan(const TcScratch& sc, int M, int N, int K, bool glu) {
   for (int j = 0; j < 2; ++j) {
     const int bn = j ? 256 : 128, nout = glu ? bn / 2 : bn;
     const long long tiles = (N + nout - 1) / nout;
-    for (int s = 1; s <= std::min(8, kb); ++s) {
+    // (256, 128) tiles have no split (their partial tiles are the largest)
+    const int smax = (base + j == 3) ? 1 : std::min(8, kb);
+    for (int s = 1; s <= smax; ++s) {
       const int kbps = (kb + s - 1) / s;
       if ((kb + kbps - 1) / kbps != s) continue;  // every split non-empty
       const long long ctas = tiles * s;
-      const long long cap = (long long)sc.maxc[base + j][s] * s;
-      if (ctas > cap) continue;
+      if (ctas > (long long)sc.maxc[base + j][s] * s) continue;
       if (ctas > best_ctas || (ctas == best_ctas && s < best_s)) {
         best = {base + j, s};
         best_ctas = (int)ctas;

@@ -16,12 +16,16 @@
 //    chunk is CH consecutive positions = 4 KB of K and 4 KB of V, each fetched
 //    by one bulk asynchronous copy (TMA engine) into shared memory;
 //  - work is split per warp, not per block: a task is (pair, split) = a run of
-//    chunks of one pair; every warp owns a two-stage ring of chunk buffers and
+//    chunks of one pair; every warp owns a ring of ST chunk buffers (2 or 3) and
 //    their mbarriers, walks its tasks chunk by chunk with the next chunk always
 //    in flight (across task boundaries too), and keeps an online softmax
 //    (running max, sum, output) in registers: no block-wide barrier;
 //  - within a chunk hd*es/16 lanes share a key row (16-byte shared loads), so a
-//    chunk is 8 passes of the warp over its rows;
+//    chunk is 8 passes of the warp over its rows; the 8 partial dot products
+//    of a lane are summed over the row's lanes by a transposed butterfly (each
+//    halving step exchanges half of the remaining values), which leaves every
+//    lane the full scores of its own passes: one exp2 per score, and each
+//    probability fetched by the lanes that need it for the value pass;
 //  - the number of splits per pair is picked on the device from t (a cost
 //    model of task rounds over all warps of the grid plus a per-task cost);
 //    the splits of a pair are merged by the warp that arrives last on the
@@ -38,10 +42,12 @@ constexpr int kXWarps = 4;           // warps per CTA (each independent)
 constexpr int kXThreads = 32 * kXWarps;
 constexpr int kXChunkBytes = 4096;   // bytes of K (and of V) per chunk
 constexpr int kXMaxSplits = 32;      // splits per pair at most (partials buffer)
-constexpr int kXBlocksPerSM = 3;     // resident CTAs per SM the kernel is built for
+// resident CTAs per SM the kernel is built for, by ring depth (shared
+// memory: 4 warps x ST stages x 8 KB)
+__host__ __device__ constexpr int xattn_blocks_per_sm(int st) { return st <= 2 ? 3 : 2; }
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <typename T_, int HD>
+template <typename T_, int HD, int ST = 2>
 struct XShape {
   static constexpr int ES = (int)sizeof(T_);
   static constexpr int EPL = 16 / ES;           // elements per lane (one 16-byte load)
@@ -51,8 +57,8 @@ struct XShape {
   static constexpr int PASSES = CH / RPW;       // = 8
   static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "unsupported head_dim");
   static_assert(CH % RPW == 0, "chunk must be a whole number of passes");
-  // per warp: 2 stages x (K, V) chunk buffers, then 4 mbarriers per warp
-  static constexpr size_t smem_bytes() { return (size_t)kXWarps * 4 * kXChunkBytes + 32 * kXWarps; }
+  // per warp: ST stages x (K, V) chunk buffers; then 2 ST mbarriers per warp
+  static constexpr size_t smem_bytes() { return (size_t)kXWarps * 2 * ST * kXChunkBytes + 16 * ST * kXWarps; }
 };
 
 struct XattnArgs {
@@ -130,15 +136,16 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
   return old;
 }
 
-template <typename T_, int HD>
-__global__ void __launch_bounds__(kXThreads, kXBlocksPerSM) dec_xattn_kernel(XattnArgs a) {
-  using S = XShape<T_, HD>;
+template <typename T_, int HD, int ST>
+__global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_kernel(XattnArgs a) {
+  using S = XShape<T_, HD, ST>;
   constexpr int CH = S::CH, EPL = S::EPL, LPR = S::LPR, RPW = S::RPW, PASSES = S::PASSES;
   constexpr int CHE = CH * HD;  // elements per chunk buffer
   extern __shared__ __align__(128) unsigned char xsm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  T_* sbuf = reinterpret_cast<T_*>(xsm + (size_t)warp * 4 * kXChunkBytes);  // [stage][K|V][CHE]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(xsm + (size_t)kXWarps * 4 * kXChunkBytes) + warp * 4;  // K0 K1 V0 V1
+  T_* sbuf = reinterpret_cast<T_*>(xsm + (size_t)warp * 2 * ST * kXChunkBytes);  // [stage][K|V][CHE]
+  // K of stage s at bar[s], V at bar[ST + s]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(xsm + (size_t)kXWarps * 2 * ST * kXChunkBytes) + warp * 2 * ST;
 
   const int sub = lane % LPR, rg = lane / LPR;
   // transposed reduction of the PASSES partial dots over the LPR lanes of a
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(kXThreads, kXBlocksPerSM) dec_xattn_kernel(Xat
   T_* out = static_cast<T_*>(a.out);
 
   if (lane == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 2 * ST; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -187,27 +194,23 @@ __global__ void __launch_bounds__(kXThreads, kXBlocksPerSM) dec_xattn_kernel(Xat
     const size_t off = ((size_t)pair * a.T_mem + c0) * HD;
     mbar_arrive_expect_tx(&bar[stage], bytes);
     bulk_g2s(sbuf + (stage * 2) * CHE, mk + off, bytes, &bar[stage]);
-    mbar_arrive_expect_tx(&bar[2 + stage], bytes);
-    bulk_g2s(sbuf + (stage * 2 + 1) * CHE, mv + off, bytes, &bar[2 + stage]);
+    mbar_arrive_expect_tx(&bar[ST + stage], bytes);
+    bulk_g2s(sbuf + (stage * 2 + 1) * CHE, mv + off, bytes, &bar[ST + stage]);
     if (++ic >= n_chunks_of(task)) {
       ++ik;
       ic = 0;
     }
   };
-  if (a.early && lane == 0) {
-    issue_next(0);
-    issue_next(1);
-  }
+  if (a.early && lane == 0)
+    for (int s0 = 0; s0 < ST; ++s0) issue_next(s0);
   pdl_wait();  // q, the ring (window) and the outputs depend on the previous kernels
   if (threadIdx.x == 0) pdl_trigger();
-  if (!a.early && lane == 0) {
-    issue_next(0);
-    issue_next(1);
-  }
+  if (!a.early && lane == 0)
+    for (int s0 = 0; s0 < ST; ++s0) issue_next(s0);
   __syncwarp();
 
   unsigned phase = 0;  // bit s: parity of the next completion of stage s
-  int used = 0;        // chunks consumed (stage = used & 1)
+  int used = 0;        // chunks consumed (stage = used % ST)
   float acc[EPL], qr[EPL];
   for (int k = 0; k < my_tasks; ++k) {
     const int task = gw + k * warps;
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kXThreads, kXBlocksPerSM) dec_xattn_kernel(Xat
     for (int c = 0; c < nct; ++c, ++used) {
       const int c0 = (sp * cps + c) * CH;
       const int nj = min(CH, t - c0);
-      const int st = used & 1;
+      const int st = used % ST;
       const unsigned par = (phase >> st) & 1u;
       if (!mbar_wait(&bar[st], par, kWaitBudget)) goto fail;
       // ---- scores: pass p covers rows p*RPW + rg; partial dots of the lane's
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(kXThreads, kXBlocksPerSM) dec_xattn_kernel(Xat
       l = l * corr + (rep0 ? ls : 0.f);  // each row counted by one lane
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] *= corr;
-      if (!mbar_wait(&bar[2 + st], par, kWaitBudget)) goto fail;
+      if (!mbar_wait(&bar[ST + st], par, kWaitBudget)) goto fail;
       const T_* Vs = sbuf + (st * 2 + 1) * CHE;
 #pragma unroll
       for (int p = 0; p < PASSES; ++p) {
@@ -357,25 +360,25 @@ fail:
   // bounded time to land (they write its shared memory), then leave
   if (lane == 0) {
     set_error(a.status, kErrTimeout);
-    for (int s2 = 0; s2 < 2; ++s2) {
+    for (int s2 = 0; s2 < ST; ++s2) {
       const unsigned p2 = (phase >> s2) & 1u;
       mbar_wait(&bar[s2], p2, kWaitBudget);
-      mbar_wait(&bar[2 + s2], p2, kWaitBudget);
+      mbar_wait(&bar[ST + s2], p2, kWaitBudget);
     }
   }
   __syncwarp();
 }
 
 // Host-side launch: grid = resident CTAs on every SM (persistent).
-template <typename T_, int HD>
-inline cudaError_t launch_xattn_hd(const XattnArgs& a, int n_sm, cudaStream_t st) {
-  using S = XShape<T_, HD>;
+template <typename T_, int HD, int ST>
+inline cudaError_t launch_xattn_st(const XattnArgs& a, int n_sm, cudaStream_t st) {
+  using S = XShape<T_, HD, ST>;
   static int occ = 0;
   if (occ == 0) {
-    cudaFuncSetAttribute(dec_xattn_kernel<T_, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(dec_xattn_kernel<T_, HD, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)S::smem_bytes());
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, dec_xattn_kernel<T_, HD>, kXThreads, S::smem_bytes()) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, dec_xattn_kernel<T_, HD, ST>, kXThreads, S::smem_bytes()) !=
             cudaSuccess ||
         o < 1)
       o = 1;
@@ -391,7 +394,15 @@ inline cudaError_t launch_xattn_hd(const XattnArgs& a, int n_sm, cudaStream_t st
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, dec_xattn_kernel<T_, HD>, a);
+  return cudaLaunchKernelEx(&cfg, dec_xattn_kernel<T_, HD, ST>, a);
+}
+// Ring depth by shape (measured on B300): three stages (two CTAs, eight
+// warps per SM) stream long memories of heads up to 64 wide faster; two
+// stages (twelve warps per SM) win for 128-wide heads and short windows.
+template <typename T_, int HD>
+inline cudaError_t launch_xattn_hd(const XattnArgs& a, int n_sm, cudaStream_t st) {
+  if (HD <= 64 && a.t_cap >= 512) return launch_xattn_st<T_, HD, 3>(a, n_sm, st);
+  return launch_xattn_st<T_, HD, 2>(a, n_sm, st);
 }
 
 template <typename T_>
