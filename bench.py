@@ -244,6 +244,17 @@ def run_gpu(args, rank, world, local_rank):
     return res
 
 
+# DRAM traffic of the cross-attention kernel, from one ncu capture of the
+# current kernel build at the workload's shapes (bench.py --profile-case xattn;
+# summaries in profiles/): (dram__bytes_read.sum + dram__bytes_write.sum,
+# algorithmic bytes of that launch).  The bench reports traffic per launch as
+# its average algorithmic bytes times this ratio.
+XATTN_TRAFFIC = {
+    "small": (16906496 + 0, 16875520),            # t = 256, ring depth 3
+    "refdep": (1075314000 + 5567232, 1074528256),  # t = 2048, ring depth 2
+}
+
+
 def kernel_roofline(wl, kernel_ms, kernel_class, bw, peak, src):
     """Roofline object of the timed kernel class from its per-launch CUDA-event durations."""
     if not kernel_ms:
@@ -256,10 +267,14 @@ def kernel_roofline(wl, kernel_ms, kernel_class, bw, peak, src):
     else:
         return None
     ach = sum(byts) / (sum(kernel_ms) / 1e3)
+    traffic = None
+    if wl.name in XATTN_TRAFFIC:
+        dram, alg = XATTN_TRAFFIC[wl.name]
+        traffic = int(round(float(np.mean(byts)) * dram / alg))
     return {"bound": "hbm", "achieved": round(ach / 1e9, 1), "peak": round(bw / 1e9, 1), "unit": "GB/s",
-            "frac": round(ach / bw, 4), "traffic": None, "kernel": "dec_xattn (partial + combine)",
+            "frac": round(ach / bw, 4), "traffic": traffic, "kernel": "dec_xattn (partial + combine)",
             "launches": len(kernel_ms), "avg_us": round(1e3 * float(np.mean(kernel_ms)), 2),
-            "peak_source": src}
+            "peak_source": src, "durations": "CUDA events around every launch of one extra step after the timed steps"}
 
 
 # ---------------------------------------------------------------------------
