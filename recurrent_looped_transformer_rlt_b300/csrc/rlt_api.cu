@@ -982,7 +982,7 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
       sa.mv = rv + l * ring_layer;
       sa.T_mem = Wn;
       sa.t_cap = Wn;
-      sa.early = 0;  // the ring entry of this step is written by the QKV projection just before
+      sa.early = 2;  // the ring entry of this step is written by the QKV projection just before
       if (launch_xattn<bf16>(sa, hd, m->n_sm, st) != cudaSuccess) return RLT_ECUDA;
       if ((rc = post())) return rc;
     }

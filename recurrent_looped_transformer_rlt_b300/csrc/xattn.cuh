@@ -26,11 +26,14 @@
 //    halving step exchanges half of the remaining values), which leaves every
 //    lane the full scores of its own passes: one exp2 per score, and each
 //    probability fetched by the lanes that need it for the value pass;
-//  - the number of splits per pair is picked on the device from t (a cost
-//    model of task rounds over all warps of the grid plus a per-task cost);
-//    the splits of a pair are merged by the warp that arrives last on the
-//    pair's counter (acquire-release atomic), and a pair with a single split
-//    is written out directly.
+//  - the work is balanced exactly: the (pair, chunk) units are cut into one
+//    contiguous run per warp (on the device, from t), a run's piece inside one
+//    pair is a segment, the segments of a pair are merged by the warp that
+//    arrives last on the pair's counter (acquire-release atomic), and a pair
+//    covered by a single segment is written out directly;
+//  - copies that do not depend on the previous kernel start before waiting for
+//    it: all of the encoder memory, and every ring chunk except the one that
+//    holds this step's slot.
 #pragma once
 
 #include "common.cuh"
@@ -70,8 +73,10 @@ struct XattnArgs {
   void* out;          // [B][d]  storage dtype
   int B, H, T_mem;
   int t_cap;          // attend to positions 0 .. min(t_cap, ctx->pos + 1) - 1
-  int early;          // keys/values written two or more kernels earlier (encoder memory): the
-                      // first copies may start before waiting for the previous kernel
+  int early;          // which first copies may start before waiting for the previous kernel:
+                      // 0 none; 1 all (keys/values written two or more kernels earlier,
+                      // the encoder memory); 2 all but the chunk holding ring slot
+                      // pos mod t_cap (the window: that entry is this step's)
   float scale;
   const StepCtx* ctx;
   int* status;
@@ -99,34 +104,7 @@ __device__ __forceinline__ void load_seg<float, 4>(const float* p, float (&v)[4]
   v[3] = f.w;
 }
 
-// Splits per pair.  A warp keeps two chunks in flight, so the stream rate
-// grows with the number of busy warps: S is at least the smallest count that
-// gives every warp a task (when the pairs have that many chunks); among the
-// S from there to min(nch, kXMaxSplits) (every split non-empty) the one with
-// the least estimated time in chunk-times - rounds of tasks over the warps
-// times (chunks per task + the per-task cost of emitting a partial and
-// merging) - ties to the smaller S.
-constexpr int kXTaskCost = 3;
-__device__ __forceinline__ int xattn_splits(int pairs, int nch, int warps) {
-  const int smax = min(nch, kXMaxSplits);
-  const int smin = max(1, min(smax, (9 * warps / 10 + pairs - 1) / pairs));
-  int best = 1;  // always valid
-  long long best_cost = -1;
-  for (int pass = 0; pass < 2 && best_cost < 0; ++pass) {
-    const int lo = pass == 0 ? smin : 1, hi = pass == 0 ? smax : smin - 1;
-    for (int s = lo; s <= hi; ++s) {
-      const int cps = (nch + s - 1) / s;
-      if ((nch + cps - 1) / cps != s) continue;  // some split would be empty
-      const long long rounds = ((long long)pairs * s + warps - 1) / warps;
-      const long long cost = rounds * (cps + (s > 1 ? kXTaskCost : 1));
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
-        best = s;
-      }
-    }
-  }
-  return best;
-}
+constexpr int kXMergeCost = 3;  // chunk times of emitting a partial and merging
 
 // Arrival on a counter with release (this warp's partial) and acquire (the
 // other warps' partials) semantics at device scope; returns the old value.
@@ -163,10 +141,19 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
   const int pairs = a.B * a.H;
   const int warps = gridDim.x * kXWarps;
   const int gw = blockIdx.x * kXWarps + warp;
-  const int ns = xattn_splits(pairs, nch, warps);
-  const int cps = (nch + ns - 1) / ns;  // chunks per split (the last split may have fewer, never none)
-  const int tasks = pairs * ns;
-  const int my_tasks = (gw < tasks) ? (tasks - gw + warps - 1) / warps : 0;
+  // balanced partition: the U = pairs x nch (pair, chunk) units are cut into
+  // wp contiguous runs, one per active warp (wp <= U so that no run is empty,
+  // wp <= 31 pairs so that a pair spans at most 32 runs); the piece of a run
+  // inside one pair is a segment, and the segments of a pair are merged
+  // When every pair fits on its own warp and a whole pair takes no longer than
+  // a balanced run plus the cost of a merge (~3 chunk times: partial store,
+  // arrival, combine), each warp takes one whole pair instead (no merges).
+  const int U = pairs * nch;
+  const int wp_bal = min(warps, min(U, 31 * pairs));
+  const int wp = (pairs <= warps && nch <= (U + wp_bal - 1) / wp_bal + kXMergeCost) ? pairs : wp_bal;
+  const long long u_beg = gw < wp ? (long long)gw * U / wp : 0;
+  const long long u_end = gw < wp ? (long long)(gw + 1) * U / wp : 0;
+  auto owner = [&](long long u) { return (int)(((u + 1) * wp - 1) / U); };  // warp whose run holds unit u
   const int d = a.H * HD;
   const T_* mk = static_cast<const T_*>(a.mk);
   const T_* mv = static_cast<const T_*>(a.mv);
@@ -178,17 +165,10 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
   }
   __syncwarp();
 
-  // chunk iterator over this warp's work: k-th task (gw + k*warps), chunk c
-  auto n_chunks_of = [&](int task) {
-    const int sp = task % ns;
-    return min(cps, nch - sp * cps);
-  };
-  int ik = 0, ic = 0;  // next chunk to issue
-  auto issue_next = [&](int stage) {  // lane 0; returns nothing, advances (ik, ic)
-    if (ik >= my_tasks) return;
-    const int task = gw + ik * warps;
-    const int pair = task / ns, sp = task - pair * ns;
-    const int c0 = (sp * cps + ic) * CH;
+  long long iu = u_beg;  // next unit to copy
+  auto issue_next = [&](int stage) {  // lane 0
+    if (iu >= u_end) return;
+    const int pair = (int)(iu / nch), c0 = (int)(iu - (long long)pair * nch) * CH;
     const int nj = min(CH, t - c0);
     const unsigned bytes = (unsigned)(nj * HD * S::ES);
     const size_t off = ((size_t)pair * a.T_mem + c0) * HD;
@@ -196,27 +176,32 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
     bulk_g2s(sbuf + (stage * 2) * CHE, mk + off, bytes, &bar[stage]);
     mbar_arrive_expect_tx(&bar[ST + stage], bytes);
     bulk_g2s(sbuf + (stage * 2 + 1) * CHE, mv + off, bytes, &bar[ST + stage]);
-    if (++ic >= n_chunks_of(task)) {
-      ++ik;
-      ic = 0;
-    }
+    ++iu;
   };
-  if (a.early && lane == 0)
-    for (int s0 = 0; s0 < ST; ++s0) issue_next(s0);
-  pdl_wait();  // q, the ring (window) and the outputs depend on the previous kernels
+  // copies that may start before the previous kernel has finished: all of the
+  // encoder memory (early = 1); the ring except the chunk that holds this
+  // step's slot pos mod W, written by the projection just before (early = 2)
+  int pre = 0;
+  if (lane == 0 && a.early) {
+    const int c_now = (a.early == 2) ? (a.ctx->pos % a.t_cap) / CH : -1;
+    while (pre < ST && iu < u_end && (int)(iu % nch) != c_now) issue_next(pre++);
+  }
+  pre = __shfl_sync(0xffffffffu, pre, 0);
+  pdl_wait();  // q, this step's ring entry and the outputs depend on the previous kernels
   if (threadIdx.x == 0) pdl_trigger();
-  if (!a.early && lane == 0)
-    for (int s0 = 0; s0 < ST; ++s0) issue_next(s0);
+  if (lane == 0)
+    for (int s0 = pre; s0 < ST; ++s0) issue_next(s0);
   __syncwarp();
 
   unsigned phase = 0;  // bit s: parity of the next completion of stage s
   int used = 0;        // chunks consumed (stage = used % ST)
   float acc[EPL], qr[EPL];
-  for (int k = 0; k < my_tasks; ++k) {
-    const int task = gw + k * warps;
-    const int pair = task / ns, sp = task - pair * ns;
+  for (long long u = u_beg; u < u_end;) {
+    const int pair = (int)(u / nch), cbeg = (int)(u - (long long)pair * nch);
+    const long long seg_end = min(u_end, (long long)(pair + 1) * nch);
+    const int nct = (int)(seg_end - u);
+    u = seg_end;
     const int b = pair / a.H, h = pair - b * a.H;
-    const int nct = n_chunks_of(task);
     {
       const float* qp = a.q + (size_t)b * d + h * HD + sub * EPL;
 #pragma unroll
@@ -226,7 +211,7 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
     for (int c = 0; c < nct; ++c, ++used) {
-      const int c0 = (sp * cps + c) * CH;
+      const int c0 = (cbeg + c) * CH;
       const int nj = min(CH, t - c0);
       const int st = used % ST;
       const unsigned par = (phase >> st) & 1u;
@@ -313,7 +298,9 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
     }
-    if (ns == 1) {
+    const int wf = owner((long long)pair * nch);
+    const int nseg = owner((long long)pair * nch + nch - 1) - wf + 1, sp = gw - wf;
+    if (nseg == 1) {
       if (rg == 0) {
         const float inv = 1.f / lt;
 #pragma unroll
@@ -333,19 +320,19 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
       }
       __syncwarp();  // the warp's partial writes are ordered before lane 0's release
       int last = 0;
-      if (lane == 0) last = (atom_add_acq_rel(&a.cnt[pair], 1) == ns - 1);
+      if (lane == 0) last = (atom_add_acq_rel(&a.cnt[pair], 1) == nseg - 1);
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         const float* pp = a.part + (size_t)pair * kXMaxSplits * (HD + 2);
         float M = -INFINITY;
-        for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(pp + (size_t)s2 * (HD + 2)));
+        for (int s2 = 0; s2 < nseg; ++s2) M = fmaxf(M, __ldcg(pp + (size_t)s2 * (HD + 2)));
         float L = 0.f;
-        for (int s2 = 0; s2 < ns; ++s2)
+        for (int s2 = 0; s2 < nseg; ++s2)
           L += __ldcg(pp + (size_t)s2 * (HD + 2) + 1) * exp2f(__ldcg(pp + (size_t)s2 * (HD + 2)) - M);
         const float inv = 1.f / L;
         for (int i = lane; i < HD; i += 32) {
           float o = 0.f;
-          for (int s2 = 0; s2 < ns; ++s2)
+          for (int s2 = 0; s2 < nseg; ++s2)
             o += __ldcg(pp + (size_t)s2 * (HD + 2) + 2 + i) * exp2f(__ldcg(pp + (size_t)s2 * (HD + 2)) - M);
           out[(size_t)b * d + h * HD + i] = from_f32<T_>(o * inv);
         }
