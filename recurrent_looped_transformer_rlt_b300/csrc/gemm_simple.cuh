@@ -1,10 +1,8 @@
-// Generic "TN" GEMM C[M,N] = A[M,K] * B[N,K]^T with fp32 accumulation and a
-// per-element epilogue functor.  The B operand may come from two row blocks
-// (rows n < n_split from B0, the rest from B1), which lets one launch cover
-// W_1 and W_3 of a SwiGLU layer.
-//
-// Two kernels: a bf16 tensor-core kernel (mma.sync m16n8k16, cp.async
-// multi-stage pipeline) and an fp32 CUDA-core kernel for the fp32 models.
+// Epilogue functors of the projections (used by the tcgen05 kernel in
+// gemm_tc.cuh and by the fp32 kernel below), and the fp32 CUDA-core GEMM of
+// the fp32 models: C[M,N] = A[M,K] * B[N,K]^T with a per-element epilogue.
+// Its B operand may come from two row blocks (rows n < n_split from B0, the
+// rest from B1), which lets one launch cover W_1 and W_3 of a SwiGLU layer.
 #pragma once
 
 #include "common.cuh"
@@ -15,7 +13,7 @@ namespace rlt {
 // epilogues: operator()(m, n, acc) is called once per in-range element.
 
 // kStore4 / kAdd4: the tensor-core kernel writes (or adds into) C four
-// columns at a time with 16-byte accesses (needs ldc % 4 == 0).
+// columns at a time with 16-byte accesses (when ldc % 4 == 0).
 struct EpiStoreF32 {
   static constexpr bool kStore4 = true;
   float* C;
@@ -198,130 +196,6 @@ struct GemmB {
   int n_split;  // rows n < n_split read B0[n], others B1[n - n_split]
   int ldb;
 };
-
-// ---------------------------------------------------------------------------
-// bf16 tensor-core kernel
-
-namespace mma_v0 {
-constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3, LDS = BK + 8, THREADS = 256;
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
-  unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-  int sz = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(sz));
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
-
-__device__ __forceinline__ void ldsm_x4(unsigned& r0, unsigned& r1, unsigned& r2, unsigned& r3, const void* p) {
-  unsigned s = (unsigned)__cvta_generic_to_shared(p);
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(s));
-}
-__device__ __forceinline__ void mma16816(float* c, const unsigned* a, const unsigned* b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-template <class Epi>
-__global__ void __launch_bounds__(THREADS) gemm_bf16_kernel(const bf16* __restrict__ A, int lda, GemmB gb,
-                                                            int M, int N, int K, Epi epi) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  bf16* sA = reinterpret_cast<bf16*>(smem_raw);
-  bf16* sB = sA + STAGES * BM * LDS;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-  const int wm = warp >> 2, wn = warp & 3;
-  const bf16* B0 = static_cast<const bf16*>(gb.B0);
-  const bf16* B1 = static_cast<const bf16*>(gb.B1);
-  const int KT = (K + BK - 1) / BK;
-
-  auto load_stage = [&](int stage, int kt) {
-    const int k0 = kt * BK;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      int c = tid + i * THREADS;
-      int row = c >> 2, col = (c & 3) * 8;
-      int gm = m0 + row, gk = k0 + col;
-      bool va = (gm < M) && (gk < K);
-      const bf16* pa = va ? (A + (size_t)gm * lda + gk) : A;
-      cp_async16(sA + (stage * BM + row) * LDS + col, pa, va);
-      int gn = n0 + row;
-      bool vb = (gn < N) && (gk < K);
-      const bf16* pb = B0;
-      if (vb) pb = (gn < gb.n_split) ? (B0 + (size_t)gn * gb.ldb + gk) : (B1 + (size_t)(gn - gb.n_split) * gb.ldb + gk);
-      cp_async16(sB + (stage * BN + row) * LDS + col, pb, vb);
-    }
-  };
-
-  float acc[4][4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.f;
-
-#pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < KT) load_stage(s, s);
-    cp_commit();
-  }
-  for (int kt = 0; kt < KT; ++kt) {
-    cp_wait<STAGES - 2>();
-    __syncthreads();
-    const int st = kt % STAGES;
-    const bf16* a_s = sA + st * BM * LDS;
-    const bf16* b_s = sB + st * BN * LDS;
-#pragma unroll
-    for (int kk = 0; kk < BK / 16; ++kk) {
-      unsigned af[4][4], bfm[4][2];
-#pragma unroll
-      for (int mi = 0; mi < 4; ++mi) {
-        int r = wm * 64 + mi * 16 + (lane & 15);
-        int c = kk * 16 + (lane >> 4) * 8;
-        ldsm_x4(af[mi][0], af[mi][1], af[mi][2], af[mi][3], a_s + r * LDS + c);
-      }
-#pragma unroll
-      for (int nj = 0; nj < 2; ++nj) {
-        int r = wn * 32 + nj * 16 + (lane & 7) + ((lane >> 4) << 3);
-        int c = kk * 16 + ((lane >> 3) & 1) * 8;
-        ldsm_x4(bfm[2 * nj][0], bfm[2 * nj][1], bfm[2 * nj + 1][0], bfm[2 * nj + 1][1], b_s + r * LDS + c);
-      }
-#pragma unroll
-      for (int mi = 0; mi < 4; ++mi)
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni) mma16816(acc[mi][ni], af[mi], bfm[ni]);
-    }
-    int nx = kt + STAGES - 1;
-    if (nx < KT) load_stage(nx % STAGES, nx);
-    cp_commit();
-  }
-  cp_wait<0>();
-
-#pragma unroll
-  for (int mi = 0; mi < 4; ++mi)
-#pragma unroll
-    for (int ni = 0; ni < 4; ++ni) {
-      int r = m0 + wm * 64 + mi * 16 + (lane >> 2);
-      int c = n0 + wn * 32 + ni * 8 + (lane & 3) * 2;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        int rr = r + h * 8;
-        if (rr < M) {
-          if (c < N) epi(rr, c, acc[mi][ni][2 * h]);
-          if (c + 1 < N) epi(rr, c + 1, acc[mi][ni][2 * h + 1]);
-        }
-      }
-    }
-}
-constexpr size_t smem_bytes() { return (size_t)STAGES * (BM + BN) * LDS * sizeof(bf16); }
-}  // namespace mma_v0
 
 // ---------------------------------------------------------------------------
 // fp32 CUDA-core kernel (fp32 models)

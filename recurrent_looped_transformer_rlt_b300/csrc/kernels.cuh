@@ -344,96 +344,6 @@ __global__ void __launch_bounds__(128) dec_swa_kernel(const float* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------
-// Decoder cross-attention to encoder memory positions 0..p (steps 1..t),
-// split over position chunks of CH (flash-decoding).  Block = (chunk, h, b).
-// Each block writes (max, sum, unnormalised o[hd]) to part; the combine
-// kernel merges chunks.  q: fp32 [B][d]; mk, mv: [B][H][T_mem][hd].
-constexpr int kXChunk = 128;
-
-template <typename T_>
-__global__ void __launch_bounds__(128) dec_xattn_part_kernel(const float* __restrict__ q, const T_* __restrict__ mk,
-                                                             const T_* __restrict__ mv, float* __restrict__ part,
-                                                             int H, int hd, int T_mem, int n_chunks, float scale,
-                                                             const StepCtx* ctx) {
-  extern __shared__ float sm[];
-  float* sq = sm;                  // [hd]
-  float* sp = sq + hd;             // [CH]
-  float* sacc = sp + kXChunk;      // [128] partial o
-  __shared__ float red[32];
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-  const int t = ctx->pos + 1;
-  const int j0 = c * kXChunk;
-  float* pr = part + (((size_t)b * H + h) * n_chunks + c) * (hd + 2);
-  if (j0 >= t) return;  // chunk beyond the visible range: not read by the combine
-  const int nj = min(kXChunk, t - j0);
-  const int d = H * hd;
-  for (int i = tid; i < hd; i += blockDim.x) sq[i] = q[(size_t)b * d + h * hd + i];
-  __syncthreads();
-  const size_t base = (((size_t)b * H + h) * T_mem) * hd;
-  float lmax = -INFINITY;
-  for (int j = tid; j < nj; j += blockDim.x) {
-    const T_* kr = mk + base + (size_t)(j0 + j) * hd;
-    float s = 0.f;
-    for (int cc = 0; cc < hd; ++cc) s = fmaf(sq[cc], to_f32(kr[cc]), s);
-    s *= scale;
-    sp[j] = s;
-    lmax = fmaxf(lmax, s);
-  }
-  lmax = warp_max(lmax);
-  if ((tid & 31) == 0) red[tid >> 5] = lmax;
-  __syncthreads();
-  float m = -INFINITY;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
-  __syncthreads();
-  float lsum = 0.f;
-  for (int j = tid; j < nj; j += blockDim.x) {
-    float e = expf(sp[j] - m);
-    sp[j] = e;
-    lsum += e;
-  }
-  lsum = warp_sum(lsum);
-  if ((tid & 31) == 0) red[tid >> 5] = lsum;
-  __syncthreads();
-  float l = 0.f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) l += red[w];
-  // o[dim] = sum_j p_j v_j[dim]; threads split (dim, j-group)
-  const int groups = blockDim.x / hd > 0 ? blockDim.x / hd : 1;
-  const int dim = tid % hd, grp = tid / hd;
-  float acc = 0.f;
-  if (grp < groups)
-    for (int j = grp; j < nj; j += groups) acc = fmaf(sp[j], to_f32(mv[base + (size_t)(j0 + j) * hd + dim]), acc);
-  sacc[tid] = acc;
-  __syncthreads();
-  if (tid < hd) {
-    float o = 0.f;
-    for (int g = 0; g < groups; ++g) o += sacc[g * hd + tid];
-    pr[2 + tid] = o;
-  }
-  if (tid == 0) {
-    pr[0] = m;
-    pr[1] = l;
-  }
-}
-
-template <typename T_>
-__global__ void dec_xattn_combine_kernel(const float* __restrict__ part, T_* __restrict__ out, int H, int hd,
-                                         int n_chunks, const StepCtx* ctx) {
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const int t = ctx->pos + 1;
-  const int used = (t + kXChunk - 1) / kXChunk;
-  const float* pr = part + (((size_t)b * H + h) * n_chunks) * (hd + 2);
-  float m = -INFINITY;
-  for (int c = 0; c < used; ++c) m = fmaxf(m, pr[(size_t)c * (hd + 2)]);
-  float l = 0.f;
-  for (int c = 0; c < used; ++c) l += pr[(size_t)c * (hd + 2) + 1] * expf(pr[(size_t)c * (hd + 2)] - m);
-  for (int i = tid; i < hd; i += blockDim.x) {
-    float o = 0.f;
-    for (int c = 0; c < used; ++c) o += pr[(size_t)c * (hd + 2) + 2 + i] * expf(pr[(size_t)c * (hd + 2)] - m);
-    out[(size_t)b * H * hd + h * hd + i] = from_f32<T_>(o / l);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // End of the decoder layers: s_t = h; a = RMSNorm_o(h) for the head GEMM.
 template <typename T_>
 __global__ void head_prep_kernel(const float* __restrict__ h, float* __restrict__ s, const float* __restrict__ g,
@@ -613,12 +523,6 @@ __global__ void set_ctx_kernel(StepCtx* ctx, int pos) {
   ctx->step = 0;
 }
 
-template <typename T_>
-__global__ void fill_kernel(T_* p, size_t n, T_ val) {
-  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (; i < n; i += stride) p[i] = val;
-}
 template <typename T_>
 __global__ void fill_nan_kernel(T_* p, size_t n) {
   size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;

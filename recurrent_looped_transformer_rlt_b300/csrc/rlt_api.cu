@@ -157,13 +157,9 @@ T* at(void* ws, size_t off) {
 template <typename T_, class Epi>
 int gemm(cudaStream_t st, const T_* A, int lda, GemmB gb, int M, int N, int K, Epi epi) {
   if (M <= 0 || N <= 0) return RLT_OK;
-  if constexpr (std::is_same<T_, bf16>::value) {
-    dim3 grid(cdiv(N, mma_v0::BN), cdiv(M, mma_v0::BM));
-    mma_v0::gemm_bf16_kernel<Epi><<<grid, mma_v0::THREADS, mma_v0::smem_bytes(), st>>>(A, lda, gb, M, N, K, epi);
-  } else {
-    dim3 grid(cdiv(N, simt_v0::BN), cdiv(M, simt_v0::BM));
-    simt_v0::gemm_f32_kernel<Epi><<<grid, simt_v0::THREADS, 0, st>>>(A, lda, gb, M, N, K, epi);
-  }
+  static_assert(std::is_same<T_, float>::value, "bf16 projections run on the tensor-core kernel");
+  dim3 grid(cdiv(N, simt_v0::BN), cdiv(M, simt_v0::BM));
+  simt_v0::gemm_f32_kernel<Epi><<<grid, simt_v0::THREADS, 0, st>>>(A, lda, gb, M, N, K, epi);
   g_launches++;
   return launch_ok();
 }
@@ -471,12 +467,6 @@ std::mutex g_attr_mu;
 
 template <typename T_>
 void set_attrs() {
-  cudaFuncSetAttribute(mma_v0::gemm_bf16_kernel<EpiStoreF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)mma_v0::smem_bytes());
-  cudaFuncSetAttribute(mma_v0::gemm_bf16_kernel<EpiAddF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)mma_v0::smem_bytes());
-  cudaFuncSetAttribute(mma_v0::gemm_bf16_kernel<EpiMemScatter<bf16>>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)mma_v0::smem_bytes());
   cudaFuncSetAttribute(enc_attn_simt_kernel<T_>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
   cudaFuncSetAttribute(head_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }

@@ -239,12 +239,25 @@ def test_stale_state_rejected_and_bounds_flag():
 # ---------------------------------------------------------------------------
 # the cross-attention step on its own
 
-@pytest.mark.parametrize("name,B,T_mem,ts", [("small", 5, 300, [1, 2, 127, 128, 129, 300]),
-                                              ("tiny", 3, 64, [1, 17, 64])])
+# Shapes that reach each way the kernel divides its work: few pairs over long
+# memories (the (pair, chunk) runs cut every pair into the most segments
+# allowed, 31-32), ring depth 3 (head_dim <= 64 and >= 512 positions) and 2,
+# head_dim 32 / 64 / 128, whole pairs per warp (short memories), and t = 1.
+PARTITION_CASES = [
+    ("small", 5, 300, [1, 2, 127, 128, 129, 300]),
+    ("tiny", 3, 64, [1, 17, 64]),
+    ("small", 1, 4096, [1, 64, 65, 2048, 4096]),
+    ("medium", 2, 1024, [1, 31, 1000, 1024]),
+    ("refdep", 1, 512, [1, 16, 17, 512]),
+]
+
+
+@pytest.mark.parametrize("name,B,T_mem,ts", PARTITION_CASES)
 def test_cross_attention_entry_point(name, B, T_mem, ts):
     import torch
     import recurrent_looped_transformer_rlt_b300 as rlt
-    wl = ri.preset(name)
+    # one layer and a small vocabulary: the entry point uses only the widths
+    wl = ri.preset(name, n_layers=1, mem_groups=1, vocab=64)
     c = wl.cfg
     W = ri.make_weights(c, wl.seed)
     model = rlt.Model(c, W)
