@@ -132,6 +132,41 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the GPU arm
 
+# ---------------------------------------------------------------------------
+# replicas: host-side logic of the N > 1 path (also run with gloo on CPU)
+
+RANK_SEED_STRIDE = 7919
+
+
+def rank_inputs(wl, rank):
+    """This rank's sequences: tokens, prompt/response splits and the scored
+    actions (teacher-forced next tokens), from a seed offset by the rank, so
+    that ranks hold disjoint draws of the same workload (weak scaling)."""
+    seed = wl.seed + RANK_SEED_STRIDE * rank
+    tok = ri.make_tokens(wl, seed=seed)
+    prompt = ri.make_splits(wl, seed=seed)
+    acts = ri.teacher_actions(tok, 0, wl.T, None if wl.score_prompt else prompt)
+    return tok, prompt, acts
+
+
+def max_over_ranks(values, world, device=None):
+    """Element-wise maximum of a list of per-rank timings over all ranks (the
+    slowest rank times the job)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    v = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(v, op=dist.ReduceOp.MAX)
+    return v.tolist()
+
+
+def job_throughput(B, T, world, t_step):
+    """Whole-job decoder tokens/s: every rank's B x T tokens over the slowest
+    rank's step time."""
+    return B * T * world / t_step
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -145,9 +180,7 @@ def run_gpu(args, rank, world, local_rank):
     B, T = wl.B, wl.T
     # weights: seeded numpy draws (identical on every rank); tokens: this rank's sequences
     W = ri.make_weights(c, wl.seed)
-    tok = ri.make_tokens(wl, seed=wl.seed + 7919 * rank)
-    prompt = ri.make_splits(wl, seed=wl.seed + 7919 * rank)
-    acts = ri.teacher_actions(tok, 0, T, None if wl.score_prompt else prompt)
+    tok, prompt, acts = rank_inputs(wl, rank)
     model = rlt.Model(c, W, device=dev)
     stream = torch.cuda.current_stream()
     buf = runner.alloc_buffers(model, B, T)
@@ -233,10 +266,7 @@ def run_gpu(args, rank, world, local_rank):
     t_step = float(np.mean(times))
     t_enc = float(np.mean(enc_times))
     t_e2e = float(np.mean(e2e))
-    if world > 1:
-        v = torch.tensor([t_step, t_enc, t_e2e], device=dev, dtype=torch.float64)
-        dist.all_reduce(v, op=dist.ReduceOp.MAX)
-        t_step, t_enc, t_e2e = v.tolist()
+    t_step, t_enc, t_e2e = max_over_ranks([t_step, t_enc, t_e2e], world, dev)
     res = dict(t_step=t_step, t_enc=t_enc, t_e2e=t_e2e, launches=launches // max(args.steps, 1),
                clocks=clk.summary(), kernel_ms=kernel_ms, B=B, T=T, wl=wl,
                h2d=tok.nbytes + acts.nbytes, d2h=B * T * 4)
@@ -446,7 +476,7 @@ def main():
         wl, B, T = r["wl"], r["B"], r["T"]
         bw, peak, src = load_peaks()
         n_tok = B * T * world
-        value = n_tok / r["t_step"]
+        value = job_throughput(B, T, world, r["t_step"])
         roof_s = decode_roofline_s(wl.cfg, B, T, bw, peak)
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
