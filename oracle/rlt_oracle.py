@@ -144,16 +144,21 @@ class Cfg:
     rms_eps: float = 1e-6
     rope_theta: float = 1e4
     gate_mode: int = 0          # 1: gate forced to discard s_{t-1} (z = 0)
+    mem_source: int = 0         # 0: every group from the final e; 1: group l from layer l's state
 
     @staticmethod
     def of(c) -> "Cfg":
         """Build from any object or dict with the same field names (dtype 'bf16'/'f32')."""
-        get = (lambda k: c[k]) if isinstance(c, dict) else (lambda k: getattr(c, k))
+        if isinstance(c, dict):
+            get = lambda k, dflt=None: c.get(k, dflt)  # noqa: E731
+        else:
+            get = lambda k, dflt=None: getattr(c, k, dflt)  # noqa: E731
         return Cfg(d=get("d"), n_layers=get("n_layers"), n_heads=get("n_heads"),
                    head_dim=get("head_dim"), d_ffn=get("d_ffn"), window=get("window"),
                    mem_groups=get("mem_groups"), vocab=get("vocab"),
                    bf16=(get("dtype") == "bf16"), rms_eps=get("rms_eps"),
-                   rope_theta=get("rope_theta"), gate_mode=get("gate_mode"))
+                   rope_theta=get("rope_theta"), gate_mode=get("gate_mode"),
+                   mem_source=get("mem_source", 0))
 
     def group_of(self, layer: int) -> int:
         """Memory group read by decoder layer l: 0 when G=1, l when G=L_D."""
@@ -189,11 +194,22 @@ def encode(cfg: Cfg, W: Dict[str, np.ndarray], tokens: np.ndarray, return_hidden
 
     tokens int [B, T] (position p = column index).  Returns e [B, T, d] and
     mem [G, 2, B, H, T, hd] (index 0 = keys, 1 = values).
+
+    Memory source.  The reading taken projects every group from the final e
+    (P5 architecture paragraph: decoder global keys and values come from the
+    final encoder states).  The other reading of per-layer memory (G = L_D, the
+    configs with per-layer memory projections) takes group l from encoder
+    layer l's state: mem_source = 1 projects group l from
+    RMSNorm_e(h^l), the residual stream after layer l under the final norm's
+    gain, so that the last group coincides with the first reading's.
     """
     nx = Numerics(cfg.bf16)
     B, T = tokens.shape
     d, H, hd = cfg.d, cfg.n_heads, cfg.head_dim
     pos = np.arange(T)
+    if cfg.mem_source == 1 and cfg.mem_groups != cfg.n_layers:
+        raise ValueError("per-layer memory needs one group per layer")
+    layer_states = []
     h = _w(W, "tok_emb")[tokens]                                  # [B, T, d]
     for l in range(cfg.n_layers):
         a = nx.r(rmsnorm(h, _w(W, "enc_attn_norm", l), cfg.rms_eps))
@@ -212,22 +228,28 @@ def encode(cfg: Cfg, W: Dict[str, np.ndarray], tokens: np.ndarray, return_hidden
         bb = nx.r(rmsnorm(h, _w(W, "enc_ffn_norm", l), cfg.rms_eps))
         m = nx.r(silu(bb @ _w(W, "W_1", l).T) * (bb @ _w(W, "W_3", l).T))
         h = h + m @ _w(W, "W_2", l).T
+        if cfg.mem_source == 1:
+            layer_states.append(nx.r(rmsnorm(h, _w(W, "enc_norm"), cfg.rms_eps)))
     e = nx.r(rmsnorm(h, _w(W, "enc_norm"), cfg.rms_eps))
-    mem = memory_projection(cfg, W, e)
+    if cfg.mem_source == 1:
+        mem = memory_projection(cfg, W, layer_states)
+    else:
+        mem = memory_projection(cfg, W, [e] * cfg.mem_groups)
     if return_hidden:
         return e, mem, h
     return e, mem
 
 
-def memory_projection(cfg: Cfg, W, e):
-    """M^g = (e W_K^g^T, e W_V^g^T) for each group g, stored [G, 2, B, H, T, hd]."""
+def memory_projection(cfg: Cfg, W, sources):
+    """M^g = (x_g W_K^g^T, x_g W_V^g^T) for each group g from its source x_g
+    [B, T, d], stored [G, 2, B, H, T, hd]."""
     nx = Numerics(cfg.bf16)
-    B, T, d = e.shape
+    B, T, d = sources[0].shape
     H, hd = cfg.n_heads, cfg.head_dim
     mem = np.empty((cfg.mem_groups, 2, B, H, T, hd), F64)
     for g in range(cfg.mem_groups):
-        kk = nx.r(e @ _w(W, "W_K", g).T)
-        vv = nx.r(e @ _w(W, "W_V", g).T)
+        kk = nx.r(sources[g] @ _w(W, "W_K", g).T)
+        vv = nx.r(sources[g] @ _w(W, "W_V", g).T)
         mem[g, 0] = kk.reshape(B, T, H, hd).transpose(0, 2, 1, 3)
         mem[g, 1] = vv.reshape(B, T, H, hd).transpose(0, 2, 1, 3)
     return mem

@@ -54,10 +54,13 @@ class RLTConfig:
     rms_eps: float = 1e-6
     rope_theta: float = 1e4
     gate_mode: int = 0       # 0 learned gate, 1 gate forced to discard s_{t-1}
+    mem_source: int = 0      # 0 every memory group from the final e, 1 group l from encoder layer l
 
     def __post_init__(self):
         assert self.d == self.n_heads * self.head_dim
         assert self.mem_groups in (1, self.n_layers)
+        assert self.mem_source in (0, 1)
+        assert self.mem_source == 0 or self.mem_groups == self.n_layers
         assert self.dtype in ("f32", "bf16")
         assert self.head_dim % 2 == 0
 

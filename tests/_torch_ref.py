@@ -46,6 +46,7 @@ def encoder(cfg, W, tokens):
     B, P = tok.shape
     pos = torch.arange(P)
     h = F.embedding(tok, T(W["tok_emb"]))
+    hidden = []
     for l in range(cfg.n_layers):
         a = F.rms_norm(h, (d,), weight=T(W["enc_attn_norm"][l]), eps=cfg.rms_eps)
         q, k, v = F.linear(a, T(W["W_qkv"][l])).split(d, dim=-1)
@@ -56,11 +57,15 @@ def encoder(cfg, W, tokens):
         b = F.rms_norm(h, (d,), weight=T(W["enc_ffn_norm"][l]), eps=cfg.rms_eps)
         h = h + F.linear(F.silu(F.linear(b, T(W["W_1"][l]))) * F.linear(b, T(W["W_3"][l])),
                          T(W["W_2"][l]))
+        hidden.append(h)
     e = F.rms_norm(h, (d,), weight=T(W["enc_norm"]), eps=cfg.rms_eps)
     mem = []
     for g in range(cfg.mem_groups):
-        mem.append(torch.stack([_heads(F.linear(e, T(W["W_K"][g])), H),
-                                _heads(F.linear(e, T(W["W_V"][g])), H)]))
+        # per-layer source: the residual stream after layer g under the final norm
+        src = F.rms_norm(hidden[g], (d,), weight=T(W["enc_norm"]), eps=cfg.rms_eps) \
+            if getattr(cfg, "mem_source", 0) == 1 else e
+        mem.append(torch.stack([_heads(F.linear(src, T(W["W_K"][g])), H),
+                                _heads(F.linear(src, T(W["W_V"][g])), H)]))
     return e.numpy(), torch.stack(mem).numpy()
 
 

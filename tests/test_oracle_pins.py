@@ -19,7 +19,7 @@ from tests import _torch_ref as TR
 
 def tiny_cfg(**kw):
     base = dict(d=32, n_layers=2, n_heads=4, head_dim=8, d_ffn=48, window=3, mem_groups=1,
-                vocab=11, dtype="f32", rms_eps=1e-6, rope_theta=1e4, gate_mode=0)
+                vocab=11, dtype="f32", rms_eps=1e-6, rope_theta=1e4, gate_mode=0, mem_source=0)
     base.update(kw)
     c = ri.RLTConfig(**{k: v for k, v in base.items()})
     return c
@@ -102,14 +102,37 @@ def test_softmax_and_lse():
 # ---------------------------------------------------------------------------
 # encoder and memory
 
-@pytest.mark.parametrize("G", [1, 2])
-def test_encoder_matches_library_composition(G):
-    cfg, W, tok = setup(mem_groups=G)
+@pytest.mark.parametrize("G,src", [(1, 0), (2, 0), (2, 1)])
+def test_encoder_matches_library_composition(G, src):
+    cfg, W, tok = setup(mem_groups=G, mem_source=src)
     e, mem = O.encode(cfg, W, tok)
     e_ref, mem_ref = TR.encoder(cfg, W, tok)
     np.testing.assert_allclose(e, e_ref, rtol=1e-11, atol=1e-11)
     np.testing.assert_allclose(mem, mem_ref, rtol=1e-11, atol=1e-11)
     assert mem.shape == (G, 2, tok.shape[0], cfg.n_heads, tok.shape[1], cfg.head_dim)
+
+
+def test_per_layer_memory_reading():
+    """Group l from encoder layer l (the other reading of per-layer memory):
+    the last group is the final-e group, a single-layer encoder gives the same
+    memory under both readings, and group l does not depend on encoder layers
+    after l."""
+    cfg0, W, tok = setup(mem_groups=2, mem_source=0)
+    cfg1, _, _ = setup(mem_groups=2, mem_source=1)
+    e0, m0 = O.encode(cfg0, W, tok)
+    e1, m1 = O.encode(cfg1, W, tok)
+    np.testing.assert_array_equal(e0, e1)
+    np.testing.assert_array_equal(m0[1], m1[1])
+    assert np.abs(m0[0] - m1[0]).max() > 1e-3 * np.abs(m0[0]).max()
+    c1a, W1, tok1 = setup(n_layers=1, mem_groups=1, mem_source=0)
+    c1b, _, _ = setup(n_layers=1, mem_groups=1, mem_source=1)
+    np.testing.assert_array_equal(O.encode(c1a, W1, tok1)[1], O.encode(c1b, W1, tok1)[1])
+    W2 = {k: v.copy() for k, v in W.items()}
+    for name in ("W_qkv", "W_O", "W_1", "W_3", "W_2", "enc_attn_norm", "enc_ffn_norm"):
+        W2[name][1] = W2[name][1] * 1.5 + 0.01
+    _, m2 = O.encode(cfg1, W2, tok)
+    np.testing.assert_array_equal(m1[0], m2[0])
+    assert np.abs(m1[1] - m2[1]).max() > 1e-3 * np.abs(m1[1]).max()
 
 
 def test_memory_depends_only_on_tokens():
@@ -388,6 +411,7 @@ def _fails(fn, *a, **kw):
 def test_planted_mistakes_are_caught(monkeypatch):
     orig_rope, orig_keep, orig_range, orig_merge = O.rope, O.history_keep, O.memory_range, O.merge
     orig_attn = O.causal_attention
+    orig_proj = O.memory_projection
 
     def rope_sign(x, pos, theta):
         hd = x.shape[-1]
@@ -397,14 +421,17 @@ def test_planted_mistakes_are_caught(monkeypatch):
         return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], axis=-1)
 
     cases = [
-        ("rope", rope_sign, lambda: test_encoder_matches_library_composition(1)),
+        ("rope", rope_sign, lambda: test_encoder_matches_library_composition(1, 0)),
         ("history_keep", lambda w: w, lambda: test_gate_discard_equals_parallel_pass(4)),
         ("memory_range", lambda t: max(t - 1, 1), lambda: test_gate_discard_equals_parallel_pass(4)),
         ("merge", lambda cfg, W, e, s, nx, trace=None: orig_merge(cfg, W, s, e, nx, trace),
          lambda: test_recurrence_equals_brute_force(3, 1)),
         ("causal_attention",
          lambda q, k, v, nx, round_p: (O.softmax_last((q @ np.swapaxes(k, -1, -2)) / math.sqrt(q.shape[-1])) @ v),
-         lambda: test_encoder_matches_library_composition(1)),
+         lambda: test_encoder_matches_library_composition(1, 0)),
+        # per-layer memory taken from the wrong layers
+        ("memory_projection", lambda cfg, W, sources: orig_proj(cfg, W, sources[::-1]),
+         lambda: test_encoder_matches_library_composition(2, 1)),
     ]
     for name, bad, pin in cases:
         with monkeypatch.context() as m:
