@@ -68,18 +68,27 @@ enum {
 
 enum { RLT_F32 = 0, RLT_BF16 = 1 };
 enum { RLT_GATE_LEARNED = 0, RLT_GATE_DISCARD_S = 1 };
+enum { RLT_MEM_FINAL = 0, RLT_MEM_PER_LAYER = 1 };
 
 /* Model shape.  d_model = n_heads * head_dim; head_dim even and <= 128;
  * mem_groups is 1 (memory shared by all decoder layers) or n_layers (one
  * group per layer).  gate_mode RLT_GATE_DISCARD_S forces the merge gate z to
  * 0 (u_t = e_t) and exists for the equivalence checks; RLT_GATE_LEARNED is
- * z = sigmoid(W_g [e_t; s_{t-1}] + b_g), u_t = z * s_{t-1} + (1 - z) * e_t. */
+ * z = sigmoid(W_g [e_t; s_{t-1}] + b_g), u_t = z * s_{t-1} + (1 - z) * e_t.
+ * mem_source picks where the memory groups are projected from: RLT_MEM_FINAL
+ * (every group from the final encoder output e; "Princeton Researcher
+ * Proposes Recurrent Looped Transformer ...", architecture paragraph: decoder
+ * keys and values from the final encoder states) or RLT_MEM_PER_LAYER (group
+ * l from RMSNorm_e of the encoder's residual stream after layer l, the other
+ * reading of the configurations with per-layer memory projections; needs
+ * mem_groups == n_layers). */
 typedef struct rlt_config {
   int32_t d_model, n_layers, n_heads, head_dim, d_ffn, window, mem_groups, vocab;
   int32_t dtype;          /* RLT_F32 or RLT_BF16 */
   float rms_eps;          /* RMSNorm: x / sqrt(mean(x^2) + eps) * g */
   float rope_theta;       /* rotate-half RoPE base on encoder and decoder self-attention */
   int32_t gate_mode;
+  int32_t mem_source;     /* RLT_MEM_FINAL or RLT_MEM_PER_LAYER */
 } rlt_config;
 
 /* Weights: device pointers, borrowed for the model's lifetime (the caller

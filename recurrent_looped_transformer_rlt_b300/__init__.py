@@ -28,6 +28,7 @@ RLT_OK, RLT_EINVAL, RLT_ESTALE, RLT_ERANGE, RLT_ECUDA = 0, -1, -2, -3, -4
 RLT_ETIMEOUT, RLT_EBOUNDS, RLT_EWORKSPACE, RLT_EUNSUPPORTED = -5, -6, -7, -8
 RLT_F32, RLT_BF16 = 0, 1
 RLT_GATE_LEARNED, RLT_GATE_DISCARD_S = 0, 1
+RLT_MEM_FINAL, RLT_MEM_PER_LAYER = 0, 1
 
 _p = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -37,7 +38,7 @@ class rlt_config(ctypes.Structure):
     _fields_ = [("d_model", _i32), ("n_layers", _i32), ("n_heads", _i32), ("head_dim", _i32),
                 ("d_ffn", _i32), ("window", _i32), ("mem_groups", _i32), ("vocab", _i32),
                 ("dtype", _i32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
-                ("gate_mode", _i32)]
+                ("gate_mode", _i32), ("mem_source", _i32)]
 
 
 WEIGHT_FIELDS = ["tok_emb", "s_star", "W_g", "b_g", "W_qkv", "W_O", "W_1", "W_3", "W_2", "W_Qx",
@@ -238,7 +239,7 @@ def make_config(c, gate_mode: Optional[int] = None) -> rlt_config:
     """rlt_config from any object with the fields of rlt_inputs.RLTConfig."""
     return rlt_config(c.d, c.n_layers, c.n_heads, c.head_dim, c.d_ffn, c.window, c.mem_groups, c.vocab,
                       RLT_BF16 if c.dtype == "bf16" else RLT_F32, c.rms_eps, c.rope_theta,
-                      c.gate_mode if gate_mode is None else gate_mode)
+                      c.gate_mode if gate_mode is None else gate_mode, getattr(c, "mem_source", RLT_MEM_FINAL))
 
 
 class Model:

@@ -561,6 +561,16 @@ int encode_bf16(const rlt_model* m, const int32_t* tok, int B, int T, bf16* e, b
   float* ss = at<float>(ws, Lw.e_ss);
   const TcScratch sc = tc_scratch(m, ws, Lw);
   int rc;
+  // memory group g (keys and values, [B][H][T][hd] each) from the source rows src [R][d]
+  const size_t plane = (size_t)B * H * T * hd;
+  auto mem_proj_bf16 = [&](cudaStream_t s_, const bf16* src, int g) -> int {
+    const bf16* WK = wl<bf16>(w.W_K, g, (size_t)d * d);
+    const bf16* WV = wl<bf16>(w.W_V, g, (size_t)d * d);
+    int r;
+    if ((r = gemm_bf16_tc(s_, src, d, R, d, WK, d, d, EpiMemScatter<bf16>{mem + (2 * g) * plane, T, H, hd}, sc)))
+      return r;
+    return gemm_bf16_tc(s_, src, d, R, d, WV, d, d, EpiMemScatter<bf16>{mem + (2 * g + 1) * plane, T, H, hd}, sc);
+  };
   rope_table_kernel<<<cdiv((size_t)T * (hd / 2), 256), 256, 0, st>>>(tab, 0, T, hd / 2, (double)c.rope_theta);
   g_launches++;
   embed_norm_kernel<<<R, d / 4, 0, st>>>(tok, static_cast<const bf16*>(w.tok_emb), h, x, w.enc_attn_norm, R, d,
@@ -580,20 +590,20 @@ int encode_bf16(const rlt_model* m, const int32_t* tok, int B, int T, bf16* e, b
     if ((rc = gemm_bf16_tc_glu(st, x, d, R, d, W1, W3, d, f, EpiStoreT<bf16>{xm, f}, sc))) return rc;
     const bf16* W2 = wl<bf16>(w.W_2, l, (size_t)d * f);
     if ((rc = gemm_bf16_tc(st, xm, f, R, f, W2, f, d, EpiResidual{HOut{h, d, nullptr, nullptr, ss, R}}, sc))) return rc;
+    // per-layer memory: group l from RMSNorm_e of this layer's output (the
+    // SwiGLU buffer is free until the next layer's W_1/W_3 projection)
+    if (c.mem_source == RLT_MEM_PER_LAYER && l + 1 < L) {
+      if ((rc = norm_rows(st, h, ss, w.enc_norm, xm, R, d, c.rms_eps))) return rc;
+      if ((rc = mem_proj_bf16(st, xm, l))) return rc;
+    }
     // RMSNorm of the next layer's attention, or the final norm producing e
     if ((rc = norm_rows(st, h, ss, (l + 1 < L) ? w.enc_attn_norm + (size_t)(l + 1) * d : w.enc_norm,
                         (l + 1 < L) ? x : e, R, d, c.rms_eps)))
       return rc;
   }
-  const size_t plane = (size_t)B * H * T * hd;
-  for (int g = 0; g < G; ++g) {
-    const bf16* WK = wl<bf16>(w.W_K, g, (size_t)d * d);
-    const bf16* WV = wl<bf16>(w.W_V, g, (size_t)d * d);
-    if ((rc = gemm_bf16_tc(st, e, d, R, d, WK, d, d, EpiMemScatter<bf16>{mem + (2 * g) * plane, T, H, hd}, sc)))
-      return rc;
-    if ((rc = gemm_bf16_tc(st, e, d, R, d, WV, d, d, EpiMemScatter<bf16>{mem + (2 * g + 1) * plane, T, H, hd}, sc)))
-      return rc;
-  }
+  if (c.mem_source == RLT_MEM_PER_LAYER) return mem_proj_bf16(st, e, L - 1);  // the last layer's source is e
+  for (int g = 0; g < G; ++g)
+    if ((rc = mem_proj_bf16(st, e, g))) return rc;
   return RLT_OK;
 }
 
@@ -623,6 +633,15 @@ int encode_impl(const rlt_model* m, const int32_t* tok, int B, int T, T_* e, T_*
   if ((rc = launch_ok())) return rc;
   const float scale = 1.0f / sqrtf((float)hd);
   const size_t att_smem = sizeof(float) * (32 * hd + 32 * (hd + 1) + 32 * hd);
+  // memory group g (keys and values, [B][H][T][hd] each) from the source rows src [R][d]
+  const size_t plane = (size_t)B * H * T * hd;
+  auto mem_proj = [&](const T_* src, int g) -> int {
+    const T_* WK = wl<T_>(w.W_K, g, (size_t)d * d);
+    const T_* WV = wl<T_>(w.W_V, g, (size_t)d * d);
+    int r;
+    if ((r = proj<T_>(st, src, d, R, d, WK, d, d, EpiMemScatter<T_>{mem + (2 * g) * plane, T, H, hd}, sc))) return r;
+    return proj<T_>(st, src, d, R, d, WV, d, d, EpiMemScatter<T_>{mem + (2 * g + 1) * plane, T, H, hd}, sc);
+  };
   for (int l = 0; l < L; ++l) {
     if ((rc = rmsnorm<T_>(st, h, w.enc_attn_norm + (size_t)l * d, a, R, d, d, c.rms_eps))) return rc;
     const T_* Wqkv = wl<T_>(w.W_qkv, l, (size_t)3 * d * d);
@@ -640,16 +659,16 @@ int encode_impl(const rlt_model* m, const int32_t* tok, int B, int T, T_* e, T_*
     if ((rc = swiglu_proj<T_>(st, a, d, R, d, W1, W3, f, am, C, sc))) return rc;
     const T_* W2 = wl<T_>(w.W_2, l, (size_t)d * f);
     if ((rc = proj<T_>(st, am, f, R, f, W2, f, d, EpiAddF32{h, d}, sc))) return rc;
+    // per-layer memory: group l from RMSNorm_e of this layer's output
+    if (c.mem_source == RLT_MEM_PER_LAYER && l + 1 < L) {
+      if ((rc = rmsnorm<T_>(st, h, w.enc_norm, a, R, d, d, c.rms_eps))) return rc;
+      if ((rc = mem_proj(a, l))) return rc;
+    }
   }
   if ((rc = rmsnorm<T_>(st, h, w.enc_norm, e, R, d, d, c.rms_eps))) return rc;
-  const size_t plane = (size_t)B * H * T * hd;
-  for (int g = 0; g < G; ++g) {
-    const T_* WK = wl<T_>(w.W_K, g, (size_t)d * d);
-    const T_* WV = wl<T_>(w.W_V, g, (size_t)d * d);
-    if ((rc = proj<T_>(st, e, d, R, d, WK, d, d, EpiMemScatter<T_>{mem + (2 * g) * plane, T, H, hd}, sc))) return rc;
-    if ((rc = proj<T_>(st, e, d, R, d, WV, d, d, EpiMemScatter<T_>{mem + (2 * g + 1) * plane, T, H, hd}, sc)))
-      return rc;
-  }
+  if (c.mem_source == RLT_MEM_PER_LAYER) return mem_proj(e, L - 1);  // the last layer's source is e
+  for (int g = 0; g < G; ++g)
+    if ((rc = mem_proj(e, g))) return rc;
   return RLT_OK;
 }
 
@@ -1135,6 +1154,8 @@ int validate_cfg(const rlt_config* c) {
   if (c->mem_groups != 1 && c->mem_groups != c->n_layers) return RLT_EINVAL;
   if (c->dtype != RLT_F32 && c->dtype != RLT_BF16) return RLT_EINVAL;
   if (c->gate_mode != RLT_GATE_LEARNED && c->gate_mode != RLT_GATE_DISCARD_S) return RLT_EINVAL;
+  if (c->mem_source != RLT_MEM_FINAL && c->mem_source != RLT_MEM_PER_LAYER) return RLT_EINVAL;
+  if (c->mem_source == RLT_MEM_PER_LAYER && c->mem_groups != c->n_layers) return RLT_EINVAL;
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return RLT_EINVAL;
   // kernel limits
   if (c->head_dim % 8 != 0 || 128 % c->head_dim != 0) return RLT_EUNSUPPORTED;
@@ -1155,7 +1176,7 @@ int validate_cfg(const rlt_config* c) {
 
 extern "C" {
 
-int rlt_abi_version(void) { return 100; }
+int rlt_abi_version(void) { return 101; }
 
 uint64_t rlt_launch_count(void) { return g_launches.load(); }
 

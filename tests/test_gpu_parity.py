@@ -118,6 +118,31 @@ def test_small_bf16_parity(B, T):
     _check_bf16(g, o, emit)
 
 
+def test_per_layer_memory_variant_parity():
+    """Memory group l projected from encoder layer l's state (the other reading
+    of per-layer memory): fp32 tiny model with one group per layer, and the
+    small bf16 model, whole sequences against the oracle."""
+    wl, W, tok, acts = _inputs("tiny", B=4, T=24, mem_groups=2, mem_source=1)
+    emit = [0, 11, 23]
+    g = gpu_run(wl, W, tok, acts, emit=emit)
+    o = oracle_run(wl, W, tok, acts, emit=emit)
+    assert g["status"] == 0
+    for key in ("e", "mem", "s"):
+        assert np.abs(g[key] - o[key]).max() <= F32_ABS, key
+    for i in emit:
+        assert np.abs(g["logits"][i] - o["logits"][i]).max() <= F32_ABS
+    # the first group is not the final-e group (the variant is live)
+    o0 = oracle_run(*_inputs("tiny", B=4, T=24, mem_groups=2, mem_source=0), emit=[])
+    assert np.abs(o0["mem"][0] - g["mem"][0]).max() > 100 * F32_ABS
+    assert np.abs(o0["mem"][1] - g["mem"][1]).max() <= F32_ABS
+    wl, W, tok, acts = _inputs("small", B=3, T=37, mem_source=1)
+    emit = list(range(37))
+    g = gpu_run(wl, W, tok, acts, emit=emit)
+    o = oracle_run(wl, W, tok, acts, emit=emit)
+    assert g["status"] == 0
+    _check_bf16(g, o, emit)
+
+
 def test_small_bf16_full_size_sampled_rows():
     """Full small workload (B=64, T=512) on the GPU; sequences 0, 21, 42, 63 against the oracle."""
     wl, W, tok, acts = _inputs("small", jitter=0.0)

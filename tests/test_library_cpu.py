@@ -44,7 +44,7 @@ def test_library_is_built_for_sm_103a():
 
 def test_abi_version_and_strerror():
     import recurrent_looped_transformer_rlt_b300 as rlt
-    assert rlt.rlt_abi_version() == 100
+    assert rlt.rlt_abi_version() == 101
     assert rlt.rlt_strerror(rlt.RLT_ESTALE).startswith("state built")
     assert rlt.rlt_strerror(12345) == "unknown error"
 
@@ -56,6 +56,8 @@ def test_abi_version_and_strerror():
     ("head_dim", 24, -1),        # d mismatch first
     ("gate_mode", 5, -1),
     ("vocab", 0, -1),
+    ("mem_source", 2, -1),
+    ("mem_source", 1, -1),       # per-layer memory needs one group per layer (tiny has G = 1, L = 2)
 ])
 def test_model_create_rejects_bad_config_without_gpu(field, value, code):
     import recurrent_looped_transformer_rlt_b300 as rlt
