@@ -230,6 +230,40 @@ RLT_API int rlt_cross_attention_noalloc(const float* q, const void* mem_k, const
                                         int32_t n_heads, int32_t head_dim, int32_t dtype, int32_t T_mem,
                                         int32_t t, void* out, rlt_stream_t stream);
 
+/* Exact prefix snapshots ("Recurrent Looped Transformer: A New Architecture
+ * for Infinite Context Reasoning", "Training and Serving Considerations";
+ * "Princeton Researcher Proposes Recurrent Looped Transformer ...",
+ * training and serving paragraph): what a multi-turn server keeps to resume a
+ * prefix - the encoder's output and memory, the whole decoder state, the
+ * position, the window convention and the weight version - and may reuse
+ * across requests because the state does not depend on how the computation
+ * was split; a weight update invalidates it.
+ *
+ * A snapshot of a state at position pos holds everything needed to continue
+ * decoding from there: s_pos, both window caches (ring slots by position mod
+ * W, W recorded), pos, and the encoder output e and memory M of positions
+ * 1..pos, tagged with the model version and shape.  Restoring it and decoding on gives
+ * bit-identical states and log-probabilities to never having stopped
+ * (Proposition 3.1), also for another request that shares the prefix (the
+ * encoder and memory of positions <= pos depend only on those tokens).
+ *   snap: caller-owned device buffer of rlt_snapshot_size(m, B, pos) bytes,
+ *         16-byte aligned; layout private to the library (a header, then s,
+ *         ring K, ring V, e [B][pos][d], M [G][2][B][H][pos][hd]).
+ *   e [B][T_mem][d] and mem [G][2][B][H][T_mem][hd]: the encoder buffers of
+ *         rlt_encode; save reads and restore writes their rows 0..pos-1.
+ * rlt_snapshot_save copies asynchronously on the stream (nothing is read on
+ * the host).  rlt_snapshot_restore reads the snapshot's header (it
+ * synchronises the stream for that), checks it against the model and the
+ * state, then copies asynchronously and sets st->pos and st->version.
+ * Errors: RLT_EINVAL (null or misaligned pointer, buffer too small, batch or
+ * shape mismatch, pos > T_mem, not a snapshot), RLT_ESTALE (the snapshot, or
+ * st for save, was taken under another model version). */
+RLT_API int rlt_snapshot_size(const rlt_model* m, int32_t B, int32_t pos, size_t* bytes);
+RLT_API int rlt_snapshot_save(const rlt_model* m, const rlt_state* st, const void* e, const void* mem,
+                              int32_t T_mem, void* snap, size_t snap_bytes, rlt_stream_t stream);
+RLT_API int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t snap_bytes, rlt_state* st,
+                                 void* e, void* mem, int32_t T_mem, rlt_stream_t stream);
+
 /* Synchronises the stream, returns the device status recorded in the workspace
  * (RLT_OK, RLT_ETIMEOUT or RLT_EBOUNDS) and clears it. */
 RLT_API int rlt_status(void* ws, rlt_stream_t stream);

@@ -83,6 +83,11 @@ _cross_attention_noalloc = _sig("rlt_cross_attention_noalloc", ctypes.c_int,
                                 [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p])
 _linear = _sig("rlt_linear", ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _i32, _i32, _p, _i32, _p,
                                           ctypes.c_size_t, _p])
+_snapshot_size = _sig("rlt_snapshot_size", ctypes.c_int, [_p, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)])
+_snapshot_save = _sig("rlt_snapshot_save", ctypes.c_int,
+                      [_p, ctypes.POINTER(rlt_state), _p, _p, _i32, _p, ctypes.c_size_t, _p])
+_snapshot_restore = _sig("rlt_snapshot_restore", ctypes.c_int,
+                         [_p, _p, ctypes.c_size_t, ctypes.POINTER(rlt_state), _p, _p, _i32, _p])
 _timer_arm = _sig("rlt_timer_arm", ctypes.c_int, [_p, _i32, _i32])
 _timer_read = _sig("rlt_timer_read", ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_float), _i32, ctypes.POINTER(_i32)])
 _strerror = _sig("rlt_strerror", ctypes.c_char_p, [ctypes.c_int])
@@ -92,7 +97,8 @@ _abi_version = _sig("rlt_abi_version", ctypes.c_int, [])
 EXPORTED = ["rlt_model_create", "rlt_model_set_version", "rlt_model_destroy", "rlt_workspace_size",
             "rlt_workspace_init", "rlt_state_sizes", "rlt_state_init", "rlt_encode", "rlt_decode_steps",
             "rlt_status", "rlt_strerror", "rlt_launch_count", "rlt_abi_version", "rlt_timer_arm",
-            "rlt_timer_read", "rlt_cross_attention", "rlt_cross_attention_noalloc", "rlt_linear"]
+            "rlt_timer_read", "rlt_cross_attention", "rlt_cross_attention_noalloc", "rlt_linear",
+            "rlt_snapshot_size", "rlt_snapshot_save", "rlt_snapshot_restore"]
 RLT_TIMER_CLASSES = {"off": 0, "xattn": 1, "swa": 2, "gemm": 3, "head": 4, "step": 5}
 
 
@@ -189,6 +195,30 @@ def rlt_decode_steps(model: int, st: rlt_state, e, mem, T_mem: int, n: int, acti
                        _ptr(ws), ws_bytes, _stream_ptr(stream))
     if check:
         _check(rc, "rlt_decode_steps")
+    return rc
+
+
+def rlt_snapshot_size(model: int, B: int, pos: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_snapshot_size(model, B, pos, ctypes.byref(n)), "rlt_snapshot_size")
+    return n.value
+
+
+def rlt_snapshot_save(model: int, st: rlt_state, e, mem, T_mem: int, snap, snap_bytes: int, stream=None,
+                      check: bool = True) -> int:
+    rc = _snapshot_save(model, ctypes.byref(st), _ptr(e), _ptr(mem), T_mem, _ptr(snap), snap_bytes,
+                        _stream_ptr(stream))
+    if check:
+        _check(rc, "rlt_snapshot_save")
+    return rc
+
+
+def rlt_snapshot_restore(model: int, snap, snap_bytes: int, st: rlt_state, e, mem, T_mem: int, stream=None,
+                         check: bool = True) -> int:
+    rc = _snapshot_restore(model, _ptr(snap), snap_bytes, ctypes.byref(st), _ptr(e), _ptr(mem), T_mem,
+                           _stream_ptr(stream))
+    if check:
+        _check(rc, "rlt_snapshot_restore")
     return rc
 
 

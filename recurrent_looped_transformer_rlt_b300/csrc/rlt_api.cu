@@ -1235,6 +1235,137 @@ int rlt_model_create(const rlt_config* cfg, const rlt_weights* w, uint64_t versi
   return RLT_OK;
 }
 
+// ---------------------------------------------------------------------------
+// prefix snapshots
+
+namespace {
+
+// Header at the start of a snapshot (64 bytes), then s, ring K, ring V, e and
+// M, each section starting on a 256-byte boundary.
+struct SnapHeader {
+  uint32_t magic, abi;
+  uint64_t version;
+  int32_t B, pos, d, L, H, hd, W, G, dtype, mem_source;
+  int32_t pad[2];
+};
+static_assert(sizeof(SnapHeader) == 64, "snapshot header");
+constexpr uint32_t kSnapMagic = 0x534c5452u;  // "RTLS"
+
+struct SnapLayout {
+  size_t s, rk, rv, e, mem, total;
+  size_t s_bytes, ring_bytes, e_row, mem_row;  // e_row: pos * d elements, mem_row: pos * hd (bytes)
+  size_t mem_rows;                              // G * 2 * B * H
+};
+SnapLayout snap_layout(const rlt_model* m, int B, int pos) {
+  const rlt_config& c = m->cfg;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  SnapLayout L{};
+  L.s_bytes = (size_t)B * c.d_model * 4;
+  L.ring_bytes = (size_t)c.n_layers * B * c.n_heads * c.window * c.head_dim * m->esz;
+  L.e_row = (size_t)pos * c.d_model * m->esz;
+  L.mem_row = (size_t)pos * c.head_dim * m->esz;
+  L.mem_rows = (size_t)c.mem_groups * 2 * B * c.n_heads;
+  size_t off = up(sizeof(SnapHeader));
+  L.s = off;
+  off += up(L.s_bytes);
+  L.rk = off;
+  off += up(L.ring_bytes);
+  L.rv = off;
+  off += up(L.ring_bytes);
+  L.e = off;
+  off += up(L.e_row * B);
+  L.mem = off;
+  off += up(L.mem_row * L.mem_rows);
+  L.total = off;
+  return L;
+}
+
+__global__ void snap_header_kernel(SnapHeader* dst, SnapHeader h) { *dst = h; }
+
+}  // namespace
+
+int rlt_snapshot_size(const rlt_model* m, int32_t B, int32_t pos, size_t* bytes) {
+  if (!m || !bytes || B <= 0 || pos < 0) return RLT_EINVAL;
+  *bytes = snap_layout(m, B, pos).total;
+  return RLT_OK;
+}
+
+int rlt_snapshot_save(const rlt_model* m, const rlt_state* st, const void* e, const void* mem, int32_t T_mem,
+                      void* snap, size_t snap_bytes, rlt_stream_t stream) {
+  if (!m || !st || !snap || !aligned16(snap) || st->batch <= 0 || !st->s || !st->ring_k || !st->ring_v)
+    return RLT_EINVAL;
+  if (st->version != m->version) return RLT_ESTALE;
+  const int B = st->batch, pos = st->pos;
+  if (pos < 0 || (pos > 0 && (!e || !mem || T_mem < pos))) return RLT_EINVAL;
+  const SnapLayout L = snap_layout(m, B, pos);
+  if (snap_bytes < L.total) return RLT_EINVAL;
+  const rlt_config& c = m->cfg;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(snap);
+  SnapHeader h{};
+  h.magic = kSnapMagic;
+  h.abi = (uint32_t)rlt_abi_version();
+  h.version = m->version;
+  h.B = B;
+  h.pos = pos;
+  h.d = c.d_model;
+  h.L = c.n_layers;
+  h.H = c.n_heads;
+  h.hd = c.head_dim;
+  h.W = c.window;
+  h.G = c.mem_groups;
+  h.dtype = c.dtype;
+  h.mem_source = c.mem_source;
+  snap_header_kernel<<<1, 1, 0, s>>>(reinterpret_cast<SnapHeader*>(base), h);
+  g_launches++;
+  RLT_CUDA_TRY(cudaGetLastError());
+  RLT_CUDA_TRY(cudaMemcpyAsync(base + L.s, st->s, L.s_bytes, cudaMemcpyDeviceToDevice, s));
+  RLT_CUDA_TRY(cudaMemcpyAsync(base + L.rk, st->ring_k, L.ring_bytes, cudaMemcpyDeviceToDevice, s));
+  RLT_CUDA_TRY(cudaMemcpyAsync(base + L.rv, st->ring_v, L.ring_bytes, cudaMemcpyDeviceToDevice, s));
+  if (pos > 0) {
+    // rows 0..pos-1 of every sequence (e) and of every (group, K/V, sequence, head) plane (M)
+    RLT_CUDA_TRY(cudaMemcpy2DAsync(base + L.e, L.e_row, e, (size_t)T_mem * c.d_model * m->esz, L.e_row, B,
+                                   cudaMemcpyDeviceToDevice, s));
+    RLT_CUDA_TRY(cudaMemcpy2DAsync(base + L.mem, L.mem_row, mem, (size_t)T_mem * c.head_dim * m->esz, L.mem_row,
+                                   L.mem_rows, cudaMemcpyDeviceToDevice, s));
+  }
+  return RLT_OK;
+}
+
+int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t snap_bytes, rlt_state* st, void* e, void* mem,
+                         int32_t T_mem, rlt_stream_t stream) {
+  if (!m || !st || !snap || !aligned16(snap) || st->batch <= 0 || !st->s || !st->ring_k || !st->ring_v ||
+      snap_bytes < sizeof(SnapHeader))
+    return RLT_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  SnapHeader h{};
+  RLT_CUDA_TRY(cudaMemcpyAsync(&h, snap, sizeof(h), cudaMemcpyDeviceToHost, s));
+  RLT_CUDA_TRY(cudaStreamSynchronize(s));
+  const rlt_config& c = m->cfg;
+  if (h.magic != kSnapMagic || h.abi != (uint32_t)rlt_abi_version()) return RLT_EINVAL;
+  if (h.d != c.d_model || h.L != c.n_layers || h.H != c.n_heads || h.hd != c.head_dim || h.W != c.window ||
+      h.G != c.mem_groups || h.dtype != c.dtype || h.mem_source != c.mem_source || h.B != st->batch)
+    return RLT_EINVAL;
+  if (h.version != m->version) return RLT_ESTALE;
+  const int B = h.B, pos = h.pos;
+  if (pos < 0 || (pos > 0 && (!e || !mem || T_mem < pos))) return RLT_EINVAL;
+  const SnapLayout L = snap_layout(m, B, pos);
+  if (snap_bytes < L.total) return RLT_EINVAL;
+  const char* base = static_cast<const char*>(snap);
+  RLT_CUDA_TRY(cudaMemcpyAsync(st->s, base + L.s, L.s_bytes, cudaMemcpyDeviceToDevice, s));
+  RLT_CUDA_TRY(cudaMemcpyAsync(st->ring_k, base + L.rk, L.ring_bytes, cudaMemcpyDeviceToDevice, s));
+  RLT_CUDA_TRY(cudaMemcpyAsync(st->ring_v, base + L.rv, L.ring_bytes, cudaMemcpyDeviceToDevice, s));
+  if (pos > 0) {
+    RLT_CUDA_TRY(cudaMemcpy2DAsync(e, (size_t)T_mem * c.d_model * m->esz, base + L.e, L.e_row, L.e_row, B,
+                                   cudaMemcpyDeviceToDevice, s));
+    RLT_CUDA_TRY(cudaMemcpy2DAsync(mem, (size_t)T_mem * c.head_dim * m->esz, base + L.mem, L.mem_row, L.mem_row,
+                                   L.mem_rows, cudaMemcpyDeviceToDevice, s));
+  }
+  st->pos = pos;
+  st->version = h.version;
+  return RLT_OK;
+}
+
 int rlt_model_set_version(rlt_model* m, uint64_t version) {
   if (!m) return RLT_EINVAL;
   m->version = version;
