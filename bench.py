@@ -161,6 +161,15 @@ def max_over_ranks(values, world, device=None):
     return v.tolist()
 
 
+def workload_config(wl, world):
+    """The `config` object of the bench line (both arms)."""
+    c = wl.cfg
+    return {"workload": f"{wl.name}: d={c.d} L_E=L_D={c.n_layers} H={c.n_heads}x{c.head_dim} f={c.d_ffn}"
+                        f" W={c.window} G={c.mem_groups} V={c.vocab}",
+            "B_per_gpu": wl.B, "T": wl.T, "global_batch": wl.B * world, "parallelism": f"replicas{world}",
+            "l2": "flushed before every timed step (256 MB write)"}
+
+
 def job_throughput(B, T, world, t_step):
     """Whole-job decoder tokens/s: every rank's B x T tokens over the slowest
     rank's step time."""
@@ -350,7 +359,7 @@ def run_reference(args, rank):
             "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(dts)), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": f"{wl.name}: d={wl.cfg.d} L={wl.cfg.n_layers} B={wl.B} T={wl.T}"},
+            "config": workload_config(wl, args.gpus),
             "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -482,11 +491,7 @@ def main():
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * r["t_step"], 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.cfg.dtype, "data": "synthetic",
-            "config": {"workload": f"{wl.name}: d={wl.cfg.d} L_E=L_D={wl.cfg.n_layers} H={wl.cfg.n_heads}"
-                                   f"x{wl.cfg.head_dim} f={wl.cfg.d_ffn} W={wl.cfg.window} G={wl.cfg.mem_groups}"
-                                   f" V={wl.cfg.vocab}",
-                       "B_per_gpu": B, "T": T, "global_batch": B * world, "parallelism": f"replicas{world}",
-                       "l2": "flushed before every timed step (256 MB write)"},
+            "config": workload_config(wl, world),
             "decode_ms": round(1e3 * (r["t_step"] - r["t_enc"]), 3),
             "encode_ms": round(1e3 * r["t_enc"], 3),
             "decode_roofline_ms": round(1e3 * roof_s, 3),

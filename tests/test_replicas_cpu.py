@@ -81,3 +81,22 @@ def test_reference_arm_runs_on_rank_zero_only():
     with contextlib.redirect_stdout(buf):
         bench.run_reference(args, rank=1)
     assert buf.getvalue() == ""
+
+
+def test_reference_arm_line_has_the_gpu_arms_keys():
+    """The reference arm times the oracle on the host cores on the same
+    workload config, metric and unit as the GPU arm."""
+    import json
+    import bench
+    import rlt_inputs as ri
+    args = argparse.Namespace(workload="tiny", steps=1, warmup=0, gpus=1)
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.run_reference(args, rank=0)
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is True and line["value"] > 0
+    assert line["config"] == bench.workload_config(ri.preset("tiny"), 1)
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
