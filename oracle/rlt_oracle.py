@@ -410,6 +410,51 @@ def score(logits, actions, temperature=1.0, top_k=0):
     return lp, lp_full
 
 
+# ----------------------------------------------------------------------------
+# generation: drawing the next token ("Understanding and Applying the Recurrent
+# Looped Transformer Architecture", "Autoregressive generation": the
+# distribution of the next token comes from the preceding state, a token is
+# sampled from it, encoded incrementally and consumed once)
+
+_M64 = (1 << 64) - 1
+
+
+def uniform24(seed: int, b: int, pos: int) -> float:
+    """The uniform number in [0, 1) of draw (seed, sequence b, position pos):
+    the SplitMix64 output function (Steele, Lea and Flood, "Fast splittable
+    pseudorandom number generators", OOPSLA 2014) on the counter
+    seed + (pos * 2^32 + b + 1) * 0x9E3779B97F4A7C15 (mod 2^64), keeping the
+    top 24 bits.  Written from the published mixing function; the library has
+    its own copy (the two share no code, only the definition)."""
+    z = (seed + ((pos << 32) + b + 1) * 0x9E3779B97F4A7C15) & _M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    z ^= z >> 31
+    return (z >> 40) / float(1 << 24)
+
+
+def sampling_distribution(logits_row, temperature=1.0, top_k=0):
+    """Probabilities of the tempered (top-k) distribution over the vocabulary
+    (zero outside the top-k set, ties to the lower id), float64."""
+    x = np.asarray(logits_row, F64)[None, :] / temperature
+    mask = topk_mask(x, top_k)[0]
+    xm = np.where(mask, x[0], -np.inf)
+    p = np.exp(xm - np.max(xm))
+    return p / p.sum()
+
+
+def sample_token(logits_row, u, temperature=1.0, top_k=0):
+    """The token drawn with uniform number u: the first id, in id order, at
+    which the cumulative probability of the tempered (top-k) distribution
+    exceeds u (the last member when rounding leaves none)."""
+    p = sampling_distribution(logits_row, temperature, top_k)
+    c = np.cumsum(p)
+    hit = np.nonzero(c > u)[0]
+    if len(hit):
+        return int(hit[0])
+    return int(np.nonzero(p > 0)[0][-1])
+
+
 @dataclass
 class StepsOut:
     logp: np.ndarray            # [B, n]

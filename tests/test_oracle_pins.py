@@ -398,6 +398,49 @@ def test_bf16_mode_rounds_at_contract_points():
 
 
 # ---------------------------------------------------------------------------
+# generation: the draw of the next token
+
+def test_uniform24_is_uniform_and_independent():
+    from scipy import stats
+    u = np.array([O.uniform24(7, b, p) for b in range(40) for p in range(1000)])
+    assert u.min() >= 0.0 and u.max() < 1.0
+    assert np.all(u * 2 ** 24 == np.floor(u * 2 ** 24))           # 24-bit grid
+    assert stats.kstest(u, "uniform").pvalue > 1e-3
+    # neighbouring sequences, positions and seeds are uncorrelated
+    a = u.reshape(40, 1000)
+    assert abs(np.corrcoef(a[0], a[1])[0, 1]) < 0.1
+    assert abs(np.corrcoef(a[:, :-1].ravel(), a[:, 1:].ravel())[0, 1]) < 0.05
+    v = np.array([O.uniform24(8, b, p) for b in range(40) for p in range(1000)])
+    assert abs(np.corrcoef(u, v)[0, 1]) < 0.05 and not np.array_equal(u, v)
+    assert O.uniform24(7, 3, 5) == O.uniform24(7, 3, 5)
+
+
+def test_sample_token_inverts_the_cdf():
+    # two tokens with probabilities 1/4 and 3/4
+    lg = np.log(np.array([1.0, 3.0]))
+    assert O.sample_token(lg, 0.0) == 0 and O.sample_token(lg, 0.2499) == 0
+    assert O.sample_token(lg, 0.2501) == 1 and O.sample_token(lg, 0.9999) == 1
+    # top-1 is the argmax with the lowest id on ties; top-k >= V is the full distribution
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(50)
+    x[[7, 31]] = x.max() + 1.0
+    assert all(O.sample_token(x, u, 0.7, 1) == 7 for u in (0.0, 0.5, 0.999))
+    np.testing.assert_allclose(O.sampling_distribution(x, 0.7, 50), O.sampling_distribution(x, 0.7, 0))
+    # top-k support: exactly k tokens, the k largest
+    p = O.sampling_distribution(x, 0.7, 5)
+    assert (p > 0).sum() == 5 and set(np.nonzero(p)[0]) == set(np.argsort(-x, kind="stable")[:5])
+    # frequencies match the tempered softmax (chi-square)
+    from scipy import stats
+    x2 = rng.standard_normal(8)
+    p2 = O.sampling_distribution(x2, 1.3, 0)
+    q = scipy.special.softmax(x2 / 1.3)
+    np.testing.assert_allclose(p2, q, rtol=1e-12)
+    draws = np.array([O.sample_token(x2, O.uniform24(11, 0, i), 1.3) for i in range(20000)])
+    counts = np.bincount(draws, minlength=8)
+    assert stats.chisquare(counts, 20000 * q).pvalue > 1e-4
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: each must make at least one pin above fail
 
 def _fails(fn, *a, **kw):
