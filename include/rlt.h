@@ -230,6 +230,36 @@ RLT_API int rlt_cross_attention_noalloc(const float* q, const void* mem_k, const
                                         int32_t n_heads, int32_t head_dim, int32_t dtype, int32_t T_mem,
                                         int32_t t, void* out, rlt_stream_t stream);
 
+/* Generation ("Understanding and Applying the Recurrent Looped Transformer
+ * Architecture", "Prompt prefill" and "Autoregressive generation"): the
+ * prompt is encoded token-parallel and consumed by the decoder; then each new
+ * token is drawn from the current state's distribution, encoded
+ * incrementally against the encoder's key/value cache, and consumed through
+ * the decoder exactly once.  bf16 models (RLT_EUNSUPPORTED otherwise).
+ *
+ * rlt_encode_kv: rlt_encode of positions 0..T-1 into buffers with room for
+ *   T_max positions, also keeping every encoder layer's keys (after RoPE) and
+ *   values: e [B][T_max][d], mem [G][2][B][H][T_max][hd], enc_kv
+ *   [L][2][B][H][T_max][hd], all dtype; workspace rlt_workspace_size(m, B,
+ *   T_max).  The prompt is then consumed with rlt_decode_steps(..., e, mem,
+ *   T_mem = T_max, n = T, ...).
+ * rlt_generate: from st (pos = p tokens consumed) draws, encodes and consumes
+ *   n tokens (positions p..p+n-1), writing them to tokens [B][n] and, when
+ *   logp is given, the log-probability of each under the distribution it was
+ *   drawn from (temperature, top-k as in rlt_decode_steps) to logp [B][n].
+ *   Draw i of sequence b uses the uniform number of (seed, b, position) - a
+ *   SplitMix64 counter - and the token is the first id, in id order, at which
+ *   the cumulative weight of the (top-k) set passes it; so the tokens do not
+ *   depend on how generation is split into calls.  Requires p + n <= T_max,
+ *   e / mem / enc_kv holding positions 0..p-1 (rlt_encode_kv, then earlier
+ *   rlt_generate calls); writes positions p..p+n-1 of them.  Errors as
+ *   rlt_decode_steps. */
+RLT_API int rlt_encode_kv(const rlt_model* m, const int32_t* tokens, int32_t B, int32_t T, int32_t T_max, void* e,
+                          void* mem, void* enc_kv, void* ws, size_t ws_bytes, rlt_stream_t stream);
+RLT_API int rlt_generate(const rlt_model* m, rlt_state* st, void* e, void* mem, void* enc_kv, int32_t T_max,
+                         int32_t n, uint64_t seed, float temperature, int32_t top_k, int32_t* tokens, float* logp,
+                         void* ws, size_t ws_bytes, rlt_stream_t stream);
+
 /* Exact prefix snapshots ("Recurrent Looped Transformer: A New Architecture
  * for Infinite Context Reasoning", "Training and Serving Considerations";
  * "Princeton Researcher Proposes Recurrent Looped Transformer ...",

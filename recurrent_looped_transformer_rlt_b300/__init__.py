@@ -83,6 +83,10 @@ _cross_attention_noalloc = _sig("rlt_cross_attention_noalloc", ctypes.c_int,
                                 [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p])
 _linear = _sig("rlt_linear", ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _i32, _i32, _p, _i32, _p,
                                           ctypes.c_size_t, _p])
+_encode_kv = _sig("rlt_encode_kv", ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _p, _p, ctypes.c_size_t, _p])
+_generate = _sig("rlt_generate", ctypes.c_int,
+                 [_p, ctypes.POINTER(rlt_state), _p, _p, _p, _i32, _i32, ctypes.c_uint64, ctypes.c_float, _i32, _p,
+                  _p, _p, ctypes.c_size_t, _p])
 _snapshot_size = _sig("rlt_snapshot_size", ctypes.c_int, [_p, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)])
 _snapshot_save = _sig("rlt_snapshot_save", ctypes.c_int,
                       [_p, ctypes.POINTER(rlt_state), _p, _p, _i32, _p, ctypes.c_size_t, _p])
@@ -98,7 +102,7 @@ EXPORTED = ["rlt_model_create", "rlt_model_set_version", "rlt_model_destroy", "r
             "rlt_workspace_init", "rlt_state_sizes", "rlt_state_init", "rlt_encode", "rlt_decode_steps",
             "rlt_status", "rlt_strerror", "rlt_launch_count", "rlt_abi_version", "rlt_timer_arm",
             "rlt_timer_read", "rlt_cross_attention", "rlt_cross_attention_noalloc", "rlt_linear",
-            "rlt_snapshot_size", "rlt_snapshot_save", "rlt_snapshot_restore"]
+            "rlt_snapshot_size", "rlt_snapshot_save", "rlt_snapshot_restore", "rlt_encode_kv", "rlt_generate"]
 RLT_TIMER_CLASSES = {"off": 0, "xattn": 1, "swa": 2, "gemm": 3, "head": 4, "step": 5}
 
 
@@ -195,6 +199,20 @@ def rlt_decode_steps(model: int, st: rlt_state, e, mem, T_mem: int, n: int, acti
                        _ptr(ws), ws_bytes, _stream_ptr(stream))
     if check:
         _check(rc, "rlt_decode_steps")
+    return rc
+
+
+def rlt_encode_kv(model: int, tokens, B: int, T: int, T_max: int, e, mem, enc_kv, ws, ws_bytes: int, stream=None):
+    _check(_encode_kv(model, _ptr(tokens), B, T, T_max, _ptr(e), _ptr(mem), _ptr(enc_kv), _ptr(ws), ws_bytes,
+                      _stream_ptr(stream)), "rlt_encode_kv")
+
+
+def rlt_generate(model: int, st: rlt_state, e, mem, enc_kv, T_max: int, n: int, seed: int, temperature: float,
+                 top_k: int, tokens, logp, ws, ws_bytes: int, stream=None, check: bool = True) -> int:
+    rc = _generate(model, ctypes.byref(st), _ptr(e), _ptr(mem), _ptr(enc_kv), T_max, n, seed, temperature, top_k,
+                   _ptr(tokens), _ptr(logp), _ptr(ws), ws_bytes, _stream_ptr(stream))
+    if check:
+        _check(rc, "rlt_generate")
     return rc
 
 

@@ -38,10 +38,26 @@ template <typename T>
 struct EpiMemScatter {
   T* dst;
   int T_len, H, hd;
+  int T_stride = 0;  // positions per (b, h) plane row of dst; 0: T_len
   __device__ __forceinline__ void operator()(int m, int n, float v) const {
     int b = m / T_len, t = m - b * T_len;
     int h = n / hd, i = n - h * hd;
-    dst[(((size_t)b * H + h) * T_len + t) * hd + i] = from_f32<T>(v);
+    const int ts = T_stride ? T_stride : T_len;
+    dst[(((size_t)b * H + h) * ts + t) * hd + i] = from_f32<T>(v);
+  }
+};
+
+// Memory keys or values of one position (incremental encoding): row m = b,
+// column n = h*hd + i, written to dst[b][h][ctx->pos][i] of a plane with
+// T_stride positions.
+template <typename T>
+struct EpiMemRow {
+  T* dst;
+  int T_stride, H, hd;
+  const StepCtx* ctx;
+  __device__ __forceinline__ void operator()(int m, int n, float v) const {
+    const int h = n / hd, i = n - h * hd;
+    dst[(((size_t)m * H + h) * T_stride + ctx->pos) * hd + i] = from_f32<T>(v);
   }
 };
 

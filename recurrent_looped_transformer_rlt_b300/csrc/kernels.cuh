@@ -372,6 +372,92 @@ __device__ __forceinline__ unsigned f2key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Draws a token from the tempered distribution over the set S: every token
+// (all), or the top-k set - keys (f2key of the tempered logit) above kth, and
+// the first `need` tokens in id order whose key equals kth.  The weights
+// exp(x - mx) are accumulated in token-id order in a fixed fp32 order: thread
+// t sums the contiguous id chunk [t C, (t + 1) C), thread 0 adds the chunk
+// sums up and finds the chunk where the running sum passes u times the total,
+// and that chunk's thread walks its ids to the first one whose running sum
+// exceeds it (the chunk's last member when rounding leaves none).  All threads
+// of the block call it; it returns the token in every thread.
+__device__ int sample_chunked(const float* sx, int V, float mx, bool all, unsigned kth, unsigned need, float u,
+                              float* s_part, unsigned* s_tie, int* s_res) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int C = (V + nthr - 1) / nthr;
+  const int v0 = min(V, tid * C), v1 = min(V, v0 + C);
+  unsigned ties = 0;
+  if (!all)
+    for (int v = v0; v < v1; ++v) ties += (f2key(sx[v]) == kth) ? 1u : 0u;
+  s_tie[tid] = ties;
+  __syncthreads();
+  if (tid == 0) {  // s_tie[t] := ties at kth in the chunks before t
+    unsigned acc = 0;
+    for (int t = 0; t < nthr; ++t) {
+      const unsigned c = s_tie[t];
+      s_tie[t] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  auto member = [&](unsigned kk, unsigned& tb) {
+    if (all || kk > kth) return true;
+    if (kk != kth) return false;
+    return tb++ < need;
+  };
+  unsigned tb = s_tie[tid];
+  float sum = 0.f;
+  for (int v = v0; v < v1; ++v)
+    if (member(f2key(sx[v]), tb)) sum += expf(sx[v] - mx);
+  s_part[tid] = sum;
+  __syncthreads();
+  if (tid == 0) {
+    s_res[4] = 0;  // kept only if no chunk holds a member (non-finite logits)
+    float tot = 0.f;
+    for (int t = 0; t < nthr; ++t) tot += s_part[t];
+    const float target = u * tot;
+    float run = 0.f;
+    int tstar = -1, tlast = -1;
+    for (int t = 0; t < nthr; ++t) {
+      if (s_part[t] > 0.f) tlast = t;
+      if (tstar < 0) {
+        if (s_part[t] > 0.f && run + s_part[t] > target)
+          tstar = t;
+        else
+          run += s_part[t];
+      }
+    }
+    int last = 0;
+    if (tstar < 0) {  // rounding: the last member overall
+      tstar = tlast;
+      last = 1;
+    }
+    s_res[0] = tstar;
+    s_res[1] = last;
+    s_res[2] = __float_as_int(run);
+    s_res[3] = __float_as_int(target);
+  }
+  __syncthreads();
+  if (s_res[0] >= 0 && tid == s_res[0]) {
+    const bool last = s_res[1] != 0;
+    float run = __int_as_float(s_res[2]);
+    const float target = __int_as_float(s_res[3]);
+    unsigned tb2 = s_tie[tid];
+    int pick = -1, lastm = -1;
+    for (int v = v0; v < v1; ++v) {
+      if (!member(f2key(sx[v]), tb2)) continue;
+      lastm = v;
+      if (!last && pick < 0) {
+        run += expf(sx[v] - mx);
+        if (run > target) pick = v;
+      }
+    }
+    if (pick >= 0 || lastm >= 0) s_res[4] = pick >= 0 ? pick : lastm;
+  }
+  __syncthreads();
+  return min(max(s_res[4], 0), V - 1);
+}
+
 struct HeadArgs {
   const float* logits;     // [B][V] fp32 (this step)
   const int* actions;      // [B][n] or null
@@ -383,7 +469,30 @@ struct HeadArgs {
   int B, V, n, top_k;
   float inv_temp;
   int* status;
+  // sampling (generation): with next_tok set, the action is drawn from the
+  // tempered (top-k) distribution instead of read from actions, with the
+  // uniform draw of position ctx->pos + sample_off (the drawn token's
+  // position); it goes to next_tok[b] and, when step + sample_off < n, to
+  // sample_tok[b][step + sample_off] with its log-probabilities at the same
+  // index
+  int* next_tok;           // [B] or null
+  int* sample_tok;         // [B][n] or null
+  int sample_off;
+  unsigned long long seed;
 };
+
+// Uniform draw in [0, 1) with 24 random bits for (seed, sequence b, position
+// pos): the SplitMix64 output function (Steele, Lea and Flood, "Fast
+// splittable pseudorandom number generators", 2014) applied to the counter
+// seed + (pos * 2^32 + b + 1) * golden gamma.  Depends on the absolute
+// position, not on how generation is split into calls.
+__device__ __forceinline__ float uniform24(unsigned long long seed, int b, int pos) {
+  unsigned long long z = seed + (((unsigned long long)(unsigned)pos << 32) + (unsigned)b + 1ull) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return (float)(z >> 40) * (1.0f / 16777216.0f);
+}
 
 __global__ void __launch_bounds__(1024) head_reduce_kernel(HeadArgs a, const StepCtx* ctx) {
   pdl_wait();
@@ -393,6 +502,9 @@ __global__ void __launch_bounds__(1024) head_reduce_kernel(HeadArgs a, const Ste
   __shared__ float fred[32];
   __shared__ int ired[32];
   __shared__ unsigned s_prefix, s_remain, s_cnt;
+  __shared__ float s_part[1024];   // sampling: per-thread sums of its id chunk
+  __shared__ unsigned s_tie[1024];  // sampling: per-thread count of ties at the k-th key
+  __shared__ int s_res[5];
   const int b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
   const int i = ctx->step;
@@ -439,14 +551,20 @@ __global__ void __launch_bounds__(1024) head_reduce_kernel(HeadArgs a, const Ste
   __syncthreads();
   const float lse = mx + logf(fred[0]);
   __syncthreads();
-  int act = a.actions ? a.actions[(size_t)b * a.n + i] : -1;
+  const bool sampling = a.next_tok != nullptr;
+  int act = (!sampling && a.actions) ? a.actions[(size_t)b * a.n + i] : -1;
   if (act >= a.V) {
     if (tid == 0) set_error(a.status, kErrBounds);
     act = -1;
   }
+  const bool topk = a.top_k > 0 && a.top_k < a.V;
+  if (sampling && !topk) {
+    act = sample_chunked(sx, a.V, mx, true, 0u, 0u, uniform24(a.seed, b, ctx->pos + a.sample_off), s_part, s_tie,
+                         s_res);
+  }
   float lp_full = (act >= 0) ? sx[act] - lse : NAN;
   float lp = lp_full;
-  if (a.top_k > 0 && a.top_k < a.V) {
+  if (topk) {
     // radix select of the k-th largest key, 8 bits at a time from the top
     if (tid == 0) { s_prefix = 0; s_remain = (unsigned)a.top_k; }
     for (int pass = 0; pass < 4; ++pass) {
@@ -475,6 +593,11 @@ __global__ void __launch_bounds__(1024) head_reduce_kernel(HeadArgs a, const Ste
     const unsigned kth = s_prefix;          // exact key of the k-th largest value
     const unsigned need = s_remain;         // ties at kth taken, lowest ids first
     const float xk = sx[0] * 0.f + __uint_as_float((kth & 0x80000000u) ? (kth & 0x7fffffffu) : ~kth);
+    if (sampling) {
+      act = sample_chunked(sx, a.V, mx, false, kth, need, uniform24(a.seed, b, ctx->pos + a.sample_off), s_part,
+                           s_tie, s_res);
+      lp_full = sx[act] - lse;
+    }
     float sg = 0.f;
     for (int v = tid; v < a.V; v += nthr) {
       unsigned kk = f2key(sx[v]);
@@ -505,11 +628,50 @@ __global__ void __launch_bounds__(1024) head_reduce_kernel(HeadArgs a, const Ste
     }
   }
   if (tid == 0) {
-    size_t o = (size_t)b * a.n + i;
-    if (a.logp) a.logp[o] = lp;
-    if (a.logp_full) a.logp_full[o] = lp_full;
-    if (a.argmax) a.argmax[o] = amax;
+    if (sampling) {
+      a.next_tok[b] = act;
+      const int j = i + a.sample_off;
+      if (j < a.n) {
+        const size_t o = (size_t)b * a.n + j;
+        if (a.sample_tok) a.sample_tok[o] = act;
+        if (a.logp) a.logp[o] = lp;
+        if (a.logp_full) a.logp_full[o] = lp_full;
+        if (a.argmax) a.argmax[o] = amax;
+      }
+    } else {
+      const size_t o = (size_t)b * a.n + i;
+      if (a.logp) a.logp[o] = lp;
+      if (a.logp_full) a.logp_full[o] = lp_full;
+      if (a.argmax) a.argmax[o] = amax;
+    }
   }
+}
+
+// Per-row sums of squares of h [rows][d] in 128-column groups, ss[g][r], with
+// the same lane mapping and warp reduction as the residual epilogue of the
+// projections (so that an RMSNorm from them is bitwise the in-step one).
+// One warp per (row, group); blockDim 128.
+__global__ void row_ss_kernel(const float* __restrict__ h, float* __restrict__ ss, int rows, int d) {
+  const int lane = threadIdx.x & 31;
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int groups = d / 128;
+  if (wid >= rows * groups) return;
+  const int r = wid / groups, g = wid - r * groups;
+  const float4 v = *reinterpret_cast<const float4*>(h + (size_t)r * d + g * 128 + lane * 4);
+  const float q2 = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+  if (lane == 0) ss[(size_t)g * rows + r] = q2;
+}
+
+// e[b][pos][:] = x[b][:] (bf16 rows, pos = ctx->pos), pos < T.
+__global__ void put_row_kernel(const bf16* __restrict__ x, bf16* __restrict__ e, int B, int d, int T,
+                               const StepCtx* ctx) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_trigger();
+  const int b = blockIdx.x;
+  const int p = ctx->pos;
+  if (b >= B || p >= T) return;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8)
+    *reinterpret_cast<uint4*>(e + ((size_t)b * T + p) * d + c) = *reinterpret_cast<const uint4*>(x + (size_t)b * d + c);
 }
 
 __global__ void advance_kernel(StepCtx* ctx) {

@@ -91,7 +91,7 @@ namespace {
 struct WsLayout {
   size_t status, ctx, emit, rope;  // header
   // decoder
-  size_t d_h, d_x, d_m, d_c, d_o, d_part, d_cnt, d_ss, d_s16;
+  size_t d_h, d_x, d_m, d_c, d_o, d_part, d_cnt, d_ss, d_s16, d_tok;
   // encoder
   size_t e_h, e_a, e_m, e_c, e_q, e_k, e_v, e_o, e_ss;
   size_t total;
@@ -128,6 +128,7 @@ WsLayout layout(const rlt_model* m, int B, int T) {
   L.d_cnt = take(sizeof(int) * (size_t)B * H);
   L.d_ss = take(4 * (size_t)B * ((d + 127) / 128));
   L.d_s16 = take(es * (size_t)B * d);
+  L.d_tok = take(sizeof(int) * (size_t)B);
   const size_t dec_end = off;
   // encoder region overlaps the decoder region (one call at a time per workspace)
   off = common_end;
@@ -542,8 +543,13 @@ int enc_attention_bf16(cudaStream_t st, const bf16* q, const bf16* k, const bf16
 // into them (the residual producers write x = bf16(h * g_next) and row sums of
 // squares; the consumers scale their output rows), RoPE and the head-major
 // q/k/v layout in the QKV epilogue, SwiGLU in the W_1/W_3 epilogue.
+// Token-parallel encoder of bf16 models.  e [B][T_stride][d] and mem
+// [G][2][B][H][T_stride][hd] receive positions 0..T-1 (T_stride >= T); with
+// enc_kv [L][2][B][H][T_stride][hd], every layer's keys (after RoPE) and
+// values are kept for incremental encoding.
 int encode_bf16(const rlt_model* m, const int32_t* tok, int B, int T, bf16* e, bf16* mem, void* ws,
-                cudaStream_t st) {
+                cudaStream_t st, int T_stride = 0, bf16* enc_kv = nullptr) {
+  if (T_stride <= 0) T_stride = T;
   const rlt_config& c = m->cfg;
   const rlt_weights& w = m->w;
   const int d = c.d_model, f = c.d_ffn, H = c.n_heads, hd = c.head_dim, L = c.n_layers, G = c.mem_groups;
@@ -561,16 +567,20 @@ int encode_bf16(const rlt_model* m, const int32_t* tok, int B, int T, bf16* e, b
   float* ss = at<float>(ws, Lw.e_ss);
   const TcScratch sc = tc_scratch(m, ws, Lw);
   int rc;
-  // memory group g (keys and values, [B][H][T][hd] each) from the source rows src [R][d]
-  const size_t plane = (size_t)B * H * T * hd;
+  // memory group g (keys and values, [B][H][T_stride][hd] each) from the source rows src [R][d]
+  const size_t plane = (size_t)B * H * T_stride * hd;
   auto mem_proj_bf16 = [&](cudaStream_t s_, const bf16* src, int g) -> int {
     const bf16* WK = wl<bf16>(w.W_K, g, (size_t)d * d);
     const bf16* WV = wl<bf16>(w.W_V, g, (size_t)d * d);
     int r;
-    if ((r = gemm_bf16_tc(s_, src, d, R, d, WK, d, d, EpiMemScatter<bf16>{mem + (2 * g) * plane, T, H, hd}, sc)))
+    if ((r = gemm_bf16_tc(s_, src, d, R, d, WK, d, d, EpiMemScatter<bf16>{mem + (2 * g) * plane, T, H, hd, T_stride},
+                          sc)))
       return r;
-    return gemm_bf16_tc(s_, src, d, R, d, WV, d, d, EpiMemScatter<bf16>{mem + (2 * g + 1) * plane, T, H, hd}, sc);
+    return gemm_bf16_tc(s_, src, d, R, d, WV, d, d,
+                        EpiMemScatter<bf16>{mem + (2 * g + 1) * plane, T, H, hd, T_stride}, sc);
   };
+  // e rows go straight to e when they are contiguous, else through x and a copy
+  bf16* e_rows = (T_stride == T) ? e : x;
   rope_table_kernel<<<cdiv((size_t)T * (hd / 2), 256), 256, 0, st>>>(tab, 0, T, hd / 2, (double)c.rope_theta);
   g_launches++;
   embed_norm_kernel<<<R, d / 4, 0, st>>>(tok, static_cast<const bf16*>(w.tok_emb), h, x, w.enc_attn_norm, R, d,
@@ -581,6 +591,13 @@ int encode_bf16(const rlt_model* m, const int32_t* tok, int B, int T, bf16* e, b
     const bf16* Wqkv = wl<bf16>(w.W_qkv, l, (size_t)3 * d * d);
     if ((rc = gemm_bf16_tc(st, x, d, R, d, Wqkv, d, 3 * d, EpiEncQKVRope<bf16>{q, k, v, tab, d, H, hd, T}, sc)))
       return rc;
+    if (enc_kv) {  // keep this layer's keys and values: [B*H] rows of T positions into T_stride
+      const size_t kvp = (size_t)B * H * T_stride * hd, row = (size_t)T * hd * 2;
+      RLT_CUDA_TRY(cudaMemcpy2DAsync(enc_kv + (2 * l) * kvp, (size_t)T_stride * hd * 2, k, row, row,
+                                     (size_t)B * H, cudaMemcpyDeviceToDevice, st));
+      RLT_CUDA_TRY(cudaMemcpy2DAsync(enc_kv + (2 * l + 1) * kvp, (size_t)T_stride * hd * 2, v, row, row,
+                                     (size_t)B * H, cudaMemcpyDeviceToDevice, st));
+    }
     if ((rc = enc_attention_bf16(st, q, k, v, o, B, T, H, hd))) return rc;
     const bf16* WO = wl<bf16>(w.W_O, l, (size_t)d * d);
     if ((rc = gemm_bf16_tc(st, o, d, R, d, WO, d, d, EpiResidual{HOut{h, d, nullptr, nullptr, ss, R}}, sc))) return rc;
@@ -598,12 +615,15 @@ int encode_bf16(const rlt_model* m, const int32_t* tok, int B, int T, bf16* e, b
     }
     // RMSNorm of the next layer's attention, or the final norm producing e
     if ((rc = norm_rows(st, h, ss, (l + 1 < L) ? w.enc_attn_norm + (size_t)(l + 1) * d : w.enc_norm,
-                        (l + 1 < L) ? x : e, R, d, c.rms_eps)))
+                        (l + 1 < L) ? x : e_rows, R, d, c.rms_eps)))
       return rc;
   }
-  if (c.mem_source == RLT_MEM_PER_LAYER) return mem_proj_bf16(st, e, L - 1);  // the last layer's source is e
+  if (e_rows != e)
+    RLT_CUDA_TRY(cudaMemcpy2DAsync(e, (size_t)T_stride * d * 2, e_rows, (size_t)T * d * 2, (size_t)T * d * 2, B,
+                                   cudaMemcpyDeviceToDevice, st));
+  if (c.mem_source == RLT_MEM_PER_LAYER) return mem_proj_bf16(st, e_rows, L - 1);  // the last layer's source is e
   for (int g = 0; g < G; ++g)
-    if ((rc = mem_proj_bf16(st, e, g))) return rc;
+    if ((rc = mem_proj_bf16(st, e_rows, g))) return rc;
   return RLT_OK;
 }
 
@@ -686,6 +706,10 @@ struct DecodeArgs {
   int32_t* argmax;
   float* logits;
   int n_emit;
+  // generation: sample the next token instead of scoring actions
+  int* next_tok = nullptr;
+  int* sample_tok = nullptr;
+  unsigned long long seed = 0;
 };
 
 template <typename T_>
@@ -1055,6 +1079,10 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
   ha.top_k = A.top_k;
   ha.inv_temp = A.inv_temp;
   ha.status = status;
+  ha.next_tok = A.next_tok;
+  ha.sample_tok = A.sample_tok;
+  ha.sample_off = 1;  // the token drawn from s_{p+1} is the one at position p + 1
+  ha.seed = A.seed;
   if ((rc = launch_pdl(head_reduce_kernel, dim3(B), dim3(1024), sizeof(float) * V, st, ha, (const StepCtx*)ctx)))
     return rc;
   if ((rc = post())) return rc;
@@ -1063,6 +1091,238 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
   if ((rc = post())) return rc;
   if ((rc = mark(RLT_TIMER_STEP))) return rc;
   *n_kernels = nk;
+  return RLT_OK;
+}
+
+// One incremental encoder step of bf16 models (generation): the token
+// next_tok[b] of every sequence, at position p = ctx->pos, through the
+// encoder layers with its keys and values appended to the encoder cache
+// enc_kv [L][2][B][H][T_max][hd], then e[:, p] and the memory rows of p.  The
+// projections and norms follow the token-parallel encoder's numerics; the
+// attention over the cached positions 0..p is the decoder's streaming kernel
+// (fp32 online softmax), where the token-parallel encoder rounds P to bf16 on
+// the final row maximum.  Uses the decoder scratch of the workspace.
+int enqueue_enc_step_bf16(const rlt_model* m, int B, int T_max, bf16* e, bf16* mem, bf16* enc_kv, void* ws,
+                          const WsLayout& Lw, cudaStream_t st, int* n_kernels) {
+  const rlt_config& c = m->cfg;
+  const rlt_weights& w = m->w;
+  const int d = c.d_model, f = c.d_ffn, H = c.n_heads, hd = c.head_dim, L = c.n_layers, G = c.mem_groups;
+  StepCtx* ctx = at<StepCtx>(ws, Lw.ctx);
+  int* status = at<int>(ws, Lw.status);
+  const float2* tab = at<float2>(ws, Lw.rope);
+  const int* tok = at<int>(ws, Lw.d_tok);
+  float* h = at<float>(ws, Lw.d_h);
+  bf16* x = at<bf16>(ws, Lw.d_x);
+  bf16* xm = at<bf16>(ws, Lw.d_m);
+  float* C = at<float>(ws, Lw.d_c);
+  bf16* o = at<bf16>(ws, Lw.d_o);
+  float* ss = at<float>(ws, Lw.d_ss);
+  const TcScratch sc = tc_scratch(m, ws, Lw);
+  auto act = [](const bf16* p, int ld) {
+    AArg a;
+    a.A = p;
+    a.lda = ld;
+    return a;
+  };
+  int rc, nk = 0;
+  const size_t kvp = (size_t)B * H * T_max * hd;   // one K or V plane of the encoder cache
+  const size_t mplane = (size_t)B * H * T_max * hd;  // one K or V plane of the memory
+  // memory rows of position p for group g from the normed rows src [B][d]
+  auto mem_rows = [&](const bf16* src, int g) -> int {
+    int r;
+    if ((r = proj_bf16<false>(st, act(src, d), B, d, wl<bf16>(w.W_K, g, (size_t)d * d), nullptr, d, d,
+                              EpiMemRow<bf16>{mem + (2 * g) * mplane, T_max, H, hd, ctx}, sc)))
+      return r;
+    nk++;
+    if ((r = proj_bf16<false>(st, act(src, d), B, d, wl<bf16>(w.W_V, g, (size_t)d * d), nullptr, d, d,
+                              EpiMemRow<bf16>{mem + (2 * g + 1) * mplane, T_max, H, hd, ctx}, sc)))
+      return r;
+    nk++;
+    return RLT_OK;
+  };
+  auto norm = [&](const float* g, bf16* out) -> int {
+    nk++;
+    return norm_rows(st, h, ss, g, out, B, d, c.rms_eps);
+  };
+  embed_norm_kernel<<<B, d / 4, 0, st>>>(tok, static_cast<const bf16*>(w.tok_emb), h, x, w.enc_attn_norm, B, d,
+                                         c.vocab, c.rms_eps, status);
+  g_launches++;
+  nk++;
+  if ((rc = launch_ok())) return rc;
+  XattnArgs xa{};
+  xa.part = at<float>(ws, Lw.d_part);
+  xa.cnt = at<int>(ws, Lw.d_cnt);
+  xa.out = o;
+  xa.q = C;
+  xa.B = B;
+  xa.H = H;
+  xa.scale = 1.0f / sqrtf((float)hd);
+  xa.ctx = ctx;
+  xa.status = status;
+  for (int l = 0; l < L; ++l) {
+    bf16* kc = enc_kv + (2 * l) * kvp;
+    bf16* vc = enc_kv + (2 * l + 1) * kvp;
+    // q, k with RoPE at p; k, v appended at cache slot p
+    EpiQKVRope<bf16> eq{C, kc, vc, tab, ctx, d, H, hd, T_max};
+    if ((rc = proj_bf16<false>(st, act(x, d), B, d, wl<bf16>(w.W_qkv, l, (size_t)3 * d * d), nullptr, d, 3 * d, eq,
+                               sc)))
+      return rc;
+    nk++;
+    XattnArgs sa = xa;
+    sa.mk = kc;
+    sa.mv = vc;
+    sa.T_mem = T_max;
+    sa.t_cap = T_max;
+    sa.early = 2;  // slot p is written by the projection just before
+    if (launch_xattn<bf16>(sa, hd, m->n_sm, st) != cudaSuccess) return RLT_ECUDA;
+    g_launches++;
+    nk++;
+    if ((rc = launch_ok())) return rc;
+    if ((rc = proj_bf16<false>(st, act(o, d), B, d, wl<bf16>(w.W_O, l, (size_t)d * d), nullptr, d, d,
+                               EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc)))
+      return rc;
+    nk++;
+    if ((rc = norm(w.enc_ffn_norm + (size_t)l * d, x))) return rc;
+    if ((rc = proj_bf16<true>(st, act(x, d), B, d, wl<bf16>(w.W_1, l, (size_t)f * d), wl<bf16>(w.W_3, l, (size_t)f * d),
+                              d, f, EpiStoreT<bf16>{xm, f}, sc)))
+      return rc;
+    nk++;
+    if ((rc = proj_bf16<false>(st, act(xm, f), B, f, wl<bf16>(w.W_2, l, (size_t)d * f), nullptr, f, d,
+                               EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc)))
+      return rc;
+    nk++;
+    if (c.mem_source == RLT_MEM_PER_LAYER && l + 1 < L) {  // group l from this layer's output
+      if ((rc = norm(w.enc_norm, o))) return rc;
+      if ((rc = mem_rows(o, l))) return rc;
+    }
+    if (l + 1 < L && (rc = norm(w.enc_attn_norm + (size_t)(l + 1) * d, x))) return rc;
+  }
+  // e_p = RMSNorm_e(h), then the memory rows of p
+  if ((rc = norm(w.enc_norm, x))) return rc;
+  if ((rc = launch_pdl(put_row_kernel, dim3(B), dim3(128), 0, st, (const bf16*)x, e, B, d, T_max,
+                       (const StepCtx*)ctx)))
+    return rc;
+  g_launches++;
+  nk++;
+  if (c.mem_source == RLT_MEM_PER_LAYER) {
+    if ((rc = mem_rows(x, L - 1))) return rc;
+  } else {
+    for (int g = 0; g < G; ++g)
+      if ((rc = mem_rows(x, g))) return rc;
+  }
+  *n_kernels = nk;
+  return RLT_OK;
+}
+
+// Autoregressive generation of bf16 models ("Understanding and Applying the
+// Recurrent Looped Transformer Architecture", "Autoregressive generation"):
+// from the state's distribution draw a token, encode it incrementally,
+// consume it through the decoder exactly once; n times.  The first draw comes
+// from the state the call starts with (its head computed here, bitwise as a
+// step's head); each captured iteration then encodes and consumes the drawn
+// token and draws the next one.
+int gen_impl(const rlt_model* m, rlt_state* sst, bf16* e, bf16* mem, bf16* enc_kv, int T_max, int n,
+             unsigned long long seed, float inv_temp, int top_k, int32_t* tokens, float* logp, void* ws,
+             cudaStream_t st) {
+  const rlt_config& c = m->cfg;
+  const int B = sst->batch, d = c.d_model, V = c.vocab;
+  WsLayout Lw = layout(m, B, T_max);
+  const int p0 = sst->pos;
+  StepCtx* ctx = at<StepCtx>(ws, Lw.ctx);
+  int rc;
+  set_ctx_kernel<<<1, 1, 0, st>>>(ctx, p0);
+  g_launches++;
+  const int half = c.head_dim / 2;
+  rope_table_kernel<<<cdiv((size_t)n * half, 256), 256, 0, st>>>(at<float2>(ws, Lw.rope), p0, n, half,
+                                                                 (double)c.rope_theta);
+  g_launches++;
+  if ((rc = launch_ok())) return rc;
+  RLT_CUDA_TRY(cudaMemsetAsync(at<int>(ws, Lw.d_cnt), 0, sizeof(int) * (size_t)B * c.n_heads, st));
+  {
+    const size_t nn = (size_t)B * d;
+    to_bf16_kernel<<<cdiv(nn, 256), 256, 0, st>>>(sst->s, at<bf16>(ws, Lw.d_s16), nn);
+    g_launches++;
+  }
+  // first draw: head of s_{p0} (sums of squares as the residual epilogue
+  // makes them, so the normed input is bitwise the in-step one)
+  float* ss = at<float>(ws, Lw.d_ss);
+  bf16* x = at<bf16>(ws, Lw.d_x);
+  float* C = at<float>(ws, Lw.d_c);
+  row_ss_kernel<<<cdiv((size_t)B * (d / 128), 4), 128, 0, st>>>(sst->s, ss, B, d);
+  g_launches++;
+  if ((rc = launch_ok())) return rc;
+  if ((rc = norm_rows(st, sst->s, ss, m->w.head_norm, x, B, d, c.rms_eps))) return rc;
+  TcScratch sc = tc_scratch(m, ws, Lw);
+  {
+    AArg a;
+    a.A = x;
+    a.lda = d;
+    if ((rc = proj_bf16<false>(st, a, B, d, static_cast<const bf16*>(m->w.W_o), nullptr, d, V, EpiStoreF32{C, V},
+                               sc)))
+      return rc;
+  }
+  HeadArgs h0{};
+  h0.logits = C;
+  h0.logp = logp;
+  h0.B = B;
+  h0.V = V;
+  h0.n = n;
+  h0.top_k = top_k;
+  h0.inv_temp = inv_temp;
+  h0.status = at<int>(ws, Lw.status);
+  h0.next_tok = at<int>(ws, Lw.d_tok);
+  h0.sample_tok = tokens;
+  h0.sample_off = 0;
+  h0.seed = seed;
+  if ((rc = launch_pdl(head_reduce_kernel, dim3(B), dim3(1024), sizeof(float) * V, st, h0, (const StepCtx*)ctx)))
+    return rc;
+  g_launches++;
+  // one captured iteration: encode the drawn token at p, consume it, draw the next
+  DecodeArgs A;
+  A.e = e;
+  A.mem = mem;
+  A.T_mem = T_max;
+  A.n = n;
+  A.actions = nullptr;
+  A.inv_temp = inv_temp;
+  A.top_k = top_k;
+  A.logp = logp;
+  A.logp_full = nullptr;
+  A.argmax = nullptr;
+  A.logits = nullptr;
+  A.n_emit = 0;
+  A.next_tok = at<int>(ws, Lw.d_tok);
+  A.sample_tok = tokens;
+  A.seed = seed;
+  cudaStream_t cs = m->cap_stream;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  RLT_CUDA_TRY(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal));
+  int nk_e = 0, nk_d = 0;
+  const uint64_t before = g_launches.load();
+  rc = enqueue_enc_step_bf16(m, B, T_max, e, mem, enc_kv, ws, Lw, cs, &nk_e);
+  if (!rc) rc = enqueue_step_bf16(m, sst, A, ws, Lw, cs, &nk_d);
+  cudaError_t ce = cudaStreamEndCapture(cs, &graph);
+  g_launches.store(before);
+  if (rc) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (ce != cudaSuccess) return RLT_ECUDA;
+  ce = cudaGraphInstantiate(&exec, graph, 0);
+  if (ce != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return RLT_ECUDA;
+  }
+  for (int i = 0; i < n; ++i) {
+    ce = cudaGraphLaunch(exec, st);
+    if (ce != cudaSuccess) break;
+    g_launches += (uint64_t)(nk_e + nk_d);
+  }
+  cudaGraphDestroy(graph);
+  cudaGraphExecDestroy(exec);
+  if (ce != cudaSuccess) return RLT_ECUDA;
+  sst->pos += n;
   return RLT_OK;
 }
 
@@ -1468,6 +1728,35 @@ int rlt_encode(const rlt_model* m, const int32_t* tokens, int32_t B, int32_t T, 
   if (m->cfg.dtype == RLT_BF16)
     return encode_bf16(m, tokens, B, T, static_cast<bf16*>(e), static_cast<bf16*>(mem), ws, s);
   return encode_impl<float>(m, tokens, B, T, static_cast<float*>(e), static_cast<float*>(mem), ws, s);
+}
+
+int rlt_encode_kv(const rlt_model* m, const int32_t* tokens, int32_t B, int32_t T, int32_t T_max, void* e, void* mem,
+                  void* enc_kv, void* ws, size_t ws_bytes, rlt_stream_t stream) {
+  if (!m || !tokens || !e || !mem || !enc_kv || !ws || B <= 0 || T <= 0 || T_max < T) return RLT_EINVAL;
+  if (!aligned16(e) || !aligned16(mem) || !aligned16(enc_kv) || !aligned16(ws) || !aligned16(tokens))
+    return RLT_EINVAL;
+  if (m->cfg.dtype != RLT_BF16) return RLT_EUNSUPPORTED;
+  if (ws_bytes < layout(m, B, T_max).total) return RLT_EWORKSPACE;
+  return encode_bf16(m, tokens, B, T, static_cast<bf16*>(e), static_cast<bf16*>(mem), ws,
+                     reinterpret_cast<cudaStream_t>(stream), T_max, static_cast<bf16*>(enc_kv));
+}
+
+int rlt_generate(const rlt_model* m, rlt_state* st, void* e, void* mem, void* enc_kv, int32_t T_max, int32_t n,
+                 uint64_t seed, float temperature, int32_t top_k, int32_t* tokens, float* logp, void* ws,
+                 size_t ws_bytes, rlt_stream_t stream) {
+  if (!m || !st || !e || !mem || !enc_kv || !tokens || !ws || T_max <= 0 || n < 0 || st->batch <= 0)
+    return RLT_EINVAL;
+  if (!st->s || !st->ring_k || !st->ring_v) return RLT_EINVAL;
+  if (!aligned16(e) || !aligned16(mem) || !aligned16(enc_kv) || !aligned16(ws)) return RLT_EINVAL;
+  if (!(temperature > 0.f) || top_k < 0) return RLT_EINVAL;
+  if (m->cfg.dtype != RLT_BF16) return RLT_EUNSUPPORTED;
+  if (st->version != m->version) return RLT_ESTALE;
+  if (st->pos < 0 || (int64_t)st->pos + n > T_max) return RLT_ERANGE;
+  if (ws_bytes < layout(m, st->batch, T_max).total) return RLT_EWORKSPACE;
+  if (n == 0) return RLT_OK;
+  return gen_impl(m, st, static_cast<bf16*>(e), static_cast<bf16*>(mem), static_cast<bf16*>(enc_kv), T_max, n,
+                  (unsigned long long)seed, 1.0f / temperature, top_k, tokens, logp, ws,
+                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, const void* mem, int32_t T_mem, int32_t n,
