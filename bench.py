@@ -450,6 +450,63 @@ def run_profile_case(args):
     model.close()
 
 
+def run_generate_case(args):
+    """Generation throughput of the workload's model: prefill of the first
+    half of each sequence (token-parallel encoder keeping its keys and values,
+    decoder over the prompt), then rlt_generate of the second half, timed with
+    CUDA events over --steps calls after --warmup; one JSON line."""
+    import torch
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from recurrent_looped_transformer_rlt_b300 import runner
+    wl = ri.preset(args.workload)
+    c, B, T = wl.cfg, wl.B, wl.T
+    if c.dtype != "bf16":
+        raise SystemExit("generation covers bf16 workloads")
+    T0, n = T // 2, T - T // 2
+    W = ri.make_weights(c, wl.seed)
+    tok = ri.make_tokens(wl, B=B, T=T0)
+    model = rlt.Model(c, W)
+    dt = model.dtype
+    e = torch.empty(B, T, c.d, dtype=dt, device="cuda")
+    mem = torch.empty(c.mem_groups, 2, B, c.n_heads, T, c.head_dim, dtype=dt, device="cuda")
+    kv = torch.empty(c.n_layers, 2, B, c.n_heads, T, c.head_dim, dtype=dt, device="cuda")
+    ws = model.workspace(B, T)
+    tok_d = torch.from_numpy(tok).cuda()
+    acts = torch.from_numpy(ri.teacher_actions(tok, 0, T0)).cuda()
+    lp0 = torch.empty(B, T0, device="cuda")
+    toks = torch.empty(B, n, dtype=torch.int32, device="cuda")
+    lp = torch.empty(B, n, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def prefill():
+        rlt.rlt_encode_kv(model.handle, tok_d, B, T0, T, e, mem, kv, ws, ws.numel(), stream)
+        st = runner.new_state(model, B, stream)
+        rlt.rlt_decode_steps(model.handle, st.c, e, mem, T, T0, acts, 1.0, 0, lp0, None, None, (), None, ws,
+                             ws.numel(), stream)
+        return st
+    ts = []
+    for it in range(args.warmup + args.steps):
+        st = prefill()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        rlt.rlt_generate(model.handle, st.c, e, mem, kv, T, n, 1234 + it, wl.temperature, wl.top_k, toks, lp, ws,
+                         ws.numel(), stream)
+        e1.record(stream)
+        e1.synchronize()
+        if it >= args.warmup:
+            ts.append(e0.elapsed_time(e1) / 1e3)
+    if rlt.rlt_status(ws, stream) != 0:
+        raise RuntimeError("device status flag set")
+    t = float(np.mean(ts))
+    print(json.dumps({"case": "generate", "workload": wl.name, "B": B, "prompt": T0, "generated": n,
+                      "tokens_per_s": round(B * n / t, 1), "us_per_token_step": round(1e6 * t / n, 2),
+                      "calls": len(ts), "temperature": wl.temperature, "top_k": wl.top_k,
+                      "timing": "CUDA events around rlt_generate (graph capture and all generated steps)"}),
+          flush=True)
+    model.close()
+
+
 # ---------------------------------------------------------------------------
 
 def main():
@@ -461,9 +518,13 @@ def main():
     ap.add_argument("--workload", default="small", choices=sorted(ri.PRESETS))
     ap.add_argument("--kernel-class", default="xattn", choices=["xattn", ""])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", default="", choices=["", "xattn", "swa", "proj", "glu"],
-                    help="time one kernel of the workload (profiler captures) instead of the bench step")
+    ap.add_argument("--profile-case", default="", choices=["", "xattn", "swa", "proj", "glu", "generate"],
+                    help="time one kernel of the workload (profiler captures), or generation, instead of the "
+                         "bench step")
     args = ap.parse_args()
+    if args.profile_case == "generate":
+        run_generate_case(args)
+        return
     if args.profile_case:
         run_profile_case(args)
         return
