@@ -28,6 +28,12 @@ output e and the memory M, through every path the state has:
   the recurrent outputs, the decoder key-value entries and the encoder
   memory; detaching any of them is an approximation.
 
+With model_gradients the encoder is part of the graph too (encode builds e
+and M from the tokens, as rlt_oracle.encode does): gradients reach the token
+embedding, the encoder norms and the memory projections, and each tied
+attention / FFN matrix collects its encoder and its decoder use - the
+full-sequence next-token training of the Princeton page's training paragraph.
+
 Named detach points (each off by default = full BPTT):
   detach_s_every = k > 0: s_t is detached after every k-th step;
   detach_cache: the window's keys and values enter later steps as constants
@@ -147,6 +153,65 @@ def sequence_loss(cfg: Cfg, P: Dict[str, torch.Tensor], e, mem, actions, n: Opti
         if detach_s_every > 0 and t % detach_s_every == 0:
             s = s.detach()
     return losses if per_step else torch.stack(losses).sum()
+
+
+ENCODER_PARAMS = ("tok_emb", "enc_attn_norm", "enc_ffn_norm", "enc_norm", "W_K", "W_V")
+
+
+def encode(cfg: Cfg, P: Dict[str, torch.Tensor], tokens):
+    """The causal encoder and memory projection of rlt_oracle.encode in float64
+    torch (float32-storage configurations): e [B, T, d] and mem
+    [G, 2, B, H, T, hd] as functions of the encoder parameters, which include
+    the attention and FFN weights it shares with the decoder (W_qkv, W_O, W_1,
+    W_3, W_2)."""
+    if cfg.bf16:
+        raise ValueError("gradients are defined for float32-storage configurations")
+    tok = torch.as_tensor(np.asarray(tokens), dtype=torch.long)
+    B, T = tok.shape
+    d, H, hd = cfg.d, cfg.n_heads, cfg.head_dim
+    causal = torch.tril(torch.ones(T, T, dtype=torch.bool))
+    h = P["tok_emb"][tok]
+    sources = []
+    for l in range(cfg.n_layers):
+        a = _rmsnorm(h, P["enc_attn_norm"][l], cfg.rms_eps)
+        qkv = a @ P["W_qkv"][l].T
+        q = qkv[..., :d].reshape(B, T, H, hd).transpose(1, 2)
+        k = qkv[..., d:2 * d].reshape(B, T, H, hd).transpose(1, 2)
+        v = qkv[..., 2 * d:].reshape(B, T, H, hd).transpose(1, 2)
+        q = torch.stack([_rope(q[:, :, p], p, cfg.rope_theta) for p in range(T)], dim=2)
+        k = torch.stack([_rope(k[:, :, p], p, cfg.rope_theta) for p in range(T)], dim=2)
+        sc = (q @ k.transpose(-1, -2)) / math.sqrt(hd)
+        sc = torch.where(causal, sc, torch.full_like(sc, -math.inf))
+        o = (torch.softmax(sc, dim=-1) @ v).transpose(1, 2).reshape(B, T, d)
+        h = h + o @ P["W_O"][l].T
+        bb = _rmsnorm(h, P["enc_ffn_norm"][l], cfg.rms_eps)
+        gate = bb @ P["W_1"][l].T
+        h = h + (gate * torch.sigmoid(gate) * (bb @ P["W_3"][l].T)) @ P["W_2"][l].T
+        if cfg.mem_source == 1:
+            sources.append(_rmsnorm(h, P["enc_norm"], cfg.rms_eps))
+    e = _rmsnorm(h, P["enc_norm"], cfg.rms_eps)
+    if cfg.mem_source != 1:
+        sources = [e] * cfg.mem_groups
+    mem = []
+    for g in range(cfg.mem_groups):
+        kk = (sources[g] @ P["W_K"][g].T).reshape(B, T, H, hd).transpose(1, 2)
+        vv = (sources[g] @ P["W_V"][g].T).reshape(B, T, H, hd).transpose(1, 2)
+        mem.append(torch.stack([kk, vv]))
+    return e, torch.stack(mem)
+
+
+def model_gradients(cfg: Cfg, W, tokens, actions, wrt: Iterable[str] = DECODER_PARAMS + ENCODER_PARAMS, **kw):
+    """(loss, {name: gradient}) of the whole model's sequence loss: the encoder
+    builds e and M from the tokens, the recurrent decoder consumes them; tied
+    weights receive the gradients of both uses."""
+    P = {k: torch.tensor(np.asarray(W[k], np.float64), dtype=F, requires_grad=True)
+         for k in DECODER_PARAMS + ENCODER_PARAMS}
+    e, mem = encode(cfg, P, tokens)
+    loss = sequence_loss(cfg, P, e, mem, actions, **kw)
+    names = list(wrt)
+    grads = torch.autograd.grad(loss, [P[k] for k in names], allow_unused=True)
+    return float(loss.detach()), {k: (np.zeros(tuple(P[k].shape)) if g is None else g.detach().numpy())
+                                  for k, g in zip(names, grads)}
 
 
 def leaves(W: Dict[str, np.ndarray], e, mem):

@@ -137,3 +137,76 @@ def test_memory_gradient_is_causal_and_detachable():
     assert np.abs(g["e"][:, 3:]).max() == 0.0 and np.abs(g["e"][:, :3]).max() > 0
     gd = BP.gradients(cfg, W, e, mem, a, wrt=("mem",), detach_memory=True)[1]
     assert np.abs(gd["mem"]).max() == 0.0
+
+
+# ---------------------------------------------------------------------------
+# the whole model: encoder and decoder, tied weights
+
+@pytest.mark.parametrize("G,src", [(1, 0), (2, 1)])
+def test_encoder_forward_equals_the_oracle_encoder(G, src):
+    c = ri.RLTConfig(d=16, n_layers=2, n_heads=2, head_dim=8, d_ffn=24, window=3, mem_groups=G, vocab=9,
+                     dtype="f32", mem_source=src)
+    W = ri.make_weights(c, 5, norm_jitter=0.1)
+    tok = (np.arange(14).reshape(2, 7) * 5 % 9).astype(np.int32)
+    cfg = O.Cfg.of(c)
+    e, mem = O.encode(cfg, W, tok)
+    P = {k: torch.tensor(np.asarray(W[k], np.float64)) for k in BP.DECODER_PARAMS + BP.ENCODER_PARAMS}
+    et, mt = BP.encode(cfg, P, tok)
+    np.testing.assert_allclose(et.numpy(), e, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(mt.numpy(), mem, rtol=1e-12, atol=1e-12)
+
+
+def _model_fd(cfg, W, tok, acts, name, idx, h=1e-6):
+    def loss_with(delta):
+        W2 = {k: np.array(v, np.float64, copy=True) for k, v in W.items()}
+        W2[name][idx] += delta
+        P = {k: torch.tensor(W2[k]) for k in BP.DECODER_PARAMS + BP.ENCODER_PARAMS}
+        with torch.no_grad():
+            e, mem = BP.encode(cfg, P, tok)
+            return float(BP.sequence_loss(cfg, P, e, mem, acts))
+    return (loss_with(h) - loss_with(-h)) / (2 * h)
+
+
+def test_whole_model_gradients_match_central_differences():
+    c = ri.RLTConfig(d=16, n_layers=2, n_heads=2, head_dim=8, d_ffn=24, window=3, mem_groups=2, vocab=9,
+                     dtype="f32")
+    W = ri.make_weights(c, 17, norm_jitter=0.1)
+    for k in W:
+        if W[k].ndim >= 2:
+            W[k] = W[k] * 25.0
+    tok = (np.arange(12).reshape(2, 6) * 4 % 9).astype(np.int32)
+    acts = ri.teacher_actions(tok, 0, 6)
+    cfg = O.Cfg.of(c)
+    _, g = BP.model_gradients(cfg, W, tok, acts)
+    for name, idx in [("tok_emb", (4, 3)), ("enc_attn_norm", (1, 2)), ("enc_ffn_norm", (0, 9)), ("enc_norm", (5,)),
+                      ("W_K", (1, 3, 4)), ("W_V", (0, 6, 2)), ("W_qkv", (0, 17, 5)), ("W_2", (1, 2, 13)),
+                      ("W_g", (1, 30)), ("W_o", (2, 7))]:
+        fd = _model_fd(cfg, W, tok, acts, name, idx)
+        assert abs(g[name][idx] - fd) <= 1e-5 * max(1.0, abs(fd)), (name, idx, g[name][idx], fd)
+
+
+def test_tied_weights_collect_both_uses():
+    """A tied matrix's gradient is the sum of its encoder use and its decoder
+    use (each measured with the other's copy held constant)."""
+    c = ri.RLTConfig(d=16, n_layers=2, n_heads=2, head_dim=8, d_ffn=24, window=3, mem_groups=1, vocab=9,
+                     dtype="f32")
+    W = ri.make_weights(c, 23, norm_jitter=0.1)
+    tok = (np.arange(10).reshape(2, 5) * 2 % 9).astype(np.int32)
+    acts = ri.teacher_actions(tok, 0, 5)
+    cfg = O.Cfg.of(c)
+    _, g = BP.model_gradients(cfg, W, tok, acts, wrt=("W_qkv", "W_2"))
+
+    def split_use(which):
+        P = {k: torch.tensor(np.asarray(W[k], np.float64), requires_grad=True)
+             for k in BP.DECODER_PARAMS + BP.ENCODER_PARAMS}
+        Pe = dict(P)
+        Pd = dict(P)
+        for k in ("W_qkv", "W_O", "W_1", "W_3", "W_2"):
+            (Pd if which == "enc" else Pe)[k] = P[k].detach()
+        e, mem = BP.encode(cfg, Pe, tok)
+        loss = BP.sequence_loss(cfg, Pd, e, mem, acts)
+        return [t.detach().numpy() for t in torch.autograd.grad(loss, [P["W_qkv"], P["W_2"]], allow_unused=True)]
+    ge, gd = split_use("enc"), split_use("dec")
+    for j, name in enumerate(("W_qkv", "W_2")):
+        np.testing.assert_allclose(g[name], ge[j] + gd[j], rtol=1e-10, atol=1e-12)
+        assert np.abs(ge[j]).max() > 0 and np.abs(gd[j]).max() > 0
