@@ -46,3 +46,23 @@ def test_roofline_is_bytes_bound_for_the_memory_heavy_configs():
 def test_job_throughput_counts_every_rank():
     assert bench.job_throughput(64, 512, 1, 0.1) == pytest.approx(327680.0)
     assert bench.job_throughput(64, 512, 4, 0.1) == pytest.approx(4 * 327680.0)
+
+
+@pytest.mark.parametrize("name", ["small", "medium", "refdep", "rlreplay"])
+def test_projection_bytes_cover_every_weight_once_per_step(name):
+    c = ri.preset(name).cfg
+    per = bench.projection_bytes(c, 0)  # no sequences: weights only
+    assert len(per) == 6 * c.n_layers + 2
+    assert sum(per) == bench.decoder_weight_bytes(c)
+    with_rows = bench.projection_bytes(c, 64)
+    assert all(a > b for a, b in zip(with_rows, per))
+
+
+def test_projection_roofline_maps_launches_in_step_order():
+    wl = ri.preset("small")
+    per = bench.projection_bytes(wl.cfg, wl.B)
+    ms = [0.005] * (2 * len(per))  # two steps of 5 us launches
+    r = bench.projection_roofline(wl, ms, 6.5e12, "measured")
+    assert r["launches"] == 2 * len(per)
+    assert r["achieved"] == pytest.approx(2 * sum(per) / (sum(ms) / 1e3) / 1e9, rel=1e-3)
+    assert bench.projection_roofline(wl, [], 6.5e12, "measured") is None
