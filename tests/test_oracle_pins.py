@@ -415,6 +415,21 @@ def test_uniform24_is_uniform_and_independent():
     assert O.uniform24(7, 3, 5) == O.uniform24(7, 3, 5)
 
 
+def test_uniform24_follows_the_published_splitmix64_outputs():
+    """Draw (seed, b, pos=0) is output b+1 of SplitMix64 started at state seed,
+    top 24 bits; the expected outputs are the generator's published reference
+    values (tests/golden/splitmix64.txt, cited there)."""
+    import pathlib
+    rows = [ln.split() for ln in (pathlib.Path(__file__).parent / "golden" / "splitmix64.txt").read_text().splitlines()
+            if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 2
+    for row in rows:
+        seed, outs = int(row[0]), [int(x) for x in row[1:]]
+        assert len(outs) == 5
+        for b, z in enumerate(outs):
+            assert O.uniform24(seed, b, 0) == (z >> 40) / float(1 << 24)
+
+
 def test_sample_token_inverts_the_cdf():
     # two tokens with probabilities 1/4 and 3/4
     lg = np.log(np.array([1.0, 3.0]))
