@@ -294,6 +294,54 @@ RLT_API int rlt_snapshot_save(const rlt_model* m, const rlt_state* st, const voi
 RLT_API int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t snap_bytes, rlt_state* st,
                                  void* e, void* mem, int32_t T_mem, rlt_stream_t stream);
 
+/* Backpropagation through time of the decoder recurrence, teacher forced
+ * ("Recurrent Looped Transformer: A New Architecture for Infinite Context
+ * Reasoning", "Training and Serving Considerations": training backpropagates
+ * through time; "Princeton Researcher Proposes Recurrent Looped Transformer
+ * ...", training paragraph: the state Jacobian has cross terms through the
+ * decoder's keys and values, so a truncated scheme names every tensor it
+ * detaches; "Understanding and Applying the Recurrent Looped Transformer
+ * Architecture", "Current-Policy Reinforcement Learning Replay": gradients
+ * pass through the recurrent outputs, the decoder key-value entries and the
+ * encoder memory).
+ *
+ * From H_0 = (s_*, empty cache), steps t = 1..n consume positions 0..n-1 of
+ * e [B][T_mem][d] with memory mem [G][2][B][H][T_mem][hd] (dtype, as written
+ * by rlt_encode), the head scoring actions [B][n] (int32, device) exactly as
+ * rlt_decode_steps does (temperature, top_k):
+ *   loss = - sum over (b, t) with 0 <= a < V of lp_t(a_{b,t})      (f32 [1])
+ *   logp [B][n] = lp (NaN for a < 0; -inf for an action outside the top-k
+ *                 set, whose gradient then keeps only the set's terms); may be NULL
+ *   grads: d loss / d every decoder parameter, fp32, the parameters' shapes
+ *          (W_qkv, W_O, W_1, W_3, W_2 get the decoder's use of the tied
+ *          matrices only; the encoder's use is the encoder backward's);
+ *          all fields required, overwritten
+ *   d_e  [B][T_mem][d] f32, d_mem [G][2][B][H][T_mem][hd] f32: gradients of
+ *          the encoder output and memory (rows past n zero); may be NULL.
+ * Named detach points (all off: full BPTT):
+ *   detach_s_every = k > 0: s_t enters step t+1 as a constant when t % k == 0;
+ *   RLT_DETACH_CACHE: the window keys/values of earlier positions enter later
+ *     steps as constants (each step keeps the gradient of its own entry);
+ *   RLT_DETACH_MEMORY: the memory is a constant (d_mem stays zero).
+ * Work: a forward pass recording s_t and every position's keys and values,
+ * then a reverse pass that recomputes each step's activations; workspace
+ * rlt_bptt_workspace_size(m, B, n) bytes (its first 256 bytes are the status
+ * word, cleared by rlt_workspace_init).  Errors: RLT_EINVAL (null or
+ * misaligned pointer, n > T_mem, bad temperature / top_k / flags),
+ * RLT_EWORKSPACE, RLT_EUNSUPPORTED (bf16 model with vocab not a multiple of
+ * 8); an action >= V sets RLT_EBOUNDS in the status word and counts as
+ * absent. */
+enum { RLT_DETACH_CACHE = 1, RLT_DETACH_MEMORY = 2 };
+typedef struct rlt_grads {
+  float *W_g, *b_g, *W_qkv, *W_O, *W_Qx, *W_Ox, *W_1, *W_3, *W_2, *W_o;
+  float *dec_attn_norm, *dec_xattn_norm, *dec_ffn_norm, *head_norm, *s_star;
+} rlt_grads;
+RLT_API int rlt_bptt_workspace_size(const rlt_model* m, int32_t B, int32_t n, size_t* bytes);
+RLT_API int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, int32_t B, int32_t n,
+                     const int32_t* actions, float temperature, int32_t top_k, int32_t detach_s_every,
+                     int32_t detach_flags, float* loss, float* logp, const rlt_grads* grads, float* d_e,
+                     float* d_mem, void* ws, size_t ws_bytes, rlt_stream_t stream);
+
 /* Synchronises the stream, returns the device status recorded in the workspace
  * (RLT_OK, RLT_ETIMEOUT or RLT_EBOUNDS) and clears it. */
 RLT_API int rlt_status(void* ws, rlt_stream_t stream);

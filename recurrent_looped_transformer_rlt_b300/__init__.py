@@ -55,6 +55,15 @@ class rlt_state(ctypes.Structure):
                 ("ring_k", _p), ("ring_v", _p)]
 
 
+GRAD_FIELDS = ["W_g", "b_g", "W_qkv", "W_O", "W_Qx", "W_Ox", "W_1", "W_3", "W_2", "W_o", "dec_attn_norm",
+               "dec_xattn_norm", "dec_ffn_norm", "head_norm", "s_star"]
+RLT_DETACH_CACHE, RLT_DETACH_MEMORY = 1, 2
+
+
+class rlt_grads(ctypes.Structure):
+    _fields_ = [(n, _p) for n in GRAD_FIELDS]
+
+
 def _sig(name, res, args):
     f = getattr(_lib, name)
     f.restype = res
@@ -92,6 +101,11 @@ _snapshot_save = _sig("rlt_snapshot_save", ctypes.c_int,
                       [_p, ctypes.POINTER(rlt_state), _p, _p, _i32, _p, ctypes.c_size_t, _p])
 _snapshot_restore = _sig("rlt_snapshot_restore", ctypes.c_int,
                          [_p, _p, ctypes.c_size_t, ctypes.POINTER(rlt_state), _p, _p, _i32, _p])
+_bptt_workspace_size = _sig("rlt_bptt_workspace_size", ctypes.c_int,
+                            [_p, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)])
+_bptt = _sig("rlt_bptt", ctypes.c_int,
+             [_p, _p, _p, _i32, _i32, _i32, _p, ctypes.c_float, _i32, _i32, _i32, _p, _p,
+              ctypes.POINTER(rlt_grads), _p, _p, _p, ctypes.c_size_t, _p])
 _timer_arm = _sig("rlt_timer_arm", ctypes.c_int, [_p, _i32, _i32])
 _timer_read = _sig("rlt_timer_read", ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_float), _i32, ctypes.POINTER(_i32)])
 _strerror = _sig("rlt_strerror", ctypes.c_char_p, [ctypes.c_int])
@@ -102,7 +116,8 @@ EXPORTED = ["rlt_model_create", "rlt_model_set_version", "rlt_model_destroy", "r
             "rlt_workspace_init", "rlt_state_sizes", "rlt_state_init", "rlt_encode", "rlt_decode_steps",
             "rlt_status", "rlt_strerror", "rlt_launch_count", "rlt_abi_version", "rlt_timer_arm",
             "rlt_timer_read", "rlt_cross_attention", "rlt_cross_attention_noalloc", "rlt_linear",
-            "rlt_snapshot_size", "rlt_snapshot_save", "rlt_snapshot_restore", "rlt_encode_kv", "rlt_generate"]
+            "rlt_snapshot_size", "rlt_snapshot_save", "rlt_snapshot_restore", "rlt_encode_kv", "rlt_generate",
+            "rlt_bptt_workspace_size", "rlt_bptt"]
 RLT_TIMER_CLASSES = {"off": 0, "xattn": 1, "swa": 2, "gemm": 3, "head": 4, "step": 5}
 
 
@@ -266,6 +281,23 @@ def rlt_linear(model: int, A, lda: int, M: int, K: int, W, W3, ldw: int, N: int,
                  _stream_ptr(stream))
     if check:
         _check(rc, "rlt_linear")
+    return rc
+
+
+def rlt_bptt_workspace_size(model: int, B: int, n: int) -> int:
+    nb = ctypes.c_size_t()
+    _check(_bptt_workspace_size(model, B, n, ctypes.byref(nb)), "rlt_bptt_workspace_size")
+    return nb.value
+
+
+def rlt_bptt(model: int, e, mem, T_mem: int, B: int, n: int, actions, temperature: float, top_k: int,
+             detach_s_every: int, detach_flags: int, loss, logp, grads: rlt_grads, d_e, d_mem, ws, ws_bytes: int,
+             stream=None, check: bool = True) -> int:
+    rc = _bptt(model, _ptr(e), _ptr(mem), T_mem, B, n, _ptr(actions), temperature, top_k, detach_s_every,
+               detach_flags, _ptr(loss), _ptr(logp), ctypes.byref(grads), _ptr(d_e), _ptr(d_mem), _ptr(ws), ws_bytes,
+               _stream_ptr(stream))
+    if check:
+        _check(rc, "rlt_bptt")
     return rc
 
 

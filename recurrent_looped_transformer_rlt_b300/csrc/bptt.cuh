@@ -1,0 +1,562 @@
+// Device kernels of the decoder's backpropagation through time (the
+// operations that bptt_plan.h sequences).  Storage type T (fp32 or bf16) for
+// GEMM operands and recorded keys/values; every gradient and reduction in
+// fp32.  Row-major [B][N] operands come with a transposed copy [N][Bp] (the
+// row-contracted operand of the weight-gradient GEMMs).
+//
+// Attention backward (per sequence b, head h, over positions j0..j1): with
+// s_j = scale q.K_j, P_j = exp(s_j - lse), o = sum_j P_j V_j and the output
+// gradient g,
+//   dP_j = g.V_j,  D = g.o,  dS_j = P_j (dP_j - D),
+//   dq = scale sum_j dS_j K_j,  dK_j = scale dS_j q,  dV_j = P_j g.
+#pragma once
+
+#include "common.cuh"
+
+namespace rlt {
+namespace bptt {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float sigmoid_acc(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// RoPE angle of pair i at position p: p * theta^(-2i/hd), in double.
+__device__ __forceinline__ void rope_cs(int p, int i, int hd, float theta, float& c, float& s) {
+  const double ang = (double)p * pow((double)theta, -2.0 * (double)i / (double)hd);
+  double sd, cd;
+  sincos(ang, &sd, &cd);
+  c = (float)cd;
+  s = (float)sd;
+}
+
+// dst[c][r] = src[r][c] through a 32x33 shared tile; block (32, 8).
+template <typename T>
+__global__ void transpose_kernel(const T* __restrict__ src, int rows, int cols, int lds, T* __restrict__ dst,
+                                 int ldd) {
+  __shared__ T tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int r = r0 + j, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[j][threadIdx.x] = src[(size_t)r * lds + c];
+  }
+  __syncthreads();
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int c = c0 + j, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) dst[(size_t)c * ldd + r] = tile[threadIdx.x][j];
+  }
+}
+
+// xg[b] = [e[b][p]; s[b]] in the storage type (and transposed).
+template <typename T>
+__global__ void merge_in_kernel(const T* __restrict__ e, int T_mem, int p, const float* __restrict__ s, int B, int d,
+                                T* __restrict__ xg, T* __restrict__ xgT, int Bp) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * 2 * d) return;
+  const int b = (int)(idx / (2 * d)), i = (int)(idx - (size_t)b * 2 * d);
+  const T v = (i < d) ? e[((size_t)b * T_mem + p) * d + i] : from_f32<T>(s[(size_t)b * d + i - d]);
+  xg[idx] = v;
+  xgT[(size_t)i * Bp + b] = v;
+}
+
+// z = sigmoid(zpre + b_g) (0 without a gate), h = z s + (1 - z) e[b][p].
+template <typename T>
+__global__ void merge_out_kernel(const float* __restrict__ zpre, const float* __restrict__ bg,
+                                 const T* __restrict__ e, int T_mem, int p, const float* __restrict__ s, int B, int d,
+                                 float* __restrict__ z, float* __restrict__ h) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * d) return;
+  const int b = (int)(idx / d), i = (int)(idx - (size_t)b * d);
+  const float zv = zpre ? sigmoid_acc(zpre[idx] + bg[i]) : 0.f;
+  const float ev = to_f32(e[((size_t)b * T_mem + p) * d + i]);
+  z[idx] = zv;
+  h[idx] = zv * s[idx] + (1.f - zv) * ev;
+}
+
+// RMSNorm rows: r = 1 / sqrt(mean(x^2) + eps), y = x r g (storage type, and
+// transposed when yT is given).  One warp per row.
+template <typename T>
+__global__ void rms_fwd_kernel(const float* __restrict__ x, const float* __restrict__ g, int B, int d, float eps,
+                               float* __restrict__ r, T* __restrict__ y, T* __restrict__ yT, int Bp) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (row >= B) return;
+  const float* xr = x + (size_t)row * d;
+  float ss = 0.f;
+  for (int i = lane; i < d; i += 32) ss = fmaf(xr[i], xr[i], ss);
+  ss = warp_sum(ss);
+  const float rv = 1.0f / sqrtf(ss / (float)d + eps);
+  if (lane == 0) r[row] = rv;
+  for (int i = lane; i < d; i += 32) {
+    const T v = from_f32<T>(xr[i] * rv * g[i]);
+    y[(size_t)row * d + i] = v;
+    if (yT) yT[(size_t)i * Bp + row] = v;
+  }
+}
+
+// q, k after RoPE at position p (q fp32 to qo, k to K[b][h][p]), v to
+// V[b][h][p]; one thread per (b, h, pair i < hd/2).
+template <typename T>
+__global__ void qkv_post_kernel(const float* __restrict__ qkv, int p, int B, int H, int hd, float theta,
+                                float* __restrict__ qo, T* __restrict__ K, T* __restrict__ V, int Tk) {
+  const int half = hd >> 1;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * H * half) return;
+  const int i = (int)(idx % half);
+  const int h = (int)((idx / half) % H);
+  const int b = (int)(idx / ((size_t)half * H));
+  const int d = H * hd;
+  float c, s;
+  rope_cs(p, i, hd, theta, c, s);
+  const float* row = qkv + (size_t)b * 3 * d + h * hd;
+  const float q1 = row[i], q2 = row[i + half];
+  qo[(size_t)b * d + h * hd + i] = q1 * c - q2 * s;
+  qo[(size_t)b * d + h * hd + i + half] = q2 * c + q1 * s;
+  const float k1 = row[d + i], k2 = row[d + i + half];
+  const size_t o = (((size_t)b * H + h) * Tk + p) * hd;
+  K[o + i] = from_f32<T>(k1 * c - k2 * s);
+  K[o + i + half] = from_f32<T>(k2 * c + k1 * s);
+  V[o + i] = from_f32<T>(row[2 * d + i]);
+  V[o + i + half] = from_f32<T>(row[2 * d + i + half]);
+}
+
+// Softmax attention of q [B][d] over positions j0..j1 of K, V [B][H][Tk][hd]:
+// lse [B][H], o fp32, oq storage type (and transposed).  One warp per (b, h);
+// lane l holds elements l, l + 32, ... of the head.
+template <typename T>
+__global__ void attn_fwd_kernel(const float* __restrict__ q, const T* __restrict__ K, const T* __restrict__ V, int Tk,
+                                int j0, int j1, int B, int H, int hd, float scale, float* __restrict__ lse,
+                                float* __restrict__ o, T* __restrict__ oq, T* __restrict__ oT, int Bp) {
+  const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (pair >= B * H) return;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd;
+  const int NC = (hd + 31) >> 5;  // <= 4
+  float qr[4], acc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    qr[c] = (c < NC && i < hd) ? q[(size_t)b * d + h * hd + i] : 0.f;
+    acc[c] = 0.f;
+  }
+  const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+  const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+  float mx = -INFINITY, l = 0.f;
+  for (int j = j0; j <= j1; ++j) {
+    float part = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) part = fmaf(qr[c], to_f32(Kb[(size_t)j * hd + i]), part);
+    }
+    const float sj = warp_sum(part) * scale;
+    const float mn = fmaxf(mx, sj);
+    const float corr = expf(mx - mn), w = expf(sj - mn);
+    l = l * corr + w;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) acc[c] = acc[c] * corr + w * to_f32(Vb[(size_t)j * hd + i]);
+    }
+    mx = mn;
+  }
+  if (lane == 0) lse[pair] = mx + logf(l);
+  const float inv = 1.0f / l;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) {
+      const float v = acc[c] * inv;
+      const size_t col = (size_t)h * hd + i;
+      o[(size_t)b * d + col] = v;
+      const T vq = from_f32<T>(v);
+      oq[(size_t)b * d + col] = vq;
+      oT[col * Bp + b] = vq;
+    }
+  }
+}
+
+// m = silu(g) u in the storage type (and transposed).
+template <typename T>
+__global__ void swiglu_fwd_kernel(const float* __restrict__ g, const float* __restrict__ u, int B, int f,
+                                  T* __restrict__ m, T* __restrict__ mT, int Bp) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * f) return;
+  const int b = (int)(idx / f), j = (int)(idx - (size_t)b * f);
+  const float gv = g[idx];
+  const T v = from_f32<T>(gv * sigmoid_acc(gv) * u[idx]);
+  m[idx] = v;
+  mT[(size_t)j * Bp + b] = v;
+}
+
+// Order-preserving unsigned key of a float.
+__device__ __forceinline__ unsigned fkey(float x) {
+  const unsigned u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Head of one step, one block of kThreadsHead per sequence b: x = logits /
+// temperature; S = all ids, or the top-k set (the k largest x, ties to the
+// lower id); lp = x_a - log sum_{v in S} exp(x_v) to lp[b][n_ld * .. + p]
+// (NaN for a < 0, -inf for a outside S); d(-lp)/d logits_v =
+// inv_temp (p_v [v in S] - [v = a]) to dl [B][V] (and transposed), 0 for
+// a < 0.  Shared memory: V floats.
+constexpr int kThreadsHead = 1024;
+__global__ void __launch_bounds__(kThreadsHead) head_bwd_kernel(const float* __restrict__ logits, int B, int V,
+                                                                 const int32_t* __restrict__ actions, int n, int p,
+                                                                 float inv_temp, int top_k, float* __restrict__ lp,
+                                                                 void* dl_, void* dlT_, int Bp, int bf16_out,
+                                                                 int* status) {
+  extern __shared__ float sx[];
+  __shared__ unsigned hist[256];
+  __shared__ float red[32];
+  __shared__ unsigned ured[kThreadsHead];
+  __shared__ unsigned s_prefix, s_remain;
+  const int b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = nthr >> 5;
+  const float* lg = logits + (size_t)b * V;
+  float mx = -INFINITY;
+  for (int v = tid; v < V; v += nthr) {
+    const float x = lg[v] * inv_temp;
+    sx[v] = x;
+    mx = fmaxf(mx, x);
+  }
+  mx = warp_max(mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  if (tid == 0) {
+    float t = red[0];
+    for (int w = 1; w < nw; ++w) t = fmaxf(t, red[w]);
+    red[0] = t;
+  }
+  __syncthreads();
+  mx = red[0];
+  __syncthreads();
+  const bool topk = top_k > 0 && top_k < V;
+  unsigned kth = 0, need = 0;
+  if (topk) {
+    // radix select of the k-th largest key, 8 bits per pass from the top
+    if (tid == 0) {
+      s_prefix = 0;
+      s_remain = (unsigned)top_k;
+    }
+    __syncthreads();
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int j = tid; j < 256; j += nthr) hist[j] = 0;
+      __syncthreads();
+      const unsigned pref = s_prefix;
+      const unsigned hmask = (pass == 0) ? 0u : (0xffffffffu << (shift + 8));
+      for (int v = tid; v < V; v += nthr) {
+        const unsigned kk = fkey(sx[v]);
+        if ((kk & hmask) == pref) atomicAdd(&hist[(kk >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        unsigned rem = s_remain;
+        int bin = 255;
+        for (; bin > 0; --bin) {
+          if (hist[bin] >= rem) break;
+          rem -= hist[bin];
+        }
+        s_prefix = pref | ((unsigned)bin << shift);
+        s_remain = rem;
+      }
+      __syncthreads();
+    }
+    kth = s_prefix;
+    need = s_remain;
+  }
+  // members: thread tid owns the contiguous ids [tid C, (tid + 1) C); the
+  // ties at kth are ranked in id order through an exclusive scan of counts
+  const int C = (V + nthr - 1) / nthr;
+  const int v0 = min(V, tid * C), v1 = min(V, v0 + C);
+  unsigned ties = 0;
+  if (topk)
+    for (int v = v0; v < v1; ++v) ties += (fkey(sx[v]) == kth) ? 1u : 0u;
+  ured[tid] = ties;
+  __syncthreads();
+  if (tid == 0) {
+    unsigned acc = 0;
+    for (int t = 0; t < nthr; ++t) {
+      const unsigned cnt = ured[t];
+      ured[t] = acc;
+      acc += cnt;
+    }
+  }
+  __syncthreads();
+  const unsigned tie0 = ured[tid];
+  // mark non-members with -inf in place (ids of this thread's chunk only)
+  {
+    unsigned tb = tie0;
+    for (int v = v0; v < v1; ++v) {
+      bool in = true;
+      if (topk) {
+        const unsigned kk = fkey(sx[v]);
+        in = kk > kth || (kk == kth && tb < need);
+        if (kk == kth) ++tb;
+      }
+      if (!in) sx[v] = -INFINITY;
+    }
+  }
+  __syncthreads();
+  float se = 0.f;
+  for (int v = tid; v < V; v += nthr) se += expf(sx[v] - mx);
+  se = warp_sum(se);
+  if (lane == 0) red[warp] = se;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < nw; ++w) t += red[w];
+    red[0] = t;
+  }
+  __syncthreads();
+  const float lse = mx + logf(red[0]);
+  int act = actions[(size_t)b * n + p];
+  if (act >= V) {
+    if (tid == 0) set_error(status, kErrBounds);
+    act = -1;
+  }
+  if (tid == 0) lp[(size_t)b * n + p] = act < 0 ? NAN : sx[act] - lse;
+  const bool a_in = act >= 0 && sx[act] > -INFINITY;
+  for (int v = tid; v < V; v += nthr) {
+    float gv = 0.f;
+    if (act >= 0) gv = inv_temp * (expf(sx[v] - lse) - ((v == act && a_in) ? 1.f : 0.f));
+    if (bf16_out) {
+      const bf16 q = __float2bfloat16_rn(gv);
+      static_cast<bf16*>(dl_)[(size_t)b * V + v] = q;
+      static_cast<bf16*>(dlT_)[(size_t)v * Bp + b] = q;
+    } else {
+      static_cast<float*>(dl_)[(size_t)b * V + v] = gv;
+      static_cast<float*>(dlT_)[(size_t)v * Bp + b] = gv;
+    }
+  }
+}
+
+// RMSNorm backward for y = x r g (r = 1/sqrt(mean(x^2) + eps)) given dy:
+//   dx_i += r g_i dy_i - x_i r^3 (sum_j g_j dy_j x_j) / d     (rows: warp per row)
+//   dg_i += sum_b dy_i x_i r                                 (columns: thread per column)
+// Blocks [0, row_blocks) do the rows, the rest the columns.
+__global__ void rms_bwd_kernel(const float* __restrict__ x, const float* __restrict__ r, const float* __restrict__ g,
+                               const float* __restrict__ dy, int B, int d, float* __restrict__ dx,
+                               float* __restrict__ dg, int row_blocks) {
+  if ((int)blockIdx.x < row_blocks) {
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (row >= B) return;
+    const float* xr = x + (size_t)row * d;
+    const float* dyr = dy + (size_t)row * d;
+    float sd = 0.f;
+    for (int i = lane; i < d; i += 32) sd = fmaf(g[i] * dyr[i], xr[i], sd);
+    sd = warp_sum(sd);
+    const float rv = r[row];
+    const float coef = rv * rv * rv * sd / (float)d;
+    for (int i = lane; i < d; i += 32) dx[(size_t)row * d + i] += rv * g[i] * dyr[i] - xr[i] * coef;
+  } else {
+    const int i = (blockIdx.x - row_blocks) * blockDim.x + threadIdx.x;
+    if (i >= d) return;
+    float acc = 0.f;
+    for (int b = 0; b < B; ++b) acc = fmaf(dy[(size_t)b * d + i] * x[(size_t)b * d + i], r[b], acc);
+    dg[i] += acc;
+  }
+}
+
+// y = x in the storage type, and transposed.
+template <typename T>
+__global__ void pack_kernel(const float* __restrict__ x, int B, int N, T* __restrict__ y, T* __restrict__ yT, int Bp) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * N) return;
+  const int b = (int)(idx / N), j = (int)(idx - (size_t)b * N);
+  const T v = from_f32<T>(x[idx]);
+  y[idx] = v;
+  yT[(size_t)j * Bp + b] = v;
+}
+
+// m = silu(g) u backward: dg = dm u sigma(g) (1 + g (1 - sigma(g))),
+// du = dm g sigma(g); dY[b] = [dg | du] (and transposed: rows j, f + j).
+template <typename T>
+__global__ void swiglu_bwd_kernel(const float* __restrict__ dm, const float* __restrict__ g,
+                                  const float* __restrict__ u, int B, int f, T* __restrict__ dY, T* __restrict__ dYT,
+                                  int Bp) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * f) return;
+  const int b = (int)(idx / f), j = (int)(idx - (size_t)b * f);
+  const float gv = g[idx], uv = u[idx], dv = dm[idx];
+  const float sg = sigmoid_acc(gv);
+  const T dgq = from_f32<T>(dv * uv * sg * (1.f + gv * (1.f - sg)));
+  const T duq = from_f32<T>(dv * gv * sg);
+  dY[(size_t)b * 2 * f + j] = dgq;
+  dY[(size_t)b * 2 * f + f + j] = duq;
+  dYT[(size_t)j * Bp + b] = dgq;
+  dYT[(size_t)(f + j) * Bp + b] = duq;
+}
+
+// Attention backward over positions j0..j1 (see the header): dq [B][d]
+// stored; dK, dV (fp32 accumulators, may be null) += for positions j >= jg,
+// at slot j mod Ta (ring) or j of [B][H][Ta][hd].  One warp per (b, h); each
+// (b, h, j) has one writer.
+template <typename T>
+__global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __restrict__ gout,
+                                const float* __restrict__ o, const float* __restrict__ lse, const T* __restrict__ K,
+                                const T* __restrict__ V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
+                                float* __restrict__ dq, float* __restrict__ dK, float* __restrict__ dV, int Ta,
+                                int ring, int jg) {
+  const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (pair >= B * H) return;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd;
+  const int NC = (hd + 31) >> 5;
+  float qr[4], gr[4], acc[4];
+  float Dp = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const bool ok = c < NC && i < hd;
+    const size_t col = (size_t)b * d + h * hd + i;
+    qr[c] = ok ? q[col] : 0.f;
+    gr[c] = ok ? gout[col] : 0.f;
+    acc[c] = 0.f;
+    if (ok) Dp = fmaf(gr[c], o[col], Dp);
+  }
+  const float D = warp_sum(Dp);
+  const float ls = lse[pair];
+  const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+  const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+  for (int j = j0; j <= j1; ++j) {
+    float kv[4], sp = 0.f, dpp = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      kv[c] = 0.f;
+      if (c < NC && i < hd) {
+        kv[c] = to_f32(Kb[(size_t)j * hd + i]);
+        sp = fmaf(qr[c], kv[c], sp);
+        dpp = fmaf(gr[c], to_f32(Vb[(size_t)j * hd + i]), dpp);
+      }
+    }
+    const float sj = warp_sum(sp) * scale;
+    const float dP = warp_sum(dpp);
+    const float P = expf(sj - ls);
+    const float dS = P * (dP - D);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = fmaf(dS, kv[c], acc[c]);
+    if (dK && j >= jg) {
+      const int slot = ring ? j % Ta : j;
+      const size_t base = (((size_t)b * H + h) * Ta + slot) * hd;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = lane + 32 * c;
+        if (c < NC && i < hd) {
+          dK[base + i] += scale * dS * qr[c];
+          dV[base + i] += P * gr[c];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) dq[(size_t)b * d + h * hd + i] = scale * acc[c];
+  }
+}
+
+// d qkv of position p: dq and the completed key gradient (ring slot p mod W)
+// back through RoPE, the value gradient as is; dY [B][3d] (and transposed).
+// Clears the ring slot.  One thread per (b, h, pair i < hd/2).
+template <typename T>
+__global__ void qkv_bwd_kernel(const float* __restrict__ dq, float* __restrict__ rK, float* __restrict__ rV, int W,
+                               int p, int B, int H, int hd, float theta, T* __restrict__ dY, T* __restrict__ dYT,
+                               int Bp) {
+  const int half = hd >> 1;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * H * half) return;
+  const int i = (int)(idx % half);
+  const int h = (int)((idx / half) % H);
+  const int b = (int)(idx / ((size_t)half * H));
+  const int d = H * hd;
+  float c, s;
+  rope_cs(p, i, hd, theta, c, s);
+  const size_t rs = (((size_t)b * H + h) * W + p % W) * hd;
+  const float q1 = dq[(size_t)b * d + h * hd + i], q2 = dq[(size_t)b * d + h * hd + i + half];
+  const float k1 = rK[rs + i], k2 = rK[rs + i + half];
+  const float v1 = rV[rs + i], v2 = rV[rs + i + half];
+  rK[rs + i] = 0.f;
+  rK[rs + i + half] = 0.f;
+  rV[rs + i] = 0.f;
+  rV[rs + i + half] = 0.f;
+  const float vals[6] = {q1 * c + q2 * s, -q1 * s + q2 * c, k1 * c + k2 * s, -k1 * s + k2 * c, v1, v2};
+  const int cols[6] = {h * hd + i, h * hd + i + half, d + h * hd + i, d + h * hd + i + half, 2 * d + h * hd + i,
+                       2 * d + h * hd + i + half};
+#pragma unroll
+  for (int j = 0; j < 6; ++j) {
+    const T v = from_f32<T>(vals[j]);
+    dY[(size_t)b * 3 * d + cols[j]] = v;
+    dYT[(size_t)cols[j] * Bp + b] = v;
+  }
+}
+
+// Merge backward, one thread per column i (loop over sequences):
+//   de[b][p][i] = dh (1 - z);  ds[b][i] = dh z;
+//   gate: dzpre = dh (s - e) z (1 - z) to dY [B][d] (and transposed),
+//         db_g[i] += sum_b dzpre.
+template <typename T>
+__global__ void merge_bwd_kernel(const float* __restrict__ dh, const float* __restrict__ z, const T* __restrict__ e,
+                                 int T_mem, int p, const float* __restrict__ s, int B, int d, int gate,
+                                 T* __restrict__ dY, T* __restrict__ dYT, int Bp, float* __restrict__ dbg,
+                                 float* __restrict__ de, float* __restrict__ ds) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d) return;
+  float acc = 0.f;
+  for (int b = 0; b < B; ++b) {
+    const size_t o = (size_t)b * d + i;
+    const size_t oe = ((size_t)b * T_mem + p) * d + i;
+    const float g = dh[o], zv = z[o];
+    if (de) de[oe] = g * (1.f - zv);
+    ds[o] = g * zv;
+    if (gate) {
+      const float dz = g * (s[o] - to_f32(e[oe])) * zv * (1.f - zv);
+      const T q = from_f32<T>(dz);
+      dY[o] = q;
+      dYT[(size_t)i * Bp + b] = q;
+      acc += dz;
+    }
+  }
+  if (gate) dbg[i] += acc;
+}
+
+// de[b][p] += dx[b][:d], ds[b] += dx[b][d:] (dx = dzpre W_g, [B][2d]).
+__global__ void merge_bwd2_kernel(const float* __restrict__ dx, int B, int d, int T_mem, int p,
+                                  float* __restrict__ de, float* __restrict__ ds) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * d) return;
+  const int b = (int)(idx / d), i = (int)(idx - (size_t)b * d);
+  if (de) de[((size_t)b * T_mem + p) * d + i] += dx[(size_t)b * 2 * d + i];
+  ds[idx] += dx[(size_t)b * 2 * d + d + i];
+}
+
+// out[i] += sum_b x[b][i].
+__global__ void colsum_kernel(const float* __restrict__ x, int B, int d, float* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d) return;
+  float acc = 0.f;
+  for (int b = 0; b < B; ++b) acc += x[(size_t)b * d + i];
+  out[i] += acc;
+}
+
+// loss = -sum over (b, t) with 0 <= a < V of lp[b][t]; one block of
+// kThreads, fixed summation order.
+__global__ void loss_sum_kernel(const float* __restrict__ lp, const int32_t* __restrict__ actions, int B, int n, int V,
+                                float* __restrict__ loss) {
+  __shared__ float red[kThreads];
+  const int tid = threadIdx.x;
+  float acc = 0.f;
+  for (size_t i = tid; i < (size_t)B * n; i += blockDim.x)
+    if (actions[i] >= 0 && actions[i] < V) acc -= lp[i];
+  red[tid] = acc;
+  __syncthreads();
+  for (int s = blockDim.x >> 1; s > 0; s >>= 1) {
+    if (tid < s) red[tid] += red[tid + s];
+    __syncthreads();
+  }
+  if (tid == 0) *loss = red[0];
+}
+
+}  // namespace bptt
+}  // namespace rlt

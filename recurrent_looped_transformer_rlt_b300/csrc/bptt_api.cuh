@@ -1,0 +1,270 @@
+// Backpropagation through time of the decoder (rlt_bptt_workspace_size,
+// rlt_bptt in include/rlt.h): the operations of bptt_plan.h as launches on
+// one CUDA stream.  Part of the rlt_api.cu translation unit (included at its
+// end): the projections go through the same launchers as the forward step -
+// tcgen05 weight streaming for bf16 models, the fp32 CUDA-core kernel for
+// fp32 models.
+#include "bptt.cuh"
+#include "bptt_plan.h"
+
+namespace {
+
+template <typename T_>
+struct BpttOps {
+  using T = T_;
+  static constexpr bool kBf16 = std::is_same<T_, bf16>::value;
+  cudaStream_t st;
+  TcScratch sc;
+  int* status;
+
+  int post() {
+    g_launches++;
+    return launch_ok();
+  }
+  static unsigned blocks(size_t work, int per_block = bptt::kThreads) { return cdiv(work, per_block); }
+
+  int zero(void* p, size_t bytes) {
+    if (!bytes) return RLT_OK;
+    return cudaMemsetAsync(p, 0, bytes, st) == cudaSuccess ? RLT_OK : RLT_ECUDA;
+  }
+  int copy(void* dst, const void* src, size_t bytes) {
+    if (!bytes) return RLT_OK;
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st) == cudaSuccess ? RLT_OK : RLT_ECUDA;
+  }
+  int transpose(const T* src, int rows, int cols, int lds, T* dst, int ldd) {
+    bptt::transpose_kernel<T><<<dim3(cdiv(cols, 32), cdiv(rows, 32)), dim3(32, 8), 0, st>>>(src, rows, cols, lds,
+                                                                                           dst, ldd);
+    return post();
+  }
+  // C[M][N] (+)= A[M][K] W[N][K]^T
+  int gemm(const T* A, int lda, int M, int K, const T* W, int ldw, int N, float* C, int ldc, bool add) {
+    if constexpr (kBf16) {
+      AArg a;
+      a.A = A;
+      a.lda = lda;
+      if (add) return proj_bf16<false>(st, a, M, K, W, nullptr, ldw, N, EpiAddF32{C, ldc}, sc);
+      return proj_bf16<false>(st, a, M, K, W, nullptr, ldw, N, EpiStoreF32{C, ldc}, sc);
+    } else {
+      if (add) return ::gemm<float>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, EpiAddF32{C, ldc});
+      return ::gemm<float>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, EpiStoreF32{C, ldc});
+    }
+  }
+  int bcast_rows(float* dst, const float* src, int rows, int d) {
+    bcast_rows_kernel<<<blocks((size_t)rows * d), bptt::kThreads, 0, st>>>(dst, src, rows, d);
+    return post();
+  }
+  int merge_in(const T* e, int T_mem, int p, const float* s, int B, int d, T* xg, T* xgT, int Bp) {
+    bptt::merge_in_kernel<T><<<blocks((size_t)B * 2 * d), bptt::kThreads, 0, st>>>(e, T_mem, p, s, B, d, xg, xgT, Bp);
+    return post();
+  }
+  int merge_out(const float* zpre, const float* bg, const T* e, int T_mem, int p, const float* s, int B, int d,
+                float* z, float* h) {
+    bptt::merge_out_kernel<T><<<blocks((size_t)B * d), bptt::kThreads, 0, st>>>(zpre, bg, e, T_mem, p, s, B, d, z, h);
+    return post();
+  }
+  int rms_fwd(const float* x, const float* g, int B, int d, float eps, float* r, T* y, T* yT, int Bp) {
+    bptt::rms_fwd_kernel<T><<<blocks((size_t)B * 32), bptt::kThreads, 0, st>>>(x, g, B, d, eps, r, y, yT, Bp);
+    return post();
+  }
+  int qkv_post(const float* qkv, int p, int B, int H, int hd, float theta, float* q, T* K, T* V, int Tk) {
+    bptt::qkv_post_kernel<T><<<blocks((size_t)B * H * (hd / 2)), bptt::kThreads, 0, st>>>(qkv, p, B, H, hd, theta, q,
+                                                                                         K, V, Tk);
+    return post();
+  }
+  int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
+               float* lse, float* o, T* oq, T* oT, int Bp) {
+    bptt::attn_fwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(q, K, V, Tk, j0, j1, B, H, hd, scale,
+                                                                             lse, o, oq, oT, Bp);
+    return post();
+  }
+  int swiglu_fwd(const float* g, const float* u, int B, int f, T* m, T* mT, int Bp) {
+    bptt::swiglu_fwd_kernel<T><<<blocks((size_t)B * f), bptt::kThreads, 0, st>>>(g, u, B, f, m, mT, Bp);
+    return post();
+  }
+  int head_bwd(const float* logits, int B, int V, const int32_t* actions, int n, int p, float inv_temp, int top_k,
+               float* lp, T* dl, T* dlT, int Bp) {
+    bptt::head_bwd_kernel<<<B, bptt::kThreadsHead, sizeof(float) * (size_t)V, st>>>(
+        logits, B, V, actions, n, p, inv_temp, top_k, lp, dl, dlT, Bp, kBf16 ? 1 : 0, status);
+    return post();
+  }
+  int rms_bwd(const float* x, const float* r, const float* g, const float* dy, int B, int d, float* dx, float* dg) {
+    const int row_blocks = (int)blocks((size_t)B * 32);
+    const int col_blocks = (int)blocks((size_t)d);
+    bptt::rms_bwd_kernel<<<row_blocks + col_blocks, bptt::kThreads, 0, st>>>(x, r, g, dy, B, d, dx, dg, row_blocks);
+    return post();
+  }
+  int pack(const float* x, int B, int N, T* y, T* yT, int Bp) {
+    bptt::pack_kernel<T><<<blocks((size_t)B * N), bptt::kThreads, 0, st>>>(x, B, N, y, yT, Bp);
+    return post();
+  }
+  int swiglu_bwd(const float* dm, const float* g, const float* u, int B, int f, T* dY, T* dYT, int Bp) {
+    bptt::swiglu_bwd_kernel<T><<<blocks((size_t)B * f), bptt::kThreads, 0, st>>>(dm, g, u, B, f, dY, dYT, Bp);
+    return post();
+  }
+  int attn_bwd(const float* q, const float* gout, const float* o, const float* lse, const T* K, const T* V, int Tk,
+               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* dK, float* dV, int Ta, bool ring,
+               int jg) {
+    bptt::attn_bwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(
+        q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd, scale, dq, dK, dV, Ta, ring ? 1 : 0, jg);
+    return post();
+  }
+  int qkv_bwd(const float* dq, float* rK, float* rV, int W, int p, int B, int H, int hd, float theta, T* dY, T* dYT,
+              int Bp) {
+    bptt::qkv_bwd_kernel<T><<<blocks((size_t)B * H * (hd / 2)), bptt::kThreads, 0, st>>>(dq, rK, rV, W, p, B, H, hd,
+                                                                                        theta, dY, dYT, Bp);
+    return post();
+  }
+  int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, int p, const float* s, int B, int d,
+                bool gate, T* dY, T* dYT, int Bp, float* dbg, float* de, float* ds) {
+    bptt::merge_bwd_kernel<T><<<blocks((size_t)d), bptt::kThreads, 0, st>>>(dh, z, e, T_mem, p, s, B, d, gate ? 1 : 0,
+                                                                            dY, dYT, Bp, dbg, de, ds);
+    return post();
+  }
+  int merge_bwd2(const float* dx, int B, int d, int T_mem, int p, float* de, float* ds) {
+    bptt::merge_bwd2_kernel<<<blocks((size_t)B * d), bptt::kThreads, 0, st>>>(dx, B, d, T_mem, p, de, ds);
+    return post();
+  }
+  int colsum(const float* x, int B, int d, float* out) {
+    bptt::colsum_kernel<<<blocks((size_t)d), bptt::kThreads, 0, st>>>(x, B, d, out);
+    return post();
+  }
+  int loss_sum(const float* lp, const int32_t* actions, int B, int n, int V, float* loss) {
+    bptt::loss_sum_kernel<<<1, bptt::kThreads, 0, st>>>(lp, actions, B, n, V, loss);
+    return post();
+  }
+};
+
+constexpr size_t kBpttHeader = kWsHeaderBytes;
+
+bpplan::Shape bptt_shape(const rlt_model* m, int B, int n, int T_mem, float temperature, int top_k) {
+  const rlt_config& c = m->cfg;
+  bpplan::Shape S{};
+  S.B = B;
+  S.n = n;
+  S.T_mem = T_mem;
+  S.d = c.d_model;
+  S.H = c.n_heads;
+  S.hd = c.head_dim;
+  S.f = c.d_ffn;
+  S.L = c.n_layers;
+  S.W = c.window;
+  S.V = c.vocab;
+  S.G = c.mem_groups;
+  S.gate_learned = c.gate_mode == RLT_GATE_LEARNED;
+  S.eps = c.rms_eps;
+  S.theta = c.rope_theta;
+  S.scale = 1.0f / sqrtf((float)c.head_dim);
+  S.inv_temp = 1.0f / temperature;
+  S.top_k = top_k;
+  // the bf16 weight-gradient GEMMs contract over Bp rows in whole 64-wide k-blocks
+  S.Bp = (c.dtype == RLT_BF16) ? (B + 63) / 64 * 64 : B;
+  return S;
+}
+
+template <typename T_>
+int bptt_impl(const rlt_model* m, const bpplan::Shape& S, const bpplan::Detach& D,
+              const bpplan::Io<T_>& io, const bpplan::Grads& G, void* ws, cudaStream_t st) {
+  const rlt_weights& w = m->w;
+  bpplan::Params<T_> P;
+  P.W_g = static_cast<const T_*>(w.W_g);
+  P.W_qkv = static_cast<const T_*>(w.W_qkv);
+  P.W_O = static_cast<const T_*>(w.W_O);
+  P.W_Qx = static_cast<const T_*>(w.W_Qx);
+  P.W_Ox = static_cast<const T_*>(w.W_Ox);
+  P.W_1 = static_cast<const T_*>(w.W_1);
+  P.W_3 = static_cast<const T_*>(w.W_3);
+  P.W_2 = static_cast<const T_*>(w.W_2);
+  P.W_o = static_cast<const T_*>(w.W_o);
+  P.b_g = w.b_g;
+  P.s_star = w.s_star;
+  P.attn_norm = w.dec_attn_norm;
+  P.xattn_norm = w.dec_xattn_norm;
+  P.ffn_norm = w.dec_ffn_norm;
+  P.head_norm = w.head_norm;
+  const bpplan::Layout Lw = bpplan::layout(S, m->esz, kBpttHeader);
+  BpttOps<T_> k;
+  k.st = st;
+  k.status = static_cast<int*>(ws);
+  k.sc.n_sm = m->n_sm;
+  k.sc.maxc = m->gemm_maxc;
+  k.sc.status = k.status;
+  return bpplan::run(k, S, D, P, io, G, static_cast<char*>(ws), Lw);
+}
+
+bool g_bptt_attr_done = false;
+std::mutex g_bptt_attr_mu;
+
+int bptt_attrs() {
+  std::lock_guard<std::mutex> lk(g_bptt_attr_mu);
+  if (g_bptt_attr_done) return RLT_OK;
+  // the head reduction keeps a row of V fp32 logits in shared memory
+  const int smem = (int)sizeof(float) * 49152;
+  if (cudaFuncSetAttribute(bptt::head_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return RLT_ECUDA;
+  g_bptt_attr_done = true;
+  return RLT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rlt_bptt_workspace_size(const rlt_model* m, int32_t B, int32_t n, size_t* bytes) {
+  if (!m || !bytes || B <= 0 || n <= 0) return RLT_EINVAL;
+  *bytes = bpplan::layout(bptt_shape(m, B, n, n, 1.0f, 0), m->esz, kBpttHeader).total;
+  return RLT_OK;
+}
+
+int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, int32_t B, int32_t n,
+             const int32_t* actions, float temperature, int32_t top_k, int32_t detach_s_every, int32_t detach_flags,
+             float* loss, float* logp, const rlt_grads* grads, float* d_e, float* d_mem, void* ws, size_t ws_bytes,
+             rlt_stream_t stream) {
+  if (!m || !e || !mem || !actions || !loss || !grads || !ws) return RLT_EINVAL;
+  if (B <= 0 || n <= 0 || T_mem < n) return RLT_EINVAL;
+  if (!(temperature > 0.f) || top_k < 0 || detach_s_every < 0) return RLT_EINVAL;
+  if (detach_flags & ~(RLT_DETACH_CACHE | RLT_DETACH_MEMORY)) return RLT_EINVAL;
+  const float* gp[] = {grads->W_g, grads->b_g, grads->W_qkv, grads->W_O, grads->W_Qx, grads->W_Ox, grads->W_1,
+                       grads->W_3, grads->W_2, grads->W_o, grads->dec_attn_norm, grads->dec_xattn_norm,
+                       grads->dec_ffn_norm, grads->head_norm, grads->s_star};
+  for (const float* p : gp)
+    if (!p || !aligned16(p)) return RLT_EINVAL;
+  if (!aligned16(e) || !aligned16(mem) || !aligned16(ws) || !aligned16(actions) || (d_e && !aligned16(d_e)) ||
+      (d_mem && !aligned16(d_mem)) || (logp && !aligned16(logp)))
+    return RLT_EINVAL;
+  // bf16 models: d logits [B][V] and W_o^T [d][V] are tensor-core operands
+  // with a row pitch of V elements (16-byte multiples)
+  if (m->cfg.dtype == RLT_BF16 && m->cfg.vocab % 8 != 0) return RLT_EUNSUPPORTED;
+  const bpplan::Shape S = bptt_shape(m, B, n, T_mem, temperature, top_k);
+  if (ws_bytes < bpplan::layout(S, m->esz, kBpttHeader).total) return RLT_EWORKSPACE;
+  int rc = bptt_attrs();
+  if (rc) return rc;
+  bpplan::Detach D;
+  D.s_every = detach_s_every;
+  D.cache = (detach_flags & RLT_DETACH_CACHE) != 0;
+  D.memory = (detach_flags & RLT_DETACH_MEMORY) != 0;
+  bpplan::Grads G;
+  G.W_g = grads->W_g;
+  G.b_g = grads->b_g;
+  G.W_qkv = grads->W_qkv;
+  G.W_O = grads->W_O;
+  G.W_Qx = grads->W_Qx;
+  G.W_Ox = grads->W_Ox;
+  G.W_1 = grads->W_1;
+  G.W_3 = grads->W_3;
+  G.W_2 = grads->W_2;
+  G.W_o = grads->W_o;
+  G.attn_norm = grads->dec_attn_norm;
+  G.xattn_norm = grads->dec_xattn_norm;
+  G.ffn_norm = grads->dec_ffn_norm;
+  G.head_norm = grads->head_norm;
+  G.s_star = grads->s_star;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (m->cfg.dtype == RLT_BF16) {
+    bpplan::Io<bf16> io{static_cast<const bf16*>(e), static_cast<const bf16*>(mem), actions, loss, logp, d_e, d_mem};
+    return bptt_impl<bf16>(m, S, D, io, G, ws, s);
+  }
+  bpplan::Io<float> io{static_cast<const float*>(e), static_cast<const float*>(mem), actions, loss, logp, d_e, d_mem};
+  return bptt_impl<float>(m, S, D, io, G, ws, s);
+}
+
+}  // extern "C"

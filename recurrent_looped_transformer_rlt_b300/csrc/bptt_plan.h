@@ -1,0 +1,383 @@
+// Backpropagation through time of the RLT decoder recurrence (teacher
+// forced, full or truncated at named detach points): the order of the
+// operations, the workspace layout and the bookkeeping of the window-gradient
+// ring, written once over a set of primitive operations (Ops, implemented by
+// the device kernels of bptt.cuh).  Plain host C++: no CUDA types.
+//
+// What is differentiated (the decoder of "Understanding and Applying the
+// Recurrent Looped Transformer Architecture", "How the Architecture Works",
+// started at H_0 = (s_*, empty cache)):
+//   L = - sum_t sum_b lp_t(a_{b,t}),  lp_t = tempered (top-k) log-softmax of
+//   W_o RMSNorm_o(s_t) at the action,
+// with respect to every decoder parameter, s_*, the encoder output e and the
+// memory M.  Gradients pass through s, the window keys and values and the
+// memory ("Princeton Researcher Proposes Recurrent Looped Transformer ...",
+// training paragraph: the state Jacobian has cross terms through the decoder
+// keys and values, so a truncation names each tensor it detaches;
+// "Current-Policy Reinforcement Learning Replay": detaching the recurrent
+// outputs, the decoder key-value entries or the memory is an approximation).
+//
+// Schedule.  A forward pass records s_t for every step and the keys and
+// values of every position and layer.  The reverse pass then visits
+// t = n..1: it recomputes step t's activations from s_{t-1} and the recorded
+// keys/values (the same kernels, so bitwise the recorded values), runs the
+// head and the layers backwards, and hands d s_{t-1} to step t-1.  The window
+// keys and values of position j receive gradient from steps j+1..j+W; those
+// arrive (in reverse order) before step j+1 itself is visited, so a ring of W
+// fp32 slots per layer (slot j mod W) holds them until position j's QKV
+// backward consumes and clears its slot, which is then free for position j-W.
+// Weight gradients are rank-B updates dW += dY^T X per step and projection,
+// from transposed copies of dY and X ([features][B] rows).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bpplan {
+
+struct Shape {
+  int B, n, T_mem;                 // sequences, steps, positions of e / mem
+  int d, H, hd, f, L, W, V, G;     // model
+  bool gate_learned;               // false: z = 0 (u_t = e_t)
+  float eps, theta, scale, inv_temp;
+  int top_k;
+  int Bp;                          // row count of the transposed operands (B rounded up; zero past B)
+};
+
+struct Detach {
+  int s_every;   // > 0: s_t enters step t+1 as a constant when t % s_every == 0
+  bool cache;    // window keys/values of earlier positions enter as constants
+  bool memory;   // the memory enters as a constant (no memory gradient)
+};
+
+// Decoder parameters: matrices in the storage type, gains, bias and s_* fp32.
+template <typename T>
+struct Params {
+  const T *W_g, *W_qkv, *W_O, *W_Qx, *W_Ox, *W_1, *W_3, *W_2, *W_o;
+  const float *b_g, *s_star, *attn_norm, *xattn_norm, *ffn_norm, *head_norm;
+};
+
+// Gradients (fp32, the parameters' shapes); zeroed and accumulated by run().
+struct Grads {
+  float *W_g, *b_g, *W_qkv, *W_O, *W_Qx, *W_Ox, *W_1, *W_3, *W_2, *W_o;
+  float *attn_norm, *xattn_norm, *ffn_norm, *head_norm, *s_star;
+};
+
+// Byte offsets into the workspace.
+struct Layout {
+  size_t wt_g, wt_qkv, wt_O, wt_Qx, wt_Ox, wt_13, wt_2, wt_o;  // transposed weights
+  size_t hist;          // [L][2][B][H][n][hd] keys (after RoPE) and values of every position
+  size_t s_all;         // [n+1][B][d] f32: s_0 = s_*, s_1..s_n
+  size_t lp;            // [B][n] f32
+  size_t ring;          // [L][2][B][H][W][hd] f32 window-gradient ring
+  size_t zero_begin;    // [zero_begin, total) and the ring start at zero
+  // one step's activations
+  size_t xg, xgT, zpre, z;
+  size_t hA, hX, hF;    // [L][B][d] f32 residual stream into attention, cross-attention, FFN
+  size_t rA, rX, rF, rO;
+  size_t a, aT, c, cT, bb, bbT;
+  size_t q, qx, o, ox, oq, oT, oxq, oxT;
+  size_t lse1, lse2;
+  size_t g, u, m, mT;
+  size_t sn, snT, qkv, logits;
+  // gradient scratch
+  size_t ds, dh, dq, dx, dY, dYT;
+  size_t total;
+};
+
+inline size_t bp_align(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace layout after a header of hdr bytes; es = bytes of the storage type.
+inline Layout layout(const Shape& S, size_t es, size_t hdr) {
+  const size_t B = S.B, n = S.n, d = S.d, H = S.H, hd = S.hd, f = S.f, L = S.L, W = S.W, V = S.V, Bp = S.Bp;
+  const size_t Bd = B * d;
+  Layout Lw{};
+  size_t off = bp_align(hdr);
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = bp_align(off + bytes);
+    return o;
+  };
+  Lw.wt_g = take(es * 2 * d * d);
+  Lw.wt_qkv = take(es * L * 3 * d * d);
+  Lw.wt_O = take(es * L * d * d);
+  Lw.wt_Qx = take(es * L * d * d);
+  Lw.wt_Ox = take(es * L * d * d);
+  Lw.wt_13 = take(es * L * 2 * f * d);
+  Lw.wt_2 = take(es * L * f * d);
+  Lw.wt_o = take(es * V * d);
+  Lw.hist = take(es * L * 2 * B * H * n * hd);
+  Lw.s_all = take(4 * (n + 1) * Bd);
+  Lw.lp = take(4 * B * n);
+  Lw.ring = take(4 * L * 2 * B * H * W * hd);
+  Lw.zero_begin = off;
+  Lw.xg = take(es * 2 * Bd);
+  Lw.xgT = take(es * 2 * d * Bp);
+  Lw.zpre = take(4 * Bd);
+  Lw.z = take(4 * Bd);
+  Lw.hA = take(4 * L * Bd);
+  Lw.hX = take(4 * L * Bd);
+  Lw.hF = take(4 * L * Bd);
+  Lw.rA = take(4 * L * B);
+  Lw.rX = take(4 * L * B);
+  Lw.rF = take(4 * L * B);
+  Lw.rO = take(4 * B);
+  Lw.a = take(es * L * Bd);
+  Lw.aT = take(es * L * d * Bp);
+  Lw.c = take(es * L * Bd);
+  Lw.cT = take(es * L * d * Bp);
+  Lw.bb = take(es * L * Bd);
+  Lw.bbT = take(es * L * d * Bp);
+  Lw.q = take(4 * L * Bd);
+  Lw.qx = take(4 * L * Bd);
+  Lw.o = take(4 * L * Bd);
+  Lw.ox = take(4 * L * Bd);
+  Lw.oq = take(es * L * Bd);
+  Lw.oT = take(es * L * d * Bp);
+  Lw.oxq = take(es * L * Bd);
+  Lw.oxT = take(es * L * d * Bp);
+  Lw.lse1 = take(4 * L * B * H);
+  Lw.lse2 = take(4 * L * B * H);
+  Lw.g = take(4 * L * B * f);
+  Lw.u = take(4 * L * B * f);
+  Lw.m = take(es * L * B * f);
+  Lw.mT = take(es * L * f * Bp);
+  Lw.sn = take(es * Bd);
+  Lw.snT = take(es * d * Bp);
+  Lw.qkv = take(4 * 3 * Bd);
+  Lw.logits = take(4 * B * V);
+  Lw.ds = take(4 * Bd);
+  Lw.dh = take(4 * Bd);
+  Lw.dq = take(4 * Bd);
+  size_t nx = 2 * d > f ? 2 * d : f;
+  Lw.dx = take(4 * B * nx);
+  size_t ny = 3 * d;
+  if (2 * f > ny) ny = 2 * f;
+  if (V > ny) ny = V;
+  Lw.dY = take(es * B * ny);
+  Lw.dYT = take(es * ny * Bp);
+  Lw.total = off;
+  return Lw;
+}
+
+#define RLT_BP_TRY(x)          \
+  do {                         \
+    int rc_ = (x);             \
+    if (rc_) return rc_;       \
+  } while (0)
+
+// Inputs/outputs of one call (device pointers for the device Ops).
+template <typename T>
+struct Io {
+  const T* e;              // [B][T_mem][d]
+  const T* mem;            // [G][2][B][H][T_mem][hd]
+  const int32_t* actions;  // [B][n]
+  float* loss;             // [1]
+  float* lp_out;           // [B][n] or null
+  float* d_e;              // [B][T_mem][d] or null
+  float* d_mem;            // [G][2][B][H][T_mem][hd] or null
+};
+
+template <class Ops>
+int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& P, const Io<typename Ops::T>& io,
+        const Grads& G, char* ws, const Layout& Lw) {
+  using T = typename Ops::T;
+  const int B = S.B, n = S.n, d = S.d, H = S.H, hd = S.hd, f = S.f, L = S.L, W = S.W, V = S.V, Bp = S.Bp;
+  const size_t Bd = (size_t)B * d, dd = (size_t)d * d, fd = (size_t)f * d, dBp = (size_t)d * Bp;
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  auto X = [&](size_t off) { return reinterpret_cast<T*>(ws + off); };
+  T* wt_g = X(Lw.wt_g);
+  T* wt_qkv = X(Lw.wt_qkv);
+  T* wt_O = X(Lw.wt_O);
+  T* wt_Qx = X(Lw.wt_Qx);
+  T* wt_Ox = X(Lw.wt_Ox);
+  T* wt_13 = X(Lw.wt_13);
+  T* wt_2 = X(Lw.wt_2);
+  T* wt_o = X(Lw.wt_o);
+  T* hist = X(Lw.hist);
+  float* s_all = F(Lw.s_all);
+  float* lp = F(Lw.lp);
+  float* ring = F(Lw.ring);
+  const size_t plane_h = (size_t)B * H * n * hd;       // one key or value plane of the history
+  const size_t plane_m = (size_t)B * H * S.T_mem * hd;  // of the memory
+  const size_t plane_r = (size_t)B * H * W * hd;       // of the ring
+
+  // ---- set up: zeroed scratch and gradients, transposed weights, s_0
+  RLT_BP_TRY(k.zero(ring, 4 * L * 2 * plane_r));
+  RLT_BP_TRY(k.zero(ws + Lw.zero_begin, Lw.total - Lw.zero_begin));
+  RLT_BP_TRY(k.zero(G.W_g, 4 * 2 * dd));
+  RLT_BP_TRY(k.zero(G.b_g, 4 * (size_t)d));
+  RLT_BP_TRY(k.zero(G.W_qkv, 4 * (size_t)L * 3 * dd));
+  RLT_BP_TRY(k.zero(G.W_O, 4 * (size_t)L * dd));
+  RLT_BP_TRY(k.zero(G.W_Qx, 4 * (size_t)L * dd));
+  RLT_BP_TRY(k.zero(G.W_Ox, 4 * (size_t)L * dd));
+  RLT_BP_TRY(k.zero(G.W_1, 4 * (size_t)L * fd));
+  RLT_BP_TRY(k.zero(G.W_3, 4 * (size_t)L * fd));
+  RLT_BP_TRY(k.zero(G.W_2, 4 * (size_t)L * fd));
+  RLT_BP_TRY(k.zero(G.W_o, 4 * (size_t)V * d));
+  RLT_BP_TRY(k.zero(G.attn_norm, 4 * (size_t)L * d));
+  RLT_BP_TRY(k.zero(G.xattn_norm, 4 * (size_t)L * d));
+  RLT_BP_TRY(k.zero(G.ffn_norm, 4 * (size_t)L * d));
+  RLT_BP_TRY(k.zero(G.head_norm, 4 * (size_t)d));
+  RLT_BP_TRY(k.zero(G.s_star, 4 * (size_t)d));
+  if (io.d_e) RLT_BP_TRY(k.zero(io.d_e, 4 * Bd * S.T_mem));
+  if (io.d_mem) RLT_BP_TRY(k.zero(io.d_mem, 4 * (size_t)S.G * 2 * plane_m));
+  RLT_BP_TRY(k.transpose(P.W_g, d, 2 * d, 2 * d, wt_g, d));
+  for (int l = 0; l < L; ++l) {
+    RLT_BP_TRY(k.transpose(P.W_qkv + l * 3 * dd, 3 * d, d, d, wt_qkv + l * 3 * dd, 3 * d));
+    RLT_BP_TRY(k.transpose(P.W_O + l * dd, d, d, d, wt_O + l * dd, d));
+    RLT_BP_TRY(k.transpose(P.W_Qx + l * dd, d, d, d, wt_Qx + l * dd, d));
+    RLT_BP_TRY(k.transpose(P.W_Ox + l * dd, d, d, d, wt_Ox + l * dd, d));
+    RLT_BP_TRY(k.transpose(P.W_1 + l * fd, f, d, d, wt_13 + l * 2 * fd, 2 * f));
+    RLT_BP_TRY(k.transpose(P.W_3 + l * fd, f, d, d, wt_13 + l * 2 * fd + f, 2 * f));
+    RLT_BP_TRY(k.transpose(P.W_2 + l * fd, d, f, f, wt_2 + l * fd, d));
+  }
+  RLT_BP_TRY(k.transpose(P.W_o, V, d, d, wt_o, V));
+  RLT_BP_TRY(k.bcast_rows(s_all, P.s_star, B, d));
+
+  // ---- step t's forward, activations to the step buffers
+  T* xg = X(Lw.xg);
+  T* xgT = X(Lw.xgT);
+  float* zpre = F(Lw.zpre);
+  float* z = F(Lw.z);
+  float* qkv = F(Lw.qkv);
+  auto fwd = [&](int t) -> int {
+    const int p = t - 1;
+    const float* s_prev = s_all + (size_t)(t - 1) * Bd;
+    if (S.gate_learned) {
+      RLT_BP_TRY(k.merge_in(io.e, S.T_mem, p, s_prev, B, d, xg, xgT, Bp));
+      RLT_BP_TRY(k.gemm(xg, 2 * d, B, 2 * d, P.W_g, 2 * d, d, zpre, d, false));
+    }
+    RLT_BP_TRY(k.merge_out(S.gate_learned ? zpre : nullptr, P.b_g, io.e, S.T_mem, p, s_prev, B, d, z, F(Lw.hA)));
+    for (int l = 0; l < L; ++l) {
+      float* hA = F(Lw.hA) + l * Bd;
+      float* hX = F(Lw.hX) + l * Bd;
+      float* hF = F(Lw.hF) + l * Bd;
+      T* Kl = hist + (size_t)(2 * l) * plane_h;
+      T* Vl = hist + (size_t)(2 * l + 1) * plane_h;
+      // window self-attention
+      RLT_BP_TRY(k.rms_fwd(hA, P.attn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rA) + l * B, X(Lw.a) + l * Bd,
+                           X(Lw.aT) + l * dBp, Bp));
+      RLT_BP_TRY(k.gemm(X(Lw.a) + l * Bd, d, B, d, P.W_qkv + l * 3 * dd, d, 3 * d, qkv, 3 * d, false));
+      RLT_BP_TRY(k.qkv_post(qkv, p, B, H, hd, S.theta, F(Lw.q) + l * Bd, Kl, Vl, n));
+      const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
+      RLT_BP_TRY(k.attn_fwd(F(Lw.q) + l * Bd, Kl, Vl, n, j0, p, B, H, hd, S.scale, F(Lw.lse1) + (size_t)l * B * H,
+                            F(Lw.o) + l * Bd, X(Lw.oq) + l * Bd, X(Lw.oT) + l * dBp, Bp));
+      RLT_BP_TRY(k.copy(hX, hA, 4 * Bd));
+      RLT_BP_TRY(k.gemm(X(Lw.oq) + l * Bd, d, B, d, P.W_O + l * dd, d, d, hX, d, true));
+      // cross-attention to memory positions 0..p
+      RLT_BP_TRY(k.rms_fwd(hX, P.xattn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rX) + l * B, X(Lw.c) + l * Bd,
+                           X(Lw.cT) + l * dBp, Bp));
+      RLT_BP_TRY(k.gemm(X(Lw.c) + l * Bd, d, B, d, P.W_Qx + l * dd, d, d, F(Lw.qx) + l * Bd, d, false));
+      const int g = S.G == 1 ? 0 : l;
+      const T* Mk = io.mem + (size_t)(2 * g) * plane_m;
+      const T* Mv = io.mem + (size_t)(2 * g + 1) * plane_m;
+      RLT_BP_TRY(k.attn_fwd(F(Lw.qx) + l * Bd, Mk, Mv, S.T_mem, 0, p, B, H, hd, S.scale,
+                            F(Lw.lse2) + (size_t)l * B * H, F(Lw.ox) + l * Bd, X(Lw.oxq) + l * Bd,
+                            X(Lw.oxT) + l * dBp, Bp));
+      RLT_BP_TRY(k.copy(hF, hX, 4 * Bd));
+      RLT_BP_TRY(k.gemm(X(Lw.oxq) + l * Bd, d, B, d, P.W_Ox + l * dd, d, d, hF, d, true));
+      // SwiGLU feed-forward
+      RLT_BP_TRY(k.rms_fwd(hF, P.ffn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rF) + l * B, X(Lw.bb) + l * Bd,
+                           X(Lw.bbT) + l * dBp, Bp));
+      float* gl = F(Lw.g) + (size_t)l * B * f;
+      float* ul = F(Lw.u) + (size_t)l * B * f;
+      RLT_BP_TRY(k.gemm(X(Lw.bb) + l * Bd, d, B, d, P.W_1 + l * fd, d, f, gl, f, false));
+      RLT_BP_TRY(k.gemm(X(Lw.bb) + l * Bd, d, B, d, P.W_3 + l * fd, d, f, ul, f, false));
+      RLT_BP_TRY(k.swiglu_fwd(gl, ul, B, f, X(Lw.m) + (size_t)l * B * f, X(Lw.mT) + (size_t)l * f * Bp, Bp));
+      float* next = (l + 1 < L) ? F(Lw.hA) + (l + 1) * Bd : s_all + (size_t)t * Bd;
+      RLT_BP_TRY(k.copy(next, hF, 4 * Bd));
+      RLT_BP_TRY(k.gemm(X(Lw.m) + (size_t)l * B * f, f, B, f, P.W_2 + l * fd, f, d, next, d, true));
+    }
+    return 0;
+  };
+
+  // ---- forward pass: s_t and the keys/values of every position
+  for (int t = 1; t <= n; ++t) RLT_BP_TRY(fwd(t));
+
+  // ---- reverse pass
+  float* ds = F(Lw.ds);  // d L / d s_t from step t+1 (then from the head too)
+  float* dh = F(Lw.dh);
+  float* dq = F(Lw.dq);
+  float* dx = F(Lw.dx);
+  T* dY = X(Lw.dY);
+  T* dYT = X(Lw.dYT);
+  for (int t = n; t >= 1; --t) {
+    const int p = t - 1;
+    RLT_BP_TRY(fwd(t));
+    const float* s_t = s_all + (size_t)t * Bd;
+    const float* s_prev = s_all + (size_t)(t - 1) * Bd;
+    // head: logits = W_o RMSNorm_o(s_t); d logits of -lp
+    RLT_BP_TRY(k.rms_fwd(s_t, P.head_norm, B, d, S.eps, F(Lw.rO), X(Lw.sn), X(Lw.snT), Bp));
+    RLT_BP_TRY(k.gemm(X(Lw.sn), d, B, d, P.W_o, d, V, F(Lw.logits), V, false));
+    RLT_BP_TRY(k.head_bwd(F(Lw.logits), B, V, io.actions, n, p, S.inv_temp, S.top_k, lp, dY, dYT, Bp));
+    RLT_BP_TRY(k.gemm(dYT, Bp, V, Bp, X(Lw.snT), Bp, d, G.W_o, d, true));
+    RLT_BP_TRY(k.gemm(dY, V, B, V, wt_o, V, d, dx, d, false));
+    RLT_BP_TRY(k.rms_bwd(s_t, F(Lw.rO), P.head_norm, dx, B, d, ds, G.head_norm));
+    RLT_BP_TRY(k.copy(dh, ds, 4 * Bd));
+    for (int l = L - 1; l >= 0; --l) {
+      const float* hA = F(Lw.hA) + l * Bd;
+      const float* hX = F(Lw.hX) + l * Bd;
+      const float* hF = F(Lw.hF) + l * Bd;
+      const T* Kl = hist + (size_t)(2 * l) * plane_h;
+      const T* Vl = hist + (size_t)(2 * l + 1) * plane_h;
+      // FFN: h_out = hF + m W_2^T, m = silu(bb W_1^T) * (bb W_3^T)
+      RLT_BP_TRY(k.pack(dh, B, d, dY, dYT, Bp));
+      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, X(Lw.mT) + (size_t)l * f * Bp, Bp, f, G.W_2 + l * fd, f, true));
+      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_2 + l * fd, d, f, dx, f, false));
+      RLT_BP_TRY(k.swiglu_bwd(dx, F(Lw.g) + (size_t)l * B * f, F(Lw.u) + (size_t)l * B * f, B, f, dY, dYT, Bp));
+      RLT_BP_TRY(k.gemm(dYT, Bp, f, Bp, X(Lw.bbT) + l * dBp, Bp, d, G.W_1 + l * fd, d, true));
+      RLT_BP_TRY(k.gemm(dYT + (size_t)f * Bp, Bp, f, Bp, X(Lw.bbT) + l * dBp, Bp, d, G.W_3 + l * fd, d, true));
+      RLT_BP_TRY(k.gemm(dY, 2 * f, B, 2 * f, wt_13 + l * 2 * fd, 2 * f, d, dx, d, false));
+      RLT_BP_TRY(k.rms_bwd(hF, F(Lw.rF) + l * B, P.ffn_norm + (size_t)l * d, dx, B, d, dh,
+                           G.ffn_norm + (size_t)l * d));
+      // cross-attention: hF = hX + ox W_Ox^T
+      RLT_BP_TRY(k.pack(dh, B, d, dY, dYT, Bp));
+      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, X(Lw.oxT) + l * dBp, Bp, d, G.W_Ox + l * dd, d, true));
+      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Ox + l * dd, d, d, dx, d, false));
+      const int g = S.G == 1 ? 0 : l;
+      const T* Mk = io.mem + (size_t)(2 * g) * plane_m;
+      const T* Mv = io.mem + (size_t)(2 * g + 1) * plane_m;
+      float* dMk = (io.d_mem && !D.memory) ? io.d_mem + (size_t)(2 * g) * plane_m : nullptr;
+      float* dMv = (io.d_mem && !D.memory) ? io.d_mem + (size_t)(2 * g + 1) * plane_m : nullptr;
+      RLT_BP_TRY(k.attn_bwd(F(Lw.qx) + l * Bd, dx, F(Lw.ox) + l * Bd, F(Lw.lse2) + (size_t)l * B * H, Mk, Mv,
+                            S.T_mem, 0, p, B, H, hd, S.scale, dq, dMk, dMv, S.T_mem, false, 0));
+      RLT_BP_TRY(k.pack(dq, B, d, dY, dYT, Bp));
+      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, X(Lw.cT) + l * dBp, Bp, d, G.W_Qx + l * dd, d, true));
+      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Qx + l * dd, d, d, dx, d, false));
+      RLT_BP_TRY(k.rms_bwd(hX, F(Lw.rX) + l * B, P.xattn_norm + (size_t)l * d, dx, B, d, dh,
+                           G.xattn_norm + (size_t)l * d));
+      // window self-attention: hX = hA + o W_O^T
+      RLT_BP_TRY(k.pack(dh, B, d, dY, dYT, Bp));
+      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, X(Lw.oT) + l * dBp, Bp, d, G.W_O + l * dd, d, true));
+      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_O + l * dd, d, d, dx, d, false));
+      float* rK = ring + (size_t)(2 * l) * plane_r;
+      float* rV = ring + (size_t)(2 * l + 1) * plane_r;
+      const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
+      RLT_BP_TRY(k.attn_bwd(F(Lw.q) + l * Bd, dx, F(Lw.o) + l * Bd, F(Lw.lse1) + (size_t)l * B * H, Kl, Vl, n, j0,
+                            p, B, H, hd, S.scale, dq, rK, rV, W, true, D.cache ? p : j0));
+      // position p's key/value gradient is complete: through RoPE into d qkv,
+      // and its ring slot is cleared for position p - W
+      RLT_BP_TRY(k.qkv_bwd(dq, rK, rV, W, p, B, H, hd, S.theta, dY, dYT, Bp));
+      RLT_BP_TRY(k.gemm(dYT, Bp, 3 * d, Bp, X(Lw.aT) + l * dBp, Bp, d, G.W_qkv + l * 3 * dd, d, true));
+      RLT_BP_TRY(k.gemm(dY, 3 * d, B, 3 * d, wt_qkv + l * 3 * dd, 3 * d, d, dx, d, false));
+      RLT_BP_TRY(k.rms_bwd(hA, F(Lw.rA) + l * B, P.attn_norm + (size_t)l * d, dx, B, d, dh,
+                           G.attn_norm + (size_t)l * d));
+    }
+    // merge u = z s_{t-1} + (1 - z) e_t, z = sigmoid(W_g [e_t; s_{t-1}] + b_g)
+    RLT_BP_TRY(k.merge_bwd(dh, z, io.e, S.T_mem, p, s_prev, B, d, S.gate_learned, dY, dYT, Bp, G.b_g, io.d_e, ds));
+    if (S.gate_learned) {
+      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, xgT, Bp, 2 * d, G.W_g, 2 * d, true));
+      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_g, d, 2 * d, dx, 2 * d, false));
+      RLT_BP_TRY(k.merge_bwd2(dx, B, d, S.T_mem, p, io.d_e, ds));
+    }
+    // s_{t-1} detached after its step: no gradient from this merge
+    if (t - 1 >= 1 && D.s_every > 0 && (t - 1) % D.s_every == 0) RLT_BP_TRY(k.zero(ds, 4 * Bd));
+  }
+  RLT_BP_TRY(k.colsum(ds, B, d, G.s_star));
+  RLT_BP_TRY(k.loss_sum(lp, io.actions, B, n, V, io.loss));
+  if (io.lp_out) RLT_BP_TRY(k.copy(io.lp_out, lp, 4 * (size_t)B * n));
+  return 0;
+}
+
+}  // namespace bpplan

@@ -1436,7 +1436,7 @@ int validate_cfg(const rlt_config* c) {
 
 extern "C" {
 
-int rlt_abi_version(void) { return 101; }
+int rlt_abi_version(void) { return 102; }
 
 uint64_t rlt_launch_count(void) { return g_launches.load(); }
 
@@ -1858,3 +1858,6 @@ int rlt_status(void* ws, rlt_stream_t stream) {
 }
 
 }  // extern "C"
+
+// backpropagation through time of the decoder (rlt_bptt)
+#include "bptt_api.cuh"

@@ -7,7 +7,8 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (Model, State, rlt_decode_steps, rlt_encode, rlt_state_init, rlt_status)
+from . import (GRAD_FIELDS, RLT_DETACH_CACHE, RLT_DETACH_MEMORY, Model, State, rlt_bptt, rlt_bptt_workspace_size,
+               rlt_decode_steps, rlt_encode, rlt_grads, rlt_state_init, rlt_status, rlt_workspace_init)
 
 
 @dataclass
@@ -64,3 +65,37 @@ def decode(model: Model, st: State, buf: Buffers, n: int, actions: Optional[torc
 
 def status(buf: Buffers, stream=None) -> int:
     return rlt_status(buf.ws, stream)
+
+
+@dataclass
+class BpttResult:
+    loss: torch.Tensor           # [1] f32
+    logp: torch.Tensor           # [B][n] f32
+    grads: dict                  # name -> f32 tensor of the parameter's shape
+    d_e: Optional[torch.Tensor]  # [B][T_mem][d] f32
+    d_mem: Optional[torch.Tensor]
+
+
+def bptt(model: Model, buf: Buffers, actions: torch.Tensor, temperature: float = 1.0, top_k: int = 0,
+         detach_s_every: int = 0, detach_cache: bool = False, detach_memory: bool = False,
+         want_inputs: bool = True, ws: Optional[torch.Tensor] = None, stream=None) -> BpttResult:
+    """Loss and gradients of the teacher-forced sequence (rlt_bptt) over the
+    first n = actions.shape[1] positions of buf's encoder output and memory."""
+    B, n = actions.shape
+    actions = actions.contiguous()
+    assert actions.dtype == torch.int32 and B == buf.B
+    t = model.t
+    grads = {k: torch.empty_like(t[k], dtype=torch.float32) for k in GRAD_FIELDS}
+    cg = rlt_grads(*[grads[k].data_ptr() for k in GRAD_FIELDS])
+    d_e = torch.empty(buf.e.shape, dtype=torch.float32, device="cuda") if want_inputs else None
+    d_mem = torch.empty(buf.mem.shape, dtype=torch.float32, device="cuda") if want_inputs else None
+    if ws is None:
+        nb = rlt_bptt_workspace_size(model.handle, B, n)
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        rlt_workspace_init(ws, nb, stream)
+    loss = torch.empty(1, device="cuda")
+    logp = torch.empty(B, n, device="cuda")
+    flags = (RLT_DETACH_CACHE if detach_cache else 0) | (RLT_DETACH_MEMORY if detach_memory else 0)
+    rlt_bptt(model.handle, buf.e, buf.mem, buf.T, B, n, actions, temperature, top_k, detach_s_every, flags, loss,
+             logp, cg, d_e, d_mem, ws, ws.numel(), stream)
+    return BpttResult(loss, logp, grads, d_e, d_mem)

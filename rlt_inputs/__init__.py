@@ -33,7 +33,7 @@ import numpy as np
 __all__ = [
     "RLTConfig", "Workload", "PRESETS", "preset", "weight_specs", "make_weights",
     "make_tokens", "make_splits", "teacher_actions", "bf16_round_f32",
-    "weights_nbytes",
+    "weights_nbytes", "make_decoder_inputs",
 ]
 
 
@@ -202,6 +202,22 @@ def make_weights(cfg: RLTConfig, seed: int, norm_jitter: float = 0.0,
             a = np.full(shape, gate_bias, np.float32)
         out[name] = np.ascontiguousarray(a, dtype=np.float32)
     return out
+
+
+def make_decoder_inputs(cfg: RLTConfig, B: int, T: int, seed: int, e_scale: float = 1.0,
+                        mem_scale: float = 0.3) -> Tuple[np.ndarray, np.ndarray]:
+    """Seeded stand-ins for the encoder output and memory, for calls that take
+    them as inputs (the decoder's backward pass): e [B, T, d] ~ N(0, e_scale^2)
+    (unit-RMS rows, like an RMSNorm output at unit gain) and mem
+    [G, 2, B, H, T, hd] ~ N(0, mem_scale^2) (a projection of such rows by
+    N(0, sigma^2) weights has std sigma sqrt(d)), float32, bf16-representable
+    for bf16 configurations."""
+    e = _stream(seed, 2000).standard_normal((B, T, cfg.d), dtype=np.float32) * np.float32(e_scale)
+    mem = _stream(seed, 2001).standard_normal((cfg.mem_groups, 2, B, cfg.n_heads, T, cfg.head_dim),
+                                              dtype=np.float32) * np.float32(mem_scale)
+    if cfg.dtype == "bf16":
+        e, mem = bf16_round_f32(e), bf16_round_f32(mem)
+    return np.ascontiguousarray(e), np.ascontiguousarray(mem)
 
 
 def make_tokens(wl: Workload, B: Optional[int] = None, T: Optional[int] = None,

@@ -1,0 +1,362 @@
+// Host-loop stand-ins for the device primitives of the decoder backward, so
+// that the schedule in bptt_plan.h (host logic: step order, the window
+// gradient ring, detach points, transposed operands, workspace layout) can be
+// checked against the float64 oracle without a GPU.  Test infrastructure:
+// the library never uses it.  Each member restates the specification of the
+// kernel of the same name in bptt.cuh, in double arithmetic over fp32
+// storage (the storage type is float here).
+#include "../recurrent_looped_transformer_rlt_b300/csrc/bptt_plan.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <numeric>
+#include <vector>
+
+namespace {
+
+double sigm(double x) { return 1.0 / (1.0 + std::exp(-x)); }
+
+void rope_cs(int p, int i, int hd, float theta, double& c, double& s) {
+  const double a = p * std::pow((double)theta, -2.0 * i / hd);
+  c = std::cos(a);
+  s = std::sin(a);
+}
+
+struct HostOps {
+  using T = float;
+
+  int zero(void* p, size_t bytes) {
+    memset(p, 0, bytes);
+    return 0;
+  }
+  int copy(void* dst, const void* src, size_t bytes) {
+    memmove(dst, src, bytes);
+    return 0;
+  }
+  int transpose(const T* src, int rows, int cols, int lds, T* dst, int ldd) {
+    for (int r = 0; r < rows; ++r)
+      for (int c = 0; c < cols; ++c) dst[(size_t)c * ldd + r] = src[(size_t)r * lds + c];
+    return 0;
+  }
+  // C[M][N] (+)= A[M][K] W[N][K]^T
+  int gemm(const T* A, int lda, int M, int K, const T* W, int ldw, int N, float* C, int ldc, bool add) {
+    for (int m = 0; m < M; ++m)
+      for (int n = 0; n < N; ++n) {
+        double acc = 0;
+        for (int k = 0; k < K; ++k) acc += (double)A[(size_t)m * lda + k] * W[(size_t)n * ldw + k];
+        float& c = C[(size_t)m * ldc + n];
+        c = add ? c + (float)acc : (float)acc;
+      }
+    return 0;
+  }
+  int bcast_rows(float* dst, const float* src, int rows, int d) {
+    for (int r = 0; r < rows; ++r) memcpy(dst + (size_t)r * d, src, sizeof(float) * d);
+    return 0;
+  }
+  int merge_in(const T* e, int T_mem, int p, const float* s, int B, int d, T* xg, T* xgT, int Bp) {
+    for (int b = 0; b < B; ++b)
+      for (int i = 0; i < 2 * d; ++i) {
+        const float v = i < d ? e[((size_t)b * T_mem + p) * d + i] : s[(size_t)b * d + i - d];
+        xg[(size_t)b * 2 * d + i] = v;
+        xgT[(size_t)i * Bp + b] = v;
+      }
+    return 0;
+  }
+  int merge_out(const float* zpre, const float* bg, const T* e, int T_mem, int p, const float* s, int B, int d,
+                float* z, float* h) {
+    for (int b = 0; b < B; ++b)
+      for (int i = 0; i < d; ++i) {
+        const size_t o = (size_t)b * d + i;
+        const double zv = zpre ? sigm((double)zpre[o] + bg[i]) : 0.0;
+        const double ev = e[((size_t)b * T_mem + p) * d + i];
+        z[o] = (float)zv;
+        h[o] = (float)(zv * s[o] + (1 - zv) * ev);
+      }
+    return 0;
+  }
+  int rms_fwd(const float* x, const float* g, int B, int d, float eps, float* r, T* y, T* yT, int Bp) {
+    for (int b = 0; b < B; ++b) {
+      const float* xr = x + (size_t)b * d;
+      double ss = 0;
+      for (int i = 0; i < d; ++i) ss += (double)xr[i] * xr[i];
+      const double rv = 1.0 / std::sqrt(ss / d + eps);
+      r[b] = (float)rv;
+      for (int i = 0; i < d; ++i) {
+        const float v = (float)(xr[i] * rv * g[i]);
+        y[(size_t)b * d + i] = v;
+        if (yT) yT[(size_t)i * Bp + b] = v;
+      }
+    }
+    return 0;
+  }
+  int qkv_post(const float* qkv, int p, int B, int H, int hd, float theta, float* qo, T* K, T* V, int Tk) {
+    const int d = H * hd, half = hd / 2;
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h)
+        for (int i = 0; i < half; ++i) {
+          double c, s;
+          rope_cs(p, i, hd, theta, c, s);
+          const float* row = qkv + (size_t)b * 3 * d + h * hd;
+          float* q = qo + (size_t)b * d + h * hd;
+          q[i] = (float)(row[i] * c - row[i + half] * s);
+          q[i + half] = (float)(row[i + half] * c + row[i] * s);
+          const size_t o = (((size_t)b * H + h) * Tk + p) * hd;
+          K[o + i] = (float)(row[d + i] * c - row[d + i + half] * s);
+          K[o + i + half] = (float)(row[d + i + half] * c + row[d + i] * s);
+          V[o + i] = row[2 * d + i];
+          V[o + i + half] = row[2 * d + i + half];
+        }
+    return 0;
+  }
+  int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
+               float* lse, float* o, T* oq, T* oT, int Bp) {
+    const int d = H * hd;
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h) {
+        const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+        const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+        const float* qq = q + (size_t)b * d + h * hd;
+        std::vector<double> sc;
+        for (int j = j0; j <= j1; ++j) {
+          double a = 0;
+          for (int i = 0; i < hd; ++i) a += (double)qq[i] * Kb[(size_t)j * hd + i];
+          sc.push_back(a * scale);
+        }
+        const double mx = *std::max_element(sc.begin(), sc.end());
+        double l = 0;
+        for (double v : sc) l += std::exp(v - mx);
+        const double ls = mx + std::log(l);
+        lse[b * H + h] = (float)ls;
+        for (int i = 0; i < hd; ++i) {
+          double acc = 0;
+          for (int j = j0; j <= j1; ++j) acc += std::exp(sc[j - j0] - ls) * Vb[(size_t)j * hd + i];
+          const size_t col = (size_t)h * hd + i;
+          o[(size_t)b * d + col] = (float)acc;
+          oq[(size_t)b * d + col] = (float)acc;
+          oT[col * Bp + b] = (float)acc;
+        }
+      }
+    return 0;
+  }
+  int swiglu_fwd(const float* g, const float* u, int B, int f, T* m, T* mT, int Bp) {
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < f; ++j) {
+        const size_t o = (size_t)b * f + j;
+        const double gv = g[o];
+        const float v = (float)(gv * sigm(gv) * u[o]);
+        m[o] = v;
+        mT[(size_t)j * Bp + b] = v;
+      }
+    return 0;
+  }
+  int head_bwd(const float* logits, int B, int V, const int32_t* actions, int n, int p, float inv_temp, int top_k,
+               float* lp, T* dl, T* dlT, int Bp) {
+    for (int b = 0; b < B; ++b) {
+      std::vector<double> x(V);
+      for (int v = 0; v < V; ++v) x[v] = (double)logits[(size_t)b * V + v] * inv_temp;
+      std::vector<char> in(V, 1);
+      if (top_k > 0 && top_k < V) {  // the k largest, ties to the lower id
+        std::vector<int> id(V);
+        std::iota(id.begin(), id.end(), 0);
+        std::stable_sort(id.begin(), id.end(), [&](int a, int c) { return x[a] > x[c]; });
+        std::fill(in.begin(), in.end(), 0);
+        for (int r = 0; r < top_k; ++r) in[id[r]] = 1;
+      }
+      double mx = -1e300, se = 0;
+      for (int v = 0; v < V; ++v)
+        if (in[v]) mx = std::max(mx, x[v]);
+      for (int v = 0; v < V; ++v)
+        if (in[v]) se += std::exp(x[v] - mx);
+      const double ls = mx + std::log(se);
+      int a = actions[(size_t)b * n + p];
+      if (a >= V) a = -1;
+      const bool ain = a >= 0 && in[a];
+      lp[(size_t)b * n + p] = a < 0 ? NAN : (ain ? (float)(x[a] - ls) : -INFINITY);
+      for (int v = 0; v < V; ++v) {
+        double gv = 0;
+        if (a >= 0) gv = inv_temp * ((in[v] ? std::exp(x[v] - ls) : 0.0) - ((v == a && ain) ? 1.0 : 0.0));
+        dl[(size_t)b * V + v] = (float)gv;
+        dlT[(size_t)v * Bp + b] = (float)gv;
+      }
+    }
+    return 0;
+  }
+  int rms_bwd(const float* x, const float* r, const float* g, const float* dy, int B, int d, float* dx, float* dg) {
+    for (int b = 0; b < B; ++b) {
+      const float* xr = x + (size_t)b * d;
+      const float* dyr = dy + (size_t)b * d;
+      double sd = 0;
+      for (int i = 0; i < d; ++i) sd += (double)g[i] * dyr[i] * xr[i];
+      const double rv = r[b], coef = rv * rv * rv * sd / d;
+      for (int i = 0; i < d; ++i) dx[(size_t)b * d + i] += (float)(rv * g[i] * dyr[i] - xr[i] * coef);
+    }
+    for (int i = 0; i < d; ++i) {
+      double acc = 0;
+      for (int b = 0; b < B; ++b) acc += (double)dy[(size_t)b * d + i] * x[(size_t)b * d + i] * r[b];
+      dg[i] += (float)acc;
+    }
+    return 0;
+  }
+  int pack(const float* x, int B, int N, T* y, T* yT, int Bp) {
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < N; ++j) {
+        y[(size_t)b * N + j] = x[(size_t)b * N + j];
+        yT[(size_t)j * Bp + b] = x[(size_t)b * N + j];
+      }
+    return 0;
+  }
+  int swiglu_bwd(const float* dm, const float* g, const float* u, int B, int f, T* dY, T* dYT, int Bp) {
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < f; ++j) {
+        const size_t o = (size_t)b * f + j;
+        const double gv = g[o], uv = u[o], dv = dm[o], sg = sigm(gv);
+        const float dgv = (float)(dv * uv * sg * (1 + gv * (1 - sg))), duv = (float)(dv * gv * sg);
+        dY[(size_t)b * 2 * f + j] = dgv;
+        dY[(size_t)b * 2 * f + f + j] = duv;
+        dYT[(size_t)j * Bp + b] = dgv;
+        dYT[(size_t)(f + j) * Bp + b] = duv;
+      }
+    return 0;
+  }
+  int attn_bwd(const float* q, const float* gout, const float* o, const float* lse, const T* K, const T* V, int Tk,
+               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* dK, float* dV, int Ta, bool ring,
+               int jg) {
+    const int d = H * hd;
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h) {
+        const float* qq = q + (size_t)b * d + h * hd;
+        const float* gg = gout + (size_t)b * d + h * hd;
+        const float* oo = o + (size_t)b * d + h * hd;
+        const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+        const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+        double D = 0;
+        for (int i = 0; i < hd; ++i) D += (double)gg[i] * oo[i];
+        std::vector<double> acc(hd, 0.0);
+        for (int j = j0; j <= j1; ++j) {
+          double s = 0, dp = 0;
+          for (int i = 0; i < hd; ++i) {
+            s += (double)qq[i] * Kb[(size_t)j * hd + i];
+            dp += (double)gg[i] * Vb[(size_t)j * hd + i];
+          }
+          const double P = std::exp(s * scale - lse[b * H + h]), dS = P * (dp - D);
+          for (int i = 0; i < hd; ++i) acc[i] += dS * Kb[(size_t)j * hd + i];
+          if (dK && j >= jg) {
+            const int slot = ring ? j % Ta : j;
+            const size_t base = (((size_t)b * H + h) * Ta + slot) * hd;
+            for (int i = 0; i < hd; ++i) {
+              dK[base + i] += (float)(scale * dS * qq[i]);
+              dV[base + i] += (float)(P * gg[i]);
+            }
+          }
+        }
+        for (int i = 0; i < hd; ++i) dq[(size_t)b * d + h * hd + i] = (float)(scale * acc[i]);
+      }
+    return 0;
+  }
+  int qkv_bwd(const float* dq, float* rK, float* rV, int W, int p, int B, int H, int hd, float theta, T* dY, T* dYT,
+              int Bp) {
+    const int d = H * hd, half = hd / 2;
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h)
+        for (int i = 0; i < half; ++i) {
+          double c, s;
+          rope_cs(p, i, hd, theta, c, s);
+          const size_t rs = (((size_t)b * H + h) * W + p % W) * hd;
+          const double q1 = dq[(size_t)b * d + h * hd + i], q2 = dq[(size_t)b * d + h * hd + i + half];
+          const double k1 = rK[rs + i], k2 = rK[rs + i + half], v1 = rV[rs + i], v2 = rV[rs + i + half];
+          rK[rs + i] = rK[rs + i + half] = rV[rs + i] = rV[rs + i + half] = 0;
+          const double vals[6] = {q1 * c + q2 * s, -q1 * s + q2 * c, k1 * c + k2 * s, -k1 * s + k2 * c, v1, v2};
+          const int cols[6] = {h * hd + i,     h * hd + i + half,     d + h * hd + i,
+                               d + h * hd + i + half, 2 * d + h * hd + i, 2 * d + h * hd + i + half};
+          for (int j = 0; j < 6; ++j) {
+            dY[(size_t)b * 3 * d + cols[j]] = (float)vals[j];
+            dYT[(size_t)cols[j] * Bp + b] = (float)vals[j];
+          }
+        }
+    return 0;
+  }
+  int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, int p, const float* s, int B, int d,
+                bool gate, T* dY, T* dYT, int Bp, float* dbg, float* de, float* ds) {
+    for (int i = 0; i < d; ++i) {
+      double acc = 0;
+      for (int b = 0; b < B; ++b) {
+        const size_t o = (size_t)b * d + i, oe = ((size_t)b * T_mem + p) * d + i;
+        const double g = dh[o], zv = z[o];
+        if (de) de[oe] = (float)(g * (1 - zv));
+        ds[o] = (float)(g * zv);
+        if (gate) {
+          const double dz = g * (s[o] - e[oe]) * zv * (1 - zv);
+          dY[o] = (float)dz;
+          dYT[(size_t)i * Bp + b] = (float)dz;
+          acc += dz;
+        }
+      }
+      if (gate) dbg[i] += (float)acc;
+    }
+    return 0;
+  }
+  int merge_bwd2(const float* dx, int B, int d, int T_mem, int p, float* de, float* ds) {
+    for (int b = 0; b < B; ++b)
+      for (int i = 0; i < d; ++i) {
+        if (de) de[((size_t)b * T_mem + p) * d + i] += dx[(size_t)b * 2 * d + i];
+        ds[(size_t)b * d + i] += dx[(size_t)b * 2 * d + d + i];
+      }
+    return 0;
+  }
+  int colsum(const float* x, int B, int d, float* out) {
+    for (int i = 0; i < d; ++i) {
+      double a = 0;
+      for (int b = 0; b < B; ++b) a += x[(size_t)b * d + i];
+      out[i] += (float)a;
+    }
+    return 0;
+  }
+  int loss_sum(const float* lp, const int32_t* actions, int B, int n, int V, float* loss) {
+    double a = 0;
+    for (size_t i = 0; i < (size_t)B * n; ++i)
+      if (actions[i] >= 0 && actions[i] < V) a -= lp[i];
+    *loss = (float)a;
+    return 0;
+  }
+};
+
+}  // namespace
+
+// sh: B n T_mem d H hd f L W V G gate_learned top_k detach_s_every detach_cache detach_memory
+// fp: rms_eps rope_theta temperature
+// P (in order): W_g W_qkv W_O W_Qx W_Ox W_1 W_3 W_2 W_o b_g s_star dec_attn_norm dec_xattn_norm dec_ffn_norm
+//   head_norm | e mem actions | loss logp | gradients in rlt_grads order | d_e d_mem
+extern "C" int bptt_host(const int* sh, const float* fp, void** P) {
+  bpplan::Shape S{};
+  S.B = sh[0];
+  S.n = sh[1];
+  S.T_mem = sh[2];
+  S.d = sh[3];
+  S.H = sh[4];
+  S.hd = sh[5];
+  S.f = sh[6];
+  S.L = sh[7];
+  S.W = sh[8];
+  S.V = sh[9];
+  S.G = sh[10];
+  S.gate_learned = sh[11] != 0;
+  S.top_k = sh[12];
+  S.eps = fp[0];
+  S.theta = fp[1];
+  S.scale = 1.0f / std::sqrt((float)S.hd);
+  S.inv_temp = 1.0f / fp[2];
+  S.Bp = S.B;
+  const bpplan::Detach D{sh[13], sh[14] != 0, sh[15] != 0};
+  auto cf = [&](int i) { return static_cast<const float*>(P[i]); };
+  auto mf = [&](int i) { return static_cast<float*>(P[i]); };
+  const bpplan::Params<float> Pp{cf(0), cf(1), cf(2),  cf(3),  cf(4),  cf(5),  cf(6), cf(7),
+                                 cf(8), cf(9), cf(10), cf(11), cf(12), cf(13), cf(14)};
+  const bpplan::Io<float> io{cf(15), cf(16), static_cast<const int32_t*>(P[17]), mf(18), mf(19), mf(35), mf(36)};
+  const bpplan::Grads G{mf(20), mf(21), mf(22), mf(23), mf(24), mf(25), mf(26), mf(27),
+                        mf(28), mf(29), mf(30), mf(31), mf(32), mf(33), mf(34)};
+  const bpplan::Layout Lw = bpplan::layout(S, sizeof(float), 256);
+  std::vector<double> ws((Lw.total + 7) / 8);  // 8-byte aligned storage
+  HostOps k;
+  return bpplan::run(k, S, D, Pp, io, G, reinterpret_cast<char*>(ws.data()), Lw);
+}
