@@ -1,7 +1,8 @@
 // Device kernels of the decoder's backpropagation through time (the
 // operations that bptt_plan.h sequences).  Storage type T (fp32 or bf16) for
 // GEMM operands and recorded keys/values; every gradient and reduction in
-// fp32.  Row-major [B][N] operands come with a transposed copy [N][Bp] (the
+// fp32.  Row-major [B][N] operands come with a transposed copy, written to
+// rows of length ldT (one step's column slot of a block operand: the
 // row-contracted operand of the weight-gradient GEMMs).
 //
 // Attention backward (per sequence b, head h, over positions j0..j1): with
@@ -49,13 +50,13 @@ __global__ void transpose_kernel(const T* __restrict__ src, int rows, int cols, 
 // xg[b] = [e[b][p]; s[b]] in the storage type (and transposed).
 template <typename T>
 __global__ void merge_in_kernel(const T* __restrict__ e, int T_mem, int p, const float* __restrict__ s, int B, int d,
-                                T* __restrict__ xg, T* __restrict__ xgT, int Bp) {
+                                T* __restrict__ xg, T* __restrict__ xgT, int ldT) {
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)B * 2 * d) return;
   const int b = (int)(idx / (2 * d)), i = (int)(idx - (size_t)b * 2 * d);
   const T v = (i < d) ? e[((size_t)b * T_mem + p) * d + i] : from_f32<T>(s[(size_t)b * d + i - d]);
   xg[idx] = v;
-  xgT[(size_t)i * Bp + b] = v;
+  if (xgT) xgT[(size_t)i * ldT + b] = v;
 }
 
 // z = sigmoid(zpre + b_g) (0 without a gate), h = z s + (1 - z) e[b][p].
@@ -76,7 +77,7 @@ __global__ void merge_out_kernel(const float* __restrict__ zpre, const float* __
 // transposed when yT is given).  One warp per row.
 template <typename T>
 __global__ void rms_fwd_kernel(const float* __restrict__ x, const float* __restrict__ g, int B, int d, float eps,
-                               float* __restrict__ r, T* __restrict__ y, T* __restrict__ yT, int Bp) {
+                               float* __restrict__ r, T* __restrict__ y, T* __restrict__ yT, int ldT) {
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (row >= B) return;
   const float* xr = x + (size_t)row * d;
@@ -88,7 +89,7 @@ __global__ void rms_fwd_kernel(const float* __restrict__ x, const float* __restr
   for (int i = lane; i < d; i += 32) {
     const T v = from_f32<T>(xr[i] * rv * g[i]);
     y[(size_t)row * d + i] = v;
-    if (yT) yT[(size_t)i * Bp + row] = v;
+    if (yT) yT[(size_t)i * ldT + row] = v;
   }
 }
 
@@ -119,12 +120,13 @@ __global__ void qkv_post_kernel(const float* __restrict__ qkv, int p, int B, int
 }
 
 // Softmax attention of q [B][d] over positions j0..j1 of K, V [B][H][Tk][hd]:
-// lse [B][H], o fp32, oq storage type (and transposed).  One warp per (b, h);
-// lane l holds elements l, l + 32, ... of the head.
+// lse [B][H], the output in the storage type to oq [B][d] (and transposed
+// when oT is given).  One warp per (b, h); lane l holds elements l, l + 32,
+// ... of the head.
 template <typename T>
 __global__ void attn_fwd_kernel(const float* __restrict__ q, const T* __restrict__ K, const T* __restrict__ V, int Tk,
                                 int j0, int j1, int B, int H, int hd, float scale, float* __restrict__ lse,
-                                float* __restrict__ o, T* __restrict__ oq, T* __restrict__ oT, int Bp) {
+                                T* __restrict__ oq, T* __restrict__ oT, int ldT) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
   const int b = pair / H, h = pair - b * H;
@@ -164,27 +166,34 @@ __global__ void attn_fwd_kernel(const float* __restrict__ q, const T* __restrict
   for (int c = 0; c < 4; ++c) {
     const int i = lane + 32 * c;
     if (c < NC && i < hd) {
-      const float v = acc[c] * inv;
       const size_t col = (size_t)h * hd + i;
-      o[(size_t)b * d + col] = v;
-      const T vq = from_f32<T>(v);
+      const T vq = from_f32<T>(acc[c] * inv);
       oq[(size_t)b * d + col] = vq;
-      oT[col * Bp + b] = vq;
+      if (oT) oT[col * ldT + b] = vq;
     }
   }
+}
+
+// yT[j][b] = x[b][j] (rows of a recorded [B][N] operand into a column slot).
+template <typename T>
+__global__ void tcopy_kernel(const T* __restrict__ x, int B, int N, T* __restrict__ yT, int ldT) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * N) return;
+  const int b = (int)(idx / N), j = (int)(idx - (size_t)b * N);
+  yT[(size_t)j * ldT + b] = x[idx];
 }
 
 // m = silu(g) u in the storage type (and transposed).
 template <typename T>
 __global__ void swiglu_fwd_kernel(const float* __restrict__ g, const float* __restrict__ u, int B, int f,
-                                  T* __restrict__ m, T* __restrict__ mT, int Bp) {
+                                  T* __restrict__ m, T* __restrict__ mT, int ldT) {
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)B * f) return;
   const int b = (int)(idx / f), j = (int)(idx - (size_t)b * f);
   const float gv = g[idx];
   const T v = from_f32<T>(gv * sigmoid_acc(gv) * u[idx]);
   m[idx] = v;
-  mT[(size_t)j * Bp + b] = v;
+  if (mT) mT[(size_t)j * ldT + b] = v;
 }
 
 // Order-preserving unsigned key of a float.
@@ -203,7 +212,7 @@ constexpr int kThreadsHead = 1024;
 __global__ void __launch_bounds__(kThreadsHead) head_bwd_kernel(const float* __restrict__ logits, int B, int V,
                                                                  const int32_t* __restrict__ actions, int n, int p,
                                                                  float inv_temp, int top_k, float* __restrict__ lp,
-                                                                 void* dl_, void* dlT_, int Bp, int bf16_out,
+                                                                 void* dl_, void* dlT_, int ldT, int bf16_out,
                                                                  int* status) {
   extern __shared__ float sx[];
   __shared__ unsigned hist[256];
@@ -323,10 +332,10 @@ __global__ void __launch_bounds__(kThreadsHead) head_bwd_kernel(const float* __r
     if (bf16_out) {
       const bf16 q = __float2bfloat16_rn(gv);
       static_cast<bf16*>(dl_)[(size_t)b * V + v] = q;
-      static_cast<bf16*>(dlT_)[(size_t)v * Bp + b] = q;
+      static_cast<bf16*>(dlT_)[(size_t)v * ldT + b] = q;
     } else {
       static_cast<float*>(dl_)[(size_t)b * V + v] = gv;
-      static_cast<float*>(dlT_)[(size_t)v * Bp + b] = gv;
+      static_cast<float*>(dlT_)[(size_t)v * ldT + b] = gv;
     }
   }
 }
@@ -360,13 +369,14 @@ __global__ void rms_bwd_kernel(const float* __restrict__ x, const float* __restr
 
 // y = x in the storage type, and transposed.
 template <typename T>
-__global__ void pack_kernel(const float* __restrict__ x, int B, int N, T* __restrict__ y, T* __restrict__ yT, int Bp) {
+__global__ void pack_kernel(const float* __restrict__ x, int B, int N, T* __restrict__ y, T* __restrict__ yT,
+                            int ldT) {
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)B * N) return;
   const int b = (int)(idx / N), j = (int)(idx - (size_t)b * N);
   const T v = from_f32<T>(x[idx]);
   y[idx] = v;
-  yT[(size_t)j * Bp + b] = v;
+  yT[(size_t)j * ldT + b] = v;
 }
 
 // m = silu(g) u backward: dg = dm u sigma(g) (1 + g (1 - sigma(g))),
@@ -374,7 +384,7 @@ __global__ void pack_kernel(const float* __restrict__ x, int B, int N, T* __rest
 template <typename T>
 __global__ void swiglu_bwd_kernel(const float* __restrict__ dm, const float* __restrict__ g,
                                   const float* __restrict__ u, int B, int f, T* __restrict__ dY, T* __restrict__ dYT,
-                                  int Bp) {
+                                  int ldT) {
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)B * f) return;
   const int b = (int)(idx / f), j = (int)(idx - (size_t)b * f);
@@ -384,19 +394,20 @@ __global__ void swiglu_bwd_kernel(const float* __restrict__ dm, const float* __r
   const T duq = from_f32<T>(dv * gv * sg);
   dY[(size_t)b * 2 * f + j] = dgq;
   dY[(size_t)b * 2 * f + f + j] = duq;
-  dYT[(size_t)j * Bp + b] = dgq;
-  dYT[(size_t)(f + j) * Bp + b] = duq;
+  dYT[(size_t)j * ldT + b] = dgq;
+  dYT[(size_t)(f + j) * ldT + b] = duq;
 }
 
-// Attention backward over positions j0..j1 (see the header): dq [B][d]
-// stored; dK, dV (fp32 accumulators, may be null) += for positions j >= jg,
-// at slot j mod Ta (ring) or j of [B][H][Ta][hd].  One warp per (b, h); each
-// (b, h, j) has one writer.
+// Attention backward over positions j0..j1 (see the header), with D = g.o
+// from the stored output o (storage type): dq [B][d] stored, D to Dout
+// [B][H] when given; dK, dV (fp32 accumulators, may be null) += for positions
+// j >= jg, at slot j mod Ta (ring) or j of [B][H][Ta][hd].  One warp per
+// (b, h); each (b, h, j) has one writer.
 template <typename T>
-__global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __restrict__ gout,
-                                const float* __restrict__ o, const float* __restrict__ lse, const T* __restrict__ K,
-                                const T* __restrict__ V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
-                                float* __restrict__ dq, float* __restrict__ dK, float* __restrict__ dV, int Ta,
+__global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __restrict__ gout, const T* __restrict__ o,
+                                const float* __restrict__ lse, const T* __restrict__ K, const T* __restrict__ V,
+                                int Tk, int j0, int j1, int B, int H, int hd, float scale, float* __restrict__ dq,
+                                float* __restrict__ Dout, float* __restrict__ dK, float* __restrict__ dV, int Ta,
                                 int ring, int jg) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
@@ -413,9 +424,10 @@ __global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __rest
     qr[c] = ok ? q[col] : 0.f;
     gr[c] = ok ? gout[col] : 0.f;
     acc[c] = 0.f;
-    if (ok) Dp = fmaf(gr[c], o[col], Dp);
+    if (ok) Dp = fmaf(gr[c], to_f32(o[col]), Dp);
   }
   const float D = warp_sum(Dp);
+  if (Dout && lane == 0) Dout[pair] = D;
   const float ls = lse[pair];
   const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
   const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
@@ -457,13 +469,122 @@ __global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __rest
   }
 }
 
+// Memory gradient of one block of steps, key-parallel: for every position
+// j <= p_hi of one (b, h),
+//   dK_j += sum scale dS q,  dV_j += sum P g,
+// over the block's steps s < nb whose position p_hi - s >= j and the layers
+// l0 <= l < l1 reading this memory group, with the step's query q (qS),
+// output gradient g (gS) [S][L][B][d], log-sum-exp (lse_all [n][L][B][H] at
+// the step's position) and D (DS [S][L][B][H]); P = exp(scale q.K_j - lse),
+// dS = P (g.V_j - D).  Grid (key blocks of kMemKeys, B * H); each warp owns
+// kMemKeysPerWarp keys (accumulators in registers, one read-modify-write per
+// key at the end); the block's queries pass through shared memory in chunks
+// of kMemQueries.
+constexpr int kMemWarps = 8, kMemKeysPerWarp = 4, kMemKeys = kMemWarps * kMemKeysPerWarp, kMemQueries = 32;
+template <typename T>
+__global__ void __launch_bounds__(kMemWarps * 32) mem_grad_kernel(
+    const T* __restrict__ K, const T* __restrict__ V, int T_mem, const float* __restrict__ qS,
+    const float* __restrict__ gS, const float* __restrict__ lse_all, const float* __restrict__ DS, int L, int l0,
+    int l1, int nb, int p_hi, int B, int H, int hd, float scale, float* __restrict__ dK, float* __restrict__ dV) {
+  __shared__ float sq[kMemQueries][128];
+  __shared__ float sg[kMemQueries][128];
+  __shared__ float sl[kMemQueries], sD[kMemQueries];
+  __shared__ int sp[kMemQueries];
+  const int bh = blockIdx.y, b = bh / H, h = bh - b * H;
+  const int d = H * hd, nl = l1 - l0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int NC = (hd + 31) >> 5;
+  const int jb = blockIdx.x * kMemKeys;            // lowest key of the block
+  if (jb > p_hi) return;                           // uniform over the block
+  const int s_end = min(nb, p_hi - jb + 1);        // steps that reach key jb
+  const int nq = s_end * nl;
+  float kr[kMemKeysPerWarp][4], vr[kMemKeysPerWarp][4], ak[kMemKeysPerWarp][4], av[kMemKeysPerWarp][4];
+  int jj[kMemKeysPerWarp];
+#pragma unroll
+  for (int u = 0; u < kMemKeysPerWarp; ++u) {
+    jj[u] = jb + warp * kMemKeysPerWarp + u;
+    const bool kv_ok = jj[u] <= p_hi;
+    const size_t base = ((size_t)bh * T_mem + (kv_ok ? jj[u] : 0)) * hd;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      const bool ok = kv_ok && c < NC && i < hd;
+      kr[u][c] = ok ? to_f32(K[base + i]) : 0.f;
+      vr[u][c] = ok ? to_f32(V[base + i]) : 0.f;
+      ak[u][c] = 0.f;
+      av[u][c] = 0.f;
+    }
+  }
+  for (int q0 = 0; q0 < nq; q0 += kMemQueries) {
+    const int cnt = min(kMemQueries, nq - q0);
+    __syncthreads();  // the previous chunk is consumed
+    for (int e = threadIdx.x; e < cnt * hd; e += blockDim.x) {
+      const int qi = e / hd, i = e - qi * hd;
+      const int s = (q0 + qi) / nl, l = l0 + (q0 + qi) - s * nl;
+      const size_t row = ((size_t)s * L + l) * B + b;
+      sq[qi][i] = qS[row * d + h * hd + i];
+      sg[qi][i] = gS[row * d + h * hd + i];
+    }
+    for (int qi = threadIdx.x; qi < cnt; qi += blockDim.x) {
+      const int s = (q0 + qi) / nl, l = l0 + (q0 + qi) - s * nl;
+      const int p = p_hi - s;
+      sp[qi] = p;
+      sl[qi] = lse_all[(((size_t)p * L + l) * B + b) * H + h];
+      sD[qi] = DS[(((size_t)s * L + l) * B + b) * H + h];
+    }
+    __syncthreads();
+    for (int qi = 0; qi < cnt; ++qi) {
+      float qv[4], gv[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = lane + 32 * c;
+        const bool ok = c < NC && i < hd;
+        qv[c] = ok ? sq[qi][i] : 0.f;
+        gv[c] = ok ? sg[qi][i] : 0.f;
+      }
+      const int p = sp[qi];
+      const float ls = sl[qi], Dq = sD[qi];
+#pragma unroll
+      for (int u = 0; u < kMemKeysPerWarp; ++u) {
+        if (jj[u] > p) continue;  // uniform over the warp
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          s1 = fmaf(qv[c], kr[u][c], s1);
+          s2 = fmaf(gv[c], vr[u][c], s2);
+        }
+        const float P = expf(warp_sum(s1) * scale - ls);
+        const float dS = P * (warp_sum(s2) - Dq);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          ak[u][c] = fmaf(scale * dS, qv[c], ak[u][c]);
+          av[u][c] = fmaf(P, gv[c], av[u][c]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kMemKeysPerWarp; ++u) {
+    if (jj[u] > p_hi) continue;
+    const size_t base = ((size_t)bh * T_mem + jj[u]) * hd;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) {
+        dK[base + i] += ak[u][c];
+        dV[base + i] += av[u][c];
+      }
+    }
+  }
+}
+
 // d qkv of position p: dq and the completed key gradient (ring slot p mod W)
 // back through RoPE, the value gradient as is; dY [B][3d] (and transposed).
 // Clears the ring slot.  One thread per (b, h, pair i < hd/2).
 template <typename T>
 __global__ void qkv_bwd_kernel(const float* __restrict__ dq, float* __restrict__ rK, float* __restrict__ rV, int W,
                                int p, int B, int H, int hd, float theta, T* __restrict__ dY, T* __restrict__ dYT,
-                               int Bp) {
+                               int ldT) {
   const int half = hd >> 1;
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)B * H * half) return;
@@ -488,7 +609,7 @@ __global__ void qkv_bwd_kernel(const float* __restrict__ dq, float* __restrict__
   for (int j = 0; j < 6; ++j) {
     const T v = from_f32<T>(vals[j]);
     dY[(size_t)b * 3 * d + cols[j]] = v;
-    dYT[(size_t)cols[j] * Bp + b] = v;
+    dYT[(size_t)cols[j] * ldT + b] = v;
   }
 }
 
@@ -499,7 +620,7 @@ __global__ void qkv_bwd_kernel(const float* __restrict__ dq, float* __restrict__
 template <typename T>
 __global__ void merge_bwd_kernel(const float* __restrict__ dh, const float* __restrict__ z, const T* __restrict__ e,
                                  int T_mem, int p, const float* __restrict__ s, int B, int d, int gate,
-                                 T* __restrict__ dY, T* __restrict__ dYT, int Bp, float* __restrict__ dbg,
+                                 T* __restrict__ dY, T* __restrict__ dYT, int ldT, float* __restrict__ dbg,
                                  float* __restrict__ de, float* __restrict__ ds) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= d) return;
@@ -514,7 +635,7 @@ __global__ void merge_bwd_kernel(const float* __restrict__ dh, const float* __re
       const float dz = g * (s[o] - to_f32(e[oe])) * zv * (1.f - zv);
       const T q = from_f32<T>(dz);
       dY[o] = q;
-      dYT[(size_t)i * Bp + b] = q;
+      dYT[(size_t)i * ldT + b] = q;
       acc += dz;
     }
   }

@@ -53,8 +53,8 @@ struct BpttOps {
     bcast_rows_kernel<<<blocks((size_t)rows * d), bptt::kThreads, 0, st>>>(dst, src, rows, d);
     return post();
   }
-  int merge_in(const T* e, int T_mem, int p, const float* s, int B, int d, T* xg, T* xgT, int Bp) {
-    bptt::merge_in_kernel<T><<<blocks((size_t)B * 2 * d), bptt::kThreads, 0, st>>>(e, T_mem, p, s, B, d, xg, xgT, Bp);
+  int merge_in(const T* e, int T_mem, int p, const float* s, int B, int d, T* xg, T* xgT, int ldT) {
+    bptt::merge_in_kernel<T><<<blocks((size_t)B * 2 * d), bptt::kThreads, 0, st>>>(e, T_mem, p, s, B, d, xg, xgT, ldT);
     return post();
   }
   int merge_out(const float* zpre, const float* bg, const T* e, int T_mem, int p, const float* s, int B, int d,
@@ -62,8 +62,8 @@ struct BpttOps {
     bptt::merge_out_kernel<T><<<blocks((size_t)B * d), bptt::kThreads, 0, st>>>(zpre, bg, e, T_mem, p, s, B, d, z, h);
     return post();
   }
-  int rms_fwd(const float* x, const float* g, int B, int d, float eps, float* r, T* y, T* yT, int Bp) {
-    bptt::rms_fwd_kernel<T><<<blocks((size_t)B * 32), bptt::kThreads, 0, st>>>(x, g, B, d, eps, r, y, yT, Bp);
+  int rms_fwd(const float* x, const float* g, int B, int d, float eps, float* r, T* y, T* yT, int ldT) {
+    bptt::rms_fwd_kernel<T><<<blocks((size_t)B * 32), bptt::kThreads, 0, st>>>(x, g, B, d, eps, r, y, yT, ldT);
     return post();
   }
   int qkv_post(const float* qkv, int p, int B, int H, int hd, float theta, float* q, T* K, T* V, int Tk) {
@@ -72,19 +72,23 @@ struct BpttOps {
     return post();
   }
   int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
-               float* lse, float* o, T* oq, T* oT, int Bp) {
+               float* lse, T* oq, T* oT, int ldT) {
     bptt::attn_fwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(q, K, V, Tk, j0, j1, B, H, hd, scale,
-                                                                             lse, o, oq, oT, Bp);
+                                                                             lse, oq, oT, ldT);
     return post();
   }
-  int swiglu_fwd(const float* g, const float* u, int B, int f, T* m, T* mT, int Bp) {
-    bptt::swiglu_fwd_kernel<T><<<blocks((size_t)B * f), bptt::kThreads, 0, st>>>(g, u, B, f, m, mT, Bp);
+  int tcopy(const T* x, int B, int N, T* yT, int ldT) {
+    bptt::tcopy_kernel<T><<<blocks((size_t)B * N), bptt::kThreads, 0, st>>>(x, B, N, yT, ldT);
+    return post();
+  }
+  int swiglu_fwd(const float* g, const float* u, int B, int f, T* m, T* mT, int ldT) {
+    bptt::swiglu_fwd_kernel<T><<<blocks((size_t)B * f), bptt::kThreads, 0, st>>>(g, u, B, f, m, mT, ldT);
     return post();
   }
   int head_bwd(const float* logits, int B, int V, const int32_t* actions, int n, int p, float inv_temp, int top_k,
-               float* lp, T* dl, T* dlT, int Bp) {
+               float* lp, T* dl, T* dlT, int ldT) {
     bptt::head_bwd_kernel<<<B, bptt::kThreadsHead, sizeof(float) * (size_t)V, st>>>(
-        logits, B, V, actions, n, p, inv_temp, top_k, lp, dl, dlT, Bp, kBf16 ? 1 : 0, status);
+        logits, B, V, actions, n, p, inv_temp, top_k, lp, dl, dlT, ldT, kBf16 ? 1 : 0, status);
     return post();
   }
   int rms_bwd(const float* x, const float* r, const float* g, const float* dy, int B, int d, float* dx, float* dg) {
@@ -93,31 +97,39 @@ struct BpttOps {
     bptt::rms_bwd_kernel<<<row_blocks + col_blocks, bptt::kThreads, 0, st>>>(x, r, g, dy, B, d, dx, dg, row_blocks);
     return post();
   }
-  int pack(const float* x, int B, int N, T* y, T* yT, int Bp) {
-    bptt::pack_kernel<T><<<blocks((size_t)B * N), bptt::kThreads, 0, st>>>(x, B, N, y, yT, Bp);
+  int pack(const float* x, int B, int N, T* y, T* yT, int ldT) {
+    bptt::pack_kernel<T><<<blocks((size_t)B * N), bptt::kThreads, 0, st>>>(x, B, N, y, yT, ldT);
     return post();
   }
-  int swiglu_bwd(const float* dm, const float* g, const float* u, int B, int f, T* dY, T* dYT, int Bp) {
-    bptt::swiglu_bwd_kernel<T><<<blocks((size_t)B * f), bptt::kThreads, 0, st>>>(dm, g, u, B, f, dY, dYT, Bp);
+  int swiglu_bwd(const float* dm, const float* g, const float* u, int B, int f, T* dY, T* dYT, int ldT) {
+    bptt::swiglu_bwd_kernel<T><<<blocks((size_t)B * f), bptt::kThreads, 0, st>>>(dm, g, u, B, f, dY, dYT, ldT);
     return post();
   }
-  int attn_bwd(const float* q, const float* gout, const float* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* dK, float* dV, int Ta, bool ring,
-               int jg) {
+  int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
+               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* Dout, float* dK, float* dV, int Ta,
+               bool ring, int jg) {
     bptt::attn_bwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(
-        q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd, scale, dq, dK, dV, Ta, ring ? 1 : 0, jg);
+        q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd, scale, dq, Dout, dK, dV, Ta, ring ? 1 : 0, jg);
+    return post();
+  }
+  int mem_grad(const T* K, const T* V, int T_mem, const float* qS, const float* gS, const float* lse_all,
+               const float* DS, int L, int l0, int l1, int nb, int p_hi, int B, int H, int hd, float scale, float* dK,
+               float* dV) {
+    const dim3 grid(cdiv((size_t)p_hi + 1, bptt::kMemKeys), (unsigned)(B * H));
+    bptt::mem_grad_kernel<T><<<grid, bptt::kMemWarps * 32, 0, st>>>(K, V, T_mem, qS, gS, lse_all, DS, L, l0, l1, nb,
+                                                                    p_hi, B, H, hd, scale, dK, dV);
     return post();
   }
   int qkv_bwd(const float* dq, float* rK, float* rV, int W, int p, int B, int H, int hd, float theta, T* dY, T* dYT,
-              int Bp) {
+              int ldT) {
     bptt::qkv_bwd_kernel<T><<<blocks((size_t)B * H * (hd / 2)), bptt::kThreads, 0, st>>>(dq, rK, rV, W, p, B, H, hd,
-                                                                                        theta, dY, dYT, Bp);
+                                                                                        theta, dY, dYT, ldT);
     return post();
   }
   int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, int p, const float* s, int B, int d,
-                bool gate, T* dY, T* dYT, int Bp, float* dbg, float* de, float* ds) {
+                bool gate, T* dY, T* dYT, int ldT, float* dbg, float* de, float* ds) {
     bptt::merge_bwd_kernel<T><<<blocks((size_t)d), bptt::kThreads, 0, st>>>(dh, z, e, T_mem, p, s, B, d, gate ? 1 : 0,
-                                                                            dY, dYT, Bp, dbg, de, ds);
+                                                                            dY, dYT, ldT, dbg, de, ds);
     return post();
   }
   int merge_bwd2(const float* dx, int B, int d, int T_mem, int p, float* de, float* ds) {
@@ -135,6 +147,9 @@ struct BpttOps {
 };
 
 constexpr size_t kBpttHeader = kWsHeaderBytes;
+// steps per block: weight gradients are added by one GEMM over the block's
+// S * B rows, and the memory gradient by one key-parallel pass per block
+constexpr int kBpttBlock = 16;
 
 bpplan::Shape bptt_shape(const rlt_model* m, int B, int n, int T_mem, float temperature, int top_k) {
   const rlt_config& c = m->cfg;
@@ -156,8 +171,10 @@ bpplan::Shape bptt_shape(const rlt_model* m, int B, int n, int T_mem, float temp
   S.scale = 1.0f / sqrtf((float)c.head_dim);
   S.inv_temp = 1.0f / temperature;
   S.top_k = top_k;
-  // the bf16 weight-gradient GEMMs contract over Bp rows in whole 64-wide k-blocks
+  // the bf16 weight-gradient GEMMs contract over step slots of Bp rows in
+  // whole 64-wide k-blocks
   S.Bp = (c.dtype == RLT_BF16) ? (B + 63) / 64 * 64 : B;
+  S.S = n < kBpttBlock ? n : kBpttBlock;
   return S;
 }
 

@@ -1,8 +1,9 @@
 // Backpropagation through time of the RLT decoder recurrence (teacher
 // forced, full or truncated at named detach points): the order of the
 // operations, the workspace layout and the bookkeeping of the window-gradient
-// ring, written once over a set of primitive operations (Ops, implemented by
-// the device kernels of bptt.cuh).  Plain host C++: no CUDA types.
+// ring and of the step blocks, written once over a set of primitive
+// operations (Ops, implemented by the device kernels of bptt.cuh).  Plain
+// host C++: no CUDA types.
 //
 // What is differentiated (the decoder of "Understanding and Applying the
 // Recurrent Looped Transformer Architecture", "How the Architecture Works",
@@ -17,17 +18,28 @@
 // "Current-Policy Reinforcement Learning Replay": detaching the recurrent
 // outputs, the decoder key-value entries or the memory is an approximation).
 //
-// Schedule.  A forward pass records s_t for every step and the keys and
-// values of every position and layer.  The reverse pass then visits
-// t = n..1: it recomputes step t's activations from s_{t-1} and the recorded
-// keys/values (the same kernels, so bitwise the recorded values), runs the
-// head and the layers backwards, and hands d s_{t-1} to step t-1.  The window
-// keys and values of position j receive gradient from steps j+1..j+W; those
-// arrive (in reverse order) before step j+1 itself is visited, so a ring of W
-// fp32 slots per layer (slot j mod W) holds them until position j's QKV
-// backward consumes and clears its slot, which is then free for position j-W.
-// Weight gradients are rank-B updates dW += dY^T X per step and projection,
-// from transposed copies of dY and X ([features][B] rows).
+// Schedule.
+//  * A forward pass records s_t for every step, the keys and values of every
+//    position and layer, and every layer's cross-attention output and
+//    log-sum-exp.
+//  * The reverse pass visits t = n..1: it recomputes step t's activations
+//    from s_{t-1}, the recorded keys/values and the recorded cross-attention
+//    results (the same kernels, so bitwise the recorded values; the memory is
+//    not read for this), runs the head and the layers backwards, and hands
+//    d s_{t-1} to step t-1.
+//  * The window keys and values of position j receive gradient from steps
+//    j+1..j+W; those arrive (in reverse order) before step j+1 itself is
+//    visited, so a ring of W fp32 slots per layer (slot j mod W) holds them
+//    until position j's QKV backward consumes and clears its slot, which is
+//    then free for position j-W.
+//  * Steps are grouped in blocks of S consecutive steps.  Within a block each
+//    step writes, into its own column slot, the transposed GEMM inputs X and
+//    output gradients dY of every projection ([features][S * Bp]), and its
+//    cross-attention query, output gradient and D = g.o.  At the end of a
+//    block, one GEMM per projection adds dY^T X over the block's S * B rows
+//    to the weight gradient, and one key-parallel pass adds the block's
+//    contributions to the memory gradient (which feeds nothing in the
+//    recurrence, so it can wait).
 #pragma once
 
 #include <stddef.h>
@@ -41,7 +53,8 @@ struct Shape {
   bool gate_learned;               // false: z = 0 (u_t = e_t)
   float eps, theta, scale, inv_temp;
   int top_k;
-  int Bp;                          // row count of the transposed operands (B rounded up; zero past B)
+  int Bp;                          // columns per step slot of the transposed operands (B rounded up; zero past B)
+  int S;                           // steps per block (weight and memory gradients are added once per block)
 };
 
 struct Detach {
@@ -67,21 +80,25 @@ struct Grads {
 struct Layout {
   size_t wt_g, wt_qkv, wt_O, wt_Qx, wt_Ox, wt_13, wt_2, wt_o;  // transposed weights
   size_t hist;          // [L][2][B][H][n][hd] keys (after RoPE) and values of every position
+  size_t xo_all;        // [n][L][B][d] cross-attention outputs (storage type)
+  size_t lse2_all;      // [n][L][B][H] f32 their log-sum-exp
   size_t s_all;         // [n+1][B][d] f32: s_0 = s_*, s_1..s_n
   size_t lp;            // [B][n] f32
   size_t ring;          // [L][2][B][H][W][hd] f32 window-gradient ring
   size_t zero_begin;    // [zero_begin, total) and the ring start at zero
   // one step's activations
-  size_t xg, xgT, zpre, z;
+  size_t xg, zpre, z;
   size_t hA, hX, hF;    // [L][B][d] f32 residual stream into attention, cross-attention, FFN
   size_t rA, rX, rF, rO;
-  size_t a, aT, c, cT, bb, bbT;
-  size_t q, qx, o, ox, oq, oT, oxq, oxT;
-  size_t lse1, lse2;
-  size_t g, u, m, mT;
-  size_t sn, snT, qkv, logits;
+  size_t a, c, bb, q, oq, lse1;
+  size_t g, u, m;
+  size_t sn, qkv, logits;
+  // block operands: [rows][S * Bp], step slot s at columns [s * Bp, (s + 1) * Bp)
+  size_t xgT, aT, cT, bbT, oT, oxT, mT, snT;
+  size_t dlT, dzT, dhfT, dhxT, dhaT, dqxT, dguT, dqkvT;
+  size_t qxS, gxS, DxS;  // [S][L][B][d], [S][L][B][d] f32, [S][L][B][H] f32
   // gradient scratch
-  size_t ds, dh, dq, dx, dY, dYT;
+  size_t ds, dh, dq, dx, dY;
   size_t total;
 };
 
@@ -89,8 +106,8 @@ inline size_t bp_align(size_t x) { return (x + 255) / 256 * 256; }
 
 // Workspace layout after a header of hdr bytes; es = bytes of the storage type.
 inline Layout layout(const Shape& S, size_t es, size_t hdr) {
-  const size_t B = S.B, n = S.n, d = S.d, H = S.H, hd = S.hd, f = S.f, L = S.L, W = S.W, V = S.V, Bp = S.Bp;
-  const size_t Bd = B * d;
+  const size_t B = S.B, n = S.n, d = S.d, H = S.H, hd = S.hd, f = S.f, L = S.L, W = S.W, V = S.V;
+  const size_t Bd = B * d, ldT = (size_t)S.S * S.Bp, SB = S.S;
   Layout Lw{};
   size_t off = bp_align(hdr);
   auto take = [&](size_t bytes) {
@@ -107,12 +124,13 @@ inline Layout layout(const Shape& S, size_t es, size_t hdr) {
   Lw.wt_2 = take(es * L * f * d);
   Lw.wt_o = take(es * V * d);
   Lw.hist = take(es * L * 2 * B * H * n * hd);
+  Lw.xo_all = take(es * n * L * Bd);
+  Lw.lse2_all = take(4 * n * L * B * H);
   Lw.s_all = take(4 * (n + 1) * Bd);
   Lw.lp = take(4 * B * n);
   Lw.ring = take(4 * L * 2 * B * H * W * hd);
   Lw.zero_begin = off;
   Lw.xg = take(es * 2 * Bd);
-  Lw.xgT = take(es * 2 * d * Bp);
   Lw.zpre = take(4 * Bd);
   Lw.z = take(4 * Bd);
   Lw.hA = take(4 * L * Bd);
@@ -123,39 +141,44 @@ inline Layout layout(const Shape& S, size_t es, size_t hdr) {
   Lw.rF = take(4 * L * B);
   Lw.rO = take(4 * B);
   Lw.a = take(es * L * Bd);
-  Lw.aT = take(es * L * d * Bp);
   Lw.c = take(es * L * Bd);
-  Lw.cT = take(es * L * d * Bp);
   Lw.bb = take(es * L * Bd);
-  Lw.bbT = take(es * L * d * Bp);
   Lw.q = take(4 * L * Bd);
-  Lw.qx = take(4 * L * Bd);
-  Lw.o = take(4 * L * Bd);
-  Lw.ox = take(4 * L * Bd);
   Lw.oq = take(es * L * Bd);
-  Lw.oT = take(es * L * d * Bp);
-  Lw.oxq = take(es * L * Bd);
-  Lw.oxT = take(es * L * d * Bp);
   Lw.lse1 = take(4 * L * B * H);
-  Lw.lse2 = take(4 * L * B * H);
   Lw.g = take(4 * L * B * f);
   Lw.u = take(4 * L * B * f);
   Lw.m = take(es * L * B * f);
-  Lw.mT = take(es * L * f * Bp);
   Lw.sn = take(es * Bd);
-  Lw.snT = take(es * d * Bp);
   Lw.qkv = take(4 * 3 * Bd);
   Lw.logits = take(4 * B * V);
+  Lw.xgT = take(es * 2 * d * ldT);
+  Lw.aT = take(es * L * d * ldT);
+  Lw.cT = take(es * L * d * ldT);
+  Lw.bbT = take(es * L * d * ldT);
+  Lw.oT = take(es * L * d * ldT);
+  Lw.oxT = take(es * L * d * ldT);
+  Lw.mT = take(es * L * f * ldT);
+  Lw.snT = take(es * d * ldT);
+  Lw.dlT = take(es * V * ldT);
+  Lw.dzT = take(es * d * ldT);
+  Lw.dhfT = take(es * L * d * ldT);
+  Lw.dhxT = take(es * L * d * ldT);
+  Lw.dhaT = take(es * L * d * ldT);
+  Lw.dqxT = take(es * L * d * ldT);
+  Lw.dguT = take(es * L * 2 * f * ldT);
+  Lw.dqkvT = take(es * L * 3 * d * ldT);
+  Lw.qxS = take(4 * SB * L * Bd);
+  Lw.gxS = take(4 * SB * L * Bd);
+  Lw.DxS = take(4 * SB * L * B * H);
   Lw.ds = take(4 * Bd);
   Lw.dh = take(4 * Bd);
   Lw.dq = take(4 * Bd);
-  size_t nx = 2 * d > f ? 2 * d : f;
-  Lw.dx = take(4 * B * nx);
+  Lw.dx = take(4 * B * (2 * d > f ? 2 * d : f));
   size_t ny = 3 * d;
   if (2 * f > ny) ny = 2 * f;
   if (V > ny) ny = V;
   Lw.dY = take(es * B * ny);
-  Lw.dYT = take(es * ny * Bp);
   Lw.total = off;
   return Lw;
 }
@@ -183,7 +206,10 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
         const Grads& G, char* ws, const Layout& Lw) {
   using T = typename Ops::T;
   const int B = S.B, n = S.n, d = S.d, H = S.H, hd = S.hd, f = S.f, L = S.L, W = S.W, V = S.V, Bp = S.Bp;
-  const size_t Bd = (size_t)B * d, dd = (size_t)d * d, fd = (size_t)f * d, dBp = (size_t)d * Bp;
+  const int SB = S.S;
+  const size_t Bd = (size_t)B * d, BH = (size_t)B * H, dd = (size_t)d * d, fd = (size_t)f * d;
+  const int ldT = SB * Bp;
+  const size_t dT = (size_t)d * ldT;  // one layer of a [L][d][S * Bp] block operand
   auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
   auto X = [&](size_t off) { return reinterpret_cast<T*>(ws + off); };
   T* wt_g = X(Lw.wt_g);
@@ -195,12 +221,15 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
   T* wt_2 = X(Lw.wt_2);
   T* wt_o = X(Lw.wt_o);
   T* hist = X(Lw.hist);
+  T* xo_all = X(Lw.xo_all);
+  float* lse2_all = F(Lw.lse2_all);
   float* s_all = F(Lw.s_all);
   float* lp = F(Lw.lp);
   float* ring = F(Lw.ring);
   const size_t plane_h = (size_t)B * H * n * hd;       // one key or value plane of the history
   const size_t plane_m = (size_t)B * H * S.T_mem * hd;  // of the memory
   const size_t plane_r = (size_t)B * H * W * hd;       // of the ring
+  const bool want_dmem = io.d_mem && !D.memory;
 
   // ---- set up: zeroed scratch and gradients, transposed weights, s_0
   RLT_BP_TRY(k.zero(ring, 4 * L * 2 * plane_r));
@@ -235,17 +264,22 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
   RLT_BP_TRY(k.transpose(P.W_o, V, d, d, wt_o, V));
   RLT_BP_TRY(k.bcast_rows(s_all, P.s_star, B, d));
 
-  // ---- step t's forward, activations to the step buffers
+  // ---- step t's forward.  slot < 0: the recording pass (cross-attention
+  // computed and recorded, no transposed operands); slot >= 0: recomputation
+  // in the reverse pass (recorded cross-attention, operands into the slot).
   T* xg = X(Lw.xg);
-  T* xgT = X(Lw.xgT);
   float* zpre = F(Lw.zpre);
   float* z = F(Lw.z);
   float* qkv = F(Lw.qkv);
-  auto fwd = [&](int t) -> int {
+  // column slot of a block operand: rows_before rows into the buffer at off
+  auto col = [&](size_t off, size_t rows_before, int slot) -> T* {
+    return slot < 0 ? nullptr : X(off) + rows_before * ldT + (size_t)slot * Bp;
+  };
+  auto fwd = [&](int t, int slot) -> int {
     const int p = t - 1;
     const float* s_prev = s_all + (size_t)(t - 1) * Bd;
     if (S.gate_learned) {
-      RLT_BP_TRY(k.merge_in(io.e, S.T_mem, p, s_prev, B, d, xg, xgT, Bp));
+      RLT_BP_TRY(k.merge_in(io.e, S.T_mem, p, s_prev, B, d, xg, col(Lw.xgT, 0, slot), ldT));
       RLT_BP_TRY(k.gemm(xg, 2 * d, B, 2 * d, P.W_g, 2 * d, d, zpre, d, false));
     }
     RLT_BP_TRY(k.merge_out(S.gate_learned ? zpre : nullptr, P.b_g, io.e, S.T_mem, p, s_prev, B, d, z, F(Lw.hA)));
@@ -257,34 +291,38 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       T* Vl = hist + (size_t)(2 * l + 1) * plane_h;
       // window self-attention
       RLT_BP_TRY(k.rms_fwd(hA, P.attn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rA) + l * B, X(Lw.a) + l * Bd,
-                           X(Lw.aT) + l * dBp, Bp));
+                           col(Lw.aT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(X(Lw.a) + l * Bd, d, B, d, P.W_qkv + l * 3 * dd, d, 3 * d, qkv, 3 * d, false));
       RLT_BP_TRY(k.qkv_post(qkv, p, B, H, hd, S.theta, F(Lw.q) + l * Bd, Kl, Vl, n));
       const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
-      RLT_BP_TRY(k.attn_fwd(F(Lw.q) + l * Bd, Kl, Vl, n, j0, p, B, H, hd, S.scale, F(Lw.lse1) + (size_t)l * B * H,
-                            F(Lw.o) + l * Bd, X(Lw.oq) + l * Bd, X(Lw.oT) + l * dBp, Bp));
+      RLT_BP_TRY(k.attn_fwd(F(Lw.q) + l * Bd, Kl, Vl, n, j0, p, B, H, hd, S.scale, F(Lw.lse1) + l * BH,
+                            X(Lw.oq) + l * Bd, col(Lw.oT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.copy(hX, hA, 4 * Bd));
       RLT_BP_TRY(k.gemm(X(Lw.oq) + l * Bd, d, B, d, P.W_O + l * dd, d, d, hX, d, true));
-      // cross-attention to memory positions 0..p
+      // cross-attention to memory positions 0..p (recorded in the first pass)
       RLT_BP_TRY(k.rms_fwd(hX, P.xattn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rX) + l * B, X(Lw.c) + l * Bd,
-                           X(Lw.cT) + l * dBp, Bp));
-      RLT_BP_TRY(k.gemm(X(Lw.c) + l * Bd, d, B, d, P.W_Qx + l * dd, d, d, F(Lw.qx) + l * Bd, d, false));
-      const int g = S.G == 1 ? 0 : l;
-      const T* Mk = io.mem + (size_t)(2 * g) * plane_m;
-      const T* Mv = io.mem + (size_t)(2 * g + 1) * plane_m;
-      RLT_BP_TRY(k.attn_fwd(F(Lw.qx) + l * Bd, Mk, Mv, S.T_mem, 0, p, B, H, hd, S.scale,
-                            F(Lw.lse2) + (size_t)l * B * H, F(Lw.ox) + l * Bd, X(Lw.oxq) + l * Bd,
-                            X(Lw.oxT) + l * dBp, Bp));
+                           col(Lw.cT, (size_t)l * d, slot), ldT));
+      float* qx = slot < 0 ? qkv : F(Lw.qxS) + ((size_t)slot * L + l) * Bd;
+      RLT_BP_TRY(k.gemm(X(Lw.c) + l * Bd, d, B, d, P.W_Qx + l * dd, d, d, qx, d, false));
+      T* xo = xo_all + ((size_t)p * L + l) * Bd;
+      if (slot < 0) {
+        const int g = S.G == 1 ? 0 : l;
+        RLT_BP_TRY(k.attn_fwd(qx, io.mem + (size_t)(2 * g) * plane_m, io.mem + (size_t)(2 * g + 1) * plane_m,
+                              S.T_mem, 0, p, B, H, hd, S.scale, lse2_all + ((size_t)p * L + l) * BH, xo, nullptr,
+                              ldT));
+      } else {
+        RLT_BP_TRY(k.tcopy(xo, B, d, col(Lw.oxT, (size_t)l * d, slot), ldT));
+      }
       RLT_BP_TRY(k.copy(hF, hX, 4 * Bd));
-      RLT_BP_TRY(k.gemm(X(Lw.oxq) + l * Bd, d, B, d, P.W_Ox + l * dd, d, d, hF, d, true));
+      RLT_BP_TRY(k.gemm(xo, d, B, d, P.W_Ox + l * dd, d, d, hF, d, true));
       // SwiGLU feed-forward
       RLT_BP_TRY(k.rms_fwd(hF, P.ffn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rF) + l * B, X(Lw.bb) + l * Bd,
-                           X(Lw.bbT) + l * dBp, Bp));
+                           col(Lw.bbT, (size_t)l * d, slot), ldT));
       float* gl = F(Lw.g) + (size_t)l * B * f;
       float* ul = F(Lw.u) + (size_t)l * B * f;
       RLT_BP_TRY(k.gemm(X(Lw.bb) + l * Bd, d, B, d, P.W_1 + l * fd, d, f, gl, f, false));
       RLT_BP_TRY(k.gemm(X(Lw.bb) + l * Bd, d, B, d, P.W_3 + l * fd, d, f, ul, f, false));
-      RLT_BP_TRY(k.swiglu_fwd(gl, ul, B, f, X(Lw.m) + (size_t)l * B * f, X(Lw.mT) + (size_t)l * f * Bp, Bp));
+      RLT_BP_TRY(k.swiglu_fwd(gl, ul, B, f, X(Lw.m) + (size_t)l * B * f, col(Lw.mT, (size_t)l * f, slot), ldT));
       float* next = (l + 1 < L) ? F(Lw.hA) + (l + 1) * Bd : s_all + (size_t)t * Bd;
       RLT_BP_TRY(k.copy(next, hF, 4 * Bd));
       RLT_BP_TRY(k.gemm(X(Lw.m) + (size_t)l * B * f, f, B, f, P.W_2 + l * fd, f, d, next, d, true));
@@ -292,8 +330,39 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
     return 0;
   };
 
-  // ---- forward pass: s_t and the keys/values of every position
-  for (int t = 1; t <= n; ++t) RLT_BP_TRY(fwd(t));
+  // ---- end of a block of nb steps whose highest position is p_hi (step slot
+  // s holds position p_hi - s): weight gradients over the block's rows, then
+  // the block's memory-gradient contributions
+  auto flush = [&](int nb, int p_hi) -> int {
+    const int K = nb * Bp;
+    RLT_BP_TRY(k.gemm(X(Lw.dlT), ldT, V, K, X(Lw.snT), ldT, d, G.W_o, d, true));
+    if (S.gate_learned) RLT_BP_TRY(k.gemm(X(Lw.dzT), ldT, d, K, X(Lw.xgT), ldT, 2 * d, G.W_g, 2 * d, true));
+    for (int l = 0; l < L; ++l) {
+      const T* bbT = X(Lw.bbT) + l * dT;
+      const T* dguT = X(Lw.dguT) + (size_t)l * 2 * f * ldT;
+      RLT_BP_TRY(k.gemm(X(Lw.dhfT) + l * dT, ldT, d, K, X(Lw.mT) + (size_t)l * f * ldT, ldT, f, G.W_2 + l * fd, f,
+                        true));
+      RLT_BP_TRY(k.gemm(dguT, ldT, f, K, bbT, ldT, d, G.W_1 + l * fd, d, true));
+      RLT_BP_TRY(k.gemm(dguT + (size_t)f * ldT, ldT, f, K, bbT, ldT, d, G.W_3 + l * fd, d, true));
+      RLT_BP_TRY(k.gemm(X(Lw.dhxT) + l * dT, ldT, d, K, X(Lw.oxT) + l * dT, ldT, d, G.W_Ox + l * dd, d, true));
+      RLT_BP_TRY(k.gemm(X(Lw.dqxT) + l * dT, ldT, d, K, X(Lw.cT) + l * dT, ldT, d, G.W_Qx + l * dd, d, true));
+      RLT_BP_TRY(k.gemm(X(Lw.dhaT) + l * dT, ldT, d, K, X(Lw.oT) + l * dT, ldT, d, G.W_O + l * dd, d, true));
+      RLT_BP_TRY(k.gemm(X(Lw.dqkvT) + (size_t)l * 3 * dT, ldT, 3 * d, K, X(Lw.aT) + l * dT, ldT, d,
+                        G.W_qkv + l * 3 * dd, d, true));
+    }
+    if (want_dmem) {
+      for (int g = 0; g < S.G; ++g) {
+        const int l0 = S.G == 1 ? 0 : g, l1 = S.G == 1 ? L : g + 1;
+        RLT_BP_TRY(k.mem_grad(io.mem + (size_t)(2 * g) * plane_m, io.mem + (size_t)(2 * g + 1) * plane_m, S.T_mem,
+                              F(Lw.qxS), F(Lw.gxS), lse2_all, F(Lw.DxS), L, l0, l1, nb, p_hi, B, H, hd, S.scale,
+                              io.d_mem + (size_t)(2 * g) * plane_m, io.d_mem + (size_t)(2 * g + 1) * plane_m));
+      }
+    }
+    return 0;
+  };
+
+  // ---- forward pass: s_t, every position's keys/values, cross-attention results
+  for (int t = 1; t <= n; ++t) RLT_BP_TRY(fwd(t, -1));
 
   // ---- reverse pass
   float* ds = F(Lw.ds);  // d L / d s_t from step t+1 (then from the head too)
@@ -301,17 +370,17 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
   float* dq = F(Lw.dq);
   float* dx = F(Lw.dx);
   T* dY = X(Lw.dY);
-  T* dYT = X(Lw.dYT);
+  int slot = 0, p_hi = n - 1;
   for (int t = n; t >= 1; --t) {
     const int p = t - 1;
-    RLT_BP_TRY(fwd(t));
+    RLT_BP_TRY(fwd(t, slot));
     const float* s_t = s_all + (size_t)t * Bd;
     const float* s_prev = s_all + (size_t)(t - 1) * Bd;
     // head: logits = W_o RMSNorm_o(s_t); d logits of -lp
-    RLT_BP_TRY(k.rms_fwd(s_t, P.head_norm, B, d, S.eps, F(Lw.rO), X(Lw.sn), X(Lw.snT), Bp));
+    RLT_BP_TRY(k.rms_fwd(s_t, P.head_norm, B, d, S.eps, F(Lw.rO), X(Lw.sn), col(Lw.snT, 0, slot), ldT));
     RLT_BP_TRY(k.gemm(X(Lw.sn), d, B, d, P.W_o, d, V, F(Lw.logits), V, false));
-    RLT_BP_TRY(k.head_bwd(F(Lw.logits), B, V, io.actions, n, p, S.inv_temp, S.top_k, lp, dY, dYT, Bp));
-    RLT_BP_TRY(k.gemm(dYT, Bp, V, Bp, X(Lw.snT), Bp, d, G.W_o, d, true));
+    RLT_BP_TRY(k.head_bwd(F(Lw.logits), B, V, io.actions, n, p, S.inv_temp, S.top_k, lp, dY, col(Lw.dlT, 0, slot),
+                          ldT));
     RLT_BP_TRY(k.gemm(dY, V, B, V, wt_o, V, d, dx, d, false));
     RLT_BP_TRY(k.rms_bwd(s_t, F(Lw.rO), P.head_norm, dx, B, d, ds, G.head_norm));
     RLT_BP_TRY(k.copy(dh, ds, 4 * Bd));
@@ -322,57 +391,56 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       const T* Kl = hist + (size_t)(2 * l) * plane_h;
       const T* Vl = hist + (size_t)(2 * l + 1) * plane_h;
       // FFN: h_out = hF + m W_2^T, m = silu(bb W_1^T) * (bb W_3^T)
-      RLT_BP_TRY(k.pack(dh, B, d, dY, dYT, Bp));
-      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, X(Lw.mT) + (size_t)l * f * Bp, Bp, f, G.W_2 + l * fd, f, true));
+      RLT_BP_TRY(k.pack(dh, B, d, dY, col(Lw.dhfT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_2 + l * fd, d, f, dx, f, false));
-      RLT_BP_TRY(k.swiglu_bwd(dx, F(Lw.g) + (size_t)l * B * f, F(Lw.u) + (size_t)l * B * f, B, f, dY, dYT, Bp));
-      RLT_BP_TRY(k.gemm(dYT, Bp, f, Bp, X(Lw.bbT) + l * dBp, Bp, d, G.W_1 + l * fd, d, true));
-      RLT_BP_TRY(k.gemm(dYT + (size_t)f * Bp, Bp, f, Bp, X(Lw.bbT) + l * dBp, Bp, d, G.W_3 + l * fd, d, true));
+      RLT_BP_TRY(k.swiglu_bwd(dx, F(Lw.g) + (size_t)l * B * f, F(Lw.u) + (size_t)l * B * f, B, f, dY,
+                              col(Lw.dguT, (size_t)l * 2 * f, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, 2 * f, B, 2 * f, wt_13 + l * 2 * fd, 2 * f, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hF, F(Lw.rF) + l * B, P.ffn_norm + (size_t)l * d, dx, B, d, dh,
                            G.ffn_norm + (size_t)l * d));
-      // cross-attention: hF = hX + ox W_Ox^T
-      RLT_BP_TRY(k.pack(dh, B, d, dY, dYT, Bp));
-      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, X(Lw.oxT) + l * dBp, Bp, d, G.W_Ox + l * dd, d, true));
-      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Ox + l * dd, d, d, dx, d, false));
+      // cross-attention: hF = hX + ox W_Ox^T; the query gradient now, the
+      // memory gradient at the end of the block
+      RLT_BP_TRY(k.pack(dh, B, d, dY, col(Lw.dhxT, (size_t)l * d, slot), ldT));
+      float* gx = F(Lw.gxS) + ((size_t)slot * L + l) * Bd;
+      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Ox + l * dd, d, d, gx, d, false));
       const int g = S.G == 1 ? 0 : l;
-      const T* Mk = io.mem + (size_t)(2 * g) * plane_m;
-      const T* Mv = io.mem + (size_t)(2 * g + 1) * plane_m;
-      float* dMk = (io.d_mem && !D.memory) ? io.d_mem + (size_t)(2 * g) * plane_m : nullptr;
-      float* dMv = (io.d_mem && !D.memory) ? io.d_mem + (size_t)(2 * g + 1) * plane_m : nullptr;
-      RLT_BP_TRY(k.attn_bwd(F(Lw.qx) + l * Bd, dx, F(Lw.ox) + l * Bd, F(Lw.lse2) + (size_t)l * B * H, Mk, Mv,
-                            S.T_mem, 0, p, B, H, hd, S.scale, dq, dMk, dMv, S.T_mem, false, 0));
-      RLT_BP_TRY(k.pack(dq, B, d, dY, dYT, Bp));
-      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, X(Lw.cT) + l * dBp, Bp, d, G.W_Qx + l * dd, d, true));
+      RLT_BP_TRY(k.attn_bwd(F(Lw.qxS) + ((size_t)slot * L + l) * Bd, gx, xo_all + ((size_t)p * L + l) * Bd,
+                            lse2_all + ((size_t)p * L + l) * BH, io.mem + (size_t)(2 * g) * plane_m,
+                            io.mem + (size_t)(2 * g + 1) * plane_m, S.T_mem, 0, p, B, H, hd, S.scale, dq,
+                            F(Lw.DxS) + ((size_t)slot * L + l) * BH, nullptr, nullptr, 0, false, 0));
+      RLT_BP_TRY(k.pack(dq, B, d, dY, col(Lw.dqxT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Qx + l * dd, d, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hX, F(Lw.rX) + l * B, P.xattn_norm + (size_t)l * d, dx, B, d, dh,
                            G.xattn_norm + (size_t)l * d));
       // window self-attention: hX = hA + o W_O^T
-      RLT_BP_TRY(k.pack(dh, B, d, dY, dYT, Bp));
-      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, X(Lw.oT) + l * dBp, Bp, d, G.W_O + l * dd, d, true));
+      RLT_BP_TRY(k.pack(dh, B, d, dY, col(Lw.dhaT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_O + l * dd, d, d, dx, d, false));
       float* rK = ring + (size_t)(2 * l) * plane_r;
       float* rV = ring + (size_t)(2 * l + 1) * plane_r;
       const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
-      RLT_BP_TRY(k.attn_bwd(F(Lw.q) + l * Bd, dx, F(Lw.o) + l * Bd, F(Lw.lse1) + (size_t)l * B * H, Kl, Vl, n, j0,
-                            p, B, H, hd, S.scale, dq, rK, rV, W, true, D.cache ? p : j0));
+      RLT_BP_TRY(k.attn_bwd(F(Lw.q) + l * Bd, dx, X(Lw.oq) + l * Bd, F(Lw.lse1) + l * BH, Kl, Vl, n, j0, p, B, H,
+                            hd, S.scale, dq, nullptr, rK, rV, W, true, D.cache ? p : j0));
       // position p's key/value gradient is complete: through RoPE into d qkv,
       // and its ring slot is cleared for position p - W
-      RLT_BP_TRY(k.qkv_bwd(dq, rK, rV, W, p, B, H, hd, S.theta, dY, dYT, Bp));
-      RLT_BP_TRY(k.gemm(dYT, Bp, 3 * d, Bp, X(Lw.aT) + l * dBp, Bp, d, G.W_qkv + l * 3 * dd, d, true));
+      RLT_BP_TRY(k.qkv_bwd(dq, rK, rV, W, p, B, H, hd, S.theta, dY, col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, 3 * d, B, 3 * d, wt_qkv + l * 3 * dd, 3 * d, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hA, F(Lw.rA) + l * B, P.attn_norm + (size_t)l * d, dx, B, d, dh,
                            G.attn_norm + (size_t)l * d));
     }
     // merge u = z s_{t-1} + (1 - z) e_t, z = sigmoid(W_g [e_t; s_{t-1}] + b_g)
-    RLT_BP_TRY(k.merge_bwd(dh, z, io.e, S.T_mem, p, s_prev, B, d, S.gate_learned, dY, dYT, Bp, G.b_g, io.d_e, ds));
+    RLT_BP_TRY(k.merge_bwd(dh, z, io.e, S.T_mem, p, s_prev, B, d, S.gate_learned, dY, col(Lw.dzT, 0, slot), ldT,
+                           G.b_g, io.d_e, ds));
     if (S.gate_learned) {
-      RLT_BP_TRY(k.gemm(dYT, Bp, d, Bp, xgT, Bp, 2 * d, G.W_g, 2 * d, true));
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_g, d, 2 * d, dx, 2 * d, false));
       RLT_BP_TRY(k.merge_bwd2(dx, B, d, S.T_mem, p, io.d_e, ds));
     }
     // s_{t-1} detached after its step: no gradient from this merge
     if (t - 1 >= 1 && D.s_every > 0 && (t - 1) % D.s_every == 0) RLT_BP_TRY(k.zero(ds, 4 * Bd));
+    if (++slot == SB || t == 1) {
+      RLT_BP_TRY(flush(slot, p_hi));
+      slot = 0;
+      p_hi = t - 2;
+    }
   }
   RLT_BP_TRY(k.colsum(ds, B, d, G.s_star));
   RLT_BP_TRY(k.loss_sum(lp, io.actions, B, n, V, io.loss));

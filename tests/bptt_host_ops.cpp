@@ -54,12 +54,12 @@ struct HostOps {
     for (int r = 0; r < rows; ++r) memcpy(dst + (size_t)r * d, src, sizeof(float) * d);
     return 0;
   }
-  int merge_in(const T* e, int T_mem, int p, const float* s, int B, int d, T* xg, T* xgT, int Bp) {
+  int merge_in(const T* e, int T_mem, int p, const float* s, int B, int d, T* xg, T* xgT, int ldT) {
     for (int b = 0; b < B; ++b)
       for (int i = 0; i < 2 * d; ++i) {
         const float v = i < d ? e[((size_t)b * T_mem + p) * d + i] : s[(size_t)b * d + i - d];
         xg[(size_t)b * 2 * d + i] = v;
-        xgT[(size_t)i * Bp + b] = v;
+        if (xgT) xgT[(size_t)i * ldT + b] = v;
       }
     return 0;
   }
@@ -75,7 +75,7 @@ struct HostOps {
       }
     return 0;
   }
-  int rms_fwd(const float* x, const float* g, int B, int d, float eps, float* r, T* y, T* yT, int Bp) {
+  int rms_fwd(const float* x, const float* g, int B, int d, float eps, float* r, T* y, T* yT, int ldT) {
     for (int b = 0; b < B; ++b) {
       const float* xr = x + (size_t)b * d;
       double ss = 0;
@@ -85,7 +85,7 @@ struct HostOps {
       for (int i = 0; i < d; ++i) {
         const float v = (float)(xr[i] * rv * g[i]);
         y[(size_t)b * d + i] = v;
-        if (yT) yT[(size_t)i * Bp + b] = v;
+        if (yT) yT[(size_t)i * ldT + b] = v;
       }
     }
     return 0;
@@ -110,7 +110,7 @@ struct HostOps {
     return 0;
   }
   int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
-               float* lse, float* o, T* oq, T* oT, int Bp) {
+               float* lse, T* oq, T* oT, int ldT) {
     const int d = H * hd;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h) {
@@ -131,27 +131,31 @@ struct HostOps {
         for (int i = 0; i < hd; ++i) {
           double acc = 0;
           for (int j = j0; j <= j1; ++j) acc += std::exp(sc[j - j0] - ls) * Vb[(size_t)j * hd + i];
-          const size_t col = (size_t)h * hd + i;
-          o[(size_t)b * d + col] = (float)acc;
-          oq[(size_t)b * d + col] = (float)acc;
-          oT[col * Bp + b] = (float)acc;
+          const size_t c = (size_t)h * hd + i;
+          oq[(size_t)b * d + c] = (float)acc;
+          if (oT) oT[c * ldT + b] = (float)acc;
         }
       }
     return 0;
   }
-  int swiglu_fwd(const float* g, const float* u, int B, int f, T* m, T* mT, int Bp) {
+  int tcopy(const T* x, int B, int N, T* yT, int ldT) {
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < N; ++j) yT[(size_t)j * ldT + b] = x[(size_t)b * N + j];
+    return 0;
+  }
+  int swiglu_fwd(const float* g, const float* u, int B, int f, T* m, T* mT, int ldT) {
     for (int b = 0; b < B; ++b)
       for (int j = 0; j < f; ++j) {
         const size_t o = (size_t)b * f + j;
         const double gv = g[o];
         const float v = (float)(gv * sigm(gv) * u[o]);
         m[o] = v;
-        mT[(size_t)j * Bp + b] = v;
+        if (mT) mT[(size_t)j * ldT + b] = v;
       }
     return 0;
   }
   int head_bwd(const float* logits, int B, int V, const int32_t* actions, int n, int p, float inv_temp, int top_k,
-               float* lp, T* dl, T* dlT, int Bp) {
+               float* lp, T* dl, T* dlT, int ldT) {
     for (int b = 0; b < B; ++b) {
       std::vector<double> x(V);
       for (int v = 0; v < V; ++v) x[v] = (double)logits[(size_t)b * V + v] * inv_temp;
@@ -177,7 +181,7 @@ struct HostOps {
         double gv = 0;
         if (a >= 0) gv = inv_temp * ((in[v] ? std::exp(x[v] - ls) : 0.0) - ((v == a && ain) ? 1.0 : 0.0));
         dl[(size_t)b * V + v] = (float)gv;
-        dlT[(size_t)v * Bp + b] = (float)gv;
+        dlT[(size_t)v * ldT + b] = (float)gv;
       }
     }
     return 0;
@@ -198,15 +202,15 @@ struct HostOps {
     }
     return 0;
   }
-  int pack(const float* x, int B, int N, T* y, T* yT, int Bp) {
+  int pack(const float* x, int B, int N, T* y, T* yT, int ldT) {
     for (int b = 0; b < B; ++b)
       for (int j = 0; j < N; ++j) {
         y[(size_t)b * N + j] = x[(size_t)b * N + j];
-        yT[(size_t)j * Bp + b] = x[(size_t)b * N + j];
+        yT[(size_t)j * ldT + b] = x[(size_t)b * N + j];
       }
     return 0;
   }
-  int swiglu_bwd(const float* dm, const float* g, const float* u, int B, int f, T* dY, T* dYT, int Bp) {
+  int swiglu_bwd(const float* dm, const float* g, const float* u, int B, int f, T* dY, T* dYT, int ldT) {
     for (int b = 0; b < B; ++b)
       for (int j = 0; j < f; ++j) {
         const size_t o = (size_t)b * f + j;
@@ -214,24 +218,27 @@ struct HostOps {
         const float dgv = (float)(dv * uv * sg * (1 + gv * (1 - sg))), duv = (float)(dv * gv * sg);
         dY[(size_t)b * 2 * f + j] = dgv;
         dY[(size_t)b * 2 * f + f + j] = duv;
-        dYT[(size_t)j * Bp + b] = dgv;
-        dYT[(size_t)(f + j) * Bp + b] = duv;
+        dYT[(size_t)j * ldT + b] = dgv;
+        dYT[(size_t)(f + j) * ldT + b] = duv;
       }
     return 0;
   }
-  int attn_bwd(const float* q, const float* gout, const float* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* dK, float* dV, int Ta, bool ring,
-               int jg) {
+  // D = g.o from the stored output o; dK/dV accumulated for positions >= jg
+  // (slot j mod Ta in a ring, else j); D written to Dout when given
+  int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
+               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* Dout, float* dK, float* dV, int Ta,
+               bool ring, int jg) {
     const int d = H * hd;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h) {
         const float* qq = q + (size_t)b * d + h * hd;
         const float* gg = gout + (size_t)b * d + h * hd;
-        const float* oo = o + (size_t)b * d + h * hd;
+        const T* oo = o + (size_t)b * d + h * hd;
         const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
         const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
         double D = 0;
         for (int i = 0; i < hd; ++i) D += (double)gg[i] * oo[i];
+        if (Dout) Dout[b * H + h] = (float)D;
         std::vector<double> acc(hd, 0.0);
         for (int j = j0; j <= j1; ++j) {
           double s = 0, dp = 0;
@@ -254,8 +261,46 @@ struct HostOps {
       }
     return 0;
   }
+  // memory gradient of one block: for every position j <= p_hi, the steps
+  // s < nb of the block (position p_hi - s >= j) and the layers [l0, l1)
+  int mem_grad(const T* K, const T* V, int T_mem, const float* qS, const float* gS, const float* lse_all,
+               const float* DS, int L, int l0, int l1, int nb, int p_hi, int B, int H, int hd, float scale, float* dK,
+               float* dV) {
+    const int d = H * hd;
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h)
+        for (int j = 0; j <= p_hi; ++j) {
+          const T* kj = K + (((size_t)b * H + h) * T_mem + j) * hd;
+          const T* vj = V + (((size_t)b * H + h) * T_mem + j) * hd;
+          std::vector<double> ak(hd, 0.0), av(hd, 0.0);
+          for (int s = 0; s < nb && p_hi - s >= j; ++s)
+            for (int l = l0; l < l1; ++l) {
+              const size_t row = ((size_t)s * L + l) * B + b;
+              const float* qq = qS + row * d + h * hd;
+              const float* gg = gS + row * d + h * hd;
+              const double ls = lse_all[(((size_t)(p_hi - s) * L + l) * B + b) * H + h];
+              const double Dv = DS[row * H + h];
+              double sc = 0, dp = 0;
+              for (int i = 0; i < hd; ++i) {
+                sc += (double)qq[i] * kj[i];
+                dp += (double)gg[i] * vj[i];
+              }
+              const double P = std::exp(sc * scale - ls), dS = P * (dp - Dv);
+              for (int i = 0; i < hd; ++i) {
+                ak[i] += scale * dS * qq[i];
+                av[i] += P * gg[i];
+              }
+            }
+          const size_t base = (((size_t)b * H + h) * T_mem + j) * hd;
+          for (int i = 0; i < hd; ++i) {
+            dK[base + i] += (float)ak[i];
+            dV[base + i] += (float)av[i];
+          }
+        }
+    return 0;
+  }
   int qkv_bwd(const float* dq, float* rK, float* rV, int W, int p, int B, int H, int hd, float theta, T* dY, T* dYT,
-              int Bp) {
+              int ldT) {
     const int d = H * hd, half = hd / 2;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h)
@@ -271,13 +316,13 @@ struct HostOps {
                                d + h * hd + i + half, 2 * d + h * hd + i, 2 * d + h * hd + i + half};
           for (int j = 0; j < 6; ++j) {
             dY[(size_t)b * 3 * d + cols[j]] = (float)vals[j];
-            dYT[(size_t)cols[j] * Bp + b] = (float)vals[j];
+            dYT[(size_t)cols[j] * ldT + b] = (float)vals[j];
           }
         }
     return 0;
   }
   int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, int p, const float* s, int B, int d,
-                bool gate, T* dY, T* dYT, int Bp, float* dbg, float* de, float* ds) {
+                bool gate, T* dY, T* dYT, int ldT, float* dbg, float* de, float* ds) {
     for (int i = 0; i < d; ++i) {
       double acc = 0;
       for (int b = 0; b < B; ++b) {
@@ -288,7 +333,7 @@ struct HostOps {
         if (gate) {
           const double dz = g * (s[o] - e[oe]) * zv * (1 - zv);
           dY[o] = (float)dz;
-          dYT[(size_t)i * Bp + b] = (float)dz;
+          dYT[(size_t)i * ldT + b] = (float)dz;
           acc += dz;
         }
       }
@@ -323,7 +368,7 @@ struct HostOps {
 
 }  // namespace
 
-// sh: B n T_mem d H hd f L W V G gate_learned top_k detach_s_every detach_cache detach_memory
+// sh: B n T_mem d H hd f L W V G gate_learned top_k detach_s_every detach_cache detach_memory S
 // fp: rms_eps rope_theta temperature
 // P (in order): W_g W_qkv W_O W_Qx W_Ox W_1 W_3 W_2 W_o b_g s_star dec_attn_norm dec_xattn_norm dec_ffn_norm
 //   head_norm | e mem actions | loss logp | gradients in rlt_grads order | d_e d_mem
@@ -347,6 +392,7 @@ extern "C" int bptt_host(const int* sh, const float* fp, void** P) {
   S.scale = 1.0f / std::sqrt((float)S.hd);
   S.inv_temp = 1.0f / fp[2];
   S.Bp = S.B;
+  S.S = sh[16];
   const bpplan::Detach D{sh[13], sh[14] != 0, sh[15] != 0};
   auto cf = [&](int i) { return static_cast<const float*>(P[i]); };
   auto mf = [&](int i) { return static_cast<float*>(P[i]); };

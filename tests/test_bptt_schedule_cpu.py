@@ -6,7 +6,8 @@ per-step recomputation, window-gradient ring, detach points, transposed
 operands, workspace layout - is compiled with g++ over host-loop stand-ins
 for its device primitives (tests/bptt_host_ops.cpp) and run on seeded
 inputs; every gradient (decoder parameters, s_*, e, memory) and the loss must
-equal the oracle's within fp32 storage rounding.  The device kernels
+equal the oracle's within fp32 storage rounding, for any size of the step
+blocks over which weight and memory gradients are added.  The device kernels
 themselves are checked against the oracle by the GPU tests.
 """
 import ctypes
@@ -60,10 +61,10 @@ def _setup(window=3, gate_mode=0, T=7, B=2, seed=41, G=1, L=2, scale=4.0):
     return c, W, e, mem, acts
 
 
-def _host(lib, c, W, e, mem, acts, tau=1.0, k=0, s_every=0, cache=False, memory=False):
+def _host(lib, c, W, e, mem, acts, tau=1.0, k=0, s_every=0, cache=False, memory=False, block=4):
     B, n = acts.shape
     sh = [B, n, e.shape[1], c.d, c.n_heads, c.head_dim, c.d_ffn, c.n_layers, c.window, c.vocab, c.mem_groups,
-          1 if c.gate_mode == 0 else 0, k, s_every, int(cache), int(memory)]
+          1 if c.gate_mode == 0 else 0, k, s_every, int(cache), int(memory), block]
     keep = []
 
     def buf(x, dt=np.float32):
@@ -83,13 +84,13 @@ def _host(lib, c, W, e, mem, acts, tau=1.0, k=0, s_every=0, cache=False, memory=
     return float(loss[0]), logp, grads, d_e, d_mem
 
 
-def _compare(lib, setup_kw=None, tau=1.0, k=0, s_every=0, cache=False, memory=False):
+def _compare(lib, setup_kw=None, tau=1.0, k=0, s_every=0, cache=False, memory=False, block=4):
     c, W, e, mem, acts = _setup(**(setup_kw or {}))
     cfg = O.Cfg.of(c)
     if k:  # actions inside the top-k set (outside it the loss is infinite)
         _, out = O.decode_steps(cfg, W, O.init_state(cfg, W, e.shape[0]), e, mem, acts.shape[1], acts, tau, k)
         acts = np.where(np.isfinite(out.logp), acts, -1).astype(np.int32)
-    loss, logp, g, d_e, d_mem = _host(lib, c, W, e, mem, acts, tau, k, s_every, cache, memory)
+    loss, logp, g, d_e, d_mem = _host(lib, c, W, e, mem, acts, tau, k, s_every, cache, memory, block)
     lref, gref = BP.gradients(cfg, W, e, mem, acts, temperature=tau, top_k=k, detach_s_every=s_every,
                               detach_cache=cache, detach_memory=memory)
     assert abs(loss - lref) <= 1e-5 * max(1.0, abs(lref))
@@ -124,6 +125,14 @@ def test_truncated_bptt_schedule_matches_the_oracle(lib, kw):
     _, _, d_mem, _ = _compare(lib, {"T": 9}, **kw)
     if kw.get("memory"):
         assert not np.any(d_mem)
+
+
+@pytest.mark.parametrize("block", [1, 3, 7, 16])
+def test_step_blocks(lib, block):
+    """Weight and memory gradients added once per block of steps: any block
+    size (a partial last block, a single block longer than the sequence) gives
+    the oracle's gradients."""
+    _compare(lib, {"T": 7, "G": 2}, block=block)
 
 
 def test_tempered_top_k_head(lib):
