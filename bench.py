@@ -72,6 +72,58 @@ def decode_roofline_s(c, B, T, bw, peak) -> float:
     return sum(max(step_bytes(c, B, t) / bw, step_flops(c, B, t) / peak) for t in range(1, T + 1))
 
 
+def decoder_params(c) -> int:
+    d, f, L, V = c.d, c.d_ffn, c.n_layers, c.vocab
+    return L * (6 * d * d + 3 * d * f) + 2 * d * d + V * d
+
+
+BPTT_BLOCK = 16   # steps per weight/memory-gradient block of rlt_bptt
+
+
+def bptt_bytes(c, B, n, S=BPTT_BLOCK):
+    """Algorithmic HBM bytes of one rlt_bptt call over n steps (full BPTT,
+    memory gradient included), as its schedule moves them:
+      recording step t: the forward step without the head, plus the writes of
+        position t's keys/values, every layer's cross-attention output and LSE;
+      reverse step t: the decoder weights twice (recomputation with the head,
+        and the transposed copies of dX = dY W), the window keys/values twice
+        (recomputation and backward) with their fp32 gradient ring read and
+        written, the recorded cross-attention outputs, the memory keys/values
+        of positions 1..t per layer (the query gradient);
+      per block of S steps: every fp32 weight gradient read and written, and
+        per memory group the memory keys/values of positions 1..p_hi read once
+        and their fp32 gradient read and written."""
+    es = 2 if c.dtype == "bf16" else 4
+    d, L, H, V, W = c.d, c.n_layers, c.n_heads, c.vocab, c.window
+    wb = decoder_weight_bytes(c)
+    head = es * V * d
+    total = 0
+    for t in range(1, n + 1):
+        win = min(W, t)
+        swa = es * B * L * win * 2 * d
+        mem = L * xattn_bytes(c, B, t)
+        rec = (wb - head) + swa + mem + es * B * L * (2 * d + d) + 4 * B * L * H + 4 * B * d * 2
+        rev = 2 * wb + 2 * swa + 8 * B * L * win * 2 * d + es * B * L * d + mem + 4 * B * d * 2
+        total += rec + rev
+    for p_hi in range(n - 1, -1, -S):
+        total += 8 * decoder_params(c) + c.mem_groups * 2 * B * (p_hi + 1) * d * (es + 8)
+    return total
+
+
+def bptt_flops(c, B, n):
+    """Algorithmic flops of one rlt_bptt call: the decoder GEMMs four times per
+    step (recording, recomputation, dX = dY W, dW += dY^T X) and the
+    attention three times (forward, the backward's two products per key, the
+    memory gradient's two per key)."""
+    d, f, L, V = c.d, c.d_ffn, c.n_layers, c.vocab
+    gemm = 2 * B * (L * (6 * d * d + 3 * d * f) + 2 * d * d + V * d)
+    tot = 0
+    for t in range(1, n + 1):
+        attn = 4 * B * d * L * (min(c.window, t) + t)
+        tot += 4 * gemm + 3 * attn
+    return tot
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -499,6 +551,60 @@ def run_profile_case(args):
     model.close()
 
 
+def run_bptt_case(args):
+    """Backpropagation through time (rlt_bptt) over the first --bptt-steps
+    positions of the workload's sequences (encoded on the GPU), full BPTT with
+    the memory gradient, timed with CUDA events over --steps calls after
+    --warmup; one JSON line with the call's algorithmic bytes and flops, its
+    roofline time and the kernels it launched."""
+    import torch
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from recurrent_looped_transformer_rlt_b300 import runner
+    wl = ri.preset(args.workload)
+    c, B = wl.cfg, wl.B
+    n = args.bptt_steps or wl.T // 4
+    T = max(n, 1)
+    W = ri.make_weights(c, wl.seed)
+    tok = ri.make_tokens(wl, B=B, T=T)
+    model = rlt.Model(c, W)
+    buf = runner.alloc_buffers(model, B, T)
+    runner.encode(model, torch.from_numpy(tok).cuda(), buf)
+    acts = torch.from_numpy(ri.teacher_actions(tok, 0, n)).cuda()
+    nb = rlt.rlt_bptt_workspace_size(model.handle, B, n)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    rlt.rlt_workspace_init(ws, nb)
+    stream = torch.cuda.current_stream()
+    res = None
+    ts, launches = [], 0
+    for it in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        l0 = rlt.rlt_launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        res = runner.bptt(model, buf, acts, ws=ws, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        if it >= args.warmup:
+            ts.append(e0.elapsed_time(e1) / 1e3)
+            launches = rlt.rlt_launch_count() - l0
+    if rlt.rlt_status(ws, stream) != 0:
+        raise RuntimeError("device status flag set")
+    bw, peak, src = load_peaks()
+    t = float(np.mean(ts))
+    nbytes, nflops = bptt_bytes(c, B, n), bptt_flops(c, B, n)
+    roof = max(nbytes / bw, nflops / peak)
+    print(json.dumps({"case": "bptt", "workload": wl.name, "B": B, "steps": n, "block": min(BPTT_BLOCK, n),
+                      "tokens_per_s": round(B * n / t, 1), "ms_per_call": round(1e3 * t, 3),
+                      "loss": float(res.loss.item()), "bytes_per_call": nbytes, "flops_per_call": nflops,
+                      "roofline_ms": round(1e3 * roof, 3), "roofline_frac": round(roof / t, 4),
+                      "bound": "hbm" if nbytes / bw >= nflops / peak else "tensor",
+                      "achieved_gbs": round(nbytes / t / 1e9, 1), "peak_gbs": round(bw / 1e9, 1),
+                      "peak_source": src, "gpu_launches": int(launches), "calls": len(ts),
+                      "timing": "CUDA events around rlt_bptt (recording pass, reverse pass, block flushes)"}),
+          flush=True)
+    model.close()
+
+
 def run_generate_case(args):
     """Generation throughput of the workload's model: prefill of the first
     half of each sequence (token-parallel encoder keeping its keys and values,
@@ -567,12 +673,16 @@ def main():
     ap.add_argument("--workload", default="small", choices=sorted(ri.PRESETS))
     ap.add_argument("--kernel-class", default="xattn", choices=["xattn", ""])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", default="", choices=["", "xattn", "swa", "proj", "glu", "generate"],
-                    help="time one kernel of the workload (profiler captures), or generation, instead of the "
-                         "bench step")
+    ap.add_argument("--profile-case", default="", choices=["", "xattn", "swa", "proj", "glu", "generate", "bptt"],
+                    help="time one kernel of the workload (profiler captures), generation, or the decoder's "
+                         "backpropagation through time, instead of the bench step")
+    ap.add_argument("--bptt-steps", type=int, default=0, help="steps of the bptt case (default: T / 4)")
     args = ap.parse_args()
     if args.profile_case == "generate":
         run_generate_case(args)
+        return
+    if args.profile_case == "bptt":
+        run_bptt_case(args)
         return
     if args.profile_case:
         run_profile_case(args)

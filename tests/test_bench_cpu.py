@@ -66,3 +66,35 @@ def test_projection_roofline_maps_launches_in_step_order():
     assert r["launches"] == 2 * len(per)
     assert r["achieved"] == pytest.approx(2 * sum(per) / (sum(ms) / 1e3) / 1e9, rel=1e-3)
     assert bench.projection_roofline(wl, [], 6.5e12, "measured") is None
+
+
+def test_bptt_byte_and_flop_accounting():
+    """rlt_bptt's algorithmic bytes: with a one-position window and memory
+    (n = 1) the call is its weight traffic (recording without the head,
+    reverse twice, one block flush of fp32 gradients) plus the small
+    activation terms; the block flush is paid once per block of steps; flops
+    are four decoder GEMM passes and three attention passes per step."""
+    import bench
+    c = ri.preset("small").cfg
+    B = 64
+    es = 2
+    wb = bench.decoder_weight_bytes(c)
+    head = es * c.vocab * c.d
+    params = bench.decoder_params(c)
+    assert wb == es * params
+    one = bench.bptt_bytes(c, B, 1)
+    weights_only = (wb - head) + 2 * wb + 8 * params
+    assert weights_only < one < weights_only * 1.3
+    # the block flush: one per block of S steps
+    n = 40
+    per_block = [bench.bptt_bytes(c, B, n, S) for S in (1, 8, 40)]
+    assert per_block[0] > per_block[1] > per_block[2]
+    assert per_block[0] - per_block[2] >= 39 * 8 * params
+    # each step costs more than a forward step and less than four
+    for t in (1, 64, 512):
+        d1 = bench.bptt_bytes(c, B, t + 1, 10 ** 9) - bench.bptt_bytes(c, B, t, 10 ** 9)
+        assert bench.step_bytes(c, B, t + 1) < d1 < 4 * bench.step_bytes(c, B, t + 1)
+    f1 = bench.bptt_flops(c, B, 1)
+    gemm = 2 * B * params
+    attn = 4 * B * c.d * c.n_layers * 2
+    assert f1 == 4 * gemm + 3 * attn
