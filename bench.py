@@ -87,9 +87,10 @@ def bptt_bytes(c, B, n, S=BPTT_BLOCK):
         position t's keys/values, every layer's cross-attention output and LSE;
       reverse step t: the decoder weights twice (recomputation with the head,
         and the transposed copies of dX = dY W), the window keys/values twice
-        (recomputation and backward) with their fp32 gradient ring read and
-        written, the recorded cross-attention outputs, the memory keys/values
-        of positions 1..t per layer (the query gradient);
+        (recomputation and backward), the fp32 query-side records (query and
+        output gradient) of the min(W, n - t + 1) positions whose queries read
+        position t's key, the recorded cross-attention outputs, the memory
+        keys/values of positions 1..t per layer (the query gradient);
       per block of S steps: every fp32 weight gradient read and written, and
         per memory group the memory keys/values of positions 1..p_hi read once
         and their fp32 gradient read and written."""
@@ -103,7 +104,8 @@ def bptt_bytes(c, B, n, S=BPTT_BLOCK):
         swa = es * B * L * win * 2 * d
         mem = L * xattn_bytes(c, B, t)
         rec = (wb - head) + swa + mem + es * B * L * (2 * d + d) + 4 * B * L * H + 4 * B * d * 2
-        rev = 2 * wb + 2 * swa + 8 * B * L * win * 2 * d + es * B * L * d + mem + 4 * B * d * 2
+        nrec = min(W, n - t + 1)
+        rev = 2 * wb + 2 * swa + 8 * B * L * nrec * d + es * B * L * d + mem + 4 * B * d * 2
         total += rec + rev
     for p_hi in range(n - 1, -1, -S):
         total += 8 * decoder_params(c) + c.mem_groups * 2 * B * (p_hi + 1) * d * (es + 8)

@@ -10,6 +10,9 @@
 // gradient g,
 //   dP_j = g.V_j,  D = g.o,  dS_j = P_j (dP_j - D),
 //   dq = scale sum_j dS_j K_j,  dK_j = scale dS_j q,  dV_j = P_j g.
+// The query gradient is taken per step; the key/value gradients are summed
+// per key over the queries that read it (kv_grad_kernel for the window,
+// mem_grad_kernel for the memory).
 #pragma once
 
 #include "common.cuh"
@@ -398,17 +401,14 @@ __global__ void swiglu_bwd_kernel(const float* __restrict__ dm, const float* __r
   dYT[(size_t)(f + j) * ldT + b] = duq;
 }
 
-// Attention backward over positions j0..j1 (see the header), with D = g.o
-// from the stored output o (storage type): dq [B][d] stored, D to Dout
-// [B][H] when given; dK, dV (fp32 accumulators, may be null) += for positions
-// j >= jg, at slot j mod Ta (ring) or j of [B][H][Ta][hd].  One warp per
-// (b, h); each (b, h, j) has one writer.
+// Query gradient of the attention over positions j0..j1 (see the header),
+// with D = g.o from the stored output o (storage type): dq [B][d], and D to
+// Dout [B][H] when given.  One warp per (b, h).
 template <typename T>
 __global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __restrict__ gout, const T* __restrict__ o,
                                 const float* __restrict__ lse, const T* __restrict__ K, const T* __restrict__ V,
                                 int Tk, int j0, int j1, int B, int H, int hd, float scale, float* __restrict__ dq,
-                                float* __restrict__ Dout, float* __restrict__ dK, float* __restrict__ dV, int Ta,
-                                int ring, int jg) {
+                                float* __restrict__ Dout) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
   const int b = pair / H, h = pair - b * H;
@@ -443,29 +443,72 @@ __global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __rest
         dpp = fmaf(gr[c], to_f32(Vb[(size_t)j * hd + i]), dpp);
       }
     }
-    const float sj = warp_sum(sp) * scale;
-    const float dP = warp_sum(dpp);
-    const float P = expf(sj - ls);
-    const float dS = P * (dP - D);
+    const float P = expf(warp_sum(sp) * scale - ls);
+    const float dS = P * (warp_sum(dpp) - D);
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[c] = fmaf(dS, kv[c], acc[c]);
-    if (dK && j >= jg) {
-      const int slot = ring ? j % Ta : j;
-      const size_t base = (((size_t)b * H + h) * Ta + slot) * hd;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int i = lane + 32 * c;
-        if (c < NC && i < hd) {
-          dK[base + i] += scale * dS * qr[c];
-          dV[base + i] += P * gr[c];
-        }
-      }
-    }
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int i = lane + 32 * c;
     if (c < NC && i < hd) dq[(size_t)b * d + h * hd + i] = scale * acc[c];
+  }
+}
+
+// Key/value gradient of window position p (one layer) from the query-side
+// records of positions p..p_last, kept in a ring of W slots (slot p' mod W):
+// q, g [W][B][d] f32 (query after RoPE, output gradient), lse, D [W][B][H]:
+//   dK = sum scale dS q,  dV = sum P g,  P = exp(scale q.K_p - lse),
+//   dS = P (g.V_p - D),
+// to dK, dV [B][d].  One warp per (b, h).
+template <typename T>
+__global__ void kv_grad_kernel(const T* __restrict__ K, const T* __restrict__ V, int Tk, int p, int p_last,
+                               const float* __restrict__ qR, const float* __restrict__ gR, const float* __restrict__ lR,
+                               const float* __restrict__ DR, int W, int B, int H, int hd, float scale,
+                               float* __restrict__ dK, float* __restrict__ dV) {
+  const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (pair >= B * H) return;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd;
+  const int NC = (hd + 31) >> 5;
+  const size_t kp = (((size_t)b * H + h) * Tk + p) * hd;
+  float kr[4], vr[4], ak[4], av[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const bool ok = c < NC && i < hd;
+    kr[c] = ok ? to_f32(K[kp + i]) : 0.f;
+    vr[c] = ok ? to_f32(V[kp + i]) : 0.f;
+    ak[c] = 0.f;
+    av[c] = 0.f;
+  }
+  for (int pp = p; pp <= p_last; ++pp) {
+    const size_t row = (size_t)(pp % W) * B + b;
+    float qv[4], gv[4], s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      const bool ok = c < NC && i < hd;
+      qv[c] = ok ? qR[row * d + h * hd + i] : 0.f;
+      gv[c] = ok ? gR[row * d + h * hd + i] : 0.f;
+      s1 = fmaf(qv[c], kr[c], s1);
+      s2 = fmaf(gv[c], vr[c], s2);
+    }
+    const float P = expf(warp_sum(s1) * scale - lR[row * H + h]);
+    const float dS = P * (warp_sum(s2) - DR[row * H + h]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      ak[c] = fmaf(scale * dS, qv[c], ak[c]);
+      av[c] = fmaf(P, gv[c], av[c]);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) {
+      dK[(size_t)b * d + h * hd + i] = ak[c];
+      dV[(size_t)b * d + h * hd + i] = av[c];
+    }
   }
 }
 
@@ -578,13 +621,12 @@ __global__ void __launch_bounds__(kMemWarps * 32) mem_grad_kernel(
   }
 }
 
-// d qkv of position p: dq and the completed key gradient (ring slot p mod W)
-// back through RoPE, the value gradient as is; dY [B][3d] (and transposed).
-// Clears the ring slot.  One thread per (b, h, pair i < hd/2).
+// d qkv of position p: dq and dK back through RoPE, dV as is; dY [B][3d]
+// (and transposed).  One thread per (b, h, pair i < hd/2).
 template <typename T>
-__global__ void qkv_bwd_kernel(const float* __restrict__ dq, float* __restrict__ rK, float* __restrict__ rV, int W,
-                               int p, int B, int H, int hd, float theta, T* __restrict__ dY, T* __restrict__ dYT,
-                               int ldT) {
+__global__ void qkv_bwd_kernel(const float* __restrict__ dq, const float* __restrict__ dK,
+                               const float* __restrict__ dV, int p, int B, int H, int hd, float theta,
+                               T* __restrict__ dY, T* __restrict__ dYT, int ldT) {
   const int half = hd >> 1;
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)B * H * half) return;
@@ -594,14 +636,10 @@ __global__ void qkv_bwd_kernel(const float* __restrict__ dq, float* __restrict__
   const int d = H * hd;
   float c, s;
   rope_cs(p, i, hd, theta, c, s);
-  const size_t rs = (((size_t)b * H + h) * W + p % W) * hd;
-  const float q1 = dq[(size_t)b * d + h * hd + i], q2 = dq[(size_t)b * d + h * hd + i + half];
-  const float k1 = rK[rs + i], k2 = rK[rs + i + half];
-  const float v1 = rV[rs + i], v2 = rV[rs + i + half];
-  rK[rs + i] = 0.f;
-  rK[rs + i + half] = 0.f;
-  rV[rs + i] = 0.f;
-  rV[rs + i + half] = 0.f;
+  const size_t o = (size_t)b * d + h * hd;
+  const float q1 = dq[o + i], q2 = dq[o + i + half];
+  const float k1 = dK[o + i], k2 = dK[o + i + half];
+  const float v1 = dV[o + i], v2 = dV[o + i + half];
   const float vals[6] = {q1 * c + q2 * s, -q1 * s + q2 * c, k1 * c + k2 * s, -k1 * s + k2 * c, v1, v2};
   const int cols[6] = {h * hd + i, h * hd + i + half, d + h * hd + i, d + h * hd + i + half, 2 * d + h * hd + i,
                        2 * d + h * hd + i + half};

@@ -106,10 +106,15 @@ struct BpttOps {
     return post();
   }
   int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* Dout, float* dK, float* dV, int Ta,
-               bool ring, int jg) {
-    bptt::attn_bwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(
-        q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd, scale, dq, Dout, dK, dV, Ta, ring ? 1 : 0, jg);
+               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* Dout) {
+    bptt::attn_bwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(q, gout, o, lse, K, V, Tk, j0, j1, B,
+                                                                             H, hd, scale, dq, Dout);
+    return post();
+  }
+  int kv_grad(const T* K, const T* V, int Tk, int p, int p_last, const float* qR, const float* gR, const float* lR,
+              const float* DR, int W, int B, int H, int hd, float scale, float* dK, float* dV) {
+    bptt::kv_grad_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(K, V, Tk, p, p_last, qR, gR, lR, DR, W,
+                                                                            B, H, hd, scale, dK, dV);
     return post();
   }
   int mem_grad(const T* K, const T* V, int T_mem, const float* qS, const float* gS, const float* lse_all,
@@ -120,9 +125,9 @@ struct BpttOps {
                                                                     p_hi, B, H, hd, scale, dK, dV);
     return post();
   }
-  int qkv_bwd(const float* dq, float* rK, float* rV, int W, int p, int B, int H, int hd, float theta, T* dY, T* dYT,
-              int ldT) {
-    bptt::qkv_bwd_kernel<T><<<blocks((size_t)B * H * (hd / 2)), bptt::kThreads, 0, st>>>(dq, rK, rV, W, p, B, H, hd,
+  int qkv_bwd(const float* dq, const float* dK, const float* dV, int p, int B, int H, int hd, float theta, T* dY,
+              T* dYT, int ldT) {
+    bptt::qkv_bwd_kernel<T><<<blocks((size_t)B * H * (hd / 2)), bptt::kThreads, 0, st>>>(dq, dK, dV, p, B, H, hd,
                                                                                         theta, dY, dYT, ldT);
     return post();
   }

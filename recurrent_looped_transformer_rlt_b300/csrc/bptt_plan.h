@@ -1,7 +1,7 @@
 // Backpropagation through time of the RLT decoder recurrence (teacher
 // forced, full or truncated at named detach points): the order of the
-// operations, the workspace layout and the bookkeeping of the window-gradient
-// ring and of the step blocks, written once over a set of primitive
+// operations, the workspace layout and the bookkeeping of the window's
+// query-side records and of the step blocks, written once over a set of primitive
 // operations (Ops, implemented by the device kernels of bptt.cuh).  Plain
 // host C++: no CUDA types.
 //
@@ -27,11 +27,14 @@
 //    results (the same kernels, so bitwise the recorded values; the memory is
 //    not read for this), runs the head and the layers backwards, and hands
 //    d s_{t-1} to step t-1.
-//  * The window keys and values of position j receive gradient from steps
-//    j+1..j+W; those arrive (in reverse order) before step j+1 itself is
-//    visited, so a ring of W fp32 slots per layer (slot j mod W) holds them
-//    until position j's QKV backward consumes and clears its slot, which is
-//    then free for position j-W.
+//  * The window keys and values of position j receive gradient from the
+//    queries of positions j..j+W-1, whose steps the reverse pass visits
+//    first.  Each step keeps, per layer, the query side of its window
+//    attention - the query (after RoPE), the output gradient, the LSE and
+//    D = g.o - in a ring of W slots (slot p mod W); position j's QKV backward
+//    computes its key/value gradient in one pass over the records of
+//    positions j..j+W-1.  Step p+1 overwrites the record of position p+W,
+//    whose keys p+1..p+W are consumed by then.
 //  * Steps are grouped in blocks of S consecutive steps.  Within a block each
 //    step writes, into its own column slot, the transposed GEMM inputs X and
 //    output gradients dY of every projection ([features][S * Bp]), and its
@@ -84,13 +87,13 @@ struct Layout {
   size_t lse2_all;      // [n][L][B][H] f32 their log-sum-exp
   size_t s_all;         // [n+1][B][d] f32: s_0 = s_*, s_1..s_n
   size_t lp;            // [B][n] f32
-  size_t ring;          // [L][2][B][H][W][hd] f32 window-gradient ring
-  size_t zero_begin;    // [zero_begin, total) and the ring start at zero
+  size_t qR, gR, lR, DR;  // [L][W][B][d], [L][W][B][d], [L][W][B][H], [L][W][B][H] f32 query-side records
+  size_t zero_begin;    // [zero_begin, total) starts at zero
   // one step's activations
   size_t xg, zpre, z;
   size_t hA, hX, hF;    // [L][B][d] f32 residual stream into attention, cross-attention, FFN
   size_t rA, rX, rF, rO;
-  size_t a, c, bb, q, oq, lse1;
+  size_t a, c, bb, oq;
   size_t g, u, m;
   size_t sn, qkv, logits;
   // block operands: [rows][S * Bp], step slot s at columns [s * Bp, (s + 1) * Bp)
@@ -98,7 +101,7 @@ struct Layout {
   size_t dlT, dzT, dhfT, dhxT, dhaT, dqxT, dguT, dqkvT;
   size_t qxS, gxS, DxS;  // [S][L][B][d], [S][L][B][d] f32, [S][L][B][H] f32
   // gradient scratch
-  size_t ds, dh, dq, dx, dY;
+  size_t ds, dh, dq, dKp, dVp, dx, dY;
   size_t total;
 };
 
@@ -128,7 +131,10 @@ inline Layout layout(const Shape& S, size_t es, size_t hdr) {
   Lw.lse2_all = take(4 * n * L * B * H);
   Lw.s_all = take(4 * (n + 1) * Bd);
   Lw.lp = take(4 * B * n);
-  Lw.ring = take(4 * L * 2 * B * H * W * hd);
+  Lw.qR = take(4 * L * W * Bd);
+  Lw.gR = take(4 * L * W * Bd);
+  Lw.lR = take(4 * L * W * B * H);
+  Lw.DR = take(4 * L * W * B * H);
   Lw.zero_begin = off;
   Lw.xg = take(es * 2 * Bd);
   Lw.zpre = take(4 * Bd);
@@ -143,9 +149,7 @@ inline Layout layout(const Shape& S, size_t es, size_t hdr) {
   Lw.a = take(es * L * Bd);
   Lw.c = take(es * L * Bd);
   Lw.bb = take(es * L * Bd);
-  Lw.q = take(4 * L * Bd);
   Lw.oq = take(es * L * Bd);
-  Lw.lse1 = take(4 * L * B * H);
   Lw.g = take(4 * L * B * f);
   Lw.u = take(4 * L * B * f);
   Lw.m = take(es * L * B * f);
@@ -174,6 +178,8 @@ inline Layout layout(const Shape& S, size_t es, size_t hdr) {
   Lw.ds = take(4 * Bd);
   Lw.dh = take(4 * Bd);
   Lw.dq = take(4 * Bd);
+  Lw.dKp = take(4 * Bd);
+  Lw.dVp = take(4 * Bd);
   Lw.dx = take(4 * B * (2 * d > f ? 2 * d : f));
   size_t ny = 3 * d;
   if (2 * f > ny) ny = 2 * f;
@@ -225,14 +231,11 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
   float* lse2_all = F(Lw.lse2_all);
   float* s_all = F(Lw.s_all);
   float* lp = F(Lw.lp);
-  float* ring = F(Lw.ring);
   const size_t plane_h = (size_t)B * H * n * hd;       // one key or value plane of the history
   const size_t plane_m = (size_t)B * H * S.T_mem * hd;  // of the memory
-  const size_t plane_r = (size_t)B * H * W * hd;       // of the ring
   const bool want_dmem = io.d_mem && !D.memory;
 
   // ---- set up: zeroed scratch and gradients, transposed weights, s_0
-  RLT_BP_TRY(k.zero(ring, 4 * L * 2 * plane_r));
   RLT_BP_TRY(k.zero(ws + Lw.zero_begin, Lw.total - Lw.zero_begin));
   RLT_BP_TRY(k.zero(G.W_g, 4 * 2 * dd));
   RLT_BP_TRY(k.zero(G.b_g, 4 * (size_t)d));
@@ -293,9 +296,10 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       RLT_BP_TRY(k.rms_fwd(hA, P.attn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rA) + l * B, X(Lw.a) + l * Bd,
                            col(Lw.aT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(X(Lw.a) + l * Bd, d, B, d, P.W_qkv + l * 3 * dd, d, 3 * d, qkv, 3 * d, false));
-      RLT_BP_TRY(k.qkv_post(qkv, p, B, H, hd, S.theta, F(Lw.q) + l * Bd, Kl, Vl, n));
+      const size_t rec = (size_t)l * W + p % W;  // this position's record slot
+      RLT_BP_TRY(k.qkv_post(qkv, p, B, H, hd, S.theta, F(Lw.qR) + rec * Bd, Kl, Vl, n));
       const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
-      RLT_BP_TRY(k.attn_fwd(F(Lw.q) + l * Bd, Kl, Vl, n, j0, p, B, H, hd, S.scale, F(Lw.lse1) + l * BH,
+      RLT_BP_TRY(k.attn_fwd(F(Lw.qR) + rec * Bd, Kl, Vl, n, j0, p, B, H, hd, S.scale, F(Lw.lR) + rec * BH,
                             X(Lw.oq) + l * Bd, col(Lw.oT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.copy(hX, hA, 4 * Bd));
       RLT_BP_TRY(k.gemm(X(Lw.oq) + l * Bd, d, B, d, P.W_O + l * dd, d, d, hX, d, true));
@@ -407,22 +411,29 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       RLT_BP_TRY(k.attn_bwd(F(Lw.qxS) + ((size_t)slot * L + l) * Bd, gx, xo_all + ((size_t)p * L + l) * Bd,
                             lse2_all + ((size_t)p * L + l) * BH, io.mem + (size_t)(2 * g) * plane_m,
                             io.mem + (size_t)(2 * g + 1) * plane_m, S.T_mem, 0, p, B, H, hd, S.scale, dq,
-                            F(Lw.DxS) + ((size_t)slot * L + l) * BH, nullptr, nullptr, 0, false, 0));
+                            F(Lw.DxS) + ((size_t)slot * L + l) * BH));
       RLT_BP_TRY(k.pack(dq, B, d, dY, col(Lw.dqxT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Qx + l * dd, d, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hX, F(Lw.rX) + l * B, P.xattn_norm + (size_t)l * d, dx, B, d, dh,
                            G.xattn_norm + (size_t)l * d));
-      // window self-attention: hX = hA + o W_O^T
+      // window self-attention: hX = hA + o W_O^T; this step's query-side
+      // record (query, output gradient, LSE, D) stays in the ring
       RLT_BP_TRY(k.pack(dh, B, d, dY, col(Lw.dhaT, (size_t)l * d, slot), ldT));
-      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_O + l * dd, d, d, dx, d, false));
-      float* rK = ring + (size_t)(2 * l) * plane_r;
-      float* rV = ring + (size_t)(2 * l + 1) * plane_r;
+      const size_t rec = (size_t)l * W + p % W;
+      float* g_rec = F(Lw.gR) + rec * Bd;
+      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_O + l * dd, d, d, g_rec, d, false));
       const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
-      RLT_BP_TRY(k.attn_bwd(F(Lw.q) + l * Bd, dx, X(Lw.oq) + l * Bd, F(Lw.lse1) + l * BH, Kl, Vl, n, j0, p, B, H,
-                            hd, S.scale, dq, nullptr, rK, rV, W, true, D.cache ? p : j0));
-      // position p's key/value gradient is complete: through RoPE into d qkv,
-      // and its ring slot is cleared for position p - W
-      RLT_BP_TRY(k.qkv_bwd(dq, rK, rV, W, p, B, H, hd, S.theta, dY, col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT));
+      RLT_BP_TRY(k.attn_bwd(F(Lw.qR) + rec * Bd, g_rec, X(Lw.oq) + l * Bd, F(Lw.lR) + rec * BH, Kl, Vl, n, j0, p,
+                            B, H, hd, S.scale, dq, F(Lw.DR) + rec * BH));
+      // position p's key/value gradient from the queries of positions
+      // p..p+W-1 (only its own with the cache detached), then through RoPE
+      // into d qkv
+      const int p_last = D.cache ? p : (p + W - 1 < n - 1 ? p + W - 1 : n - 1);
+      RLT_BP_TRY(k.kv_grad(Kl, Vl, n, p, p_last, F(Lw.qR) + (size_t)l * W * Bd, F(Lw.gR) + (size_t)l * W * Bd,
+                           F(Lw.lR) + (size_t)l * W * BH, F(Lw.DR) + (size_t)l * W * BH, W, B, H, hd, S.scale,
+                           F(Lw.dKp), F(Lw.dVp)));
+      RLT_BP_TRY(k.qkv_bwd(dq, F(Lw.dKp), F(Lw.dVp), p, B, H, hd, S.theta, dY,
+                           col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, 3 * d, B, 3 * d, wt_qkv + l * 3 * dd, 3 * d, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hA, F(Lw.rA) + l * B, P.attn_norm + (size_t)l * d, dx, B, d, dh,
                            G.attn_norm + (size_t)l * d));

@@ -1,6 +1,7 @@
 // Host-loop stand-ins for the device primitives of the decoder backward, so
-// that the schedule in bptt_plan.h (host logic: step order, the window
-// gradient ring, detach points, transposed operands, workspace layout) can be
+// that the schedule in bptt_plan.h (host logic: step order, the window's
+// query-side records, step blocks, detach points, transposed operands,
+// workspace layout) can be
 // checked against the float64 oracle without a GPU.  Test infrastructure:
 // the library never uses it.  Each member restates the specification of the
 // kernel of the same name in bptt.cuh, in double arithmetic over fp32
@@ -223,11 +224,10 @@ struct HostOps {
       }
     return 0;
   }
-  // D = g.o from the stored output o; dK/dV accumulated for positions >= jg
-  // (slot j mod Ta in a ring, else j); D written to Dout when given
+  // dq of the attention over positions j0..j1, D = g.o from the stored output
+  // o (written to Dout when given)
   int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* Dout, float* dK, float* dV, int Ta,
-               bool ring, int jg) {
+               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* Dout) {
     const int d = H * hd;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h) {
@@ -248,16 +248,41 @@ struct HostOps {
           }
           const double P = std::exp(s * scale - lse[b * H + h]), dS = P * (dp - D);
           for (int i = 0; i < hd; ++i) acc[i] += dS * Kb[(size_t)j * hd + i];
-          if (dK && j >= jg) {
-            const int slot = ring ? j % Ta : j;
-            const size_t base = (((size_t)b * H + h) * Ta + slot) * hd;
-            for (int i = 0; i < hd; ++i) {
-              dK[base + i] += (float)(scale * dS * qq[i]);
-              dV[base + i] += (float)(P * gg[i]);
-            }
-          }
         }
         for (int i = 0; i < hd; ++i) dq[(size_t)b * d + h * hd + i] = (float)(scale * acc[i]);
+      }
+    return 0;
+  }
+  // key/value gradient of window position p from the query-side records of
+  // positions p..p_last (ring slot p' mod W of one layer: q, g [W][B][d],
+  // lse, D [W][B][H]) into dK, dV [B][d]
+  int kv_grad(const T* K, const T* V, int Tk, int p, int p_last, const float* qR, const float* gR, const float* lR,
+              const float* DR, int W, int B, int H, int hd, float scale, float* dK, float* dV) {
+    const int d = H * hd;
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h) {
+        const T* kp = K + (((size_t)b * H + h) * Tk + p) * hd;
+        const T* vp = V + (((size_t)b * H + h) * Tk + p) * hd;
+        std::vector<double> ak(hd, 0.0), av(hd, 0.0);
+        for (int pp = p; pp <= p_last; ++pp) {
+          const size_t row = (size_t)(pp % W) * B + b;
+          const float* qq = qR + row * d + h * hd;
+          const float* gg = gR + row * d + h * hd;
+          double sc = 0, dp = 0;
+          for (int i = 0; i < hd; ++i) {
+            sc += (double)qq[i] * kp[i];
+            dp += (double)gg[i] * vp[i];
+          }
+          const double P = std::exp(sc * scale - lR[row * H + h]), dS = P * (dp - DR[row * H + h]);
+          for (int i = 0; i < hd; ++i) {
+            ak[i] += scale * dS * qq[i];
+            av[i] += P * gg[i];
+          }
+        }
+        for (int i = 0; i < hd; ++i) {
+          dK[(size_t)b * d + h * hd + i] = (float)ak[i];
+          dV[(size_t)b * d + h * hd + i] = (float)av[i];
+        }
       }
     return 0;
   }
@@ -299,18 +324,18 @@ struct HostOps {
         }
     return 0;
   }
-  int qkv_bwd(const float* dq, float* rK, float* rV, int W, int p, int B, int H, int hd, float theta, T* dY, T* dYT,
-              int ldT) {
+  // d qkv of position p: dq and dK back through RoPE, dV as is
+  int qkv_bwd(const float* dq, const float* dK, const float* dV, int p, int B, int H, int hd, float theta, T* dY,
+              T* dYT, int ldT) {
     const int d = H * hd, half = hd / 2;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h)
         for (int i = 0; i < half; ++i) {
           double c, s;
           rope_cs(p, i, hd, theta, c, s);
-          const size_t rs = (((size_t)b * H + h) * W + p % W) * hd;
-          const double q1 = dq[(size_t)b * d + h * hd + i], q2 = dq[(size_t)b * d + h * hd + i + half];
-          const double k1 = rK[rs + i], k2 = rK[rs + i + half], v1 = rV[rs + i], v2 = rV[rs + i + half];
-          rK[rs + i] = rK[rs + i + half] = rV[rs + i] = rV[rs + i + half] = 0;
+          const size_t o = (size_t)b * d + h * hd;
+          const double q1 = dq[o + i], q2 = dq[o + i + half];
+          const double k1 = dK[o + i], k2 = dK[o + i + half], v1 = dV[o + i], v2 = dV[o + i + half];
           const double vals[6] = {q1 * c + q2 * s, -q1 * s + q2 * c, k1 * c + k2 * s, -k1 * s + k2 * c, v1, v2};
           const int cols[6] = {h * hd + i,     h * hd + i + half,     d + h * hd + i,
                                d + h * hd + i + half, 2 * d + h * hd + i, 2 * d + h * hd + i + half};
