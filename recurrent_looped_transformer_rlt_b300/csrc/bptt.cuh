@@ -346,10 +346,14 @@ __global__ void __launch_bounds__(kThreadsHead) head_bwd_kernel(const float* __r
 // RMSNorm backward for y = x r g (r = 1/sqrt(mean(x^2) + eps)) given dy:
 //   dx_i += r g_i dy_i - x_i r^3 (sum_j g_j dy_j x_j) / d     (rows: warp per row)
 //   dg_i += sum_b dy_i x_i r                                 (columns: thread per column)
+// With out given, the updated dx rows are also written in the storage type
+// to out [B][d] and transposed to outT (the next projection's operands).
 // Blocks [0, row_blocks) do the rows, the rest the columns.
+template <typename T>
 __global__ void rms_bwd_kernel(const float* __restrict__ x, const float* __restrict__ r, const float* __restrict__ g,
                                const float* __restrict__ dy, int B, int d, float* __restrict__ dx,
-                               float* __restrict__ dg, int row_blocks) {
+                               float* __restrict__ dg, int row_blocks, T* __restrict__ out, T* __restrict__ outT,
+                               int ldT) {
   if ((int)blockIdx.x < row_blocks) {
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (row >= B) return;
@@ -360,7 +364,15 @@ __global__ void rms_bwd_kernel(const float* __restrict__ x, const float* __restr
     sd = warp_sum(sd);
     const float rv = r[row];
     const float coef = rv * rv * rv * sd / (float)d;
-    for (int i = lane; i < d; i += 32) dx[(size_t)row * d + i] += rv * g[i] * dyr[i] - xr[i] * coef;
+    for (int i = lane; i < d; i += 32) {
+      const float v = dx[(size_t)row * d + i] + (rv * g[i] * dyr[i] - xr[i] * coef);
+      dx[(size_t)row * d + i] = v;
+      if (out) {
+        const T q = from_f32<T>(v);
+        out[(size_t)row * d + i] = q;
+        outT[(size_t)i * ldT + row] = q;
+      }
+    }
   } else {
     const int i = (blockIdx.x - row_blocks) * blockDim.x + threadIdx.x;
     if (i >= d) return;
@@ -369,6 +381,18 @@ __global__ void rms_bwd_kernel(const float* __restrict__ x, const float* __restr
     dg[i] += acc;
   }
 }
+
+// Residual update into a new buffer: C[m][n] = R[m][n] + acc (the GEMMs'
+// per-element epilogue path).
+struct EpiResidualInto {
+  const float* R;
+  float* C;
+  int ldc;
+  __device__ __forceinline__ void operator()(int m, int n, float v) const {
+    const size_t o = (size_t)m * ldc + n;
+    C[o] = R[o] + v;
+  }
+};
 
 // y = x in the storage type, and transposed.
 template <typename T>

@@ -49,6 +49,18 @@ struct BpttOps {
       return ::gemm<float>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, EpiStoreF32{C, ldc});
     }
   }
+  // C[M][N] = R[M][N] + A[M][K] W[N][K]^T
+  int gemm_res(const T* A, int lda, int M, int K, const T* W, int ldw, int N, const float* R, float* C, int ldc) {
+    const bptt::EpiResidualInto epi{R, C, ldc};
+    if constexpr (kBf16) {
+      AArg a;
+      a.A = A;
+      a.lda = lda;
+      return proj_bf16<false>(st, a, M, K, W, nullptr, ldw, N, epi, sc);
+    } else {
+      return ::gemm<float>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, epi);
+    }
+  }
   int bcast_rows(float* dst, const float* src, int rows, int d) {
     bcast_rows_kernel<<<blocks((size_t)rows * d), bptt::kThreads, 0, st>>>(dst, src, rows, d);
     return post();
@@ -91,10 +103,12 @@ struct BpttOps {
         logits, B, V, actions, n, p, inv_temp, top_k, lp, dl, dlT, ldT, kBf16 ? 1 : 0, status);
     return post();
   }
-  int rms_bwd(const float* x, const float* r, const float* g, const float* dy, int B, int d, float* dx, float* dg) {
+  int rms_bwd(const float* x, const float* r, const float* g, const float* dy, int B, int d, float* dx, float* dg,
+              T* out, T* outT, int ldT) {
     const int row_blocks = (int)blocks((size_t)B * 32);
     const int col_blocks = (int)blocks((size_t)d);
-    bptt::rms_bwd_kernel<<<row_blocks + col_blocks, bptt::kThreads, 0, st>>>(x, r, g, dy, B, d, dx, dg, row_blocks);
+    bptt::rms_bwd_kernel<T><<<row_blocks + col_blocks, bptt::kThreads, 0, st>>>(x, r, g, dy, B, d, dx, dg,
+                                                                               row_blocks, out, outT, ldT);
     return post();
   }
   int pack(const float* x, int B, int N, T* y, T* yT, int ldT) {

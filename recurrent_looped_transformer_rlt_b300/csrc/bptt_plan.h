@@ -301,8 +301,7 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
       RLT_BP_TRY(k.attn_fwd(F(Lw.qR) + rec * Bd, Kl, Vl, n, j0, p, B, H, hd, S.scale, F(Lw.lR) + rec * BH,
                             X(Lw.oq) + l * Bd, col(Lw.oT, (size_t)l * d, slot), ldT));
-      RLT_BP_TRY(k.copy(hX, hA, 4 * Bd));
-      RLT_BP_TRY(k.gemm(X(Lw.oq) + l * Bd, d, B, d, P.W_O + l * dd, d, d, hX, d, true));
+      RLT_BP_TRY(k.gemm_res(X(Lw.oq) + l * Bd, d, B, d, P.W_O + l * dd, d, d, hA, hX, d));
       // cross-attention to memory positions 0..p (recorded in the first pass)
       RLT_BP_TRY(k.rms_fwd(hX, P.xattn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rX) + l * B, X(Lw.c) + l * Bd,
                            col(Lw.cT, (size_t)l * d, slot), ldT));
@@ -317,8 +316,7 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       } else {
         RLT_BP_TRY(k.tcopy(xo, B, d, col(Lw.oxT, (size_t)l * d, slot), ldT));
       }
-      RLT_BP_TRY(k.copy(hF, hX, 4 * Bd));
-      RLT_BP_TRY(k.gemm(xo, d, B, d, P.W_Ox + l * dd, d, d, hF, d, true));
+      RLT_BP_TRY(k.gemm_res(xo, d, B, d, P.W_Ox + l * dd, d, d, hX, hF, d));
       // SwiGLU feed-forward
       RLT_BP_TRY(k.rms_fwd(hF, P.ffn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rF) + l * B, X(Lw.bb) + l * Bd,
                            col(Lw.bbT, (size_t)l * d, slot), ldT));
@@ -328,8 +326,7 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       RLT_BP_TRY(k.gemm(X(Lw.bb) + l * Bd, d, B, d, P.W_3 + l * fd, d, f, ul, f, false));
       RLT_BP_TRY(k.swiglu_fwd(gl, ul, B, f, X(Lw.m) + (size_t)l * B * f, col(Lw.mT, (size_t)l * f, slot), ldT));
       float* next = (l + 1 < L) ? F(Lw.hA) + (l + 1) * Bd : s_all + (size_t)t * Bd;
-      RLT_BP_TRY(k.copy(next, hF, 4 * Bd));
-      RLT_BP_TRY(k.gemm(X(Lw.m) + (size_t)l * B * f, f, B, f, P.W_2 + l * fd, f, d, next, d, true));
+      RLT_BP_TRY(k.gemm_res(X(Lw.m) + (size_t)l * B * f, f, B, f, P.W_2 + l * fd, f, d, hF, next, d));
     }
     return 0;
   };
@@ -386,7 +383,10 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
     RLT_BP_TRY(k.head_bwd(F(Lw.logits), B, V, io.actions, n, p, S.inv_temp, S.top_k, lp, dY, col(Lw.dlT, 0, slot),
                           ldT));
     RLT_BP_TRY(k.gemm(dY, V, B, V, wt_o, V, d, dx, d, false));
-    RLT_BP_TRY(k.rms_bwd(s_t, F(Lw.rO), P.head_norm, dx, B, d, ds, G.head_norm));
+    // (each RMSNorm backward also writes the updated gradient as the next
+    // section's dY operand and its transposed slot)
+    RLT_BP_TRY(k.rms_bwd(s_t, F(Lw.rO), P.head_norm, dx, B, d, ds, G.head_norm, dY,
+                         col(Lw.dhfT, (size_t)(L - 1) * d, slot), ldT));
     RLT_BP_TRY(k.copy(dh, ds, 4 * Bd));
     for (int l = L - 1; l >= 0; --l) {
       const float* hA = F(Lw.hA) + l * Bd;
@@ -394,17 +394,15 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       const float* hF = F(Lw.hF) + l * Bd;
       const T* Kl = hist + (size_t)(2 * l) * plane_h;
       const T* Vl = hist + (size_t)(2 * l + 1) * plane_h;
-      // FFN: h_out = hF + m W_2^T, m = silu(bb W_1^T) * (bb W_3^T)
-      RLT_BP_TRY(k.pack(dh, B, d, dY, col(Lw.dhfT, (size_t)l * d, slot), ldT));
+      // FFN: h_out = hF + m W_2^T, m = silu(bb W_1^T) * (bb W_3^T); dY holds dh
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_2 + l * fd, d, f, dx, f, false));
       RLT_BP_TRY(k.swiglu_bwd(dx, F(Lw.g) + (size_t)l * B * f, F(Lw.u) + (size_t)l * B * f, B, f, dY,
                               col(Lw.dguT, (size_t)l * 2 * f, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, 2 * f, B, 2 * f, wt_13 + l * 2 * fd, 2 * f, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hF, F(Lw.rF) + l * B, P.ffn_norm + (size_t)l * d, dx, B, d, dh,
-                           G.ffn_norm + (size_t)l * d));
+                           G.ffn_norm + (size_t)l * d, dY, col(Lw.dhxT, (size_t)l * d, slot), ldT));
       // cross-attention: hF = hX + ox W_Ox^T; the query gradient now, the
       // memory gradient at the end of the block
-      RLT_BP_TRY(k.pack(dh, B, d, dY, col(Lw.dhxT, (size_t)l * d, slot), ldT));
       float* gx = F(Lw.gxS) + ((size_t)slot * L + l) * Bd;
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Ox + l * dd, d, d, gx, d, false));
       const int g = S.G == 1 ? 0 : l;
@@ -415,10 +413,9 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       RLT_BP_TRY(k.pack(dq, B, d, dY, col(Lw.dqxT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Qx + l * dd, d, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hX, F(Lw.rX) + l * B, P.xattn_norm + (size_t)l * d, dx, B, d, dh,
-                           G.xattn_norm + (size_t)l * d));
+                           G.xattn_norm + (size_t)l * d, dY, col(Lw.dhaT, (size_t)l * d, slot), ldT));
       // window self-attention: hX = hA + o W_O^T; this step's query-side
       // record (query, output gradient, LSE, D) stays in the ring
-      RLT_BP_TRY(k.pack(dh, B, d, dY, col(Lw.dhaT, (size_t)l * d, slot), ldT));
       const size_t rec = (size_t)l * W + p % W;
       float* g_rec = F(Lw.gR) + rec * Bd;
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_O + l * dd, d, d, g_rec, d, false));
@@ -435,8 +432,10 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       RLT_BP_TRY(k.qkv_bwd(dq, F(Lw.dKp), F(Lw.dVp), p, B, H, hd, S.theta, dY,
                            col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, 3 * d, B, 3 * d, wt_qkv + l * 3 * dd, 3 * d, d, dx, d, false));
+      // (layer l-1's FFN section reads dh as its dY; the merge reads dh)
       RLT_BP_TRY(k.rms_bwd(hA, F(Lw.rA) + l * B, P.attn_norm + (size_t)l * d, dx, B, d, dh,
-                           G.attn_norm + (size_t)l * d));
+                           G.attn_norm + (size_t)l * d, l > 0 ? dY : nullptr,
+                           l > 0 ? col(Lw.dhfT, (size_t)(l - 1) * d, slot) : nullptr, ldT));
     }
     // merge u = z s_{t-1} + (1 - z) e_t, z = sigmoid(W_g [e_t; s_{t-1}] + b_g)
     RLT_BP_TRY(k.merge_bwd(dh, z, io.e, S.T_mem, p, s_prev, B, d, S.gate_learned, dY, col(Lw.dzT, 0, slot), ldT,

@@ -51,6 +51,16 @@ struct HostOps {
       }
     return 0;
   }
+  // C[M][N] = R[M][N] + A[M][K] W[N][K]^T (a residual update into a new buffer)
+  int gemm_res(const T* A, int lda, int M, int K, const T* W, int ldw, int N, const float* R, float* C, int ldc) {
+    for (int m = 0; m < M; ++m)
+      for (int n = 0; n < N; ++n) {
+        double acc = 0;
+        for (int k = 0; k < K; ++k) acc += (double)A[(size_t)m * lda + k] * W[(size_t)n * ldw + k];
+        C[(size_t)m * ldc + n] = R[(size_t)m * ldc + n] + (float)acc;
+      }
+    return 0;
+  }
   int bcast_rows(float* dst, const float* src, int rows, int d) {
     for (int r = 0; r < rows; ++r) memcpy(dst + (size_t)r * d, src, sizeof(float) * d);
     return 0;
@@ -187,19 +197,29 @@ struct HostOps {
     }
     return 0;
   }
-  int rms_bwd(const float* x, const float* r, const float* g, const float* dy, int B, int d, float* dx, float* dg) {
+  // dx += RMSNorm backward, dg += the gain gradient; with y given, the
+  // updated dx rows also go to y (storage type) and yT (transposed)
+  int rms_bwd(const float* x, const float* r, const float* g, const float* dy, int B, int d, float* dx, float* dg,
+              T* y, T* yT, int ldT) {
+    for (int i = 0; i < d; ++i) {
+      double acc = 0;
+      for (int b = 0; b < B; ++b) acc += (double)dy[(size_t)b * d + i] * x[(size_t)b * d + i] * r[b];
+      dg[i] += (float)acc;
+    }
     for (int b = 0; b < B; ++b) {
       const float* xr = x + (size_t)b * d;
       const float* dyr = dy + (size_t)b * d;
       double sd = 0;
       for (int i = 0; i < d; ++i) sd += (double)g[i] * dyr[i] * xr[i];
       const double rv = r[b], coef = rv * rv * rv * sd / d;
-      for (int i = 0; i < d; ++i) dx[(size_t)b * d + i] += (float)(rv * g[i] * dyr[i] - xr[i] * coef);
-    }
-    for (int i = 0; i < d; ++i) {
-      double acc = 0;
-      for (int b = 0; b < B; ++b) acc += (double)dy[(size_t)b * d + i] * x[(size_t)b * d + i] * r[b];
-      dg[i] += (float)acc;
+      for (int i = 0; i < d; ++i) {
+        float& v = dx[(size_t)b * d + i];
+        v += (float)(rv * g[i] * dyr[i] - xr[i] * coef);
+        if (y) {
+          y[(size_t)b * d + i] = v;
+          yT[(size_t)i * ldT + b] = v;
+        }
+      }
     }
     return 0;
   }
