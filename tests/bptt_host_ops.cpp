@@ -5,11 +5,13 @@
 // checked against the float64 oracle without a GPU.  Test infrastructure:
 // the library never uses it.  Each member restates the specification of the
 // kernel of the same name in bptt.cuh, in double arithmetic over fp32
-// storage (the storage type is float here).
+// storage, with the storage-type writes optionally rounded to bf16 as the
+// device's bf16 models round them.
 #include "../recurrent_looped_transformer_rlt_b300/csrc/bptt_plan.h"
 
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 #include <numeric>
 #include <vector>
@@ -17,6 +19,16 @@
 namespace {
 
 double sigm(double x) { return 1.0 / (1.0 + std::exp(-x)); }
+
+// Round to the nearest bfloat16 (ties to even), kept as a float: the values
+// a bf16 model stores in its storage-type buffers.
+float bf16_round(float x) {
+  uint32_t u;
+  memcpy(&u, &x, 4);
+  if ((u & 0x7f800000u) != 0x7f800000u) u = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;
+  memcpy(&x, &u, 4);
+  return x;
+}
 
 void rope_cs(int p, int i, int hd, float theta, double& c, double& s) {
   const double a = p * std::pow((double)theta, -2.0 * i / hd);
@@ -26,6 +38,8 @@ void rope_cs(int p, int i, int hd, float theta, double& c, double& s) {
 
 struct HostOps {
   using T = float;
+  bool bf16 = false;  // storage-type writes rounded to bf16 (the device's bf16 models)
+  float st(double v) const { return bf16 ? bf16_round((float)v) : (float)v; }
 
   int zero(void* p, size_t bytes) {
     memset(p, 0, bytes);
@@ -68,7 +82,7 @@ struct HostOps {
   int merge_in(const T* e, int T_mem, int p, const float* s, int B, int d, T* xg, T* xgT, int ldT) {
     for (int b = 0; b < B; ++b)
       for (int i = 0; i < 2 * d; ++i) {
-        const float v = i < d ? e[((size_t)b * T_mem + p) * d + i] : s[(size_t)b * d + i - d];
+        const float v = i < d ? e[((size_t)b * T_mem + p) * d + i] : st(s[(size_t)b * d + i - d]);
         xg[(size_t)b * 2 * d + i] = v;
         if (xgT) xgT[(size_t)i * ldT + b] = v;
       }
@@ -94,7 +108,7 @@ struct HostOps {
       const double rv = 1.0 / std::sqrt(ss / d + eps);
       r[b] = (float)rv;
       for (int i = 0; i < d; ++i) {
-        const float v = (float)(xr[i] * rv * g[i]);
+        const float v = st(xr[i] * rv * g[i]);
         y[(size_t)b * d + i] = v;
         if (yT) yT[(size_t)i * ldT + b] = v;
       }
@@ -113,10 +127,10 @@ struct HostOps {
           q[i] = (float)(row[i] * c - row[i + half] * s);
           q[i + half] = (float)(row[i + half] * c + row[i] * s);
           const size_t o = (((size_t)b * H + h) * Tk + p) * hd;
-          K[o + i] = (float)(row[d + i] * c - row[d + i + half] * s);
-          K[o + i + half] = (float)(row[d + i + half] * c + row[d + i] * s);
-          V[o + i] = row[2 * d + i];
-          V[o + i + half] = row[2 * d + i + half];
+          K[o + i] = st(row[d + i] * c - row[d + i + half] * s);
+          K[o + i + half] = st(row[d + i + half] * c + row[d + i] * s);
+          V[o + i] = st(row[2 * d + i]);
+          V[o + i + half] = st(row[2 * d + i + half]);
         }
     return 0;
   }
@@ -143,8 +157,8 @@ struct HostOps {
           double acc = 0;
           for (int j = j0; j <= j1; ++j) acc += std::exp(sc[j - j0] - ls) * Vb[(size_t)j * hd + i];
           const size_t c = (size_t)h * hd + i;
-          oq[(size_t)b * d + c] = (float)acc;
-          if (oT) oT[c * ldT + b] = (float)acc;
+          oq[(size_t)b * d + c] = st(acc);
+          if (oT) oT[c * ldT + b] = st(acc);
         }
       }
     return 0;
@@ -159,7 +173,7 @@ struct HostOps {
       for (int j = 0; j < f; ++j) {
         const size_t o = (size_t)b * f + j;
         const double gv = g[o];
-        const float v = (float)(gv * sigm(gv) * u[o]);
+        const float v = st(gv * sigm(gv) * u[o]);
         m[o] = v;
         if (mT) mT[(size_t)j * ldT + b] = v;
       }
@@ -191,8 +205,8 @@ struct HostOps {
       for (int v = 0; v < V; ++v) {
         double gv = 0;
         if (a >= 0) gv = inv_temp * ((in[v] ? std::exp(x[v] - ls) : 0.0) - ((v == a && ain) ? 1.0 : 0.0));
-        dl[(size_t)b * V + v] = (float)gv;
-        dlT[(size_t)v * ldT + b] = (float)gv;
+        dl[(size_t)b * V + v] = st(gv);
+        dlT[(size_t)v * ldT + b] = st(gv);
       }
     }
     return 0;
@@ -216,8 +230,8 @@ struct HostOps {
         float& v = dx[(size_t)b * d + i];
         v += (float)(rv * g[i] * dyr[i] - xr[i] * coef);
         if (y) {
-          y[(size_t)b * d + i] = v;
-          yT[(size_t)i * ldT + b] = v;
+          y[(size_t)b * d + i] = st(v);
+          yT[(size_t)i * ldT + b] = st(v);
         }
       }
     }
@@ -226,8 +240,8 @@ struct HostOps {
   int pack(const float* x, int B, int N, T* y, T* yT, int ldT) {
     for (int b = 0; b < B; ++b)
       for (int j = 0; j < N; ++j) {
-        y[(size_t)b * N + j] = x[(size_t)b * N + j];
-        yT[(size_t)j * ldT + b] = x[(size_t)b * N + j];
+        y[(size_t)b * N + j] = st(x[(size_t)b * N + j]);
+        yT[(size_t)j * ldT + b] = st(x[(size_t)b * N + j]);
       }
     return 0;
   }
@@ -236,7 +250,7 @@ struct HostOps {
       for (int j = 0; j < f; ++j) {
         const size_t o = (size_t)b * f + j;
         const double gv = g[o], uv = u[o], dv = dm[o], sg = sigm(gv);
-        const float dgv = (float)(dv * uv * sg * (1 + gv * (1 - sg))), duv = (float)(dv * gv * sg);
+        const float dgv = st(dv * uv * sg * (1 + gv * (1 - sg))), duv = st(dv * gv * sg);
         dY[(size_t)b * 2 * f + j] = dgv;
         dY[(size_t)b * 2 * f + f + j] = duv;
         dYT[(size_t)j * ldT + b] = dgv;
@@ -360,8 +374,8 @@ struct HostOps {
           const int cols[6] = {h * hd + i,     h * hd + i + half,     d + h * hd + i,
                                d + h * hd + i + half, 2 * d + h * hd + i, 2 * d + h * hd + i + half};
           for (int j = 0; j < 6; ++j) {
-            dY[(size_t)b * 3 * d + cols[j]] = (float)vals[j];
-            dYT[(size_t)cols[j] * ldT + b] = (float)vals[j];
+            dY[(size_t)b * 3 * d + cols[j]] = st(vals[j]);
+            dYT[(size_t)cols[j] * ldT + b] = st(vals[j]);
           }
         }
     return 0;
@@ -377,8 +391,8 @@ struct HostOps {
         ds[o] = (float)(g * zv);
         if (gate) {
           const double dz = g * (s[o] - e[oe]) * zv * (1 - zv);
-          dY[o] = (float)dz;
-          dYT[(size_t)i * ldT + b] = (float)dz;
+          dY[o] = st(dz);
+          dYT[(size_t)i * ldT + b] = st(dz);
           acc += dz;
         }
       }
@@ -413,7 +427,7 @@ struct HostOps {
 
 }  // namespace
 
-// sh: B n T_mem d H hd f L W V G gate_learned top_k detach_s_every detach_cache detach_memory S
+// sh: B n T_mem d H hd f L W V G gate_learned top_k detach_s_every detach_cache detach_memory S bf16
 // fp: rms_eps rope_theta temperature
 // P (in order): W_g W_qkv W_O W_Qx W_Ox W_1 W_3 W_2 W_o b_g s_star dec_attn_norm dec_xattn_norm dec_ffn_norm
 //   head_norm | e mem actions | loss logp | gradients in rlt_grads order | d_e d_mem
@@ -438,6 +452,7 @@ extern "C" int bptt_host(const int* sh, const float* fp, void** P) {
   S.inv_temp = 1.0f / fp[2];
   S.Bp = S.B;
   S.S = sh[16];
+  const bool bf16 = sh[17] != 0;
   const bpplan::Detach D{sh[13], sh[14] != 0, sh[15] != 0};
   auto cf = [&](int i) { return static_cast<const float*>(P[i]); };
   auto mf = [&](int i) { return static_cast<float*>(P[i]); };
@@ -449,5 +464,6 @@ extern "C" int bptt_host(const int* sh, const float* fp, void** P) {
   const bpplan::Layout Lw = bpplan::layout(S, sizeof(float), 256);
   std::vector<double> ws((Lw.total + 7) / 8);  // 8-byte aligned storage
   HostOps k;
+  k.bf16 = bf16;
   return bpplan::run(k, S, D, Pp, io, G, reinterpret_cast<char*>(ws.data()), Lw);
 }

@@ -61,10 +61,10 @@ def _setup(window=3, gate_mode=0, T=7, B=2, seed=41, G=1, L=2, scale=4.0):
     return c, W, e, mem, acts
 
 
-def _host(lib, c, W, e, mem, acts, tau=1.0, k=0, s_every=0, cache=False, memory=False, block=4):
+def _host(lib, c, W, e, mem, acts, tau=1.0, k=0, s_every=0, cache=False, memory=False, block=4, bf16=False):
     B, n = acts.shape
     sh = [B, n, e.shape[1], c.d, c.n_heads, c.head_dim, c.d_ffn, c.n_layers, c.window, c.vocab, c.mem_groups,
-          1 if c.gate_mode == 0 else 0, k, s_every, int(cache), int(memory), block]
+          1 if c.gate_mode == 0 else 0, k, s_every, int(cache), int(memory), block, int(bf16)]
     keep = []
 
     def buf(x, dt=np.float32):
@@ -152,3 +152,27 @@ def test_detaching_only_s_leaves_cache_paths(lib):
     assert np.abs(de_s[:, 2]).max() > 0        # position 2 is in step 4's window
     assert np.abs(de_sc[:, 2]).max() == 0      # ... and reaches it only through the cache
     assert np.abs(de_sc[:, 3]).max() > 0       # the step's own input always has gradient
+
+
+def test_bf16_storage_stays_within_bf16_error(lib):
+    """With every storage-type write rounded to bf16 (what the bf16 models'
+    kernels store: normalised activations, attention outputs, keys and
+    values, and every gradient that enters a GEMM), the gradients stay within
+    a few bf16 roundings of the float64 oracle on the same bf16 weights and
+    inputs: relative Frobenius error ~3e-3 per gradient at this size."""
+    c = ri.RLTConfig(d=256, n_layers=2, n_heads=8, head_dim=32, d_ffn=512, window=4, mem_groups=2, vocab=64,
+                     dtype="bf16")
+    W = ri.make_weights(c, 41, norm_jitter=0.1)
+    B, T = 2, 10
+    e, mem = ri.make_decoder_inputs(c, B, T, 48, mem_scale=0.5)
+    wl = ri.Workload("t", c, B=B, T=T, tokens="uniform5", split=(2, 2), seed=41)
+    tok = ((ri.make_tokens(wl) + np.arange(T)[None, :] * 2) % c.vocab).astype(np.int32)
+    acts = ri.teacher_actions(tok, 0, T)
+    loss, _, g, d_e, d_mem = _host(lib, c, W, e, mem, acts, block=16, bf16=True)
+    cfg = O.Cfg.of(ri.RLTConfig(**{**c.__dict__, "dtype": "f32"}))  # float64 arithmetic on the same values
+    lref, gref = BP.gradients(cfg, W, e, mem, acts)
+    assert abs(loss - lref) <= 1e-3 * abs(lref)
+    for name, x in list(g.items()) + [("e", d_e), ("mem", d_mem)]:
+        r = gref[name]
+        rel = np.linalg.norm((x - r).ravel()) / np.linalg.norm(r.ravel())
+        assert 1e-5 < rel < 1e-2, (name, rel)   # rounding is visible, and small
