@@ -85,8 +85,9 @@ def bptt_bytes(c, B, n, S=BPTT_BLOCK):
     memory gradient included), as its schedule moves them:
       recording step t: the forward step without the head, plus the writes of
         position t's keys/values, every layer's cross-attention output and LSE;
-      reverse step t: the decoder weights twice (recomputation with the head,
-        and the transposed copies of dX = dY W), the window keys/values twice
+      reverse step t: the decoder weights twice (recomputation with the head
+        but without the last layer's W_2, whose output s_t is recorded, and
+        the transposed copies of dX = dY W), the window keys/values twice
         (recomputation and backward), the fp32 query-side records (query and
         output gradient) of the min(W, n - t + 1) positions whose queries read
         position t's key, the recorded cross-attention outputs, the memory
@@ -105,7 +106,7 @@ def bptt_bytes(c, B, n, S=BPTT_BLOCK):
         mem = L * xattn_bytes(c, B, t)
         rec = (wb - head) + swa + mem + es * B * L * (2 * d + d) + 4 * B * L * H + 4 * B * d * 2
         nrec = min(W, n - t + 1)
-        rev = 2 * wb + 2 * swa + 8 * B * L * nrec * d + es * B * L * d + mem + 4 * B * d * 2
+        rev = 2 * wb - es * d * c.d_ffn + 2 * swa + 8 * B * L * nrec * d + es * B * L * d + mem + 4 * B * d * 2
         total += rec + rev
     for p_hi in range(n - 1, -1, -S):
         total += 8 * decoder_params(c) + c.mem_groups * 2 * B * (p_hi + 1) * d * (es + 8)

@@ -11,7 +11,7 @@
 //   dP_j = g.V_j,  D = g.o,  dS_j = P_j (dP_j - D),
 //   dq = scale sum_j dS_j K_j,  dK_j = scale dS_j q,  dV_j = P_j g.
 // The query gradient is taken per step; the key/value gradients are summed
-// per key over the queries that read it (kv_grad_kernel for the window,
+// per key over the queries that read it (swa_bwd_kernel for the window,
 // mem_grad_kernel for the memory).
 #pragma once
 
@@ -31,6 +31,22 @@ __device__ __forceinline__ void rope_cs(int p, int i, int hd, float theta, float
   sincos(ang, &sd, &cd);
   c = (float)cd;
   s = (float)sd;
+}
+
+// Head rows held by a warp: lane l holds elements l + 32 c (c < 4) of a
+// head of hd <= 128.  The RoPE partner of element i is i ^ (hd / 2): for
+// hd >= 64 it is in the same lane, register c ^ (hd / 64); for hd <= 32 it is
+// lane l ^ (hd / 2) (a full-warp shuffle; lanes past hd hold zeros).
+__device__ __forceinline__ float rope_partner(const float (&v)[4], int c, int hd) {
+  const int half = hd >> 1;
+  if (half >= 32) {
+    const int pc = c ^ (half >> 5);
+    float r = v[0];
+#pragma unroll
+    for (int k = 1; k < 4; ++k) r = (k == pc) ? v[k] : r;
+    return r;
+  }
+  return __shfl_xor_sync(0xffffffffu, v[c], half);
 }
 
 // dst[c][r] = src[r][c] through a 32x33 shared tile; block (32, 8).
@@ -96,32 +112,6 @@ __global__ void rms_fwd_kernel(const float* __restrict__ x, const float* __restr
   }
 }
 
-// q, k after RoPE at position p (q fp32 to qo, k to K[b][h][p]), v to
-// V[b][h][p]; one thread per (b, h, pair i < hd/2).
-template <typename T>
-__global__ void qkv_post_kernel(const float* __restrict__ qkv, int p, int B, int H, int hd, float theta,
-                                float* __restrict__ qo, T* __restrict__ K, T* __restrict__ V, int Tk) {
-  const int half = hd >> 1;
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (size_t)B * H * half) return;
-  const int i = (int)(idx % half);
-  const int h = (int)((idx / half) % H);
-  const int b = (int)(idx / ((size_t)half * H));
-  const int d = H * hd;
-  float c, s;
-  rope_cs(p, i, hd, theta, c, s);
-  const float* row = qkv + (size_t)b * 3 * d + h * hd;
-  const float q1 = row[i], q2 = row[i + half];
-  qo[(size_t)b * d + h * hd + i] = q1 * c - q2 * s;
-  qo[(size_t)b * d + h * hd + i + half] = q2 * c + q1 * s;
-  const float k1 = row[d + i], k2 = row[d + i + half];
-  const size_t o = (((size_t)b * H + h) * Tk + p) * hd;
-  K[o + i] = from_f32<T>(k1 * c - k2 * s);
-  K[o + i + half] = from_f32<T>(k2 * c + k1 * s);
-  V[o + i] = from_f32<T>(row[2 * d + i]);
-  V[o + i + half] = from_f32<T>(row[2 * d + i + half]);
-}
-
 // Softmax attention of q [B][d] over positions j0..j1 of K, V [B][H][Tk][hd]:
 // lse [B][H], the output in the storage type to oq [B][d] (and transposed
 // when oT is given).  One warp per (b, h); lane l holds elements l, l + 32,
@@ -160,6 +150,86 @@ __global__ void attn_fwd_kernel(const float* __restrict__ q, const T* __restrict
     for (int c = 0; c < 4; ++c) {
       const int i = lane + 32 * c;
       if (c < NC && i < hd) acc[c] = acc[c] * corr + w * to_f32(Vb[(size_t)j * hd + i]);
+    }
+    mx = mn;
+  }
+  if (lane == 0) lse[pair] = mx + logf(l);
+  const float inv = 1.0f / l;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) {
+      const size_t col = (size_t)h * hd + i;
+      const T vq = from_f32<T>(acc[c] * inv);
+      oq[(size_t)b * d + col] = vq;
+      if (oT) oT[col * ldT + b] = vq;
+    }
+  }
+}
+
+// Window attention forward of position p, one warp per (b, h): q and k of
+// qkv [B][3d] rotated by RoPE at p (q fp32 to qo [B][d]; k and v rounded to
+// the storage type and written to K, V [B][H][Tk][hd] at p), then the
+// attention of q over positions j0..p (position p from registers, the same
+// rounded values): lse [B][H], the output to oq [B][d] (storage type) and
+// its transposed slot oT.
+template <typename T>
+__global__ void swa_fwd_kernel(const float* __restrict__ qkv, int p, int j0, int B, int H, int hd, float theta,
+                               float scale, float* __restrict__ qo, T* __restrict__ K, T* __restrict__ V, int Tk,
+                               float* __restrict__ lse, T* __restrict__ oq, T* __restrict__ oT, int ldT) {
+  const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (pair >= B * H) return;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd, half = hd >> 1;
+  const int NC = (hd + 31) >> 5;
+  const float* row = qkv + (size_t)b * 3 * d + h * hd;
+  float qv[4], kv[4], vv[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const bool ok = c < NC && i < hd;
+    qv[c] = ok ? row[i] : 0.f;
+    kv[c] = ok ? row[d + i] : 0.f;
+    vv[c] = ok ? row[2 * d + i] : 0.f;
+  }
+  float qr[4], kr[4], acc[4];
+  const size_t kp = (((size_t)b * H + h) * Tk + p) * hd;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const float qp = rope_partner(qv, c, hd), kpv = rope_partner(kv, c, hd);
+    float cs = 1.f, sn = 0.f;
+    if (c < NC && i < hd) rope_cs(p, i % half, hd, theta, cs, sn);
+    // (x1, x2) -> (x1 c - x2 s, x2 c + x1 s): element i < half is x1
+    const float sg = (i % hd) < half ? -1.f : 1.f;
+    qr[c] = qv[c] * cs + sg * qp * sn;
+    kr[c] = round_st<T>(kv[c] * cs + sg * kpv * sn);
+    vv[c] = round_st<T>(vv[c]);
+    acc[c] = 0.f;
+    if (c < NC && i < hd) {
+      qo[(size_t)b * d + h * hd + i] = qr[c];
+      K[kp + i] = from_f32<T>(kr[c]);
+      V[kp + i] = from_f32<T>(vv[c]);
+    }
+  }
+  const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+  const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+  float mx = -INFINITY, l = 0.f;
+  for (int j = j0; j <= p; ++j) {
+    float part = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) part = fmaf(qr[c], j == p ? kr[c] : to_f32(Kb[(size_t)j * hd + i]), part);
+    }
+    const float sj = warp_sum(part) * scale;
+    const float mn = fmaxf(mx, sj);
+    const float corr = expf(mx - mn), w = expf(sj - mn);
+    l = l * corr + w;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) acc[c] = acc[c] * corr + w * (j == p ? vv[c] : to_f32(Vb[(size_t)j * hd + i]));
     }
     mx = mn;
   }
@@ -394,45 +464,54 @@ struct EpiResidualInto {
   }
 };
 
-// y = x in the storage type, and transposed.
+// SwiGLU backward of dm = acc at (b, j): dg = dm u sigma(g) (1 + g (1 -
+// sigma(g))), du = dm g sigma(g) to dY [B][2f] (columns j, f + j) and the
+// transposed rows j, f + j of dYT.
 template <typename T>
-__global__ void pack_kernel(const float* __restrict__ x, int B, int N, T* __restrict__ y, T* __restrict__ yT,
-                            int ldT) {
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (size_t)B * N) return;
-  const int b = (int)(idx / N), j = (int)(idx - (size_t)b * N);
-  const T v = from_f32<T>(x[idx]);
-  y[idx] = v;
-  yT[(size_t)j * ldT + b] = v;
-}
+struct EpiSwigluBwd {
+  const float* g;
+  const float* u;
+  int f;
+  T* dY;
+  T* dYT;
+  int ldT;
+  __device__ __forceinline__ void operator()(int m, int n, float v) const {
+    const size_t o = (size_t)m * f + n;
+    const float gv = g[o], uv = u[o];
+    const float sg = sigmoid_acc(gv);
+    const T dgq = from_f32<T>(v * uv * sg * (1.f + gv * (1.f - sg)));
+    const T duq = from_f32<T>(v * gv * sg);
+    dY[(size_t)m * 2 * f + n] = dgq;
+    dY[(size_t)m * 2 * f + f + n] = duq;
+    dYT[(size_t)n * ldT + m] = dgq;
+    dYT[(size_t)(f + n) * ldT + m] = duq;
+  }
+};
 
-// m = silu(g) u backward: dg = dm u sigma(g) (1 + g (1 - sigma(g))),
-// du = dm g sigma(g); dY[b] = [dg | du] (and transposed: rows j, f + j).
-template <typename T>
-__global__ void swiglu_bwd_kernel(const float* __restrict__ dm, const float* __restrict__ g,
-                                  const float* __restrict__ u, int B, int f, T* __restrict__ dY, T* __restrict__ dYT,
-                                  int ldT) {
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (size_t)B * f) return;
-  const int b = (int)(idx / f), j = (int)(idx - (size_t)b * f);
-  const float gv = g[idx], uv = u[idx], dv = dm[idx];
-  const float sg = sigmoid_acc(gv);
-  const T dgq = from_f32<T>(dv * uv * sg * (1.f + gv * (1.f - sg)));
-  const T duq = from_f32<T>(dv * gv * sg);
-  dY[(size_t)b * 2 * f + j] = dgq;
-  dY[(size_t)b * 2 * f + f + j] = duq;
-  dYT[(size_t)j * ldT + b] = dgq;
-  dYT[(size_t)(f + j) * ldT + b] = duq;
-}
+// d[e; s] = acc at (b, n): n < d adds to the e gradient of position p,
+// the rest to ds [B][d].
+struct EpiMergeBwd {
+  float* de;  // [B][T_mem][d] or null
+  float* ds;
+  int d, T_mem, p;
+  __device__ __forceinline__ void operator()(int m, int n, float v) const {
+    if (n < d) {
+      if (de) de[((size_t)m * T_mem + p) * d + n] += v;
+    } else {
+      ds[(size_t)m * d + n - d] += v;
+    }
+  }
+};
 
 // Query gradient of the attention over positions j0..j1 (see the header),
-// with D = g.o from the stored output o (storage type): dq [B][d], and D to
-// Dout [B][H] when given.  One warp per (b, h).
+// with D = g.o from the stored output o (storage type), written as the next
+// projection's operands: dqY [B][d] in the storage type and transposed to
+// dqT; D to Dout [B][H] when given.  One warp per (b, h).
 template <typename T>
 __global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __restrict__ gout, const T* __restrict__ o,
                                 const float* __restrict__ lse, const T* __restrict__ K, const T* __restrict__ V,
-                                int Tk, int j0, int j1, int B, int H, int hd, float scale, float* __restrict__ dq,
-                                float* __restrict__ Dout) {
+                                int Tk, int j0, int j1, int B, int H, int hd, float scale, float* __restrict__ Dout,
+                                T* __restrict__ dqY, T* __restrict__ dqT, int ldT) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
   const int b = pair / H, h = pair - b * H;
@@ -475,63 +554,121 @@ __global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __rest
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int i = lane + 32 * c;
-    if (c < NC && i < hd) dq[(size_t)b * d + h * hd + i] = scale * acc[c];
+    if (c < NC && i < hd) {
+      const size_t col = (size_t)h * hd + i;
+      const T v = from_f32<T>(scale * acc[c]);
+      dqY[(size_t)b * d + col] = v;
+      dqT[col * ldT + b] = v;
+    }
   }
 }
 
-// Key/value gradient of window position p (one layer) from the query-side
-// records of positions p..p_last, kept in a ring of W slots (slot p' mod W):
-// q, g [W][B][d] f32 (query after RoPE, output gradient), lse, D [W][B][H]:
+// Window attention backward of position p (one layer), one warp per (b, h):
+// from this step's record (ring slot p mod W: query q, output gradient g,
+// lse) and the stored output o, D = g.o (written to the record), the query
+// gradient over positions j0..p; the key/value gradient of position p from
+// the records of positions p..p_last (this step's from registers):
 //   dK = sum scale dS q,  dV = sum P g,  P = exp(scale q.K_p - lse),
-//   dS = P (g.V_p - D),
-// to dK, dV [B][d].  One warp per (b, h).
+//   dS = P (g.V_p - D);
+// then dq and dK back through RoPE at p and dV as is, into d qkv
+// dY [B][3d] (storage type) and its transposed slot dYT.
 template <typename T>
-__global__ void kv_grad_kernel(const T* __restrict__ K, const T* __restrict__ V, int Tk, int p, int p_last,
-                               const float* __restrict__ qR, const float* __restrict__ gR, const float* __restrict__ lR,
-                               const float* __restrict__ DR, int W, int B, int H, int hd, float scale,
-                               float* __restrict__ dK, float* __restrict__ dV) {
+__global__ void swa_bwd_kernel(const T* __restrict__ K, const T* __restrict__ V, int Tk, int j0, int p, int p_last,
+                               const T* __restrict__ o, const float* __restrict__ qR, const float* __restrict__ gR,
+                               const float* __restrict__ lR, float* __restrict__ DR, int W, int B, int H, int hd,
+                               float scale, float theta, T* __restrict__ dY, T* __restrict__ dYT, int ldT) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
   const int b = pair / H, h = pair - b * H;
-  const int d = H * hd;
+  const int d = H * hd, half = hd >> 1;
   const int NC = (hd + 31) >> 5;
-  const size_t kp = (((size_t)b * H + h) * Tk + p) * hd;
-  float kr[4], vr[4], ak[4], av[4];
+  const size_t r0 = (size_t)(p % W) * B + b;  // this step's record row
+  float qr[4], gr[4], kp[4], vp[4], dq[4], dk[4], dv[4];
+  float Dp = 0.f;
+  const size_t kpo = (((size_t)b * H + h) * Tk + p) * hd;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int i = lane + 32 * c;
     const bool ok = c < NC && i < hd;
-    kr[c] = ok ? to_f32(K[kp + i]) : 0.f;
-    vr[c] = ok ? to_f32(V[kp + i]) : 0.f;
-    ak[c] = 0.f;
-    av[c] = 0.f;
+    qr[c] = ok ? qR[r0 * d + h * hd + i] : 0.f;
+    gr[c] = ok ? gR[r0 * d + h * hd + i] : 0.f;
+    kp[c] = ok ? to_f32(K[kpo + i]) : 0.f;
+    vp[c] = ok ? to_f32(V[kpo + i]) : 0.f;
+    dq[c] = dk[c] = dv[c] = 0.f;
+    if (ok) Dp = fmaf(gr[c], to_f32(o[(size_t)b * d + h * hd + i]), Dp);
   }
+  const float D = warp_sum(Dp);
+  const float ls = lR[r0 * H + h];
+  if (lane == 0) DR[r0 * H + h] = D;
+  const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+  const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+  // query gradient over the window
+  for (int j = j0; j <= p; ++j) {
+    float kv[4], sp = 0.f, dpp = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      kv[c] = 0.f;
+      if (c < NC && i < hd) {
+        kv[c] = to_f32(Kb[(size_t)j * hd + i]);
+        sp = fmaf(qr[c], kv[c], sp);
+        dpp = fmaf(gr[c], to_f32(Vb[(size_t)j * hd + i]), dpp);
+      }
+    }
+    const float P = expf(warp_sum(sp) * scale - ls);
+    const float dS = P * (warp_sum(dpp) - D);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dq[c] = fmaf(dS, kv[c], dq[c]);
+  }
+  // key/value gradient of position p from the records of p..p_last
   for (int pp = p; pp <= p_last; ++pp) {
-    const size_t row = (size_t)(pp % W) * B + b;
+    const size_t rr = (size_t)(pp % W) * B + b;
     float qv[4], gv[4], s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int i = lane + 32 * c;
       const bool ok = c < NC && i < hd;
-      qv[c] = ok ? qR[row * d + h * hd + i] : 0.f;
-      gv[c] = ok ? gR[row * d + h * hd + i] : 0.f;
-      s1 = fmaf(qv[c], kr[c], s1);
-      s2 = fmaf(gv[c], vr[c], s2);
+      qv[c] = pp == p ? qr[c] : (ok ? qR[rr * d + h * hd + i] : 0.f);
+      gv[c] = pp == p ? gr[c] : (ok ? gR[rr * d + h * hd + i] : 0.f);
+      s1 = fmaf(qv[c], kp[c], s1);
+      s2 = fmaf(gv[c], vp[c], s2);
     }
-    const float P = expf(warp_sum(s1) * scale - lR[row * H + h]);
-    const float dS = P * (warp_sum(s2) - DR[row * H + h]);
+    const float lsr = pp == p ? ls : lR[rr * H + h];
+    const float Dr = pp == p ? D : DR[rr * H + h];
+    const float P = expf(warp_sum(s1) * scale - lsr);
+    const float dS = P * (warp_sum(s2) - Dr);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      ak[c] = fmaf(scale * dS, qv[c], ak[c]);
-      av[c] = fmaf(P, gv[c], av[c]);
+      dk[c] = fmaf(scale * dS, qv[c], dk[c]);
+      dv[c] = fmaf(P, gv[c], dv[c]);
     }
+  }
+  // back through RoPE at p: (y1, y2) -> (y1 c + y2 s, -y1 s + y2 c)
+#pragma unroll
+  for (int c = 0; c < 4; ++c) dq[c] *= scale;
+  float out_q[4], out_k[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const float qp = rope_partner(dq, c, hd), kpp = rope_partner(dk, c, hd);
+    float cs = 1.f, sn = 0.f;
+    if (c < NC && i < hd) rope_cs(p, i % half, hd, theta, cs, sn);
+    const float sg = (i % hd) < half ? 1.f : -1.f;
+    out_q[c] = dq[c] * cs + sg * qp * sn;
+    out_k[c] = dk[c] * cs + sg * kpp * sn;
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int i = lane + 32 * c;
     if (c < NC && i < hd) {
-      dK[(size_t)b * d + h * hd + i] = ak[c];
-      dV[(size_t)b * d + h * hd + i] = av[c];
+      const int cq = h * hd + i, ck = d + h * hd + i, cv = 2 * d + h * hd + i;
+      const T vq = from_f32<T>(out_q[c]), vk = from_f32<T>(out_k[c]), vv = from_f32<T>(dv[c]);
+      dY[(size_t)b * 3 * d + cq] = vq;
+      dY[(size_t)b * 3 * d + ck] = vk;
+      dY[(size_t)b * 3 * d + cv] = vv;
+      dYT[(size_t)cq * ldT + b] = vq;
+      dYT[(size_t)ck * ldT + b] = vk;
+      dYT[(size_t)cv * ldT + b] = vv;
     }
   }
 }
@@ -645,36 +782,6 @@ __global__ void __launch_bounds__(kMemWarps * 32) mem_grad_kernel(
   }
 }
 
-// d qkv of position p: dq and dK back through RoPE, dV as is; dY [B][3d]
-// (and transposed).  One thread per (b, h, pair i < hd/2).
-template <typename T>
-__global__ void qkv_bwd_kernel(const float* __restrict__ dq, const float* __restrict__ dK,
-                               const float* __restrict__ dV, int p, int B, int H, int hd, float theta,
-                               T* __restrict__ dY, T* __restrict__ dYT, int ldT) {
-  const int half = hd >> 1;
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (size_t)B * H * half) return;
-  const int i = (int)(idx % half);
-  const int h = (int)((idx / half) % H);
-  const int b = (int)(idx / ((size_t)half * H));
-  const int d = H * hd;
-  float c, s;
-  rope_cs(p, i, hd, theta, c, s);
-  const size_t o = (size_t)b * d + h * hd;
-  const float q1 = dq[o + i], q2 = dq[o + i + half];
-  const float k1 = dK[o + i], k2 = dK[o + i + half];
-  const float v1 = dV[o + i], v2 = dV[o + i + half];
-  const float vals[6] = {q1 * c + q2 * s, -q1 * s + q2 * c, k1 * c + k2 * s, -k1 * s + k2 * c, v1, v2};
-  const int cols[6] = {h * hd + i, h * hd + i + half, d + h * hd + i, d + h * hd + i + half, 2 * d + h * hd + i,
-                       2 * d + h * hd + i + half};
-#pragma unroll
-  for (int j = 0; j < 6; ++j) {
-    const T v = from_f32<T>(vals[j]);
-    dY[(size_t)b * 3 * d + cols[j]] = v;
-    dYT[(size_t)cols[j] * ldT + b] = v;
-  }
-}
-
 // Merge backward, one thread per column i (loop over sequences):
 //   de[b][p][i] = dh (1 - z);  ds[b][i] = dh z;
 //   gate: dzpre = dh (s - e) z (1 - z) to dY [B][d] (and transposed),
@@ -702,16 +809,6 @@ __global__ void merge_bwd_kernel(const float* __restrict__ dh, const float* __re
     }
   }
   if (gate) dbg[i] += acc;
-}
-
-// de[b][p] += dx[b][:d], ds[b] += dx[b][d:] (dx = dzpre W_g, [B][2d]).
-__global__ void merge_bwd2_kernel(const float* __restrict__ dx, int B, int d, int T_mem, int p,
-                                  float* __restrict__ de, float* __restrict__ ds) {
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (size_t)B * d) return;
-  const int b = (int)(idx / d), i = (int)(idx - (size_t)b * d);
-  if (de) de[((size_t)b * T_mem + p) * d + i] += dx[(size_t)b * 2 * d + i];
-  ds[idx] += dx[(size_t)b * 2 * d + d + i];
 }
 
 // out[i] += sum_b x[b][i].

@@ -49,9 +49,9 @@ struct BpttOps {
       return ::gemm<float>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, EpiStoreF32{C, ldc});
     }
   }
-  // C[M][N] = R[M][N] + A[M][K] W[N][K]^T
-  int gemm_res(const T* A, int lda, int M, int K, const T* W, int ldw, int N, const float* R, float* C, int ldc) {
-    const bptt::EpiResidualInto epi{R, C, ldc};
+  // A[M][K] W[N][K]^T through the epilogue functor
+  template <class Epi>
+  int gemm_epi(const T* A, int lda, int M, int K, const T* W, int ldw, int N, Epi epi) {
     if constexpr (kBf16) {
       AArg a;
       a.A = A;
@@ -60,6 +60,21 @@ struct BpttOps {
     } else {
       return ::gemm<float>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, epi);
     }
+  }
+  // C[M][N] = R[M][N] + A[M][K] W[N][K]^T
+  int gemm_res(const T* A, int lda, int M, int K, const T* W, int ldw, int N, const float* R, float* C, int ldc) {
+    return gemm_epi(A, lda, M, K, W, ldw, N, bptt::EpiResidualInto{R, C, ldc});
+  }
+  // dm = A W^T, SwiGLU backward in the epilogue into dY [M][2f] and dYT
+  int gemm_swiglu_bwd(const T* A, int lda, int M, int K, const T* W, int ldw, int f, const float* g, const float* u,
+                      T* dY, T* dYT, int ldT) {
+    return gemm_epi(A, lda, M, K, W, ldw, f, bptt::EpiSwigluBwd<T>{g, u, f, dY, dYT, ldT});
+  }
+  // d[e; s] = dzpre W_g (A = dzpre, W = the transposed copy of W_g), added to
+  // the e gradient of position p and to ds
+  int gemm_merge_bwd(const T* A, int lda, int M, int K, const T* W, int ldw, int d, int T_mem, int p, float* de,
+                     float* ds) {
+    return gemm_epi(A, lda, M, K, W, ldw, 2 * d, bptt::EpiMergeBwd{de, ds, d, T_mem, p});
   }
   int bcast_rows(float* dst, const float* src, int rows, int d) {
     bcast_rows_kernel<<<blocks((size_t)rows * d), bptt::kThreads, 0, st>>>(dst, src, rows, d);
@@ -78,9 +93,10 @@ struct BpttOps {
     bptt::rms_fwd_kernel<T><<<blocks((size_t)B * 32), bptt::kThreads, 0, st>>>(x, g, B, d, eps, r, y, yT, ldT);
     return post();
   }
-  int qkv_post(const float* qkv, int p, int B, int H, int hd, float theta, float* q, T* K, T* V, int Tk) {
-    bptt::qkv_post_kernel<T><<<blocks((size_t)B * H * (hd / 2)), bptt::kThreads, 0, st>>>(qkv, p, B, H, hd, theta, q,
-                                                                                         K, V, Tk);
+  int swa_fwd(const float* qkv, int p, int j0, int B, int H, int hd, float theta, float scale, float* qo, T* K, T* V,
+              int Tk, float* lse, T* oq, T* oT, int ldT) {
+    bptt::swa_fwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(qkv, p, j0, B, H, hd, theta, scale, qo,
+                                                                            K, V, Tk, lse, oq, oT, ldT);
     return post();
   }
   int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
@@ -111,24 +127,17 @@ struct BpttOps {
                                                                                row_blocks, out, outT, ldT);
     return post();
   }
-  int pack(const float* x, int B, int N, T* y, T* yT, int ldT) {
-    bptt::pack_kernel<T><<<blocks((size_t)B * N), bptt::kThreads, 0, st>>>(x, B, N, y, yT, ldT);
-    return post();
-  }
-  int swiglu_bwd(const float* dm, const float* g, const float* u, int B, int f, T* dY, T* dYT, int ldT) {
-    bptt::swiglu_bwd_kernel<T><<<blocks((size_t)B * f), bptt::kThreads, 0, st>>>(dm, g, u, B, f, dY, dYT, ldT);
-    return post();
-  }
   int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* Dout) {
+               int j0, int j1, int B, int H, int hd, float scale, float* Dout, T* dqY, T* dqT, int ldT) {
     bptt::attn_bwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(q, gout, o, lse, K, V, Tk, j0, j1, B,
-                                                                             H, hd, scale, dq, Dout);
+                                                                             H, hd, scale, Dout, dqY, dqT, ldT);
     return post();
   }
-  int kv_grad(const T* K, const T* V, int Tk, int p, int p_last, const float* qR, const float* gR, const float* lR,
-              const float* DR, int W, int B, int H, int hd, float scale, float* dK, float* dV) {
-    bptt::kv_grad_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(K, V, Tk, p, p_last, qR, gR, lR, DR, W,
-                                                                            B, H, hd, scale, dK, dV);
+  int swa_bwd(const T* K, const T* V, int Tk, int j0, int p, int p_last, const T* o, const float* qR,
+              const float* gR, float* lR, float* DR, int W, int B, int H, int hd, float scale, float theta, T* dY,
+              T* dYT, int ldT) {
+    bptt::swa_bwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(
+        K, V, Tk, j0, p, p_last, o, qR, gR, lR, DR, W, B, H, hd, scale, theta, dY, dYT, ldT);
     return post();
   }
   int mem_grad(const T* K, const T* V, int T_mem, const float* qS, const float* gS, const float* lse_all,
@@ -139,20 +148,10 @@ struct BpttOps {
                                                                     p_hi, B, H, hd, scale, dK, dV);
     return post();
   }
-  int qkv_bwd(const float* dq, const float* dK, const float* dV, int p, int B, int H, int hd, float theta, T* dY,
-              T* dYT, int ldT) {
-    bptt::qkv_bwd_kernel<T><<<blocks((size_t)B * H * (hd / 2)), bptt::kThreads, 0, st>>>(dq, dK, dV, p, B, H, hd,
-                                                                                        theta, dY, dYT, ldT);
-    return post();
-  }
   int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, int p, const float* s, int B, int d,
                 bool gate, T* dY, T* dYT, int ldT, float* dbg, float* de, float* ds) {
     bptt::merge_bwd_kernel<T><<<blocks((size_t)d), bptt::kThreads, 0, st>>>(dh, z, e, T_mem, p, s, B, d, gate ? 1 : 0,
                                                                             dY, dYT, ldT, dbg, de, ds);
-    return post();
-  }
-  int merge_bwd2(const float* dx, int B, int d, int T_mem, int p, float* de, float* ds) {
-    bptt::merge_bwd2_kernel<<<blocks((size_t)B * d), bptt::kThreads, 0, st>>>(dx, B, d, T_mem, p, de, ds);
     return post();
   }
   int colsum(const float* x, int B, int d, float* out) {

@@ -101,7 +101,7 @@ struct Layout {
   size_t dlT, dzT, dhfT, dhxT, dhaT, dqxT, dguT, dqkvT;
   size_t qxS, gxS, DxS;  // [S][L][B][d], [S][L][B][d] f32, [S][L][B][H] f32
   // gradient scratch
-  size_t ds, dh, dq, dKp, dVp, dx, dY;
+  size_t ds, dh, dx, dY, dY2;
   size_t total;
 };
 
@@ -177,14 +177,12 @@ inline Layout layout(const Shape& S, size_t es, size_t hdr) {
   Lw.DxS = take(4 * SB * L * B * H);
   Lw.ds = take(4 * Bd);
   Lw.dh = take(4 * Bd);
-  Lw.dq = take(4 * Bd);
-  Lw.dKp = take(4 * Bd);
-  Lw.dVp = take(4 * Bd);
-  Lw.dx = take(4 * B * (2 * d > f ? 2 * d : f));
+  Lw.dx = take(4 * Bd);
   size_t ny = 3 * d;
   if (2 * f > ny) ny = 2 * f;
   if (V > ny) ny = V;
   Lw.dY = take(es * B * ny);
+  Lw.dY2 = take(es * B * 2 * f);
   Lw.total = off;
   return Lw;
 }
@@ -297,10 +295,9 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
                            col(Lw.aT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(X(Lw.a) + l * Bd, d, B, d, P.W_qkv + l * 3 * dd, d, 3 * d, qkv, 3 * d, false));
       const size_t rec = (size_t)l * W + p % W;  // this position's record slot
-      RLT_BP_TRY(k.qkv_post(qkv, p, B, H, hd, S.theta, F(Lw.qR) + rec * Bd, Kl, Vl, n));
       const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
-      RLT_BP_TRY(k.attn_fwd(F(Lw.qR) + rec * Bd, Kl, Vl, n, j0, p, B, H, hd, S.scale, F(Lw.lR) + rec * BH,
-                            X(Lw.oq) + l * Bd, col(Lw.oT, (size_t)l * d, slot), ldT));
+      RLT_BP_TRY(k.swa_fwd(qkv, p, j0, B, H, hd, S.theta, S.scale, F(Lw.qR) + rec * Bd, Kl, Vl, n,
+                           F(Lw.lR) + rec * BH, X(Lw.oq) + l * Bd, col(Lw.oT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm_res(X(Lw.oq) + l * Bd, d, B, d, P.W_O + l * dd, d, d, hA, hX, d));
       // cross-attention to memory positions 0..p (recorded in the first pass)
       RLT_BP_TRY(k.rms_fwd(hX, P.xattn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rX) + l * B, X(Lw.c) + l * Bd,
@@ -325,6 +322,8 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       RLT_BP_TRY(k.gemm(X(Lw.bb) + l * Bd, d, B, d, P.W_1 + l * fd, d, f, gl, f, false));
       RLT_BP_TRY(k.gemm(X(Lw.bb) + l * Bd, d, B, d, P.W_3 + l * fd, d, f, ul, f, false));
       RLT_BP_TRY(k.swiglu_fwd(gl, ul, B, f, X(Lw.m) + (size_t)l * B * f, col(Lw.mT, (size_t)l * f, slot), ldT));
+      // the last layer's output is s_t, recorded by the first pass
+      if (slot >= 0 && l + 1 == L) continue;
       float* next = (l + 1 < L) ? F(Lw.hA) + (l + 1) * Bd : s_all + (size_t)t * Bd;
       RLT_BP_TRY(k.gemm_res(X(Lw.m) + (size_t)l * B * f, f, B, f, P.W_2 + l * fd, f, d, hF, next, d));
     }
@@ -368,9 +367,9 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
   // ---- reverse pass
   float* ds = F(Lw.ds);  // d L / d s_t from step t+1 (then from the head too)
   float* dh = F(Lw.dh);
-  float* dq = F(Lw.dq);
   float* dx = F(Lw.dx);
   T* dY = X(Lw.dY);
+  T* dY2 = X(Lw.dY2);
   int slot = 0, p_hi = n - 1;
   for (int t = n; t >= 1; --t) {
     const int p = t - 1;
@@ -395,10 +394,9 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       const T* Kl = hist + (size_t)(2 * l) * plane_h;
       const T* Vl = hist + (size_t)(2 * l + 1) * plane_h;
       // FFN: h_out = hF + m W_2^T, m = silu(bb W_1^T) * (bb W_3^T); dY holds dh
-      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_2 + l * fd, d, f, dx, f, false));
-      RLT_BP_TRY(k.swiglu_bwd(dx, F(Lw.g) + (size_t)l * B * f, F(Lw.u) + (size_t)l * B * f, B, f, dY,
-                              col(Lw.dguT, (size_t)l * 2 * f, slot), ldT));
-      RLT_BP_TRY(k.gemm(dY, 2 * f, B, 2 * f, wt_13 + l * 2 * fd, 2 * f, d, dx, d, false));
+      RLT_BP_TRY(k.gemm_swiglu_bwd(dY, d, B, d, wt_2 + l * fd, d, f, F(Lw.g) + (size_t)l * B * f,
+                                   F(Lw.u) + (size_t)l * B * f, dY2, col(Lw.dguT, (size_t)l * 2 * f, slot), ldT));
+      RLT_BP_TRY(k.gemm(dY2, 2 * f, B, 2 * f, wt_13 + l * 2 * fd, 2 * f, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hF, F(Lw.rF) + l * B, P.ffn_norm + (size_t)l * d, dx, B, d, dh,
                            G.ffn_norm + (size_t)l * d, dY, col(Lw.dhxT, (size_t)l * d, slot), ldT));
       // cross-attention: hF = hX + ox W_Ox^T; the query gradient now, the
@@ -408,9 +406,8 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       const int g = S.G == 1 ? 0 : l;
       RLT_BP_TRY(k.attn_bwd(F(Lw.qxS) + ((size_t)slot * L + l) * Bd, gx, xo_all + ((size_t)p * L + l) * Bd,
                             lse2_all + ((size_t)p * L + l) * BH, io.mem + (size_t)(2 * g) * plane_m,
-                            io.mem + (size_t)(2 * g + 1) * plane_m, S.T_mem, 0, p, B, H, hd, S.scale, dq,
-                            F(Lw.DxS) + ((size_t)slot * L + l) * BH));
-      RLT_BP_TRY(k.pack(dq, B, d, dY, col(Lw.dqxT, (size_t)l * d, slot), ldT));
+                            io.mem + (size_t)(2 * g + 1) * plane_m, S.T_mem, 0, p, B, H, hd, S.scale,
+                            F(Lw.DxS) + ((size_t)slot * L + l) * BH, dY, col(Lw.dqxT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Qx + l * dd, d, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hX, F(Lw.rX) + l * B, P.xattn_norm + (size_t)l * d, dx, B, d, dh,
                            G.xattn_norm + (size_t)l * d, dY, col(Lw.dhaT, (size_t)l * d, slot), ldT));
@@ -419,18 +416,14 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       const size_t rec = (size_t)l * W + p % W;
       float* g_rec = F(Lw.gR) + rec * Bd;
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_O + l * dd, d, d, g_rec, d, false));
+      // the query gradient over the window and position p's key/value
+      // gradient from the queries of positions p..p+W-1 (only its own with
+      // the cache detached), both back through RoPE into d qkv
       const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
-      RLT_BP_TRY(k.attn_bwd(F(Lw.qR) + rec * Bd, g_rec, X(Lw.oq) + l * Bd, F(Lw.lR) + rec * BH, Kl, Vl, n, j0, p,
-                            B, H, hd, S.scale, dq, F(Lw.DR) + rec * BH));
-      // position p's key/value gradient from the queries of positions
-      // p..p+W-1 (only its own with the cache detached), then through RoPE
-      // into d qkv
       const int p_last = D.cache ? p : (p + W - 1 < n - 1 ? p + W - 1 : n - 1);
-      RLT_BP_TRY(k.kv_grad(Kl, Vl, n, p, p_last, F(Lw.qR) + (size_t)l * W * Bd, F(Lw.gR) + (size_t)l * W * Bd,
-                           F(Lw.lR) + (size_t)l * W * BH, F(Lw.DR) + (size_t)l * W * BH, W, B, H, hd, S.scale,
-                           F(Lw.dKp), F(Lw.dVp)));
-      RLT_BP_TRY(k.qkv_bwd(dq, F(Lw.dKp), F(Lw.dVp), p, B, H, hd, S.theta, dY,
-                           col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT));
+      RLT_BP_TRY(k.swa_bwd(Kl, Vl, n, j0, p, p_last, X(Lw.oq) + l * Bd, F(Lw.qR) + (size_t)l * W * Bd,
+                           F(Lw.gR) + (size_t)l * W * Bd, F(Lw.lR) + (size_t)l * W * BH, F(Lw.DR) + (size_t)l * W * BH,
+                           W, B, H, hd, S.scale, S.theta, dY, col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT));
       RLT_BP_TRY(k.gemm(dY, 3 * d, B, 3 * d, wt_qkv + l * 3 * dd, 3 * d, d, dx, d, false));
       // (layer l-1's FFN section reads dh as its dY; the merge reads dh)
       RLT_BP_TRY(k.rms_bwd(hA, F(Lw.rA) + l * B, P.attn_norm + (size_t)l * d, dx, B, d, dh,
@@ -440,10 +433,8 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
     // merge u = z s_{t-1} + (1 - z) e_t, z = sigmoid(W_g [e_t; s_{t-1}] + b_g)
     RLT_BP_TRY(k.merge_bwd(dh, z, io.e, S.T_mem, p, s_prev, B, d, S.gate_learned, dY, col(Lw.dzT, 0, slot), ldT,
                            G.b_g, io.d_e, ds));
-    if (S.gate_learned) {
-      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_g, d, 2 * d, dx, 2 * d, false));
-      RLT_BP_TRY(k.merge_bwd2(dx, B, d, S.T_mem, p, io.d_e, ds));
-    }
+    if (S.gate_learned)
+      RLT_BP_TRY(k.gemm_merge_bwd(dY, d, B, d, wt_g, d, d, S.T_mem, p, io.d_e, ds));
     // s_{t-1} detached after its step: no gradient from this merge
     if (t - 1 >= 1 && D.s_every > 0 && (t - 1) % D.s_every == 0) RLT_BP_TRY(k.zero(ds, 4 * Bd));
     if (++slot == SB || t == 1) {

@@ -75,6 +75,21 @@ struct HostOps {
       }
     return 0;
   }
+  // dm = A W^T, then the SwiGLU backward of every element into dY [B][2f]
+  // (and transposed)
+  int gemm_swiglu_bwd(const T* A, int lda, int M, int K, const T* W, int ldw, int f, const float* g, const float* u,
+                      T* dY, T* dYT, int ldT) {
+    std::vector<float> dm((size_t)M * f);
+    gemm(A, lda, M, K, W, ldw, f, dm.data(), f, false);
+    return swiglu_bwd(dm.data(), g, u, M, f, dY, dYT, ldT);
+  }
+  // d[e; s] = A W_g (columns < d to the e gradient row p, the rest to ds)
+  int gemm_merge_bwd(const T* A, int lda, int M, int K, const T* W, int ldw, int d, int T_mem, int p, float* de,
+                     float* ds) {
+    std::vector<float> dx((size_t)M * 2 * d);
+    gemm(A, lda, M, K, W, ldw, 2 * d, dx.data(), 2 * d, false);
+    return merge_bwd2(dx.data(), M, d, T_mem, p, de, ds);
+  }
   int bcast_rows(float* dst, const float* src, int rows, int d) {
     for (int r = 0; r < rows; ++r) memcpy(dst + (size_t)r * d, src, sizeof(float) * d);
     return 0;
@@ -115,7 +130,7 @@ struct HostOps {
     }
     return 0;
   }
-  int qkv_post(const float* qkv, int p, int B, int H, int hd, float theta, float* qo, T* K, T* V, int Tk) {
+  void qkv_post(const float* qkv, int p, int B, int H, int hd, float theta, float* qo, T* K, T* V, int Tk) {
     const int d = H * hd, half = hd / 2;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h)
@@ -132,7 +147,6 @@ struct HostOps {
           V[o + i] = st(row[2 * d + i]);
           V[o + i + half] = st(row[2 * d + i + half]);
         }
-    return 0;
   }
   int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
                float* lse, T* oq, T* oT, int ldT) {
@@ -162,6 +176,14 @@ struct HostOps {
         }
       }
     return 0;
+  }
+  // window attention forward of position p: RoPE of q and k at p (q to qo
+  // fp32, k and v to K/V [B][H][Tk][hd] at p), then the attention of q over
+  // positions j0..p (lse, oq and its transposed slot)
+  int swa_fwd(const float* qkv, int p, int j0, int B, int H, int hd, float theta, float scale, float* qo, T* K, T* V,
+              int Tk, float* lse, T* oq, T* oT, int ldT) {
+    qkv_post(qkv, p, B, H, hd, theta, qo, K, V, Tk);
+    return attn_fwd(qo, K, V, Tk, j0, p, B, H, hd, scale, lse, oq, oT, ldT);
   }
   int tcopy(const T* x, int B, int N, T* yT, int ldT) {
     for (int b = 0; b < B; ++b)
@@ -258,10 +280,10 @@ struct HostOps {
       }
     return 0;
   }
-  // dq of the attention over positions j0..j1, D = g.o from the stored output
-  // o (written to Dout when given)
-  int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* dq, float* Dout) {
+  // dq of the attention over positions j0..j1 (fp32 [B][d]), D = g.o from the
+  // stored output o (written to Dout when given)
+  void attn_dq(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk, int j0,
+               int j1, int B, int H, int hd, float scale, float* dq, float* Dout) {
     const int d = H * hd;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h) {
@@ -285,13 +307,21 @@ struct HostOps {
         }
         for (int i = 0; i < hd; ++i) dq[(size_t)b * d + h * hd + i] = (float)(scale * acc[i]);
       }
-    return 0;
+  }
+  // the query gradient of the cross-attention, written as the next
+  // projection's operands (storage type [B][d] and transposed)
+  int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
+               int j0, int j1, int B, int H, int hd, float scale, float* Dout, T* dqY, T* dqT, int ldT) {
+    const int d = H * hd;
+    std::vector<float> dq((size_t)B * d);
+    attn_dq(q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd, scale, dq.data(), Dout);
+    return pack(dq.data(), B, d, dqY, dqT, ldT);
   }
   // key/value gradient of window position p from the query-side records of
   // positions p..p_last (ring slot p' mod W of one layer: q, g [W][B][d],
   // lse, D [W][B][H]) into dK, dV [B][d]
-  int kv_grad(const T* K, const T* V, int Tk, int p, int p_last, const float* qR, const float* gR, const float* lR,
-              const float* DR, int W, int B, int H, int hd, float scale, float* dK, float* dV) {
+  void kv_grad(const T* K, const T* V, int Tk, int p, int p_last, const float* qR, const float* gR, const float* lR,
+               const float* DR, int W, int B, int H, int hd, float scale, float* dK, float* dV) {
     const int d = H * hd;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h) {
@@ -318,7 +348,6 @@ struct HostOps {
           dV[(size_t)b * d + h * hd + i] = (float)av[i];
         }
       }
-    return 0;
   }
   // memory gradient of one block: for every position j <= p_hi, the steps
   // s < nb of the block (position p_hi - s >= j) and the layers [l0, l1)
@@ -359,8 +388,8 @@ struct HostOps {
     return 0;
   }
   // d qkv of position p: dq and dK back through RoPE, dV as is
-  int qkv_bwd(const float* dq, const float* dK, const float* dV, int p, int B, int H, int hd, float theta, T* dY,
-              T* dYT, int ldT) {
+  void qkv_bwd(const float* dq, const float* dK, const float* dV, int p, int B, int H, int hd, float theta, T* dY,
+               T* dYT, int ldT) {
     const int d = H * hd, half = hd / 2;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h)
@@ -378,6 +407,20 @@ struct HostOps {
             dYT[(size_t)cols[j] * ldT + b] = st(vals[j]);
           }
         }
+  }
+  // window attention backward of position p (one layer): the query gradient
+  // over positions j0..p from this step's record (slot p mod W; D is written
+  // there), the key/value gradient of position p from the records of
+  // positions p..p_last, both back through RoPE, the value gradient as is,
+  // into d qkv [B][3d] (storage type, and transposed)
+  int swa_bwd(const T* K, const T* V, int Tk, int j0, int p, int p_last, const T* o, const float* qR,
+              const float* gR, float* lR, float* DR, int W, int B, int H, int hd, float scale, float theta, T* dY,
+              T* dYT, int ldT) {
+    const size_t Bd = (size_t)B * H * hd, BH = (size_t)B * H, r = (size_t)(p % W);
+    std::vector<float> dq(Bd), dK(Bd), dV(Bd);
+    attn_dq(qR + r * Bd, gR + r * Bd, o, lR + r * BH, K, V, Tk, j0, p, B, H, hd, scale, dq.data(), DR + r * BH);
+    kv_grad(K, V, Tk, p, p_last, qR, gR, lR, DR, W, B, H, hd, scale, dK.data(), dV.data());
+    qkv_bwd(dq.data(), dK.data(), dV.data(), p, B, H, hd, theta, dY, dYT, ldT);
     return 0;
   }
   int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, int p, const float* s, int B, int d,

@@ -83,7 +83,7 @@ def test_bptt_byte_and_flop_accounting():
     params = bench.decoder_params(c)
     assert wb == es * params
     one = bench.bptt_bytes(c, B, 1)
-    weights_only = (wb - head) + 2 * wb + 8 * params
+    weights_only = (wb - head) + 2 * wb - es * c.d * c.d_ffn + 8 * params
     assert weights_only < one < weights_only * 1.3
     # the block flush: one per block of S steps
     n = 40
