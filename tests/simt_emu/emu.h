@@ -1,0 +1,172 @@
+// A host emulation of the CUDA execution model, for testing the index logic
+// of plain CUDA kernels without a GPU: one host thread per CUDA thread,
+// blocks run one after another, __syncthreads and warp shuffles are
+// barriers, __shared__ becomes static storage (one block at a time).  Test
+// infrastructure only: results obtained here are not GPU parity.
+#pragma once
+#include <atomic>
+#include <barrier>
+#include <condition_variable>
+#include <mutex>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <memory>
+#include <thread>
+#include <vector>
+#include <algorithm>
+
+struct dim3 {
+  unsigned x = 1, y = 1, z = 1;
+  dim3(unsigned a = 1, unsigned b = 1, unsigned c = 1) : x(a), y(b), z(c) {}
+};
+typedef struct CUstream_st* cudaStream_t;
+typedef int cudaError_t;
+constexpr int cudaSuccess = 0;
+
+inline thread_local dim3 threadIdx, blockIdx;
+inline dim3 blockDim, gridDim;
+inline thread_local int emu_lane = 0, emu_warp = 0;
+
+struct EmuWarp {
+  std::unique_ptr<std::barrier<>> bar;
+  float f[32];
+  int i[32];
+  unsigned u[32];
+};
+inline std::vector<EmuWarp>* emu_warps = nullptr;
+inline std::barrier<>* emu_block_bar = nullptr;
+inline std::vector<char> emu_dyn;
+
+#define __global__
+#define __device__
+#define __host__
+#define __forceinline__ inline
+#define __restrict__ __restrict
+#define __shared__ static
+#define __launch_bounds__(...)
+#define __grid_constant__
+
+inline void __syncthreads() { emu_block_bar->arrive_and_wait(); }
+inline void __syncwarp(unsigned = 0xffffffffu) { (*emu_warps)[emu_warp].bar->arrive_and_wait(); }
+inline float __shfl_xor_sync(unsigned, float v, int m) {
+  auto& w = (*emu_warps)[emu_warp];
+  w.f[emu_lane] = v;
+  w.bar->arrive_and_wait();
+  float r = w.f[emu_lane ^ m];
+  w.bar->arrive_and_wait();
+  return r;
+}
+inline int __shfl_xor_sync(unsigned, int v, int m) {
+  auto& w = (*emu_warps)[emu_warp];
+  w.i[emu_lane] = v;
+  w.bar->arrive_and_wait();
+  int r = w.i[emu_lane ^ m];
+  w.bar->arrive_and_wait();
+  return r;
+}
+inline unsigned atomicAdd(unsigned* p, unsigned v) { return std::atomic_ref<unsigned>(*p).fetch_add(v); }
+inline int atomicCAS(int* p, int cmp, int val) {
+  std::atomic_ref<int> a(*p);
+  int c = cmp;
+  a.compare_exchange_strong(c, val);
+  return c;
+}
+inline unsigned __float_as_uint(float x) { unsigned u; memcpy(&u, &x, 4); return u; }
+inline float __uint_as_float(unsigned u) { float x; memcpy(&x, &u, 4); return x; }
+inline float __int_as_float(int u) { float x; memcpy(&x, &u, 4); return x; }
+inline int __float_as_int(float x) { int u; memcpy(&u, &x, 4); return u; }
+inline float rsqrtf(float x) { return 1.0f / std::sqrt(x); }
+inline float __expf(float x) { return std::exp(x); }
+inline void sincos(double a, double* s, double* c) { *s = std::sin(a); *c = std::cos(a); }
+using std::min;
+using std::max;
+
+template <class T> T* emu_dyn_smem() { return reinterpret_cast<T*>(emu_dyn.data()); }
+
+// A pool of persistent host threads, one per CUDA thread slot of a block;
+// run(n, f) calls f(t) on threads t < n and returns when all of them are done.
+struct EmuPool {
+  std::vector<std::thread> th;
+  std::mutex mu;
+  std::condition_variable cv, done_cv;
+  std::function<void(unsigned)> job;
+  unsigned gen = 0, active = 0, nthr = 0;
+  bool stop = false;
+  explicit EmuPool(unsigned n) {
+    for (unsigned t = 0; t < n; ++t)
+      th.emplace_back([this, t]() {
+        unsigned seen = 0;
+        std::unique_lock<std::mutex> lk(mu);
+        for (;;) {
+          cv.wait(lk, [&] { return stop || gen != seen; });
+          if (stop) return;
+          seen = gen;
+          if (t >= nthr) continue;
+          auto j = job;
+          lk.unlock();
+          j(t);
+          lk.lock();
+          if (--active == 0) done_cv.notify_all();
+        }
+      });
+  }
+  ~EmuPool() {
+    {
+      std::lock_guard<std::mutex> lk(mu);
+      stop = true;
+    }
+    cv.notify_all();
+    for (auto& x : th) x.join();
+  }
+  void run(unsigned n, std::function<void(unsigned)> f) {
+    std::unique_lock<std::mutex> lk(mu);
+    job = std::move(f);
+    nthr = n;
+    active = n;
+    ++gen;
+    cv.notify_all();
+    done_cv.wait(lk, [&] { return active == 0; });
+  }
+};
+inline EmuPool& emu_pool() {
+  static EmuPool pool(1024);
+  return pool;
+}
+
+// Runs kernel(args...) over grid x block, one pool thread per CUDA thread,
+// blocks one after another.  Threads leave the barriers when they return.
+template <class F, class... A>
+void emu_launch(dim3 grid, dim3 block, size_t smem, F kernel, A... args) {
+  gridDim = grid;
+  blockDim = block;
+  const unsigned nthr = block.x * block.y * block.z;
+  const unsigned nw = (nthr + 31) / 32;
+  emu_dyn.assign(smem + 16, 0);
+  for (unsigned bz = 0; bz < grid.z; ++bz)
+    for (unsigned by = 0; by < grid.y; ++by)
+      for (unsigned bx = 0; bx < grid.x; ++bx) {
+        std::vector<EmuWarp> warps(nw);
+        for (unsigned w = 0; w < nw; ++w)
+          warps[w].bar = std::make_unique<std::barrier<>>(std::min(32u, nthr - 32 * w));
+        std::barrier<> bb(nthr);
+        emu_warps = &warps;
+        emu_block_bar = &bb;
+        emu_pool().run(nthr, [&](unsigned t) {
+          threadIdx = dim3(t % block.x, (t / block.x) % block.y, t / (block.x * block.y));
+          blockIdx = dim3(bx, by, bz);
+          emu_lane = t % 32;
+          emu_warp = t / 32;
+          kernel(args...);
+          (*emu_warps)[emu_warp].bar->arrive_and_drop();
+          emu_block_bar->arrive_and_drop();
+        });
+      }
+}
+
+struct float2 { float x, y; };
+struct float4 { float x, y, z, w; };
+struct uint2 { unsigned x, y; };
+inline float2 make_float2(float a, float b) { return float2{a, b}; }
+inline float4 make_float4(float a, float b, float c, float d) { return float4{a, b, c, d}; }
