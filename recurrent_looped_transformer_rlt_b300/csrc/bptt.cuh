@@ -247,6 +247,106 @@ __global__ void swa_fwd_kernel(const float* __restrict__ qkv, int p, int j0, int
   }
 }
 
+// Memory attention split over the keys: warp w = pair * nsplit + s takes
+// keys [j0 + s C, min(j1, j0 + (s + 1) C - 1)] (C = kAttnChunk), so that long
+// memories fill the GPU instead of one warp per (b, h) walking every key.
+// Partials part[(pair * nsplit + s) * (hd + 2) + ...]: the forward writes
+// acc[hd], the chunk's max and sum of exponentials; the backward writes the
+// unscaled query-gradient partial sum_j dS_j K_j and D.  The combines read the
+// splits in order (deterministic).
+#ifndef RLT_BPTT_ATTN_CHUNK
+#define RLT_BPTT_ATTN_CHUNK 64  // a compile-time parameter (the CPU tests build with small chunks)
+#endif
+constexpr int kAttnChunk = RLT_BPTT_ATTN_CHUNK;
+template <typename T>
+__global__ void attn_part_fwd_kernel(const float* __restrict__ q, const T* __restrict__ K, const T* __restrict__ V,
+                                     int Tk, int j0, int j1, int B, int H, int hd, float scale, int nsplit,
+                                     float* __restrict__ part) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= B * H * nsplit) return;
+  const int pair = wid / nsplit, sp = wid - pair * nsplit;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd;
+  const int NC = (hd + 31) >> 5;
+  const int ja = j0 + sp * kAttnChunk, jb = min(j1, ja + kAttnChunk - 1);
+  float qr[4], acc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    qr[c] = (c < NC && i < hd) ? q[(size_t)b * d + h * hd + i] : 0.f;
+    acc[c] = 0.f;
+  }
+  const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+  const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+  float mx = -INFINITY, l = 0.f;
+  for (int j = ja; j <= jb; ++j) {
+    float part_s = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) part_s = fmaf(qr[c], to_f32(Kb[(size_t)j * hd + i]), part_s);
+    }
+    const float sj = warp_sum(part_s) * scale;
+    const float mn = fmaxf(mx, sj);
+    const float corr = expf(mx - mn), w = expf(sj - mn);
+    l = l * corr + w;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) acc[c] = acc[c] * corr + w * to_f32(Vb[(size_t)j * hd + i]);
+    }
+    mx = mn;
+  }
+  float* pp = part + (size_t)wid * (hd + 2);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) pp[i] = acc[c];
+  }
+  if (lane == 0) {
+    pp[hd] = mx;
+    pp[hd + 1] = l;
+  }
+}
+
+// Combine of the forward partials, one warp per (b, h): lse, the output in
+// the storage type to oq [B][d] (and to oT when given).
+template <typename T>
+__global__ void attn_combine_fwd_kernel(const float* __restrict__ part, int nsplit, int B, int H, int hd,
+                                        float* __restrict__ lse, T* __restrict__ oq, T* __restrict__ oT, int ldT) {
+  const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (pair >= B * H) return;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd;
+  const int NC = (hd + 31) >> 5;
+  const float* pp = part + (size_t)pair * nsplit * (hd + 2);
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pp[(size_t)s * (hd + 2) + hd]);
+  float Lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < nsplit; ++s) {
+    const float* ps = pp + (size_t)s * (hd + 2);
+    const float w = expf(ps[hd] - M);
+    Lsum = fmaf(ps[hd + 1], w, Lsum);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) acc[c] = fmaf(ps[i], w, acc[c]);
+    }
+  }
+  if (lane == 0) lse[pair] = M + logf(Lsum);
+  const float inv = 1.0f / Lsum;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) {
+      const size_t col = (size_t)h * hd + i;
+      const T vq = from_f32<T>(acc[c] * inv);
+      oq[(size_t)b * d + col] = vq;
+      if (oT) oT[col * ldT + b] = vq;
+    }
+  }
+}
+
 // yT[j][b] = x[b][j] (rows of a recorded [B][N] operand into a column slot).
 template <typename T>
 __global__ void tcopy_kernel(const T* __restrict__ x, int B, int N, T* __restrict__ yT, int ldT) {
@@ -551,6 +651,95 @@ __global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __rest
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[c] = fmaf(dS, kv[c], acc[c]);
   }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) {
+      const size_t col = (size_t)h * hd + i;
+      const T v = from_f32<T>(scale * acc[c]);
+      dqY[(size_t)b * d + col] = v;
+      dqT[col * ldT + b] = v;
+    }
+  }
+}
+
+// Query-gradient partials over the key split (see attn_part_fwd_kernel):
+// warp (pair, s) writes sum_{j in its chunk} dS_j K_j (unscaled) and D = g.o.
+template <typename T>
+__global__ void attn_part_bwd_kernel(const float* __restrict__ q, const float* __restrict__ gout,
+                                     const T* __restrict__ o, const float* __restrict__ lse, const T* __restrict__ K,
+                                     const T* __restrict__ V, int Tk, int j0, int j1, int B, int H, int hd,
+                                     float scale, int nsplit, float* __restrict__ part) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= B * H * nsplit) return;
+  const int pair = wid / nsplit, sp = wid - pair * nsplit;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd;
+  const int NC = (hd + 31) >> 5;
+  const int ja = j0 + sp * kAttnChunk, jb = min(j1, ja + kAttnChunk - 1);
+  float qr[4], gr[4], acc[4];
+  float Dp = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const bool ok = c < NC && i < hd;
+    const size_t col = (size_t)b * d + h * hd + i;
+    qr[c] = ok ? q[col] : 0.f;
+    gr[c] = ok ? gout[col] : 0.f;
+    acc[c] = 0.f;
+    if (ok) Dp = fmaf(gr[c], to_f32(o[col]), Dp);
+  }
+  const float D = warp_sum(Dp);
+  const float ls = lse[pair];
+  const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+  const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+  for (int j = ja; j <= jb; ++j) {
+    float kv[4], spq = 0.f, dpp = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      kv[c] = 0.f;
+      if (c < NC && i < hd) {
+        kv[c] = to_f32(Kb[(size_t)j * hd + i]);
+        spq = fmaf(qr[c], kv[c], spq);
+        dpp = fmaf(gr[c], to_f32(Vb[(size_t)j * hd + i]), dpp);
+      }
+    }
+    const float P = expf(warp_sum(spq) * scale - ls);
+    const float dS = P * (warp_sum(dpp) - D);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = fmaf(dS, kv[c], acc[c]);
+  }
+  float* pp = part + (size_t)wid * (hd + 2);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) pp[i] = acc[c];
+  }
+  if (lane == 0) pp[hd] = D;
+}
+
+// Combine of the query-gradient partials, one warp per (b, h): dq = scale *
+// sum over splits in order, written as the next projection's operands (dqY
+// [B][d] storage type, dqT transposed); D to Dout [B][H] when given.
+template <typename T>
+__global__ void attn_combine_bwd_kernel(const float* __restrict__ part, int nsplit, int B, int H, int hd, float scale,
+                                        float* __restrict__ Dout, T* __restrict__ dqY, T* __restrict__ dqT, int ldT) {
+  const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (pair >= B * H) return;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd;
+  const int NC = (hd + 31) >> 5;
+  const float* pp = part + (size_t)pair * nsplit * (hd + 2);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < nsplit; ++s) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) acc[c] += pp[(size_t)s * (hd + 2) + i];
+    }
+  }
+  if (Dout && lane == 0) Dout[pair] = pp[hd];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int i = lane + 32 * c;

@@ -99,10 +99,23 @@ struct BpttOps {
                                                                             K, V, Tk, lse, oq, oT, ldT);
     return post();
   }
+  // attention over positions j0..j1: one warp per (b, h) for short ranges,
+  // else split over the keys (part: scratch of the partials) and combined
   int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
-               float* lse, T* oq, T* oT, int ldT) {
-    bptt::attn_fwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(q, K, V, Tk, j0, j1, B, H, hd, scale,
-                                                                             lse, oq, oT, ldT);
+               float* lse, T* oq, T* oT, int ldT, float* part) {
+    const int nsplit = (j1 - j0 + bptt::kAttnChunk) / bptt::kAttnChunk;
+    const size_t pairs = (size_t)B * H;
+    if (nsplit <= 1) {
+      bptt::attn_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(q, K, V, Tk, j0, j1, B, H, hd, scale, lse,
+                                                                        oq, oT, ldT);
+      return post();
+    }
+    bptt::attn_part_fwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(q, K, V, Tk, j0, j1, B, H, hd,
+                                                                                    scale, nsplit, part);
+    int rc = post();
+    if (rc) return rc;
+    bptt::attn_combine_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(part, nsplit, B, H, hd, lse, oq, oT,
+                                                                             ldT);
     return post();
   }
   int tcopy(const T* x, int B, int N, T* yT, int ldT) {
@@ -128,9 +141,20 @@ struct BpttOps {
     return post();
   }
   int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* Dout, T* dqY, T* dqT, int ldT) {
-    bptt::attn_bwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(q, gout, o, lse, K, V, Tk, j0, j1, B,
-                                                                             H, hd, scale, Dout, dqY, dqT, ldT);
+               int j0, int j1, int B, int H, int hd, float scale, float* Dout, T* dqY, T* dqT, int ldT, float* part) {
+    const int nsplit = (j1 - j0 + bptt::kAttnChunk) / bptt::kAttnChunk;
+    const size_t pairs = (size_t)B * H;
+    if (nsplit <= 1) {
+      bptt::attn_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd,
+                                                                        scale, Dout, dqY, dqT, ldT);
+      return post();
+    }
+    bptt::attn_part_bwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(
+        q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd, scale, nsplit, part);
+    int rc = post();
+    if (rc) return rc;
+    bptt::attn_combine_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(part, nsplit, B, H, hd, scale, Dout,
+                                                                             dqY, dqT, ldT);
     return post();
   }
   int swa_bwd(const T* K, const T* V, int Tk, int j0, int p, int p_last, const T* o, const float* qR,
@@ -193,6 +217,7 @@ bpplan::Shape bptt_shape(const rlt_model* m, int B, int n, int T_mem, float temp
   // whole 64-wide k-blocks
   S.Bp = (c.dtype == RLT_BF16) ? (B + 63) / 64 * 64 : B;
   S.S = n < kBpttBlock ? n : kBpttBlock;
+  S.chunk = bptt::kAttnChunk;
   return S;
 }
 

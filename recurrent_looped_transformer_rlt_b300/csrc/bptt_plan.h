@@ -58,6 +58,7 @@ struct Shape {
   int top_k;
   int Bp;                          // columns per step slot of the transposed operands (B rounded up; zero past B)
   int S;                           // steps per block (weight and memory gradients are added once per block)
+  int chunk;                       // keys per warp of the split memory attention (scratch sizing)
 };
 
 struct Detach {
@@ -100,6 +101,7 @@ struct Layout {
   size_t xgT, aT, cT, bbT, oT, oxT, mT, snT;
   size_t dlT, dzT, dhfT, dhxT, dhaT, dqxT, dguT, dqkvT;
   size_t qxS, gxS, DxS;  // [S][L][B][d], [S][L][B][d] f32, [S][L][B][H] f32
+  size_t part;          // [B][H][ceil(n / chunk)][hd + 2] f32 split-attention partials
   // gradient scratch
   size_t ds, dh, dx, dY, dY2;
   size_t total;
@@ -175,6 +177,8 @@ inline Layout layout(const Shape& S, size_t es, size_t hdr) {
   Lw.qxS = take(4 * SB * L * Bd);
   Lw.gxS = take(4 * SB * L * Bd);
   Lw.DxS = take(4 * SB * L * B * H);
+  const size_t nsplit = S.chunk > 0 ? (n + S.chunk - 1) / S.chunk : 1;
+  Lw.part = take(4 * B * H * nsplit * (hd + 2));
   Lw.ds = take(4 * Bd);
   Lw.dh = take(4 * Bd);
   Lw.dx = take(4 * Bd);
@@ -309,7 +313,7 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
         const int g = S.G == 1 ? 0 : l;
         RLT_BP_TRY(k.attn_fwd(qx, io.mem + (size_t)(2 * g) * plane_m, io.mem + (size_t)(2 * g + 1) * plane_m,
                               S.T_mem, 0, p, B, H, hd, S.scale, lse2_all + ((size_t)p * L + l) * BH, xo, nullptr,
-                              ldT));
+                              ldT, F(Lw.part)));
       } else {
         RLT_BP_TRY(k.tcopy(xo, B, d, col(Lw.oxT, (size_t)l * d, slot), ldT));
       }
@@ -407,7 +411,8 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       RLT_BP_TRY(k.attn_bwd(F(Lw.qxS) + ((size_t)slot * L + l) * Bd, gx, xo_all + ((size_t)p * L + l) * Bd,
                             lse2_all + ((size_t)p * L + l) * BH, io.mem + (size_t)(2 * g) * plane_m,
                             io.mem + (size_t)(2 * g + 1) * plane_m, S.T_mem, 0, p, B, H, hd, S.scale,
-                            F(Lw.DxS) + ((size_t)slot * L + l) * BH, dY, col(Lw.dqxT, (size_t)l * d, slot), ldT));
+                            F(Lw.DxS) + ((size_t)slot * L + l) * BH, dY, col(Lw.dqxT, (size_t)l * d, slot), ldT,
+                            F(Lw.part)));
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Qx + l * dd, d, d, dx, d, false));
       RLT_BP_TRY(k.rms_bwd(hX, F(Lw.rX) + l * B, P.xattn_norm + (size_t)l * d, dx, B, d, dh,
                            G.xattn_norm + (size_t)l * d, dY, col(Lw.dhaT, (size_t)l * d, slot), ldT));

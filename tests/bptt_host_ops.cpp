@@ -149,7 +149,7 @@ struct HostOps {
         }
   }
   int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
-               float* lse, T* oq, T* oT, int ldT) {
+               float* lse, T* oq, T* oT, int ldT, float* /* scratch of the device's key split */ = nullptr) {
     const int d = H * hd;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h) {
@@ -311,7 +311,8 @@ struct HostOps {
   // the query gradient of the cross-attention, written as the next
   // projection's operands (storage type [B][d] and transposed)
   int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* Dout, T* dqY, T* dqT, int ldT) {
+               int j0, int j1, int B, int H, int hd, float scale, float* Dout, T* dqY, T* dqT, int ldT,
+               float* /* scratch of the device's key split */) {
     const int d = H * hd;
     std::vector<float> dq((size_t)B * d);
     attn_dq(q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd, scale, dq.data(), Dout);
@@ -495,6 +496,7 @@ extern "C" int bptt_host(const int* sh, const float* fp, void** P) {
   S.inv_temp = 1.0f / fp[2];
   S.Bp = S.B;
   S.S = sh[16];
+  S.chunk = 0;
   const bool bf16 = sh[17] != 0;
   const bpplan::Detach D{sh[13], sh[14] != 0, sh[15] != 0};
   auto cf = [&](int i) { return static_cast<const float*>(P[i]); };

@@ -75,6 +75,7 @@ static int run_emu(const int* sh, const float* fp, void** P, const size_t* nel) 
   const bool bf = std::is_same<T, bf16>::value;
   S.Bp = bf ? (S.B + 63) / 64 * 64 : S.B;
   S.S = sh[16];
+  S.chunk = bptt::kAttnChunk;  // the partials scratch is sized for the kernels' key split
   bpplan::Detach D{sh[13], sh[14] != 0, sh[15] != 0};
   // matrices in the storage type (indices 0..8 and e, mem), the rest fp32
   std::vector<std::vector<T>> keepT;

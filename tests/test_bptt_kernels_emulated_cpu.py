@@ -53,8 +53,11 @@ def emu(tmp_path_factory):
     d = str(tmp_path_factory.mktemp("simt_emu"))
     _generate(d)
     lib = os.path.join(d, "libemu.so")
-    r = subprocess.run([cxx, "-std=c++20", "-O1", "-shared", "-fPIC", "-pthread", "-I", d, "-I", EMU, "-I", CSRC,
-                        "-o", lib, os.path.join(EMU, "emu_harness.cpp")], capture_output=True, text=True)
+    # keys per warp of the split memory attention: 3, so that the short test
+    # sequences take both the single-warp and the split-and-combine paths
+    r = subprocess.run([cxx, "-std=c++20", "-O1", "-shared", "-fPIC", "-pthread", "-DRLT_BPTT_ATTN_CHUNK=3", "-I", d,
+                        "-I", EMU, "-I", CSRC, "-o", lib, os.path.join(EMU, "emu_harness.cpp")],
+                       capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-3000:]
     h = ctypes.CDLL(lib)
     h.bptt_emu.restype = ctypes.c_int
