@@ -347,6 +347,87 @@ __global__ void attn_combine_fwd_kernel(const float* __restrict__ part, int nspl
   }
 }
 
+// Window attention forward of position p split over the keys: warp
+// (pair, s) applies RoPE to q (and the split holding position p also to k,
+// writing k and v at p) and attends over its chunk of positions j0..p;
+// split 0 writes the rotated q to qo.  Partials as attn_part_fwd_kernel (its
+// combine finishes).
+template <typename T>
+__global__ void swa_part_fwd_kernel(const float* __restrict__ qkv, int p, int j0, int B, int H, int hd, float theta,
+                                    float scale, int nsplit, float* __restrict__ qo, T* __restrict__ K,
+                                    T* __restrict__ V, int Tk, float* __restrict__ part) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= B * H * nsplit) return;
+  const int pair = wid / nsplit, sp = wid - pair * nsplit;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd, half = hd >> 1;
+  const int NC = (hd + 31) >> 5;
+  const int ja = j0 + sp * kAttnChunk, jb = min(p, ja + kAttnChunk - 1);
+  const bool has_p = jb == p;
+  const float* row = qkv + (size_t)b * 3 * d + h * hd;
+  float qv[4], kv[4], vv[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const bool ok = c < NC && i < hd;
+    qv[c] = ok ? row[i] : 0.f;
+    kv[c] = ok ? row[d + i] : 0.f;
+    vv[c] = ok ? row[2 * d + i] : 0.f;
+  }
+  float qr[4], kr[4], acc[4];
+  const size_t kp = (((size_t)b * H + h) * Tk + p) * hd;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const float qp = rope_partner(qv, c, hd), kpv = rope_partner(kv, c, hd);
+    float cs = 1.f, sn = 0.f;
+    if (c < NC && i < hd) rope_cs(p, i % half, hd, theta, cs, sn);
+    const float sg = (i % hd) < half ? -1.f : 1.f;
+    qr[c] = qv[c] * cs + sg * qp * sn;
+    kr[c] = round_st<T>(kv[c] * cs + sg * kpv * sn);
+    vv[c] = round_st<T>(vv[c]);
+    acc[c] = 0.f;
+    if (c < NC && i < hd) {
+      if (sp == 0) qo[(size_t)b * d + h * hd + i] = qr[c];
+      if (has_p) {
+        K[kp + i] = from_f32<T>(kr[c]);
+        V[kp + i] = from_f32<T>(vv[c]);
+      }
+    }
+  }
+  const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+  const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+  float mx = -INFINITY, l = 0.f;
+  for (int j = ja; j <= jb; ++j) {
+    float part_s = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) part_s = fmaf(qr[c], j == p ? kr[c] : to_f32(Kb[(size_t)j * hd + i]), part_s);
+    }
+    const float sj = warp_sum(part_s) * scale;
+    const float mn = fmaxf(mx, sj);
+    const float corr = expf(mx - mn), w = expf(sj - mn);
+    l = l * corr + w;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) acc[c] = acc[c] * corr + w * (j == p ? vv[c] : to_f32(Vb[(size_t)j * hd + i]));
+    }
+    mx = mn;
+  }
+  float* pp = part + (size_t)wid * (hd + 2);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) pp[i] = acc[c];
+  }
+  if (lane == 0) {
+    pp[hd] = mx;
+    pp[hd + 1] = l;
+  }
+}
+
 // yT[j][b] = x[b][j] (rows of a recorded [B][N] operand into a column slot).
 template <typename T>
 __global__ void tcopy_kernel(const T* __restrict__ x, int B, int N, T* __restrict__ yT, int ldT) {
@@ -748,6 +829,153 @@ __global__ void attn_combine_bwd_kernel(const float* __restrict__ part, int nspl
       const T v = from_f32<T>(scale * acc[c]);
       dqY[(size_t)b * d + col] = v;
       dqT[col * ldT + b] = v;
+    }
+  }
+}
+
+// Window attention backward of position p split over warps (pair, s): the
+// query-gradient partial over key chunk s of positions j0..p and the
+// key/value-gradient partial of position p over record chunk s of positions
+// p..p_last (either may be empty); D = g.o from this step's record and the
+// stored output.  Partials part[(pair * nsplit + s) * (3 hd + 1)]: dq (unscaled),
+// dK, dV, then D.  swa_combine_bwd_kernel finishes.
+template <typename T>
+__global__ void swa_part_bwd_kernel(const T* __restrict__ K, const T* __restrict__ V, int Tk, int j0, int p,
+                                    int p_last, const T* __restrict__ o, const float* __restrict__ qR,
+                                    const float* __restrict__ gR, const float* __restrict__ lR,
+                                    const float* __restrict__ DR, int W, int B, int H, int hd, float scale, int nsplit,
+                                    float* __restrict__ part) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= B * H * nsplit) return;
+  const int pair = wid / nsplit, sp = wid - pair * nsplit;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd;
+  const int NC = (hd + 31) >> 5;
+  const size_t r0 = (size_t)(p % W) * B + b;
+  float qr[4], gr[4], kp[4], vp[4], dq[4], dk[4], dv[4];
+  float Dp = 0.f;
+  const size_t kpo = (((size_t)b * H + h) * Tk + p) * hd;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const bool ok = c < NC && i < hd;
+    qr[c] = ok ? qR[r0 * d + h * hd + i] : 0.f;
+    gr[c] = ok ? gR[r0 * d + h * hd + i] : 0.f;
+    kp[c] = ok ? to_f32(K[kpo + i]) : 0.f;
+    vp[c] = ok ? to_f32(V[kpo + i]) : 0.f;
+    dq[c] = dk[c] = dv[c] = 0.f;
+    if (ok) Dp = fmaf(gr[c], to_f32(o[(size_t)b * d + h * hd + i]), Dp);
+  }
+  const float D = warp_sum(Dp);
+  const float ls = lR[r0 * H + h];
+  const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
+  const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
+  const int ja = j0 + sp * kAttnChunk, jb = min(p, ja + kAttnChunk - 1);
+  for (int j = ja; j <= jb; ++j) {
+    float kv[4], s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      kv[c] = 0.f;
+      if (c < NC && i < hd) {
+        kv[c] = to_f32(Kb[(size_t)j * hd + i]);
+        s1 = fmaf(qr[c], kv[c], s1);
+        s2 = fmaf(gr[c], to_f32(Vb[(size_t)j * hd + i]), s2);
+      }
+    }
+    const float P = expf(warp_sum(s1) * scale - ls);
+    const float dS = P * (warp_sum(s2) - D);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dq[c] = fmaf(dS, kv[c], dq[c]);
+  }
+  const int ra = p + sp * kAttnChunk, rb = min(p_last, ra + kAttnChunk - 1);
+  for (int pp = ra; pp <= rb; ++pp) {
+    const size_t rr = (size_t)(pp % W) * B + b;
+    float qv[4], gv[4], s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      const bool ok = c < NC && i < hd;
+      qv[c] = pp == p ? qr[c] : (ok ? qR[rr * d + h * hd + i] : 0.f);
+      gv[c] = pp == p ? gr[c] : (ok ? gR[rr * d + h * hd + i] : 0.f);
+      s1 = fmaf(qv[c], kp[c], s1);
+      s2 = fmaf(gv[c], vp[c], s2);
+    }
+    const float lsr = pp == p ? ls : lR[rr * H + h];
+    const float Dr = pp == p ? D : DR[rr * H + h];
+    const float P = expf(warp_sum(s1) * scale - lsr);
+    const float dS = P * (warp_sum(s2) - Dr);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      dk[c] = fmaf(scale * dS, qv[c], dk[c]);
+      dv[c] = fmaf(P, gv[c], dv[c]);
+    }
+  }
+  float* pp_ = part + (size_t)wid * (3 * hd + 1);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) {
+      pp_[i] = dq[c];
+      pp_[hd + i] = dk[c];
+      pp_[2 * hd + i] = dv[c];
+    }
+  }
+  if (lane == 0) pp_[3 * hd] = D;
+}
+
+// Combine of the window-backward partials, one warp per (b, h): sums in split
+// order, D to this step's record, then dq (scaled) and dK back through RoPE at
+// p and dV as is into d qkv dY [B][3d] and its transposed slot dYT.
+template <typename T>
+__global__ void swa_combine_bwd_kernel(const float* __restrict__ part, int nsplit, int p, int W, int B, int H, int hd,
+                                       float scale, float theta, float* __restrict__ DR, T* __restrict__ dY,
+                                       T* __restrict__ dYT, int ldT) {
+  const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (pair >= B * H) return;
+  const int b = pair / H, h = pair - b * H;
+  const int d = H * hd, half = hd >> 1;
+  const int NC = (hd + 31) >> 5;
+  const float* pp = part + (size_t)pair * nsplit * (3 * hd + 1);
+  float dq[4] = {0.f, 0.f, 0.f, 0.f}, dk[4] = {0.f, 0.f, 0.f, 0.f}, dv[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < nsplit; ++s) {
+    const float* ps = pp + (size_t)s * (3 * hd + 1);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = lane + 32 * c;
+      if (c < NC && i < hd) {
+        dq[c] += ps[i];
+        dk[c] += ps[hd + i];
+        dv[c] += ps[2 * hd + i];
+      }
+    }
+  }
+  if (lane == 0) DR[((size_t)(p % W) * B + b) * H + h] = pp[3 * hd];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) dq[c] *= scale;
+  float out_q[4], out_k[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    const float qp = rope_partner(dq, c, hd), kpp = rope_partner(dk, c, hd);
+    float cs = 1.f, sn = 0.f;
+    if (c < NC && i < hd) rope_cs(p, i % half, hd, theta, cs, sn);
+    const float sg = (i % hd) < half ? 1.f : -1.f;
+    out_q[c] = dq[c] * cs + sg * qp * sn;
+    out_k[c] = dk[c] * cs + sg * kpp * sn;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int i = lane + 32 * c;
+    if (c < NC && i < hd) {
+      const int cq = h * hd + i, ck = d + h * hd + i, cv = 2 * d + h * hd + i;
+      const T vq = from_f32<T>(out_q[c]), vk = from_f32<T>(out_k[c]), vv = from_f32<T>(dv[c]);
+      dY[(size_t)b * 3 * d + cq] = vq;
+      dY[(size_t)b * 3 * d + ck] = vk;
+      dY[(size_t)b * 3 * d + cv] = vv;
+      dYT[(size_t)cq * ldT + b] = vq;
+      dYT[(size_t)ck * ldT + b] = vk;
+      dYT[(size_t)cv * ldT + b] = vv;
     }
   }
 }

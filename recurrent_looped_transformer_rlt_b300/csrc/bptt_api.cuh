@@ -93,10 +93,23 @@ struct BpttOps {
     bptt::rms_fwd_kernel<T><<<blocks((size_t)B * 32), bptt::kThreads, 0, st>>>(x, g, B, d, eps, r, y, yT, ldT);
     return post();
   }
+  // window attention forward: one warp per (b, h) for windows of one chunk,
+  // else split over the keys and combined (part: scratch of the partials)
   int swa_fwd(const float* qkv, int p, int j0, int B, int H, int hd, float theta, float scale, float* qo, T* K, T* V,
-              int Tk, float* lse, T* oq, T* oT, int ldT) {
-    bptt::swa_fwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(qkv, p, j0, B, H, hd, theta, scale, qo,
-                                                                            K, V, Tk, lse, oq, oT, ldT);
+              int Tk, float* lse, T* oq, T* oT, int ldT, float* part) {
+    const int nsplit = (p - j0 + bptt::kAttnChunk) / bptt::kAttnChunk;
+    const size_t pairs = (size_t)B * H;
+    if (nsplit <= 1) {
+      bptt::swa_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(qkv, p, j0, B, H, hd, theta, scale, qo, K, V,
+                                                                       Tk, lse, oq, oT, ldT);
+      return post();
+    }
+    bptt::swa_part_fwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(qkv, p, j0, B, H, hd, theta,
+                                                                                   scale, nsplit, qo, K, V, Tk, part);
+    int rc = post();
+    if (rc) return rc;
+    bptt::attn_combine_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(part, nsplit, B, H, hd, lse, oq, oT,
+                                                                             ldT);
     return post();
   }
   // attention over positions j0..j1: one warp per (b, h) for short ranges,
@@ -157,11 +170,26 @@ struct BpttOps {
                                                                              dqY, dqT, ldT);
     return post();
   }
+  // window attention backward: one warp per (b, h) when the window and the
+  // records fit one chunk each, else split and combined
   int swa_bwd(const T* K, const T* V, int Tk, int j0, int p, int p_last, const T* o, const float* qR,
               const float* gR, float* lR, float* DR, int W, int B, int H, int hd, float scale, float theta, T* dY,
-              T* dYT, int ldT) {
-    bptt::swa_bwd_kernel<T><<<blocks((size_t)B * H * 32, 128), 128, 0, st>>>(
-        K, V, Tk, j0, p, p_last, o, qR, gR, lR, DR, W, B, H, hd, scale, theta, dY, dYT, ldT);
+              T* dYT, int ldT, float* part) {
+    const int nk = (p - j0 + bptt::kAttnChunk) / bptt::kAttnChunk;
+    const int nr = (p_last - p + bptt::kAttnChunk) / bptt::kAttnChunk;
+    const int nsplit = nk > nr ? nk : nr;
+    const size_t pairs = (size_t)B * H;
+    if (nsplit <= 1) {
+      bptt::swa_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(
+          K, V, Tk, j0, p, p_last, o, qR, gR, lR, DR, W, B, H, hd, scale, theta, dY, dYT, ldT);
+      return post();
+    }
+    bptt::swa_part_bwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(
+        K, V, Tk, j0, p, p_last, o, qR, gR, lR, DR, W, B, H, hd, scale, nsplit, part);
+    int rc = post();
+    if (rc) return rc;
+    bptt::swa_combine_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(part, nsplit, p, W, B, H, hd, scale,
+                                                                            theta, DR, dY, dYT, ldT);
     return post();
   }
   int mem_grad(const T* K, const T* V, int T_mem, const float* qS, const float* gS, const float* lse_all,

@@ -101,7 +101,7 @@ struct Layout {
   size_t xgT, aT, cT, bbT, oT, oxT, mT, snT;
   size_t dlT, dzT, dhfT, dhxT, dhaT, dqxT, dguT, dqkvT;
   size_t qxS, gxS, DxS;  // [S][L][B][d], [S][L][B][d] f32, [S][L][B][H] f32
-  size_t part;          // [B][H][ceil(n / chunk)][hd + 2] f32 split-attention partials
+  size_t part;          // f32 split-attention partials: [B][H][splits][hd + 2] or [3 hd + 1] (window backward)
   // gradient scratch
   size_t ds, dh, dx, dY, dY2;
   size_t total;
@@ -178,7 +178,9 @@ inline Layout layout(const Shape& S, size_t es, size_t hdr) {
   Lw.gxS = take(4 * SB * L * Bd);
   Lw.DxS = take(4 * SB * L * B * H);
   const size_t nsplit = S.chunk > 0 ? (n + S.chunk - 1) / S.chunk : 1;
-  Lw.part = take(4 * B * H * nsplit * (hd + 2));
+  const size_t wsplit = S.chunk > 0 ? (W + S.chunk - 1) / S.chunk : 1;
+  const size_t per_pair = nsplit * (hd + 2) > wsplit * (3 * hd + 1) ? nsplit * (hd + 2) : wsplit * (3 * hd + 1);
+  Lw.part = take(4 * B * H * per_pair);
   Lw.ds = take(4 * Bd);
   Lw.dh = take(4 * Bd);
   Lw.dx = take(4 * Bd);
@@ -301,7 +303,8 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       const size_t rec = (size_t)l * W + p % W;  // this position's record slot
       const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
       RLT_BP_TRY(k.swa_fwd(qkv, p, j0, B, H, hd, S.theta, S.scale, F(Lw.qR) + rec * Bd, Kl, Vl, n,
-                           F(Lw.lR) + rec * BH, X(Lw.oq) + l * Bd, col(Lw.oT, (size_t)l * d, slot), ldT));
+                           F(Lw.lR) + rec * BH, X(Lw.oq) + l * Bd, col(Lw.oT, (size_t)l * d, slot), ldT,
+                           F(Lw.part)));
       RLT_BP_TRY(k.gemm_res(X(Lw.oq) + l * Bd, d, B, d, P.W_O + l * dd, d, d, hA, hX, d));
       // cross-attention to memory positions 0..p (recorded in the first pass)
       RLT_BP_TRY(k.rms_fwd(hX, P.xattn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rX) + l * B, X(Lw.c) + l * Bd,
@@ -428,7 +431,8 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       const int p_last = D.cache ? p : (p + W - 1 < n - 1 ? p + W - 1 : n - 1);
       RLT_BP_TRY(k.swa_bwd(Kl, Vl, n, j0, p, p_last, X(Lw.oq) + l * Bd, F(Lw.qR) + (size_t)l * W * Bd,
                            F(Lw.gR) + (size_t)l * W * Bd, F(Lw.lR) + (size_t)l * W * BH, F(Lw.DR) + (size_t)l * W * BH,
-                           W, B, H, hd, S.scale, S.theta, dY, col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT));
+                           W, B, H, hd, S.scale, S.theta, dY, col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT,
+                           F(Lw.part)));
       RLT_BP_TRY(k.gemm(dY, 3 * d, B, 3 * d, wt_qkv + l * 3 * dd, 3 * d, d, dx, d, false));
       // (layer l-1's FFN section reads dh as its dY; the merge reads dh)
       RLT_BP_TRY(k.rms_bwd(hA, F(Lw.rA) + l * B, P.attn_norm + (size_t)l * d, dx, B, d, dh,

@@ -181,7 +181,7 @@ struct HostOps {
   // fp32, k and v to K/V [B][H][Tk][hd] at p), then the attention of q over
   // positions j0..p (lse, oq and its transposed slot)
   int swa_fwd(const float* qkv, int p, int j0, int B, int H, int hd, float theta, float scale, float* qo, T* K, T* V,
-              int Tk, float* lse, T* oq, T* oT, int ldT) {
+              int Tk, float* lse, T* oq, T* oT, int ldT, float* /* scratch of the device's key split */) {
     qkv_post(qkv, p, B, H, hd, theta, qo, K, V, Tk);
     return attn_fwd(qo, K, V, Tk, j0, p, B, H, hd, scale, lse, oq, oT, ldT);
   }
@@ -416,7 +416,7 @@ struct HostOps {
   // into d qkv [B][3d] (storage type, and transposed)
   int swa_bwd(const T* K, const T* V, int Tk, int j0, int p, int p_last, const T* o, const float* qR,
               const float* gR, float* lR, float* DR, int W, int B, int H, int hd, float scale, float theta, T* dY,
-              T* dYT, int ldT) {
+              T* dYT, int ldT, float* /* scratch of the device's split */) {
     const size_t Bd = (size_t)B * H * hd, BH = (size_t)B * H, r = (size_t)(p % W);
     std::vector<float> dq(Bd), dK(Bd), dV(Bd);
     attn_dq(qR + r * Bd, gR + r * Bd, o, lR + r * BH, K, V, Tk, j0, p, B, H, hd, scale, dq.data(), DR + r * BH);

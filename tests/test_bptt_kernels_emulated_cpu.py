@@ -95,6 +95,7 @@ def _worst(loss, g, d_e, d_mem, lref, gref):
 @pytest.mark.parametrize("setup_kw,kw", [
     ({"G": 2}, {}),                                        # ring wraps, one memory group per layer
     ({"T": 9}, {"s_every": 3, "cache": True, "memory": True}),
+    ({"T": 9, "window": 7}, {}),                           # window and records over several 3-key chunks
 ])
 def test_emulated_kernels_fp32(emu, setup_kw, kw):
     c, W, e, mem, acts = S._setup(**setup_kw)
