@@ -329,8 +329,8 @@ RLT_API int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t sn
  * word, cleared by rlt_workspace_init).  Errors: RLT_EINVAL (null or
  * misaligned pointer, n > T_mem, bad temperature / top_k / flags),
  * RLT_EWORKSPACE, RLT_EUNSUPPORTED (bf16 model with vocab not a multiple of
- * 8); an action >= V sets RLT_EBOUNDS in the status word and counts as
- * absent. */
+ * 8, or B * n_heads > 65535); an action >= V sets RLT_EBOUNDS in the status
+ * word and counts as absent. */
 enum { RLT_DETACH_CACHE = 1, RLT_DETACH_MEMORY = 2 };
 typedef struct rlt_grads {
   float *W_g, *b_g, *W_qkv, *W_O, *W_Qx, *W_Ox, *W_1, *W_3, *W_2, *W_o;

@@ -322,6 +322,8 @@ int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, 
   // bf16 models: d logits [B][V] and W_o^T [d][V] are tensor-core operands
   // with a row pitch of V elements (16-byte multiples)
   if (m->cfg.dtype == RLT_BF16 && m->cfg.vocab % 8 != 0) return RLT_EUNSUPPORTED;
+  // the memory-gradient grid has one row per (sequence, head)
+  if ((int64_t)B * m->cfg.n_heads > 65535) return RLT_EUNSUPPORTED;
   const bpplan::Shape S = bptt_shape(m, B, n, T_mem, temperature, top_k);
   if (ws_bytes < bpplan::layout(S, m->esz, kBpttHeader).total) return RLT_EWORKSPACE;
   int rc = bptt_attrs();
