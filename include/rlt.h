@@ -323,6 +323,10 @@ RLT_API int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t sn
  *   RLT_DETACH_CACHE: the window keys/values of earlier positions enter later
  *     steps as constants (each step keeps the gradient of its own entry);
  *   RLT_DETACH_MEMORY: the memory is a constant (d_mem stays zero).
+ * Execution (flags): each step's launches are captured once as a CUDA graph
+ * (on the model's capture stream; one graph for the recording step and one
+ * per slot of a 16-step block) and replayed on the caller's stream;
+ * RLT_BPTT_NO_GRAPHS launches them one by one instead (same results).
  * Work: a forward pass recording s_t and every position's keys and values,
  * then a reverse pass that recomputes each step's activations; workspace
  * rlt_bptt_workspace_size(m, B, n) bytes (its first 256 bytes are the status
@@ -331,7 +335,7 @@ RLT_API int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t sn
  * RLT_EWORKSPACE, RLT_EUNSUPPORTED (bf16 model with vocab not a multiple of
  * 8, or B * n_heads > 65535); an action >= V sets RLT_EBOUNDS in the status
  * word and counts as absent. */
-enum { RLT_DETACH_CACHE = 1, RLT_DETACH_MEMORY = 2 };
+enum { RLT_DETACH_CACHE = 1, RLT_DETACH_MEMORY = 2, RLT_BPTT_NO_GRAPHS = 4 };
 typedef struct rlt_grads {
   float *W_g, *b_g, *W_qkv, *W_O, *W_Qx, *W_Ox, *W_1, *W_3, *W_2, *W_o;
   float *dec_attn_norm, *dec_xattn_norm, *dec_ffn_norm, *head_norm, *s_star;
@@ -339,7 +343,7 @@ typedef struct rlt_grads {
 RLT_API int rlt_bptt_workspace_size(const rlt_model* m, int32_t B, int32_t n, size_t* bytes);
 RLT_API int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, int32_t B, int32_t n,
                      const int32_t* actions, float temperature, int32_t top_k, int32_t detach_s_every,
-                     int32_t detach_flags, float* loss, float* logp, const rlt_grads* grads, float* d_e,
+                     int32_t flags, float* loss, float* logp, const rlt_grads* grads, float* d_e,
                      float* d_mem, void* ws, size_t ws_bytes, rlt_stream_t stream);
 
 /* Synchronises the stream, returns the device status recorded in the workspace

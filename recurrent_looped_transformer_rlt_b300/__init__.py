@@ -57,7 +57,7 @@ class rlt_state(ctypes.Structure):
 
 GRAD_FIELDS = ["W_g", "b_g", "W_qkv", "W_O", "W_Qx", "W_Ox", "W_1", "W_3", "W_2", "W_o", "dec_attn_norm",
                "dec_xattn_norm", "dec_ffn_norm", "head_norm", "s_star"]
-RLT_DETACH_CACHE, RLT_DETACH_MEMORY = 1, 2
+RLT_DETACH_CACHE, RLT_DETACH_MEMORY, RLT_BPTT_NO_GRAPHS = 1, 2, 4
 
 
 class rlt_grads(ctypes.Structure):
@@ -291,10 +291,10 @@ def rlt_bptt_workspace_size(model: int, B: int, n: int) -> int:
 
 
 def rlt_bptt(model: int, e, mem, T_mem: int, B: int, n: int, actions, temperature: float, top_k: int,
-             detach_s_every: int, detach_flags: int, loss, logp, grads: rlt_grads, d_e, d_mem, ws, ws_bytes: int,
+             detach_s_every: int, flags: int, loss, logp, grads: rlt_grads, d_e, d_mem, ws, ws_bytes: int,
              stream=None, check: bool = True) -> int:
     rc = _bptt(model, _ptr(e), _ptr(mem), T_mem, B, n, _ptr(actions), temperature, top_k, detach_s_every,
-               detach_flags, _ptr(loss), _ptr(logp), ctypes.byref(grads), _ptr(d_e), _ptr(d_mem), _ptr(ws), ws_bytes,
+               flags, _ptr(loss), _ptr(logp), ctypes.byref(grads), _ptr(d_e), _ptr(d_mem), _ptr(ws), ws_bytes,
                _stream_ptr(stream))
     if check:
         _check(rc, "rlt_bptt")

@@ -13,6 +13,11 @@
 // The query gradient is taken per step; the key/value gradients are summed
 // per key over the queries that read it (swa_bwd_kernel for the window,
 // mem_grad_kernel for the memory).
+//
+// Step kernels read the step's position p from a device cell (*pos) rather
+// than from their arguments, so that a step can be captured once and
+// replayed; split grids are sized for the largest range and chunks past the
+// current one write neutral partials.
 #pragma once
 
 #include "common.cuh"
@@ -66,12 +71,15 @@ __global__ void transpose_kernel(const T* __restrict__ src, int rows, int cols, 
   }
 }
 
-// xg[b] = [e[b][p]; s[b]] in the storage type (and transposed).
+// xg[b] = [e[b][p]; s_p[b]] in the storage type (and transposed).
 template <typename T>
-__global__ void merge_in_kernel(const T* __restrict__ e, int T_mem, int p, const float* __restrict__ s, int B, int d,
-                                T* __restrict__ xg, T* __restrict__ xgT, int ldT) {
+__global__ void merge_in_kernel(const T* __restrict__ e, int T_mem, const int* __restrict__ pos,
+                                const float* __restrict__ s_all, int B, int d, T* __restrict__ xg,
+                                T* __restrict__ xgT, int ldT) {
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)B * 2 * d) return;
+  const int p = *pos;
+  const float* s = s_all + (size_t)p * B * d;
   const int b = (int)(idx / (2 * d)), i = (int)(idx - (size_t)b * 2 * d);
   const T v = (i < d) ? e[((size_t)b * T_mem + p) * d + i] : from_f32<T>(s[(size_t)b * d + i - d]);
   xg[idx] = v;
@@ -81,10 +89,13 @@ __global__ void merge_in_kernel(const T* __restrict__ e, int T_mem, int p, const
 // z = sigmoid(zpre + b_g) (0 without a gate), h = z s + (1 - z) e[b][p].
 template <typename T>
 __global__ void merge_out_kernel(const float* __restrict__ zpre, const float* __restrict__ bg,
-                                 const T* __restrict__ e, int T_mem, int p, const float* __restrict__ s, int B, int d,
-                                 float* __restrict__ z, float* __restrict__ h) {
+                                 const T* __restrict__ e, int T_mem, const int* __restrict__ pos,
+                                 const float* __restrict__ s_all, int B, int d, float* __restrict__ z,
+                                 float* __restrict__ h) {
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)B * d) return;
+  const int p = *pos;
+  const float* s = s_all + (size_t)p * B * d;
   const int b = (int)(idx / d), i = (int)(idx - (size_t)b * d);
   const float zv = zpre ? sigmoid_acc(zpre[idx] + bg[i]) : 0.f;
   const float ev = to_f32(e[((size_t)b * T_mem + p) * d + i]);
@@ -93,12 +104,15 @@ __global__ void merge_out_kernel(const float* __restrict__ zpre, const float* __
 }
 
 // RMSNorm rows: r = 1 / sqrt(mean(x^2) + eps), y = x r g (storage type, and
-// transposed when yT is given).  One warp per row.
+// transposed when yT is given); x is [B][d], or with pos the rows of position
+// *pos + off of [.][B][d].  One warp per row.
 template <typename T>
-__global__ void rms_fwd_kernel(const float* __restrict__ x, const float* __restrict__ g, int B, int d, float eps,
-                               float* __restrict__ r, T* __restrict__ y, T* __restrict__ yT, int ldT) {
+__global__ void rms_fwd_kernel(const float* __restrict__ x, const int* __restrict__ pos, int off,
+                               const float* __restrict__ g, int B, int d, float eps, float* __restrict__ r,
+                               T* __restrict__ y, T* __restrict__ yT, int ldT) {
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (row >= B) return;
+  if (pos) x += (size_t)(*pos + off) * B * d;
   const float* xr = x + (size_t)row * d;
   float ss = 0.f;
   for (int i = lane; i < d; i += 32) ss = fmaf(xr[i], xr[i], ss);
@@ -112,16 +126,18 @@ __global__ void rms_fwd_kernel(const float* __restrict__ x, const float* __restr
   }
 }
 
-// Softmax attention of q [B][d] over positions j0..j1 of K, V [B][H][Tk][hd]:
-// lse [B][H], the output in the storage type to oq [B][d] (and transposed
-// when oT is given).  One warp per (b, h); lane l holds elements l, l + 32,
-// ... of the head.
+// Memory attention of position p = *pos, one warp per (b, h): q [B][d] over
+// positions 0..p of K, V [B][H][Tk][hd]; the output in the storage type to
+// o_step [B][d] and to row p of the record o_rec (+ p * o_stride), the LSE to
+// lse_rec + p * lse_stride.  Lane l holds elements l, l + 32, ... of the head.
 template <typename T>
 __global__ void attn_fwd_kernel(const float* __restrict__ q, const T* __restrict__ K, const T* __restrict__ V, int Tk,
-                                int j0, int j1, int B, int H, int hd, float scale, float* __restrict__ lse,
-                                T* __restrict__ oq, T* __restrict__ oT, int ldT) {
+                                const int* __restrict__ pos, int B, int H, int hd, float scale,
+                                float* __restrict__ lse_rec, size_t lse_stride, T* __restrict__ o_step,
+                                T* __restrict__ o_rec, size_t o_stride) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
+  const int p = *pos;
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd;
   const int NC = (hd + 31) >> 5;  // <= 4
@@ -135,7 +151,7 @@ __global__ void attn_fwd_kernel(const float* __restrict__ q, const T* __restrict
   const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
   const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
   float mx = -INFINITY, l = 0.f;
-  for (int j = j0; j <= j1; ++j) {
+  for (int j = 0; j <= p; ++j) {
     float part = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -153,7 +169,7 @@ __global__ void attn_fwd_kernel(const float* __restrict__ q, const T* __restrict
     }
     mx = mn;
   }
-  if (lane == 0) lse[pair] = mx + logf(l);
+  if (lane == 0) lse_rec[(size_t)p * lse_stride + pair] = mx + logf(l);
   const float inv = 1.0f / l;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -161,24 +177,29 @@ __global__ void attn_fwd_kernel(const float* __restrict__ q, const T* __restrict
     if (c < NC && i < hd) {
       const size_t col = (size_t)h * hd + i;
       const T vq = from_f32<T>(acc[c] * inv);
-      oq[(size_t)b * d + col] = vq;
-      if (oT) oT[col * ldT + b] = vq;
+      o_step[(size_t)b * d + col] = vq;
+      o_rec[(size_t)p * o_stride + (size_t)b * d + col] = vq;
     }
   }
 }
 
-// Window attention forward of position p, one warp per (b, h): q and k of
-// qkv [B][3d] rotated by RoPE at p (q fp32 to qo [B][d]; k and v rounded to
-// the storage type and written to K, V [B][H][Tk][hd] at p), then the
-// attention of q over positions j0..p (position p from registers, the same
-// rounded values): lse [B][H], the output to oq [B][d] (storage type) and
-// its transposed slot oT.
+// Window attention forward of position p = *pos, one warp per (b, h): q and
+// k of qkv [B][3d] rotated by RoPE at p (q fp32 to its record slot p mod W of
+// qR [W][B][d]; k and v rounded to the storage type and written to K, V
+// [B][H][Tk][hd] at p), then the attention of q over positions
+// max(0, p - W + 1)..p (position p from registers, the same rounded values):
+// the LSE to its record slot of lR [W][B][H], the output to oq [B][d]
+// (storage type) and its transposed slot oT.
 template <typename T>
-__global__ void swa_fwd_kernel(const float* __restrict__ qkv, int p, int j0, int B, int H, int hd, float theta,
-                               float scale, float* __restrict__ qo, T* __restrict__ K, T* __restrict__ V, int Tk,
-                               float* __restrict__ lse, T* __restrict__ oq, T* __restrict__ oT, int ldT) {
+__global__ void swa_fwd_kernel(const float* __restrict__ qkv, const int* __restrict__ pos, int W, int B, int H,
+                               int hd, float theta, float scale, float* __restrict__ qR, float* __restrict__ lR,
+                               T* __restrict__ K, T* __restrict__ V, int Tk, T* __restrict__ oq, T* __restrict__ oT,
+                               int ldT) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
+  const int p = *pos, j0 = p - W + 1 > 0 ? p - W + 1 : 0;
+  float* qo = qR + (size_t)(p % W) * B * H * hd;
+  float* lse = lR + (size_t)(p % W) * B * H;
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd, half = hd >> 1;
   const int NC = (hd + 31) >> 5;
@@ -260,15 +281,16 @@ __global__ void swa_fwd_kernel(const float* __restrict__ qkv, int p, int j0, int
 constexpr int kAttnChunk = RLT_BPTT_ATTN_CHUNK;
 template <typename T>
 __global__ void attn_part_fwd_kernel(const float* __restrict__ q, const T* __restrict__ K, const T* __restrict__ V,
-                                     int Tk, int j0, int j1, int B, int H, int hd, float scale, int nsplit,
-                                     float* __restrict__ part) {
+                                     int Tk, const int* __restrict__ pos, int B, int H, int hd, float scale,
+                                     int nsplit, float* __restrict__ part) {
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= B * H * nsplit) return;
+  const int p = *pos;
   const int pair = wid / nsplit, sp = wid - pair * nsplit;
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd;
   const int NC = (hd + 31) >> 5;
-  const int ja = j0 + sp * kAttnChunk, jb = min(j1, ja + kAttnChunk - 1);
+  const int ja = sp * kAttnChunk, jb = min(p, ja + kAttnChunk - 1);  // memory positions 0..p
   float qr[4], acc[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -278,7 +300,7 @@ __global__ void attn_part_fwd_kernel(const float* __restrict__ q, const T* __res
   }
   const T* Kb = K + ((size_t)b * H + h) * Tk * hd;
   const T* Vb = V + ((size_t)b * H + h) * Tk * hd;
-  float mx = -INFINITY, l = 0.f;
+  float mx = -INFINITY, l = 0.f;  // an empty chunk leaves the neutral partial
   for (int j = ja; j <= jb; ++j) {
     float part_s = 0.f;
 #pragma unroll
@@ -309,13 +331,19 @@ __global__ void attn_part_fwd_kernel(const float* __restrict__ q, const T* __res
   }
 }
 
-// Combine of the forward partials, one warp per (b, h): lse, the output in
-// the storage type to oq [B][d] (and to oT when given).
+// Combine of the forward partials, one warp per (b, h), splits in order
+// (neutral partials of empty chunks weigh nothing): the LSE to lse_rec + row *
+// lse_stride with row = p mod ring (ring > 0) or p; the output in the storage
+// type to oq [B][d], to oT when given, and to row p of o_rec (+ p * o_stride)
+// when given.
 template <typename T>
 __global__ void attn_combine_fwd_kernel(const float* __restrict__ part, int nsplit, int B, int H, int hd,
-                                        float* __restrict__ lse, T* __restrict__ oq, T* __restrict__ oT, int ldT) {
+                                        const int* __restrict__ pos, float* __restrict__ lse_rec, size_t lse_stride,
+                                        int ring, T* __restrict__ oq, T* __restrict__ oT, int ldT,
+                                        T* __restrict__ o_rec, size_t o_stride) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
+  const int p = *pos;
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd;
   const int NC = (hd + 31) >> 5;
@@ -333,7 +361,8 @@ __global__ void attn_combine_fwd_kernel(const float* __restrict__ part, int nspl
       if (c < NC && i < hd) acc[c] = fmaf(ps[i], w, acc[c]);
     }
   }
-  if (lane == 0) lse[pair] = M + logf(Lsum);
+  const size_t row = ring > 0 ? (size_t)(p % ring) : (size_t)p;
+  if (lane == 0) lse_rec[row * lse_stride + pair] = M + logf(Lsum);
   const float inv = 1.0f / Lsum;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -343,21 +372,25 @@ __global__ void attn_combine_fwd_kernel(const float* __restrict__ part, int nspl
       const T vq = from_f32<T>(acc[c] * inv);
       oq[(size_t)b * d + col] = vq;
       if (oT) oT[col * ldT + b] = vq;
+      if (o_rec) o_rec[(size_t)p * o_stride + (size_t)b * d + col] = vq;
     }
   }
 }
 
-// Window attention forward of position p split over the keys: warp
+// Window attention forward of position p = *pos split over the keys: warp
 // (pair, s) applies RoPE to q (and the split holding position p also to k,
-// writing k and v at p) and attends over its chunk of positions j0..p;
-// split 0 writes the rotated q to qo.  Partials as attn_part_fwd_kernel (its
-// combine finishes).
+// writing k and v at p) and attends over its chunk of positions
+// max(0, p - W + 1)..p (empty chunks leave neutral partials); split 0 writes
+// the rotated q to its record slot of qR.  Partials as
+// attn_part_fwd_kernel (attn_combine_fwd_kernel finishes, with ring W).
 template <typename T>
-__global__ void swa_part_fwd_kernel(const float* __restrict__ qkv, int p, int j0, int B, int H, int hd, float theta,
-                                    float scale, int nsplit, float* __restrict__ qo, T* __restrict__ K,
-                                    T* __restrict__ V, int Tk, float* __restrict__ part) {
+__global__ void swa_part_fwd_kernel(const float* __restrict__ qkv, const int* __restrict__ pos, int W, int B, int H,
+                                    int hd, float theta, float scale, int nsplit, float* __restrict__ qR,
+                                    T* __restrict__ K, T* __restrict__ V, int Tk, float* __restrict__ part) {
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= B * H * nsplit) return;
+  const int p = *pos, j0 = p - W + 1 > 0 ? p - W + 1 : 0;
+  float* qo = qR + (size_t)(p % W) * B * H * hd;
   const int pair = wid / nsplit, sp = wid - pair * nsplit;
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd, half = hd >> 1;
@@ -428,13 +461,37 @@ __global__ void swa_part_fwd_kernel(const float* __restrict__ qkv, int p, int j0
   }
 }
 
-// yT[j][b] = x[b][j] (rows of a recorded [B][N] operand into a column slot).
+// Row p = *pos of a record x_l [n][L][B][N] (layer offset folded into x_l)
+// to the fixed rows y [B][N] and the column slot yT.
 template <typename T>
-__global__ void tcopy_kernel(const T* __restrict__ x, int B, int N, T* __restrict__ yT, int ldT) {
+__global__ void tcopy_kernel(const T* __restrict__ x_l, int L, const int* __restrict__ pos, int B, int N,
+                             T* __restrict__ y, T* __restrict__ yT, int ldT) {
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)B * N) return;
+  const T* x = x_l + (size_t)(*pos) * L * B * N;
   const int b = (int)(idx / N), j = (int)(idx - (size_t)b * N);
-  yT[(size_t)j * ldT + b] = x[idx];
+  const T v = x[idx];
+  y[idx] = v;
+  yT[(size_t)j * ldT + b] = v;
+}
+
+// dst[(*pos + off) * count + i] = src[i].
+__global__ void put_row_kernel(float* __restrict__ dst, const int* __restrict__ pos, int off,
+                               const float* __restrict__ src, int count) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < count) dst[(size_t)(*pos + off) * count + i] = src[i];
+}
+
+// The position cell: *pos = v, *pos += dv.
+__global__ void set_pos_kernel(int* pos, int v) { *pos = v; }
+__global__ void add_pos_kernel(int* pos, int dv) { *pos += dv; }
+
+// ds = 0 when s_p was detached after its step (p >= 1, p % s_every == 0).
+__global__ void zero_if_detached_kernel(float* __restrict__ ds, const int* __restrict__ pos, int s_every, int count) {
+  const int p = *pos;
+  if (p < 1 || p % s_every != 0) return;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < count) ds[i] = 0.f;
 }
 
 // m = silu(g) u in the storage type (and transposed).
@@ -458,14 +515,15 @@ __device__ __forceinline__ unsigned fkey(float x) {
 
 // Head of one step, one block of kThreadsHead per sequence b: x = logits /
 // temperature; S = all ids, or the top-k set (the k largest x, ties to the
-// lower id); lp = x_a - log sum_{v in S} exp(x_v) to lp[b][n_ld * .. + p]
+// lower id); lp = x_a - log sum_{v in S} exp(x_v) to lp[b][p] (p = *pos)
 // (NaN for a < 0, -inf for a outside S); d(-lp)/d logits_v =
 // inv_temp (p_v [v in S] - [v = a]) to dl [B][V] (and transposed), 0 for
 // a < 0.  Shared memory: V floats.
 constexpr int kThreadsHead = 1024;
 __global__ void __launch_bounds__(kThreadsHead) head_bwd_kernel(const float* __restrict__ logits, int B, int V,
-                                                                 const int32_t* __restrict__ actions, int n, int p,
-                                                                 float inv_temp, int top_k, float* __restrict__ lp,
+                                                                 const int32_t* __restrict__ actions, int n,
+                                                                 const int* __restrict__ pos, float inv_temp,
+                                                                 int top_k, float* __restrict__ lp,
                                                                  void* dl_, void* dlT_, int ldT, int bf16_out,
                                                                  int* status) {
   extern __shared__ float sx[];
@@ -475,6 +533,7 @@ __global__ void __launch_bounds__(kThreadsHead) head_bwd_kernel(const float* __r
   __shared__ unsigned s_prefix, s_remain;
   const int b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int nw = nthr >> 5;
+  const int p = *pos;
   const float* lg = logits + (size_t)b * V;
   float mx = -INFINITY;
   for (int v = tid; v < V; v += nthr) {
@@ -599,12 +658,15 @@ __global__ void __launch_bounds__(kThreadsHead) head_bwd_kernel(const float* __r
 //   dg_i += sum_b dy_i x_i r                                 (columns: thread per column)
 // With out given, the updated dx rows are also written in the storage type
 // to out [B][d] and transposed to outT (the next projection's operands).
+// x is [B][d], or with pos the rows of position *pos + off of [.][B][d].
 // Blocks [0, row_blocks) do the rows, the rest the columns.
 template <typename T>
-__global__ void rms_bwd_kernel(const float* __restrict__ x, const float* __restrict__ r, const float* __restrict__ g,
+__global__ void rms_bwd_kernel(const float* __restrict__ x, const int* __restrict__ pos, int off,
+                               const float* __restrict__ r, const float* __restrict__ g,
                                const float* __restrict__ dy, int B, int d, float* __restrict__ dx,
                                float* __restrict__ dg, int row_blocks, T* __restrict__ out, T* __restrict__ outT,
                                int ldT) {
+  if (pos) x += (size_t)(*pos + off) * B * d;
   if ((int)blockIdx.x < row_blocks) {
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (row >= B) return;
@@ -669,32 +731,37 @@ struct EpiSwigluBwd {
   }
 };
 
-// d[e; s] = acc at (b, n): n < d adds to the e gradient of position p,
+// d[e; s] = acc at (b, n): n < d adds to the e gradient of position *pos,
 // the rest to ds [B][d].
 struct EpiMergeBwd {
   float* de;  // [B][T_mem][d] or null
   float* ds;
-  int d, T_mem, p;
+  int d, T_mem;
+  const int* pos;
   __device__ __forceinline__ void operator()(int m, int n, float v) const {
     if (n < d) {
-      if (de) de[((size_t)m * T_mem + p) * d + n] += v;
+      if (de) de[((size_t)m * T_mem + *pos) * d + n] += v;
     } else {
       ds[(size_t)m * d + n - d] += v;
     }
   }
 };
 
-// Query gradient of the attention over positions j0..j1 (see the header),
-// with D = g.o from the stored output o (storage type), written as the next
-// projection's operands: dqY [B][d] in the storage type and transposed to
-// dqT; D to Dout [B][H] when given.  One warp per (b, h).
+// Query gradient of the memory attention of position p = *pos (positions
+// 0..p, see the header; LSE from lse_rec + p * lse_stride), with D = g.o from
+// the stored output o (storage type), written as the next projection's
+// operands: dqY [B][d] in the storage type and transposed to dqT; D to Dout
+// [B][H] when given.  One warp per (b, h).
 template <typename T>
 __global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __restrict__ gout, const T* __restrict__ o,
-                                const float* __restrict__ lse, const T* __restrict__ K, const T* __restrict__ V,
-                                int Tk, int j0, int j1, int B, int H, int hd, float scale, float* __restrict__ Dout,
-                                T* __restrict__ dqY, T* __restrict__ dqT, int ldT) {
+                                const float* __restrict__ lse_rec, size_t lse_stride, const T* __restrict__ K,
+                                const T* __restrict__ V, int Tk, const int* __restrict__ pos, int B, int H, int hd,
+                                float scale, float* __restrict__ Dout, T* __restrict__ dqY, T* __restrict__ dqT,
+                                int ldT) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
+  const int j0 = 0, j1 = *pos;
+  const float* lse = lse_rec + (size_t)j1 * lse_stride;
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd;
   const int NC = (hd + 31) >> 5;
@@ -744,15 +811,19 @@ __global__ void attn_bwd_kernel(const float* __restrict__ q, const float* __rest
   }
 }
 
-// Query-gradient partials over the key split (see attn_part_fwd_kernel):
-// warp (pair, s) writes sum_{j in its chunk} dS_j K_j (unscaled) and D = g.o.
+// Query-gradient partials over the key split of memory positions 0..*pos
+// (see attn_part_fwd_kernel): warp (pair, s) writes sum_{j in its chunk}
+// dS_j K_j (unscaled; zero for an empty chunk) and D = g.o.
 template <typename T>
 __global__ void attn_part_bwd_kernel(const float* __restrict__ q, const float* __restrict__ gout,
-                                     const T* __restrict__ o, const float* __restrict__ lse, const T* __restrict__ K,
-                                     const T* __restrict__ V, int Tk, int j0, int j1, int B, int H, int hd,
-                                     float scale, int nsplit, float* __restrict__ part) {
+                                     const T* __restrict__ o, const float* __restrict__ lse_rec, size_t lse_stride,
+                                     const T* __restrict__ K, const T* __restrict__ V, int Tk,
+                                     const int* __restrict__ pos, int B, int H, int hd, float scale, int nsplit,
+                                     float* __restrict__ part) {
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= B * H * nsplit) return;
+  const int j0 = 0, j1 = *pos;
+  const float* lse = lse_rec + (size_t)j1 * lse_stride;
   const int pair = wid / nsplit, sp = wid - pair * nsplit;
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd;
@@ -833,20 +904,25 @@ __global__ void attn_combine_bwd_kernel(const float* __restrict__ part, int nspl
   }
 }
 
-// Window attention backward of position p split over warps (pair, s): the
-// query-gradient partial over key chunk s of positions j0..p and the
-// key/value-gradient partial of position p over record chunk s of positions
-// p..p_last (either may be empty); D = g.o from this step's record and the
-// stored output.  Partials part[(pair * nsplit + s) * (3 hd + 1)]: dq (unscaled),
-// dK, dV, then D.  swa_combine_bwd_kernel finishes.
+// Window attention backward of position p = *pos split over warps (pair,
+// s): the query-gradient partial over key chunk s of positions
+// max(0, p - W + 1)..p and the key/value-gradient partial of position p over
+// record chunk s of positions p..p_last (p_last = p with the cache detached,
+// else min(p + W - 1, Tk - 1); either chunk may be empty); this step's output
+// gradient g (split 0 stores it in its record slot of gR), D = g.o with the
+// stored output.  Partials part[(pair * nsplit + s) * (3 hd + 1)]: dq
+// (unscaled), dK, dV, then D.  swa_combine_bwd_kernel finishes.
 template <typename T>
-__global__ void swa_part_bwd_kernel(const T* __restrict__ K, const T* __restrict__ V, int Tk, int j0, int p,
-                                    int p_last, const T* __restrict__ o, const float* __restrict__ qR,
-                                    const float* __restrict__ gR, const float* __restrict__ lR,
-                                    const float* __restrict__ DR, int W, int B, int H, int hd, float scale, int nsplit,
+__global__ void swa_part_bwd_kernel(const T* __restrict__ K, const T* __restrict__ V, int Tk,
+                                    const int* __restrict__ pos, int W, int cache, const T* __restrict__ o,
+                                    const float* __restrict__ g, const float* __restrict__ qR,
+                                    float* __restrict__ gR, const float* __restrict__ lR,
+                                    const float* __restrict__ DR, int B, int H, int hd, float scale, int nsplit,
                                     float* __restrict__ part) {
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= B * H * nsplit) return;
+  const int p = *pos, j0 = p - W + 1 > 0 ? p - W + 1 : 0;
+  const int p_last = cache ? p : min(p + W - 1, Tk - 1);
   const int pair = wid / nsplit, sp = wid - pair * nsplit;
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd;
@@ -860,11 +936,12 @@ __global__ void swa_part_bwd_kernel(const T* __restrict__ K, const T* __restrict
     const int i = lane + 32 * c;
     const bool ok = c < NC && i < hd;
     qr[c] = ok ? qR[r0 * d + h * hd + i] : 0.f;
-    gr[c] = ok ? gR[r0 * d + h * hd + i] : 0.f;
+    gr[c] = ok ? g[(size_t)b * d + h * hd + i] : 0.f;
     kp[c] = ok ? to_f32(K[kpo + i]) : 0.f;
     vp[c] = ok ? to_f32(V[kpo + i]) : 0.f;
     dq[c] = dk[c] = dv[c] = 0.f;
     if (ok) Dp = fmaf(gr[c], to_f32(o[(size_t)b * d + h * hd + i]), Dp);
+    if (ok && sp == 0) gR[r0 * d + h * hd + i] = gr[c];  // this step's record
   }
   const float D = warp_sum(Dp);
   const float ls = lR[r0 * H + h];
@@ -928,11 +1005,12 @@ __global__ void swa_part_bwd_kernel(const T* __restrict__ K, const T* __restrict
 // order, D to this step's record, then dq (scaled) and dK back through RoPE at
 // p and dV as is into d qkv dY [B][3d] and its transposed slot dYT.
 template <typename T>
-__global__ void swa_combine_bwd_kernel(const float* __restrict__ part, int nsplit, int p, int W, int B, int H, int hd,
-                                       float scale, float theta, float* __restrict__ DR, T* __restrict__ dY,
-                                       T* __restrict__ dYT, int ldT) {
+__global__ void swa_combine_bwd_kernel(const float* __restrict__ part, int nsplit, const int* __restrict__ pos, int W,
+                                       int B, int H, int hd, float scale, float theta, float* __restrict__ DR,
+                                       T* __restrict__ dY, T* __restrict__ dYT, int ldT) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
+  const int p = *pos;
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd, half = hd >> 1;
   const int NC = (hd + 31) >> 5;
@@ -980,22 +1058,27 @@ __global__ void swa_combine_bwd_kernel(const float* __restrict__ part, int nspli
   }
 }
 
-// Window attention backward of position p (one layer), one warp per (b, h):
-// from this step's record (ring slot p mod W: query q, output gradient g,
-// lse) and the stored output o, D = g.o (written to the record), the query
-// gradient over positions j0..p; the key/value gradient of position p from
-// the records of positions p..p_last (this step's from registers):
+// Window attention backward of position p = *pos (one layer), one warp per
+// (b, h): this step's output gradient g (stored to its record slot p mod W of
+// gR), its record's query and LSE, and the stored output o give D = g.o
+// (written to the record) and the query gradient over positions
+// max(0, p - W + 1)..p; the key/value gradient of position p comes from the
+// records of positions p..p_last (p_last = p with the cache detached, else
+// min(p + W - 1, Tk - 1); this step's from registers):
 //   dK = sum scale dS q,  dV = sum P g,  P = exp(scale q.K_p - lse),
 //   dS = P (g.V_p - D);
 // then dq and dK back through RoPE at p and dV as is, into d qkv
 // dY [B][3d] (storage type) and its transposed slot dYT.
 template <typename T>
-__global__ void swa_bwd_kernel(const T* __restrict__ K, const T* __restrict__ V, int Tk, int j0, int p, int p_last,
-                               const T* __restrict__ o, const float* __restrict__ qR, const float* __restrict__ gR,
-                               const float* __restrict__ lR, float* __restrict__ DR, int W, int B, int H, int hd,
-                               float scale, float theta, T* __restrict__ dY, T* __restrict__ dYT, int ldT) {
+__global__ void swa_bwd_kernel(const T* __restrict__ K, const T* __restrict__ V, int Tk, const int* __restrict__ pos,
+                               int W, int cache, const T* __restrict__ o, const float* __restrict__ g,
+                               const float* __restrict__ qR, float* __restrict__ gR, const float* __restrict__ lR,
+                               float* __restrict__ DR, int B, int H, int hd, float scale, float theta,
+                               T* __restrict__ dY, T* __restrict__ dYT, int ldT) {
   const int pair = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (pair >= B * H) return;
+  const int p = *pos, j0 = p - W + 1 > 0 ? p - W + 1 : 0;
+  const int p_last = cache ? p : min(p + W - 1, Tk - 1);
   const int b = pair / H, h = pair - b * H;
   const int d = H * hd, half = hd >> 1;
   const int NC = (hd + 31) >> 5;
@@ -1008,11 +1091,12 @@ __global__ void swa_bwd_kernel(const T* __restrict__ K, const T* __restrict__ V,
     const int i = lane + 32 * c;
     const bool ok = c < NC && i < hd;
     qr[c] = ok ? qR[r0 * d + h * hd + i] : 0.f;
-    gr[c] = ok ? gR[r0 * d + h * hd + i] : 0.f;
+    gr[c] = ok ? g[(size_t)b * d + h * hd + i] : 0.f;
     kp[c] = ok ? to_f32(K[kpo + i]) : 0.f;
     vp[c] = ok ? to_f32(V[kpo + i]) : 0.f;
     dq[c] = dk[c] = dv[c] = 0.f;
     if (ok) Dp = fmaf(gr[c], to_f32(o[(size_t)b * d + h * hd + i]), Dp);
+    if (ok) gR[r0 * d + h * hd + i] = gr[c];  // this step's record
   }
   const float D = warp_sum(Dp);
   const float ls = lR[r0 * H + h];
@@ -1205,11 +1289,13 @@ __global__ void __launch_bounds__(kMemWarps * 32) mem_grad_kernel(
 //         db_g[i] += sum_b dzpre.
 template <typename T>
 __global__ void merge_bwd_kernel(const float* __restrict__ dh, const float* __restrict__ z, const T* __restrict__ e,
-                                 int T_mem, int p, const float* __restrict__ s, int B, int d, int gate,
-                                 T* __restrict__ dY, T* __restrict__ dYT, int ldT, float* __restrict__ dbg,
-                                 float* __restrict__ de, float* __restrict__ ds) {
+                                 int T_mem, const int* __restrict__ pos, const float* __restrict__ s_all, int B,
+                                 int d, int gate, T* __restrict__ dY, T* __restrict__ dYT, int ldT,
+                                 float* __restrict__ dbg, float* __restrict__ de, float* __restrict__ ds) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= d) return;
+  const int p = *pos;
+  const float* s = s_all + (size_t)p * B * d;
   float acc = 0.f;
   for (int b = 0; b < B; ++b) {
     const size_t o = (size_t)b * d + i;

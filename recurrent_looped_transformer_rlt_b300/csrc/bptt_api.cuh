@@ -13,15 +13,68 @@ template <typename T_>
 struct BpttOps {
   using T = T_;
   static constexpr bool kBf16 = std::is_same<T_, bf16>::value;
-  cudaStream_t st;
+  cudaStream_t st;   // the stream launches go to (the capture stream while capturing)
+  cudaStream_t user; // the caller's stream (graphs are replayed on it)
+  cudaStream_t cap;  // the model's capture stream
+  bool graphs = true;
   TcScratch sc;
   int* status;
+  // one captured step per key: -1 the recording step, s >= 0 the reverse
+  // step of block slot s
+  struct Step {
+    int key;
+    cudaGraphExec_t exec;
+    uint64_t launches;
+  };
+  std::vector<Step> steps;
 
+  ~BpttOps() {
+    for (auto& x : steps) cudaGraphExecDestroy(x.exec);
+  }
   int post() {
     g_launches++;
     return launch_ok();
   }
   static unsigned blocks(size_t work, int per_block = bptt::kThreads) { return cdiv(work, per_block); }
+  static int splits(int range) { return (range + bptt::kAttnChunk - 1) / bptt::kAttnChunk; }
+
+  // Runs fn's launches as one step: captured on the first call of a key into
+  // a graph, replayed on the caller's stream from then on (the launches read
+  // the step's position from the device cell, so every replay is the step at
+  // the cell's current position).
+  template <class Fn>
+  int step(int key, Fn fn) {
+    if (!graphs) return fn();
+    for (auto& x : steps)
+      if (x.key == key) {
+        if (cudaGraphLaunch(x.exec, user) != cudaSuccess) return RLT_ECUDA;
+        g_launches += x.launches;
+        return RLT_OK;
+      }
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    // the capture stream starts after the caller's stream's earlier work
+    RLT_CUDA_TRY(cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal));
+    const uint64_t before = g_launches.load();
+    st = cap;
+    int rc = fn();
+    st = user;
+    const uint64_t nk = g_launches.load() - before;
+    g_launches.store(before);
+    const cudaError_t ce = cudaStreamEndCapture(cap, &graph);
+    if (rc) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    if (ce != cudaSuccess) return RLT_ECUDA;
+    const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) return RLT_ECUDA;
+    steps.push_back({key, exec, nk});
+    if (cudaGraphLaunch(exec, user) != cudaSuccess) return RLT_ECUDA;
+    g_launches += nk;
+    return RLT_OK;
+  }
 
   int zero(void* p, size_t bytes) {
     if (!bytes) return RLT_OK;
@@ -31,164 +84,180 @@ struct BpttOps {
     if (!bytes) return RLT_OK;
     return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st) == cudaSuccess ? RLT_OK : RLT_ECUDA;
   }
+  int set_pos(int* pos, int v) {
+    bptt::set_pos_kernel<<<1, 1, 0, st>>>(pos, v);
+    return post();
+  }
+  int add_pos(int* pos, int dv) {
+    bptt::add_pos_kernel<<<1, 1, 0, st>>>(pos, dv);
+    return post();
+  }
+  int put_row(float* dst, const int* pos, int off, const float* src, int count) {
+    bptt::put_row_kernel<<<blocks((size_t)count), bptt::kThreads, 0, st>>>(dst, pos, off, src, count);
+    return post();
+  }
+  int zero_if_detached(float* ds, const int* pos, int s_every, int count) {
+    bptt::zero_if_detached_kernel<<<blocks((size_t)count), bptt::kThreads, 0, st>>>(ds, pos, s_every, count);
+    return post();
+  }
   int transpose(const T* src, int rows, int cols, int lds, T* dst, int ldd) {
     bptt::transpose_kernel<T><<<dim3(cdiv(cols, 32), cdiv(rows, 32)), dim3(32, 8), 0, st>>>(src, rows, cols, lds,
                                                                                            dst, ldd);
     return post();
   }
   // C[M][N] (+)= A[M][K] W[N][K]^T
-  int gemm(const T* A, int lda, int M, int K, const T* W, int ldw, int N, float* C, int ldc, bool add) {
-    if constexpr (kBf16) {
-      AArg a;
-      a.A = A;
-      a.lda = lda;
-      if (add) return proj_bf16<false>(st, a, M, K, W, nullptr, ldw, N, EpiAddF32{C, ldc}, sc);
-      return proj_bf16<false>(st, a, M, K, W, nullptr, ldw, N, EpiStoreF32{C, ldc}, sc);
-    } else {
-      if (add) return ::gemm<float>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, EpiAddF32{C, ldc});
-      return ::gemm<float>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, EpiStoreF32{C, ldc});
-    }
+  int gemm(const T* A, int lda, int M, int K, const T* W_, int ldw, int N, float* C, int ldc, bool add) {
+    if (add) return gemm_epi(A, lda, M, K, W_, ldw, N, EpiAddF32{C, ldc});
+    return gemm_epi(A, lda, M, K, W_, ldw, N, EpiStoreF32{C, ldc});
   }
   // A[M][K] W[N][K]^T through the epilogue functor
   template <class Epi>
-  int gemm_epi(const T* A, int lda, int M, int K, const T* W, int ldw, int N, Epi epi) {
+  int gemm_epi(const T* A, int lda, int M, int K, const T* W_, int ldw, int N, Epi epi) {
     if constexpr (kBf16) {
       AArg a;
       a.A = A;
       a.lda = lda;
-      return proj_bf16<false>(st, a, M, K, W, nullptr, ldw, N, epi, sc);
+      return proj_bf16<false>(st, a, M, K, W_, nullptr, ldw, N, epi, sc);
     } else {
-      return ::gemm<float>(st, A, lda, GemmB{W, W, N, ldw}, M, N, K, epi);
+      return ::gemm<float>(st, A, lda, GemmB{W_, W_, N, ldw}, M, N, K, epi);
     }
   }
   // C[M][N] = R[M][N] + A[M][K] W[N][K]^T
-  int gemm_res(const T* A, int lda, int M, int K, const T* W, int ldw, int N, const float* R, float* C, int ldc) {
-    return gemm_epi(A, lda, M, K, W, ldw, N, bptt::EpiResidualInto{R, C, ldc});
+  int gemm_res(const T* A, int lda, int M, int K, const T* W_, int ldw, int N, const float* R, float* C, int ldc) {
+    return gemm_epi(A, lda, M, K, W_, ldw, N, bptt::EpiResidualInto{R, C, ldc});
   }
   // dm = A W^T, SwiGLU backward in the epilogue into dY [M][2f] and dYT
-  int gemm_swiglu_bwd(const T* A, int lda, int M, int K, const T* W, int ldw, int f, const float* g, const float* u,
+  int gemm_swiglu_bwd(const T* A, int lda, int M, int K, const T* W_, int ldw, int f, const float* g, const float* u,
                       T* dY, T* dYT, int ldT) {
-    return gemm_epi(A, lda, M, K, W, ldw, f, bptt::EpiSwigluBwd<T>{g, u, f, dY, dYT, ldT});
+    return gemm_epi(A, lda, M, K, W_, ldw, f, bptt::EpiSwigluBwd<T>{g, u, f, dY, dYT, ldT});
   }
   // d[e; s] = dzpre W_g (A = dzpre, W = the transposed copy of W_g), added to
-  // the e gradient of position p and to ds
-  int gemm_merge_bwd(const T* A, int lda, int M, int K, const T* W, int ldw, int d, int T_mem, int p, float* de,
-                     float* ds) {
-    return gemm_epi(A, lda, M, K, W, ldw, 2 * d, bptt::EpiMergeBwd{de, ds, d, T_mem, p});
+  // the e gradient of position *pos and to ds
+  int gemm_merge_bwd(const T* A, int lda, int M, int K, const T* W_, int ldw, int d, int T_mem, const int* pos,
+                     float* de, float* ds) {
+    return gemm_epi(A, lda, M, K, W_, ldw, 2 * d, bptt::EpiMergeBwd{de, ds, d, T_mem, pos});
   }
   int bcast_rows(float* dst, const float* src, int rows, int d) {
     bcast_rows_kernel<<<blocks((size_t)rows * d), bptt::kThreads, 0, st>>>(dst, src, rows, d);
     return post();
   }
-  int merge_in(const T* e, int T_mem, int p, const float* s, int B, int d, T* xg, T* xgT, int ldT) {
-    bptt::merge_in_kernel<T><<<blocks((size_t)B * 2 * d), bptt::kThreads, 0, st>>>(e, T_mem, p, s, B, d, xg, xgT, ldT);
+  int merge_in(const T* e, int T_mem, const int* pos, const float* s_all, int B, int d, T* xg, T* xgT, int ldT) {
+    bptt::merge_in_kernel<T><<<blocks((size_t)B * 2 * d), bptt::kThreads, 0, st>>>(e, T_mem, pos, s_all, B, d, xg,
+                                                                                  xgT, ldT);
     return post();
   }
-  int merge_out(const float* zpre, const float* bg, const T* e, int T_mem, int p, const float* s, int B, int d,
-                float* z, float* h) {
-    bptt::merge_out_kernel<T><<<blocks((size_t)B * d), bptt::kThreads, 0, st>>>(zpre, bg, e, T_mem, p, s, B, d, z, h);
+  int merge_out(const float* zpre, const float* bg, const T* e, int T_mem, const int* pos, const float* s_all, int B,
+                int d, float* z, float* h) {
+    bptt::merge_out_kernel<T><<<blocks((size_t)B * d), bptt::kThreads, 0, st>>>(zpre, bg, e, T_mem, pos, s_all, B, d,
+                                                                              z, h);
     return post();
   }
-  int rms_fwd(const float* x, const float* g, int B, int d, float eps, float* r, T* y, T* yT, int ldT) {
-    bptt::rms_fwd_kernel<T><<<blocks((size_t)B * 32), bptt::kThreads, 0, st>>>(x, g, B, d, eps, r, y, yT, ldT);
+  int rms_fwd(const float* x, const int* pos, int off, const float* g, int B, int d, float eps, float* r, T* y, T* yT,
+              int ldT) {
+    bptt::rms_fwd_kernel<T><<<blocks((size_t)B * 32), bptt::kThreads, 0, st>>>(x, pos, off, g, B, d, eps, r, y, yT,
+                                                                              ldT);
     return post();
   }
   // window attention forward: one warp per (b, h) for windows of one chunk,
-  // else split over the keys and combined (part: scratch of the partials)
-  int swa_fwd(const float* qkv, int p, int j0, int B, int H, int hd, float theta, float scale, float* qo, T* K, T* V,
-              int Tk, float* lse, T* oq, T* oT, int ldT, float* part) {
-    const int nsplit = (p - j0 + bptt::kAttnChunk) / bptt::kAttnChunk;
+  // else split over the keys (grid sized for the full window) and combined
+  int swa_fwd(const float* qkv, const int* pos, int Wn, int B, int H, int hd, float theta, float scale, float* qR,
+              float* lR, T* K, T* V, int Tk, T* oq, T* oT, int ldT, float* part) {
+    const int nsplit = splits(Wn);
     const size_t pairs = (size_t)B * H;
     if (nsplit <= 1) {
-      bptt::swa_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(qkv, p, j0, B, H, hd, theta, scale, qo, K, V,
-                                                                       Tk, lse, oq, oT, ldT);
+      bptt::swa_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(qkv, pos, Wn, B, H, hd, theta, scale, qR, lR,
+                                                                       K, V, Tk, oq, oT, ldT);
       return post();
     }
-    bptt::swa_part_fwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(qkv, p, j0, B, H, hd, theta,
-                                                                                   scale, nsplit, qo, K, V, Tk, part);
+    bptt::swa_part_fwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(qkv, pos, Wn, B, H, hd, theta,
+                                                                                   scale, nsplit, qR, K, V, Tk, part);
     int rc = post();
     if (rc) return rc;
-    bptt::attn_combine_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(part, nsplit, B, H, hd, lse, oq, oT,
-                                                                             ldT);
+    bptt::attn_combine_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(
+        part, nsplit, B, H, hd, pos, lR, pairs, Wn, oq, oT, ldT, static_cast<T*>(nullptr), 0);
     return post();
   }
-  // attention over positions j0..j1: one warp per (b, h) for short ranges,
-  // else split over the keys (part: scratch of the partials) and combined
-  int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
-               float* lse, T* oq, T* oT, int ldT, float* part) {
-    const int nsplit = (j1 - j0 + bptt::kAttnChunk) / bptt::kAttnChunk;
-    const size_t pairs = (size_t)B * H;
+  // memory attention of the position in the cell over positions 0..p: one
+  // warp per (b, h) when the call's steps fit one chunk, else split over the
+  // keys (grid sized for the call's last position) and combined
+  int attn_fwd(const float* q, const T* K, const T* V, int Tk, const int* pos, int n, int B, int H, int hd,
+               float scale, float* lse_l, T* o_l, int L, T* o_step, float* part) {
+    const int nsplit = splits(n);
+    const size_t pairs = (size_t)B * H, d = (size_t)H * hd;
     if (nsplit <= 1) {
-      bptt::attn_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(q, K, V, Tk, j0, j1, B, H, hd, scale, lse,
-                                                                        oq, oT, ldT);
+      bptt::attn_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(q, K, V, Tk, pos, B, H, hd, scale, lse_l,
+                                                                        (size_t)L * pairs, o_step, o_l,
+                                                                        (size_t)L * B * d);
       return post();
     }
-    bptt::attn_part_fwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(q, K, V, Tk, j0, j1, B, H, hd,
+    bptt::attn_part_fwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(q, K, V, Tk, pos, B, H, hd,
                                                                                     scale, nsplit, part);
     int rc = post();
     if (rc) return rc;
-    bptt::attn_combine_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(part, nsplit, B, H, hd, lse, oq, oT,
-                                                                             ldT);
+    bptt::attn_combine_fwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(
+        part, nsplit, B, H, hd, pos, lse_l, (size_t)L * pairs, 0, o_step, static_cast<T*>(nullptr), 0, o_l,
+        (size_t)L * B * d);
     return post();
   }
-  int tcopy(const T* x, int B, int N, T* yT, int ldT) {
-    bptt::tcopy_kernel<T><<<blocks((size_t)B * N), bptt::kThreads, 0, st>>>(x, B, N, yT, ldT);
+  int tcopy(const T* x_l, int L, const int* pos, int B, int N, T* y, T* yT, int ldT) {
+    bptt::tcopy_kernel<T><<<blocks((size_t)B * N), bptt::kThreads, 0, st>>>(x_l, L, pos, B, N, y, yT, ldT);
     return post();
   }
   int swiglu_fwd(const float* g, const float* u, int B, int f, T* m, T* mT, int ldT) {
     bptt::swiglu_fwd_kernel<T><<<blocks((size_t)B * f), bptt::kThreads, 0, st>>>(g, u, B, f, m, mT, ldT);
     return post();
   }
-  int head_bwd(const float* logits, int B, int V, const int32_t* actions, int n, int p, float inv_temp, int top_k,
-               float* lp, T* dl, T* dlT, int ldT) {
+  int head_bwd(const float* logits, int B, int V, const int32_t* actions, int n, const int* pos, float inv_temp,
+               int top_k, float* lp, T* dl, T* dlT, int ldT) {
     bptt::head_bwd_kernel<<<B, bptt::kThreadsHead, sizeof(float) * (size_t)V, st>>>(
-        logits, B, V, actions, n, p, inv_temp, top_k, lp, dl, dlT, ldT, kBf16 ? 1 : 0, status);
+        logits, B, V, actions, n, pos, inv_temp, top_k, lp, dl, dlT, ldT, kBf16 ? 1 : 0, status);
     return post();
   }
-  int rms_bwd(const float* x, const float* r, const float* g, const float* dy, int B, int d, float* dx, float* dg,
-              T* out, T* outT, int ldT) {
+  int rms_bwd(const float* x, const int* pos, int off, const float* r, const float* g, const float* dy, int B, int d,
+              float* dx, float* dg, T* out, T* outT, int ldT) {
     const int row_blocks = (int)blocks((size_t)B * 32);
     const int col_blocks = (int)blocks((size_t)d);
-    bptt::rms_bwd_kernel<T><<<row_blocks + col_blocks, bptt::kThreads, 0, st>>>(x, r, g, dy, B, d, dx, dg,
+    bptt::rms_bwd_kernel<T><<<row_blocks + col_blocks, bptt::kThreads, 0, st>>>(x, pos, off, r, g, dy, B, d, dx, dg,
                                                                                row_blocks, out, outT, ldT);
     return post();
   }
-  int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* Dout, T* dqY, T* dqT, int ldT, float* part) {
-    const int nsplit = (j1 - j0 + bptt::kAttnChunk) / bptt::kAttnChunk;
+  int attn_bwd(const float* q, const float* gout, const T* o, const float* lse_l, int L, const T* K, const T* V,
+               int Tk, const int* pos, int n, int B, int H, int hd, float scale, float* Dout, T* dqY, T* dqT, int ldT,
+               float* part) {
+    const int nsplit = splits(n);
     const size_t pairs = (size_t)B * H;
     if (nsplit <= 1) {
-      bptt::attn_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd,
-                                                                        scale, Dout, dqY, dqT, ldT);
+      bptt::attn_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(q, gout, o, lse_l, (size_t)L * pairs, K, V,
+                                                                        Tk, pos, B, H, hd, scale, Dout, dqY, dqT,
+                                                                        ldT);
       return post();
     }
     bptt::attn_part_bwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(
-        q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd, scale, nsplit, part);
+        q, gout, o, lse_l, (size_t)L * pairs, K, V, Tk, pos, B, H, hd, scale, nsplit, part);
     int rc = post();
     if (rc) return rc;
     bptt::attn_combine_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(part, nsplit, B, H, hd, scale, Dout,
                                                                              dqY, dqT, ldT);
     return post();
   }
-  // window attention backward: one warp per (b, h) when the window and the
-  // records fit one chunk each, else split and combined
-  int swa_bwd(const T* K, const T* V, int Tk, int j0, int p, int p_last, const T* o, const float* qR,
-              const float* gR, float* lR, float* DR, int W, int B, int H, int hd, float scale, float theta, T* dY,
+  // window attention backward: one warp per (b, h) when the window fits one
+  // chunk, else split over key and record chunks (grid sized for the full
+  // window) and combined
+  int swa_bwd(const T* K, const T* V, int Tk, const int* pos, int Wn, bool cache, const T* o, const float* g,
+              float* qR, float* gR, float* lR, float* DR, int B, int H, int hd, float scale, float theta, T* dY,
               T* dYT, int ldT, float* part) {
-    const int nk = (p - j0 + bptt::kAttnChunk) / bptt::kAttnChunk;
-    const int nr = (p_last - p + bptt::kAttnChunk) / bptt::kAttnChunk;
-    const int nsplit = nk > nr ? nk : nr;
+    const int nsplit = splits(Wn);
     const size_t pairs = (size_t)B * H;
     if (nsplit <= 1) {
       bptt::swa_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(
-          K, V, Tk, j0, p, p_last, o, qR, gR, lR, DR, W, B, H, hd, scale, theta, dY, dYT, ldT);
+          K, V, Tk, pos, Wn, cache ? 1 : 0, o, g, qR, gR, lR, DR, B, H, hd, scale, theta, dY, dYT, ldT);
       return post();
     }
     bptt::swa_part_bwd_kernel<T><<<blocks(pairs * nsplit * 32, 128), 128, 0, st>>>(
-        K, V, Tk, j0, p, p_last, o, qR, gR, lR, DR, W, B, H, hd, scale, nsplit, part);
+        K, V, Tk, pos, Wn, cache ? 1 : 0, o, g, qR, gR, lR, DR, B, H, hd, scale, nsplit, part);
     int rc = post();
     if (rc) return rc;
-    bptt::swa_combine_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(part, nsplit, p, W, B, H, hd, scale,
+    bptt::swa_combine_bwd_kernel<T><<<blocks(pairs * 32, 128), 128, 0, st>>>(part, nsplit, pos, Wn, B, H, hd, scale,
                                                                             theta, DR, dY, dYT, ldT);
     return post();
   }
@@ -200,10 +269,10 @@ struct BpttOps {
                                                                     p_hi, B, H, hd, scale, dK, dV);
     return post();
   }
-  int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, int p, const float* s, int B, int d,
-                bool gate, T* dY, T* dYT, int ldT, float* dbg, float* de, float* ds) {
-    bptt::merge_bwd_kernel<T><<<blocks((size_t)d), bptt::kThreads, 0, st>>>(dh, z, e, T_mem, p, s, B, d, gate ? 1 : 0,
-                                                                            dY, dYT, ldT, dbg, de, ds);
+  int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, const int* pos, const float* s_all, int B,
+                int d, bool gate, T* dY, T* dYT, int ldT, float* dbg, float* de, float* ds) {
+    bptt::merge_bwd_kernel<T><<<blocks((size_t)d), bptt::kThreads, 0, st>>>(dh, z, e, T_mem, pos, s_all, B, d,
+                                                                            gate ? 1 : 0, dY, dYT, ldT, dbg, de, ds);
     return post();
   }
   int colsum(const float* x, int B, int d, float* out) {
@@ -251,7 +320,7 @@ bpplan::Shape bptt_shape(const rlt_model* m, int B, int n, int T_mem, float temp
 
 template <typename T_>
 int bptt_impl(const rlt_model* m, const bpplan::Shape& S, const bpplan::Detach& D,
-              const bpplan::Io<T_>& io, const bpplan::Grads& G, void* ws, cudaStream_t st) {
+              const bpplan::Io<T_>& io, const bpplan::Grads& G, void* ws, cudaStream_t st, bool graphs) {
   const rlt_weights& w = m->w;
   bpplan::Params<T_> P;
   P.W_g = static_cast<const T_*>(w.W_g);
@@ -272,6 +341,9 @@ int bptt_impl(const rlt_model* m, const bpplan::Shape& S, const bpplan::Detach& 
   const bpplan::Layout Lw = bpplan::layout(S, m->esz, kBpttHeader);
   BpttOps<T_> k;
   k.st = st;
+  k.user = st;
+  k.cap = m->cap_stream;
+  k.graphs = graphs;
   k.status = static_cast<int*>(ws);
   k.sc.n_sm = m->n_sm;
   k.sc.maxc = m->gemm_maxc;
@@ -304,13 +376,13 @@ int rlt_bptt_workspace_size(const rlt_model* m, int32_t B, int32_t n, size_t* by
 }
 
 int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, int32_t B, int32_t n,
-             const int32_t* actions, float temperature, int32_t top_k, int32_t detach_s_every, int32_t detach_flags,
+             const int32_t* actions, float temperature, int32_t top_k, int32_t detach_s_every, int32_t flags,
              float* loss, float* logp, const rlt_grads* grads, float* d_e, float* d_mem, void* ws, size_t ws_bytes,
              rlt_stream_t stream) {
   if (!m || !e || !mem || !actions || !loss || !grads || !ws) return RLT_EINVAL;
   if (B <= 0 || n <= 0 || T_mem < n) return RLT_EINVAL;
   if (!(temperature > 0.f) || top_k < 0 || detach_s_every < 0) return RLT_EINVAL;
-  if (detach_flags & ~(RLT_DETACH_CACHE | RLT_DETACH_MEMORY)) return RLT_EINVAL;
+  if (flags & ~(RLT_DETACH_CACHE | RLT_DETACH_MEMORY | RLT_BPTT_NO_GRAPHS)) return RLT_EINVAL;
   const float* gp[] = {grads->W_g, grads->b_g, grads->W_qkv, grads->W_O, grads->W_Qx, grads->W_Ox, grads->W_1,
                        grads->W_3, grads->W_2, grads->W_o, grads->dec_attn_norm, grads->dec_xattn_norm,
                        grads->dec_ffn_norm, grads->head_norm, grads->s_star};
@@ -330,8 +402,9 @@ int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, 
   if (rc) return rc;
   bpplan::Detach D;
   D.s_every = detach_s_every;
-  D.cache = (detach_flags & RLT_DETACH_CACHE) != 0;
-  D.memory = (detach_flags & RLT_DETACH_MEMORY) != 0;
+  D.cache = (flags & RLT_DETACH_CACHE) != 0;
+  D.memory = (flags & RLT_DETACH_MEMORY) != 0;
+  const bool graphs = (flags & RLT_BPTT_NO_GRAPHS) == 0;
   bpplan::Grads G;
   G.W_g = grads->W_g;
   G.b_g = grads->b_g;
@@ -351,10 +424,10 @@ int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (m->cfg.dtype == RLT_BF16) {
     bpplan::Io<bf16> io{static_cast<const bf16*>(e), static_cast<const bf16*>(mem), actions, loss, logp, d_e, d_mem};
-    return bptt_impl<bf16>(m, S, D, io, G, ws, s);
+    return bptt_impl<bf16>(m, S, D, io, G, ws, s, graphs);
   }
   bpplan::Io<float> io{static_cast<const float*>(e), static_cast<const float*>(mem), actions, loss, logp, d_e, d_mem};
-  return bptt_impl<float>(m, S, D, io, G, ws, s);
+  return bptt_impl<float>(m, S, D, io, G, ws, s, graphs);
 }
 
 }  // extern "C"

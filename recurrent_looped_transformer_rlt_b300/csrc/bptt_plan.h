@@ -104,6 +104,7 @@ struct Layout {
   size_t part;          // f32 split-attention partials: [B][H][splits][hd + 2] or [3 hd + 1] (window backward)
   // gradient scratch
   size_t ds, dh, dx, dY, dY2;
+  size_t pos, xo_step, g_step, s_cur;  // position cell (int); [L][B][d] T; [B][d] f32; [B][d] f32
   size_t total;
 };
 
@@ -189,6 +190,10 @@ inline Layout layout(const Shape& S, size_t es, size_t hdr) {
   if (V > ny) ny = V;
   Lw.dY = take(es * B * ny);
   Lw.dY2 = take(es * B * 2 * f);
+  Lw.pos = take(sizeof(int));
+  Lw.xo_step = take(es * L * Bd);
+  Lw.g_step = take(4 * Bd);
+  Lw.s_cur = take(4 * Bd);
   Lw.total = off;
   return Lw;
 }
@@ -271,59 +276,61 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
   RLT_BP_TRY(k.transpose(P.W_o, V, d, d, wt_o, V));
   RLT_BP_TRY(k.bcast_rows(s_all, P.s_star, B, d));
 
-  // ---- step t's forward.  slot < 0: the recording pass (cross-attention
-  // computed and recorded, no transposed operands); slot >= 0: recomputation
-  // in the reverse pass (recorded cross-attention, operands into the slot).
+  // ---- one step, written so that it can be captured once and replayed:
+  // every quantity that depends on the step's position p is read on the
+  // device from the position cell (*pos), and every pointer handed to an
+  // operation depends only on the step's slot.  slot < 0: the recording pass
+  // (cross-attention computed and recorded, s_t stored, no transposed
+  // operands); slot >= 0: recomputation in the reverse pass (recorded
+  // cross-attention, operands into the slot).
+  int* pos = reinterpret_cast<int*>(ws + Lw.pos);
   T* xg = X(Lw.xg);
   float* zpre = F(Lw.zpre);
   float* z = F(Lw.z);
   float* qkv = F(Lw.qkv);
+  T* xo_step = X(Lw.xo_step);
   // column slot of a block operand: rows_before rows into the buffer at off
   auto col = [&](size_t off, size_t rows_before, int slot) -> T* {
     return slot < 0 ? nullptr : X(off) + rows_before * ldT + (size_t)slot * Bp;
   };
-  auto fwd = [&](int t, int slot) -> int {
-    const int p = t - 1;
-    const float* s_prev = s_all + (size_t)(t - 1) * Bd;
+  auto fwd = [&](int slot) -> int {
     if (S.gate_learned) {
-      RLT_BP_TRY(k.merge_in(io.e, S.T_mem, p, s_prev, B, d, xg, col(Lw.xgT, 0, slot), ldT));
+      RLT_BP_TRY(k.merge_in(io.e, S.T_mem, pos, s_all, B, d, xg, col(Lw.xgT, 0, slot), ldT));
       RLT_BP_TRY(k.gemm(xg, 2 * d, B, 2 * d, P.W_g, 2 * d, d, zpre, d, false));
     }
-    RLT_BP_TRY(k.merge_out(S.gate_learned ? zpre : nullptr, P.b_g, io.e, S.T_mem, p, s_prev, B, d, z, F(Lw.hA)));
+    RLT_BP_TRY(k.merge_out(S.gate_learned ? zpre : nullptr, P.b_g, io.e, S.T_mem, pos, s_all, B, d, z, F(Lw.hA)));
     for (int l = 0; l < L; ++l) {
       float* hA = F(Lw.hA) + l * Bd;
       float* hX = F(Lw.hX) + l * Bd;
       float* hF = F(Lw.hF) + l * Bd;
       T* Kl = hist + (size_t)(2 * l) * plane_h;
       T* Vl = hist + (size_t)(2 * l + 1) * plane_h;
-      // window self-attention
-      RLT_BP_TRY(k.rms_fwd(hA, P.attn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rA) + l * B, X(Lw.a) + l * Bd,
-                           col(Lw.aT, (size_t)l * d, slot), ldT));
+      // window self-attention (q and the LSE into this position's record slot)
+      RLT_BP_TRY(k.rms_fwd(hA, nullptr, 0, P.attn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rA) + l * B,
+                           X(Lw.a) + l * Bd, col(Lw.aT, (size_t)l * d, slot), ldT));
       RLT_BP_TRY(k.gemm(X(Lw.a) + l * Bd, d, B, d, P.W_qkv + l * 3 * dd, d, 3 * d, qkv, 3 * d, false));
-      const size_t rec = (size_t)l * W + p % W;  // this position's record slot
-      const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
-      RLT_BP_TRY(k.swa_fwd(qkv, p, j0, B, H, hd, S.theta, S.scale, F(Lw.qR) + rec * Bd, Kl, Vl, n,
-                           F(Lw.lR) + rec * BH, X(Lw.oq) + l * Bd, col(Lw.oT, (size_t)l * d, slot), ldT,
-                           F(Lw.part)));
+      RLT_BP_TRY(k.swa_fwd(qkv, pos, W, B, H, hd, S.theta, S.scale, F(Lw.qR) + (size_t)l * W * Bd,
+                           F(Lw.lR) + (size_t)l * W * BH, Kl, Vl, n, X(Lw.oq) + l * Bd,
+                           col(Lw.oT, (size_t)l * d, slot), ldT, F(Lw.part)));
       RLT_BP_TRY(k.gemm_res(X(Lw.oq) + l * Bd, d, B, d, P.W_O + l * dd, d, d, hA, hX, d));
       // cross-attention to memory positions 0..p (recorded in the first pass)
-      RLT_BP_TRY(k.rms_fwd(hX, P.xattn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rX) + l * B, X(Lw.c) + l * Bd,
-                           col(Lw.cT, (size_t)l * d, slot), ldT));
+      RLT_BP_TRY(k.rms_fwd(hX, nullptr, 0, P.xattn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rX) + l * B,
+                           X(Lw.c) + l * Bd, col(Lw.cT, (size_t)l * d, slot), ldT));
       float* qx = slot < 0 ? qkv : F(Lw.qxS) + ((size_t)slot * L + l) * Bd;
       RLT_BP_TRY(k.gemm(X(Lw.c) + l * Bd, d, B, d, P.W_Qx + l * dd, d, d, qx, d, false));
-      T* xo = xo_all + ((size_t)p * L + l) * Bd;
+      T* xo = xo_step + l * Bd;  // this step's output row (the record is [p][l])
       if (slot < 0) {
         const int g = S.G == 1 ? 0 : l;
         RLT_BP_TRY(k.attn_fwd(qx, io.mem + (size_t)(2 * g) * plane_m, io.mem + (size_t)(2 * g + 1) * plane_m,
-                              S.T_mem, 0, p, B, H, hd, S.scale, lse2_all + ((size_t)p * L + l) * BH, xo, nullptr,
-                              ldT, F(Lw.part)));
+                              S.T_mem, pos, n, B, H, hd, S.scale, lse2_all + l * BH, xo_all + l * Bd, L, xo,
+                              F(Lw.part)));
       } else {
-        RLT_BP_TRY(k.tcopy(xo, B, d, col(Lw.oxT, (size_t)l * d, slot), ldT));
+        RLT_BP_TRY(k.tcopy(xo_all + l * Bd, L, pos, B, d, xo, col(Lw.oxT, (size_t)l * d, slot), ldT));
       }
       RLT_BP_TRY(k.gemm_res(xo, d, B, d, P.W_Ox + l * dd, d, d, hX, hF, d));
       // SwiGLU feed-forward
-      RLT_BP_TRY(k.rms_fwd(hF, P.ffn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rF) + l * B, X(Lw.bb) + l * Bd,
-                           col(Lw.bbT, (size_t)l * d, slot), ldT));
+      RLT_BP_TRY(k.rms_fwd(hF, nullptr, 0, P.ffn_norm + (size_t)l * d, B, d, S.eps, F(Lw.rF) + l * B,
+                           X(Lw.bb) + l * Bd, col(Lw.bbT, (size_t)l * d, slot), ldT));
       float* gl = F(Lw.g) + (size_t)l * B * f;
       float* ul = F(Lw.u) + (size_t)l * B * f;
       RLT_BP_TRY(k.gemm(X(Lw.bb) + l * Bd, d, B, d, P.W_1 + l * fd, d, f, gl, f, false));
@@ -331,9 +338,10 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       RLT_BP_TRY(k.swiglu_fwd(gl, ul, B, f, X(Lw.m) + (size_t)l * B * f, col(Lw.mT, (size_t)l * f, slot), ldT));
       // the last layer's output is s_t, recorded by the first pass
       if (slot >= 0 && l + 1 == L) continue;
-      float* next = (l + 1 < L) ? F(Lw.hA) + (l + 1) * Bd : s_all + (size_t)t * Bd;
+      float* next = (l + 1 < L) ? F(Lw.hA) + (l + 1) * Bd : F(Lw.s_cur);
       RLT_BP_TRY(k.gemm_res(X(Lw.m) + (size_t)l * B * f, f, B, f, P.W_2 + l * fd, f, d, hF, next, d));
     }
+    if (slot < 0) RLT_BP_TRY(k.put_row(s_all, pos, 1, F(Lw.s_cur), B * d));  // s_{p+1}
     return 0;
   };
 
@@ -368,30 +376,24 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
     return 0;
   };
 
-  // ---- forward pass: s_t, every position's keys/values, cross-attention results
-  for (int t = 1; t <= n; ++t) RLT_BP_TRY(fwd(t, -1));
-
-  // ---- reverse pass
+  // ---- the reverse step of slot `slot` at the position in the cell
   float* ds = F(Lw.ds);  // d L / d s_t from step t+1 (then from the head too)
   float* dh = F(Lw.dh);
   float* dx = F(Lw.dx);
   T* dY = X(Lw.dY);
   T* dY2 = X(Lw.dY2);
-  int slot = 0, p_hi = n - 1;
-  for (int t = n; t >= 1; --t) {
-    const int p = t - 1;
-    RLT_BP_TRY(fwd(t, slot));
-    const float* s_t = s_all + (size_t)t * Bd;
-    const float* s_prev = s_all + (size_t)(t - 1) * Bd;
-    // head: logits = W_o RMSNorm_o(s_t); d logits of -lp
-    RLT_BP_TRY(k.rms_fwd(s_t, P.head_norm, B, d, S.eps, F(Lw.rO), X(Lw.sn), col(Lw.snT, 0, slot), ldT));
+  float* g_step = F(Lw.g_step);
+  auto rev = [&](int slot) -> int {
+    RLT_BP_TRY(fwd(slot));
+    // head: logits = W_o RMSNorm_o(s_t) (s_t = s_all row p + 1); d logits of -lp
+    RLT_BP_TRY(k.rms_fwd(s_all, pos, 1, P.head_norm, B, d, S.eps, F(Lw.rO), X(Lw.sn), col(Lw.snT, 0, slot), ldT));
     RLT_BP_TRY(k.gemm(X(Lw.sn), d, B, d, P.W_o, d, V, F(Lw.logits), V, false));
-    RLT_BP_TRY(k.head_bwd(F(Lw.logits), B, V, io.actions, n, p, S.inv_temp, S.top_k, lp, dY, col(Lw.dlT, 0, slot),
-                          ldT));
+    RLT_BP_TRY(k.head_bwd(F(Lw.logits), B, V, io.actions, n, pos, S.inv_temp, S.top_k, lp, dY,
+                          col(Lw.dlT, 0, slot), ldT));
     RLT_BP_TRY(k.gemm(dY, V, B, V, wt_o, V, d, dx, d, false));
     // (each RMSNorm backward also writes the updated gradient as the next
     // section's dY operand and its transposed slot)
-    RLT_BP_TRY(k.rms_bwd(s_t, F(Lw.rO), P.head_norm, dx, B, d, ds, G.head_norm, dY,
+    RLT_BP_TRY(k.rms_bwd(s_all, pos, 1, F(Lw.rO), P.head_norm, dx, B, d, ds, G.head_norm, dY,
                          col(Lw.dhfT, (size_t)(L - 1) * d, slot), ldT));
     RLT_BP_TRY(k.copy(dh, ds, 4 * Bd));
     for (int l = L - 1; l >= 0; --l) {
@@ -404,48 +406,62 @@ int run(Ops& k, const Shape& S, const Detach& D, const Params<typename Ops::T>& 
       RLT_BP_TRY(k.gemm_swiglu_bwd(dY, d, B, d, wt_2 + l * fd, d, f, F(Lw.g) + (size_t)l * B * f,
                                    F(Lw.u) + (size_t)l * B * f, dY2, col(Lw.dguT, (size_t)l * 2 * f, slot), ldT));
       RLT_BP_TRY(k.gemm(dY2, 2 * f, B, 2 * f, wt_13 + l * 2 * fd, 2 * f, d, dx, d, false));
-      RLT_BP_TRY(k.rms_bwd(hF, F(Lw.rF) + l * B, P.ffn_norm + (size_t)l * d, dx, B, d, dh,
+      RLT_BP_TRY(k.rms_bwd(hF, nullptr, 0, F(Lw.rF) + l * B, P.ffn_norm + (size_t)l * d, dx, B, d, dh,
                            G.ffn_norm + (size_t)l * d, dY, col(Lw.dhxT, (size_t)l * d, slot), ldT));
       // cross-attention: hF = hX + ox W_Ox^T; the query gradient now, the
       // memory gradient at the end of the block
       float* gx = F(Lw.gxS) + ((size_t)slot * L + l) * Bd;
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Ox + l * dd, d, d, gx, d, false));
       const int g = S.G == 1 ? 0 : l;
-      RLT_BP_TRY(k.attn_bwd(F(Lw.qxS) + ((size_t)slot * L + l) * Bd, gx, xo_all + ((size_t)p * L + l) * Bd,
-                            lse2_all + ((size_t)p * L + l) * BH, io.mem + (size_t)(2 * g) * plane_m,
-                            io.mem + (size_t)(2 * g + 1) * plane_m, S.T_mem, 0, p, B, H, hd, S.scale,
-                            F(Lw.DxS) + ((size_t)slot * L + l) * BH, dY, col(Lw.dqxT, (size_t)l * d, slot), ldT,
-                            F(Lw.part)));
+      RLT_BP_TRY(k.attn_bwd(F(Lw.qxS) + ((size_t)slot * L + l) * Bd, gx, xo_step + l * Bd, lse2_all + l * BH, L,
+                            io.mem + (size_t)(2 * g) * plane_m, io.mem + (size_t)(2 * g + 1) * plane_m, S.T_mem, pos,
+                            n, B, H, hd, S.scale, F(Lw.DxS) + ((size_t)slot * L + l) * BH, dY,
+                            col(Lw.dqxT, (size_t)l * d, slot), ldT, F(Lw.part)));
       RLT_BP_TRY(k.gemm(dY, d, B, d, wt_Qx + l * dd, d, d, dx, d, false));
-      RLT_BP_TRY(k.rms_bwd(hX, F(Lw.rX) + l * B, P.xattn_norm + (size_t)l * d, dx, B, d, dh,
+      RLT_BP_TRY(k.rms_bwd(hX, nullptr, 0, F(Lw.rX) + l * B, P.xattn_norm + (size_t)l * d, dx, B, d, dh,
                            G.xattn_norm + (size_t)l * d, dY, col(Lw.dhaT, (size_t)l * d, slot), ldT));
-      // window self-attention: hX = hA + o W_O^T; this step's query-side
-      // record (query, output gradient, LSE, D) stays in the ring
-      const size_t rec = (size_t)l * W + p % W;
-      float* g_rec = F(Lw.gR) + rec * Bd;
-      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_O + l * dd, d, d, g_rec, d, false));
-      // the query gradient over the window and position p's key/value
-      // gradient from the queries of positions p..p+W-1 (only its own with
-      // the cache detached), both back through RoPE into d qkv
-      const int j0 = p - W + 1 > 0 ? p - W + 1 : 0;
-      const int p_last = D.cache ? p : (p + W - 1 < n - 1 ? p + W - 1 : n - 1);
-      RLT_BP_TRY(k.swa_bwd(Kl, Vl, n, j0, p, p_last, X(Lw.oq) + l * Bd, F(Lw.qR) + (size_t)l * W * Bd,
-                           F(Lw.gR) + (size_t)l * W * Bd, F(Lw.lR) + (size_t)l * W * BH, F(Lw.DR) + (size_t)l * W * BH,
-                           W, B, H, hd, S.scale, S.theta, dY, col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT,
-                           F(Lw.part)));
+      // window self-attention: hX = hA + o W_O^T.  The output gradient goes to
+      // this step's record with the query, LSE and D; the query gradient over
+      // the window and position p's key/value gradient from the records of
+      // positions p..p+W-1 (only its own with the cache detached), both back
+      // through RoPE into d qkv
+      RLT_BP_TRY(k.gemm(dY, d, B, d, wt_O + l * dd, d, d, g_step, d, false));
+      RLT_BP_TRY(k.swa_bwd(Kl, Vl, n, pos, W, D.cache, X(Lw.oq) + l * Bd, g_step, F(Lw.qR) + (size_t)l * W * Bd,
+                           F(Lw.gR) + (size_t)l * W * Bd, F(Lw.lR) + (size_t)l * W * BH,
+                           F(Lw.DR) + (size_t)l * W * BH, B, H, hd, S.scale, S.theta, dY,
+                           col(Lw.dqkvT, (size_t)l * 3 * d, slot), ldT, F(Lw.part)));
       RLT_BP_TRY(k.gemm(dY, 3 * d, B, 3 * d, wt_qkv + l * 3 * dd, 3 * d, d, dx, d, false));
       // (layer l-1's FFN section reads dh as its dY; the merge reads dh)
-      RLT_BP_TRY(k.rms_bwd(hA, F(Lw.rA) + l * B, P.attn_norm + (size_t)l * d, dx, B, d, dh,
+      RLT_BP_TRY(k.rms_bwd(hA, nullptr, 0, F(Lw.rA) + l * B, P.attn_norm + (size_t)l * d, dx, B, d, dh,
                            G.attn_norm + (size_t)l * d, l > 0 ? dY : nullptr,
                            l > 0 ? col(Lw.dhfT, (size_t)(l - 1) * d, slot) : nullptr, ldT));
     }
     // merge u = z s_{t-1} + (1 - z) e_t, z = sigmoid(W_g [e_t; s_{t-1}] + b_g)
-    RLT_BP_TRY(k.merge_bwd(dh, z, io.e, S.T_mem, p, s_prev, B, d, S.gate_learned, dY, col(Lw.dzT, 0, slot), ldT,
+    RLT_BP_TRY(k.merge_bwd(dh, z, io.e, S.T_mem, pos, s_all, B, d, S.gate_learned, dY, col(Lw.dzT, 0, slot), ldT,
                            G.b_g, io.d_e, ds));
-    if (S.gate_learned)
-      RLT_BP_TRY(k.gemm_merge_bwd(dY, d, B, d, wt_g, d, d, S.T_mem, p, io.d_e, ds));
-    // s_{t-1} detached after its step: no gradient from this merge
-    if (t - 1 >= 1 && D.s_every > 0 && (t - 1) % D.s_every == 0) RLT_BP_TRY(k.zero(ds, 4 * Bd));
+    if (S.gate_learned) RLT_BP_TRY(k.gemm_merge_bwd(dY, d, B, d, wt_g, d, d, S.T_mem, pos, io.d_e, ds));
+    // s_{t-1} = s_p detached after its step: no gradient from this merge
+    if (D.s_every > 0) RLT_BP_TRY(k.zero_if_detached(ds, pos, D.s_every, B * d));
+    return 0;
+  };
+
+  // ---- forward pass: s_t, every position's keys/values, cross-attention
+  // results; one replayable step per position
+  RLT_BP_TRY(k.set_pos(pos, 0));
+  for (int t = 1; t <= n; ++t)
+    RLT_BP_TRY(k.step(-1, [&]() -> int {
+      RLT_BP_TRY(fwd(-1));
+      return k.add_pos(pos, 1);
+    }));
+
+  // ---- reverse pass, one replayable step per slot of a block
+  RLT_BP_TRY(k.set_pos(pos, n - 1));
+  int slot = 0, p_hi = n - 1;
+  for (int t = n; t >= 1; --t) {
+    RLT_BP_TRY(k.step(slot, [&]() -> int {
+      RLT_BP_TRY(rev(slot));
+      return k.add_pos(pos, -1);
+    }));
     if (++slot == SB || t == 1) {
       RLT_BP_TRY(flush(slot, p_hi));
       slot = 0;

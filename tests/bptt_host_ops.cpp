@@ -84,8 +84,9 @@ struct HostOps {
     return swiglu_bwd(dm.data(), g, u, M, f, dY, dYT, ldT);
   }
   // d[e; s] = A W_g (columns < d to the e gradient row p, the rest to ds)
-  int gemm_merge_bwd(const T* A, int lda, int M, int K, const T* W, int ldw, int d, int T_mem, int p, float* de,
-                     float* ds) {
+  int gemm_merge_bwd(const T* A, int lda, int M, int K, const T* W, int ldw, int d, int T_mem, const int* pos,
+                     float* de, float* ds) {
+    const int p = *pos;
     std::vector<float> dx((size_t)M * 2 * d);
     gemm(A, lda, M, K, W, ldw, 2 * d, dx.data(), 2 * d, false);
     return merge_bwd2(dx.data(), M, d, T_mem, p, de, ds);
@@ -94,7 +95,10 @@ struct HostOps {
     for (int r = 0; r < rows; ++r) memcpy(dst + (size_t)r * d, src, sizeof(float) * d);
     return 0;
   }
-  int merge_in(const T* e, int T_mem, int p, const float* s, int B, int d, T* xg, T* xgT, int ldT) {
+  // position-dependent operands are read from the position cell *pos
+  int merge_in(const T* e, int T_mem, const int* pos, const float* s_all, int B, int d, T* xg, T* xgT, int ldT) {
+    const int p = *pos;
+    const float* s = s_all + (size_t)p * B * d;
     for (int b = 0; b < B; ++b)
       for (int i = 0; i < 2 * d; ++i) {
         const float v = i < d ? e[((size_t)b * T_mem + p) * d + i] : st(s[(size_t)b * d + i - d]);
@@ -103,8 +107,10 @@ struct HostOps {
       }
     return 0;
   }
-  int merge_out(const float* zpre, const float* bg, const T* e, int T_mem, int p, const float* s, int B, int d,
-                float* z, float* h) {
+  int merge_out(const float* zpre, const float* bg, const T* e, int T_mem, const int* pos, const float* s_all, int B,
+                int d, float* z, float* h) {
+    const int p = *pos;
+    const float* s = s_all + (size_t)p * B * d;
     for (int b = 0; b < B; ++b)
       for (int i = 0; i < d; ++i) {
         const size_t o = (size_t)b * d + i;
@@ -115,7 +121,10 @@ struct HostOps {
       }
     return 0;
   }
-  int rms_fwd(const float* x, const float* g, int B, int d, float eps, float* r, T* y, T* yT, int ldT) {
+  // x: rows [B][d], or with pos the rows of position (*pos + off) of [.][B][d]
+  int rms_fwd(const float* x, const int* pos, int off, const float* g, int B, int d, float eps, float* r, T* y, T* yT,
+              int ldT) {
+    if (pos) x += (size_t)(*pos + off) * B * d;
     for (int b = 0; b < B; ++b) {
       const float* xr = x + (size_t)b * d;
       double ss = 0;
@@ -148,8 +157,9 @@ struct HostOps {
           V[o + i + half] = st(row[2 * d + i + half]);
         }
   }
-  int attn_fwd(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
-               float* lse, T* oq, T* oT, int ldT, float* /* scratch of the device's key split */ = nullptr) {
+  // attention of q over positions j0..j1 (lse, output rows; oT optional)
+  void attend(const float* q, const T* K, const T* V, int Tk, int j0, int j1, int B, int H, int hd, float scale,
+              float* lse, T* oq, T* oT, int ldT) {
     const int d = H * hd;
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h) {
@@ -158,9 +168,9 @@ struct HostOps {
         const float* qq = q + (size_t)b * d + h * hd;
         std::vector<double> sc;
         for (int j = j0; j <= j1; ++j) {
-          double a = 0;
-          for (int i = 0; i < hd; ++i) a += (double)qq[i] * Kb[(size_t)j * hd + i];
-          sc.push_back(a * scale);
+          double a2 = 0;
+          for (int i = 0; i < hd; ++i) a2 += (double)qq[i] * Kb[(size_t)j * hd + i];
+          sc.push_back(a2 * scale);
         }
         const double mx = *std::max_element(sc.begin(), sc.end());
         double l = 0;
@@ -175,19 +185,59 @@ struct HostOps {
           if (oT) oT[c * ldT + b] = st(acc);
         }
       }
+  }
+  // memory attention of position p = *pos over positions 0..p: the LSE and
+  // the output to the records (row p of [n][L] at lse_l, o_l with L rows per
+  // position) and the output to o_step
+  int attn_fwd(const float* q, const T* K, const T* V, int Tk, const int* pos, int /* n: the device's split grid */,
+               int B, int H, int hd, float scale, float* lse_l, T* o_l, int L, T* o_step,
+               float* /* scratch of the device's key split */) {
+    const int p = *pos, d = H * hd;
+    attend(q, K, V, Tk, 0, p, B, H, hd, scale, lse_l + (size_t)p * L * B * H, o_step, nullptr, 0);
+    memcpy(o_l + (size_t)p * L * B * d, o_step, sizeof(T) * (size_t)B * d);
     return 0;
   }
-  // window attention forward of position p: RoPE of q and k at p (q to qo
-  // fp32, k and v to K/V [B][H][Tk][hd] at p), then the attention of q over
-  // positions j0..p (lse, oq and its transposed slot)
-  int swa_fwd(const float* qkv, int p, int j0, int B, int H, int hd, float theta, float scale, float* qo, T* K, T* V,
-              int Tk, float* lse, T* oq, T* oT, int ldT, float* /* scratch of the device's key split */) {
+  // window attention forward of position p = *pos: RoPE of q and k at p (q to
+  // its record slot p mod W of qR, k and v to K/V at p), then the attention
+  // over positions max(0, p - W + 1)..p (LSE to the record slot of lR)
+  int swa_fwd(const float* qkv, const int* pos, int W, int B, int H, int hd, float theta, float scale, float* qR,
+              float* lR, T* K, T* V, int Tk, T* oq, T* oT, int ldT, float* /* scratch of the device's key split */) {
+    const int p = *pos, j0 = p - W + 1 > 0 ? p - W + 1 : 0;
+    float* qo = qR + (size_t)(p % W) * B * H * hd;
     qkv_post(qkv, p, B, H, hd, theta, qo, K, V, Tk);
-    return attn_fwd(qo, K, V, Tk, j0, p, B, H, hd, scale, lse, oq, oT, ldT);
+    attend(qo, K, V, Tk, j0, p, B, H, hd, scale, lR + (size_t)(p % W) * B * H, oq, oT, ldT);
+    return 0;
   }
-  int tcopy(const T* x, int B, int N, T* yT, int ldT) {
+  // row p (L rows per position) of a recorded [n][L][B][N] operand into the
+  // fixed rows y and the column slot yT
+  int tcopy(const T* x_l, int L, const int* pos, int B, int N, T* y, T* yT, int ldT) {
+    const T* x = x_l + (size_t)(*pos) * L * B * N;
     for (int b = 0; b < B; ++b)
-      for (int j = 0; j < N; ++j) yT[(size_t)j * ldT + b] = x[(size_t)b * N + j];
+      for (int j = 0; j < N; ++j) {
+        y[(size_t)b * N + j] = x[(size_t)b * N + j];
+        yT[(size_t)j * ldT + b] = x[(size_t)b * N + j];
+      }
+    return 0;
+  }
+  int put_row(float* dst, const int* pos, int off, const float* src, int count) {
+    memcpy(dst + (size_t)(*pos + off) * count, src, sizeof(float) * count);
+    return 0;
+  }
+  int set_pos(int* pos, int v) {
+    *pos = v;
+    return 0;
+  }
+  int add_pos(int* pos, int dv) {
+    *pos += dv;
+    return 0;
+  }
+  template <class Fn>
+  int step(int /* key of the device's captured step */, Fn fn) {
+    return fn();
+  }
+  int zero_if_detached(float* ds, const int* pos, int s_every, int count) {
+    const int p = *pos;
+    if (p >= 1 && s_every > 0 && p % s_every == 0) memset(ds, 0, sizeof(float) * count);
     return 0;
   }
   int swiglu_fwd(const float* g, const float* u, int B, int f, T* m, T* mT, int ldT) {
@@ -201,8 +251,9 @@ struct HostOps {
       }
     return 0;
   }
-  int head_bwd(const float* logits, int B, int V, const int32_t* actions, int n, int p, float inv_temp, int top_k,
-               float* lp, T* dl, T* dlT, int ldT) {
+  int head_bwd(const float* logits, int B, int V, const int32_t* actions, int n, const int* pos, float inv_temp,
+               int top_k, float* lp, T* dl, T* dlT, int ldT) {
+    const int p = *pos;
     for (int b = 0; b < B; ++b) {
       std::vector<double> x(V);
       for (int v = 0; v < V; ++v) x[v] = (double)logits[(size_t)b * V + v] * inv_temp;
@@ -235,8 +286,9 @@ struct HostOps {
   }
   // dx += RMSNorm backward, dg += the gain gradient; with y given, the
   // updated dx rows also go to y (storage type) and yT (transposed)
-  int rms_bwd(const float* x, const float* r, const float* g, const float* dy, int B, int d, float* dx, float* dg,
-              T* y, T* yT, int ldT) {
+  int rms_bwd(const float* x, const int* pos, int off, const float* r, const float* g, const float* dy, int B, int d,
+              float* dx, float* dg, T* y, T* yT, int ldT) {
+    if (pos) x += (size_t)(*pos + off) * B * d;
     for (int i = 0; i < d; ++i) {
       double acc = 0;
       for (int b = 0; b < B; ++b) acc += (double)dy[(size_t)b * d + i] * x[(size_t)b * d + i] * r[b];
@@ -308,14 +360,15 @@ struct HostOps {
         for (int i = 0; i < hd; ++i) dq[(size_t)b * d + h * hd + i] = (float)(scale * acc[i]);
       }
   }
-  // the query gradient of the cross-attention, written as the next
+  // the query gradient of the memory attention of position p = *pos (LSE
+  // row p of lse_l with L rows per position), written as the next
   // projection's operands (storage type [B][d] and transposed)
-  int attn_bwd(const float* q, const float* gout, const T* o, const float* lse, const T* K, const T* V, int Tk,
-               int j0, int j1, int B, int H, int hd, float scale, float* Dout, T* dqY, T* dqT, int ldT,
-               float* /* scratch of the device's key split */) {
-    const int d = H * hd;
+  int attn_bwd(const float* q, const float* gout, const T* o, const float* lse_l, int L, const T* K, const T* V, int Tk,
+               const int* pos, int /* n: the device's split grid */, int B, int H, int hd, float scale, float* Dout,
+               T* dqY, T* dqT, int ldT, float* /* scratch of the device's key split */) {
+    const int p = *pos, d = H * hd;
     std::vector<float> dq((size_t)B * d);
-    attn_dq(q, gout, o, lse, K, V, Tk, j0, j1, B, H, hd, scale, dq.data(), Dout);
+    attn_dq(q, gout, o, lse_l + (size_t)p * L * B * H, K, V, Tk, 0, p, B, H, hd, scale, dq.data(), Dout);
     return pack(dq.data(), B, d, dqY, dqT, ldT);
   }
   // key/value gradient of window position p from the query-side records of
@@ -409,23 +462,30 @@ struct HostOps {
           }
         }
   }
-  // window attention backward of position p (one layer): the query gradient
-  // over positions j0..p from this step's record (slot p mod W; D is written
-  // there), the key/value gradient of position p from the records of
-  // positions p..p_last, both back through RoPE, the value gradient as is,
-  // into d qkv [B][3d] (storage type, and transposed)
-  int swa_bwd(const T* K, const T* V, int Tk, int j0, int p, int p_last, const T* o, const float* qR,
-              const float* gR, float* lR, float* DR, int W, int B, int H, int hd, float scale, float theta, T* dY,
-              T* dYT, int ldT, float* /* scratch of the device's split */) {
+  // window attention backward of position p = *pos (one layer): this step's
+  // output gradient g into its record (slot p mod W), the query gradient over
+  // positions max(0, p - W + 1)..p (D written to the record), the key/value
+  // gradient of position p from the records of positions p..p_last (p_last =
+  // p with the cache detached, else min(p + W - 1, n - 1); n = Tk), both back
+  // through RoPE, the value gradient as is, into d qkv [B][3d] (storage type,
+  // and transposed)
+  int swa_bwd(const T* K, const T* V, int Tk, const int* pos, int W, bool cache, const T* o, const float* g,
+              float* qR, float* gR, float* lR, float* DR, int B, int H, int hd, float scale, float theta, T* dY, T* dYT,
+              int ldT, float* /* scratch of the device's split */) {
+    const int p = *pos, j0 = p - W + 1 > 0 ? p - W + 1 : 0;
+    const int p_last = cache ? p : (p + W - 1 < Tk - 1 ? p + W - 1 : Tk - 1);
     const size_t Bd = (size_t)B * H * hd, BH = (size_t)B * H, r = (size_t)(p % W);
+    memcpy(gR + r * Bd, g, sizeof(float) * Bd);
     std::vector<float> dq(Bd), dK(Bd), dV(Bd);
     attn_dq(qR + r * Bd, gR + r * Bd, o, lR + r * BH, K, V, Tk, j0, p, B, H, hd, scale, dq.data(), DR + r * BH);
     kv_grad(K, V, Tk, p, p_last, qR, gR, lR, DR, W, B, H, hd, scale, dK.data(), dV.data());
     qkv_bwd(dq.data(), dK.data(), dV.data(), p, B, H, hd, theta, dY, dYT, ldT);
     return 0;
   }
-  int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, int p, const float* s, int B, int d,
-                bool gate, T* dY, T* dYT, int ldT, float* dbg, float* de, float* ds) {
+  int merge_bwd(const float* dh, const float* z, const T* e, int T_mem, const int* pos, const float* s_all, int B,
+                int d, bool gate, T* dY, T* dYT, int ldT, float* dbg, float* de, float* ds) {
+    const int p = *pos;
+    const float* s = s_all + (size_t)p * B * d;
     for (int i = 0; i < d; ++i) {
       double acc = 0;
       for (int b = 0; b < B; ++b) {

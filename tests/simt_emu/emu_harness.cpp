@@ -22,6 +22,21 @@ inline unsigned cdiv(size_t a, size_t b) { return (unsigned)((a + b - 1) / b); }
 inline int cudaMemsetAsync(void* p, int v, size_t n, cudaStream_t) { memset(p, v, n); return cudaSuccess; }
 inline int cudaMemcpyAsync(void* d, const void* s, size_t n, int, cudaStream_t) { memmove(d, s, n); return cudaSuccess; }
 struct TcScratch { int n_sm; int* status; const int (*maxc)[9]; };
+// graph capture is not emulated: the harness runs the steps eagerly (these
+// stand-ins only let the capture path compile)
+typedef struct GraphStub* cudaGraph_t;
+typedef struct GraphExecStub* cudaGraphExec_t;
+constexpr int cudaStreamCaptureModeThreadLocal = 1;
+inline int cudaStreamBeginCapture(cudaStream_t, int) { return -1; }
+inline int cudaStreamEndCapture(cudaStream_t, cudaGraph_t*) { return -1; }
+inline int cudaGraphInstantiate(cudaGraphExec_t*, cudaGraph_t, int) { return -1; }
+inline int cudaGraphDestroy(cudaGraph_t) { return 0; }
+inline int cudaGraphLaunch(cudaGraphExec_t, cudaStream_t) { return -1; }
+inline int cudaGraphExecDestroy(cudaGraphExec_t) { return 0; }
+#define RLT_CUDA_TRY(x)                         \
+  do {                                          \
+    if ((x) != cudaSuccess) return RLT_ECUDA;   \
+  } while (0)
 struct AArg { const bf16* A; int lda; };
 __global__ void bcast_rows_kernel(float* dst, const float* src, int rows, int d) {
   size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -93,6 +108,9 @@ static int run_emu(const int* sh, const float* fp, void** P, const size_t* nel) 
   std::vector<double> ws((Lw.total + 7) / 8, 0.0);
   EmuOps<T> k;
   k.st = nullptr;
+  k.user = nullptr;
+  k.cap = nullptr;
+  k.graphs = false;
   k.status = reinterpret_cast<int*>(ws.data());
   return bpplan::run(k, S, D, Pp, io, G, reinterpret_cast<char*>(ws.data()), Lw);
 }

@@ -42,7 +42,7 @@ def _generate(out_dir):
     b = api.index("};", api.index("  int loss_sum(")) + 2
     ops, n = re.subn(r"([\w:<>]+)<<<(.*?), st>>>\((.*?)\);", r"emu_launch(\2, \1, \3);", api[a:b], flags=re.S)
     assert n >= 15 and "<<<" not in ops
-    open(os.path.join(out_dir, "emu_ops.inc"), "w").write(ops.replace("struct BpttOps {", "struct EmuOps {"))
+    open(os.path.join(out_dir, "emu_ops.inc"), "w").write(ops.replace("BpttOps", "EmuOps"))
 
 
 @pytest.fixture(scope="module")
