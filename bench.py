@@ -596,13 +596,18 @@ def run_bptt_case(args):
     t = float(np.mean(ts))
     nbytes, nflops = bptt_bytes(c, B, n), bptt_flops(c, B, n)
     roof = max(nbytes / bw, nflops / peak)
+    hbm = nbytes / bw >= nflops / peak
+    roofline = {"bound": "hbm" if hbm else "tensor",
+                "achieved": round((nbytes / t / 1e9) if hbm else (nflops / t / 1e12), 1),
+                "peak": round(bw / 1e9, 1) if hbm else round(peak / 1e12, 1),
+                "unit": "GB/s" if hbm else "TFLOP/s",
+                "frac": round(roof / t, 4), "traffic": None, "kernel": "rlt_bptt (whole call)",
+                "peak_source": src}
     print(json.dumps({"case": "bptt", "workload": wl.name, "B": B, "steps": n, "block": min(BPTT_BLOCK, n),
                       "tokens_per_s": round(B * n / t, 1), "ms_per_call": round(1e3 * t, 3),
                       "loss": float(res.loss.item()), "bytes_per_call": nbytes, "flops_per_call": nflops,
-                      "roofline_ms": round(1e3 * roof, 3), "roofline_frac": round(roof / t, 4),
-                      "bound": "hbm" if nbytes / bw >= nflops / peak else "tensor",
-                      "achieved_gbs": round(nbytes / t / 1e9, 1), "peak_gbs": round(bw / 1e9, 1),
-                      "peak_source": src, "gpu_launches": int(launches), "calls": len(ts),
+                      "roofline_ms": round(1e3 * roof, 3), "roofline": roofline,
+                      "gpu_launches": int(launches), "calls": len(ts),
                       "timing": "CUDA events around rlt_bptt (recording pass, reverse pass, block flushes)"}),
           flush=True)
     model.close()
