@@ -43,6 +43,10 @@
 //    to the weight gradient, and one key-parallel pass adds the block's
 //    contributions to the memory gradient (which feeds nothing in the
 //    recurrence, so it can wait).
+//  * A step is replayable: the operations read the step's position from a
+//    device cell (Ops::step's last operation moves it) and get pointers that
+//    depend only on the block slot, so the device Ops can capture the
+//    recording step and each reverse slot once and replay them.
 #pragma once
 
 #include <stddef.h>
