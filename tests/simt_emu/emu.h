@@ -66,6 +66,22 @@ inline int __shfl_xor_sync(unsigned, int v, int m) {
   w.bar->arrive_and_wait();
   return r;
 }
+inline float __shfl_sync(unsigned, float v, int src) {
+  auto& w = (*emu_warps)[emu_warp];
+  w.f[emu_lane] = v;
+  w.bar->arrive_and_wait();
+  float r = w.f[src & 31];
+  w.bar->arrive_and_wait();
+  return r;
+}
+inline int __shfl_sync(unsigned, int v, int src) {
+  auto& w = (*emu_warps)[emu_warp];
+  w.i[emu_lane] = v;
+  w.bar->arrive_and_wait();
+  int r = w.i[src & 31];
+  w.bar->arrive_and_wait();
+  return r;
+}
 inline unsigned atomicAdd(unsigned* p, unsigned v) { return std::atomic_ref<unsigned>(*p).fetch_add(v); }
 inline int atomicCAS(int* p, int cmp, int val) {
   std::atomic_ref<int> a(*p);
@@ -168,5 +184,6 @@ void emu_launch(dim3 grid, dim3 block, size_t smem, F kernel, A... args) {
 struct float2 { float x, y; };
 struct float4 { float x, y, z, w; };
 struct uint2 { unsigned x, y; };
+struct uint4 { unsigned x, y, z, w; };
 inline float2 make_float2(float a, float b) { return float2{a, b}; }
 inline float4 make_float4(float a, float b, float c, float d) { return float4{a, b, c, d}; }
