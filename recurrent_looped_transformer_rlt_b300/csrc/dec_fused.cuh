@@ -1,0 +1,767 @@
+// Persistent cluster decoder: all n steps of a decode call of bf16 models in
+// one launch, one thread-block cluster per group of sequences (the plan and
+// the shared-memory layout are in fused_plan.h).
+//
+// A step is the transition of "Understanding and Applying the Recurrent
+// Looped Transformer Architecture" (architecture section): the gated merge
+// u = z s_{t-1} + (1 - z) e_t, then per decoder layer sliding-window
+// self-attention over the ring of the last W keys and values (the current one
+// included), cross-attention to encoder memory positions 1..t, and a SwiGLU
+// feed-forward, each with a pre-RMSNorm and a residual add; s_t is the last
+// residual stream, and the head scores the next action under
+// softmax(W_o RMSNorm_o(s_t) / temperature), optionally truncated to the
+// top k.  The values stored in bf16 are the ones the other decoder path
+// stores: the normalised projection inputs, the RoPE'd keys and the values,
+// the two attention outputs and the SwiGLU product.
+//
+// Phases of a step (one cluster barrier after each but the head):
+//   gate  rows of z, h = z s + (1 - z) e        -> h rows pushed to every CTA
+//   per layer:
+//   QKV   q, k, v of this CTA's heads, RoPE, ring write, window attention
+//                                                -> attention output pushed
+//   O     rows of h += O o                       -> h rows pushed
+//   Qx    queries of this CTA's heads, cross-attention over memory 0..p
+//                                                -> cross-attention output pushed
+//   Ox    rows of h += Ox ox                     -> h rows pushed
+//   W13   rows of m = silu(W_1 b) * (W_3 b)      -> m rows pushed
+//   W2    rows of h += W_2 m                     -> h rows pushed
+//   head  (CTAs that score) logits of every row, scores of the CTA's rows
+// Projections run on the tensor cores as warp-level bf16 MMAs with the
+// weights as the 16-row operand and the cluster's sequences as the 8-column
+// operand; the weights of phase q + 1 are copied from L2 into one half of a
+// double-buffered stage while phase q computes from the other half, and the
+// memory rows of the next layer's cross-attention are prefetched into L2.
+// The residual streams of step i live in h buffer i mod 2, so the step's
+// first pushes never land on the buffer another CTA may still be reading for
+// the previous step's head.
+#pragma once
+#include "common.cuh"
+#include "fused_plan.h"
+#include "fused_ptx.cuh"
+
+namespace rlt {
+namespace fused {
+
+struct Args {
+  const bf16 *W_g, *W_qkv, *W_O, *W_Qx, *W_Ox, *W_1, *W_3, *W_2, *W_o;
+  const float *b_g, *attn_norm, *xattn_norm, *ffn_norm, *head_norm;
+  const bf16* e;         // [B][T_mem][d]
+  const bf16* mem;       // [G][2][B][H][T_mem][hd]
+  const int* actions;    // [B][n] or null
+  const int* emit_map;   // [n]: index into logits_out or -1; or null
+  float* logits_out;     // [n_emit][B][V] or null
+  float* logp;           // [B][n] or null
+  float* logp_full;      // [B][n] or null
+  int* argmax;           // [B][n] or null
+  float* s;              // [B][d] f32 state, read at the start and written at the end
+  bf16* ring_k;          // [L][B][H][W][hd]
+  bf16* ring_v;
+  int* status;
+  int B, T_mem, p0, n, top_k;
+  float eps, theta, scale, inv_temp;
+  Shape sh;
+  Plan P;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ unsigned okey(float x) {  // order-preserving key of a float
+  const unsigned u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float bround(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
+  const unsigned w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// The heads and sequences CTA r attends for.
+struct Work {
+  int hlo, hpc, blo, bhi, npairs;
+};
+__device__ __forceinline__ Work work_of(const Plan& P, int r, int nbv) {
+  Work w;
+  w.hpc = P.hpc;
+  if (P.gph > 0) {
+    w.hlo = r / P.gph;
+    const int sg = r % P.gph;
+    w.blo = sg * P.Bc / P.gph;
+    w.bhi = (sg + 1) * P.Bc / P.gph;
+  } else {
+    w.hlo = r * P.hpc;
+    w.blo = 0;
+    w.bhi = P.Bc;
+  }
+  w.bhi = min(w.bhi, nbv);
+  w.blo = min(w.blo, w.bhi);
+  w.npairs = (w.bhi - w.blo) * w.hpc;
+  return w;
+}
+
+struct Ph {
+  int kind, l, nt, K, U;
+};
+struct Tile {
+  const bf16* W;
+  int row0, N;
+};
+
+// Phase k of a step on CTA r (scorer: the CTA scores at least one sequence).
+__device__ __forceinline__ Ph phase_at(const Args& a, int k, int r, const Work& wk) {
+  const Shape& s = a.sh;
+  const int CS = a.P.CS;
+  Ph ph{};
+  if (s.gate && k == 0) {
+    ph.kind = kGate;
+  } else {
+    const int kk = k - (s.gate ? 1 : 0);
+    if (kk < 6 * s.L) {
+      ph.kind = kQKV + kk % 6;
+      ph.l = kk / 6;
+    } else {
+      ph.kind = kHead;
+    }
+  }
+  int lo, hi;
+  const int th = wk.npairs > 0 ? wk.hpc * (s.hd / 16) : 0;
+  switch (ph.kind) {
+    case kGate: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = 2 * s.d; break;
+    case kQKV: ph.nt = 3 * th; ph.K = s.d; break;
+    case kQx: ph.nt = th; ph.K = s.d; break;
+    case kO:
+    case kOx: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = s.d; break;
+    case kW13: part_range(cdivi(s.f, 16), CS, r, &lo, &hi); ph.nt = 2 * (hi - lo); ph.K = s.d; break;
+    case kW2: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = s.f; break;
+    default: ph.nt = cdivi(s.V, 16); ph.K = s.d; break;
+  }
+  ph.U = round32(ph.K) / 32;
+  return ph;
+}
+
+// Weight rows of tile t of phase ph on CTA r.
+__device__ __forceinline__ Tile tile_at(const Args& a, const Ph& ph, int t, int r, const Work& wk) {
+  const Shape& s = a.sh;
+  const int d = s.d, hd = s.hd, nh = hd / 16, CS = a.P.CS;
+  const size_t dd = (size_t)d * d, fd = (size_t)s.f * d;
+  Tile T;
+  int lo, hi;
+  switch (ph.kind) {
+    case kGate:
+      part_range(d / 16, CS, r, &lo, &hi);
+      T = Tile{a.W_g, (lo + t) * 16, d};
+      break;
+    case kQKV: {
+      const int hh = t / (3 * nh), rem = t - hh * 3 * nh, part = rem / nh, j = rem - part * nh;
+      T = Tile{a.W_qkv + (size_t)ph.l * 3 * dd, part * d + (wk.hlo + hh) * hd + 16 * j, 3 * d};
+      break;
+    }
+    case kQx: {
+      const int hh = t / nh, j = t - hh * nh;
+      T = Tile{a.W_Qx + (size_t)ph.l * dd, (wk.hlo + hh) * hd + 16 * j, d};
+      break;
+    }
+    case kO:
+    case kOx:
+      part_range(d / 16, CS, r, &lo, &hi);
+      T = Tile{(ph.kind == kO ? a.W_O : a.W_Ox) + (size_t)ph.l * dd, (lo + t) * 16, d};
+      break;
+    case kW13:
+      part_range(cdivi(s.f, 16), CS, r, &lo, &hi);
+      T = Tile{((t & 1) ? a.W_3 : a.W_1) + (size_t)ph.l * fd, (lo + (t >> 1)) * 16, s.f};
+      break;
+    case kW2:
+      part_range(d / 16, CS, r, &lo, &hi);
+      T = Tile{a.W_2 + (size_t)ph.l * fd, (lo + t) * 16, d};
+      break;
+    default:
+      T = Tile{a.W_o, 16 * t, s.V};
+      break;
+  }
+  return T;
+}
+
+// Copies the weights of phase ph into a stage buffer: unit (t, u) holds rows
+// row0 .. row0 + 15 and columns 32 u .. 32 u + 31 of tile t, as lane L's
+// 16 bytes of row row0 + L/4 (first 512 bytes) and of row row0 + 8 + L/4
+// (second 512), columns 32 u + 8 (L % 4) .. + 7 - the A operand of two MMAs
+// with the 16 columns of one MMA taken as 8 (L % 4) + {0, 1, 2, 3} and the
+// other's as + {4, 5, 6, 7} (B uses the same pairing).  Rows past N and
+// columns past K are zero.
+__device__ __forceinline__ void issue(const Args& a, const Ph& ph, int r, const Work& wk, unsigned char* stg) {
+  const int total = ph.nt * ph.U * 64;
+  for (int idx = threadIdx.x; idx < total; idx += kThreads) {
+    const int unit = idx >> 6, jj = idx & 63, half = jj >> 5, ln = jj & 31;
+    const int t = unit / ph.U, u = unit - t * ph.U;
+    const Tile T = tile_at(a, ph, t, r, wk);
+    const int row = T.row0 + (ln >> 2) + 8 * half, k = u * 32 + 8 * (ln & 3);
+    const bf16* src = T.W;
+    int bytes = 0;
+    if (row < T.N && k < ph.K) {
+      src = T.W + (size_t)row * ph.K + k;
+      bytes = min(16, (ph.K - k) * 2);
+    }
+    cp_async16(stg + (size_t)unit * kUnitBytes + half * 512 + ln * 16, src, bytes);
+  }
+}
+
+// out[t][16][cols] = W_tile X^T for the phase's tiles from the stage, with X
+// [cols][ldX] bf16 (zero past K).  With at least kWarps tiles each warp
+// takes whole tiles; otherwise each tile's K is split over kWarps / nt warps
+// and their partial sums are added in split order.  Ends with a block
+// barrier.
+__device__ __forceinline__ void proj(const Ph& ph, int cols, const unsigned char* stg, const bf16* X, int ldX,
+                                     float* out, float* part) {
+  const int nt = ph.nt, U = ph.U, NT = cols / 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  if (nt == 0) return;
+  auto run = [&](int t, int u0, int u1, float (&acc)[2][4]) {
+    for (int u = u0; u < u1; ++u) {
+      const uint4* up = reinterpret_cast<const uint4*>(stg + ((size_t)t * U + u) * kUnitBytes);
+      const uint4 w0 = up[lane], w1 = up[32 + lane];
+      const unsigned A1[4] = {w0.x, w1.x, w0.y, w1.y}, A2[4] = {w0.z, w1.z, w0.w, w1.w};
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (j < NT) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(X + (size_t)(8 * j + g) * ldX + u * 32 + 8 * c);
+          const unsigned B1[2] = {xv.x, xv.y}, B2[2] = {xv.z, xv.w};
+          mma_bf16(acc[j], A1, B1);
+          mma_bf16(acc[j], A2, B2);
+        }
+      }
+    }
+  };
+  if (nt >= kWarps) {
+    for (int t = warp; t < nt; t += kWarps) {
+      float acc[2][4] = {};
+      run(t, 0, U, acc);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (j < NT) {
+          float* o0 = out + (size_t)(t * 16 + g) * cols + 8 * j + 2 * c;
+          float* o1 = o0 + 8 * cols;
+          o0[0] = acc[j][0];
+          o0[1] = acc[j][1];
+          o1[0] = acc[j][2];
+          o1[1] = acc[j][3];
+        }
+      }
+    }
+    __syncthreads();
+    return;
+  }
+  const int ks = kWarps / nt, t = warp / ks, sp = warp - t * ks;
+  if (t < nt) {
+    float acc[2][4] = {};
+    run(t, sp * U / ks, (sp + 1) * U / ks, acc);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) part[((warp * 2 + j) * 32 + lane) * 4 + q] = acc[j][q];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < nt * NT * 128; e += kThreads) {
+    const int tt = e / (NT * 128), rem = e - tt * NT * 128, j = rem >> 7, ln = (rem & 127) >> 2, q = rem & 3;
+    float v = 0.f;
+    for (int s2 = 0; s2 < ks; ++s2) v += part[(((tt * ks + s2) * 2 + j) * 32 + ln) * 4 + q];
+    const int row = (ln >> 2) + 8 * (q >> 1), col = 8 * j + 2 * (ln & 3) + (q & 1);
+    out[(size_t)(tt * 16 + row) * cols + col] = v;
+  }
+  __syncthreads();
+}
+
+// Scores column b (global sequence bg) of the head logits in out at step i.
+__device__ void score_col(const Args& a, const float* out, int cols, int b, int bg, int i, unsigned char* misc) {
+  float* fred = reinterpret_cast<float*>(misc);                // [32]
+  int* ired = reinterpret_cast<int*>(misc + 128);              // [32]
+  unsigned* hist = reinterpret_cast<unsigned*>(misc + 256);    // [256]
+  unsigned* sc = reinterpret_cast<unsigned*>(misc + 1280);     // prefix, remain, count
+  const int V = a.sh.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float it = a.inv_temp;
+  auto lg = [&](int v) { return out[(size_t)((v >> 4) * 16 + (v & 15)) * cols + b]; };
+  float bmax = -INFINITY;
+  int barg = 0x7fffffff;
+  for (int v = tid; v < V; v += kThreads) {
+    const float x = lg(v);
+    if (x > bmax || (x == bmax && v < barg)) {
+      bmax = x;
+      barg = v;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, bmax, o);
+    const int oa = __shfl_xor_sync(0xffffffffu, barg, o);
+    if (om > bmax || (om == bmax && oa < barg)) {
+      bmax = om;
+      barg = oa;
+    }
+  }
+  if (lane == 0) {
+    fred[warp] = bmax;
+    ired[warp] = barg;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float mm = fred[0];
+    int aa = ired[0];
+    for (int w = 1; w < kWarps; ++w)
+      if (fred[w] > mm || (fred[w] == mm && ired[w] < aa)) {
+        mm = fred[w];
+        aa = ired[w];
+      }
+    fred[0] = mm;
+    ired[0] = aa;
+  }
+  __syncthreads();
+  const int amax = ired[0];
+  const float mx = fred[0] * it;
+  __syncthreads();
+  float se = 0.f;
+  for (int v = tid; v < V; v += kThreads) se += expf(lg(v) * it - mx);
+  se = warp_sum(se);
+  if (lane == 0) fred[warp] = se;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kWarps; ++w) t += fred[w];
+    fred[0] = t;
+  }
+  __syncthreads();
+  const float lse = mx + logf(fred[0]);
+  __syncthreads();
+  int act = a.actions ? a.actions[(size_t)bg * a.n + i] : -1;
+  if (act >= V) {
+    if (tid == 0) set_error(a.status, kErrBounds);
+    act = -1;
+  }
+  const float lp_full = act >= 0 ? lg(act) * it - lse : NAN;
+  float lp = lp_full;
+  if (a.top_k > 0 && a.top_k < V) {
+    // k-th largest key by radix select, 8 bits at a time from the top
+    if (tid == 0) {
+      sc[0] = 0;
+      sc[1] = (unsigned)a.top_k;
+    }
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int j = tid; j < 256; j += kThreads) hist[j] = 0;
+      __syncthreads();
+      const unsigned pref = sc[0];
+      const unsigned hmask = pass == 0 ? 0u : (0xffffffffu << (shift + 8));
+      for (int v = tid; v < V; v += kThreads) {
+        const unsigned kk = okey(lg(v) * it);
+        if ((kk & hmask) == pref) atomicAdd(&hist[(kk >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        unsigned rem = sc[1];
+        int bin = 255;
+        for (; bin > 0; --bin) {
+          if (hist[bin] >= rem) break;
+          rem -= hist[bin];
+        }
+        sc[0] = pref | ((unsigned)bin << shift);
+        sc[1] = rem;
+      }
+      __syncthreads();
+    }
+    const unsigned kth = sc[0], need = sc[1];
+    const float xk = __uint_as_float((kth & 0x80000000u) ? (kth & 0x7fffffffu) : ~kth);
+    float sg = 0.f;
+    for (int v = tid; v < V; v += kThreads) {
+      const float x = lg(v) * it;
+      if (okey(x) > kth) sg += expf(x - mx);
+    }
+    sg = warp_sum(sg);
+    unsigned below = 0;  // ids below the action with the k-th key
+    if (act >= 0 && okey(lg(act) * it) == kth)
+      for (int v = tid; v < act; v += kThreads) below += okey(lg(v) * it) == kth ? 1u : 0u;
+    __syncthreads();
+    if (lane == 0) fred[warp] = sg;
+    if (tid == 0) sc[2] = 0;
+    __syncthreads();
+    if (below) atomicAdd(&sc[2], below);
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < kWarps; ++w) t += fred[w];
+      fred[0] = t;
+    }
+    __syncthreads();
+    const float lse_k = mx + logf(fred[0] + (float)need * expf(xk - mx));
+    if (act >= 0) {
+      const unsigned ka = okey(lg(act) * it);
+      const bool in = ka > kth || (ka == kth && sc[2] < need);
+      lp = in ? lg(act) * it - lse_k : -INFINITY;
+    }
+  }
+  const int em = a.emit_map ? a.emit_map[i] : -1;
+  if (em >= 0 && a.logits_out)
+    for (int v = tid; v < V; v += kThreads) a.logits_out[((size_t)em * a.B + bg) * V + v] = lg(v);
+  if (tid == 0) {
+    const size_t o = (size_t)bg * a.n + i;
+    if (a.logp) a.logp[o] = lp;
+    if (a.logp_full) a.logp_full[o] = lp_full;
+    if (a.argmax) a.argmax[o] = amax;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_constant__ Args a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Shape& s = a.sh;
+  const Plan& P = a.P;
+  const int CS = P.CS, cols = P.cols;
+  const int r = (int)cluster_rank();
+  const int b0 = (int)(blockIdx.x / CS) * P.Bc;  // first sequence of the cluster
+  const int nbv = min(P.Bc, a.B - b0);           // its sequences
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int d = s.d, hd = s.hd, H = s.H, W = s.W, nh = hd / 16;
+  float* hb = reinterpret_cast<float*>(smem + P.o_h);     // [2][cols][d] residual streams
+  bf16* xb = reinterpret_cast<bf16*>(smem + P.o_x);       // [cols][ldx] local projection input
+  bf16* ob = reinterpret_cast<bf16*>(smem + P.o_ob);      // [cols][ldo] gathered attention output
+  bf16* mb = reinterpret_cast<bf16*>(smem + P.o_mb);      // [cols][ldm] gathered SwiGLU product
+  float* out = reinterpret_cast<float*>(smem + P.o_out);  // [maxT][16][cols] projection outputs
+  float* part = reinterpret_cast<float*>(smem + P.o_part);
+  float* pr = reinterpret_cast<float*>(smem + P.o_pr);    // [npairs][3][hd] q, k, v of the pairs
+  float* pw = reinterpret_cast<float*>(smem + P.o_pw);    // [kWarps][W] window weights
+  float* xp = reinterpret_cast<float*>(smem + P.o_xp);    // [units][hd + 2] cross-attention partials
+  unsigned char* misc = smem + P.o_misc;
+  unsigned char* stage = smem + P.o_stage;
+  const Work wk = work_of(P, r, nbv);
+  const bool scorer = r < nbv;
+
+  // zero operands and streams (padding rows and columns stay zero), s -> h buffer 1
+  for (size_t i = tid; i < P.o_stage / 16; i += kThreads) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  for (int i = tid; i < nbv * d; i += kThreads) hb[(size_t)cols * d + i] = a.s[(size_t)b0 * d + i];
+  cluster_sync();  // no CTA pushes into one that is still zeroing
+
+  // L2 prefetch of the memory rows the cross-attention of (layer l, position p) reads
+  auto prefetch_mem = [&](int l, int p) {
+    const int g = s.G == 1 ? 0 : l;
+    const unsigned bytes = (unsigned)(p + 1) * hd * 2;
+    for (int j = tid; j < 2 * wk.npairs; j += kThreads) {
+      const int pi = j >> 1, kv = j & 1;
+      const int b = wk.blo + pi / wk.hpc, h = wk.hlo + pi % wk.hpc;
+      prefetch_l2(a.mem + ((((size_t)g * 2 + kv) * a.B + b0 + b) * H + h) * (size_t)a.T_mem * hd, bytes);
+    }
+  };
+  auto push_f = [&](float* p, float v) {
+    for (int rk = 0; rk < CS; ++rk) *map_rank(p, (unsigned)rk) = v;
+  };
+  auto push_b = [&](bf16* p, float v) {
+    const bf16 q = __float2bfloat16_rn(v);
+    for (int rk = 0; rk < CS; ++rk) *map_rank(p, (unsigned)rk) = q;
+  };
+  auto rmsnorm_x = [&](const float* h, const float* g) {  // xb = bf16(RMSNorm(h) g)
+    for (int b = warp; b < nbv; b += kWarps) {
+      const float* hr = h + (size_t)b * d;
+      float ss = 0.f;
+      for (int j = lane; j < d; j += 32) ss = fmaf(hr[j], hr[j], ss);
+      ss = warp_sum(ss);
+      const float rv = 1.0f / sqrtf(ss / (float)d + a.eps);
+      for (int j = lane; j < d; j += 32) xb[(size_t)b * P.ldx + j] = __float2bfloat16_rn(hr[j] * rv * g[j]);
+    }
+    __syncthreads();
+  };
+  // residual add of this CTA's d rows (tiles of part_range) and push
+  auto residual = [&](float* h) {
+    int lo, hi;
+    part_range(d / 16, CS, r, &lo, &hi);
+    const int nrow = (hi - lo) * 16;
+    for (int i2 = tid; i2 < nbv * nrow; i2 += kThreads) {
+      const int b = i2 / nrow, rr = i2 - b * nrow, row = lo * 16 + rr;
+      push_f(h + (size_t)b * d + row, h[(size_t)b * d + row] + out[(size_t)rr * cols + b]);
+    }
+  };
+
+  const int PPS = (s.gate ? 1 : 0) + 6 * s.L + (scorer ? 1 : 0);
+  const int NPH = a.n * PPS;
+  auto stage_of = [&](int q) { return stage + (size_t)(q & 1) * P.stage_units * kUnitBytes; };
+  issue(a, phase_at(a, 0, r, wk), r, wk, stage_of(0));
+  cp_async_commit();
+  prefetch_mem(0, a.p0);
+
+  for (int i = 0; i < a.n; ++i) {
+    const int p = a.p0 + i, t = p + 1;
+    float* hcur = hb + (size_t)(i & 1) * cols * d;
+    const float* hprev = hb + (size_t)((i + 1) & 1) * cols * d;
+    if (!s.gate) {  // the gate discards s: h = e_p
+      for (int i2 = tid; i2 < nbv * d; i2 += kThreads) {
+        const int b = i2 / d, j = i2 - b * d;
+        hcur[i2] = __bfloat162float(a.e[((size_t)(b0 + b) * a.T_mem + p) * d + j]);
+      }
+    }
+    for (int k = 0; k < PPS; ++k) {
+      const int q = i * PPS + k;
+      const Ph ph = phase_at(a, k, r, wk);
+      if (q + 1 < NPH) issue(a, phase_at(a, (k + 1) % PPS, r, wk), r, wk, stage_of(q + 1));
+      cp_async_commit();
+      cp_async_wait1();
+      __syncthreads();
+      const unsigned char* stg = stage_of(q);
+      const int l = ph.l;
+      switch (ph.kind) {
+        case kGate: {
+          for (int i2 = tid; i2 < nbv * 2 * d; i2 += kThreads) {
+            const int b = i2 / (2 * d), k2 = i2 - b * 2 * d;
+            xb[(size_t)b * P.ldx + k2] = k2 < d ? a.e[((size_t)(b0 + b) * a.T_mem + p) * d + k2]
+                                                 : __float2bfloat16_rn(hprev[(size_t)b * d + k2 - d]);
+          }
+          __syncthreads();
+          proj(ph, cols, stg, xb, P.ldx, out, part);
+          int lo, hi;
+          part_range(d / 16, CS, r, &lo, &hi);
+          const int nrow = (hi - lo) * 16;
+          for (int i2 = tid; i2 < nbv * nrow; i2 += kThreads) {
+            const int b = i2 / nrow, rr = i2 - b * nrow, row = lo * 16 + rr;
+            const float z = sigmoid_f(out[(size_t)rr * cols + b] + a.b_g[row]);
+            const float ev = __bfloat162float(a.e[((size_t)(b0 + b) * a.T_mem + p) * d + row]);
+            push_f(hcur + (size_t)b * d + row, z * hprev[(size_t)b * d + row] + (1.f - z) * ev);
+          }
+          cluster_sync();
+          break;
+        }
+        case kQKV: {
+          rmsnorm_x(hcur, a.attn_norm + (size_t)l * d);
+          if (l + 1 < s.L) prefetch_mem(l + 1, p);
+          else if (i + 1 < a.n) prefetch_mem(0, p + 1);
+          proj(ph, cols, stg, xb, P.ldx, out, part);
+          // RoPE of q and k (rotate-half pairs j, j + hd/2), k and v rounded
+          // to bf16 and written to ring slot p mod W
+          const int half = hd / 2;
+          for (int i2 = tid; i2 < wk.npairs * half; i2 += kThreads) {
+            const int pi = i2 / half, j = i2 - pi * half;
+            const int b = wk.blo + pi / wk.hpc, hh = pi % wk.hpc, h = wk.hlo + hh;
+            auto val = [&](int part3, int e) {
+              const int tt = (hh * 3 + part3) * nh + (e >> 4);
+              return out[(size_t)(tt * 16 + (e & 15)) * cols + b];
+            };
+            const double inv = pow((double)a.theta, -2.0 * (double)j / (double)hd);
+            double sn, cs;
+            sincos((double)p * inv, &sn, &cs);
+            const float cf = (float)cs, sf = (float)sn;
+            const float q1 = val(0, j), q2 = val(0, j + half), k1 = val(1, j), k2 = val(1, j + half);
+            float* pq = pr + (size_t)pi * 3 * hd;
+            pq[j] = q1 * cf - q2 * sf;
+            pq[j + half] = q2 * cf + q1 * sf;
+            const float kr1 = bround(k1 * cf - k2 * sf), kr2 = bround(k2 * cf + k1 * sf);
+            const float v1 = bround(val(2, j)), v2 = bround(val(2, j + half));
+            pq[hd + j] = kr1;
+            pq[hd + j + half] = kr2;
+            pq[2 * hd + j] = v1;
+            pq[2 * hd + j + half] = v2;
+            const size_t ro = ((((size_t)l * a.B + b0 + b) * H + h) * W + p % W) * hd;
+            a.ring_k[ro + j] = __float2bfloat16_rn(kr1);
+            a.ring_k[ro + j + half] = __float2bfloat16_rn(kr2);
+            a.ring_v[ro + j] = __float2bfloat16_rn(v1);
+            a.ring_v[ro + j + half] = __float2bfloat16_rn(v2);
+          }
+          __syncthreads();
+          // window attention over slots 0..min(W, t) - 1, one warp per pair
+          const int nv = min(W, t), cur = p % W;
+          for (int pi = warp; pi < wk.npairs; pi += kWarps) {
+            const int b = wk.blo + pi / wk.hpc, h = wk.hlo + pi % wk.hpc;
+            const float* qv = pr + (size_t)pi * 3 * hd;
+            const float* kc = qv + hd;
+            const float* vc = qv + 2 * hd;
+            const size_t rb = (((size_t)l * a.B + b0 + b) * H + h) * W * hd;
+            float* pwv = pw + (size_t)warp * W;
+            float mx = -INFINITY;
+            for (int j = lane; j < nv; j += 32) {
+              float dot = 0.f;
+              if (j == cur) {
+                for (int e = 0; e < hd; ++e) dot = fmaf(qv[e], kc[e], dot);
+              } else {
+                for (int e = 0; e < hd; e += 8) {
+                  float kv[8];
+                  unpack8(ld_cg16(a.ring_k + rb + (size_t)j * hd + e), kv);
+#pragma unroll
+                  for (int u = 0; u < 8; ++u) dot = fmaf(qv[e + u], kv[u], dot);
+                }
+              }
+              dot *= a.scale;
+              pwv[j] = dot;
+              mx = fmaxf(mx, dot);
+            }
+            mx = warp_max(mx);
+            float sum = 0.f;
+            for (int j = lane; j < nv; j += 32) {
+              const float ex = expf(pwv[j] - mx);
+              pwv[j] = ex;
+              sum += ex;
+            }
+            sum = warp_sum(sum);
+            __syncwarp();
+            const float inv = 1.0f / sum;
+            for (int e = lane; e < hd; e += 32) {
+              float acc = 0.f;
+              for (int j = 0; j < nv; ++j) {
+                const float vv = j == cur ? vc[e] : __bfloat162float(ld_cg_bf16(a.ring_v + rb + (size_t)j * hd + e));
+                acc = fmaf(pwv[j], vv, acc);
+              }
+              push_b(ob + (size_t)b * P.ldo + h * hd + e, acc * inv);
+            }
+            __syncwarp();
+          }
+          cluster_sync();
+          break;
+        }
+        case kO:
+        case kOx:
+          proj(ph, cols, stg, ob, P.ldo, out, part);
+          residual(hcur);
+          cluster_sync();
+          break;
+        case kQx: {
+          rmsnorm_x(hcur, a.xattn_norm + (size_t)l * d);
+          proj(ph, cols, stg, xb, P.ldx, out, part);
+          for (int i2 = tid; i2 < wk.npairs * hd; i2 += kThreads) {
+            const int pi = i2 / hd, e = i2 - pi * hd;
+            const int b = wk.blo + pi / wk.hpc, hh = pi % wk.hpc;
+            const int tt = hh * nh + (e >> 4);
+            pr[(size_t)pi * 3 * hd + e] = out[(size_t)(tt * 16 + (e & 15)) * cols + b] * (a.scale * kLog2e);
+          }
+          __syncthreads();
+          // cross-attention over memory positions 0..p; each pair's keys are
+          // split over ns warps, CH lanes per key row (8 elements a lane),
+          // an online softmax per row group in log2 units
+          const int g = s.G == 1 ? 0 : l;
+          const int ns = wk.npairs >= kWarps ? 1 : kWarps / max(wk.npairs, 1);
+          const int CH = hd / 8, RPW = 32 / CH, rg = lane / CH, cc = lane - rg * CH;
+          for (int w0 = warp; w0 < wk.npairs * ns; w0 += kWarps) {
+            const int pi = w0 / ns, sp = w0 - pi * ns;
+            const int b = wk.blo + pi / wk.hpc, h = wk.hlo + pi % wk.hpc;
+            const size_t plane = (size_t)a.T_mem * hd;
+            const bf16* Kp = a.mem + (((size_t)g * 2 * a.B + b0 + b) * H + h) * plane;
+            const bf16* Vp = a.mem + ((((size_t)g * 2 + 1) * a.B + b0 + b) * H + h) * plane;
+            const int ka = sp * t / ns, kb = (sp + 1) * t / ns;
+            float qv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) qv[u] = pr[(size_t)pi * 3 * hd + 8 * cc + u];
+            float m = -INFINITY, ls = 0.f, acc[8] = {};
+            for (int j0 = ka; j0 < kb; j0 += 4 * RPW) {
+              uint4 kk[4], vv[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * RPW + rg;
+                if (j < kb) {
+                  kk[u] = ld_nc16(Kp + (size_t)j * hd + 8 * cc);
+                  vv[u] = ld_nc16(Vp + (size_t)j * hd + 8 * cc);
+                } else {
+                  kk[u] = make_uint4(0, 0, 0, 0);
+                  vv[u] = make_uint4(0, 0, 0, 0);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * RPW + rg;
+                float kf[8];
+                unpack8(kk[u], kf);
+                float dot = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dot = fmaf(qv[e], kf[e], dot);
+                for (int o = 1; o < CH; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                if (j < kb) {
+                  const float mn = fmaxf(m, dot);
+                  const float corr = exp2f(m - mn), pj = exp2f(dot - mn);
+                  float vf[8];
+                  unpack8(vv[u], vf);
+                  ls = ls * corr + pj;
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) acc[e] = fmaf(pj, vf[e], acc[e] * corr);
+                  m = mn;
+                }
+              }
+            }
+            for (int o = CH; o < 32; o <<= 1) {  // merge the row groups of the warp
+              const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, ls, o);
+              float a2[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) a2[e] = __shfl_xor_sync(0xffffffffu, acc[e], o);
+              const float mn = fmaxf(m, m2);
+              const float c1 = m == -INFINITY ? 0.f : exp2f(m - mn), c2 = m2 == -INFINITY ? 0.f : exp2f(m2 - mn);
+              ls = ls * c1 + l2 * c2;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[e] = acc[e] * c1 + a2[e] * c2;
+              m = mn;
+            }
+            float* xw = xp + (size_t)w0 * (hd + 2);
+            if (rg == 0) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) xw[8 * cc + e] = acc[e];
+            }
+            if (lane == 0) {
+              xw[hd] = m;
+              xw[hd + 1] = ls;
+            }
+          }
+          __syncthreads();
+          for (int i2 = tid; i2 < wk.npairs * hd; i2 += kThreads) {  // splits combined in order
+            const int pi = i2 / hd, e = i2 - pi * hd;
+            const int b = wk.blo + pi / wk.hpc, h = wk.hlo + pi % wk.hpc;
+            float M = -INFINITY;
+            for (int sp = 0; sp < ns; ++sp) {
+              const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
+              if (xw[hd + 1] > 0.f) M = fmaxf(M, xw[hd]);
+            }
+            float num = 0.f, den = 0.f;
+            for (int sp = 0; sp < ns; ++sp) {
+              const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
+              if (xw[hd + 1] > 0.f) {
+                const float cf = exp2f(xw[hd] - M);
+                num = fmaf(xw[e], cf, num);
+                den = fmaf(xw[hd + 1], cf, den);
+              }
+            }
+            push_b(ob + (size_t)b * P.ldo + h * hd + e, num / den);
+          }
+          cluster_sync();
+          break;
+        }
+        case kW13: {
+          rmsnorm_x(hcur, a.ffn_norm + (size_t)l * d);
+          proj(ph, cols, stg, xb, P.ldx, out, part);
+          int lo, hi;
+          part_range(cdivi(s.f, 16), CS, r, &lo, &hi);
+          const int nrow = (hi - lo) * 16;
+          for (int i2 = tid; i2 < nbv * nrow; i2 += kThreads) {
+            const int b = i2 / nrow, rr = i2 - b * nrow, row = lo * 16 + rr;
+            if (row >= s.f) continue;
+            const int pi = rr >> 4, w = rr & 15;
+            const float gv = out[(size_t)((2 * pi) * 16 + w) * cols + b];
+            const float uv = out[(size_t)((2 * pi + 1) * 16 + w) * cols + b];
+            push_b(mb + (size_t)b * P.ldm + row, silu_f(gv) * uv);
+          }
+          cluster_sync();
+          break;
+        }
+        case kW2:
+          proj(ph, cols, stg, mb, P.ldm, out, part);
+          residual(hcur);
+          cluster_sync();
+          break;
+        default: {  // head
+          rmsnorm_x(hcur, a.head_norm);
+          proj(ph, cols, stg, xb, P.ldx, out, part);
+          for (int b = r; b < nbv; b += CS) score_col(a, out, cols, b, b0 + b, i, misc);
+          break;
+        }
+      }
+    }
+  }
+  cp_async_wait0();
+  // s_n: the last step's streams
+  if (r == 0) {
+    const float* hl = hb + (size_t)((a.n - 1) & 1) * cols * d;
+    for (int i = tid; i < nbv * d; i += kThreads) a.s[(size_t)b0 * d + i] = hl[i];
+  }
+  cluster_sync();  // no CTA leaves while another may still address its shared memory
+}
+
+}  // namespace fused
+}  // namespace rlt

@@ -1,0 +1,135 @@
+// Plan of the persistent cluster decoder (dec_fused.cuh): which CTA of a
+// thread-block cluster computes which rows of every projection and which
+// (sequence, head) pairs of the two attentions, and the layout of its
+// shared memory.  Plain C++ (no CUDA types): the library's host code and the
+// host emulation of the kernel share it.
+//
+// One cluster of CS CTAs advances Bc sequences through all n steps of a
+// decode call.  Every CTA keeps the cluster's residual streams h [Bc][d]
+// (fp32) in its own shared memory; a projection is split by output rows
+// (16-row tiles) across the CTAs, each CTA pushes the rows it produced into
+// every CTA's copy (distributed shared memory), and a cluster barrier ends
+// the phase.  The self- and cross-attention queries of a head are produced
+// by the CTAs that attend with that head, so attention needs no exchange
+// before it.  The weights of the next phase stream from L2 into a
+// double-buffered stage while the current phase runs.
+#pragma once
+#include <stddef.h>
+
+#ifdef __CUDACC__
+#define RLT_HD __host__ __device__
+#else
+#define RLT_HD
+#endif
+
+namespace rlt {
+namespace fused {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCols = 16;          // sequences per cluster: two 8-column MMA tiles
+constexpr int kUnitBytes = 1024;      // one staged weight unit: 16 rows x 32 columns, bf16
+constexpr size_t kMaxSmem = 232448;   // dynamic shared memory per CTA (227 KB)
+
+// phase kinds, in step order
+enum Kind { kGate = 0, kQKV, kO, kQx, kOx, kW13, kW2, kHead };
+
+struct Shape {
+  int d, H, hd, f, L, W, V, G;
+  int gate;  // 1: learned merge gate; 0: the gate discards s (h = e)
+};
+
+struct Plan {
+  int CS;      // CTAs per cluster
+  int Bc;      // sequences per cluster (the last cluster may hold fewer)
+  int nclu;    // clusters
+  int cols;    // MMA columns: Bc rounded up to 8
+  int hpc;     // heads per CTA
+  int gph;     // CTAs per head (their sequence groups split the cluster's sequences)
+  int nseq;    // most sequences a CTA attends for
+  int npairs;  // most (sequence, head) pairs of a CTA
+  int ldx, ldo, ldm;  // row pitches (elements) of the bf16 operand buffers
+  int maxT;           // most 16-row tiles of one phase on one CTA
+  int stage_units;    // units of one stage buffer
+  size_t o_h, o_x, o_ob, o_mb, o_out, o_part, o_pr, o_pw, o_xp, o_misc, o_stage, total;
+};
+
+RLT_HD inline int cdivi(int a, int b) { return (a + b - 1) / b; }
+RLT_HD inline int round32(int k) { return (k + 31) / 32 * 32; }
+inline size_t al128(size_t x) { return (x + 127) / 128 * 128; }
+
+// Rows of a d- or f-row projection taken by CTA r: tiles [lo, hi) of nt.
+RLT_HD inline void part_range(int nt, int CS, int r, int* lo, int* hi) {
+  *lo = (int)((long long)r * nt / CS);
+  *hi = (int)((long long)(r + 1) * nt / CS);
+}
+inline int part_max(int nt, int CS) { return cdivi(nt, CS); }
+
+// Returns 0 and fills P when the kernel supports the shape with CS CTAs per
+// cluster and Bc sequences per cluster, -1 otherwise.
+inline int make_plan(const Shape& s, int B, int CS, int Bc, Plan* P) {
+  if (CS < 1 || CS > 16 || Bc < 1 || Bc > kMaxCols || B < 1) return -1;
+  if (s.d % 32 || s.hd % 16 || s.hd > 128 || s.f % 8 || s.H * s.hd != s.d || s.W < 1 || s.V < 1 || s.L < 1)
+    return -1;
+  if (!(s.hd == 16 || s.hd == 32 || s.hd == 64 || s.hd == 128)) return -1;  // lanes per key row: hd / 8
+  if (!(CS % s.H == 0 || s.H % CS == 0)) return -1;
+  Plan p{};
+  p.CS = CS;
+  p.Bc = Bc;
+  p.nclu = cdivi(B, Bc);
+  p.cols = cdivi(Bc, 8) * 8;
+  if (CS >= s.H) {
+    p.hpc = 1;
+    p.gph = CS / s.H;
+    p.nseq = cdivi(Bc, p.gph);
+  } else {
+    p.hpc = s.H / CS;
+    p.gph = 0;
+    p.nseq = Bc;
+  }
+  p.npairs = p.nseq * p.hpc;
+  const int Kx = round32(s.gate ? 2 * s.d : s.d);
+  p.ldx = Kx + 8;
+  p.ldo = round32(s.d) + 8;
+  p.ldm = round32(s.f) + 8;
+  const int td = part_max(s.d / 16, CS), tf = part_max(cdivi(s.f, 16), CS), th = p.hpc * (s.hd / 16);
+  const int tv = cdivi(s.V, 16);
+  const int Ud = round32(s.d) / 32, Uf = round32(s.f) / 32, U2 = round32(2 * s.d) / 32;
+  int maxT = 3 * th, units = 3 * th * Ud;
+  auto take = [&](int t, int u) {
+    if (t > maxT) maxT = t;
+    if (t * u > units) units = t * u;
+  };
+  if (s.gate) take(td, U2);
+  take(td, Ud);       // O, Ox
+  take(th, Ud);       // Qx
+  take(2 * tf, Ud);   // W_1 / W_3 pairs
+  take(td, Uf);       // W_2
+  take(tv, Ud);       // head
+  p.maxT = maxT;
+  p.stage_units = units;
+  size_t off = 0;
+  auto put = [&](size_t bytes) {
+    size_t o = off;
+    off = al128(off + bytes);
+    return o;
+  };
+  p.o_h = put((size_t)2 * p.cols * s.d * 4);
+  p.o_x = put((size_t)p.cols * p.ldx * 2);
+  p.o_ob = put((size_t)p.cols * p.ldo * 2);
+  p.o_mb = put((size_t)p.cols * p.ldm * 2);
+  p.o_out = put((size_t)maxT * 16 * p.cols * 4);
+  p.o_part = put((size_t)kWarps * 2 * 32 * 4 * 4);
+  p.o_pr = put((size_t)p.npairs * 3 * s.hd * 4);
+  p.o_pw = put((size_t)kWarps * s.W * 4);
+  p.o_xp = put((size_t)(p.npairs > kWarps ? p.npairs : kWarps) * (s.hd + 2) * 4);  // cross-attention partials
+  p.o_misc = put(2048);
+  p.o_stage = put((size_t)2 * units * kUnitBytes);
+  p.total = off;
+  if (p.total > kMaxSmem) return -1;
+  *P = p;
+  return 0;
+}
+
+}  // namespace fused
+}  // namespace rlt

@@ -34,10 +34,19 @@ struct EmuWarp {
   float f[32];
   int i[32];
   unsigned u[32];
+  unsigned ma[32][4], mb[32][2];  // warp-level MMA operands
 };
-inline std::vector<EmuWarp>* emu_warps = nullptr;
-inline std::barrier<>* emu_block_bar = nullptr;
+// the calling thread's block: its warps, block barrier and dynamic shared
+// memory; with cluster launches also its rank, the cluster barrier and every
+// block's shared memory
+inline thread_local std::vector<EmuWarp>* emu_warps = nullptr;
+inline thread_local std::barrier<>* emu_block_bar = nullptr;
+inline thread_local char* emu_tl_smem = nullptr;
+inline thread_local unsigned emu_rank = 0;
+inline thread_local std::barrier<>* emu_cluster_bar = nullptr;
+inline thread_local char* const* emu_cluster_smem = nullptr;
 inline std::vector<char> emu_dyn;
+#define __align__(n) alignas(n)
 
 #define __global__
 #define __device__
@@ -99,7 +108,7 @@ inline void sincos(double a, double* s, double* c) { *s = std::sin(a); *c = std:
 using std::min;
 using std::max;
 
-template <class T> T* emu_dyn_smem() { return reinterpret_cast<T*>(emu_dyn.data()); }
+template <class T> T* emu_dyn_smem() { return reinterpret_cast<T*>(emu_tl_smem); }
 
 // A pool of persistent host threads, one per CUDA thread slot of a block;
 // run(n, f) calls f(t) on threads t < n and returns when all of them are done.
@@ -147,7 +156,7 @@ struct EmuPool {
   }
 };
 inline EmuPool& emu_pool() {
-  static EmuPool pool(1024);
+  static EmuPool pool(2048);
   return pool;
 }
 
@@ -167,9 +176,10 @@ void emu_launch(dim3 grid, dim3 block, size_t smem, F kernel, A... args) {
         for (unsigned w = 0; w < nw; ++w)
           warps[w].bar = std::make_unique<std::barrier<>>(std::min(32u, nthr - 32 * w));
         std::barrier<> bb(nthr);
-        emu_warps = &warps;
-        emu_block_bar = &bb;
         emu_pool().run(nthr, [&](unsigned t) {
+          emu_warps = &warps;
+          emu_block_bar = &bb;
+          emu_tl_smem = emu_dyn.data();
           threadIdx = dim3(t % block.x, (t / block.x) % block.y, t / (block.x * block.y));
           blockIdx = dim3(bx, by, bz);
           emu_lane = t % 32;
@@ -181,9 +191,54 @@ void emu_launch(dim3 grid, dim3 block, size_t smem, F kernel, A... args) {
       }
 }
 
+// Runs kernel(args...) over a 1-D grid of clusters of CS blocks: clusters
+// one after another, the blocks of a cluster concurrently, each with its own
+// dynamic shared memory (filled with 0xff bytes, NaN as floats, so that a
+// read of memory the kernel did not initialise shows).
+template <class F, class... A>
+void emu_launch_cluster(dim3 grid, dim3 block, size_t smem, unsigned CS, F kernel, A... args) {
+  gridDim = grid;
+  blockDim = block;
+  const unsigned nthr = block.x * block.y * block.z;
+  const unsigned nw = (nthr + 31) / 32;
+  std::vector<std::vector<char>> bufs(CS, std::vector<char>(smem + 16));
+  std::vector<char*> bases(CS);
+  for (unsigned c = 0; c < CS; ++c) bases[c] = bufs[c].data();
+  for (unsigned cl = 0; cl < grid.x / CS; ++cl) {
+    for (auto& b : bufs) std::fill(b.begin(), b.end(), (char)0xff);
+    std::vector<std::vector<EmuWarp>> warps(CS);
+    std::vector<std::unique_ptr<std::barrier<>>> bbs;
+    for (unsigned c = 0; c < CS; ++c) {
+      warps[c] = std::vector<EmuWarp>(nw);
+      for (unsigned w = 0; w < nw; ++w)
+        warps[c][w].bar = std::make_unique<std::barrier<>>(std::min(32u, nthr - 32 * w));
+      bbs.push_back(std::make_unique<std::barrier<>>(nthr));
+    }
+    std::barrier<> cb(CS * nthr);
+    emu_pool().run(CS * nthr, [&](unsigned tt) {
+      const unsigned rk = tt / nthr, t = tt % nthr;
+      emu_warps = &warps[rk];
+      emu_block_bar = bbs[rk].get();
+      emu_tl_smem = bases[rk];
+      emu_rank = rk;
+      emu_cluster_bar = &cb;
+      emu_cluster_smem = bases.data();
+      threadIdx = dim3(t % block.x, (t / block.x) % block.y, t / (block.x * block.y));
+      blockIdx = dim3(cl * CS + rk, 0, 0);
+      emu_lane = t % 32;
+      emu_warp = t / 32;
+      kernel(args...);
+      (*emu_warps)[emu_warp].bar->arrive_and_drop();
+      emu_block_bar->arrive_and_drop();
+      emu_cluster_bar->arrive_and_drop();
+    });
+  }
+}
+
 struct float2 { float x, y; };
 struct float4 { float x, y, z, w; };
 struct uint2 { unsigned x, y; };
 struct uint4 { unsigned x, y, z, w; };
+inline uint4 make_uint4(unsigned a, unsigned b, unsigned c, unsigned d) { return uint4{a, b, c, d}; }
 inline float2 make_float2(float a, float b) { return float2{a, b}; }
 inline float4 make_float4(float a, float b, float c, float d) { return float4{a, b, c, d}; }

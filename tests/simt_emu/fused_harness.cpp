@@ -1,0 +1,65 @@
+// Runs the persistent cluster decoder (dec_fused_kernel) under the host
+// emulation of emu.h: the library's plan (fused_plan.h), grid, block, cluster
+// size and shared-memory layout, with the PTX operations of fused_ptx.cuh
+// replaced by this directory's stand-ins.  The generated input
+// dec_fused_emu.cuh comes from the test (dec_fused.cuh with its dynamic
+// shared array taken from the emulator).  Test infrastructure only.
+#include "emu.h"
+#include "cuda_bf16.h"
+#include <vector>
+#include "dec_fused_emu.cuh"
+
+using namespace rlt;
+
+static std::vector<bf16> tob(const float* x, size_t n) {
+  std::vector<bf16> v(n);
+  for (size_t i = 0; i < n; ++i) v[i] = __float2bfloat16_rn(x[i]);
+  return v;
+}
+
+// sh: B, T_mem, d, H, hd, f, L, W, V, G, gate, p0, n, top_k, CS, Bc
+// fp: eps, theta, temperature
+// P:  W_g, W_qkv, W_O, W_Qx, W_Ox, W_1, W_3, W_2, W_o (f32 values, stored as bf16),
+//     b_g, attn_norm, xattn_norm, ffn_norm, head_norm (f32),
+//     e [B][T_mem][d], mem [G][2][B][H][T_mem][hd] (f32 values, stored as bf16),
+//     s [B][d] f32 (in/out), ring_k, ring_v [L][B][H][W][hd] (f32 values in/out, stored as bf16),
+//     actions [B][n] i32 or null, emit_map [n] i32 or null, logits_out f32 or null,
+//     logp, logp_full f32 [B][n], argmax i32 [B][n], status i32 [1]
+// Returns the plan's status (-1: shape not supported), else 0.
+extern "C" int fused_emu(const int* sh, const float* fp, void** P) {
+  fused::Shape S{sh[2], sh[3], sh[4], sh[5], sh[6], sh[7], sh[8], sh[9], sh[10]};
+  const int B = sh[0], T_mem = sh[1], CS = sh[14], Bc = sh[15];
+  fused::Plan plan;
+  if (fused::make_plan(S, B, CS, Bc, &plan)) return -1;
+  const size_t d = S.d, f = S.f, L = S.L, V = S.V, H = S.H, hd = S.hd, G = S.G, W = S.W;
+  const size_t dd = d * d;
+  auto wb = [&](int i, size_t n) { return tob((const float*)P[i], n); };
+  std::vector<bf16> Wg = wb(0, 2 * dd), Wqkv = wb(1, L * 3 * dd), WO = wb(2, L * dd), WQx = wb(3, L * dd),
+                    WOx = wb(4, L * dd), W1 = wb(5, L * f * d), W3 = wb(6, L * f * d), W2 = wb(7, L * f * d),
+                    Wo = wb(8, V * d);
+  std::vector<bf16> e = wb(14, (size_t)B * T_mem * d), mem = wb(15, G * 2 * B * H * T_mem * hd);
+  const size_t ring_n = L * B * H * W * hd;
+  std::vector<bf16> rk = wb(17, ring_n), rv = wb(18, ring_n);
+  fused::Args a{};
+  a.W_g = Wg.data(); a.W_qkv = Wqkv.data(); a.W_O = WO.data(); a.W_Qx = WQx.data(); a.W_Ox = WOx.data();
+  a.W_1 = W1.data(); a.W_3 = W3.data(); a.W_2 = W2.data(); a.W_o = Wo.data();
+  a.b_g = (const float*)P[9]; a.attn_norm = (const float*)P[10]; a.xattn_norm = (const float*)P[11];
+  a.ffn_norm = (const float*)P[12]; a.head_norm = (const float*)P[13];
+  a.e = e.data(); a.mem = mem.data();
+  a.s = (float*)P[16]; a.ring_k = rk.data(); a.ring_v = rv.data();
+  a.actions = (const int*)P[19]; a.emit_map = (const int*)P[20]; a.logits_out = (float*)P[21];
+  a.logp = (float*)P[22]; a.logp_full = (float*)P[23]; a.argmax = (int*)P[24]; a.status = (int*)P[25];
+  a.B = B; a.T_mem = T_mem; a.p0 = sh[11]; a.n = sh[12]; a.top_k = sh[13];
+  a.eps = fp[0]; a.theta = fp[1]; a.scale = 1.0f / std::sqrt((float)hd); a.inv_temp = 1.0f / fp[2];
+  a.sh = S;
+  a.P = plan;
+  emu_launch_cluster(dim3(plan.nclu * CS), dim3(fused::kThreads), plan.total, (unsigned)CS, fused::dec_fused_kernel,
+                     a);
+  float* rko = (float*)P[17];
+  float* rvo = (float*)P[18];
+  for (size_t i = 0; i < ring_n; ++i) {
+    rko[i] = __bfloat162float(rk[i]);
+    rvo[i] = __bfloat162float(rv[i]);
+  }
+  return 0;
+}

@@ -1,0 +1,168 @@
+"""The persistent cluster decoder (dec_fused_kernel: every step of a decode
+call in one launch, one thread-block cluster per group of sequences) run
+under the host emulation of the CUDA execution model (tests/simt_emu),
+against the oracle's decode_steps on bf16 models.
+
+The kernel is compiled with g++ against stand-in CUDA headers: one host
+thread per CUDA thread, the blocks of a cluster concurrently with their own
+shared memory (filled with NaN bytes before the launch), cluster barriers,
+distributed shared memory as addresses into the other blocks' buffers, and
+the warp-level bf16 MMA computed from its documented fragment layout.  The
+launch uses the library's plan (fused_plan.h): cluster size, sequences per
+cluster, row split of every projection, shared-memory layout.  This checks
+the kernel's work split, exchanges and index arithmetic without a GPU; the
+GPU tests check the same kernel on the device.
+"""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import rlt_inputs as ri
+from oracle import rlt_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "recurrent_looped_transformer_rlt_b300", "csrc")
+EMU = os.path.join(ROOT, "tests", "simt_emu")
+MATS = ["W_g", "W_qkv", "W_O", "W_Qx", "W_Ox", "W_1", "W_3", "W_2", "W_o"]
+VECS = ["b_g", "dec_attn_norm", "dec_xattn_norm", "dec_ffn_norm", "head_norm"]
+
+
+@pytest.fixture(scope="module")
+def fz(tmp_path_factory):
+    cxx = shutil.which("g++")
+    if cxx is None:
+        pytest.skip("g++ not available")
+    d = str(tmp_path_factory.mktemp("fused_emu"))
+    src = open(os.path.join(CSRC, "dec_fused.cuh")).read()
+    src, n = re.subn(r"extern __shared__ __align__\(128\) unsigned char (\w+)\[\];",
+                     r"unsigned char* \1 = emu_dyn_smem<unsigned char>();", src)
+    assert n == 1
+    open(os.path.join(d, "dec_fused_emu.cuh"), "w").write(src)
+    lib = os.path.join(d, "libfused.so")
+    # the emulator's directory first: its fused_ptx.cuh stands in for the library's
+    r = subprocess.run([cxx, "-std=c++20", "-O1", "-shared", "-fPIC", "-pthread", "-I", d, "-I", EMU, "-I", CSRC,
+                        "-o", lib, os.path.join(EMU, "fused_harness.cpp")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
+    h = ctypes.CDLL(lib)
+    h.fused_emu.restype = ctypes.c_int
+    return h
+
+
+def _call(h, c, W, e, mem, s, rk, rv, acts, p0, n, CS, Bc, tau=1.0, k=0, emit=()):
+    B, T = e.shape[:2]
+    sh = [B, T, c.d, c.n_heads, c.head_dim, c.d_ffn, c.n_layers, c.window, c.vocab, c.mem_groups,
+          1 if c.gate_mode == 0 else 0, p0, n, k, CS, Bc]
+    keep = []
+
+    def f32(x):
+        a = np.ascontiguousarray(np.asarray(x, np.float32))
+        keep.append(a)
+        return a.ctypes.data
+
+    s, rk, rv = np.array(s, np.float32), rk.copy(), rv.copy()
+    a = np.ascontiguousarray(acts[:, p0:p0 + n], np.int32)
+    emap = np.full(n, -1, np.int32)
+    for j, i in enumerate(emit):
+        emap[i] = j
+    lg = np.zeros((max(len(emit), 1), B, c.vocab), np.float32)
+    lp, lf = np.zeros((B, n), np.float32), np.zeros((B, n), np.float32)
+    am, status = np.zeros((B, n), np.int32), np.zeros(1, np.int32)
+    ptr = [f32(W[p]) for p in MATS] + [f32(W[p]) for p in VECS] + [f32(e), f32(mem)]
+    ptr += [s.ctypes.data, rk.ctypes.data, rv.ctypes.data, a.ctypes.data, emap.ctypes.data, lg.ctypes.data,
+            lp.ctypes.data, lf.ctypes.data, am.ctypes.data, status.ctypes.data]
+    rc = h.fused_emu((ctypes.c_int * 16)(*sh), (ctypes.c_float * 3)(c.rms_eps, c.rope_theta, tau),
+                     (ctypes.c_void_p * len(ptr))(*ptr))
+    assert rc == 0, "plan rejected the shape"
+    assert status[0] == 0
+    return dict(s=s, rk=rk, rv=rv, logp=lp, logp_full=lf, argmax=am, logits=lg[:len(emit)])
+
+
+def _case(h, CS, Bc, B=5, T=8, d=64, H=2, hd=32, f=96, L=2, window=3, G=2, V=40, gate_mode=0, tau=1.0, k=0,
+          split=(), emit=(), seed=5):
+    c = ri.RLTConfig(d=d, n_layers=L, n_heads=H, head_dim=hd, d_ffn=f, window=window, mem_groups=G, vocab=V,
+                     dtype="bf16", gate_mode=gate_mode)
+    W = ri.make_weights(c, seed, norm_jitter=0.1)
+    e, mem = ri.make_decoder_inputs(c, B, T, seed + 4, mem_scale=0.5)
+    acts = (np.arange(B * T).reshape(B, T) * 7 % V).astype(np.int32)
+    acts[0, 1] = -1                                   # an unscored step
+    cfg = O.Cfg.of(c)
+    st0 = O.init_state(cfg, W, B)
+    rk = np.full((L, B, H, window, hd), np.nan, np.float32)
+    s, rv = st0.s, rk.copy()
+    cuts = [0] + list(split) + [T]
+    outs = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        o = _call(h, c, W, e, mem, s, rk, rv, acts, a, b - a, CS, Bc, tau, k, [i - a for i in emit if a <= i < b])
+        s, rk, rv = o["s"], o["rk"], o["rv"]
+        outs.append(o)
+    got = dict(s=s, rk=rk, rv=rv, **{key: np.concatenate([o[key] for o in outs], 1)
+                                       for key in ("logp", "logp_full", "argmax")})
+    got["logits"] = np.concatenate([o["logits"] for o in outs], 0) if emit else None
+    ref_st, ref = O.decode_steps(cfg, W, st0, e, mem, T, acts, tau, k, emit=emit)
+    return c, got, ref_st, ref
+
+
+def _check(c, got, ref_st, ref, T):
+    # bf16 model: the same values rounded at the same points; a rounding that
+    # lands on the other side of a bf16 boundary moves a stored value by one
+    # bf16 step (2^-8 relative), which is all the difference there is
+    assert np.abs(got["s"] - ref_st.s).max() <= 2e-3 * np.abs(ref_st.s).max()
+    fin = np.isfinite(ref.logp)
+    assert np.array_equal(np.isfinite(got["logp"]), fin)
+    assert np.isnan(got["logp"][0, 1]) and np.isnan(got["logp_full"][0, 1])
+    assert np.nanmax(np.abs(got["logp"][fin] - ref.logp[fin])) <= 2e-3 * max(1.0, np.abs(ref.logp[fin]).max())
+    assert np.nanmax(np.abs(got["logp_full"] - ref.logp_full)) <= 2e-3 * max(1.0, np.nanmax(np.abs(ref.logp_full)))
+    assert (got["argmax"] == ref.argmax).mean() >= 0.99
+    for l in range(c.n_layers):  # the ring holds the window's keys (after RoPE) and values
+        ents = ref_st.cache[l]
+        for j, (kk, vv) in enumerate(ents):
+            p = T - len(ents) + j
+            assert np.abs(got["rk"][l, :, :, p % c.window] - kk).max() <= 1e-2 * max(1.0, np.abs(kk).max())
+            assert np.abs(got["rv"][l, :, :, p % c.window] - vv).max() <= 1e-2 * max(1.0, np.abs(vv).max())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(CS=2, Bc=3),                                 # two CTAs per head, ragged last cluster
+    dict(CS=4, Bc=8, B=11),                           # four CTAs per head: d rows split 1:1
+    dict(CS=2, Bc=16, B=17),                          # two 8-column MMA tiles
+    dict(CS=1, Bc=5),                                 # one CTA: no exchange
+    dict(CS=2, Bc=4, H=4, hd=16),                     # two heads per CTA
+    dict(CS=4, Bc=4, H=4, hd=16, gate_mode=1),        # the gate discards s: h = e
+    dict(CS=2, Bc=5, k=7, tau=0.7),                   # tempered top-k scoring
+    dict(CS=2, Bc=3, window=1),                       # the window holds the current token only
+    dict(CS=2, Bc=3, G=1, window=5, T=11),            # one memory group; the ring wraps
+    dict(CS=4, Bc=2, d=128, hd=64, f=200, V=70),      # 64-wide heads, ragged f and V tiles
+    dict(CS=2, Bc=5, split=(3, 4), emit=(0, 5)),      # three calls, logits of two steps
+])
+def test_fused_decoder_matches_the_oracle(fz, kw):
+    c, got, ref_st, ref = _case(fz, **kw)
+    _check(c, got, ref_st, ref, kw.get("T", 8))
+    for j, i in enumerate(kw.get("emit", ())):
+        assert np.abs(got["logits"][j] - ref.logits[i]).max() <= 2e-3 * max(1.0, np.abs(ref.logits[i]).max())
+
+
+def test_fused_decoder_call_split_is_bitwise(fz):
+    """Proposition 3.1 for this path: splitting the n steps across calls gives
+    bit-identical states, caches and scores."""
+    _, a, _, _ = _case(fz, CS=2, Bc=5)
+    _, b, _, _ = _case(fz, CS=2, Bc=5, split=(3, 4))
+    for key in ("s", "rk", "rv", "logp", "logp_full", "argmax"):
+        assert np.array_equal(a[key], b[key], equal_nan=True), key
+
+
+def test_plan_rejects_unsupported_shapes(fz):
+    c = ri.RLTConfig(d=64, n_layers=1, n_heads=2, head_dim=32, d_ffn=96, window=3, mem_groups=1, vocab=40,
+                     dtype="bf16")
+    W = ri.make_weights(c, 5)
+    e, mem = ri.make_decoder_inputs(c, 2, 4, 9)
+    st = O.init_state(O.Cfg.of(c), W, 2)
+    rk = np.zeros((1, 2, 2, 3, 32), np.float32)
+    acts = np.zeros((2, 4), np.int32)
+    for CS, Bc in ((3, 2), (2, 17), (32, 2)):  # cluster not a multiple or divisor of H; > 16 columns; > 16 CTAs
+        with pytest.raises(AssertionError, match="plan rejected"):
+            _call(fz, c, W, e, mem, st.s, rk, rk, acts, 0, 4, CS, Bc)
