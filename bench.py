@@ -246,6 +246,7 @@ def run_gpu(args, rank, world, local_rank):
     W = ri.make_weights(c, wl.seed)
     tok, prompt, acts = rank_inputs(wl, rank)
     model = rlt.Model(c, W, device=dev)
+    model.set_decode_path(args.decode_path)
     stream = torch.cuda.current_stream()
     buf = runner.alloc_buffers(model, B, T)
     tok_d = torch.from_numpy(tok).to(dev)
@@ -298,7 +299,8 @@ def run_gpu(args, rank, world, local_rank):
     # programmatic overlap, so the instrumented step runs slower than the
     # timed ones)
     kernel_ms = []
-    if args.kernel_class:
+    fused = args.decode_path == "fused"
+    if args.kernel_class and not fused:  # the per-launch timers instrument the graph path's step
         model.timer_arm(args.kernel_class, min(T * c.n_layers, 1 << 18))  # one launch per layer and step
         flush.fill_(1.0)
         step(tok_d, acts_d)
@@ -308,7 +310,7 @@ def run_gpu(args, rank, world, local_rank):
     # projections dominate the small workload's step time); a failure here
     # only drops the extra object
     proj_ms = []
-    if args.kernel_class and c.dtype == "bf16" and float(np.mean(times)) < 2.0:
+    if args.kernel_class and not fused and c.dtype == "bf16" and float(np.mean(times)) < 2.0:
         try:
             model.timer_arm("gemm", min(T * (6 * c.n_layers + 2), 1 << 18))
             flush.fill_(1.0)
@@ -386,6 +388,21 @@ def kernel_roofline(wl, kernel_ms, kernel_class, bw, peak, src):
             "frac": round(ach / bw, 4), "traffic": traffic, "kernel": "dec_xattn (partial + combine)",
             "launches": len(kernel_ms), "avg_us": round(1e3 * float(np.mean(kernel_ms)), 2),
             "peak_source": src, "durations": "CUDA events around every launch of one extra step after the timed steps"}
+
+
+def fused_roofline(wl, t_dec, bw, src):
+    """Roofline object of the persistent decoder kernel: one launch runs the
+    whole decode call, so its algorithmic bytes are every step's (weights,
+    memory K/V of positions 1..t, window, state) and its duration is the
+    decode part of the timed step (CUDA events after the encoder and after
+    the decode call)."""
+    c, B, T = wl.cfg, wl.B, wl.T
+    byts = sum(step_bytes(c, B, t) for t in range(1, T + 1))
+    ach = byts / t_dec
+    return {"bound": "hbm", "achieved": round(ach / 1e9, 1), "peak": round(bw / 1e9, 1), "unit": "GB/s",
+            "frac": round(ach / bw, 4), "traffic": None, "kernel": "dec_fused (all steps of the call)",
+            "launches": 1, "avg_us": round(1e6 * t_dec, 2), "peak_source": src,
+            "durations": "CUDA events around the decode call inside the timed steps"}
 
 
 def projection_bytes(c, B):
@@ -681,6 +698,8 @@ def main():
     ap.add_argument("--workload", default="small", choices=sorted(ri.PRESETS))
     ap.add_argument("--kernel-class", default="xattn", choices=["xattn", ""])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-path", default="graph", choices=["graph", "fused"],
+                    help="decoder path of rlt_decode_steps: the per-step graph or the persistent cluster kernel")
     ap.add_argument("--profile-case", default="", choices=["", "xattn", "swa", "proj", "glu", "generate", "bptt"],
                     help="time one kernel of the workload (profiler captures), generation, or the decoder's "
                          "backpropagation through time, instead of the bench step")
@@ -724,7 +743,9 @@ def main():
             "encode_ms": round(1e3 * r["t_enc"], 3),
             "decode_roofline_ms": round(1e3 * roof_s, 3),
             "decode_roofline_frac": round(roof_s / (r["t_step"] - r["t_enc"]), 4),
-            "roofline": kernel_roofline(wl, r["kernel_ms"], args.kernel_class, bw, peak, src),
+            "roofline": (fused_roofline(wl, r["t_step"] - r["t_enc"], bw, src) if args.decode_path == "fused"
+                         else kernel_roofline(wl, r["kernel_ms"], args.kernel_class, bw, peak, src)),
+            "decode_path": args.decode_path,
             "e2e": {"value": round(n_tok / r["t_e2e"], 1), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": int(r["launches"]),

@@ -184,6 +184,39 @@ RLT_API int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, c
                      const int32_t* emit_steps, int32_t n_emit, float* logits,
                      void* ws, size_t ws_bytes, rlt_stream_t stream);
 
+/* Decoder path of rlt_decode_steps.
+ *  RLT_DECODE_GRAPH  one step is captured as a CUDA graph of per-operation
+ *                    kernels (tensor-core projections with split-K clusters,
+ *                    attention, norms, head) and replayed n times.  Every
+ *                    configuration.
+ *  RLT_DECODE_FUSED  one persistent launch runs all n steps: one thread-block
+ *                    cluster per group of at most 16 sequences, the
+ *                    projections split by rows across the cluster's CTAs and
+ *                    exchanged through distributed shared memory, the next
+ *                    phase's weights streamed from L2 while the current one
+ *                    computes.  bf16 models whose per-CTA working set fits in
+ *                    shared memory (small widths); rlt_decode_steps returns
+ *                    RLT_EUNSUPPORTED otherwise.  The same values are
+ *                    stored in bf16 as on the graph path; sums run in
+ *                    another order, so the two paths agree to rounding, not
+ *                    bitwise.  Splitting n across calls is bit-identical
+ *                    within this path.
+ *  RLT_DECODE_AUTO   the graph path.
+ * cluster_size 0 lets the fused path choose per call (the largest of
+ * 16, 8, 4, 2, 1 whose clusters all fit on the device at once); 1, 2, 4, 8 or
+ * 16 forces it.  Host-side setting of the model object; not thread-safe with
+ * concurrent calls on the same model. */
+enum { RLT_DECODE_AUTO = 0, RLT_DECODE_GRAPH = 1, RLT_DECODE_FUSED = 2 };
+RLT_API int rlt_set_decode_path(rlt_model* m, int32_t path, int32_t cluster_size);
+
+/* The fused path's plan for B sequences: CTAs per cluster, sequences per
+ * cluster, clusters, and dynamic shared memory per CTA.  RLT_EUNSUPPORTED
+ * when the fused path does not take this model (fp32 models, widths whose
+ * working set exceeds shared memory, head counts that are neither a multiple
+ * nor a divisor of the cluster size).  Any output pointer may be NULL. */
+RLT_API int rlt_fused_plan(const rlt_model* m, int32_t B, int32_t* cluster_size, int32_t* seqs_per_cluster,
+                           int32_t* clusters, int32_t* smem_bytes);
+
 /* Cross-attention of one decoder layer (the step that reads encoder memory),
  * as a standalone call: for every sequence b and head h,
  *   out[b][h*hd + i] = sum_{j < t} softmax_j(q[b][h] . K[b][h][j] / sqrt(hd)) V[b][h][j][i]

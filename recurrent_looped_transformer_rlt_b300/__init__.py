@@ -106,6 +106,9 @@ _bptt_workspace_size = _sig("rlt_bptt_workspace_size", ctypes.c_int,
 _bptt = _sig("rlt_bptt", ctypes.c_int,
              [_p, _p, _p, _i32, _i32, _i32, _p, ctypes.c_float, _i32, _i32, _i32, _p, _p,
               ctypes.POINTER(rlt_grads), _p, _p, _p, ctypes.c_size_t, _p])
+_set_decode_path = _sig("rlt_set_decode_path", ctypes.c_int, [_p, _i32, _i32])
+_fused_plan = _sig("rlt_fused_plan", ctypes.c_int, [_p, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32),
+                                                   ctypes.POINTER(_i32), ctypes.POINTER(_i32)])
 _timer_arm = _sig("rlt_timer_arm", ctypes.c_int, [_p, _i32, _i32])
 _timer_read = _sig("rlt_timer_read", ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_float), _i32, ctypes.POINTER(_i32)])
 _strerror = _sig("rlt_strerror", ctypes.c_char_p, [ctypes.c_int])
@@ -117,7 +120,9 @@ EXPORTED = ["rlt_model_create", "rlt_model_set_version", "rlt_model_destroy", "r
             "rlt_status", "rlt_strerror", "rlt_launch_count", "rlt_abi_version", "rlt_timer_arm",
             "rlt_timer_read", "rlt_cross_attention", "rlt_cross_attention_noalloc", "rlt_linear",
             "rlt_snapshot_size", "rlt_snapshot_save", "rlt_snapshot_restore", "rlt_encode_kv", "rlt_generate",
-            "rlt_bptt_workspace_size", "rlt_bptt"]
+            "rlt_bptt_workspace_size", "rlt_bptt", "rlt_set_decode_path", "rlt_fused_plan"]
+RLT_DECODE_AUTO, RLT_DECODE_GRAPH, RLT_DECODE_FUSED = 0, 1, 2
+DECODE_PATHS = {"auto": RLT_DECODE_AUTO, "graph": RLT_DECODE_GRAPH, "fused": RLT_DECODE_FUSED}
 RLT_TIMER_CLASSES = {"off": 0, "xattn": 1, "swa": 2, "gemm": 3, "head": 4, "step": 5}
 
 
@@ -301,6 +306,21 @@ def rlt_bptt(model: int, e, mem, T_mem: int, B: int, n: int, actions, temperatur
     return rc
 
 
+def rlt_set_decode_path(model: int, path: int, cluster_size: int = 0):
+    _check(_set_decode_path(model, path, cluster_size), "rlt_set_decode_path")
+
+
+def rlt_fused_plan(model: int, B: int):
+    """(cluster_size, seqs_per_cluster, clusters, smem_bytes), or None when the
+    fused decoder path does not take this model."""
+    out = [_i32() for _ in range(4)]
+    rc = _fused_plan(model, B, *[ctypes.byref(x) for x in out])
+    if rc == RLT_EUNSUPPORTED:
+        return None
+    _check(rc, "rlt_fused_plan")
+    return tuple(x.value for x in out)
+
+
 def rlt_timer_arm(model: int, kernel_class: int, max_launches: int):
     _check(_timer_arm(model, kernel_class, max_launches), "rlt_timer_arm")
 
@@ -346,6 +366,13 @@ class Model:
     def set_version(self, v: int):
         rlt_model_set_version(self.handle, v)
         self.version = v
+
+    def set_decode_path(self, path: str, cluster_size: int = 0):
+        """'graph', 'fused' or 'auto' (rlt_set_decode_path)."""
+        rlt_set_decode_path(self.handle, DECODE_PATHS[path], cluster_size)
+
+    def fused_plan(self, B: int):
+        return rlt_fused_plan(self.handle, B)
 
     def timer_arm(self, kernel_class: str, max_launches: int) -> bool:
         rlt_timer_arm(self.handle, RLT_TIMER_CLASSES[kernel_class], max_launches)

@@ -22,6 +22,7 @@
 #include "kernels.cuh"
 #include "attn_enc.cuh"
 #include "xattn.cuh"
+#include "dec_fused.cuh"
 
 using namespace rlt;
 
@@ -81,6 +82,10 @@ struct rlt_model {
   // co-resident clusters of the deep projection kernels, [config][cluster
   // size] (size 1: CTAs), measured on the device at creation
   int gemm_maxc[4][9];
+  // decoder path of rlt_decode_steps (RLT_DECODE_*) and the cluster size of
+  // the persistent path (0: chosen per call)
+  int decode_path;
+  int fused_cs;
 };
 
 // ---------------------------------------------------------------------------
@@ -1405,6 +1410,137 @@ int decode_impl(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const i
   return RLT_OK;
 }
 
+// ---------------------------------------------------------------------------
+// persistent cluster decoder (dec_fused.cuh)
+
+fused::Shape fused_shape(const rlt_config& c) {
+  return fused::Shape{c.d_model, c.n_heads, c.head_dim, c.d_ffn, c.n_layers, c.window, c.vocab, c.mem_groups,
+                      c.gate_mode == RLT_GATE_DISCARD_S ? 0 : 1};
+}
+
+// Clusters of CS CTAs with smem bytes each that the device holds at once.
+int fused_max_clusters(int CS, size_t smem) {
+  if (cudaFuncSetAttribute(fused::dec_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(fused::dec_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CS);
+  cfg.blockDim = dim3(fused::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CS;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fused::dec_fused_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return n;
+}
+
+// The plan for B sequences: the largest cluster size (16, 8, 4, 2, 1; or the
+// one set with rlt_set_decode_path) whose clusters of at most 16 sequences
+// all fit on the device at once (one CTA per SM); failing that, the largest
+// that fits at all (its clusters then run in several waves).
+int fused_choose(const rlt_model* m, int B, fused::Plan* out) {
+  if (m->cfg.dtype != RLT_BF16) return RLT_EUNSUPPORTED;
+  const fused::Shape S = fused_shape(m->cfg);
+  const int cands[5] = {16, 8, 4, 2, 1};
+  bool have = false;
+  for (int CS : cands) {
+    if (m->fused_cs > 0 && CS != m->fused_cs) continue;
+    fused::Plan p;
+    if (fused::make_plan(S, B, CS, std::min(B, fused::kMaxCols), &p)) continue;
+    const int mac = fused_max_clusters(CS, p.total);
+    if (mac <= 0) continue;
+    const int Bc = std::min(fused::kMaxCols, (B + mac - 1) / mac);
+    if (fused::make_plan(S, B, CS, Bc, &p)) continue;
+    if (p.nclu <= mac) {
+      *out = p;
+      return RLT_OK;
+    }
+    if (!have) {
+      *out = p;
+      have = true;
+    }
+  }
+  return have ? RLT_OK : RLT_EUNSUPPORTED;
+}
+
+int decode_fused(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const int32_t* emit_steps, void* ws,
+                 cudaStream_t st) {
+  const rlt_config& c = m->cfg;
+  const int B = sst->batch;
+  fused::Plan P;
+  int rc = fused_choose(m, B, &P);
+  if (rc) return rc;
+  if (!aligned16(A.e) || !aligned16(A.mem) || !aligned16(sst->ring_k) || !aligned16(sst->ring_v)) return RLT_EINVAL;
+  WsLayout Lw = layout(m, B, A.T_mem);
+  std::vector<int> emap(A.n, -1);
+  for (int j = 0; j < A.n_emit; ++j) emap[emit_steps[j]] = j;
+  RLT_CUDA_TRY(cudaMemcpyAsync(at<int>(ws, Lw.emit), emap.data(), sizeof(int) * A.n, cudaMemcpyHostToDevice, st));
+  const rlt_weights& w = m->w;
+  fused::Args a = {};
+  a.W_g = static_cast<const bf16*>(w.W_g);
+  a.W_qkv = static_cast<const bf16*>(w.W_qkv);
+  a.W_O = static_cast<const bf16*>(w.W_O);
+  a.W_Qx = static_cast<const bf16*>(w.W_Qx);
+  a.W_Ox = static_cast<const bf16*>(w.W_Ox);
+  a.W_1 = static_cast<const bf16*>(w.W_1);
+  a.W_3 = static_cast<const bf16*>(w.W_3);
+  a.W_2 = static_cast<const bf16*>(w.W_2);
+  a.W_o = static_cast<const bf16*>(w.W_o);
+  a.b_g = w.b_g;
+  a.attn_norm = w.dec_attn_norm;
+  a.xattn_norm = w.dec_xattn_norm;
+  a.ffn_norm = w.dec_ffn_norm;
+  a.head_norm = w.head_norm;
+  a.e = static_cast<const bf16*>(A.e);
+  a.mem = static_cast<const bf16*>(A.mem);
+  a.actions = A.actions;
+  a.emit_map = at<int>(ws, Lw.emit);
+  a.logits_out = A.logits;
+  a.logp = A.logp;
+  a.logp_full = A.logp_full;
+  a.argmax = A.argmax;
+  a.s = sst->s;
+  a.ring_k = static_cast<bf16*>(sst->ring_k);
+  a.ring_v = static_cast<bf16*>(sst->ring_v);
+  a.status = at<int>(ws, Lw.status);
+  a.B = B;
+  a.T_mem = A.T_mem;
+  a.p0 = sst->pos;
+  a.n = A.n;
+  a.top_k = A.top_k;
+  a.eps = c.rms_eps;
+  a.theta = c.rope_theta;
+  a.scale = 1.0f / sqrtf((float)c.head_dim);
+  a.inv_temp = A.inv_temp;
+  a.sh = fused_shape(c);
+  a.P = P;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P.nclu * P.CS);
+  cfg.blockDim = dim3(fused::kThreads);
+  cfg.dynamicSmemBytes = P.total;
+  cfg.stream = st;
+  cudaLaunchAttribute lat[1];
+  lat[0].id = cudaLaunchAttributeClusterDimension;
+  lat[0].val.clusterDim.x = P.CS;
+  lat[0].val.clusterDim.y = 1;
+  lat[0].val.clusterDim.z = 1;
+  cfg.attrs = lat;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fused::dec_fused_kernel, a) != cudaSuccess) return RLT_ECUDA;
+  g_launches++;
+  sst->pos += A.n;
+  return RLT_OK;
+}
+
 int validate_cfg(const rlt_config* c) {
   if (!c) return RLT_EINVAL;
   if (c->d_model <= 0 || c->n_layers <= 0 || c->n_heads <= 0 || c->head_dim <= 0 || c->d_ffn <= 0 ||
@@ -1436,7 +1572,7 @@ int validate_cfg(const rlt_config* c) {
 
 extern "C" {
 
-int rlt_abi_version(void) { return 102; }
+int rlt_abi_version(void) { return 103; }
 
 uint64_t rlt_launch_count(void) { return g_launches.load(); }
 
@@ -1787,8 +1923,33 @@ int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, const voi
   A.logits = logits;
   A.n_emit = n_emit;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (m->decode_path == RLT_DECODE_FUSED) return decode_fused(m, st, A, emit_steps, ws, s);
   if (m->cfg.dtype == RLT_BF16) return decode_impl<bf16>(m, st, A, emit_steps, ws, s);
   return decode_impl<float>(m, st, A, emit_steps, ws, s);
+}
+
+int rlt_set_decode_path(rlt_model* m, int32_t path, int32_t cluster_size) {
+  if (!m) return RLT_EINVAL;
+  if (path != RLT_DECODE_AUTO && path != RLT_DECODE_GRAPH && path != RLT_DECODE_FUSED) return RLT_EINVAL;
+  if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8 &&
+      cluster_size != 16)
+    return RLT_EINVAL;
+  m->decode_path = path;
+  m->fused_cs = cluster_size;
+  return RLT_OK;
+}
+
+int rlt_fused_plan(const rlt_model* m, int32_t B, int32_t* cluster_size, int32_t* seqs_per_cluster,
+                   int32_t* clusters, int32_t* smem_bytes) {
+  if (!m || B <= 0) return RLT_EINVAL;
+  fused::Plan P;
+  const int rc = fused_choose(m, B, &P);
+  if (rc) return rc;
+  if (cluster_size) *cluster_size = P.CS;
+  if (seqs_per_cluster) *seqs_per_cluster = P.Bc;
+  if (clusters) *clusters = P.nclu;
+  if (smem_bytes) *smem_bytes = (int32_t)P.total;
+  return RLT_OK;
 }
 
 int rlt_cross_attention(const rlt_model* m, const float* q, const void* mem_k, const void* mem_v, int32_t B,

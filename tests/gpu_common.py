@@ -12,8 +12,9 @@ BF16_ARGMAX_AGREE = 0.999
 
 
 def gpu_run(wl, W, tok, acts, n_split=None, emit=(), temperature=1.0, top_k=0, gate_mode=None, window=None,
-            return_model=False):
-    """Encode tok and decode all positions on the GPU; returns numpy outputs."""
+            return_model=False, decode_path=None, cluster_size=0):
+    """Encode tok and decode all positions on the GPU; returns numpy outputs.
+    decode_path: None (the library's default), 'graph' or 'fused'."""
     import torch
     import recurrent_looped_transformer_rlt_b300 as rlt
     from recurrent_looped_transformer_rlt_b300 import runner
@@ -23,6 +24,8 @@ def gpu_run(wl, W, tok, acts, n_split=None, emit=(), temperature=1.0, top_k=0, g
                               **({"window": window} if window is not None else {})})
     B, T = tok.shape
     model = rlt.Model(cfg, W)
+    if decode_path:
+        model.set_decode_path(decode_path, cluster_size)
     buf = runner.alloc_buffers(model, B, T)
     runner.encode(model, torch.from_numpy(tok).cuda(), buf)
     st = runner.new_state(model, B)

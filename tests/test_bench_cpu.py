@@ -98,3 +98,18 @@ def test_bptt_byte_and_flop_accounting():
     gemm = 2 * B * params
     attn = 4 * B * c.d * c.n_layers * 2
     assert f1 == 4 * gemm + 3 * attn
+
+
+def test_fused_roofline_counts_every_step_once():
+    """The persistent decoder's roofline object: one launch for the whole
+    decode call, whose algorithmic bytes are the sum of the per-step bytes;
+    at the roofline time (bytes / HBM) the fraction is 1."""
+    wl = ri.preset("small")
+    c, B, T = wl.cfg, wl.B, wl.T
+    total = sum(bench.step_bytes(c, B, t) for t in range(1, T + 1))
+    # the small decode moves ~39 GB: ~0.146 GB at t = T, ~0.008 GB at t = 1, linear in t
+    assert total / 1e9 == pytest.approx((0.008 + 0.146) / 2 * T, rel=0.03)
+    bw = 7.0e12
+    r = bench.fused_roofline(wl, total / bw, bw, "test")
+    assert r["frac"] == pytest.approx(1.0, abs=1e-3) and r["launches"] == 1 and r["bound"] == "hbm"
+    assert bench.fused_roofline(wl, 2 * total / bw, bw, "test")["frac"] == pytest.approx(0.5, abs=1e-3)

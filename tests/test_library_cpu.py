@@ -44,7 +44,7 @@ def test_library_is_built_for_sm_103a():
 
 def test_abi_version_and_strerror():
     import recurrent_looped_transformer_rlt_b300 as rlt
-    assert rlt.rlt_abi_version() == 102
+    assert rlt.rlt_abi_version() == 103
     assert rlt.rlt_strerror(rlt.RLT_ESTALE).startswith("state built")
     assert rlt.rlt_strerror(12345) == "unknown error"
 
