@@ -33,7 +33,9 @@
 // memory rows of the next layer's cross-attention are prefetched into L2.
 // The residual streams of step i live in h buffer i mod 2, so the step's
 // first pushes never land on the buffer another CTA may still be reading for
-// the previous step's head.
+// the previous step's head.  Each CTA keeps the window keys and values of its
+// pairs in shared memory (loaded from the state's ring at the start, written
+// through to it every step).  Exchanges move 16 bytes per store.
 #pragma once
 #include "common.cuh"
 #include "fused_plan.h"
@@ -45,6 +47,7 @@ namespace fused {
 struct Args {
   const bf16 *W_g, *W_qkv, *W_O, *W_Qx, *W_Ox, *W_1, *W_3, *W_2, *W_o;
   const float *b_g, *attn_norm, *xattn_norm, *ffn_norm, *head_norm;
+  const float2* rope;    // [T_mem][hd / 2] (cos, sin) of position p, rows p0 .. p0 + n - 1
   const bf16* e;         // [B][T_mem][d]
   const bf16* mem;       // [G][2][B][H][T_mem][hd]
   const int* actions;    // [B][n] or null
@@ -70,6 +73,13 @@ __device__ __forceinline__ unsigned okey(float x) {  // order-preserving key of 
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ float bround(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ unsigned bf16x2(float lo, float hi) {
+  return (unsigned)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+         ((unsigned)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  return make_uint4(bf16x2(v[0], v[1]), bf16x2(v[2], v[3]), bf16x2(v[4], v[5]), bf16x2(v[6], v[7]));
+}
 __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
   const unsigned w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -192,12 +202,24 @@ __device__ __forceinline__ Tile tile_at(const Args& a, const Ph& ph, int t, int 
 // other's as + {4, 5, 6, 7} (B uses the same pairing).  Rows past N and
 // columns past K are zero.
 __device__ __forceinline__ void issue(const Args& a, const Ph& ph, int r, const Work& wk, unsigned char* stg) {
-  const int total = ph.nt * ph.U * 64;
-  for (int idx = threadIdx.x; idx < total; idx += kThreads) {
-    const int unit = idx >> 6, jj = idx & 63, half = jj >> 5, ln = jj & 31;
-    const int t = unit / ph.U, u = unit - t * ph.U;
-    const Tile T = tile_at(a, ph, t, r, wk);
-    const int row = T.row0 + (ln >> 2) + 8 * half, k = u * 32 + 8 * (ln & 3);
+  // thread t copies piece t % 64 of units t / 64, t / 64 + kThreads / 64, ...
+  const int jj = threadIdx.x & 63, half = jj >> 5, ln = jj & 31;
+  const int rofs = (ln >> 2) + 8 * half, kofs = 8 * (ln & 3);
+  const int nunits = ph.nt * ph.U;
+  constexpr int kStep = kThreads / 64;
+  int t = 0, u = threadIdx.x >> 6;
+  while (u >= ph.U && t < ph.nt) {
+    u -= ph.U;
+    ++t;
+  }
+  Tile T{};
+  int tcur = -1;
+  for (int unit = threadIdx.x >> 6; unit < nunits; unit += kStep) {
+    if (t != tcur) {
+      T = tile_at(a, ph, t, r, wk);
+      tcur = t;
+    }
+    const int row = T.row0 + rofs, k = u * 32 + kofs;
     const bf16* src = T.W;
     int bytes = 0;
     if (row < T.N && k < ph.K) {
@@ -205,6 +227,11 @@ __device__ __forceinline__ void issue(const Args& a, const Ph& ph, int r, const 
       bytes = min(16, (ph.K - k) * 2);
     }
     cp_async16(stg + (size_t)unit * kUnitBytes + half * 512 + ln * 16, src, bytes);
+    u += kStep;
+    while (u >= ph.U) {
+      u -= ph.U;
+      ++t;
+    }
   }
 }
 
@@ -410,6 +437,11 @@ __device__ void score_col(const Args& a, const float* out, int cols, int b, int 
   __syncthreads();
 }
 
+template <class T>
+__device__ __forceinline__ void push(T* p, const T& v, int CS) {  // the same address in every CTA of the cluster
+  for (int rk = 0; rk < CS; ++rk) *map_rank(p, (unsigned)rk) = v;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Shape& s = a.sh;
@@ -419,25 +451,42 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   const int b0 = (int)(blockIdx.x / CS) * P.Bc;  // first sequence of the cluster
   const int nbv = min(P.Bc, a.B - b0);           // its sequences
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int d = s.d, hd = s.hd, H = s.H, W = s.W, nh = hd / 16;
+  const int d = s.d, hd = s.hd, H = s.H, W = s.W, nh = hd / 16, half = hd / 2, hd8 = hd / 8;
   float* hb = reinterpret_cast<float*>(smem + P.o_h);     // [2][cols][d] residual streams
   bf16* xb = reinterpret_cast<bf16*>(smem + P.o_x);       // [cols][ldx] local projection input
   bf16* ob = reinterpret_cast<bf16*>(smem + P.o_ob);      // [cols][ldo] gathered attention output
   bf16* mb = reinterpret_cast<bf16*>(smem + P.o_mb);      // [cols][ldm] gathered SwiGLU product
   float* out = reinterpret_cast<float*>(smem + P.o_out);  // [maxT][16][cols] projection outputs
   float* part = reinterpret_cast<float*>(smem + P.o_part);
-  float* pr = reinterpret_cast<float*>(smem + P.o_pr);    // [npairs][3][hd] q, k, v of the pairs
-  float* pw = reinterpret_cast<float*>(smem + P.o_pw);    // [kWarps][W] window weights
+  float* pr = reinterpret_cast<float*>(smem + P.o_pr);    // [npairs][hd] queries (log2 units)
+  bf16* ringK = reinterpret_cast<bf16*>(smem + P.o_ring); // [L][npairs][W][hd]
+  bf16* ringV = ringK + (size_t)s.L * P.npairs * W * hd;
   float* xp = reinterpret_cast<float*>(smem + P.o_xp);    // [units][hd + 2] cross-attention partials
   unsigned char* misc = smem + P.o_misc;
+  float2* rope_row = reinterpret_cast<float2*>(misc + 1536);  // [hd / 2] this step's (cos, sin)
   unsigned char* stage = smem + P.o_stage;
   const Work wk = work_of(P, r, nbv);
   const bool scorer = r < nbv;
+  const float qscale = a.scale * kLog2e;
+  const int CH = hd8, RPW = 32 / CH, rg = lane / CH, cc = lane - rg * CH;  // attention lanes: CH per key row
+  auto pair_b = [&](int pi) { return wk.blo + pi / wk.hpc; };
+  auto pair_h = [&](int pi) { return wk.hlo + pi % wk.hpc; };
+  auto gring = [&](int l, int pi) {  // the pair's ring rows in the state, [W][hd]
+    return (((size_t)l * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * W * hd;
+  };
 
-  // zero operands and streams (padding rows and columns stay zero), s -> h buffer 1
+  // zero operands and streams (padding rows and columns stay zero); s -> h
+  // buffer 1; the pairs' ring rows -> shared memory
   for (size_t i = tid; i < P.o_stage / 16; i += kThreads) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   for (int i = tid; i < nbv * d; i += kThreads) hb[(size_t)cols * d + i] = a.s[(size_t)b0 * d + i];
+  for (int i = tid; i < s.L * wk.npairs * W * hd8; i += kThreads) {
+    const int c8 = i % hd8, row = i / hd8, slot = row % W, lp = row / W, pi = lp % wk.npairs, l = lp / wk.npairs;
+    const size_t go = gring(l, pi) + (size_t)slot * hd + 8 * c8;
+    const size_t so = (((size_t)l * P.npairs + pi) * W + slot) * hd + 8 * c8;
+    *reinterpret_cast<uint4*>(ringK + so) = ld_cg16(a.ring_k + go);
+    *reinterpret_cast<uint4*>(ringV + so) = ld_cg16(a.ring_v + go);
+  }
   cluster_sync();  // no CTA pushes into one that is still zeroing
 
   // L2 prefetch of the memory rows the cross-attention of (layer l, position p) reads
@@ -446,16 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     const unsigned bytes = (unsigned)(p + 1) * hd * 2;
     for (int j = tid; j < 2 * wk.npairs; j += kThreads) {
       const int pi = j >> 1, kv = j & 1;
-      const int b = wk.blo + pi / wk.hpc, h = wk.hlo + pi % wk.hpc;
-      prefetch_l2(a.mem + ((((size_t)g * 2 + kv) * a.B + b0 + b) * H + h) * (size_t)a.T_mem * hd, bytes);
+      prefetch_l2(a.mem + ((((size_t)g * 2 + kv) * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * (size_t)a.T_mem * hd,
+                  bytes);
     }
-  };
-  auto push_f = [&](float* p, float v) {
-    for (int rk = 0; rk < CS; ++rk) *map_rank(p, (unsigned)rk) = v;
-  };
-  auto push_b = [&](bf16* p, float v) {
-    const bf16 q = __float2bfloat16_rn(v);
-    for (int rk = 0; rk < CS; ++rk) *map_rank(p, (unsigned)rk) = q;
   };
   auto rmsnorm_x = [&](const float* h, const float* g) {  // xb = bf16(RMSNorm(h) g)
     for (int b = warp; b < nbv; b += kWarps) {
@@ -468,15 +510,74 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     }
     __syncthreads();
   };
-  // residual add of this CTA's d rows (tiles of part_range) and push
+  // residual add of this CTA's d rows, four rows per push
   auto residual = [&](float* h) {
     int lo, hi;
     part_range(d / 16, CS, r, &lo, &hi);
-    const int nrow = (hi - lo) * 16;
-    for (int i2 = tid; i2 < nbv * nrow; i2 += kThreads) {
-      const int b = i2 / nrow, rr = i2 - b * nrow, row = lo * 16 + rr;
-      push_f(h + (size_t)b * d + row, h[(size_t)b * d + row] + out[(size_t)rr * cols + b]);
+    const int nq = (hi - lo) * 4;
+    for (int i2 = tid; i2 < nbv * nq; i2 += kThreads) {
+      const int b = i2 / nq, rr = 4 * (i2 - b * nq), row = lo * 16 + rr;
+      float* hp = h + (size_t)b * d + row;
+      const float4 v = make_float4(hp[0] + out[(size_t)rr * cols + b], hp[1] + out[(size_t)(rr + 1) * cols + b],
+                                   hp[2] + out[(size_t)(rr + 2) * cols + b], hp[3] + out[(size_t)(rr + 3) * cols + b]);
+      push(reinterpret_cast<float4*>(hp), v, CS);
     }
+  };
+  // online-softmax attention of one warp's query (8 elements a lane, CH lanes
+  // per key row) over key rows [ka, kb) read by ldk / ldv; merged over the
+  // warp's row groups, the result is in every lane of row group 0
+  struct Acc {
+    float m, l, o[8];
+  };
+  auto attend = [&](const float (&qv)[8], int ka, int kb, auto ldk, auto ldv) {
+    Acc A;
+    A.m = -INFINITY;
+    A.l = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) A.o[e] = 0.f;
+    constexpr int UN = 8;
+    for (int j0 = ka; j0 < kb; j0 += UN * RPW) {
+      uint4 kk[UN], vv[UN];
+#pragma unroll
+      for (int u = 0; u < UN; ++u) {
+        const int j = j0 + u * RPW + rg;
+        kk[u] = j < kb ? ldk(j) : make_uint4(0, 0, 0, 0);
+        vv[u] = j < kb ? ldv(j) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < UN; ++u) {
+        const int j = j0 + u * RPW + rg;
+        float kf[8];
+        unpack8(kk[u], kf);
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dot = fmaf(qv[e], kf[e], dot);
+        for (int o = 1; o < CH; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (j < kb) {
+          const float mn = fmaxf(A.m, dot);
+          const float corr = exp2f(A.m - mn), pj = exp2f(dot - mn);
+          float vf[8];
+          unpack8(vv[u], vf);
+          A.l = A.l * corr + pj;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) A.o[e] = fmaf(pj, vf[e], A.o[e] * corr);
+          A.m = mn;
+        }
+      }
+    }
+    for (int o = CH; o < 32; o <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, A.m, o), l2 = __shfl_xor_sync(0xffffffffu, A.l, o);
+      float a2[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a2[e] = __shfl_xor_sync(0xffffffffu, A.o[e], o);
+      const float mn = fmaxf(A.m, m2);
+      const float c1 = A.m == -INFINITY ? 0.f : exp2f(A.m - mn), c2 = m2 == -INFINITY ? 0.f : exp2f(m2 - mn);
+      A.l = A.l * c1 + l2 * c2;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) A.o[e] = A.o[e] * c1 + a2[e] * c2;
+      A.m = mn;
+    }
+    return A;
   };
 
   const int PPS = (s.gate ? 1 : 0) + 6 * s.L + (scorer ? 1 : 0);
@@ -490,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     const int p = a.p0 + i, t = p + 1;
     float* hcur = hb + (size_t)(i & 1) * cols * d;
     const float* hprev = hb + (size_t)((i + 1) & 1) * cols * d;
+    for (int j = tid; j < half; j += kThreads) rope_row[j] = a.rope[(size_t)p * half + j];
     if (!s.gate) {  // the gate discards s: h = e_p
       for (int i2 = tid; i2 < nbv * d; i2 += kThreads) {
         const int b = i2 / d, j = i2 - b * d;
@@ -516,12 +618,18 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           proj(ph, cols, stg, xb, P.ldx, out, part);
           int lo, hi;
           part_range(d / 16, CS, r, &lo, &hi);
-          const int nrow = (hi - lo) * 16;
-          for (int i2 = tid; i2 < nbv * nrow; i2 += kThreads) {
-            const int b = i2 / nrow, rr = i2 - b * nrow, row = lo * 16 + rr;
-            const float z = sigmoid_f(out[(size_t)rr * cols + b] + a.b_g[row]);
-            const float ev = __bfloat162float(a.e[((size_t)(b0 + b) * a.T_mem + p) * d + row]);
-            push_f(hcur + (size_t)b * d + row, z * hprev[(size_t)b * d + row] + (1.f - z) * ev);
+          const int nq = (hi - lo) * 4;
+          for (int i2 = tid; i2 < nbv * nq; i2 += kThreads) {
+            const int b = i2 / nq, rr = 4 * (i2 - b * nq), row = lo * 16 + rr;
+            const bf16* ep = a.e + ((size_t)(b0 + b) * a.T_mem + p) * d + row;
+            const float* sp = hprev + (size_t)b * d + row;
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float z = sigmoid_f(out[(size_t)(rr + u) * cols + b] + a.b_g[row + u]);
+              v[u] = z * sp[u] + (1.f - z) * __bfloat162float(ep[u]);
+            }
+            push(reinterpret_cast<float4*>(hcur + (size_t)b * d + row), make_float4(v[0], v[1], v[2], v[3]), CS);
           }
           cluster_sync();
           break;
@@ -531,82 +639,53 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           if (l + 1 < s.L) prefetch_mem(l + 1, p);
           else if (i + 1 < a.n) prefetch_mem(0, p + 1);
           proj(ph, cols, stg, xb, P.ldx, out, part);
-          // RoPE of q and k (rotate-half pairs j, j + hd/2), k and v rounded
-          // to bf16 and written to ring slot p mod W
-          const int half = hd / 2;
+          // RoPE of q and k (rotate-half pairs j, j + hd/2); k and v rounded
+          // to bf16 into ring slot p mod W, in shared memory and in the state
+          const int slot = p % W;
           for (int i2 = tid; i2 < wk.npairs * half; i2 += kThreads) {
             const int pi = i2 / half, j = i2 - pi * half;
-            const int b = wk.blo + pi / wk.hpc, hh = pi % wk.hpc, h = wk.hlo + hh;
+            const int b = pair_b(pi), hh = pi % wk.hpc;
             auto val = [&](int part3, int e) {
               const int tt = (hh * 3 + part3) * nh + (e >> 4);
               return out[(size_t)(tt * 16 + (e & 15)) * cols + b];
             };
-            const double inv = pow((double)a.theta, -2.0 * (double)j / (double)hd);
-            double sn, cs;
-            sincos((double)p * inv, &sn, &cs);
-            const float cf = (float)cs, sf = (float)sn;
+            const float cf = rope_row[j].x, sf = rope_row[j].y;
             const float q1 = val(0, j), q2 = val(0, j + half), k1 = val(1, j), k2 = val(1, j + half);
-            float* pq = pr + (size_t)pi * 3 * hd;
-            pq[j] = q1 * cf - q2 * sf;
-            pq[j + half] = q2 * cf + q1 * sf;
-            const float kr1 = bround(k1 * cf - k2 * sf), kr2 = bround(k2 * cf + k1 * sf);
-            const float v1 = bround(val(2, j)), v2 = bround(val(2, j + half));
-            pq[hd + j] = kr1;
-            pq[hd + j + half] = kr2;
-            pq[2 * hd + j] = v1;
-            pq[2 * hd + j + half] = v2;
-            const size_t ro = ((((size_t)l * a.B + b0 + b) * H + h) * W + p % W) * hd;
-            a.ring_k[ro + j] = __float2bfloat16_rn(kr1);
-            a.ring_k[ro + j + half] = __float2bfloat16_rn(kr2);
-            a.ring_v[ro + j] = __float2bfloat16_rn(v1);
-            a.ring_v[ro + j + half] = __float2bfloat16_rn(v2);
+            pr[(size_t)pi * hd + j] = (q1 * cf - q2 * sf) * qscale;
+            pr[(size_t)pi * hd + j + half] = (q2 * cf + q1 * sf) * qscale;
+            const bf16 kr1 = __float2bfloat16_rn(k1 * cf - k2 * sf), kr2 = __float2bfloat16_rn(k2 * cf + k1 * sf);
+            const bf16 v1 = __float2bfloat16_rn(val(2, j)), v2 = __float2bfloat16_rn(val(2, j + half));
+            const size_t so = (((size_t)l * P.npairs + pi) * W + slot) * hd;
+            ringK[so + j] = kr1;
+            ringK[so + j + half] = kr2;
+            ringV[so + j] = v1;
+            ringV[so + j + half] = v2;
+            const size_t go = gring(l, pi) + (size_t)slot * hd;
+            a.ring_k[go + j] = kr1;
+            a.ring_k[go + j + half] = kr2;
+            a.ring_v[go + j] = v1;
+            a.ring_v[go + j + half] = v2;
           }
           __syncthreads();
-          // window attention over slots 0..min(W, t) - 1, one warp per pair
-          const int nv = min(W, t), cur = p % W;
+          // window attention over slots 0..min(W, t) - 1 (softmax does not
+          // depend on their order), one warp per pair
+          const int nv = min(W, t);
           for (int pi = warp; pi < wk.npairs; pi += kWarps) {
-            const int b = wk.blo + pi / wk.hpc, h = wk.hlo + pi % wk.hpc;
-            const float* qv = pr + (size_t)pi * 3 * hd;
-            const float* kc = qv + hd;
-            const float* vc = qv + 2 * hd;
-            const size_t rb = (((size_t)l * a.B + b0 + b) * H + h) * W * hd;
-            float* pwv = pw + (size_t)warp * W;
-            float mx = -INFINITY;
-            for (int j = lane; j < nv; j += 32) {
-              float dot = 0.f;
-              if (j == cur) {
-                for (int e = 0; e < hd; ++e) dot = fmaf(qv[e], kc[e], dot);
-              } else {
-                for (int e = 0; e < hd; e += 8) {
-                  float kv[8];
-                  unpack8(ld_cg16(a.ring_k + rb + (size_t)j * hd + e), kv);
+            const bf16* Ks = ringK + ((size_t)l * P.npairs + pi) * W * hd;
+            const bf16* Vs = ringV + ((size_t)l * P.npairs + pi) * W * hd;
+            float qv[8];
 #pragma unroll
-                  for (int u = 0; u < 8; ++u) dot = fmaf(qv[e + u], kv[u], dot);
-                }
-              }
-              dot *= a.scale;
-              pwv[j] = dot;
-              mx = fmaxf(mx, dot);
+            for (int e = 0; e < 8; ++e) qv[e] = pr[(size_t)pi * hd + 8 * cc + e];
+            const Acc A = attend(
+                qv, 0, nv, [&](int j) { return *reinterpret_cast<const uint4*>(Ks + (size_t)j * hd + 8 * cc); },
+                [&](int j) { return *reinterpret_cast<const uint4*>(Vs + (size_t)j * hd + 8 * cc); });
+            if (rg == 0) {
+              float o[8];
+              const float inv = 1.0f / A.l;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = A.o[e] * inv;
+              push(reinterpret_cast<uint4*>(ob + (size_t)pair_b(pi) * P.ldo + pair_h(pi) * hd + 8 * cc), pack8(o), CS);
             }
-            mx = warp_max(mx);
-            float sum = 0.f;
-            for (int j = lane; j < nv; j += 32) {
-              const float ex = expf(pwv[j] - mx);
-              pwv[j] = ex;
-              sum += ex;
-            }
-            sum = warp_sum(sum);
-            __syncwarp();
-            const float inv = 1.0f / sum;
-            for (int e = lane; e < hd; e += 32) {
-              float acc = 0.f;
-              for (int j = 0; j < nv; ++j) {
-                const float vv = j == cur ? vc[e] : __bfloat162float(ld_cg_bf16(a.ring_v + rb + (size_t)j * hd + e));
-                acc = fmaf(pwv[j], vv, acc);
-              }
-              push_b(ob + (size_t)b * P.ldo + h * hd + e, acc * inv);
-            }
-            __syncwarp();
           }
           cluster_sync();
           break;
@@ -622,103 +701,57 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           proj(ph, cols, stg, xb, P.ldx, out, part);
           for (int i2 = tid; i2 < wk.npairs * hd; i2 += kThreads) {
             const int pi = i2 / hd, e = i2 - pi * hd;
-            const int b = wk.blo + pi / wk.hpc, hh = pi % wk.hpc;
-            const int tt = hh * nh + (e >> 4);
-            pr[(size_t)pi * 3 * hd + e] = out[(size_t)(tt * 16 + (e & 15)) * cols + b] * (a.scale * kLog2e);
+            const int tt = (pi % wk.hpc) * nh + (e >> 4);
+            pr[(size_t)pi * hd + e] = out[(size_t)(tt * 16 + (e & 15)) * cols + pair_b(pi)] * qscale;
           }
           __syncthreads();
-          // cross-attention over memory positions 0..p; each pair's keys are
-          // split over ns warps, CH lanes per key row (8 elements a lane),
-          // an online softmax per row group in log2 units
+          // cross-attention over memory positions 0..p, each pair's keys
+          // split over ns warps; partials combined in split order
           const int g = s.G == 1 ? 0 : l;
           const int ns = wk.npairs >= kWarps ? 1 : kWarps / max(wk.npairs, 1);
-          const int CH = hd / 8, RPW = 32 / CH, rg = lane / CH, cc = lane - rg * CH;
           for (int w0 = warp; w0 < wk.npairs * ns; w0 += kWarps) {
             const int pi = w0 / ns, sp = w0 - pi * ns;
-            const int b = wk.blo + pi / wk.hpc, h = wk.hlo + pi % wk.hpc;
             const size_t plane = (size_t)a.T_mem * hd;
-            const bf16* Kp = a.mem + (((size_t)g * 2 * a.B + b0 + b) * H + h) * plane;
-            const bf16* Vp = a.mem + ((((size_t)g * 2 + 1) * a.B + b0 + b) * H + h) * plane;
-            const int ka = sp * t / ns, kb = (sp + 1) * t / ns;
+            const bf16* Kp = a.mem + (((size_t)g * 2 * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * plane + 8 * cc;
+            const bf16* Vp = a.mem + ((((size_t)g * 2 + 1) * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * plane + 8 * cc;
             float qv[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) qv[u] = pr[(size_t)pi * 3 * hd + 8 * cc + u];
-            float m = -INFINITY, ls = 0.f, acc[8] = {};
-            for (int j0 = ka; j0 < kb; j0 += 4 * RPW) {
-              uint4 kk[4], vv[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int j = j0 + u * RPW + rg;
-                if (j < kb) {
-                  kk[u] = ld_nc16(Kp + (size_t)j * hd + 8 * cc);
-                  vv[u] = ld_nc16(Vp + (size_t)j * hd + 8 * cc);
-                } else {
-                  kk[u] = make_uint4(0, 0, 0, 0);
-                  vv[u] = make_uint4(0, 0, 0, 0);
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int j = j0 + u * RPW + rg;
-                float kf[8];
-                unpack8(kk[u], kf);
-                float dot = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) dot = fmaf(qv[e], kf[e], dot);
-                for (int o = 1; o < CH; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                if (j < kb) {
-                  const float mn = fmaxf(m, dot);
-                  const float corr = exp2f(m - mn), pj = exp2f(dot - mn);
-                  float vf[8];
-                  unpack8(vv[u], vf);
-                  ls = ls * corr + pj;
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) acc[e] = fmaf(pj, vf[e], acc[e] * corr);
-                  m = mn;
-                }
-              }
-            }
-            for (int o = CH; o < 32; o <<= 1) {  // merge the row groups of the warp
-              const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, ls, o);
-              float a2[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) a2[e] = __shfl_xor_sync(0xffffffffu, acc[e], o);
-              const float mn = fmaxf(m, m2);
-              const float c1 = m == -INFINITY ? 0.f : exp2f(m - mn), c2 = m2 == -INFINITY ? 0.f : exp2f(m2 - mn);
-              ls = ls * c1 + l2 * c2;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) acc[e] = acc[e] * c1 + a2[e] * c2;
-              m = mn;
-            }
+            for (int e = 0; e < 8; ++e) qv[e] = pr[(size_t)pi * hd + 8 * cc + e];
+            const Acc A = attend(qv, sp * t / ns, (sp + 1) * t / ns,
+                                 [&](int j) { return ld_nc16(Kp + (size_t)j * hd); },
+                                 [&](int j) { return ld_nc16(Vp + (size_t)j * hd); });
             float* xw = xp + (size_t)w0 * (hd + 2);
             if (rg == 0) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) xw[8 * cc + e] = acc[e];
+              for (int e = 0; e < 8; ++e) xw[8 * cc + e] = A.o[e];
             }
             if (lane == 0) {
-              xw[hd] = m;
-              xw[hd + 1] = ls;
+              xw[hd] = A.m;
+              xw[hd + 1] = A.l;
             }
           }
           __syncthreads();
-          for (int i2 = tid; i2 < wk.npairs * hd; i2 += kThreads) {  // splits combined in order
-            const int pi = i2 / hd, e = i2 - pi * hd;
-            const int b = wk.blo + pi / wk.hpc, h = wk.hlo + pi % wk.hpc;
+          for (int i2 = tid; i2 < wk.npairs * hd8; i2 += kThreads) {
+            const int pi = i2 / hd8, c8 = i2 - pi * hd8;
             float M = -INFINITY;
             for (int sp = 0; sp < ns; ++sp) {
               const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
               if (xw[hd + 1] > 0.f) M = fmaxf(M, xw[hd]);
             }
-            float num = 0.f, den = 0.f;
+            float num[8] = {}, den = 0.f;
             for (int sp = 0; sp < ns; ++sp) {
               const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
               if (xw[hd + 1] > 0.f) {
                 const float cf = exp2f(xw[hd] - M);
-                num = fmaf(xw[e], cf, num);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) num[e] = fmaf(xw[8 * c8 + e], cf, num[e]);
                 den = fmaf(xw[hd + 1], cf, den);
               }
             }
-            push_b(ob + (size_t)b * P.ldo + h * hd + e, num / den);
+            const float inv = 1.0f / den;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) num[e] *= inv;
+            push(reinterpret_cast<uint4*>(ob + (size_t)pair_b(pi) * P.ldo + pair_h(pi) * hd + 8 * c8), pack8(num), CS);
           }
           cluster_sync();
           break;
@@ -728,14 +761,19 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           proj(ph, cols, stg, xb, P.ldx, out, part);
           int lo, hi;
           part_range(cdivi(s.f, 16), CS, r, &lo, &hi);
-          const int nrow = (hi - lo) * 16;
-          for (int i2 = tid; i2 < nbv * nrow; i2 += kThreads) {
-            const int b = i2 / nrow, rr = i2 - b * nrow, row = lo * 16 + rr;
+          const int n8 = (hi - lo) * 2;  // eight rows per push
+          for (int i2 = tid; i2 < nbv * n8; i2 += kThreads) {
+            const int b = i2 / n8, rr = 8 * (i2 - b * n8), row = lo * 16 + rr;
             if (row >= s.f) continue;
             const int pi = rr >> 4, w = rr & 15;
-            const float gv = out[(size_t)((2 * pi) * 16 + w) * cols + b];
-            const float uv = out[(size_t)((2 * pi + 1) * 16 + w) * cols + b];
-            push_b(mb + (size_t)b * P.ldm + row, silu_f(gv) * uv);
+            float m8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float gv = out[(size_t)((2 * pi) * 16 + w + u) * cols + b];
+              const float uv = out[(size_t)((2 * pi + 1) * 16 + w + u) * cols + b];
+              m8[u] = silu_f(gv) * uv;
+            }
+            push(reinterpret_cast<uint4*>(mb + (size_t)b * P.ldm + row), pack8(m8), CS);
           }
           cluster_sync();
           break;

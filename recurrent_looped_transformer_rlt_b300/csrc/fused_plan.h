@@ -6,7 +6,9 @@
 //
 // One cluster of CS CTAs advances Bc sequences through all n steps of a
 // decode call.  Every CTA keeps the cluster's residual streams h [Bc][d]
-// (fp32) in its own shared memory; a projection is split by output rows
+// (fp32) in its own shared memory, and the window keys and values of the
+// (sequence, head) pairs it attends for (the state's ring, written through
+// to global memory every step); a projection is split by output rows
 // (16-row tiles) across the CTAs, each CTA pushes the rows it produced into
 // every CTA's copy (distributed shared memory), and a cluster barrier ends
 // the phase.  The self- and cross-attention queries of a head are produced
@@ -51,7 +53,7 @@ struct Plan {
   int ldx, ldo, ldm;  // row pitches (elements) of the bf16 operand buffers
   int maxT;           // most 16-row tiles of one phase on one CTA
   int stage_units;    // units of one stage buffer
-  size_t o_h, o_x, o_ob, o_mb, o_out, o_part, o_pr, o_pw, o_xp, o_misc, o_stage, total;
+  size_t o_h, o_x, o_ob, o_mb, o_out, o_part, o_pr, o_ring, o_xp, o_misc, o_stage, total;
 };
 
 RLT_HD inline int cdivi(int a, int b) { return (a + b - 1) / b; }
@@ -120,8 +122,8 @@ inline int make_plan(const Shape& s, int B, int CS, int Bc, Plan* P) {
   p.o_mb = put((size_t)p.cols * p.ldm * 2);
   p.o_out = put((size_t)maxT * 16 * p.cols * 4);
   p.o_part = put((size_t)kWarps * 2 * 32 * 4 * 4);
-  p.o_pr = put((size_t)p.npairs * 3 * s.hd * 4);
-  p.o_pw = put((size_t)kWarps * s.W * 4);
+  p.o_pr = put((size_t)p.npairs * s.hd * 4);                        // queries of the pairs
+  p.o_ring = put((size_t)s.L * p.npairs * s.W * s.hd * 2 * 2);       // the pairs' window keys and values
   p.o_xp = put((size_t)(p.npairs > kWarps ? p.npairs : kWarps) * (s.hd + 2) * 4);  // cross-attention partials
   p.o_misc = put(2048);
   p.o_stage = put((size_t)2 * units * kUnitBytes);

@@ -1418,12 +1418,19 @@ fused::Shape fused_shape(const rlt_config& c) {
                       c.gate_mode == RLT_GATE_DISCARD_S ? 0 : 1};
 }
 
-// Clusters of CS CTAs with smem bytes each that the device holds at once.
-int fused_max_clusters(int CS, size_t smem) {
+// The kernel's launch attributes for smem bytes of dynamic shared memory
+// (clusters of up to 16 CTAs are outside the portable size 8).
+int fused_attrs(size_t smem) {
   if (cudaFuncSetAttribute(fused::dec_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(fused::dec_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-    return -1;
+    return RLT_ECUDA;
+  return RLT_OK;
+}
+
+// Clusters of CS CTAs with smem bytes each that the device holds at once.
+int fused_max_clusters(int CS, size_t smem) {
+  if (fused_attrs(smem) != RLT_OK) return -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CS);
   cfg.blockDim = dim3(fused::kThreads);
@@ -1484,8 +1491,14 @@ int decode_fused(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const 
   std::vector<int> emap(A.n, -1);
   for (int j = 0; j < A.n_emit; ++j) emap[emit_steps[j]] = j;
   RLT_CUDA_TRY(cudaMemcpyAsync(at<int>(ws, Lw.emit), emap.data(), sizeof(int) * A.n, cudaMemcpyHostToDevice, st));
+  const int half = c.head_dim / 2;  // RoPE rows of positions p0 .. p0 + n - 1
+  rope_table_kernel<<<cdiv((size_t)A.n * half, 256), 256, 0, st>>>(at<float2>(ws, Lw.rope), sst->pos, A.n, half,
+                                                                   (double)c.rope_theta);
+  g_launches++;
+  if ((rc = launch_ok())) return rc;
   const rlt_weights& w = m->w;
   fused::Args a = {};
+  a.rope = at<const float2>(ws, Lw.rope);
   a.W_g = static_cast<const bf16*>(w.W_g);
   a.W_qkv = static_cast<const bf16*>(w.W_qkv);
   a.W_O = static_cast<const bf16*>(w.W_O);
@@ -1523,6 +1536,7 @@ int decode_fused(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const 
   a.inv_temp = A.inv_temp;
   a.sh = fused_shape(c);
   a.P = P;
+  if ((rc = fused_attrs(P.total))) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P.nclu * P.CS);
   cfg.blockDim = dim3(fused::kThreads);

@@ -24,6 +24,7 @@ inline float __bfloat162float(__nv_bfloat16 b) {
   return f;
 }
 inline __nv_bfloat16 __ushort_as_bfloat16(unsigned short s) { __nv_bfloat16 b; b.x = s; return b; }
+inline unsigned short __bfloat16_as_ushort(__nv_bfloat16 b) { return b.x; }
 
 inline float2 __bfloat1622float2(__nv_bfloat162 v) { return make_float2(__bfloat162float(v.x), __bfloat162float(v.y)); }
 inline __nv_bfloat162 __floats2bfloat162_rn(float a, float b) { return __nv_bfloat162{__float2bfloat16_rn(a), __float2bfloat16_rn(b)}; }

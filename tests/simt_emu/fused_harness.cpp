@@ -45,6 +45,14 @@ extern "C" int fused_emu(const int* sh, const float* fp, void** P) {
   a.W_1 = W1.data(); a.W_3 = W3.data(); a.W_2 = W2.data(); a.W_o = Wo.data();
   a.b_g = (const float*)P[9]; a.attn_norm = (const float*)P[10]; a.xattn_norm = (const float*)P[11];
   a.ffn_norm = (const float*)P[12]; a.head_norm = (const float*)P[13];
+  // (cos, sin) of every position in float from double, as the library's table
+  std::vector<float2> rope((size_t)T_mem * (hd / 2));
+  for (int pp = 0; pp < T_mem; ++pp)
+    for (size_t i = 0; i < hd / 2; ++i) {
+      const double inv = std::pow((double)fp[1], -2.0 * (double)i / (double)hd);
+      rope[pp * (hd / 2) + i] = make_float2((float)std::cos(pp * inv), (float)std::sin(pp * inv));
+    }
+  a.rope = rope.data();
   a.e = e.data(); a.mem = mem.data();
   a.s = (float*)P[16]; a.ring_k = rk.data(); a.ring_v = rv.data();
   a.actions = (const int*)P[19]; a.emit_map = (const int*)P[20]; a.logits_out = (float*)P[21];
