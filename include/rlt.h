@@ -202,9 +202,10 @@ RLT_API int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, c
  *                    bitwise.  Splitting n across calls is bit-identical
  *                    within this path.
  *  RLT_DECODE_AUTO   the graph path.
- * cluster_size 0 lets the fused path choose per call (the largest of
- * 16, 8, 4, 2, 1 whose clusters all fit on the device at once); 1, 2, 4, 8 or
- * 16 forces it.  Host-side setting of the model object; not thread-safe with
+ * cluster_size 0 lets the fused path choose per call among 16, 8, 4, 2, 1
+ * CTAs per cluster: the most sequences per cluster whose working set fits in
+ * shared memory, the fewest waves of clusters the device holds at once, then
+ * the largest cluster; 1, 2, 4, 8 or 16 forces the cluster size.  Host-side setting of the model object; not thread-safe with
  * concurrent calls on the same model. */
 enum { RLT_DECODE_AUTO = 0, RLT_DECODE_GRAPH = 1, RLT_DECODE_FUSED = 2 };
 RLT_API int rlt_set_decode_path(rlt_model* m, int32_t path, int32_t cluster_size);
