@@ -156,7 +156,7 @@ struct EmuPool {
   }
 };
 inline EmuPool& emu_pool() {
-  static EmuPool pool(2048);
+  static EmuPool pool(4096);
   return pool;
 }
 

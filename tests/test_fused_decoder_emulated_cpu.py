@@ -166,3 +166,22 @@ def test_plan_rejects_unsupported_shapes(fz):
     for CS, Bc in ((3, 2), (2, 17), (32, 2)):  # cluster not a multiple or divisor of H; > 16 columns; > 16 CTAs
         with pytest.raises(AssertionError, match="plan rejected"):
             _call(fz, c, W, e, mem, st.s, rk, rk, acts, 0, 4, CS, Bc)
+
+
+def test_fused_decoder_small_workload_plan(fz):
+    """The plan the library picks for the small bf16 model on a B300 (16 CTAs
+    per cluster, 8 sequences per cluster, two CTAs per head, 43 W_1/W_3 tiles
+    over 16 CTAs, a 16-slot window), three steps of one cluster."""
+    c = ri.preset("small").cfg
+    W = ri.make_weights(c, 3, norm_jitter=0.1)
+    B, n = 8, 3
+    e, mem = ri.make_decoder_inputs(c, B, n, 7, mem_scale=0.5)
+    acts = (np.arange(B * n).reshape(B, n) * 5 % c.vocab).astype(np.int32)
+    cfg = O.Cfg.of(c)
+    st0 = O.init_state(cfg, W, B)
+    rk = np.full((c.n_layers, B, c.n_heads, c.window, c.head_dim), np.nan, np.float32)
+    got = _call(fz, c, W, e, mem, st0.s, rk, rk.copy(), acts, 0, n, 16, 8)
+    ref_st, ref = O.decode_steps(cfg, W, st0, e, mem, n, acts)
+    assert np.abs(got["s"] - ref_st.s).max() <= 2e-3 * np.abs(ref_st.s).max()
+    assert np.nanmax(np.abs(got["logp"] - ref.logp)) <= 2e-3 * max(1.0, np.nanmax(np.abs(ref.logp)))
+    assert (got["argmax"] == ref.argmax).mean() >= 0.99
