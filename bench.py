@@ -571,6 +571,68 @@ def run_profile_case(args):
     model.close()
 
 
+def run_fused_case(args):
+    """One rlt_decode_steps call of the persistent cluster decoder over n =
+    --bptt-steps (default 32) steps from the middle of the workload's
+    sequences (the state is brought to position T/2 - n/2 first and restored
+    before each timed call), timed with CUDA events over --steps calls after
+    --warmup; one JSON line with the call's algorithmic bytes and its
+    fraction of HBM bandwidth.  A short single launch for ncu captures."""
+    import torch
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from recurrent_looped_transformer_rlt_b300 import runner
+    wl = ri.preset(args.workload)
+    c, B, T = wl.cfg, wl.B, wl.T
+    n = args.bptt_steps or 32
+    p0 = max(0, T // 2 - n // 2)
+    W = ri.make_weights(c, wl.seed)
+    tok = ri.make_tokens(wl)
+    model = rlt.Model(c, W)
+    model.set_decode_path("fused")
+    plan = model.fused_plan(B)
+    if plan is None:
+        raise SystemExit(f"the fused decoder does not take the {wl.name} model")
+    buf = runner.alloc_buffers(model, B, T)
+    runner.encode(model, torch.from_numpy(tok).cuda(), buf)
+    acts = torch.from_numpy(ri.teacher_actions(tok, 0, T)).cuda()
+    st = runner.new_state(model, B)
+    if p0 > 0:
+        runner.decode(model, st, buf, p0, acts[:, :p0].contiguous())
+    saved = (st.s.clone(), st.ring_k.clone(), st.ring_v.clone())
+    a_n = acts[:, p0:p0 + n].contiguous()
+    out = runner.StepOutputs(torch.empty(B, n, device="cuda"), torch.empty(B, n, device="cuda"),
+                             torch.empty(B, n, dtype=torch.int32, device="cuda"), None)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    ts = []
+    for it in range(args.warmup + args.steps):
+        st.s.copy_(saved[0])
+        st.ring_k.copy_(saved[1])
+        st.ring_v.copy_(saved[2])
+        st.c.pos = p0
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        runner.decode(model, st, buf, n, a_n, wl.temperature, wl.top_k, out=out)
+        e1.record(stream)
+        e1.synchronize()
+        if it >= args.warmup:
+            ts.append(e0.elapsed_time(e1) / 1e3)
+    if runner.status(buf) != 0:
+        raise RuntimeError("device status flag set")
+    bw, _, src = load_peaks()
+    t = float(np.mean(ts))
+    nbytes = sum(step_bytes(c, B, p + 1) for p in range(p0, p0 + n))
+    print(json.dumps({"case": "fused", "workload": wl.name, "kernel": "dec_fused_kernel", "B": B, "p0": p0,
+                      "steps": n, "plan": {"cluster": plan[0], "seqs_per_cluster": plan[1], "clusters": plan[2],
+                                           "smem_bytes": plan[3]},
+                      "us_per_call": round(1e6 * t, 2), "us_per_step": round(1e6 * t / n, 2),
+                      "bytes_per_call": nbytes, "achieved_gbs": round(nbytes / t / 1e9, 1),
+                      "peak_gbs": round(bw / 1e9, 1), "frac": round(nbytes / t / bw, 4), "peak_source": src,
+                      "l2": "flushed before each call"}), flush=True)
+    model.close()
+
+
 def run_bptt_case(args):
     """Backpropagation through time (rlt_bptt) over the first --bptt-steps
     positions of the workload's sequences (encoded on the GPU), full BPTT with
@@ -700,16 +762,22 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-path", default="graph", choices=["graph", "fused"],
                     help="decoder path of rlt_decode_steps: the per-step graph or the persistent cluster kernel")
-    ap.add_argument("--profile-case", default="", choices=["", "xattn", "swa", "proj", "glu", "generate", "bptt"],
-                    help="time one kernel of the workload (profiler captures), generation, or the decoder's "
-                         "backpropagation through time, instead of the bench step")
-    ap.add_argument("--bptt-steps", type=int, default=0, help="steps of the bptt case (default: T / 4)")
+    ap.add_argument("--profile-case", default="",
+                    choices=["", "xattn", "swa", "proj", "glu", "generate", "bptt", "fused"],
+                    help="time one kernel of the workload (profiler captures), generation, the decoder's "
+                         "backpropagation through time, or one call of the persistent decoder, instead of the "
+                         "bench step")
+    ap.add_argument("--bptt-steps", type=int, default=0,
+                    help="steps of the bptt case (default: T / 4) and of the fused case (default: 32)")
     args = ap.parse_args()
     if args.profile_case == "generate":
         run_generate_case(args)
         return
     if args.profile_case == "bptt":
         run_bptt_case(args)
+        return
+    if args.profile_case == "fused":
+        run_fused_case(args)
         return
     if args.profile_case:
         run_profile_case(args)
