@@ -6,6 +6,7 @@
 #pragma once
 #include <atomic>
 #include <barrier>
+#include <semaphore>
 #include <condition_variable>
 #include <mutex>
 #include <cmath>
@@ -110,48 +111,43 @@ using std::max;
 
 template <class T> T* emu_dyn_smem() { return reinterpret_cast<T*>(emu_tl_smem); }
 
-// A pool of persistent host threads, one per CUDA thread slot of a block;
-// run(n, f) calls f(t) on threads t < n and returns when all of them are done.
+// A pool of persistent host threads, one per CUDA thread slot of a block (or
+// of a cluster); run(n, f) calls f(t) on threads t < n and returns when all
+// of them are done.  Only the n threads a launch uses are woken.
 struct EmuPool {
   std::vector<std::thread> th;
+  std::vector<std::unique_ptr<std::binary_semaphore>> go;
   std::mutex mu;
-  std::condition_variable cv, done_cv;
+  std::condition_variable done_cv;
   std::function<void(unsigned)> job;
-  unsigned gen = 0, active = 0, nthr = 0;
+  unsigned active = 0;
   bool stop = false;
   explicit EmuPool(unsigned n) {
+    for (unsigned t = 0; t < n; ++t) go.push_back(std::make_unique<std::binary_semaphore>(0));
     for (unsigned t = 0; t < n; ++t)
       th.emplace_back([this, t]() {
-        unsigned seen = 0;
-        std::unique_lock<std::mutex> lk(mu);
         for (;;) {
-          cv.wait(lk, [&] { return stop || gen != seen; });
+          go[t]->acquire();
           if (stop) return;
-          seen = gen;
-          if (t >= nthr) continue;
-          auto j = job;
-          lk.unlock();
-          j(t);
-          lk.lock();
+          job(t);
+          std::lock_guard<std::mutex> lk(mu);
           if (--active == 0) done_cv.notify_all();
         }
       });
   }
   ~EmuPool() {
-    {
-      std::lock_guard<std::mutex> lk(mu);
-      stop = true;
-    }
-    cv.notify_all();
+    stop = true;
+    for (auto& g : go) g->release();
     for (auto& x : th) x.join();
   }
   void run(unsigned n, std::function<void(unsigned)> f) {
-    std::unique_lock<std::mutex> lk(mu);
     job = std::move(f);
-    nthr = n;
-    active = n;
-    ++gen;
-    cv.notify_all();
+    {
+      std::lock_guard<std::mutex> lk(mu);
+      active = n;
+    }
+    for (unsigned t = 0; t < n; ++t) go[t]->release();
+    std::unique_lock<std::mutex> lk(mu);
     done_cv.wait(lk, [&] { return active == 0; });
   }
 };

@@ -138,3 +138,38 @@ def test_emulated_kernels_bf16(emu):
     for name, x in list(g.items()) + [("e", d_e), ("mem", d_mem)]:
         r = gref[name]
         assert np.linalg.norm((x - r).ravel()) <= 1e-2 * np.linalg.norm(r.ravel()), name
+
+
+@pytest.fixture(scope="module")
+def emu64(tmp_path_factory):
+    """The kernels with the library's own key chunk (64 keys per warp)."""
+    cxx = shutil.which("g++")
+    if cxx is None:
+        pytest.skip("g++ not available")
+    d = str(tmp_path_factory.mktemp("simt_emu64"))
+    _generate(d)
+    lib = os.path.join(d, "libemu.so")
+    r = subprocess.run([cxx, "-std=c++20", "-O2", "-shared", "-fPIC", "-pthread", "-I", d, "-I", EMU, "-I", CSRC,
+                        "-o", lib, os.path.join(EMU, "emu_harness.cpp")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
+    h = ctypes.CDLL(lib)
+    h.bptt_emu.restype = ctypes.c_int
+    return h
+
+
+def test_emulated_kernels_production_chunk(emu64):
+    """67 steps with the library's 64-key chunk: the last steps' memory
+    attention is split in two and combined, the last 16-step block is ragged
+    (67 = 4 x 16 + 3)."""
+    c = ri.RLTConfig(d=64, n_layers=1, n_heads=2, head_dim=32, d_ffn=96, window=16, mem_groups=1, vocab=40,
+                     dtype="f32")
+    W = ri.make_weights(c, 41, norm_jitter=0.1)
+    for k in W:
+        if W[k].ndim >= 2:
+            W[k] = W[k] * 2.0
+    B, T = 1, 67
+    e, mem = ri.make_decoder_inputs(c, B, T, 48, mem_scale=0.5)
+    acts = (np.arange(B * T).reshape(B, T) * 7 % c.vocab).astype(np.int32)
+    loss, g, d_e, d_mem = _run(emu64, c, W, e, mem, acts, block=16)
+    lref, gref = BP.gradients(O.Cfg.of(c), W, e, mem, acts)
+    assert _worst(loss, g, d_e, d_mem, lref, gref) < 1e-4
