@@ -133,5 +133,37 @@ inline int make_plan(const Shape& s, int B, int CS, int Bc, Plan* P) {
   return 0;
 }
 
+// The plan for B sequences: over the cluster sizes 16, 8, 4, 2, 1 (only
+// `force` when it is not 0), the most sequences per cluster (at most 16, at
+// most what spreads B over the clusters the device holds at once) whose
+// working set fits in shared memory; of these the plan with the fewest waves
+// of clusters, then the largest cluster (fewer weight rows per CTA).
+// max_clusters(CS, smem) is the number of clusters of CS CTAs with smem
+// bytes each that the device holds at once (<= 0: none).  Returns 0 and fills
+// P, or -1 when no cluster size takes the shape.
+template <class MaxClusters>
+inline int choose_plan(const Shape& s, int B, int force, MaxClusters max_clusters, Plan* P) {
+  const int cands[5] = {16, 8, 4, 2, 1};
+  int best_waves = 0;
+  for (int CS : cands) {
+    if (force > 0 && CS != force) continue;
+    Plan p;
+    int Bc = B < kMaxCols ? B : kMaxCols;
+    while (Bc > 0 && make_plan(s, B, CS, Bc, &p)) --Bc;
+    if (Bc == 0) continue;
+    const int mac = max_clusters(CS, p.total);  // at the largest Bc: the most shared memory
+    if (mac <= 0) continue;
+    const int spread = (B + mac - 1) / mac;
+    if (spread < Bc) Bc = spread;
+    if (make_plan(s, B, CS, Bc, &p)) continue;
+    const int waves = (p.nclu + mac - 1) / mac;
+    if (best_waves == 0 || waves < best_waves) {
+      *P = p;
+      best_waves = waves;
+    }
+  }
+  return best_waves > 0 ? 0 : -1;
+}
+
 }  // namespace fused
 }  // namespace rlt

@@ -1450,33 +1450,12 @@ int fused_max_clusters(int CS, size_t smem) {
   return n;
 }
 
-// The plan for B sequences: over the cluster sizes 16, 8, 4, 2, 1 (or the one
-// set with rlt_set_decode_path), the most sequences per cluster (at most 16,
-// at most what spreads B over the clusters the device holds at once) whose
-// working set fits in shared memory; of these the plan with the fewest waves
-// of clusters, then the largest cluster (fewer weight rows per CTA).
+// The plan for B sequences (fused::choose_plan) with the device's
+// co-resident clusters.
 int fused_choose(const rlt_model* m, int B, fused::Plan* out) {
   if (m->cfg.dtype != RLT_BF16) return RLT_EUNSUPPORTED;
-  const fused::Shape S = fused_shape(m->cfg);
-  const int cands[5] = {16, 8, 4, 2, 1};
-  int best_waves = 0;
-  for (int CS : cands) {
-    if (m->fused_cs > 0 && CS != m->fused_cs) continue;
-    fused::Plan p;
-    int Bc = std::min(B, fused::kMaxCols);
-    while (Bc > 0 && fused::make_plan(S, B, CS, Bc, &p)) --Bc;
-    if (Bc == 0) continue;  // the shape does not fit this cluster size
-    const int mac = fused_max_clusters(CS, p.total);  // largest accepted Bc: the most shared memory
-    if (mac <= 0) continue;
-    Bc = std::min(Bc, (B + mac - 1) / mac);
-    if (fused::make_plan(S, B, CS, Bc, &p)) continue;
-    const int waves = (p.nclu + mac - 1) / mac;
-    if (best_waves == 0 || waves < best_waves) {
-      *out = p;
-      best_waves = waves;
-    }
-  }
-  return best_waves > 0 ? RLT_OK : RLT_EUNSUPPORTED;
+  const int rc = fused::choose_plan(fused_shape(m->cfg), B, m->fused_cs, fused_max_clusters, out);
+  return rc ? RLT_EUNSUPPORTED : RLT_OK;
 }
 
 int decode_fused(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const int32_t* emit_steps, void* ws,
