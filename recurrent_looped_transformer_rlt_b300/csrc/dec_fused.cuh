@@ -29,8 +29,9 @@
 // Projections run on the tensor cores as warp-level bf16 MMAs with the
 // weights as the 16-row operand and the cluster's sequences as the 8-column
 // operand; the weights of phase q + 1 are copied from L2 into one half of a
-// double-buffered stage while phase q computes from the other half, and the
-// memory rows of the next layer's cross-attention are prefetched into L2.
+// double-buffered stage while phase q computes from the other half (the
+// copy starts once phase q - 1 has read that half), and the memory rows of
+// the next layer's cross-attention are prefetched into L2.
 // The residual streams of step i live in h buffer i mod 2, so the step's
 // first pushes never land on the buffer another CTA may still be reading for
 // the previous step's head.  Each CTA keeps the window keys and values of its
@@ -583,7 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   const int PPS = (s.gate ? 1 : 0) + 6 * s.L + (scorer ? 1 : 0);
   const int NPH = a.n * PPS;
   auto stage_of = [&](int q) { return stage + (size_t)(q & 1) * P.stage_units * kUnitBytes; };
+  // phase q's weights go to stage q mod 2; they are requested right after
+  // phase q - 2's projection has read that half (one cp.async group per
+  // phase), so each copy has most of two phases to land
   issue(a, phase_at(a, 0, r, wk), r, wk, stage_of(0));
+  cp_async_commit();
+  if (NPH > 1) issue(a, phase_at(a, 1 % PPS, r, wk), r, wk, stage_of(1));
   cp_async_commit();
   prefetch_mem(0, a.p0);
 
@@ -601,11 +607,15 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     for (int k = 0; k < PPS; ++k) {
       const int q = i * PPS + k;
       const Ph ph = phase_at(a, k, r, wk);
-      if (q + 1 < NPH) issue(a, phase_at(a, (k + 1) % PPS, r, wk), r, wk, stage_of(q + 1));
-      cp_async_commit();
-      cp_async_wait1();
+      cp_async_wait1();  // this phase's group (the next phase's may still be in flight)
       __syncthreads();
-      const unsigned char* stg = stage_of(q);
+      unsigned char* stg = stage_of(q);
+      // the projection of this phase, then the request of phase q + 2 into the half it has read
+      auto project = [&](const bf16* X, int ldX) {
+        proj(ph, cols, stg, X, ldX, out, part);
+        if (q + 2 < NPH) issue(a, phase_at(a, (k + 2) % PPS, r, wk), r, wk, stg);
+        cp_async_commit();
+      };
       const int l = ph.l;
       switch (ph.kind) {
         case kGate: {
@@ -615,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
                                                  : __float2bfloat16_rn(hprev[(size_t)b * d + k2 - d]);
           }
           __syncthreads();
-          proj(ph, cols, stg, xb, P.ldx, out, part);
+          project(xb, P.ldx);
           int lo, hi;
           part_range(d / 16, CS, r, &lo, &hi);
           const int nq = (hi - lo) * 4;
@@ -638,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           rmsnorm_x(hcur, a.attn_norm + (size_t)l * d);
           if (l + 1 < s.L) prefetch_mem(l + 1, p);
           else if (i + 1 < a.n) prefetch_mem(0, p + 1);
-          proj(ph, cols, stg, xb, P.ldx, out, part);
+          project(xb, P.ldx);
           // RoPE of q and k (rotate-half pairs j, j + hd/2); k and v rounded
           // to bf16 into ring slot p mod W, in shared memory and in the state
           const int slot = p % W;
@@ -692,13 +702,13 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
         }
         case kO:
         case kOx:
-          proj(ph, cols, stg, ob, P.ldo, out, part);
+          project(ob, P.ldo);
           residual(hcur);
           cluster_sync();
           break;
         case kQx: {
           rmsnorm_x(hcur, a.xattn_norm + (size_t)l * d);
-          proj(ph, cols, stg, xb, P.ldx, out, part);
+          project(xb, P.ldx);
           for (int i2 = tid; i2 < wk.npairs * hd; i2 += kThreads) {
             const int pi = i2 / hd, e = i2 - pi * hd;
             const int tt = (pi % wk.hpc) * nh + (e >> 4);
@@ -758,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
         }
         case kW13: {
           rmsnorm_x(hcur, a.ffn_norm + (size_t)l * d);
-          proj(ph, cols, stg, xb, P.ldx, out, part);
+          project(xb, P.ldx);
           int lo, hi;
           part_range(cdivi(s.f, 16), CS, r, &lo, &hi);
           const int n8 = (hi - lo) * 2;  // eight rows per push
@@ -779,13 +789,13 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           break;
         }
         case kW2:
-          proj(ph, cols, stg, mb, P.ldm, out, part);
+          project(mb, P.ldm);
           residual(hcur);
           cluster_sync();
           break;
         default: {  // head
           rmsnorm_x(hcur, a.head_norm);
-          proj(ph, cols, stg, xb, P.ldx, out, part);
+          project(xb, P.ldx);
           for (int b = r; b < nbv; b += CS) score_col(a, out, cols, b, b0 + b, i, misc);
           break;
         }
