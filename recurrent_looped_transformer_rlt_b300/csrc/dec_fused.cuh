@@ -465,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   float* xp = reinterpret_cast<float*>(smem + P.o_xp);    // [units][hd + 2] cross-attention partials
   unsigned char* misc = smem + P.o_misc;
   float2* rope_row = reinterpret_cast<float2*>(misc + 1536);  // [hd / 2] this step's (cos, sin)
+  bf16* eb = reinterpret_cast<bf16*>(smem + P.o_e);       // [2][cols][d] e_p of step i in half i mod 2
   unsigned char* stage = smem + P.o_stage;
   const Work wk = work_of(P, r, nbv);
   const bool scorer = r < nbv;
@@ -581,6 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     return A;
   };
 
+  // e_p of step `step` (p = p0 + step) into its half of eb, in this thread's current cp.async group
+  auto issue_e = [&](int step) {
+    const int p = a.p0 + step, d8 = d / 8;
+    for (int j = tid; j < nbv * d8; j += kThreads) {
+      const int b = j / d8, c8 = j - b * d8;
+      cp_async16(eb + ((size_t)(step & 1) * cols + b) * d + 8 * c8, a.e + ((size_t)(b0 + b) * a.T_mem + p) * d + 8 * c8,
+                 16);
+    }
+  };
   const int PPS = (s.gate ? 1 : 0) + 6 * s.L + (scorer ? 1 : 0);
   const int NPH = a.n * PPS;
   auto stage_of = [&](int q) { return stage + (size_t)(q & 1) * P.stage_units * kUnitBytes; };
@@ -588,6 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   // phase q - 2's projection has read that half (one cp.async group per
   // phase), so each copy has most of two phases to land
   issue(a, phase_at(a, 0, r, wk), r, wk, stage_of(0));
+  issue_e(0);
   cp_async_commit();
   if (NPH > 1) issue(a, phase_at(a, 1 % PPS, r, wk), r, wk, stage_of(1));
   cp_async_commit();
@@ -597,13 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     const int p = a.p0 + i, t = p + 1;
     float* hcur = hb + (size_t)(i & 1) * cols * d;
     const float* hprev = hb + (size_t)((i + 1) & 1) * cols * d;
+    const bf16* ecur = eb + (size_t)(i & 1) * cols * d;  // e_p, rows of the cluster's sequences
     for (int j = tid; j < half; j += kThreads) rope_row[j] = a.rope[(size_t)p * half + j];
-    if (!s.gate) {  // the gate discards s: h = e_p
-      for (int i2 = tid; i2 < nbv * d; i2 += kThreads) {
-        const int b = i2 / d, j = i2 - b * d;
-        hcur[i2] = __bfloat162float(a.e[((size_t)(b0 + b) * a.T_mem + p) * d + j]);
-      }
-    }
     for (int k = 0; k < PPS; ++k) {
       const int q = i * PPS + k;
       const Ph ph = phase_at(a, k, r, wk);
@@ -614,14 +620,19 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
       auto project = [&](const bf16* X, int ldX) {
         proj(ph, cols, stg, X, ldX, out, part);
         if (q + 2 < NPH) issue(a, phase_at(a, (k + 2) % PPS, r, wk), r, wk, stg);
+        if (k == 0 && i + 1 < a.n) issue_e(i + 1);  // e of the next step, landed long before its first phase
         cp_async_commit();
       };
+      if (k == 0 && !s.gate) {  // the gate discards s: h = e_p
+        for (int i2 = tid; i2 < nbv * d; i2 += kThreads) hcur[i2] = __bfloat162float(ecur[i2]);
+        __syncthreads();
+      }
       const int l = ph.l;
       switch (ph.kind) {
         case kGate: {
           for (int i2 = tid; i2 < nbv * 2 * d; i2 += kThreads) {
             const int b = i2 / (2 * d), k2 = i2 - b * 2 * d;
-            xb[(size_t)b * P.ldx + k2] = k2 < d ? a.e[((size_t)(b0 + b) * a.T_mem + p) * d + k2]
+            xb[(size_t)b * P.ldx + k2] = k2 < d ? ecur[(size_t)b * d + k2]
                                                  : __float2bfloat16_rn(hprev[(size_t)b * d + k2 - d]);
           }
           __syncthreads();
@@ -631,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           const int nq = (hi - lo) * 4;
           for (int i2 = tid; i2 < nbv * nq; i2 += kThreads) {
             const int b = i2 / nq, rr = 4 * (i2 - b * nq), row = lo * 16 + rr;
-            const bf16* ep = a.e + ((size_t)(b0 + b) * a.T_mem + p) * d + row;
+            const bf16* ep = ecur + (size_t)b * d + row;
             const float* sp = hprev + (size_t)b * d + row;
             float v[4];
 #pragma unroll

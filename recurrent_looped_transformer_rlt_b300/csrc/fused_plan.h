@@ -53,7 +53,7 @@ struct Plan {
   int ldx, ldo, ldm;  // row pitches (elements) of the bf16 operand buffers
   int maxT;           // most 16-row tiles of one phase on one CTA
   int stage_units;    // units of one stage buffer
-  size_t o_h, o_x, o_ob, o_mb, o_out, o_part, o_pr, o_ring, o_xp, o_misc, o_stage, total;
+  size_t o_h, o_x, o_ob, o_mb, o_out, o_part, o_pr, o_ring, o_xp, o_misc, o_e, o_stage, total;
 };
 
 RLT_HD inline int cdivi(int a, int b) { return (a + b - 1) / b; }
@@ -126,6 +126,7 @@ inline int make_plan(const Shape& s, int B, int CS, int Bc, Plan* P) {
   p.o_ring = put((size_t)s.L * p.npairs * s.W * s.hd * 2 * 2);       // the pairs' window keys and values
   p.o_xp = put((size_t)(p.npairs > kWarps ? p.npairs : kWarps) * (s.hd + 2) * 4);  // cross-attention partials
   p.o_misc = put(2048);
+  p.o_e = put((size_t)2 * p.cols * s.d * 2);                          // e_p rows of this step and the next
   p.o_stage = put((size_t)2 * units * kUnitBytes);
   p.total = off;
   if (p.total > kMaxSmem) return -1;
