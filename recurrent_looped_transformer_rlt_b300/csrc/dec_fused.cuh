@@ -464,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   bf16* ringV = ringK + (size_t)s.L * P.npairs * W * hd;
   float* xp = reinterpret_cast<float*>(smem + P.o_xp);    // [units][hd + 2] cross-attention partials
   unsigned char* misc = smem + P.o_misc;
-  float2* rope_row = reinterpret_cast<float2*>(misc + 1536);  // [hd / 2] this step's (cos, sin)
   bf16* eb = reinterpret_cast<bf16*>(smem + P.o_e);       // [2][cols][d] e_p of step i in half i mod 2
+  float2* rb = reinterpret_cast<float2*>(eb + (size_t)2 * cols * d);  // [2][hd / 2] its (cos, sin) row
   unsigned char* stage = smem + P.o_stage;
   const Work wk = work_of(P, r, nbv);
   const bool scorer = r < nbv;
@@ -582,7 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     return A;
   };
 
-  // e_p of step `step` (p = p0 + step) into its half of eb, in this thread's current cp.async group
+  // e_p and the RoPE row of step `step` (p = p0 + step) into their halves of
+  // eb and rb, in this thread's current cp.async group
   auto issue_e = [&](int step) {
     const int p = a.p0 + step, d8 = d / 8;
     for (int j = tid; j < nbv * d8; j += kThreads) {
@@ -590,6 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
       cp_async16(eb + ((size_t)(step & 1) * cols + b) * d + 8 * c8, a.e + ((size_t)(b0 + b) * a.T_mem + p) * d + 8 * c8,
                  16);
     }
+    for (int j = tid; j < half / 2; j += kThreads)  // two (cos, sin) pairs per copy
+      cp_async16(rb + (size_t)(step & 1) * half + 2 * j, a.rope + (size_t)p * half + 2 * j, 16);
   };
   const int PPS = (s.gate ? 1 : 0) + 6 * s.L + (scorer ? 1 : 0);
   const int NPH = a.n * PPS;
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     float* hcur = hb + (size_t)(i & 1) * cols * d;
     const float* hprev = hb + (size_t)((i + 1) & 1) * cols * d;
     const bf16* ecur = eb + (size_t)(i & 1) * cols * d;  // e_p, rows of the cluster's sequences
-    for (int j = tid; j < half; j += kThreads) rope_row[j] = a.rope[(size_t)p * half + j];
+    const float2* rope_row = rb + (size_t)(i & 1) * half;  // (cos, sin) of position p
     for (int k = 0; k < PPS; ++k) {
       const int q = i * PPS + k;
       const Ph ph = phase_at(a, k, r, wk);

@@ -126,7 +126,7 @@ inline int make_plan(const Shape& s, int B, int CS, int Bc, Plan* P) {
   p.o_ring = put((size_t)s.L * p.npairs * s.W * s.hd * 2 * 2);       // the pairs' window keys and values
   p.o_xp = put((size_t)(p.npairs > kWarps ? p.npairs : kWarps) * (s.hd + 2) * 4);  // cross-attention partials
   p.o_misc = put(2048);
-  p.o_e = put((size_t)2 * p.cols * s.d * 2);                          // e_p rows of this step and the next
+  p.o_e = put((size_t)2 * p.cols * s.d * 2 + (size_t)2 * s.hd * 4);  // e_p rows and RoPE rows of this step and the next
   p.o_stage = put((size_t)2 * units * kUnitBytes);
   p.total = off;
   if (p.total > kMaxSmem) return -1;
