@@ -6,6 +6,8 @@
 #pragma once
 #include <atomic>
 #include <barrier>
+#include <chrono>
+#include <cstdlib>
 #include <semaphore>
 #include <condition_variable>
 #include <mutex>
@@ -58,7 +60,28 @@ inline std::vector<char> emu_dyn;
 #define __launch_bounds__(...)
 #define __grid_constant__
 
-inline void __syncthreads() { emu_block_bar->arrive_and_wait(); }
+// EMU_JITTER=1 in the environment: every thread sleeps a random 0-63 us after
+// each block or cluster barrier, so that threads leave barriers in a
+// scrambled order and an access that is not ordered by a barrier shows as a
+// result that differs from run to run.
+inline bool emu_jitter() {
+  static const bool on = [] {
+    const char* v = std::getenv("EMU_JITTER");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+inline void emu_jitter_sleep() {
+  thread_local unsigned x = 0x9e3779b9u ^ (unsigned)(uintptr_t)&x;
+  x ^= x << 13;
+  x ^= x >> 17;
+  x ^= x << 5;
+  std::this_thread::sleep_for(std::chrono::microseconds(x & 63u));
+}
+inline void __syncthreads() {
+  emu_block_bar->arrive_and_wait();
+  if (emu_jitter()) emu_jitter_sleep();
+}
 inline void __syncwarp(unsigned = 0xffffffffu) { (*emu_warps)[emu_warp].bar->arrive_and_wait(); }
 inline float __shfl_xor_sync(unsigned, float v, int m) {
   auto& w = (*emu_warps)[emu_warp];

@@ -16,7 +16,10 @@ namespace rlt {
 namespace fused {
 
 inline unsigned cluster_rank() { return emu_rank; }
-inline void cluster_sync() { emu_cluster_bar->arrive_and_wait(); }
+inline void cluster_sync() {
+  emu_cluster_bar->arrive_and_wait();
+  if (emu_jitter()) emu_jitter_sleep();
+}
 template <class T>
 inline T* map_rank(T* p, unsigned rank) {
   return reinterpret_cast<T*>(emu_cluster_smem[rank] + (reinterpret_cast<char*>(p) - emu_tl_smem));

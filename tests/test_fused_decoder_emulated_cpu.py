@@ -18,6 +18,7 @@ import os
 import re
 import shutil
 import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -185,3 +186,27 @@ def test_fused_decoder_small_workload_plan(fz):
     assert np.abs(got["s"] - ref_st.s).max() <= 2e-3 * np.abs(ref_st.s).max()
     assert np.nanmax(np.abs(got["logp"] - ref.logp)) <= 2e-3 * max(1.0, np.nanmax(np.abs(ref.logp)))
     assert (got["argmax"] == ref.argmax).mean() >= 0.99
+
+
+def test_fused_decoder_has_no_unordered_shared_accesses(fz, tmp_path):
+    """With EMU_JITTER=1 every emulated thread sleeps a random time after each
+    block and cluster barrier, so a shared-memory access not ordered by a
+    barrier gives results that differ between runs (a barrier removed from
+    the kernel does).  Three jittered runs of a 4-CTA cluster case and of a
+    two-column-tile case must be bitwise identical."""
+    lib = os.path.join(os.path.dirname(fz._name), "libfused.so")
+    script = tmp_path / "jitter.py"
+    script.write_text(
+        "import ctypes, sys\n"
+        "import numpy as np\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "from tests import test_fused_decoder_emulated_cpu as T\n"
+        f"h = ctypes.CDLL({lib!r})\n"
+        "h.fused_emu.restype = ctypes.c_int\n"
+        "for kw in (dict(CS=4, Bc=8, B=11), dict(CS=2, Bc=16, B=17)):\n"
+        "    runs = [T._case(h, **kw)[1] for _ in range(3)]\n"
+        "    for k in ('s', 'rk', 'rv', 'logp', 'logp_full', 'argmax'):\n"
+        "        assert all(np.array_equal(runs[0][k], r[k], equal_nan=True) for r in runs[1:]), (kw, k)\n")
+    env = dict(os.environ, EMU_JITTER="1")
+    r = subprocess.run([sys.executable, str(script)], capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
