@@ -15,6 +15,7 @@ import os
 import re
 import shutil
 import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -173,3 +174,29 @@ def test_emulated_kernels_production_chunk(emu64):
     loss, g, d_e, d_mem = _run(emu64, c, W, e, mem, acts, block=16)
     lref, gref = BP.gradients(O.Cfg.of(c), W, e, mem, acts)
     assert _worst(loss, g, d_e, d_mem, lref, gref) < 1e-4
+
+
+def test_emulated_kernels_have_no_unordered_shared_accesses(emu, tmp_path):
+    """Two runs with EMU_JITTER=1 (a random sleep after every block barrier,
+    so that an access no barrier orders gives run-dependent results) are
+    bitwise identical."""
+    lib = emu._name
+    script = tmp_path / "jitter.py"
+    script.write_text(
+        "import ctypes, sys\n"
+        "import numpy as np\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "from tests import test_bptt_kernels_emulated_cpu as E\n"
+        "from tests import test_bptt_schedule_cpu as S\n"
+        f"h = ctypes.CDLL({lib!r})\n"
+        "h.bptt_emu.restype = ctypes.c_int\n"
+        "c, W, e, mem, acts = S._setup(T=9, window=7)\n"
+        "a = E._run(h, c, W, e, mem, acts)\n"
+        "b = E._run(h, c, W, e, mem, acts)\n"
+        "assert a[0] == b[0]\n"
+        "for k in a[1]:\n"
+        "    assert np.array_equal(a[1][k], b[1][k]), k\n"
+        "assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])\n")
+    env = dict(os.environ, EMU_JITTER="1")
+    r = subprocess.run([sys.executable, str(script)], capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
