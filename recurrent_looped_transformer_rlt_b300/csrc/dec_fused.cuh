@@ -236,16 +236,32 @@ __device__ __forceinline__ void issue(const Args& a, const Ph& ph, int r, const 
   }
 }
 
-// out[t][16][cols] = W_tile X^T for the phase's tiles from the stage, with X
-// [cols][ldX] bf16 (zero past K).  With at least kWarps tiles each warp
-// takes whole tiles; otherwise each tile's K is split over kWarps / nt warps
-// and their partial sums are added in split order.  Ends with a block
-// barrier.
-__device__ __forceinline__ void proj(const Ph& ph, int cols, const unsigned char* stg, const bf16* X, int ldX,
-                                     float* out, float* part) {
+// The outputs of a projection phase: y(t, row, col) of tile t, either in
+// out [t][16][cols] or as the split-K partial sums of the warps in part
+// (added in split order when read).
+struct PY {
+  const float* out;
+  const float* part;
+  int cols, ks;  // ks = 0: whole tiles in out
+  __device__ __forceinline__ float operator()(int t, int row, int col) const {
+    if (ks == 0) return out[(size_t)(t * 16 + row) * cols + col];
+    const int lane = (row & 7) * 4 + ((col & 7) >> 1), q = (row >> 3) * 2 + (col & 1), j = col >> 3;
+    float v = 0.f;
+    for (int s2 = 0; s2 < ks; ++s2) v += part[(((t * ks + s2) * 2 + j) * 32 + lane) * 4 + q];
+    return v;
+  }
+};
+
+// W_tile X^T for the phase's tiles from the stage, with X [cols][ldX] bf16
+// (zero past K).  With at least kWarps tiles each warp takes whole tiles and
+// writes out; otherwise each tile's K is split over kWarps / nt warps whose
+// partial sums stay in part (reduce: added into out here, in split order).
+// Ends with a block barrier; the stage is no longer read after it.
+__device__ __forceinline__ PY proj(const Ph& ph, int cols, const unsigned char* stg, const bf16* X, int ldX,
+                                   float* out, float* part, bool reduce) {
   const int nt = ph.nt, U = ph.U, NT = cols / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  if (nt == 0) return;
+  if (nt == 0) return PY{out, part, cols, 0};
   auto run = [&](int t, int u0, int u1, float (&acc)[2][4]) {
     for (int u = u0; u < u1; ++u) {
       const uint4* up = reinterpret_cast<const uint4*>(stg + ((size_t)t * U + u) * kUnitBytes);
@@ -279,7 +295,7 @@ __device__ __forceinline__ void proj(const Ph& ph, int cols, const unsigned char
       }
     }
     __syncthreads();
-    return;
+    return PY{out, part, cols, 0};
   }
   const int ks = kWarps / nt, t = warp / ks, sp = warp - t * ks;
   if (t < nt) {
@@ -291,14 +307,14 @@ __device__ __forceinline__ void proj(const Ph& ph, int cols, const unsigned char
       for (int q = 0; q < 4; ++q) part[((warp * 2 + j) * 32 + lane) * 4 + q] = acc[j][q];
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < nt * NT * 128; e += kThreads) {
-    const int tt = e / (NT * 128), rem = e - tt * NT * 128, j = rem >> 7, ln = (rem & 127) >> 2, q = rem & 3;
-    float v = 0.f;
-    for (int s2 = 0; s2 < ks; ++s2) v += part[(((tt * ks + s2) * 2 + j) * 32 + ln) * 4 + q];
-    const int row = (ln >> 2) + 8 * (q >> 1), col = 8 * j + 2 * (ln & 3) + (q & 1);
-    out[(size_t)(tt * 16 + row) * cols + col] = v;
+  const PY y{out, part, cols, ks};
+  if (!reduce) return y;
+  for (int e = threadIdx.x; e < nt * 16 * cols; e += kThreads) {
+    const int tt = e / (16 * cols), rem = e - tt * 16 * cols, row = rem / cols, col = rem - row * cols;
+    out[e] = y(tt, row, col);
   }
   __syncthreads();
+  return PY{out, part, cols, 0};
 }
 
 // Scores column b (global sequence bg) of the head logits in out at step i.
@@ -513,15 +529,15 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     __syncthreads();
   };
   // residual add of this CTA's d rows, four rows per push
-  auto residual = [&](float* h) {
+  auto residual = [&](float* h, const PY& y) {
     int lo, hi;
     part_range(d / 16, CS, r, &lo, &hi);
     const int nq = (hi - lo) * 4;
     for (int i2 = tid; i2 < nbv * nq; i2 += kThreads) {
-      const int b = i2 / nq, rr = 4 * (i2 - b * nq), row = lo * 16 + rr;
+      const int b = i2 / nq, rr = 4 * (i2 - b * nq), row = lo * 16 + rr, t0 = rr >> 4, w = rr & 15;
       float* hp = h + (size_t)b * d + row;
-      const float4 v = make_float4(hp[0] + out[(size_t)rr * cols + b], hp[1] + out[(size_t)(rr + 1) * cols + b],
-                                   hp[2] + out[(size_t)(rr + 2) * cols + b], hp[3] + out[(size_t)(rr + 3) * cols + b]);
+      const float4 v = make_float4(hp[0] + y(t0, w, b), hp[1] + y(t0, w + 1, b), hp[2] + y(t0, w + 2, b),
+                                   hp[3] + y(t0, w + 3, b));
       push(reinterpret_cast<float4*>(hp), v, CS);
     }
   };
@@ -620,11 +636,12 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
       __syncthreads();
       unsigned char* stg = stage_of(q);
       // the projection of this phase, then the request of phase q + 2 into the half it has read
-      auto project = [&](const bf16* X, int ldX) {
-        proj(ph, cols, stg, X, ldX, out, part);
+      auto project = [&](const bf16* X, int ldX, bool reduce = false) {
+        const PY y = proj(ph, cols, stg, X, ldX, out, part, reduce);
         if (q + 2 < NPH) issue(a, phase_at(a, (k + 2) % PPS, r, wk), r, wk, stg);
         if (k == 0 && i + 1 < a.n) issue_e(i + 1);  // e of the next step, landed long before its first phase
         cp_async_commit();
+        return y;
       };
       if (k == 0 && !s.gate) {  // the gate discards s: h = e_p
         for (int i2 = tid; i2 < nbv * d; i2 += kThreads) hcur[i2] = __bfloat162float(ecur[i2]);
@@ -639,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
                                                  : __float2bfloat16_rn(hprev[(size_t)b * d + k2 - d]);
           }
           __syncthreads();
-          project(xb, P.ldx);
+          const PY y = project(xb, P.ldx);
           int lo, hi;
           part_range(d / 16, CS, r, &lo, &hi);
           const int nq = (hi - lo) * 4;
@@ -650,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
             float v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const float z = sigmoid_f(out[(size_t)(rr + u) * cols + b] + a.b_g[row + u]);
+              const float z = sigmoid_f(y((rr + u) >> 4, (rr + u) & 15, b) + a.b_g[row + u]);
               v[u] = z * sp[u] + (1.f - z) * __bfloat162float(ep[u]);
             }
             push(reinterpret_cast<float4*>(hcur + (size_t)b * d + row), make_float4(v[0], v[1], v[2], v[3]), CS);
@@ -662,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           rmsnorm_x(hcur, a.attn_norm + (size_t)l * d);
           if (l + 1 < s.L) prefetch_mem(l + 1, p);
           else if (i + 1 < a.n) prefetch_mem(0, p + 1);
-          project(xb, P.ldx);
+          const PY y = project(xb, P.ldx);
           // RoPE of q and k (rotate-half pairs j, j + hd/2); k and v rounded
           // to bf16 into ring slot p mod W, in shared memory and in the state
           const int slot = p % W;
@@ -671,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
             const int b = pair_b(pi), hh = pi % wk.hpc;
             auto val = [&](int part3, int e) {
               const int tt = (hh * 3 + part3) * nh + (e >> 4);
-              return out[(size_t)(tt * 16 + (e & 15)) * cols + b];
+              return y(tt, e & 15, b);
             };
             const float cf = rope_row[j].x, sf = rope_row[j].y;
             const float q1 = val(0, j), q2 = val(0, j + half), k1 = val(1, j), k2 = val(1, j + half);
@@ -716,17 +733,16 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
         }
         case kO:
         case kOx:
-          project(ob, P.ldo);
-          residual(hcur);
+          residual(hcur, project(ob, P.ldo));
           cluster_sync();
           break;
         case kQx: {
           rmsnorm_x(hcur, a.xattn_norm + (size_t)l * d);
-          project(xb, P.ldx);
+          const PY y = project(xb, P.ldx);
           for (int i2 = tid; i2 < wk.npairs * hd; i2 += kThreads) {
             const int pi = i2 / hd, e = i2 - pi * hd;
             const int tt = (pi % wk.hpc) * nh + (e >> 4);
-            pr[(size_t)pi * hd + e] = out[(size_t)(tt * 16 + (e & 15)) * cols + pair_b(pi)] * qscale;
+            pr[(size_t)pi * hd + e] = y(tt, e & 15, pair_b(pi)) * qscale;
           }
           __syncthreads();
           // cross-attention over memory positions 0..p, each pair's keys
@@ -782,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
         }
         case kW13: {
           rmsnorm_x(hcur, a.ffn_norm + (size_t)l * d);
-          project(xb, P.ldx);
+          const PY y = project(xb, P.ldx);
           int lo, hi;
           part_range(cdivi(s.f, 16), CS, r, &lo, &hi);
           const int n8 = (hi - lo) * 2;  // eight rows per push
@@ -793,8 +809,8 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
             float m8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const float gv = out[(size_t)((2 * pi) * 16 + w + u) * cols + b];
-              const float uv = out[(size_t)((2 * pi + 1) * 16 + w + u) * cols + b];
+              const float gv = y(2 * pi, w + u, b);
+              const float uv = y(2 * pi + 1, w + u, b);
               m8[u] = silu_f(gv) * uv;
             }
             push(reinterpret_cast<uint4*>(mb + (size_t)b * P.ldm + row), pack8(m8), CS);
@@ -803,13 +819,12 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           break;
         }
         case kW2:
-          project(mb, P.ldm);
-          residual(hcur);
+          residual(hcur, project(mb, P.ldm));
           cluster_sync();
           break;
         default: {  // head
           rmsnorm_x(hcur, a.head_norm);
-          project(xb, P.ldx);
+          project(xb, P.ldx, true);  // logits materialised in out: the scoring reads them many times
           for (int b = r; b < nbv; b += CS) score_col(a, out, cols, b, b0 + b, i, misc);
           break;
         }
