@@ -189,11 +189,14 @@ def causal_attention(q, k, v, nx: Numerics, round_p: bool):
     return (pv @ v) / lsum
 
 
-def encode(cfg: Cfg, W: Dict[str, np.ndarray], tokens: np.ndarray, return_hidden=False):
+def encode(cfg: Cfg, W: Dict[str, np.ndarray], tokens: np.ndarray, return_hidden=False, return_kv=False):
     """Causal encoder and memory projection.
 
     tokens int [B, T] (position p = column index).  Returns e [B, T, d] and
-    mem [G, 2, B, H, T, hd] (index 0 = keys, 1 = values).
+    mem [G, 2, B, H, T, hd] (index 0 = keys, 1 = values); with return_kv
+    also every layer's self-attention keys (after RoPE) and values
+    [L, 2, B, H, T, hd] as the attention used them (the encoder cache that
+    incremental encoding of later tokens attends to).
 
     Memory source.  The reading taken projects every group from the final e
     (P5 architecture paragraph: decoder global keys and values come from the
@@ -210,6 +213,7 @@ def encode(cfg: Cfg, W: Dict[str, np.ndarray], tokens: np.ndarray, return_hidden
     if cfg.mem_source == 1 and cfg.mem_groups != cfg.n_layers:
         raise ValueError("per-layer memory needs one group per layer")
     layer_states = []
+    kv = np.empty((cfg.n_layers, 2, B, H, T, hd), F64) if return_kv else None
     h = _w(W, "tok_emb")[tokens]                                  # [B, T, d]
     for l in range(cfg.n_layers):
         a = nx.r(rmsnorm(h, _w(W, "enc_attn_norm", l), cfg.rms_eps))
@@ -220,6 +224,8 @@ def encode(cfg: Cfg, W: Dict[str, np.ndarray], tokens: np.ndarray, return_hidden
         q = nx.r(rope(q, pos, cfg.rope_theta))
         k = nx.r(rope(k, pos, cfg.rope_theta))
         v = nx.r(v)
+        if return_kv:
+            kv[l, 0], kv[l, 1] = k, v
         o = np.empty((B, H, T, hd), F64)
         for b in range(B):
             o[b] = causal_attention(q[b], k[b], v[b], nx, round_p=cfg.bf16)
@@ -235,9 +241,12 @@ def encode(cfg: Cfg, W: Dict[str, np.ndarray], tokens: np.ndarray, return_hidden
         mem = memory_projection(cfg, W, layer_states)
     else:
         mem = memory_projection(cfg, W, [e] * cfg.mem_groups)
+    out = (e, mem)
     if return_hidden:
-        return e, mem, h
-    return e, mem
+        out += (h,)
+    if return_kv:
+        out += (kv,)
+    return out
 
 
 def memory_projection(cfg: Cfg, W, sources):

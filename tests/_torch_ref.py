@@ -39,19 +39,22 @@ def _merge_heads(x):
     return x.transpose(1, 2).reshape(B, P, H * hd)
 
 
-def encoder(cfg, W, tokens):
-    """Return e [B,T,d] and memory [G,2,B,H,T,hd] for an f32-storage config."""
+def encoder(cfg, W, tokens, return_kv=False):
+    """Return e [B,T,d] and memory [G,2,B,H,T,hd] for an f32-storage config
+    (and with return_kv every layer's keys after RoPE and values
+    [L,2,B,H,T,hd])."""
     d, H = cfg.d, cfg.n_heads
     tok = torch.as_tensor(tokens, dtype=torch.long)
     B, P = tok.shape
     pos = torch.arange(P)
     h = F.embedding(tok, T(W["tok_emb"]))
-    hidden = []
+    hidden, kv = [], []
     for l in range(cfg.n_layers):
         a = F.rms_norm(h, (d,), weight=T(W["enc_attn_norm"][l]), eps=cfg.rms_eps)
         q, k, v = F.linear(a, T(W["W_qkv"][l])).split(d, dim=-1)
         q, k, v = _heads(q, H), _heads(k, H), _heads(v, H)
         q, k = rope_complex(q, pos, cfg.rope_theta), rope_complex(k, pos, cfg.rope_theta)
+        kv.append(torch.stack([k, v]))
         o = F.scaled_dot_product_attention(q, k, v, is_causal=True)
         h = h + F.linear(_merge_heads(o), T(W["W_O"][l]))
         b = F.rms_norm(h, (d,), weight=T(W["enc_ffn_norm"][l]), eps=cfg.rms_eps)
@@ -66,6 +69,8 @@ def encoder(cfg, W, tokens):
             if getattr(cfg, "mem_source", 0) == 1 else e
         mem.append(torch.stack([_heads(F.linear(src, T(W["W_K"][g])), H),
                                 _heads(F.linear(src, T(W["W_V"][g])), H)]))
+    if return_kv:
+        return e.numpy(), torch.stack(mem).numpy(), torch.stack(kv).numpy()
     return e.numpy(), torch.stack(mem).numpy()
 
 

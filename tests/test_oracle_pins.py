@@ -112,6 +112,21 @@ def test_encoder_matches_library_composition(G, src):
     assert mem.shape == (G, 2, tok.shape[0], cfg.n_heads, tok.shape[1], cfg.head_dim)
 
 
+def test_encoder_cache_matches_library_composition():
+    """The encoder keys (after RoPE) and values that incremental encoding of
+    later tokens attends to: every layer's, equal to the torch composition's
+    (complex-form RoPE, scaled_dot_product_attention), and causal - those of
+    a prefix equal the prefix of those of the whole sequence."""
+    cfg, W, tok = setup(mem_groups=2, mem_source=1)
+    e, mem, kv = O.encode(cfg, W, tok, return_kv=True)
+    e_ref, mem_ref, kv_ref = TR.encoder(cfg, W, tok, return_kv=True)
+    assert kv.shape == (cfg.n_layers, 2, tok.shape[0], cfg.n_heads, tok.shape[1], cfg.head_dim)
+    np.testing.assert_allclose(kv, kv_ref, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(e, e_ref, rtol=1e-11, atol=1e-11)
+    _, _, kv4 = O.encode(cfg, W, tok[:, :4], return_kv=True)
+    np.testing.assert_array_equal(kv4, kv[:, :, :, :, :4])
+
+
 def test_per_layer_memory_reading():
     """Group l from encoder layer l (the other reading of per-layer memory):
     the last group is the final-e group, a single-layer encoder gives the same
