@@ -41,6 +41,7 @@
 #include "common.cuh"
 #include "fused_plan.h"
 #include "fused_ptx.cuh"
+#include "sampling.cuh"
 
 namespace rlt {
 namespace fused {
@@ -49,8 +50,8 @@ struct Args {
   const bf16 *W_g, *W_qkv, *W_O, *W_Qx, *W_Ox, *W_1, *W_3, *W_2, *W_o;
   const float *b_g, *attn_norm, *xattn_norm, *ffn_norm, *head_norm;
   const float2* rope;    // [T_mem][hd / 2] (cos, sin) of position p, rows p0 .. p0 + n - 1
-  const bf16* e;         // [B][T_mem][d]
-  const bf16* mem;       // [G][2][B][H][T_mem][hd]
+  bf16* e;               // [B][T_mem][d] (written at p in generation)
+  bf16* mem;             // [G][2][B][H][T_mem][hd] (written at p in generation)
   const int* actions;    // [B][n] or null
   const int* emit_map;   // [n]: index into logits_out or -1; or null
   float* logits_out;     // [n_emit][B][V] or null
@@ -63,16 +64,24 @@ struct Args {
   int* status;
   int B, T_mem, p0, n, top_k;
   float eps, theta, scale, inv_temp;
+  // generation (gen != 0): step i draws x_p (p = p0 + i) from the state's
+  // tempered top-k distribution with the uniform number of (seed, b, p),
+  // writes it to tokens [B][n] and its log-probability to logp, encodes it
+  // against the encoder cache enc_kv [L][2][B][H][T_mem][hd] (writing row p
+  // of enc_kv, e and mem) and consumes it
+  int gen;
+  const bf16* tok_emb;   // [V][d]
+  const float *enc_attn_norm, *enc_ffn_norm, *enc_norm;
+  const bf16 *W_K, *W_V;  // [G][d][d]
+  bf16* enc_kv;
+  int* tokens;
+  unsigned long long seed;
   Shape sh;
   Plan P;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ unsigned okey(float x) {  // order-preserving key of a float
-  const unsigned u = __float_as_uint(x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 __device__ __forceinline__ float bround(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 __device__ __forceinline__ unsigned bf16x2(float lo, float hi) {
   return (unsigned)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
@@ -121,32 +130,67 @@ struct Tile {
   int row0, N;
 };
 
+// Phases of a generation step before the decoder's: the draw, per encoder
+// layer QKV + attention, O, W_1/W_3, W_2 (with per-layer memory also the
+// memory rows of group l after layer l), then the memory rows e_p feeds.
+__device__ __forceinline__ int enc_phases(const Shape& s) { return 4 * s.L + (s.mem_source ? s.L : s.G); }
+
 // Phase k of a step on CTA r (scorer: the CTA scores at least one sequence).
-__device__ __forceinline__ Ph phase_at(const Args& a, int k, int r, const Work& wk) {
+__device__ __forceinline__ Ph phase_at(const Args& a, int k, int r, const Work& wk, bool scorer) {
   const Shape& s = a.sh;
   const int CS = a.P.CS;
   Ph ph{};
-  if (s.gate && k == 0) {
-    ph.kind = kGate;
-  } else {
-    const int kk = k - (s.gate ? 1 : 0);
-    if (kk < 6 * s.L) {
-      ph.kind = kQKV + kk % 6;
-      ph.l = kk / 6;
+  int kd = k;  // index among the decoder step's phases
+  if (a.gen) {
+    if (k == 0) {
+      ph.kind = kTok;
+      kd = -1;
+    } else if (k - 1 < enc_phases(s)) {
+      const int e = k - 1;
+      if (s.mem_source) {
+        ph.l = e / 5;
+        ph.kind = e % 5 < 4 ? kEQKV + e % 5 : kMem;
+      } else if (e < 4 * s.L) {
+        ph.l = e / 4;
+        ph.kind = kEQKV + e % 4;
+      } else {
+        ph.l = e - 4 * s.L;
+        ph.kind = kMem;
+      }
+      kd = -1;
     } else {
-      ph.kind = kHead;
+      kd = k - 1 - enc_phases(s);
+    }
+  }
+  if (kd >= 0) {
+    if (s.gate && kd == 0) {
+      ph.kind = kGate;
+    } else {
+      const int kk = kd - (s.gate ? 1 : 0);
+      if (kk < 6 * s.L) {
+        ph.kind = kQKV + kk % 6;
+        ph.l = kk / 6;
+      } else {
+        ph.kind = kHead;
+      }
     }
   }
   int lo, hi;
   const int th = wk.npairs > 0 ? wk.hpc * (s.hd / 16) : 0;
   switch (ph.kind) {
     case kGate: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = 2 * s.d; break;
-    case kQKV: ph.nt = 3 * th; ph.K = s.d; break;
+    case kQKV:
+    case kEQKV: ph.nt = 3 * th; ph.K = s.d; break;
     case kQx: ph.nt = th; ph.K = s.d; break;
+    case kMem: ph.nt = 2 * th; ph.K = s.d; break;
     case kO:
-    case kOx: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = s.d; break;
-    case kW13: part_range(cdivi(s.f, 16), CS, r, &lo, &hi); ph.nt = 2 * (hi - lo); ph.K = s.d; break;
-    case kW2: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = s.f; break;
+    case kOx:
+    case kEO: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = s.d; break;
+    case kW13:
+    case kEW13: part_range(cdivi(s.f, 16), CS, r, &lo, &hi); ph.nt = 2 * (hi - lo); ph.K = s.d; break;
+    case kW2:
+    case kEW2: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = s.f; break;
+    case kTok: ph.nt = scorer ? cdivi(s.V, 16) : 0; ph.K = s.d; break;
     default: ph.nt = cdivi(s.V, 16); ph.K = s.d; break;
   }
   ph.U = round32(ph.K) / 32;
@@ -165,7 +209,8 @@ __device__ __forceinline__ Tile tile_at(const Args& a, const Ph& ph, int t, int 
       part_range(d / 16, CS, r, &lo, &hi);
       T = Tile{a.W_g, (lo + t) * 16, d};
       break;
-    case kQKV: {
+    case kQKV:
+    case kEQKV: {
       const int hh = t / (3 * nh), rem = t - hh * 3 * nh, part = rem / nh, j = rem - part * nh;
       T = Tile{a.W_qkv + (size_t)ph.l * 3 * dd, part * d + (wk.hlo + hh) * hd + 16 * j, 3 * d};
       break;
@@ -175,16 +220,24 @@ __device__ __forceinline__ Tile tile_at(const Args& a, const Ph& ph, int t, int 
       T = Tile{a.W_Qx + (size_t)ph.l * dd, (wk.hlo + hh) * hd + 16 * j, d};
       break;
     }
+    case kMem: {  // keys then values of the CTA's heads, group ph.l
+      const int hh = t / (2 * nh), rem = t - hh * 2 * nh, kv = rem / nh, j = rem - kv * nh;
+      T = Tile{(kv ? a.W_V : a.W_K) + (size_t)ph.l * dd, (wk.hlo + hh) * hd + 16 * j, d};
+      break;
+    }
     case kO:
     case kOx:
+    case kEO:
       part_range(d / 16, CS, r, &lo, &hi);
-      T = Tile{(ph.kind == kO ? a.W_O : a.W_Ox) + (size_t)ph.l * dd, (lo + t) * 16, d};
+      T = Tile{(ph.kind == kOx ? a.W_Ox : a.W_O) + (size_t)ph.l * dd, (lo + t) * 16, d};
       break;
     case kW13:
+    case kEW13:
       part_range(cdivi(s.f, 16), CS, r, &lo, &hi);
       T = Tile{((t & 1) ? a.W_3 : a.W_1) + (size_t)ph.l * fd, (lo + (t >> 1)) * 16, s.f};
       break;
     case kW2:
+    case kEW2:
       part_range(d / 16, CS, r, &lo, &hi);
       T = Tile{a.W_2 + (size_t)ph.l * fd, (lo + t) * 16, d};
       break;
@@ -317,12 +370,22 @@ __device__ __forceinline__ PY proj(const Ph& ph, int cols, const unsigned char* 
   return PY{out, part, cols, 0};
 }
 
-// Scores column b (global sequence bg) of the head logits in out at step i.
-__device__ void score_col(const Args& a, const float* out, int cols, int b, int bg, int i, unsigned char* misc) {
+// The head of column b (global sequence bg) at step i (position p) from the
+// logits in out: the tempered log-softmax, the top-k set (exact k-th largest
+// key by radix select, ties to the lower id) and the argmax (lowest id on
+// ties).  Scoring: the action's lp, lp_full, argmax and the optional logits
+// copy.  Generation: the draw with the uniform number of (seed, bg, p)
+// (sample_chunked), written to tokens with its lp and pushed to every CTA's
+// tok[b].  sx: V floats of shared memory.
+__device__ void head_col(const Args& a, const float* out, int cols, int b, int bg, int i, int p,
+                         unsigned char* misc, float* sx, int* tok) {
   float* fred = reinterpret_cast<float*>(misc);                // [32]
   int* ired = reinterpret_cast<int*>(misc + 128);              // [32]
   unsigned* hist = reinterpret_cast<unsigned*>(misc + 256);    // [256]
   unsigned* sc = reinterpret_cast<unsigned*>(misc + 1280);     // prefix, remain, count
+  int* s_res = reinterpret_cast<int*>(misc + 1296);            // [5]
+  float* s_part = reinterpret_cast<float*>(misc + 1536);       // [kThreads]
+  unsigned* s_tie = reinterpret_cast<unsigned*>(misc + 2560);  // [kThreads]
   const int V = a.sh.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float it = a.inv_temp;
   auto lg = [&](int v) { return out[(size_t)((v >> 4) * 16 + (v & 15)) * cols + b]; };
@@ -330,6 +393,7 @@ __device__ void score_col(const Args& a, const float* out, int cols, int b, int 
   int barg = 0x7fffffff;
   for (int v = tid; v < V; v += kThreads) {
     const float x = lg(v);
+    sx[v] = x * it;
     if (x > bmax || (x == bmax && v < barg)) {
       bmax = x;
       barg = v;
@@ -364,7 +428,7 @@ __device__ void score_col(const Args& a, const float* out, int cols, int b, int 
   const float mx = fred[0] * it;
   __syncthreads();
   float se = 0.f;
-  for (int v = tid; v < V; v += kThreads) se += expf(lg(v) * it - mx);
+  for (int v = tid; v < V; v += kThreads) se += expf(sx[v] - mx);
   se = warp_sum(se);
   if (lane == 0) fred[warp] = se;
   __syncthreads();
@@ -376,14 +440,16 @@ __device__ void score_col(const Args& a, const float* out, int cols, int b, int 
   __syncthreads();
   const float lse = mx + logf(fred[0]);
   __syncthreads();
-  int act = a.actions ? a.actions[(size_t)bg * a.n + i] : -1;
+  const bool topk = a.top_k > 0 && a.top_k < V;
+  int act = a.gen ? -1 : (a.actions ? a.actions[(size_t)bg * a.n + i] : -1);
   if (act >= V) {
     if (tid == 0) set_error(a.status, kErrBounds);
     act = -1;
   }
-  const float lp_full = act >= 0 ? lg(act) * it - lse : NAN;
+  if (a.gen && !topk) act = sample_chunked(sx, V, mx, true, 0u, 0u, uniform24(a.seed, bg, p), s_part, s_tie, s_res);
+  float lp_full = act >= 0 ? sx[act] - lse : NAN;
   float lp = lp_full;
-  if (a.top_k > 0 && a.top_k < V) {
+  if (topk) {
     // k-th largest key by radix select, 8 bits at a time from the top
     if (tid == 0) {
       sc[0] = 0;
@@ -396,7 +462,7 @@ __device__ void score_col(const Args& a, const float* out, int cols, int b, int 
       const unsigned pref = sc[0];
       const unsigned hmask = pass == 0 ? 0u : (0xffffffffu << (shift + 8));
       for (int v = tid; v < V; v += kThreads) {
-        const unsigned kk = okey(lg(v) * it);
+        const unsigned kk = f2key(sx[v]);
         if ((kk & hmask) == pref) atomicAdd(&hist[(kk >> shift) & 255u], 1u);
       }
       __syncthreads();
@@ -414,15 +480,17 @@ __device__ void score_col(const Args& a, const float* out, int cols, int b, int 
     }
     const unsigned kth = sc[0], need = sc[1];
     const float xk = __uint_as_float((kth & 0x80000000u) ? (kth & 0x7fffffffu) : ~kth);
-    float sg = 0.f;
-    for (int v = tid; v < V; v += kThreads) {
-      const float x = lg(v) * it;
-      if (okey(x) > kth) sg += expf(x - mx);
+    if (a.gen) {
+      act = sample_chunked(sx, V, mx, false, kth, need, uniform24(a.seed, bg, p), s_part, s_tie, s_res);
+      lp_full = sx[act] - lse;
     }
+    float sg = 0.f;
+    for (int v = tid; v < V; v += kThreads)
+      if (f2key(sx[v]) > kth) sg += expf(sx[v] - mx);
     sg = warp_sum(sg);
     unsigned below = 0;  // ids below the action with the k-th key
-    if (act >= 0 && okey(lg(act) * it) == kth)
-      for (int v = tid; v < act; v += kThreads) below += okey(lg(v) * it) == kth ? 1u : 0u;
+    if (act >= 0 && f2key(sx[act]) == kth)
+      for (int v = tid; v < act; v += kThreads) below += f2key(sx[v]) == kth ? 1u : 0u;
     __syncthreads();
     if (lane == 0) fred[warp] = sg;
     if (tid == 0) sc[2] = 0;
@@ -437,19 +505,27 @@ __device__ void score_col(const Args& a, const float* out, int cols, int b, int 
     __syncthreads();
     const float lse_k = mx + logf(fred[0] + (float)need * expf(xk - mx));
     if (act >= 0) {
-      const unsigned ka = okey(lg(act) * it);
+      const unsigned ka = f2key(sx[act]);
       const bool in = ka > kth || (ka == kth && sc[2] < need);
-      lp = in ? lg(act) * it - lse_k : -INFINITY;
+      lp = in ? sx[act] - lse_k : -INFINITY;
     }
   }
-  const int em = a.emit_map ? a.emit_map[i] : -1;
-  if (em >= 0 && a.logits_out)
-    for (int v = tid; v < V; v += kThreads) a.logits_out[((size_t)em * a.B + bg) * V + v] = lg(v);
-  if (tid == 0) {
-    const size_t o = (size_t)bg * a.n + i;
-    if (a.logp) a.logp[o] = lp;
-    if (a.logp_full) a.logp_full[o] = lp_full;
-    if (a.argmax) a.argmax[o] = amax;
+  const size_t o = (size_t)bg * a.n + i;
+  if (a.gen) {
+    if (tid == 0) {
+      a.tokens[o] = act;
+      if (a.logp) a.logp[o] = lp;
+    }
+    if (tid < a.P.CS) *map_rank(tok + b, (unsigned)tid) = act;
+  } else {
+    const int em = a.emit_map ? a.emit_map[i] : -1;
+    if (em >= 0 && a.logits_out)
+      for (int v = tid; v < V; v += kThreads) a.logits_out[((size_t)em * a.B + bg) * V + v] = lg(v);
+    if (tid == 0) {
+      if (a.logp) a.logp[o] = lp;
+      if (a.logp_full) a.logp_full[o] = lp_full;
+      if (a.argmax) a.argmax[o] = amax;
+    }
   }
   __syncthreads();
 }
@@ -482,6 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   unsigned char* misc = smem + P.o_misc;
   bf16* eb = reinterpret_cast<bf16*>(smem + P.o_e);       // [2][cols][d] e_p of step i in half i mod 2
   float2* rb = reinterpret_cast<float2*>(eb + (size_t)2 * cols * d);  // [2][hd / 2] its (cos, sin) row
+  float* he = reinterpret_cast<float*>(smem + P.o_he);    // [cols][d] generation: encoder streams
+  int* tokb = reinterpret_cast<int*>(smem + P.o_tok);     // [cols] generation: this step's tokens
+  float* sx = reinterpret_cast<float*>(smem + P.o_sx);    // [V] tempered logits of the scored row
   unsigned char* stage = smem + P.o_stage;
   const Work wk = work_of(P, r, nbv);
   const bool scorer = r < nbv;
@@ -602,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   // eb and rb, in this thread's current cp.async group
   auto issue_e = [&](int step) {
     const int p = a.p0 + step, d8 = d / 8;
-    for (int j = tid; j < nbv * d8; j += kThreads) {
+    for (int j = tid; j < (a.gen ? 0 : nbv * d8); j += kThreads) {  // generation computes e_p
       const int b = j / d8, c8 = j - b * d8;
       cp_async16(eb + ((size_t)(step & 1) * cols + b) * d + 8 * c8, a.e + ((size_t)(b0 + b) * a.T_mem + p) * d + 8 * c8,
                  16);
@@ -610,16 +689,105 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     for (int j = tid; j < half / 2; j += kThreads)  // two (cos, sin) pairs per copy
       cp_async16(rb + (size_t)(step & 1) * half + 2 * j, a.rope + (size_t)p * half + 2 * j, 16);
   };
-  const int PPS = (s.gate ? 1 : 0) + 6 * s.L + (scorer ? 1 : 0);
+  // attention of each pair's query (pr, log2 units) over key rows 0..nk-1 at
+  // Kb(pi), Vb(pi) ([nk][hd] bf16): each pair's keys split over ns warps,
+  // partials combined in split order, the result pushed to ob.  coherent:
+  // rows written during this launch, read through L2.
+  auto pair_attention = [&](auto Kb, auto Vb, int nk, bool coherent) {
+    const int ns = wk.npairs >= kWarps ? 1 : kWarps / max(wk.npairs, 1);
+    for (int w0 = warp; w0 < wk.npairs * ns; w0 += kWarps) {
+      const int pi = w0 / ns, sp = w0 - pi * ns;
+      const bf16* Kp = Kb(pi) + 8 * cc;
+      const bf16* Vp = Vb(pi) + 8 * cc;
+      float qv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qv[e] = pr[(size_t)pi * hd + 8 * cc + e];
+      const Acc A = attend(
+          qv, sp * nk / ns, (sp + 1) * nk / ns,
+          [&](int j) { return coherent ? ld_cg16(Kp + (size_t)j * hd) : ld_nc16(Kp + (size_t)j * hd); },
+          [&](int j) { return coherent ? ld_cg16(Vp + (size_t)j * hd) : ld_nc16(Vp + (size_t)j * hd); });
+      float* xw = xp + (size_t)w0 * (hd + 2);
+      if (rg == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xw[8 * cc + e] = A.o[e];
+      }
+      if (lane == 0) {
+        xw[hd] = A.m;
+        xw[hd + 1] = A.l;
+      }
+    }
+    __syncthreads();
+    for (int i2 = tid; i2 < wk.npairs * hd8; i2 += kThreads) {
+      const int pi = i2 / hd8, c8 = i2 - pi * hd8;
+      float M = -INFINITY;
+      for (int sp = 0; sp < ns; ++sp) {
+        const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
+        if (xw[hd + 1] > 0.f) M = fmaxf(M, xw[hd]);
+      }
+      float num[8] = {}, den = 0.f;
+      for (int sp = 0; sp < ns; ++sp) {
+        const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
+        if (xw[hd + 1] > 0.f) {
+          const float cf = exp2f(xw[hd] - M);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) num[e] = fmaf(xw[8 * c8 + e], cf, num[e]);
+          den = fmaf(xw[hd + 1], cf, den);
+        }
+      }
+      const float inv = 1.0f / den;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) num[e] *= inv;
+      push(reinterpret_cast<uint4*>(ob + (size_t)pair_b(pi) * P.ldo + pair_h(pi) * hd + 8 * c8), pack8(num), CS);
+    }
+  };
+  // m = silu(W_1 b) * (W_3 b) of this CTA's f rows, eight rows per push
+  auto swiglu_push = [&](const PY& y) {
+    int lo, hi;
+    part_range(cdivi(s.f, 16), CS, r, &lo, &hi);
+    const int n8 = (hi - lo) * 2;
+    for (int i2 = tid; i2 < nbv * n8; i2 += kThreads) {
+      const int b = i2 / n8, rr = 8 * (i2 - b * n8), row = lo * 16 + rr;
+      if (row >= s.f) continue;
+      const int pi = rr >> 4, w = rr & 15;
+      float m8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m8[u] = silu_f(y(2 * pi, w + u, b)) * y(2 * pi + 1, w + u, b);
+      push(reinterpret_cast<uint4*>(mb + (size_t)b * P.ldm + row), pack8(m8), CS);
+    }
+  };
+  // RoPE (rotate-half pairs j, j + hd/2) of this CTA's q and k at position p
+  // from the QKV tiles of y; q to pr (log2 units, rounded to bf16 first when
+  // round_q), k and v rounded to bf16 and handed to put(pi, j, k1, k2, v1, v2)
+  auto rope_qkv = [&](const PY& y, const float2* rope_row, bool round_q, auto put) {
+    const int half_ = hd / 2;
+    for (int i2 = tid; i2 < wk.npairs * half_; i2 += kThreads) {
+      const int pi = i2 / half_, j = i2 - pi * half_;
+      const int b = pair_b(pi), hh = pi % wk.hpc;
+      auto val = [&](int part3, int e) { return y((hh * 3 + part3) * nh + (e >> 4), e & 15, b); };
+      const float cf = rope_row[j].x, sf = rope_row[j].y;
+      const float q1 = val(0, j), q2 = val(0, j + half_), k1 = val(1, j), k2 = val(1, j + half_);
+      float qr1 = q1 * cf - q2 * sf, qr2 = q2 * cf + q1 * sf;
+      if (round_q) {
+        qr1 = bround(qr1);
+        qr2 = bround(qr2);
+      }
+      pr[(size_t)pi * hd + j] = qr1 * qscale;
+      pr[(size_t)pi * hd + j + half_] = qr2 * qscale;
+      put(pi, j, __float2bfloat16_rn(k1 * cf - k2 * sf), __float2bfloat16_rn(k2 * cf + k1 * sf),
+          __float2bfloat16_rn(val(2, j)), __float2bfloat16_rn(val(2, j + half_)));
+    }
+  };
+  const int kdec0 = a.gen ? 1 + enc_phases(s) : 0;  // the decoder step's first phase
+  const int PPS = kdec0 + (s.gate ? 1 : 0) + 6 * s.L + (a.gen ? 0 : (scorer ? 1 : 0));
   const int NPH = a.n * PPS;
   auto stage_of = [&](int q) { return stage + (size_t)(q & 1) * P.stage_units * kUnitBytes; };
   // phase q's weights go to stage q mod 2; they are requested right after
   // phase q - 2's projection has read that half (one cp.async group per
   // phase), so each copy has most of two phases to land
-  issue(a, phase_at(a, 0, r, wk), r, wk, stage_of(0));
+  issue(a, phase_at(a, 0, r, wk, scorer), r, wk, stage_of(0));
   issue_e(0);
   cp_async_commit();
-  if (NPH > 1) issue(a, phase_at(a, 1 % PPS, r, wk), r, wk, stage_of(1));
+  if (NPH > 1) issue(a, phase_at(a, 1 % PPS, r, wk, scorer), r, wk, stage_of(1));
   cp_async_commit();
   prefetch_mem(0, a.p0);
 
@@ -631,19 +799,19 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     const float2* rope_row = rb + (size_t)(i & 1) * half;  // (cos, sin) of position p
     for (int k = 0; k < PPS; ++k) {
       const int q = i * PPS + k;
-      const Ph ph = phase_at(a, k, r, wk);
+      const Ph ph = phase_at(a, k, r, wk, scorer);
       cp_async_wait1();  // this phase's group (the next phase's may still be in flight)
       __syncthreads();
       unsigned char* stg = stage_of(q);
       // the projection of this phase, then the request of phase q + 2 into the half it has read
       auto project = [&](const bf16* X, int ldX, bool reduce = false) {
         const PY y = proj(ph, cols, stg, X, ldX, out, part, reduce);
-        if (q + 2 < NPH) issue(a, phase_at(a, (k + 2) % PPS, r, wk), r, wk, stg);
+        if (q + 2 < NPH) issue(a, phase_at(a, (k + 2) % PPS, r, wk, scorer), r, wk, stg);
         if (k == 0 && i + 1 < a.n) issue_e(i + 1);  // e of the next step, landed long before its first phase
         cp_async_commit();
         return y;
       };
-      if (k == 0 && !s.gate) {  // the gate discards s: h = e_p
+      if (k == kdec0 && !s.gate) {  // the gate discards s: h = e_p
         for (int i2 = tid; i2 < nbv * d; i2 += kThreads) hcur[i2] = __bfloat162float(ecur[i2]);
         __syncthreads();
       }
@@ -680,22 +848,10 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           if (l + 1 < s.L) prefetch_mem(l + 1, p);
           else if (i + 1 < a.n) prefetch_mem(0, p + 1);
           const PY y = project(xb, P.ldx);
-          // RoPE of q and k (rotate-half pairs j, j + hd/2); k and v rounded
-          // to bf16 into ring slot p mod W, in shared memory and in the state
+          // q and k after RoPE; k and v rounded to bf16 into ring slot p mod
+          // W, in shared memory and in the state
           const int slot = p % W;
-          for (int i2 = tid; i2 < wk.npairs * half; i2 += kThreads) {
-            const int pi = i2 / half, j = i2 - pi * half;
-            const int b = pair_b(pi), hh = pi % wk.hpc;
-            auto val = [&](int part3, int e) {
-              const int tt = (hh * 3 + part3) * nh + (e >> 4);
-              return y(tt, e & 15, b);
-            };
-            const float cf = rope_row[j].x, sf = rope_row[j].y;
-            const float q1 = val(0, j), q2 = val(0, j + half), k1 = val(1, j), k2 = val(1, j + half);
-            pr[(size_t)pi * hd + j] = (q1 * cf - q2 * sf) * qscale;
-            pr[(size_t)pi * hd + j + half] = (q2 * cf + q1 * sf) * qscale;
-            const bf16 kr1 = __float2bfloat16_rn(k1 * cf - k2 * sf), kr2 = __float2bfloat16_rn(k2 * cf + k1 * sf);
-            const bf16 v1 = __float2bfloat16_rn(val(2, j)), v2 = __float2bfloat16_rn(val(2, j + half));
+          rope_qkv(y, rope_row, false, [&](int pi, int j, bf16 kr1, bf16 kr2, bf16 v1, bf16 v2) {
             const size_t so = (((size_t)l * P.npairs + pi) * W + slot) * hd;
             ringK[so + j] = kr1;
             ringK[so + j + half] = kr2;
@@ -706,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
             a.ring_k[go + j + half] = kr2;
             a.ring_v[go + j] = v1;
             a.ring_v[go + j + half] = v2;
-          }
+          });
           __syncthreads();
           // window attention over slots 0..min(W, t) - 1 (softmax does not
           // depend on their order), one warp per pair
@@ -745,76 +901,21 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
             pr[(size_t)pi * hd + e] = y(tt, e & 15, pair_b(pi)) * qscale;
           }
           __syncthreads();
-          // cross-attention over memory positions 0..p, each pair's keys
-          // split over ns warps; partials combined in split order
+          // cross-attention over memory positions 0..p (rows this launch
+          // wrote, in generation, are read through L2)
           const int g = s.G == 1 ? 0 : l;
-          const int ns = wk.npairs >= kWarps ? 1 : kWarps / max(wk.npairs, 1);
-          for (int w0 = warp; w0 < wk.npairs * ns; w0 += kWarps) {
-            const int pi = w0 / ns, sp = w0 - pi * ns;
-            const size_t plane = (size_t)a.T_mem * hd;
-            const bf16* Kp = a.mem + (((size_t)g * 2 * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * plane + 8 * cc;
-            const bf16* Vp = a.mem + ((((size_t)g * 2 + 1) * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * plane + 8 * cc;
-            float qv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qv[e] = pr[(size_t)pi * hd + 8 * cc + e];
-            const Acc A = attend(qv, sp * t / ns, (sp + 1) * t / ns,
-                                 [&](int j) { return ld_nc16(Kp + (size_t)j * hd); },
-                                 [&](int j) { return ld_nc16(Vp + (size_t)j * hd); });
-            float* xw = xp + (size_t)w0 * (hd + 2);
-            if (rg == 0) {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) xw[8 * cc + e] = A.o[e];
-            }
-            if (lane == 0) {
-              xw[hd] = A.m;
-              xw[hd + 1] = A.l;
-            }
-          }
-          __syncthreads();
-          for (int i2 = tid; i2 < wk.npairs * hd8; i2 += kThreads) {
-            const int pi = i2 / hd8, c8 = i2 - pi * hd8;
-            float M = -INFINITY;
-            for (int sp = 0; sp < ns; ++sp) {
-              const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
-              if (xw[hd + 1] > 0.f) M = fmaxf(M, xw[hd]);
-            }
-            float num[8] = {}, den = 0.f;
-            for (int sp = 0; sp < ns; ++sp) {
-              const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
-              if (xw[hd + 1] > 0.f) {
-                const float cf = exp2f(xw[hd] - M);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) num[e] = fmaf(xw[8 * c8 + e], cf, num[e]);
-                den = fmaf(xw[hd + 1], cf, den);
-              }
-            }
-            const float inv = 1.0f / den;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) num[e] *= inv;
-            push(reinterpret_cast<uint4*>(ob + (size_t)pair_b(pi) * P.ldo + pair_h(pi) * hd + 8 * c8), pack8(num), CS);
-          }
+          const size_t plane = (size_t)a.T_mem * hd;
+          pair_attention(
+              [&](int pi) { return a.mem + (((size_t)g * 2 * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * plane; },
+              [&](int pi) { return a.mem + ((((size_t)g * 2 + 1) * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * plane; },
+              t, a.gen != 0);
           cluster_sync();
           break;
         }
         case kW13: {
           rmsnorm_x(hcur, a.ffn_norm + (size_t)l * d);
           const PY y = project(xb, P.ldx);
-          int lo, hi;
-          part_range(cdivi(s.f, 16), CS, r, &lo, &hi);
-          const int n8 = (hi - lo) * 2;  // eight rows per push
-          for (int i2 = tid; i2 < nbv * n8; i2 += kThreads) {
-            const int b = i2 / n8, rr = 8 * (i2 - b * n8), row = lo * 16 + rr;
-            if (row >= s.f) continue;
-            const int pi = rr >> 4, w = rr & 15;
-            float m8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float gv = y(2 * pi, w + u, b);
-              const float uv = y(2 * pi + 1, w + u, b);
-              m8[u] = silu_f(gv) * uv;
-            }
-            push(reinterpret_cast<uint4*>(mb + (size_t)b * P.ldm + row), pack8(m8), CS);
-          }
+          swiglu_push(y);
           cluster_sync();
           break;
         }
@@ -822,10 +923,84 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           residual(hcur, project(mb, P.ldm));
           cluster_sync();
           break;
+        case kTok: {  // generation: x_p drawn from s_p by the CTAs that score, shared with every CTA
+          if (scorer) rmsnorm_x(hprev, a.head_norm);
+          project(xb, P.ldx, true);
+          if (scorer)
+            for (int b = r; b < nbv; b += CS) head_col(a, out, cols, b, b0 + b, i, p, misc, sx, tokb);
+          cluster_sync();
+          break;
+        }
+        case kEQKV: {  // encoder layer l at p: q, k, v, cache row p, causal attention over rows 0..p
+          if (l == 0) {
+            for (int i2 = tid; i2 < nbv * d; i2 += kThreads) {
+              const int b = i2 / d, j = i2 - b * d;
+              he[i2] = __bfloat162float(a.tok_emb[(size_t)tokb[b] * d + j]);
+            }
+            __syncthreads();
+          }
+          rmsnorm_x(he, a.enc_attn_norm + (size_t)l * d);
+          const PY y = project(xb, P.ldx);
+          const size_t plane = (size_t)a.T_mem * hd;
+          auto kv_rows = [&](int kv, int pi) {
+            return a.enc_kv + ((((size_t)l * 2 + kv) * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * plane;
+          };
+          rope_qkv(y, rope_row, true, [&](int pi, int j, bf16 kr1, bf16 kr2, bf16 v1, bf16 v2) {
+            bf16* kp = kv_rows(0, pi) + (size_t)p * hd;
+            bf16* vp = kv_rows(1, pi) + (size_t)p * hd;
+            kp[j] = kr1;
+            kp[j + half] = kr2;
+            vp[j] = v1;
+            vp[j + half] = v2;
+          });
+          __syncthreads();
+          pair_attention([&](int pi) { return kv_rows(0, pi); }, [&](int pi) { return kv_rows(1, pi); }, t, true);
+          cluster_sync();
+          break;
+        }
+        case kEO:
+          residual(he, project(ob, P.ldo));
+          cluster_sync();
+          break;
+        case kEW13: {
+          rmsnorm_x(he, a.enc_ffn_norm + (size_t)l * d);
+          swiglu_push(project(xb, P.ldx));
+          cluster_sync();
+          break;
+        }
+        case kEW2:
+          residual(he, project(mb, P.ldm));
+          cluster_sync();
+          break;
+        case kMem: {  // memory rows of group g at p, for this CTA's pairs
+          const int g = l;
+          const bool final_src = s.mem_source ? g == s.L - 1 : g == 0;
+          if (s.mem_source || g == 0) rmsnorm_x(he, a.enc_norm);  // RMSNorm_e of the encoder stream
+          if (final_src) {  // e_p: the decoder's input, and row p of e
+            bf16* ew = eb + (size_t)(i & 1) * cols * d;
+            for (int i2 = tid; i2 < nbv * d; i2 += kThreads) {
+              const int b = i2 / d, j = i2 - b * d;
+              const bf16 v = xb[(size_t)b * P.ldx + j];
+              ew[i2] = v;
+              if (r == 0) a.e[((size_t)(b0 + b) * a.T_mem + p) * d + j] = v;
+            }
+          }
+          const PY y = project(xb, P.ldx);
+          const size_t plane = (size_t)a.T_mem * hd;
+          for (int i2 = tid; i2 < wk.npairs * 2 * hd; i2 += kThreads) {
+            const int pi = i2 / (2 * hd), rem = i2 - pi * 2 * hd, kv = rem / hd, e = rem - kv * hd;
+            const int hh = pi % wk.hpc;
+            const float v = y((hh * 2 + kv) * nh + (e >> 4), e & 15, pair_b(pi));
+            a.mem[((((size_t)g * 2 + kv) * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) * plane + (size_t)p * hd + e] =
+                __float2bfloat16_rn(v);
+          }
+          __syncthreads();
+          break;
+        }
         default: {  // head
           rmsnorm_x(hcur, a.head_norm);
           project(xb, P.ldx, true);  // logits materialised in out: the scoring reads them many times
-          for (int b = r; b < nbv; b += CS) score_col(a, out, cols, b, b0 + b, i, misc);
+          for (int b = r; b < nbv; b += CS) head_col(a, out, cols, b, b0 + b, i, p, misc, sx, tokb);
           break;
         }
       }

@@ -33,12 +33,14 @@ constexpr int kMaxCols = 16;          // sequences per cluster: two 8-column MMA
 constexpr int kUnitBytes = 1024;      // one staged weight unit: 16 rows x 32 columns, bf16
 constexpr size_t kMaxSmem = 232448;   // dynamic shared memory per CTA (227 KB)
 
-// phase kinds, in step order
-enum Kind { kGate = 0, kQKV, kO, kQx, kOx, kW13, kW2, kHead };
+// phase kinds: the decoder step's (in step order) and, in generation, the
+// draw and the incremental encoder step's
+enum Kind { kGate = 0, kQKV, kO, kQx, kOx, kW13, kW2, kHead, kTok, kEQKV, kEO, kEW13, kEW2, kMem };
 
 struct Shape {
   int d, H, hd, f, L, W, V, G;
-  int gate;  // 1: learned merge gate; 0: the gate discards s (h = e)
+  int gate;        // 1: learned merge gate; 0: the gate discards s (h = e)
+  int mem_source;  // generation: 0 every memory group from e; 1 group l from encoder layer l
 };
 
 struct Plan {
@@ -53,7 +55,7 @@ struct Plan {
   int ldx, ldo, ldm;  // row pitches (elements) of the bf16 operand buffers
   int maxT;           // most 16-row tiles of one phase on one CTA
   int stage_units;    // units of one stage buffer
-  size_t o_h, o_x, o_ob, o_mb, o_out, o_part, o_pr, o_ring, o_xp, o_misc, o_e, o_stage, total;
+  size_t o_h, o_x, o_ob, o_mb, o_out, o_part, o_pr, o_ring, o_xp, o_misc, o_e, o_he, o_tok, o_sx, o_stage, total;
 };
 
 RLT_HD inline int cdivi(int a, int b) { return (a + b - 1) / b; }
@@ -125,8 +127,11 @@ inline int make_plan(const Shape& s, int B, int CS, int Bc, Plan* P) {
   p.o_pr = put((size_t)p.npairs * s.hd * 4);                        // queries of the pairs
   p.o_ring = put((size_t)s.L * p.npairs * s.W * s.hd * 2 * 2);       // the pairs' window keys and values
   p.o_xp = put((size_t)(p.npairs > kWarps ? p.npairs : kWarps) * (s.hd + 2) * 4);  // cross-attention partials
-  p.o_misc = put(2048);
+  p.o_misc = put(4096);
   p.o_e = put((size_t)2 * p.cols * s.d * 2 + (size_t)2 * s.hd * 4);  // e_p rows and RoPE rows of this step and the next
+  p.o_he = put((size_t)p.cols * s.d * 4);                            // generation: the encoder's residual streams
+  p.o_tok = put((size_t)p.cols * 4);                                 // generation: the drawn tokens
+  p.o_sx = put((size_t)s.V * 4);                                     // the scored row's tempered logits
   p.o_stage = put((size_t)2 * units * kUnitBytes);
   p.total = off;
   if (p.total > kMaxSmem) return -1;

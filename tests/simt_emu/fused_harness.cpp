@@ -17,7 +17,7 @@ static std::vector<bf16> tob(const float* x, size_t n) {
   return v;
 }
 
-// sh: B, T_mem, d, H, hd, f, L, W, V, G, gate, p0, n, top_k, CS, Bc
+// sh: B, T_mem, d, H, hd, f, L, W, V, G, gate, p0, n, top_k, CS, Bc (, mem_source, seed hi, seed lo)
 // fp: eps, theta, temperature
 // P:  W_g, W_qkv, W_O, W_Qx, W_Ox, W_1, W_3, W_2, W_o (f32 values, stored as bf16),
 //     b_g, attn_norm, xattn_norm, ffn_norm, head_norm (f32),
@@ -26,8 +26,9 @@ static std::vector<bf16> tob(const float* x, size_t n) {
 //     actions [B][n] i32 or null, emit_map [n] i32 or null, logits_out f32 or null,
 //     logp, logp_full f32 [B][n], argmax i32 [B][n], status i32 [1]
 // Returns the plan's status (-1: shape not supported), else 0.
-extern "C" int fused_emu(const int* sh, const float* fp, void** P) {
-  fused::Shape S{sh[2], sh[3], sh[4], sh[5], sh[6], sh[7], sh[8], sh[9], sh[10]};
+// sh[16]: mem_source (generation)
+static int run(const int* sh, const float* fp, void** P, void** Q) {
+  fused::Shape S{sh[2], sh[3], sh[4], sh[5], sh[6], sh[7], sh[8], sh[9], sh[10], sh[16]};
   const int B = sh[0], T_mem = sh[1], CS = sh[14], Bc = sh[15];
   fused::Plan plan;
   if (fused::make_plan(S, B, CS, Bc, &plan)) return -1;
@@ -38,6 +39,15 @@ extern "C" int fused_emu(const int* sh, const float* fp, void** P) {
                     WOx = wb(4, L * dd), W1 = wb(5, L * f * d), W3 = wb(6, L * f * d), W2 = wb(7, L * f * d),
                     Wo = wb(8, V * d);
   std::vector<bf16> e = wb(14, (size_t)B * T_mem * d), mem = wb(15, G * 2 * B * H * T_mem * hd);
+  // generation: Q = tok_emb, enc_attn_norm, enc_ffn_norm, enc_norm, W_K, W_V (f32 values),
+  // enc_kv [L][2][B][H][T_mem][hd] (f32 values in/out), tokens i32 [B][n], e out, mem out (f32)
+  std::vector<bf16> temb, WK, WV, ekv;
+  if (Q) {
+    temb = tob((const float*)Q[0], V * d);
+    WK = tob((const float*)Q[4], G * dd);
+    WV = tob((const float*)Q[5], G * dd);
+    ekv = tob((const float*)Q[6], L * 2 * B * H * T_mem * hd);
+  }
   const size_t ring_n = L * B * H * W * hd;
   std::vector<bf16> rk = wb(17, ring_n), rv = wb(18, ring_n);
   fused::Args a{};
@@ -61,6 +71,18 @@ extern "C" int fused_emu(const int* sh, const float* fp, void** P) {
   a.eps = fp[0]; a.theta = fp[1]; a.scale = 1.0f / std::sqrt((float)hd); a.inv_temp = 1.0f / fp[2];
   a.sh = S;
   a.P = plan;
+  if (Q) {
+    a.gen = 1;
+    a.tok_emb = temb.data();
+    a.enc_attn_norm = (const float*)Q[1];
+    a.enc_ffn_norm = (const float*)Q[2];
+    a.enc_norm = (const float*)Q[3];
+    a.W_K = WK.data();
+    a.W_V = WV.data();
+    a.enc_kv = ekv.data();
+    a.tokens = (int*)Q[7];
+    a.seed = ((unsigned long long)(unsigned)sh[17] << 32) | (unsigned)sh[18];
+  }
   emu_launch_cluster(dim3(plan.nclu * CS), dim3(fused::kThreads), plan.total, (unsigned)CS, fused::dec_fused_kernel,
                      a);
   float* rko = (float*)P[17];
@@ -69,5 +91,19 @@ extern "C" int fused_emu(const int* sh, const float* fp, void** P) {
     rko[i] = __bfloat162float(rk[i]);
     rvo[i] = __bfloat162float(rv[i]);
   }
+  if (Q) {
+    auto back = [](const std::vector<bf16>& v, void* dst) {
+      float* o = (float*)dst;
+      for (size_t i = 0; i < v.size(); ++i) o[i] = __bfloat162float(v[i]);
+    };
+    back(ekv, Q[6]);
+    back(e, Q[8]);
+    back(mem, Q[9]);
+  }
   return 0;
 }
+
+extern "C" int fused_emu(const int* sh, const float* fp, void** P) { return run(sh, fp, P, nullptr); }
+
+// generation: sh[16] mem_source, sh[17], sh[18] the seed's high and low words
+extern "C" int fused_gen_emu(const int* sh, const float* fp, void** P, void** Q) { return run(sh, fp, P, Q); }

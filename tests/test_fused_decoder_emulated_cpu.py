@@ -57,7 +57,7 @@ def fz(tmp_path_factory):
 def _call(h, c, W, e, mem, s, rk, rv, acts, p0, n, CS, Bc, tau=1.0, k=0, emit=()):
     B, T = e.shape[:2]
     sh = [B, T, c.d, c.n_heads, c.head_dim, c.d_ffn, c.n_layers, c.window, c.vocab, c.mem_groups,
-          1 if c.gate_mode == 0 else 0, p0, n, k, CS, Bc]
+          1 if c.gate_mode == 0 else 0, p0, n, k, CS, Bc, 0, 0, 0]
     keep = []
 
     def f32(x):
@@ -76,7 +76,7 @@ def _call(h, c, W, e, mem, s, rk, rv, acts, p0, n, CS, Bc, tau=1.0, k=0, emit=()
     ptr = [f32(W[p]) for p in MATS] + [f32(W[p]) for p in VECS] + [f32(e), f32(mem)]
     ptr += [s.ctypes.data, rk.ctypes.data, rv.ctypes.data, a.ctypes.data, emap.ctypes.data, lg.ctypes.data,
             lp.ctypes.data, lf.ctypes.data, am.ctypes.data, status.ctypes.data]
-    rc = h.fused_emu((ctypes.c_int * 16)(*sh), (ctypes.c_float * 3)(c.rms_eps, c.rope_theta, tau),
+    rc = h.fused_emu((ctypes.c_int * len(sh))(*sh), (ctypes.c_float * 3)(c.rms_eps, c.rope_theta, tau),
                      (ctypes.c_void_p * len(ptr))(*ptr))
     assert rc == 0, "plan rejected the shape"
     assert status[0] == 0
@@ -210,3 +210,127 @@ def test_fused_decoder_has_no_unordered_shared_accesses(fz, tmp_path):
     env = dict(os.environ, EMU_JITTER="1")
     r = subprocess.run([sys.executable, str(script)], capture_output=True, text=True, env=env, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
+
+
+# ---------------------------------------------------------------------------
+# generation through the persistent kernel: each step draws x_p from s_p,
+# encodes it against the encoder cache and consumes it
+
+def _prefill_state(c, W, prompt, n):
+    """The oracle's prefill of the prompt (e, memory and encoder cache of its
+    positions, the decoder state after it) in buffers with room for n more
+    positions."""
+    cfg = O.Cfg.of(c)
+    B, T0 = prompt.shape
+    L, H, hd, G, d, Wn = c.n_layers, c.n_heads, c.head_dim, c.mem_groups, c.d, c.window
+    Tm = T0 + n
+    e0, mem0, kv0 = O.encode(cfg, W, prompt, return_kv=True)
+    st, _ = O.decode_steps(cfg, W, O.init_state(cfg, W, B), e0, mem0, T0)
+    e = np.full((B, Tm, d), np.nan, np.float32)
+    e[:, :T0] = e0
+    mem = np.full((G, 2, B, H, Tm, hd), np.nan, np.float32)
+    mem[..., :T0, :] = mem0
+    kv = np.full((L, 2, B, H, Tm, hd), np.nan, np.float32)
+    kv[..., :T0, :] = kv0
+    rk = np.full((L, B, H, Wn, hd), np.nan, np.float32)
+    rv = rk.copy()
+    for l in range(L):
+        for j, (kk, vv) in enumerate(st.cache[l]):
+            pos = T0 - len(st.cache[l]) + j
+            rk[l, :, :, pos % Wn], rv[l, :, :, pos % Wn] = kk, vv
+    return dict(s=np.asarray(st.s, np.float32), rk=rk, rv=rv, e=e, mem=mem, kv=kv, pos=T0, T_max=Tm)
+
+
+def _gen(h, c, W, state, n, CS, Bc, seed, tau=1.0, k=0):
+    """n emulated generation steps from state (see _prefill_state); returns
+    the tokens, their log-probabilities and the state after them."""
+    B = state["s"].shape[0]
+    keep = []
+
+    def f32(x):
+        a = np.ascontiguousarray(np.asarray(x, np.float32))
+        keep.append(a)
+        return a.ctypes.data
+
+    s, rk, rv, kv = (np.array(state[key], np.float32) for key in ("s", "rk", "rv", "kv"))
+    e_out, m_out = np.array(state["e"], np.float32), np.array(state["mem"], np.float32)
+    lp, status, toks = np.zeros((B, n), np.float32), np.zeros(1, np.int32), np.full((B, n), -7, np.int32)
+    P = [f32(W[p]) for p in MATS] + [f32(W[p]) for p in VECS] + [f32(state["e"]), f32(state["mem"])]
+    P += [s.ctypes.data, rk.ctypes.data, rv.ctypes.data, None, None, None, lp.ctypes.data, None, None,
+          status.ctypes.data]
+    Q = [f32(W["tok_emb"]), f32(W["enc_attn_norm"]), f32(W["enc_ffn_norm"]), f32(W["enc_norm"]), f32(W["W_K"]),
+         f32(W["W_V"]), kv.ctypes.data, toks.ctypes.data, e_out.ctypes.data, m_out.ctypes.data]
+    p0 = state["pos"]
+    sh = [B, state["T_max"], c.d, c.n_heads, c.head_dim, c.d_ffn, c.n_layers, c.window, c.vocab, c.mem_groups,
+          1 if c.gate_mode == 0 else 0, p0, n, k, CS, Bc, c.mem_source, seed >> 32, seed & 0xffffffff]
+    rc = h.fused_gen_emu((ctypes.c_int * len(sh))(*sh), (ctypes.c_float * 3)(c.rms_eps, c.rope_theta, tau),
+                         (ctypes.c_void_p * len(P))(*P), (ctypes.c_void_p * len(Q))(*Q))
+    assert rc == 0 and status[0] == 0
+    return toks, lp, dict(s=s, rk=rk, rv=rv, e=e_out, mem=m_out, kv=kv, pos=p0 + n, T_max=state["T_max"])
+
+
+def _gen_cfg(G=2, mem_source=0, gate_mode=0):
+    c = ri.RLTConfig(d=64, n_layers=2, n_heads=2, head_dim=32, d_ffn=96, window=3, mem_groups=G, vocab=40,
+                     dtype="bf16", gate_mode=gate_mode, mem_source=mem_source)
+    return c, ri.make_weights(c, 5, norm_jitter=0.1)
+
+
+SEED = 0x12345678ABCD
+
+
+@pytest.mark.parametrize("kw,ckw", [
+    (dict(CS=2, Bc=3), {}),
+    (dict(CS=4, Bc=8, B=9), {}),                              # one full and one ragged cluster
+    (dict(CS=2, Bc=4), dict(mem_source=1)),                   # memory group l from encoder layer l
+    (dict(CS=2, Bc=3, k=5, tau=0.8), {}),                     # tempered top-k draws
+    (dict(CS=2, Bc=3), dict(gate_mode=1, G=1)),               # the gate discards s; one memory group
+])
+def test_fused_generation_matches_the_oracle(fz, kw, ckw):
+    """The generated tokens, fed to the oracle teacher-forced (encoder over
+    prompt + generated tokens, decoder from H_0): every draw is the oracle's
+    draw at the same uniform number (unless that number lies within 1e-3 of a
+    CDF boundary), and the draw's log-probability, the final state and the
+    encoder rows, memory rows and encoder cache the kernel wrote agree within
+    bf16 rounding (the incremental encoder keeps the attention weights in
+    fp32 where the token-parallel oracle rounds them to bf16)."""
+    kw = dict(kw)
+    B = kw.pop("B", 5)
+    k, tau = kw.pop("k", 0), kw.pop("tau", 1.0)
+    c, W = _gen_cfg(**ckw)
+    T0, n = 5, 4
+    prompt = (np.arange(B * T0).reshape(B, T0) * 7 % c.vocab).astype(np.int32)
+    toks, lp, st = _gen(fz, c, W, _prefill_state(c, W, prompt, n), n, kw["CS"], kw["Bc"], SEED, tau, k)
+    cfg = O.Cfg.of(c)
+    full = np.concatenate([prompt, toks], 1)
+    e, mem, kv = O.encode(cfg, W, full, return_kv=True)
+    acts = np.concatenate([full[:, 1:], np.full((B, 1), -1)], 1).astype(np.int32)
+    ref, out = O.decode_steps(cfg, W, O.init_state(cfg, W, B), e, mem, T0 + n, acts, tau, k,
+                              emit=range(T0 - 1, T0 + n - 1))
+    assert np.abs(lp - out.logp[:, T0 - 1:T0 + n - 1]).max() <= 5e-3
+    assert np.abs(st["s"] - ref.s).max() <= 1e-2 * np.abs(ref.s).max()
+    for got, want in ((st["e"][:, T0:], e[:, T0:]), (st["mem"][..., T0:, :], mem[..., T0:, :]),
+                      (st["kv"][..., T0:, :], kv[..., T0:, :])):
+        assert np.abs(got - want).max() <= 2e-2 * np.abs(want).max()
+    for b in range(B):
+        for j in range(n):
+            row, u = out.logits[T0 - 1 + j][b], O.uniform24(SEED, b, T0 + j)
+            want = O.sample_token(row, u, tau, k)
+            if toks[b, j] != want:
+                assert np.abs(np.cumsum(O.sampling_distribution(row, tau, k)) - u).min() < 1e-3, (b, j)
+
+
+def test_fused_generation_call_split_is_bitwise(fz):
+    """Draws use the uniform number of the absolute position, so generating
+    4 tokens in one call or in calls of 1 and 3 gives the same tokens,
+    log-probabilities, state and written rows, bit for bit."""
+    c, W = _gen_cfg()
+    B, T0 = 5, 5
+    prompt = (np.arange(B * T0).reshape(B, T0) * 7 % c.vocab).astype(np.int32)
+    st0 = _prefill_state(c, W, prompt, 4)
+    t4, lp4, s4 = _gen(fz, c, W, st0, 4, 2, 3, SEED)
+    ta, la, sa = _gen(fz, c, W, st0, 1, 2, 3, SEED)
+    tb, lb, sb = _gen(fz, c, W, sa, 3, 2, 3, SEED)
+    assert np.array_equal(np.concatenate([ta, tb], 1), t4)
+    assert np.array_equal(np.concatenate([la, lb], 1), lp4)
+    for key in ("s", "rk", "rv", "e", "mem", "kv"):
+        assert np.array_equal(sb[key], s4[key], equal_nan=True), key
