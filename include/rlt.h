@@ -201,6 +201,10 @@ RLT_API int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, c
  *                    another order, so the two paths agree to rounding, not
  *                    bitwise.  Splitting n across calls is bit-identical
  *                    within this path.
+ *                    On this path rlt_generate runs too: per token the draw,
+ *                    the incremental encoder step (embedding, every encoder
+ *                    layer against the encoder cache, RMSNorm_e, the memory
+ *                    rows) and the decoder step, all n tokens in one launch.
  *  RLT_DECODE_AUTO   the graph path.
  * cluster_size 0 lets the fused path choose per call among 16, 8, 4, 2, 1
  * CTAs per cluster: the most sequences per cluster whose working set fits in

@@ -1415,8 +1415,15 @@ int decode_impl(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const i
 
 fused::Shape fused_shape(const rlt_config& c) {
   return fused::Shape{c.d_model, c.n_heads, c.head_dim, c.d_ffn, c.n_layers, c.window, c.vocab, c.mem_groups,
-                      c.gate_mode == RLT_GATE_DISCARD_S ? 0 : 1};
+                      c.gate_mode == RLT_GATE_DISCARD_S ? 0 : 1, c.mem_source == RLT_MEM_PER_LAYER ? 1 : 0};
 }
+
+// Generation through the persistent kernel (rlt_generate on the fused path).
+struct FusedGen {
+  bf16* enc_kv;
+  int32_t* tokens;
+  unsigned long long seed;
+};
 
 // The kernel's launch attributes for smem bytes of dynamic shared memory
 // (clusters of up to 16 CTAs are outside the portable size 8).
@@ -1459,7 +1466,7 @@ int fused_choose(const rlt_model* m, int B, fused::Plan* out) {
 }
 
 int decode_fused(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const int32_t* emit_steps, void* ws,
-                 cudaStream_t st) {
+                 cudaStream_t st, const FusedGen* gen = nullptr) {
   const rlt_config& c = m->cfg;
   const int B = sst->batch;
   fused::Plan P;
@@ -1492,8 +1499,20 @@ int decode_fused(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, const 
   a.xattn_norm = w.dec_xattn_norm;
   a.ffn_norm = w.dec_ffn_norm;
   a.head_norm = w.head_norm;
-  a.e = static_cast<const bf16*>(A.e);
-  a.mem = static_cast<const bf16*>(A.mem);
+  a.e = static_cast<bf16*>(const_cast<void*>(A.e));  // written only in generation
+  a.mem = static_cast<bf16*>(const_cast<void*>(A.mem));
+  if (gen) {
+    a.gen = 1;
+    a.tok_emb = static_cast<const bf16*>(w.tok_emb);
+    a.enc_attn_norm = w.enc_attn_norm;
+    a.enc_ffn_norm = w.enc_ffn_norm;
+    a.enc_norm = w.enc_norm;
+    a.W_K = static_cast<const bf16*>(w.W_K);
+    a.W_V = static_cast<const bf16*>(w.W_V);
+    a.enc_kv = gen->enc_kv;
+    a.tokens = gen->tokens;
+    a.seed = gen->seed;
+  }
   a.actions = A.actions;
   a.emit_map = at<int>(ws, Lw.emit);
   a.logits_out = A.logits;
@@ -1883,6 +1902,23 @@ int rlt_generate(const rlt_model* m, rlt_state* st, void* e, void* mem, void* en
   if (st->pos < 0 || (int64_t)st->pos + n > T_max) return RLT_ERANGE;
   if (ws_bytes < layout(m, st->batch, T_max).total) return RLT_EWORKSPACE;
   if (n == 0) return RLT_OK;
+  if (m->decode_path == RLT_DECODE_FUSED) {
+    DecodeArgs A;
+    A.e = e;
+    A.mem = mem;
+    A.T_mem = T_max;
+    A.n = n;
+    A.actions = nullptr;
+    A.inv_temp = 1.0f / temperature;
+    A.top_k = top_k;
+    A.logp = logp;
+    A.logp_full = nullptr;
+    A.argmax = nullptr;
+    A.logits = nullptr;
+    A.n_emit = 0;
+    const FusedGen g{static_cast<bf16*>(enc_kv), tokens, (unsigned long long)seed};
+    return decode_fused(m, st, A, nullptr, ws, reinterpret_cast<cudaStream_t>(stream), &g);
+  }
   return gen_impl(m, st, static_cast<bf16*>(e), static_cast<bf16*>(mem), static_cast<bf16*>(enc_kv), T_max, n,
                   (unsigned long long)seed, 1.0f / temperature, top_k, tokens, logp, ws,
                   reinterpret_cast<cudaStream_t>(stream));
