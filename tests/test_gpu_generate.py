@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 
 class Gen:
-    def __init__(self, B=4, T0=24, T_max=64, name="small"):
+    def __init__(self, B=4, T0=24, T_max=64, name="small", path=None):
         import recurrent_looped_transformer_rlt_b300 as rlt
         from recurrent_looped_transformer_rlt_b300 import runner
         self.rlt, self.runner = rlt, runner
@@ -31,6 +31,8 @@ class Gen:
         self.B, self.T0, self.T_max = B, T0, T_max
         self.tok = ri.make_tokens(self.wl, B=B, T=T0)
         self.model = rlt.Model(c, self.W)
+        if path:
+            self.model.set_decode_path(path)
         dt = self.model.dtype
         self.e = torch.empty(B, T_max, c.d, dtype=dt, device="cuda")
         self.mem = torch.empty(c.mem_groups, 2, B, c.n_heads, T_max, c.head_dim, dtype=dt, device="cuda")
@@ -57,8 +59,8 @@ class Gen:
         return rc, toks.cpu().numpy()[:, :n], lp.cpu().numpy()[:, :n]
 
 
-def test_generation_matches_the_oracle_on_the_generated_sequence():
-    g = Gen()
+def test_generation_matches_the_oracle_on_the_generated_sequence(path=None):
+    g = Gen(path=path)
     B, T0, n, seed, tau, k = g.B, g.T0, 40, 123, 0.8, 5
     st = g.prefill()
     rc, gtok, glp = g.generate(st, n, seed, tau, k)
@@ -99,8 +101,8 @@ def test_generation_matches_the_oracle_on_the_generated_sequence():
     g.model.close()
 
 
-def test_generation_does_not_depend_on_the_call_split():
-    ga, gb = Gen(B=3, T0=16, T_max=48), Gen(B=3, T0=16, T_max=48)
+def test_generation_does_not_depend_on_the_call_split(path=None):
+    ga, gb = Gen(B=3, T0=16, T_max=48, path=path), Gen(B=3, T0=16, T_max=48, path=path)
     sa, sb = ga.prefill(), gb.prefill()
     _, ta, la = ga.generate(sa, 24, 5, 1.0, 0)
     _, t1, l1 = gb.generate(sb, 9, 5, 1.0, 0)
