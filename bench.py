@@ -708,6 +708,7 @@ def run_generate_case(args):
     W = ri.make_weights(c, wl.seed)
     tok = ri.make_tokens(wl, B=B, T=T0)
     model = rlt.Model(c, W)
+    model.set_decode_path(args.decode_path)  # the prompt's decode and the generation both take it
     dt = model.dtype
     e = torch.empty(B, T, c.d, dtype=dt, device="cuda")
     mem = torch.empty(c.mem_groups, 2, B, c.n_heads, T, c.head_dim, dtype=dt, device="cuda")
@@ -741,7 +742,8 @@ def run_generate_case(args):
     if rlt.rlt_status(ws, stream) != 0:
         raise RuntimeError("device status flag set")
     t = float(np.mean(ts))
-    print(json.dumps({"case": "generate", "workload": wl.name, "B": B, "prompt": T0, "generated": n,
+    print(json.dumps({"case": "generate", "workload": wl.name, "decode_path": args.decode_path, "B": B,
+                      "prompt": T0, "generated": n,
                       "tokens_per_s": round(B * n / t, 1), "us_per_token_step": round(1e6 * t / n, 2),
                       "calls": len(ts), "temperature": wl.temperature, "top_k": wl.top_k,
                       "timing": "CUDA events around rlt_generate (graph capture and all generated steps)"}),
