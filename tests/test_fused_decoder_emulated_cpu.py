@@ -334,3 +334,24 @@ def test_fused_generation_call_split_is_bitwise(fz):
     assert np.array_equal(np.concatenate([la, lb], 1), lp4)
     for key in ("s", "rk", "rv", "e", "mem", "kv"):
         assert np.array_equal(sb[key], s4[key], equal_nan=True), key
+
+
+def test_fused_generation_small_workload_plan(fz):
+    """Generation with the plan the library picks for the small bf16 model
+    (16 CTAs per cluster, 8 sequences, four memory groups), two tokens."""
+    c = ri.preset("small").cfg
+    W = ri.make_weights(c, 3, norm_jitter=0.1)
+    B, T0, n = 8, 4, 2
+    prompt = (np.arange(B * T0).reshape(B, T0) * 3 % c.vocab).astype(np.int32)
+    toks, lp, st = _gen(fz, c, W, _prefill_state(c, W, prompt, n), n, 16, 8, SEED, 0.7, 20)
+    cfg = O.Cfg.of(c)
+    full = np.concatenate([prompt, toks], 1)
+    e, mem = O.encode(cfg, W, full)
+    acts = np.concatenate([full[:, 1:], np.full((B, 1), -1)], 1).astype(np.int32)
+    ref, out = O.decode_steps(cfg, W, O.init_state(cfg, W, B), e, mem, T0 + n, acts, 0.7, 20,
+                              emit=range(T0 - 1, T0 + n - 1))
+    assert np.abs(lp - out.logp[:, T0 - 1:T0 + n - 1]).max() <= 5e-3
+    assert np.abs(st["s"] - ref.s).max() <= 1e-2 * np.abs(ref.s).max()
+    agree = sum(int(toks[b, j] == O.sample_token(out.logits[T0 - 1 + j][b], O.uniform24(SEED, b, T0 + j), 0.7, 20))
+                for b in range(B) for j in range(n))
+    assert agree >= B * n - 1
