@@ -365,6 +365,9 @@ RLT_API int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t sn
  * (on the model's capture stream; one graph for the recording step and one
  * per slot of a 16-step block) and replayed on the caller's stream;
  * RLT_BPTT_NO_GRAPHS launches them one by one instead (same results).
+ * Memory gradient: on bf16 models with head_dim 32, 64 or 128 it runs on the
+ * tensor cores (bf16 MMA operands: the queries, output gradients, P and dS
+ * rounded to bf16); RLT_BPTT_CORE_MEMGRAD keeps it on CUDA cores in fp32.
  * Work: a forward pass recording s_t and every position's keys and values,
  * then a reverse pass that recomputes each step's activations; workspace
  * rlt_bptt_workspace_size(m, B, n) bytes (its first 256 bytes are the status
@@ -373,7 +376,7 @@ RLT_API int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t sn
  * RLT_EWORKSPACE, RLT_EUNSUPPORTED (bf16 model with vocab not a multiple of
  * 8, or B * n_heads > 65535); an action >= V sets RLT_EBOUNDS in the status
  * word and counts as absent. */
-enum { RLT_DETACH_CACHE = 1, RLT_DETACH_MEMORY = 2, RLT_BPTT_NO_GRAPHS = 4 };
+enum { RLT_DETACH_CACHE = 1, RLT_DETACH_MEMORY = 2, RLT_BPTT_NO_GRAPHS = 4, RLT_BPTT_CORE_MEMGRAD = 8 };
 typedef struct rlt_grads {
   float *W_g, *b_g, *W_qkv, *W_O, *W_Qx, *W_Ox, *W_1, *W_3, *W_2, *W_o;
   float *dec_attn_norm, *dec_xattn_norm, *dec_ffn_norm, *head_norm, *s_star;

@@ -57,7 +57,7 @@ class rlt_state(ctypes.Structure):
 
 GRAD_FIELDS = ["W_g", "b_g", "W_qkv", "W_O", "W_Qx", "W_Ox", "W_1", "W_3", "W_2", "W_o", "dec_attn_norm",
                "dec_xattn_norm", "dec_ffn_norm", "head_norm", "s_star"]
-RLT_DETACH_CACHE, RLT_DETACH_MEMORY, RLT_BPTT_NO_GRAPHS = 1, 2, 4
+RLT_DETACH_CACHE, RLT_DETACH_MEMORY, RLT_BPTT_NO_GRAPHS, RLT_BPTT_CORE_MEMGRAD = 1, 2, 4, 8
 
 
 class rlt_grads(ctypes.Structure):

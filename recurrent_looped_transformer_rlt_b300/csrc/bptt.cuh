@@ -21,6 +21,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "fused_ptx.cuh"
 
 namespace rlt {
 namespace bptt {
@@ -1281,6 +1282,142 @@ __global__ void __launch_bounds__(kMemWarps * 32) mem_grad_kernel(
       }
     }
   }
+}
+
+// Memory gradient on the tensor cores (bf16 models): the sums of
+// mem_grad_kernel as a flash-attention backward without the query gradient.
+// Per (b, h) and 16-key tile of a warp, over the block's queries in chunks of
+// 16 (staged in shared memory as bf16, row-major and transposed):
+//   S^T = K Q^T, dP^T = V G^T          (keys x queries, bf16 MMAs over hd)
+//   P^T = exp(scale S^T - lse), zero for keys past the query's position,
+//   dS^T = P^T (dP^T - D),
+//   dK += (scale dS^T) Q,  dV += P^T G  (MMAs over the queries)
+// with the accumulators in registers for the whole block of steps and one
+// fp32 read-modify-write per key at the end.  The MMA operands q, g, P and
+// dS are rounded to bf16 (the CUDA-core kernel keeps them in fp32).
+constexpr int kMgWarps = 4, kMgKeys = 16 * kMgWarps, kMgQ = 16;
+template <int HD>
+__global__ void __launch_bounds__(kMgWarps * 32) mem_grad_tc_kernel(
+    const bf16* __restrict__ K, const bf16* __restrict__ V, int T_mem, const float* __restrict__ qS,
+    const float* __restrict__ gS, const float* __restrict__ lse_all, const float* __restrict__ DS, int L, int l0,
+    int l1, int nb, int p_hi, int B, int H, float scale, float* __restrict__ dK, float* __restrict__ dV) {
+  __shared__ __align__(16) bf16 sq[kMgQ][HD + 8];
+  __shared__ __align__(16) bf16 sg[kMgQ][HD + 8];
+  __shared__ __align__(16) bf16 sqT[HD][kMgQ + 8];
+  __shared__ __align__(16) bf16 sgT[HD][kMgQ + 8];
+  __shared__ float sl[kMgQ], sD[kMgQ];
+  __shared__ int sp[kMgQ];
+  constexpr int NK = HD / 16, NN = HD / 8;
+  const int bh = blockIdx.y, b = bh / H, h = bh - b * H, d = H * HD, nl = l1 - l0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
+  const int jb = blockIdx.x * kMgKeys;
+  if (jb > p_hi) return;  // uniform over the block
+  const int j0 = jb + warp * 16;  // this warp's keys j0 .. j0 + 15
+  const int s_end = min(nb, p_hi - jb + 1);
+  const int nq = s_end * nl;
+  const size_t base = (size_t)bh * T_mem;
+  auto ldpair = [&](const bf16* M, int row, int col) -> unsigned {  // elements (row, col), (row, col + 1)
+    return row > p_hi ? 0u : *reinterpret_cast<const unsigned*>(M + (base + row) * HD + col);
+  };
+  auto spair = [](const bf16* p) { return *reinterpret_cast<const unsigned*>(p); };
+  auto pack = [](float lo, float hi) {
+    return (unsigned)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((unsigned)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+  };
+  unsigned ka[NK][4], va[NK][4];  // the warp's K and V rows as A operands (16 keys x 16 of hd)
+#pragma unroll
+  for (int kk = 0; kk < NK; ++kk) {
+    const int c0 = 16 * kk + 2 * c;
+    ka[kk][0] = ldpair(K, j0 + g, c0);
+    ka[kk][1] = ldpair(K, j0 + g + 8, c0);
+    ka[kk][2] = ldpair(K, j0 + g, c0 + 8);
+    ka[kk][3] = ldpair(K, j0 + g + 8, c0 + 8);
+    va[kk][0] = ldpair(V, j0 + g, c0);
+    va[kk][1] = ldpair(V, j0 + g + 8, c0);
+    va[kk][2] = ldpair(V, j0 + g, c0 + 8);
+    va[kk][3] = ldpair(V, j0 + g + 8, c0 + 8);
+  }
+  float dk[NN][4], dv[NN][4];
+#pragma unroll
+  for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dk[nn][q] = dv[nn][q] = 0.f;
+  for (int q0 = 0; q0 < nq; q0 += kMgQ) {
+    const int cnt = min(kMgQ, nq - q0);
+    __syncthreads();  // the previous chunk is consumed
+    for (int e = threadIdx.x; e < kMgQ * HD; e += blockDim.x) {
+      const int qi = e / HD, i = e - qi * HD;
+      float qv = 0.f, gv = 0.f;
+      if (qi < cnt) {
+        const int s = (q0 + qi) / nl, l = l0 + (q0 + qi) - s * nl;
+        const size_t row = ((size_t)s * L + l) * B + b;
+        qv = qS[row * d + h * HD + i];
+        gv = gS[row * d + h * HD + i];
+      }
+      const bf16 qb = __float2bfloat16_rn(qv), gb = __float2bfloat16_rn(gv);
+      sq[qi][i] = qb;
+      sqT[i][qi] = qb;
+      sg[qi][i] = gb;
+      sgT[i][qi] = gb;
+    }
+    for (int qi = threadIdx.x; qi < kMgQ; qi += blockDim.x) {
+      if (qi < cnt) {
+        const int s = (q0 + qi) / nl, l = l0 + (q0 + qi) - s * nl, p = p_hi - s;
+        sp[qi] = p;
+        sl[qi] = lse_all[(((size_t)p * L + l) * B + b) * H + h];
+        sD[qi] = DS[(((size_t)s * L + l) * B + b) * H + h];
+      } else {  // padding: every key masked
+        sp[qi] = -1;
+        sl[qi] = 0.f;
+        sD[qi] = 0.f;
+      }
+    }
+    __syncthreads();
+    if (j0 > p_hi) continue;  // uniform over the warp
+    float st[2][4] = {}, dpt[2][4] = {};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int kk = 0; kk < NK; ++kk) {
+        const unsigned bq[2] = {spair(&sq[8 * nt + g][16 * kk + 2 * c]), spair(&sq[8 * nt + g][16 * kk + 2 * c + 8])};
+        const unsigned bg[2] = {spair(&sg[8 * nt + g][16 * kk + 2 * c]), spair(&sg[8 * nt + g][16 * kk + 2 * c + 8])};
+        fused::mma_bf16(st[nt], ka[kk], bq);
+        fused::mma_bf16(dpt[nt], va[kk], bg);
+      }
+    float P[2][4], dS[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int key = j0 + g + 8 * (q >> 1), qi = 8 * nt + 2 * c + (q & 1);
+        const float pv = key <= sp[qi] ? expf(st[nt][q] * scale - sl[qi]) : 0.f;
+        P[nt][q] = pv;
+        dS[nt][q] = scale * pv * (dpt[nt][q] - sD[qi]);
+      }
+    // the 16 x 16 accumulator tiles as A operands (queries on k)
+    const unsigned pa[4] = {pack(P[0][0], P[0][1]), pack(P[0][2], P[0][3]), pack(P[1][0], P[1][1]),
+                            pack(P[1][2], P[1][3])};
+    const unsigned sa[4] = {pack(dS[0][0], dS[0][1]), pack(dS[0][2], dS[0][3]), pack(dS[1][0], dS[1][1]),
+                            pack(dS[1][2], dS[1][3])};
+#pragma unroll
+    for (int nn = 0; nn < NN; ++nn) {
+      const unsigned bq[2] = {spair(&sqT[8 * nn + g][2 * c]), spair(&sqT[8 * nn + g][2 * c + 8])};
+      const unsigned bg[2] = {spair(&sgT[8 * nn + g][2 * c]), spair(&sgT[8 * nn + g][2 * c + 8])};
+      fused::mma_bf16(dk[nn], sa, bq);
+      fused::mma_bf16(dv[nn], pa, bg);
+    }
+  }
+  if (j0 > p_hi) return;
+#pragma unroll
+  for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int key = j0 + g + 8 * (q >> 1), col = 8 * nn + 2 * c + (q & 1);
+      if (key <= p_hi) {
+        dK[(base + key) * HD + col] += dk[nn][q];
+        dV[(base + key) * HD + col] += dv[nn][q];
+      }
+    }
 }
 
 // Merge backward, one thread per column i (loop over sequences):

@@ -17,6 +17,7 @@ struct BpttOps {
   cudaStream_t user; // the caller's stream (graphs are replayed on it)
   cudaStream_t cap;  // the model's capture stream
   bool graphs = true;
+  bool mg_tc = true;  // bf16 models: the memory gradient on the tensor cores (mem_grad_tc_kernel)
   TcScratch sc;
   int* status;
   // one captured step per key: -1 the recording step, s >= 0 the reverse
@@ -264,6 +265,21 @@ struct BpttOps {
   int mem_grad(const T* K, const T* V, int T_mem, const float* qS, const float* gS, const float* lse_all,
                const float* DS, int L, int l0, int l1, int nb, int p_hi, int B, int H, int hd, float scale, float* dK,
                float* dV) {
+    if constexpr (kBf16) {
+      if (mg_tc && (hd == 32 || hd == 64 || hd == 128)) {
+        const dim3 g2(cdiv((size_t)p_hi + 1, bptt::kMgKeys), (unsigned)(B * H));
+        if (hd == 32)
+          bptt::mem_grad_tc_kernel<32><<<g2, bptt::kMgWarps * 32, 0, st>>>(K, V, T_mem, qS, gS, lse_all, DS, L, l0, l1,
+                                                                           nb, p_hi, B, H, scale, dK, dV);
+        else if (hd == 64)
+          bptt::mem_grad_tc_kernel<64><<<g2, bptt::kMgWarps * 32, 0, st>>>(K, V, T_mem, qS, gS, lse_all, DS, L, l0, l1,
+                                                                           nb, p_hi, B, H, scale, dK, dV);
+        else
+          bptt::mem_grad_tc_kernel<128><<<g2, bptt::kMgWarps * 32, 0, st>>>(K, V, T_mem, qS, gS, lse_all, DS, L, l0,
+                                                                            l1, nb, p_hi, B, H, scale, dK, dV);
+        return post();
+      }
+    }
     const dim3 grid(cdiv((size_t)p_hi + 1, bptt::kMemKeys), (unsigned)(B * H));
     bptt::mem_grad_kernel<T><<<grid, bptt::kMemWarps * 32, 0, st>>>(K, V, T_mem, qS, gS, lse_all, DS, L, l0, l1, nb,
                                                                     p_hi, B, H, hd, scale, dK, dV);
@@ -320,7 +336,8 @@ bpplan::Shape bptt_shape(const rlt_model* m, int B, int n, int T_mem, float temp
 
 template <typename T_>
 int bptt_impl(const rlt_model* m, const bpplan::Shape& S, const bpplan::Detach& D,
-              const bpplan::Io<T_>& io, const bpplan::Grads& G, void* ws, cudaStream_t st, bool graphs) {
+              const bpplan::Io<T_>& io, const bpplan::Grads& G, void* ws, cudaStream_t st, bool graphs,
+              bool mg_tc) {
   const rlt_weights& w = m->w;
   bpplan::Params<T_> P;
   P.W_g = static_cast<const T_*>(w.W_g);
@@ -344,6 +361,7 @@ int bptt_impl(const rlt_model* m, const bpplan::Shape& S, const bpplan::Detach& 
   k.user = st;
   k.cap = m->cap_stream;
   k.graphs = graphs;
+  k.mg_tc = mg_tc;
   k.status = static_cast<int*>(ws);
   k.sc.n_sm = m->n_sm;
   k.sc.maxc = m->gemm_maxc;
@@ -382,7 +400,7 @@ int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, 
   if (!m || !e || !mem || !actions || !loss || !grads || !ws) return RLT_EINVAL;
   if (B <= 0 || n <= 0 || T_mem < n) return RLT_EINVAL;
   if (!(temperature > 0.f) || top_k < 0 || detach_s_every < 0) return RLT_EINVAL;
-  if (flags & ~(RLT_DETACH_CACHE | RLT_DETACH_MEMORY | RLT_BPTT_NO_GRAPHS)) return RLT_EINVAL;
+  if (flags & ~(RLT_DETACH_CACHE | RLT_DETACH_MEMORY | RLT_BPTT_NO_GRAPHS | RLT_BPTT_CORE_MEMGRAD)) return RLT_EINVAL;
   const float* gp[] = {grads->W_g, grads->b_g, grads->W_qkv, grads->W_O, grads->W_Qx, grads->W_Ox, grads->W_1,
                        grads->W_3, grads->W_2, grads->W_o, grads->dec_attn_norm, grads->dec_xattn_norm,
                        grads->dec_ffn_norm, grads->head_norm, grads->s_star};
@@ -405,6 +423,7 @@ int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, 
   D.cache = (flags & RLT_DETACH_CACHE) != 0;
   D.memory = (flags & RLT_DETACH_MEMORY) != 0;
   const bool graphs = (flags & RLT_BPTT_NO_GRAPHS) == 0;
+  const bool mg_tc = (flags & RLT_BPTT_CORE_MEMGRAD) == 0;
   bpplan::Grads G;
   G.W_g = grads->W_g;
   G.b_g = grads->b_g;
@@ -424,10 +443,10 @@ int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t T_mem, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (m->cfg.dtype == RLT_BF16) {
     bpplan::Io<bf16> io{static_cast<const bf16*>(e), static_cast<const bf16*>(mem), actions, loss, logp, d_e, d_mem};
-    return bptt_impl<bf16>(m, S, D, io, G, ws, s, graphs);
+    return bptt_impl<bf16>(m, S, D, io, G, ws, s, graphs, mg_tc);
   }
   bpplan::Io<float> io{static_cast<const float*>(e), static_cast<const float*>(mem), actions, loss, logp, d_e, d_mem};
-  return bptt_impl<float>(m, S, D, io, G, ws, s, graphs);
+  return bptt_impl<float>(m, S, D, io, G, ws, s, graphs, mg_tc);
 }
 
 }  // extern "C"

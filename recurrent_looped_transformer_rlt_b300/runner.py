@@ -7,9 +7,9 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (GRAD_FIELDS, RLT_BPTT_NO_GRAPHS, RLT_DETACH_CACHE, RLT_DETACH_MEMORY, Model, State, rlt_bptt,
-               rlt_bptt_workspace_size,
-               rlt_decode_steps, rlt_encode, rlt_grads, rlt_state_init, rlt_status, rlt_workspace_init)
+from . import (GRAD_FIELDS, RLT_BPTT_CORE_MEMGRAD, RLT_BPTT_NO_GRAPHS, RLT_DETACH_CACHE, RLT_DETACH_MEMORY,
+               Model, State, rlt_bptt, rlt_bptt_workspace_size, rlt_decode_steps, rlt_encode, rlt_grads,
+               rlt_state_init, rlt_status, rlt_workspace_init)
 
 
 @dataclass
@@ -80,9 +80,10 @@ class BpttResult:
 def bptt(model: Model, buf: Buffers, actions: torch.Tensor, temperature: float = 1.0, top_k: int = 0,
          detach_s_every: int = 0, detach_cache: bool = False, detach_memory: bool = False,
          want_inputs: bool = True, ws: Optional[torch.Tensor] = None, graphs: bool = True,
-         stream=None) -> BpttResult:
+         core_memgrad: bool = False, stream=None) -> BpttResult:
     """Loss and gradients of the teacher-forced sequence (rlt_bptt) over the
-    first n = actions.shape[1] positions of buf's encoder output and memory."""
+    first n = actions.shape[1] positions of buf's encoder output and memory.
+    core_memgrad: the memory gradient on CUDA cores (RLT_BPTT_CORE_MEMGRAD)."""
     B, n = actions.shape
     actions = actions.contiguous()
     assert actions.dtype == torch.int32 and B == buf.B
@@ -99,6 +100,7 @@ def bptt(model: Model, buf: Buffers, actions: torch.Tensor, temperature: float =
     logp = torch.empty(B, n, device="cuda")
     flags = (RLT_DETACH_CACHE if detach_cache else 0) | (RLT_DETACH_MEMORY if detach_memory else 0)
     flags |= 0 if graphs else RLT_BPTT_NO_GRAPHS
+    flags |= RLT_BPTT_CORE_MEMGRAD if core_memgrad else 0
     rlt_bptt(model.handle, buf.e, buf.mem, buf.T, B, n, actions, temperature, top_k, detach_s_every, flags, loss,
              logp, cg, d_e, d_mem, ws, ws.numel(), stream)
     return BpttResult(loss, logp, grads, d_e, d_mem)

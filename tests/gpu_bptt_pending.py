@@ -140,10 +140,13 @@ def test_fp32_tempered_top_k():
         assert _max_rel(g["grads"][k], gref[k]) <= F32_REL or np.abs(gref[k]).max() == 0, k
 
 
-def test_bf16_gradients_match_the_oracle_on_the_same_weights():
+@pytest.mark.parametrize("core_memgrad", [False, True])
+def test_bf16_gradients_match_the_oracle_on_the_same_weights(core_memgrad):
+    """Both memory-gradient kernels: the tensor-core one (default for bf16
+    models) and the CUDA-core one (RLT_BPTT_CORE_MEMGRAD)."""
     c, W, tok, acts = _setup(dtype="bf16", d=256, H=8, hd=32, f=512, V=64, L=2, G=2, window=4, B=2, T=10, scale=1.0)
     e, mem = _inputs(c, *tok.shape)
-    g = _gpu(c, W, e, mem, acts)
+    g = _gpu(c, W, e, mem, acts, core_memgrad=core_memgrad)
     lref, gref = _oracle(c, W, e, mem, acts)
     assert abs(g["loss"] - lref) <= 2e-3 * max(1.0, abs(lref))
     for k in GRADS:
@@ -235,3 +238,18 @@ def test_bf16_batch_past_one_k_block():
     assert abs(g["loss"] - lref) <= 2e-3 * max(1.0, abs(lref))
     for k in GRADS:
         assert _fro(g["grads"][k], gref[k]) <= BF16_FRO, k
+
+
+@pytest.mark.parametrize("hd,T", [(64, 70), (128, 40)])
+def test_bf16_tensor_core_memory_gradient_head_widths(hd, T):
+    """The tensor-core memory gradient at head widths 64 and 128 over more
+    keys than one 64-key block, against the CUDA-core kernel on the same
+    inputs (relative Frobenius error of d_mem within bf16 operand rounding)."""
+    c, W, tok, acts = _setup(dtype="bf16", d=2 * hd, H=2, hd=hd, f=256, V=64, L=1, G=1, window=4, B=2, T=T,
+                             scale=1.0)
+    e, mem = _inputs(c, *tok.shape)
+    a = _gpu(c, W, e, mem, acts)
+    b = _gpu(c, W, e, mem, acts, core_memgrad=True)
+    assert _fro(a["d_mem"], b["d_mem"]) <= 1e-2
+    lref, gref = _oracle(c, W, e, mem, acts)
+    assert _fro(a["d_mem"], gref["mem"]) <= BF16_FRO

@@ -49,7 +49,7 @@ inline thread_local unsigned emu_rank = 0;
 inline thread_local std::barrier<>* emu_cluster_bar = nullptr;
 inline thread_local char* const* emu_cluster_smem = nullptr;
 inline std::vector<char> emu_dyn;
-#define __align__(n) alignas(n)
+#define __align__(n) __attribute__((aligned(n)))
 
 #define __global__
 #define __device__
