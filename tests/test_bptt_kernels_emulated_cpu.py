@@ -200,3 +200,20 @@ def test_emulated_kernels_have_no_unordered_shared_accesses(emu, tmp_path):
     env = dict(os.environ, EMU_JITTER="1")
     r = subprocess.run([sys.executable, str(script)], capture_output=True, text=True, env=env, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_emulated_tensor_core_memory_gradient_wide_heads(emu, hd):
+    """bf16 models take the tensor-core memory gradient (one template per head
+    width): at widths 64 and 128, within bf16 rounding of the oracle."""
+    c = ri.RLTConfig(d=2 * hd, n_layers=1, n_heads=2, head_dim=hd, d_ffn=128, window=2, mem_groups=1, vocab=32,
+                     dtype="bf16")
+    W = ri.make_weights(c, 41, norm_jitter=0.1)
+    B, T = 2, 5
+    e, mem = ri.make_decoder_inputs(c, B, T, 48, mem_scale=0.5)
+    acts = (np.arange(B * T).reshape(B, T) * 5 % c.vocab).astype(np.int32)
+    loss, g, d_e, d_mem = _run(emu, c, W, e, mem, acts, block=16, bf16=True)
+    cfg = O.Cfg.of(ri.RLTConfig(**{**c.__dict__, "dtype": "f32"}))
+    lref, gref = BP.gradients(cfg, W, e, mem, acts)
+    assert np.linalg.norm((d_mem - gref["mem"]).ravel()) <= 1e-2 * np.linalg.norm(gref["mem"].ravel())
+    assert abs(loss - lref) <= 1e-3 * abs(lref)
