@@ -139,6 +139,7 @@ def _check(c, got, ref_st, ref, T):
     dict(CS=2, Bc=3, G=1, window=5, T=11),            # one memory group; the ring wraps
     dict(CS=4, Bc=2, d=128, hd=64, f=200, V=70),      # 64-wide heads, ragged f and V tiles
     dict(CS=2, Bc=5, split=(3, 4), emit=(0, 5)),      # three calls, logits of two steps
+    dict(CS=2, Bc=2, B=2, L=1, G=1, window=70, T=75),     # window over several row passes; the ring wraps
 ])
 def test_fused_decoder_matches_the_oracle(fz, kw):
     c, got, ref_st, ref = _case(fz, **kw)
