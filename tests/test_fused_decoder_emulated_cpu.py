@@ -270,8 +270,8 @@ def _gen(h, c, W, state, n, CS, Bc, seed, tau=1.0, k=0):
     return toks, lp, dict(s=s, rk=rk, rv=rv, e=e_out, mem=m_out, kv=kv, pos=p0 + n, T_max=state["T_max"])
 
 
-def _gen_cfg(G=2, mem_source=0, gate_mode=0):
-    c = ri.RLTConfig(d=64, n_layers=2, n_heads=2, head_dim=32, d_ffn=96, window=3, mem_groups=G, vocab=40,
+def _gen_cfg(G=2, mem_source=0, gate_mode=0, hd=32, window=3):
+    c = ri.RLTConfig(d=2 * hd, n_layers=2, n_heads=2, head_dim=hd, d_ffn=96, window=window, mem_groups=G, vocab=40,
                      dtype="bf16", gate_mode=gate_mode, mem_source=mem_source)
     return c, ri.make_weights(c, 5, norm_jitter=0.1)
 
@@ -285,6 +285,7 @@ SEED = 0x12345678ABCD
     (dict(CS=2, Bc=4), dict(mem_source=1)),                   # memory group l from encoder layer l
     (dict(CS=2, Bc=3, k=5, tau=0.8), {}),                     # tempered top-k draws
     (dict(CS=2, Bc=3), dict(gate_mode=1, G=1)),               # the gate discards s; one memory group
+    (dict(CS=4, Bc=3), dict(hd=64, window=1)),                # 64-wide heads; the window holds the current token
 ])
 def test_fused_generation_matches_the_oracle(fz, kw, ckw):
     """The generated tokens, fed to the oracle teacher-forced (encoder over
