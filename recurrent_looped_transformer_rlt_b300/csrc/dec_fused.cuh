@@ -932,6 +932,14 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           break;
         }
         case kEQKV: {  // encoder layer l at p: q, k, v, cache row p, causal attention over rows 0..p
+          if (l + 1 < s.L && p > 0) {  // the next layer's cache rows 0..p-1 into L2
+            for (int j = tid; j < 2 * wk.npairs; j += kThreads) {
+              const int pi = j >> 1, kv = j & 1;
+              prefetch_l2(a.enc_kv + ((((size_t)(l + 1) * 2 + kv) * a.B + b0 + pair_b(pi)) * H + pair_h(pi)) *
+                                         (size_t)a.T_mem * hd,
+                          (unsigned)p * hd * 2);
+            }
+          }
           if (l == 0) {
             for (int i2 = tid; i2 < nbv * d; i2 += kThreads) {
               const int b = i2 / d, j = i2 - b * d;
