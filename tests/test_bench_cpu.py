@@ -113,3 +113,18 @@ def test_fused_roofline_counts_every_step_once():
     r = bench.fused_roofline(wl, total / bw, bw, "test")
     assert r["frac"] == pytest.approx(1.0, abs=1e-3) and r["launches"] == 1 and r["bound"] == "hbm"
     assert bench.fused_roofline(wl, 2 * total / bw, bw, "test")["frac"] == pytest.approx(0.5, abs=1e-3)
+
+
+def test_fused_case_bytes_are_the_steps_it_runs():
+    """--profile-case fused times n steps from p0 = T/2 - n/2: its bytes are
+    those of steps p0 + 1 .. p0 + n, the decoder weights once per step plus
+    the memory read growing with t."""
+    wl = ri.preset("small")
+    c, B, T = wl.cfg, wl.B, wl.T
+    n = 32
+    p0 = T // 2 - n // 2
+    total = sum(bench.step_bytes(c, B, p + 1) for p in range(p0, p0 + n))
+    mid = bench.step_bytes(c, B, p0 + n // 2)
+    assert total == pytest.approx(n * mid, rel=0.02)     # linear in t: the mean is the middle step
+    assert bench.step_bytes(c, B, p0 + n) - bench.step_bytes(c, B, p0 + 1) == \
+        (n - 1) * c.n_layers * bench.xattn_bytes(c, B, 1)
