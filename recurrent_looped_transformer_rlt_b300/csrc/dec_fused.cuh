@@ -163,10 +163,16 @@ __device__ __forceinline__ Ph phase_at(const Args& a, int k, int r, const Work& 
     }
   }
   if (kd >= 0) {
+    // decoding with a gate: the head of the previous step runs right after
+    // the gate (between the halves of its cluster barrier) on the CTAs that
+    // score; otherwise it ends the step
+    const bool hov = !a.gen && s.gate;
     if (s.gate && kd == 0) {
       ph.kind = kGate;
+    } else if (hov && scorer && kd == 1) {
+      ph.kind = kHead;
     } else {
-      const int kk = kd - (s.gate ? 1 : 0);
+      const int kk = kd - (s.gate ? 1 : 0) - (hov && scorer ? 1 : 0);
       if (kk < 6 * s.L) {
         ph.kind = kQKV + kk % 6;
         ph.l = kk / 6;
@@ -779,15 +785,20 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   };
   const int kdec0 = a.gen ? 1 + enc_phases(s) : 0;  // the decoder step's first phase
   const int PPS = kdec0 + (s.gate ? 1 : 0) + 6 * s.L + (a.gen ? 0 : (scorer ? 1 : 0));
-  const int NPH = a.n * PPS;
+  const bool hov = !a.gen && s.gate;      // the head of step i - 1 runs after step i's gate
+  const bool tail = hov && scorer;        // ... and the last step's head after the loop
+  const int NPH = a.n * PPS + (tail ? 1 : 0);
+  auto phase_of = [&](int qq) {  // phase qq of the launch (the tail: the head, phase 1 of a step)
+    return phase_at(a, qq < a.n * PPS ? qq % PPS : 1, r, wk, scorer);
+  };
   auto stage_of = [&](int q) { return stage + (size_t)(q & 1) * P.stage_units * kUnitBytes; };
   // phase q's weights go to stage q mod 2; they are requested right after
   // phase q - 2's projection has read that half (one cp.async group per
   // phase), so each copy has most of two phases to land
-  issue(a, phase_at(a, 0, r, wk, scorer), r, wk, stage_of(0));
+  issue(a, phase_of(0), r, wk, stage_of(0));
   issue_e(0);
   cp_async_commit();
-  if (NPH > 1) issue(a, phase_at(a, 1 % PPS, r, wk, scorer), r, wk, stage_of(1));
+  if (NPH > 1) issue(a, phase_of(1), r, wk, stage_of(1));
   cp_async_commit();
   prefetch_mem(0, a.p0);
 
@@ -806,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
       // the projection of this phase, then the request of phase q + 2 into the half it has read
       auto project = [&](const bf16* X, int ldX, bool reduce = false) {
         const PY y = proj(ph, cols, stg, X, ldX, out, part, reduce);
-        if (q + 2 < NPH) issue(a, phase_at(a, (k + 2) % PPS, r, wk, scorer), r, wk, stg);
+        if (q + 2 < NPH) issue(a, phase_of(q + 2), r, wk, stg);
         if (k == 0 && i + 1 < a.n) issue_e(i + 1);  // e of the next step, landed long before its first phase
         cp_async_commit();
         return y;
@@ -840,7 +851,8 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
             }
             push(reinterpret_cast<float4*>(hcur + (size_t)b * d + row), make_float4(v[0], v[1], v[2], v[3]), CS);
           }
-          cluster_sync();
+          cluster_arrive();
+          if (!(hov && scorer)) cluster_wait();  // the CTAs that score wait after the previous step's head
           break;
         }
         case kQKV: {
@@ -1005,14 +1017,33 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           __syncthreads();
           break;
         }
-        default: {  // head
-          rmsnorm_x(hcur, a.head_norm);
-          project(xb, P.ldx, true);  // logits materialised in out: the scoring reads them many times
-          for (int b = r; b < nbv; b += CS) head_col(a, out, cols, b, b0 + b, i, p, misc, sx, tokb);
+        default: {  // head (logits materialised in out: the scoring reads them many times)
+          if (!hov) {
+            rmsnorm_x(hcur, a.head_norm);
+            project(xb, P.ldx, true);
+            for (int b = r; b < nbv; b += CS) head_col(a, out, cols, b, b0 + b, i, p, misc, sx, tokb);
+          } else {  // the previous step's head, s_{p} = hprev; nothing to score before the first step
+            if (i > 0) {
+              rmsnorm_x(hprev, a.head_norm);
+            } else {
+              __syncthreads();  // the gate's epilogue has read the partial sums
+            }
+            project(xb, P.ldx, true);
+            if (i > 0)
+              for (int b = r; b < nbv; b += CS) head_col(a, out, cols, b, b0 + b, i - 1, p - 1, misc, sx, tokb);
+            cluster_wait();
+          }
           break;
         }
       }
     }
+  }
+  if (tail) {  // the last step's head
+    cp_async_wait1();
+    __syncthreads();
+    rmsnorm_x(hb + (size_t)((a.n - 1) & 1) * cols * d, a.head_norm);
+    proj(phase_of(NPH - 1), cols, stage_of(NPH - 1), xb, P.ldx, out, part, true);
+    for (int b = r; b < nbv; b += CS) head_col(a, out, cols, b, b0 + b, a.n - 1, a.p0 + a.n - 1, misc, sx, tokb);
   }
   cp_async_wait0();
   // s_n: the last step's streams

@@ -10,6 +10,7 @@
 // Each 32-bit register holds two bf16, the lower column in the low half.
 // Test infrastructure only.
 #pragma once
+#include <optional>
 #include "emu.h"
 
 namespace rlt {
@@ -18,6 +19,13 @@ namespace fused {
 inline unsigned cluster_rank() { return emu_rank; }
 inline void cluster_sync() {
   emu_cluster_bar->arrive_and_wait();
+  if (emu_jitter()) emu_jitter_sleep();
+}
+inline thread_local std::optional<std::barrier<>::arrival_token> emu_cluster_token;
+inline void cluster_arrive() { emu_cluster_token.emplace(emu_cluster_bar->arrive()); }
+inline void cluster_wait() {
+  emu_cluster_bar->wait(std::move(*emu_cluster_token));
+  emu_cluster_token.reset();
   if (emu_jitter()) emu_jitter_sleep();
 }
 template <class T>
