@@ -91,3 +91,19 @@ def test_unsupported_head_dim_reported():
     w = rlt.rlt_weights(*([16] * len(rlt.WEIGHT_FIELDS)))
     h = ctypes.c_void_p()
     assert rlt._model_create(ctypes.byref(cfg), ctypes.byref(w), 0, ctypes.byref(h)) == rlt.RLT_EUNSUPPORTED
+
+
+def test_decode_path_calls_reject_bad_arguments_without_gpu():
+    """rlt_set_decode_path and rlt_fused_plan validate on the host: a null
+    model, an unknown path, a cluster size that is not 0, 1, 2, 4, 8 or 16, a
+    non-positive batch."""
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    assert rlt._set_decode_path(None, rlt.RLT_DECODE_FUSED, 0) == rlt.RLT_EINVAL
+    out = [ctypes.c_int32() for _ in range(4)]
+    assert rlt._fused_plan(None, 8, *[ctypes.byref(x) for x in out]) == rlt.RLT_EINVAL
+    # a fake (non-null) handle is never dereferenced before the argument checks fail
+    fake = ctypes.c_void_p(16)
+    assert rlt._set_decode_path(fake, 3, 0) == rlt.RLT_EINVAL
+    assert rlt._set_decode_path(fake, rlt.RLT_DECODE_FUSED, 3) == rlt.RLT_EINVAL
+    assert rlt._set_decode_path(fake, rlt.RLT_DECODE_FUSED, 32) == rlt.RLT_EINVAL
+    assert rlt._fused_plan(fake, 0, *[ctypes.byref(x) for x in out]) == rlt.RLT_EINVAL
