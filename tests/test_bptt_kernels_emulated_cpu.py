@@ -179,7 +179,8 @@ def test_emulated_kernels_production_chunk(emu64):
 def test_emulated_kernels_have_no_unordered_shared_accesses(emu, tmp_path):
     """Two runs with EMU_JITTER=1 (a random sleep after every block barrier,
     so that an access no barrier orders gives run-dependent results) are
-    bitwise identical."""
+    bitwise identical: an fp32 model, and a bf16 model (tensor-core memory
+    gradient)."""
     lib = emu._name
     script = tmp_path / "jitter.py"
     script.write_text(
@@ -190,13 +191,20 @@ def test_emulated_kernels_have_no_unordered_shared_accesses(emu, tmp_path):
         "from tests import test_bptt_schedule_cpu as S\n"
         f"h = ctypes.CDLL({lib!r})\n"
         "h.bptt_emu.restype = ctypes.c_int\n"
+        "import rlt_inputs as ri\n"
         "c, W, e, mem, acts = S._setup(T=9, window=7)\n"
-        "a = E._run(h, c, W, e, mem, acts)\n"
-        "b = E._run(h, c, W, e, mem, acts)\n"
-        "assert a[0] == b[0]\n"
-        "for k in a[1]:\n"
-        "    assert np.array_equal(a[1][k], b[1][k]), k\n"
-        "assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])\n")
+        "cb = ri.RLTConfig(d=64, n_layers=1, n_heads=2, head_dim=32, d_ffn=96, window=3, mem_groups=1, vocab=32,\n"
+        "                  dtype='bf16')\n"
+        "Wb = ri.make_weights(cb, 41, norm_jitter=0.1)\n"
+        "eb, mb = ri.make_decoder_inputs(cb, 2, 5, 48, mem_scale=0.5)\n"
+        "ab = (np.arange(10).reshape(2, 5) * 5 % 32).astype(np.int32)\n"
+        "for args, kw in (((c, W, e, mem, acts), {}), ((cb, Wb, eb, mb, ab), dict(block=16, bf16=True))):\n"
+        "    a = E._run(h, *args, **kw)\n"
+        "    b = E._run(h, *args, **kw)\n"
+        "    assert a[0] == b[0]\n"
+        "    for k in a[1]:\n"
+        "        assert np.array_equal(a[1][k], b[1][k]), k\n"
+        "    assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])\n")
     env = dict(os.environ, EMU_JITTER="1")
     r = subprocess.run([sys.executable, str(script)], capture_output=True, text=True, env=env, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
