@@ -115,3 +115,19 @@ def test_fused_generation_matches_the_oracle():
 def test_fused_generation_call_split_bitwise():
     from tests import test_gpu_generate as TG
     TG.test_generation_does_not_depend_on_the_call_split(path="fused")
+
+
+def test_fused_plan_of_the_small_workload():
+    """The plan the bench's workload gets: 16-CTA clusters of 8 sequences,
+    8 clusters, all resident at once (one wave).  A failure here means the
+    device holds fewer 16-CTA clusters than the design assumes (two waves)."""
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    wl = ri.preset("small")
+    m = rlt.Model(wl.cfg, ri.make_weights(wl.cfg, wl.seed))
+    m.set_decode_path("fused")
+    plan = m.fused_plan(wl.B)
+    m.close()
+    assert plan is not None
+    cs, bc, ncl, smem = plan
+    assert cs == 16 and bc == 8 and ncl == 8, plan
+    assert smem <= 232448
