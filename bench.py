@@ -247,6 +247,8 @@ def run_gpu(args, rank, world, local_rank):
     tok, prompt, acts = rank_inputs(wl, rank)
     model = rlt.Model(c, W, device=dev)
     model.set_decode_path(args.decode_path)
+    if args.decode_path == "fused" and model.fused_plan(B) is None:
+        raise SystemExit(f"the fused decoder does not take the {wl.name} model (rlt_fused_plan)")
     stream = torch.cuda.current_stream()
     buf = runner.alloc_buffers(model, B, T)
     tok_d = torch.from_numpy(tok).to(dev)
