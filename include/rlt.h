@@ -184,7 +184,10 @@ RLT_API int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, c
                      const int32_t* emit_steps, int32_t n_emit, float* logits,
                      void* ws, size_t ws_bytes, rlt_stream_t stream);
 
-/* Decoder path of rlt_decode_steps.
+/* Decoder path of rlt_decode_steps (both compute the transition above; the
+ * step stays sequential in t while independent sequences share the launch -
+ * "Princeton Researcher Proposes Recurrent Looped Transformer ...", design
+ * principles paragraph).
  *  RLT_DECODE_GRAPH  one step is captured as a CUDA graph of per-operation
  *                    kernels (tensor-core projections with split-K clusters,
  *                    attention, norms, head) and replayed n times.  Every
@@ -209,8 +212,10 @@ RLT_API int rlt_decode_steps(const rlt_model* m, rlt_state* st, const void* e, c
  * cluster_size 0 lets the fused path choose per call among 16, 8, 4, 2, 1
  * CTAs per cluster: the most sequences per cluster whose working set fits in
  * shared memory, the fewest waves of clusters the device holds at once, then
- * the largest cluster; 1, 2, 4, 8 or 16 forces the cluster size.  Host-side setting of the model object; not thread-safe with
- * concurrent calls on the same model. */
+ * the largest cluster; 1, 2, 4, 8 or 16 forces the cluster size.
+ * Host-side setting of the model object; not thread-safe with concurrent
+ * calls on the same model.  Errors: RLT_EINVAL (null model, unknown path or
+ * cluster size). */
 enum { RLT_DECODE_AUTO = 0, RLT_DECODE_GRAPH = 1, RLT_DECODE_FUSED = 2 };
 RLT_API int rlt_set_decode_path(rlt_model* m, int32_t path, int32_t cluster_size);
 
