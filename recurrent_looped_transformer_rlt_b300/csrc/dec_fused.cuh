@@ -261,14 +261,16 @@ __device__ __forceinline__ Tile tile_at(const Args& a, const Ph& ph, int t, int 
 // with the 16 columns of one MMA taken as 8 (L % 4) + {0, 1, 2, 3} and the
 // other's as + {4, 5, 6, 7} (B uses the same pairing).  Rows past N and
 // columns past K are zero.
-__device__ __forceinline__ void issue(const Args& a, const Ph& ph, int r, const Work& wk, unsigned char* stg) {
+__device__ __forceinline__ void issue(const Args& a, const Ph& ph, int r, const Work& wk, unsigned char* stg, int t0,
+                                      int t1) {
+  // tiles t0 .. t1 - 1 of the phase, unit (t - t0, u) at ((t - t0) U + u);
   // thread t copies piece t % 64 of units t / 64, t / 64 + kThreads / 64, ...
   const int jj = threadIdx.x & 63, half = jj >> 5, ln = jj & 31;
   const int rofs = (ln >> 2) + 8 * half, kofs = 8 * (ln & 3);
-  const int nunits = ph.nt * ph.U;
+  const int nunits = (t1 - t0) * ph.U;
   constexpr int kStep = kThreads / 64;
-  int t = 0, u = threadIdx.x >> 6;
-  while (u >= ph.U && t < ph.nt) {
+  int t = t0, u = threadIdx.x >> 6;
+  while (u >= ph.U && t < t1) {
     u -= ph.U;
     ++t;
   }
@@ -317,7 +319,7 @@ struct PY {
 // partial sums stay in part (reduce: added into out here, in split order).
 // Ends with a block barrier; the stage is no longer read after it.
 __device__ __forceinline__ PY proj(const Ph& ph, int cols, const unsigned char* stg, const bf16* X, int ldX,
-                                   float* out, float* part, bool reduce) {
+                                   float* out, float* part, bool reduce, int tout = 0) {
   const int nt = ph.nt, U = ph.U, NT = cols / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   if (nt == 0) return PY{out, part, cols, 0};
@@ -344,7 +346,7 @@ __device__ __forceinline__ PY proj(const Ph& ph, int cols, const unsigned char* 
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         if (j < NT) {
-          float* o0 = out + (size_t)(t * 16 + g) * cols + 8 * j + 2 * c;
+          float* o0 = out + (size_t)((tout + t) * 16 + g) * cols + 8 * j + 2 * c;
           float* o1 = o0 + 8 * cols;
           o0[0] = acc[j][0];
           o0[1] = acc[j][1];
@@ -370,7 +372,7 @@ __device__ __forceinline__ PY proj(const Ph& ph, int cols, const unsigned char* 
   if (!reduce) return y;
   for (int e = threadIdx.x; e < nt * 16 * cols; e += kThreads) {
     const int tt = e / (16 * cols), rem = e - tt * 16 * cols, row = rem / cols, col = rem - row * cols;
-    out[e] = y(tt, row, col);
+    out[(size_t)tout * 16 * cols + e] = y(tt, row, col);
   }
   __syncthreads();
   return PY{out, part, cols, 0};
@@ -787,18 +789,44 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   const int PPS = kdec0 + (s.gate ? 1 : 0) + 6 * s.L + (a.gen ? 0 : (scorer ? 1 : 0));
   const bool hov = !a.gen && s.gate;      // the head of step i - 1 runs after step i's gate
   const bool tail = hov && scorer;        // ... and the last step's head after the loop
-  const int NPH = a.n * PPS + (tail ? 1 : 0);
-  auto phase_of = [&](int qq) {  // phase qq of the launch (the tail: the head, phase 1 of a step)
-    return phase_at(a, qq < a.n * PPS ? qq % PPS : 1, r, wk, scorer);
+  // A phase whose tiles do not fit one stage half runs its projection in
+  // parts (tile ranges of tpp tiles), each a pipeline step of its own; the
+  // pipeline's steps are numbered over the launch (PSS per decoder step,
+  // then the tail's)
+  auto tpp_of = [&](const Ph& ph) { return max(1, P.stage_units / ph.U); };
+  auto nparts_of = [&](const Ph& ph) { return ph.nt == 0 ? 1 : (ph.nt + tpp_of(ph) - 1) / tpp_of(ph); };
+  int PSS = 0;
+  for (int k = 0; k < PPS; ++k) PSS += nparts_of(phase_at(a, k, r, wk, scorer));
+  const Ph ph_tail = phase_at(a, 1, r, wk, scorer);  // the head (phase 1 of a step when it is the tail)
+  const int NQ = a.n * PSS + (tail ? nparts_of(ph_tail) : 0);
+  auto issue_step = [&](int qq, unsigned char* stg) {  // weights of pipeline step qq
+    Ph ph;
+    int pt;
+    if (qq >= a.n * PSS) {
+      ph = ph_tail;
+      pt = qq - a.n * PSS;
+    } else {
+      int j = qq % PSS;
+      for (int k = 0;; ++k) {
+        ph = phase_at(a, k, r, wk, scorer);
+        const int np = nparts_of(ph);
+        if (j < np) break;
+        j -= np;
+      }
+      pt = j;
+    }
+    const int tpp = tpp_of(ph), t0 = pt * tpp;
+    issue(a, ph, r, wk, stg, min(t0, ph.nt), min(ph.nt, t0 + tpp));
   };
   auto stage_of = [&](int q) { return stage + (size_t)(q & 1) * P.stage_units * kUnitBytes; };
-  // phase q's weights go to stage q mod 2; they are requested right after
-  // phase q - 2's projection has read that half (one cp.async group per
-  // phase), so each copy has most of two phases to land
-  issue(a, phase_of(0), r, wk, stage_of(0));
+  // step q's weights go to stage q mod 2; they are requested right after
+  // step q - 2's projection has read that half (one cp.async group per
+  // step), so each copy has most of two steps to land
+  int qc = 0;  // the pipeline step being computed
+  issue_step(0, stage_of(0));
   issue_e(0);
   cp_async_commit();
-  if (NPH > 1) issue(a, phase_of(1), r, wk, stage_of(1));
+  if (NQ > 1) issue_step(1, stage_of(1));
   cp_async_commit();
   prefetch_mem(0, a.p0);
 
@@ -809,18 +837,31 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     const bf16* ecur = eb + (size_t)(i & 1) * cols * d;  // e_p, rows of the cluster's sequences
     const float2* rope_row = rb + (size_t)(i & 1) * half;  // (cos, sin) of position p
     for (int k = 0; k < PPS; ++k) {
-      const int q = i * PPS + k;
       const Ph ph = phase_at(a, k, r, wk, scorer);
-      cp_async_wait1();  // this phase's group (the next phase's may still be in flight)
+      cp_async_wait1();  // this step's group (the next step's may still be in flight)
       __syncthreads();
-      unsigned char* stg = stage_of(q);
-      // the projection of this phase, then the request of phase q + 2 into the half it has read
+      // the projection of this phase (in parts when it has more tiles than a
+      // stage half holds), each part followed by the request of pipeline
+      // step qc + 2 into the half it has read
       auto project = [&](const bf16* X, int ldX, bool reduce = false) {
-        const PY y = proj(ph, cols, stg, X, ldX, out, part, reduce);
-        if (q + 2 < NPH) issue(a, phase_of(q + 2), r, wk, stg);
-        if (k == 0 && i + 1 < a.n) issue_e(i + 1);  // e of the next step, landed long before its first phase
-        cp_async_commit();
-        return y;
+        const int np = nparts_of(ph), tpp = tpp_of(ph);
+        PY y{out, part, cols, 0};
+        for (int pt = 0; pt < np; ++pt) {
+          if (pt > 0) {
+            cp_async_wait1();
+            __syncthreads();
+          }
+          unsigned char* stg = stage_of(qc);
+          Ph sub = ph;
+          const int t0 = min(pt * tpp, ph.nt);
+          sub.nt = min(ph.nt, t0 + tpp) - t0;
+          y = proj(sub, cols, stg, X, ldX, out, part, reduce || np > 1, t0);
+          if (qc + 2 < NQ) issue_step(qc + 2, stg);
+          if (k == 0 && pt == 0 && i + 1 < a.n) issue_e(i + 1);  // the next step's e, landed long before it is read
+          cp_async_commit();
+          ++qc;
+        }
+        return np > 1 ? PY{out, part, cols, 0} : y;
       };
       if (k == kdec0 && !s.gate) {  // the gate discards s: h = e_p
         for (int i2 = tid; i2 < nbv * d; i2 += kThreads) hcur[i2] = __bfloat162float(ecur[i2]);
@@ -1039,10 +1080,19 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     }
   }
   if (tail) {  // the last step's head
-    cp_async_wait1();
-    __syncthreads();
     rmsnorm_x(hb + (size_t)((a.n - 1) & 1) * cols * d, a.head_norm);
-    proj(phase_of(NPH - 1), cols, stage_of(NPH - 1), xb, P.ldx, out, part, true);
+    const int np = nparts_of(ph_tail), tpp = tpp_of(ph_tail);
+    for (int pt = 0; pt < np; ++pt) {
+      cp_async_wait1();
+      __syncthreads();
+      Ph sub = ph_tail;
+      const int t0 = min(pt * tpp, ph_tail.nt);
+      sub.nt = min(ph_tail.nt, t0 + tpp) - t0;
+      proj(sub, cols, stage_of(qc), xb, P.ldx, out, part, true, t0);
+      if (qc + 2 < NQ) issue_step(qc + 2, stage_of(qc));
+      cp_async_commit();
+      ++qc;
+    }
     for (int b = r; b < nbv; b += CS) head_col(a, out, cols, b, b0 + b, a.n - 1, a.p0 + a.n - 1, misc, sx, tokb);
   }
   cp_async_wait0();

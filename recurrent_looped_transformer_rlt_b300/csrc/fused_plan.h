@@ -54,7 +54,7 @@ struct Plan {
   int npairs;  // most (sequence, head) pairs of a CTA
   int ldx, ldo, ldm;  // row pitches (elements) of the bf16 operand buffers
   int maxT;           // most 16-row tiles of one phase on one CTA
-  int stage_units;    // units of one stage buffer
+  int stage_units;    // units of one stage half (a phase with more runs in parts)
   size_t o_h, o_x, o_ob, o_mb, o_out, o_part, o_pr, o_ring, o_xp, o_misc, o_e, o_he, o_tok, o_sx, o_stage, total;
 };
 
@@ -111,7 +111,6 @@ inline int make_plan(const Shape& s, int B, int CS, int Bc, Plan* P) {
   take(td, Uf);       // W_2
   take(tv, Ud);       // head
   p.maxT = maxT;
-  p.stage_units = units;
   size_t off = 0;
   auto put = [&](size_t bytes) {
     size_t o = off;
@@ -132,6 +131,18 @@ inline int make_plan(const Shape& s, int B, int CS, int Bc, Plan* P) {
   p.o_he = put((size_t)p.cols * s.d * 4);                            // generation: the encoder's residual streams
   p.o_tok = put((size_t)p.cols * 4);                                 // generation: the drawn tokens
   p.o_sx = put((size_t)s.V * 4);                                     // the scored row's tempered logits
+  // the weight stage: two halves of the largest phase's units, or, when that
+  // does not fit, of what does (phases with more tiles then run in parts;
+  // one tile of the widest K must fit)
+  const size_t rest = off;
+  if (rest + (size_t)2 * units * kUnitBytes > kMaxSmem) {
+    const int room = rest < kMaxSmem ? (int)((kMaxSmem - rest) / (2 * kUnitBytes)) : 0;
+    int umax = Ud > Uf ? Ud : Uf;
+    if (s.gate && U2 > umax) umax = U2;
+    if (room < umax) return -1;
+    units = room;
+  }
+  p.stage_units = units;
   p.o_stage = put((size_t)2 * units * kUnitBytes);
   p.total = off;
   if (p.total > kMaxSmem) return -1;

@@ -357,3 +357,23 @@ def test_fused_generation_small_workload_plan(fz):
     agree = sum(int(toks[b, j] == O.sample_token(out.logits[T0 - 1 + j][b], O.uniform24(SEED, b, T0 + j), 0.7, 20))
                 for b in range(B) for j in range(n))
     assert agree >= B * n - 1
+
+
+@pytest.mark.parametrize("CS,Bc", [(16, 10), (8, 8)])
+def test_fused_decoder_phases_in_parts(fz, CS, Bc):
+    """Plans whose largest weight phases exceed a stage half (10 sequences
+    on 16-CTA clusters; 8-CTA clusters) run those projections in tile-range
+    parts, each its own pipeline step: the small model, two steps."""
+    c = ri.preset("small").cfg
+    W = ri.make_weights(c, 3, norm_jitter=0.1)
+    B, n = Bc, 2
+    e, mem = ri.make_decoder_inputs(c, B, n, 7, mem_scale=0.5)
+    acts = (np.arange(B * n).reshape(B, n) * 5 % c.vocab).astype(np.int32)
+    cfg = O.Cfg.of(c)
+    st0 = O.init_state(cfg, W, B)
+    rk = np.full((c.n_layers, B, c.n_heads, c.window, c.head_dim), np.nan, np.float32)
+    got = _call(fz, c, W, e, mem, st0.s, rk, rk.copy(), acts, 0, n, CS, Bc)
+    ref_st, ref = O.decode_steps(cfg, W, st0, e, mem, n, acts)
+    assert np.abs(got["s"] - ref_st.s).max() <= 2e-3 * np.abs(ref_st.s).max()
+    assert np.nanmax(np.abs(got["logp"] - ref.logp)) <= 2e-3 * max(1.0, np.nanmax(np.abs(ref.logp)))
+    assert (got["argmax"] == ref.argmax).mean() >= 0.95

@@ -73,8 +73,22 @@ def test_small_batches_spread_over_clusters(shim):
 def test_forced_cluster_sizes(shim):
     c = ri.preset("small").cfg
     assert choose(shim, c, 64, force=16)["CS"] == 16
-    # 8 CTAs per cluster: each CTA's W_1/W_3 rows need a 192 KB weight stage
-    assert choose(shim, c, 64, force=8) is None
+    # 8 CTAs per cluster: each CTA's W_1/W_3 rows (96 units) exceed what a
+    # stage half can hold next to the doubled window ring, so the phase runs
+    # in parts; the plan still fits
+    p = choose(shim, c, 64, force=8)
+    assert (p["CS"], p["Bc"], p["nclu"]) == (8, 4, 16) and p["smem"] <= SMEM_MAX   # 18 clusters fit: spread
+    assert make(shim, c, 64, 8, 8)["smem"] <= SMEM_MAX
+    p4 = choose(shim, c, 64, force=4)                # two heads per CTA: only 2 sequences per cluster fit
+    assert (p4["CS"], p4["Bc"], p4["nclu"]) == (4, 2, 32)
+
+
+def test_fewer_16_cta_clusters_take_more_sequences_each(shim):
+    """With only 7 co-resident 16-CTA clusters, the weight phases run in
+    parts so that 10 sequences fit a cluster: 7 clusters, one wave."""
+    c = ri.preset("small").cfg
+    p = choose(shim, c, 64, mac=(148, 74, 37, 16, 7))
+    assert (p["CS"], p["Bc"], p["nclu"]) == (16, 10, 7) and p["smem"] <= SMEM_MAX
 
 
 def test_shapes_the_plan_rejects(shim):
