@@ -194,7 +194,8 @@ def test_fused_decoder_has_no_unordered_shared_accesses(fz, tmp_path):
     block and cluster barrier, so a shared-memory access not ordered by a
     barrier gives results that differ between runs (a barrier removed from
     the kernel does).  Three jittered runs of a 4-CTA cluster case and of a
-    two-column-tile case must be bitwise identical."""
+    two-column-tile case must be bitwise identical, and two of generation
+    (token exchange, encoder cache, per-layer memory rows)."""
     lib = os.path.join(os.path.dirname(fz._name), "libfused.so")
     script = tmp_path / "jitter.py"
     script.write_text(
@@ -207,7 +208,14 @@ def test_fused_decoder_has_no_unordered_shared_accesses(fz, tmp_path):
         "for kw in (dict(CS=4, Bc=8, B=11), dict(CS=2, Bc=16, B=17)):\n"
         "    runs = [T._case(h, **kw)[1] for _ in range(3)]\n"
         "    for k in ('s', 'rk', 'rv', 'logp', 'logp_full', 'argmax'):\n"
-        "        assert all(np.array_equal(runs[0][k], r[k], equal_nan=True) for r in runs[1:]), (kw, k)\n")
+        "        assert all(np.array_equal(runs[0][k], r[k], equal_nan=True) for r in runs[1:]), (kw, k)\n"
+        "c, W = T._gen_cfg(mem_source=1)\n"
+        "prompt = (np.arange(20).reshape(4, 5) * 7 % c.vocab).astype(np.int32)\n"
+        "st0 = T._prefill_state(c, W, prompt, 3)\n"
+        "g = [T._gen(h, c, W, st0, 3, 4, 4, T.SEED, 0.8, 5) for _ in range(2)]\n"
+        "assert np.array_equal(g[0][0], g[1][0]) and np.array_equal(g[0][1], g[1][1])\n"
+        "for k in ('s', 'rk', 'rv', 'e', 'mem', 'kv'):\n"
+        "    assert np.array_equal(g[0][2][k], g[1][2][k], equal_nan=True), k\n")
     env = dict(os.environ, EMU_JITTER="1")
     r = subprocess.run([sys.executable, str(script)], capture_output=True, text=True, env=env, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
