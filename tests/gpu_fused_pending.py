@@ -119,8 +119,8 @@ def test_fused_generation_call_split_bitwise():
 
 def test_fused_plan_of_the_small_workload():
     """The plan the bench's workload gets: 16-CTA clusters of 8 sequences,
-    8 clusters, all resident at once (one wave).  A failure here means the
-    device holds fewer 16-CTA clusters than the design assumes (two waves)."""
+    8 clusters (one per GPC, one wave); with only 7 resident 16-CTA clusters
+    the plan takes 10 sequences each (weight phases in parts)."""
     import recurrent_looped_transformer_rlt_b300 as rlt
     wl = ri.preset("small")
     m = rlt.Model(wl.cfg, ri.make_weights(wl.cfg, wl.seed))
@@ -129,5 +129,5 @@ def test_fused_plan_of_the_small_workload():
     m.close()
     assert plan is not None
     cs, bc, ncl, smem = plan
-    assert cs == 16 and bc == 8 and ncl == 8, plan
+    assert (cs, bc, ncl) in ((16, 8, 8), (16, 10, 7)), plan
     assert smem <= 232448
