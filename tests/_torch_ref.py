@@ -108,3 +108,107 @@ def parallel_decoder(cfg, W, e, mem, window, u=None):
 def head_logits(cfg, W, s):
     a = F.rms_norm(T(s), (cfg.d,), weight=T(W["head_norm"]), eps=cfg.rms_eps)
     return F.linear(a, T(W["W_o"])).numpy()
+
+
+# ---------------------------------------------------------------------------
+# bf16 storage configurations: the same compositions with a rounding to
+# bfloat16 at each storage point of the bf16 numerics contract (every matrix
+# product input, e, the memory, the window keys/values after RoPE, the
+# encoder's q/k/v after RoPE, and the encoder's unnormalised attention
+# weights before they multiply the values).  Rounding uses torch's own
+# float32 and bfloat16 conversions.
+
+def bf16_rne(x):
+    """float64 -> nearest bfloat16 value (ties to even) -> float64, through
+    torch's float32 and bfloat16 conversions.  torch converts float64 through
+    float32, which rounds twice; a value that the float32 step lands exactly
+    on a bfloat16 tie is therefore moved one float32 ulp back towards itself
+    first (the float32 step only carried it onto the tie), which makes the
+    result the single rounding of x."""
+    x = torch.as_tensor(x, dtype=D)
+    f = x.to(torch.float32)
+    back = f.to(D)
+    tie = (f.view(torch.int32) & 0xFFFF) == 0x8000
+    fix = tie & (back != x)
+    toward = torch.where(x > back, torch.full_like(f, math.inf), torch.full_like(f, -math.inf))
+    f = torch.where(fix, torch.nextafter(f, toward), f)
+    return f.to(torch.bfloat16).to(D)
+
+
+def encoder_bf16(cfg, W, tokens):
+    """e [B,T,d] and memory [G,2,B,H,T,hd] of a bf16-storage config."""
+    R = bf16_rne
+    d, H, hd = cfg.d, cfg.n_heads, cfg.head_dim
+    tok = torch.as_tensor(tokens, dtype=torch.long)
+    B, P = tok.shape
+    pos = torch.arange(P)
+    causal = torch.ones(P, P, dtype=torch.bool).tril()
+    h = F.embedding(tok, T(W["tok_emb"]))
+    hidden = []
+    for l in range(cfg.n_layers):
+        a = R(F.rms_norm(h, (d,), weight=T(W["enc_attn_norm"][l]), eps=cfg.rms_eps))
+        q, k, v = F.linear(a, T(W["W_qkv"][l])).split(d, dim=-1)
+        q, k, v = _heads(q, H), _heads(k, H), R(_heads(v, H))
+        q, k = R(rope_complex(q, pos, cfg.rope_theta)), R(rope_complex(k, pos, cfg.rope_theta))
+        s = torch.matmul(q, k.transpose(-1, -2)).div(math.sqrt(hd)).masked_fill(~causal, -math.inf)
+        w = torch.exp(s - s.amax(dim=-1, keepdim=True))
+        o = torch.matmul(R(w), v) / w.sum(dim=-1, keepdim=True)
+        h = h + F.linear(R(_merge_heads(o)), T(W["W_O"][l]))
+        b = R(F.rms_norm(h, (d,), weight=T(W["enc_ffn_norm"][l]), eps=cfg.rms_eps))
+        h = h + F.linear(R(F.silu(F.linear(b, T(W["W_1"][l]))) * F.linear(b, T(W["W_3"][l]))),
+                         T(W["W_2"][l]))
+        hidden.append(h)
+    e = R(F.rms_norm(h, (d,), weight=T(W["enc_norm"]), eps=cfg.rms_eps))
+    mem = []
+    for g in range(cfg.mem_groups):
+        src = R(F.rms_norm(hidden[g], (d,), weight=T(W["enc_norm"]), eps=cfg.rms_eps)) \
+            if getattr(cfg, "mem_source", 0) == 1 else e
+        mem.append(torch.stack([_heads(R(F.linear(src, T(W["W_K"][g]))), H),
+                                _heads(R(F.linear(src, T(W["W_V"][g]))), H)]))
+    return e.numpy(), torch.stack(mem).numpy()
+
+
+def decoder_bf16(cfg, W, e, mem, n):
+    """n recurrent steps of a bf16-storage config from H_0, with the window
+    cache as a list per layer: the current entry is appended, attention runs
+    over the last `window` entries, and the last window - 1 are kept.
+    Returns s_n [B,d], the logits of every step [n][B,V] and the caches
+    (per layer a list of (k, v) [B,H,hd], oldest first)."""
+    R = bf16_rne
+    d, H, hd, Wn = cfg.d, cfg.n_heads, cfg.head_dim, cfg.window
+    e = T(e)
+    B = e.shape[0]
+    s = T(W["s_star"]).expand(B, d).clone()
+    caches = [[] for _ in range(cfg.n_layers)]
+    logits = []
+    for p in range(n):
+        et = e[:, p]
+        if cfg.gate_mode == 1:
+            z = torch.zeros_like(s)
+        else:
+            z = torch.sigmoid(F.linear(R(torch.cat([et, s], dim=-1)), T(W["W_g"]), T(W["b_g"])))
+        h = z * s + (1.0 - z) * et
+        for l in range(cfg.n_layers):
+            a = R(F.rms_norm(h, (d,), weight=T(W["dec_attn_norm"][l]), eps=cfg.rms_eps))
+            q, k, v = F.linear(a, T(W["W_qkv"][l])).split(d, dim=-1)
+            q = rope_complex(q.reshape(B, H, 1, hd), [p], cfg.rope_theta)
+            k = R(rope_complex(k.reshape(B, H, 1, hd), [p], cfg.rope_theta))
+            v = R(v.reshape(B, H, 1, hd))
+            entries = (caches[l] + [(k, v)])[-Wn:]
+            o = F.scaled_dot_product_attention(q, torch.cat([x for x, _ in entries], dim=2),
+                                               torch.cat([x for _, x in entries], dim=2))
+            caches[l] = entries[1:] if len(entries) == Wn else entries
+            h = h + F.linear(R(o.reshape(B, d)), T(W["W_O"][l]))
+            c = R(F.rms_norm(h, (d,), weight=T(W["dec_xattn_norm"][l]), eps=cfg.rms_eps))
+            qx = F.linear(c, T(W["W_Qx"][l])).reshape(B, H, 1, hd)
+            g = 0 if cfg.mem_groups == 1 else l
+            ox = F.scaled_dot_product_attention(qx, T(mem[g, 0, :, :, :p + 1]), T(mem[g, 1, :, :, :p + 1]))
+            h = h + F.linear(R(ox.reshape(B, d)), T(W["W_Ox"][l]))
+            b = R(F.rms_norm(h, (d,), weight=T(W["dec_ffn_norm"][l]), eps=cfg.rms_eps))
+            h = h + F.linear(R(F.silu(F.linear(b, T(W["W_1"][l]))) * F.linear(b, T(W["W_3"][l]))),
+                             T(W["W_2"][l]))
+        s = h
+        a = R(F.rms_norm(s, (d,), weight=T(W["head_norm"]), eps=cfg.rms_eps))
+        logits.append(F.linear(a, T(W["W_o"])).numpy())
+    caches = [[(k[:, :, 0].numpy(), v[:, :, 0].numpy()) for k, v in cl] for cl in caches]
+    return s.numpy(), logits, caches
