@@ -1,11 +1,7 @@
 """GPU parity of the decoder backward (rlt_bptt) against the float64
-autograd oracle (oracle/rlt_bptt.py) - pending its first GPU run.
-
-This module is not collected (its name does not start with test_): the
-backward's device kernels have been checked on the CPU (tests/
-test_bptt_schedule_cpu.py, tests/test_bptt_kernels_emulated_cpu.py) but not
-yet on a GPU.  Run it with `python -m pytest tests/gpu_bptt_pending.py -m gpu`
-on a GPU and rename it to test_gpu_bptt.py once it passes.
+autograd oracle (oracle/rlt_bptt.py).  The schedule and the device kernels
+are also checked on the CPU (tests/test_bptt_schedule_cpu.py,
+tests/test_bptt_kernels_emulated_cpu.py).
 
 fp32 models: every gradient (all decoder parameters, s_*, e, the memory) and
 the loss within fp32 tolerance, for full BPTT and each named detach point.
@@ -193,7 +189,8 @@ def test_argument_errors():
                                     None, None, ws, o.get("wsb", nb), check=False)
     assert call(n=9) == rlt.RLT_EINVAL               # n > T_mem
     assert call(tau=0.0) == rlt.RLT_EINVAL
-    assert call(fl=4) == rlt.RLT_EINVAL
+    assert call(fl=16) == rlt.RLT_EINVAL             # no such flag
+    assert call(se=-1) == rlt.RLT_EINVAL
     assert call(wsb=nb - 1) == rlt.RLT_EWORKSPACE
     assert call() == rlt.RLT_OK
     model.close()
@@ -245,7 +242,7 @@ def test_bf16_tensor_core_memory_gradient_head_widths(hd, T):
     """The tensor-core memory gradient at head widths 64 and 128 over more
     keys than one 64-key block, against the CUDA-core kernel on the same
     inputs (relative Frobenius error of d_mem within bf16 operand rounding)."""
-    c, W, tok, acts = _setup(dtype="bf16", d=2 * hd, H=2, hd=hd, f=256, V=64, L=1, G=1, window=4, B=2, T=T,
+    c, W, tok, acts = _setup(dtype="bf16", d=256, H=256 // hd, hd=hd, f=256, V=64, L=1, G=1, window=4, B=2, T=T,
                              scale=1.0)
     e, mem = _inputs(c, *tok.shape)
     a = _gpu(c, W, e, mem, acts)

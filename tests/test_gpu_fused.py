@@ -1,11 +1,7 @@
 """GPU parity of the persistent cluster decoder (rlt_set_decode_path(...,
-RLT_DECODE_FUSED)) - pending its first GPU run.
-
-This module is not collected (its name does not start with test_): the
-kernel has been checked on the CPU under the host emulation of the CUDA
-execution model (tests/test_fused_decoder_emulated_cpu.py) but not yet on a
-GPU.  Run it with `python -m pytest tests/gpu_fused_pending.py -m gpu` on a
-GPU and rename it to test_gpu_fused.py once it passes.
+RLT_DECODE_FUSED)).  The same kernel is also checked on the CPU under the
+host emulation of the CUDA execution model
+(tests/test_fused_decoder_emulated_cpu.py).
 
 Small bf16 model against the oracle with the bf16 tolerances of the other
 parity tests (relative logit error, argmax agreement), against the graph path
@@ -73,12 +69,12 @@ def test_fused_split_invariance_bitwise():
 
 def test_fused_top_k_and_gate_discard():
     wl, W, tok, acts = _inputs("small", B=6, T=30)
-    emit = [3, 29]
+    emit = list(range(30))
     for kw in (dict(temperature=0.7, top_k=5), dict(gate_mode=1)):
         g = gpu_run(wl, W, tok, acts, emit=emit, decode_path="fused", **kw)
         o = oracle_run(wl, W, tok, acts, emit=emit, **kw)
         assert g["status"] == 0
-        _check_bf16(g, o, emit)
+        _check_bf16(g, o, emit, kw.get("top_k", 0), acts, kw.get("temperature", 1.0))
 
 
 def test_fused_full_size_sampled_rows():
