@@ -128,3 +128,27 @@ def test_fused_case_bytes_are_the_steps_it_runs():
     assert total == pytest.approx(n * mid, rel=0.02)     # linear in t: the mean is the middle step
     assert bench.step_bytes(c, B, p0 + n) - bench.step_bytes(c, B, p0 + 1) == \
         (n - 1) * c.n_layers * bench.xattn_bytes(c, B, 1)
+
+
+def test_segments_cover_every_position_once():
+    """The K bench steps are consecutive rlt_decode_steps ranges that consume
+    positions 0..T-1 exactly once, in order, with lengths differing by at
+    most one."""
+    for T, K in [(4096, 20), (512, 20), (64, 64), (7, 3), (5, 1)]:
+        segs = bench.segments(T, K)
+        assert len(segs) == K
+        p = 0
+        for p0, n in segs:
+            assert p0 == p and n >= 1
+            p += n
+        assert p == T
+        assert max(n for _, n in segs) - min(n for _, n in segs) <= 1
+    with pytest.raises(SystemExit):
+        bench.segments(10, 11)
+
+
+def test_config_names_the_step():
+    import rlt_inputs as ri
+    cfg = bench.workload_config(ri.preset("refdep"), 1, 20)
+    assert cfg["T"] == 4096 and cfg["B_per_gpu"] == 64
+    assert "205 positions" in cfg["step"] and "1..4096" in cfg["step"]

@@ -96,7 +96,7 @@ def test_reference_arm_line_has_the_gpu_arms_keys():
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
     assert line["higher_is_better"] is True and line["value"] > 0
-    assert line["config"] == bench.workload_config(ri.preset("tiny"), 1)
+    assert line["config"] == bench.workload_config(ri.preset("tiny"), 1, 1)
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
