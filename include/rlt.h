@@ -266,12 +266,20 @@ RLT_API int rlt_linear(const rlt_model* m, const void* A, int32_t lda, int32_t M
  *    fit in 16 MiB - 256 B, i.e. B * n_heads <= 1007 at head_dim 128; larger
  *    requests return RLT_EUNSUPPORTED.
  *  - The first call on a device looks up the array's device address (set-up);
- *    make that first call before any stream capture.
+ *    make that first call before any stream capture.  The address is kept
+ *    for the life of the process: do not use the entry point on a device
+ *    after cudaDeviceReset (or another teardown of its primary context).
  *  - Every call shares the array: calls that overlap on the GPU race.
+ *  - Device-side conditions (a bounded wait that gave up) go to a status word
+ *    inside the array, not to a workspace: read and clear it with
+ *    rlt_cross_attention_noalloc_status (it synchronises the stream and
+ *    returns RLT_OK, RLT_ETIMEOUT, or RLT_ECUDA when the set-up or the read
+ *    fails).  The first condition recorded wins until it is read.
  *  - Allocates nothing; its launches are not included in rlt_launch_count(). */
 RLT_API int rlt_cross_attention_noalloc(const float* q, const void* mem_k, const void* mem_v, int32_t B,
                                         int32_t n_heads, int32_t head_dim, int32_t dtype, int32_t T_mem,
                                         int32_t t, void* out, rlt_stream_t stream);
+RLT_API int rlt_cross_attention_noalloc_status(rlt_stream_t stream);
 
 /* Generation ("Understanding and Applying the Recurrent Looped Transformer
  * Architecture", "Prompt prefill" and "Autoregressive generation"): the
@@ -315,27 +323,37 @@ RLT_API int rlt_generate(const rlt_model* m, rlt_state* st, void* e, void* mem, 
  * A snapshot of a state at position pos holds everything needed to continue
  * decoding from there: s_pos, both window caches (ring slots by position mod
  * W, W recorded), pos, and the encoder output e and memory M of positions
- * 1..pos, tagged with the model version and shape.  Restoring it and decoding on gives
- * bit-identical states and log-probabilities to never having stopped
- * (Proposition 3.1), also for another request that shares the prefix (the
- * encoder and memory of positions <= pos depend only on those tokens).
- *   snap: caller-owned device buffer of rlt_snapshot_size(m, B, pos) bytes,
- *         16-byte aligned; layout private to the library (a header, then s,
- *         ring K, ring V, e [B][pos][d], M [G][2][B][H][pos][hd]).
- *   e [B][T_mem][d] and mem [G][2][B][H][T_mem][hd]: the encoder buffers of
- *         rlt_encode; save reads and restore writes their rows 0..pos-1.
+ * 1..pos, tagged with the model version and shape; optionally also the
+ * encoder's key/value cache of positions 1..pos (rlt_encode_kv, rlt_generate),
+ * which is what continuing generation needs.  Restoring it and decoding (or
+ * generating) on gives bit-identical states, tokens and log-probabilities to
+ * never having stopped (Proposition 3.1), also for another request that
+ * shares the prefix (the encoder, its cache and the memory of positions <= pos
+ * depend only on those tokens).
+ *   snap: caller-owned device buffer of rlt_snapshot_size(m, B, pos,
+ *         with_enc_kv) bytes, 16-byte aligned; layout private to the library
+ *         (a header, then s, ring K, ring V, e [B][pos][d],
+ *         M [G][2][B][H][pos][hd], and with the cache section
+ *         [L][2][B][H][pos][hd]).
+ *   e [B][T_mem][d], mem [G][2][B][H][T_mem][hd] and enc_kv
+ *         [L][2][B][H][T_mem][hd]: the encoder buffers of rlt_encode /
+ *         rlt_encode_kv; save reads and restore writes their rows 0..pos-1.
+ *         enc_kv NULL: no cache section (save), the snapshot holds none
+ *         (restore: a snapshot with the section needs enc_kv, one without it
+ *         takes enc_kv NULL).
  * rlt_snapshot_save copies asynchronously on the stream (nothing is read on
  * the host).  rlt_snapshot_restore reads the snapshot's header (it
  * synchronises the stream for that), checks it against the model and the
  * state, then copies asynchronously and sets st->pos and st->version.
  * Errors: RLT_EINVAL (null or misaligned pointer, buffer too small, batch or
- * shape mismatch, pos > T_mem, not a snapshot), RLT_ESTALE (the snapshot, or
- * st for save, was taken under another model version). */
-RLT_API int rlt_snapshot_size(const rlt_model* m, int32_t B, int32_t pos, size_t* bytes);
+ * shape mismatch, pos > T_mem, not a snapshot, cache section asked for and
+ * absent or present and not asked for, with_enc_kv not 0 or 1), RLT_ESTALE
+ * (the snapshot, or st for save, was taken under another model version). */
+RLT_API int rlt_snapshot_size(const rlt_model* m, int32_t B, int32_t pos, int32_t with_enc_kv, size_t* bytes);
 RLT_API int rlt_snapshot_save(const rlt_model* m, const rlt_state* st, const void* e, const void* mem,
-                              int32_t T_mem, void* snap, size_t snap_bytes, rlt_stream_t stream);
+                              const void* enc_kv, int32_t T_mem, void* snap, size_t snap_bytes, rlt_stream_t stream);
 RLT_API int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t snap_bytes, rlt_state* st,
-                                 void* e, void* mem, int32_t T_mem, rlt_stream_t stream);
+                                 void* e, void* mem, void* enc_kv, int32_t T_mem, rlt_stream_t stream);
 
 /* Backpropagation through time of the decoder recurrence, teacher forced
  * ("Recurrent Looped Transformer: A New Architecture for Infinite Context
@@ -391,6 +409,30 @@ RLT_API int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t
                      const int32_t* actions, float temperature, int32_t top_k, int32_t detach_s_every,
                      int32_t flags, float* loss, float* logp, const rlt_grads* grads, float* d_e,
                      float* d_mem, void* ws, size_t ws_bytes, rlt_stream_t stream);
+
+/* Failure injection for the bounded device waits, so that their give-up
+ * path can be exercised without a GPU fault (a wait whose arrival never
+ * comes).  Every wait of the library's kernels on a copy, an MMA or a cluster
+ * peer is bounded by a clock budget (about one second); a wait that runs out
+ * records RLT_ETIMEOUT in the workspace's status word, waits (bounded) for
+ * the launch's other copies in flight, frees its tensor memory and returns.
+ * This call arms that path for the next launch of one kernel through its
+ * standalone entry point on this model:
+ *   RLT_KERNEL_XATTN  rlt_cross_attention: one warp never requests its first
+ *                     value chunk;
+ *   RLT_KERNEL_GEMM   rlt_linear (bf16 models): the first CTA never requests
+ *                     its first A tile (its split-K cluster peers then wait on
+ *                     it at the cluster barrier until it gives up and arrives);
+ * and gives every wait of that launch budget_cycles clock cycles (1e3 ..
+ * 4e9) instead of the default.  The launch's output is then unspecified and
+ * rlt_status() of its workspace returns RLT_ETIMEOUT; later launches are not
+ * affected (one-shot; the attention's arrival counters are cleared by every
+ * rlt_cross_attention call).  Host-side setting, not thread-safe with
+ * concurrent calls on the same model.  Errors: RLT_EINVAL (null model,
+ * unknown kernel, budget out of range), RLT_EUNSUPPORTED (RLT_KERNEL_GEMM on
+ * an fp32 model). */
+enum { RLT_KERNEL_XATTN = 1, RLT_KERNEL_GEMM = 2 };
+RLT_API int rlt_debug_withhold_copy(rlt_model* m, int32_t kernel, int64_t budget_cycles);
 
 /* Synchronises the stream, returns the device status recorded in the workspace
  * (RLT_OK, RLT_ETIMEOUT or RLT_EBOUNDS) and clears it. */

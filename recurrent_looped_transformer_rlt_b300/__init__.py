@@ -90,17 +90,18 @@ _cross_attention = _sig("rlt_cross_attention", ctypes.c_int, [_p, _p, _p, _p, _i
                                                               ctypes.c_size_t, _p])
 _cross_attention_noalloc = _sig("rlt_cross_attention_noalloc", ctypes.c_int,
                                 [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p])
+_cross_attention_noalloc_status = _sig("rlt_cross_attention_noalloc_status", ctypes.c_int, [_p])
 _linear = _sig("rlt_linear", ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _i32, _i32, _p, _i32, _p,
                                           ctypes.c_size_t, _p])
 _encode_kv = _sig("rlt_encode_kv", ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _p, _p, ctypes.c_size_t, _p])
 _generate = _sig("rlt_generate", ctypes.c_int,
                  [_p, ctypes.POINTER(rlt_state), _p, _p, _p, _i32, _i32, ctypes.c_uint64, ctypes.c_float, _i32, _p,
                   _p, _p, ctypes.c_size_t, _p])
-_snapshot_size = _sig("rlt_snapshot_size", ctypes.c_int, [_p, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)])
+_snapshot_size = _sig("rlt_snapshot_size", ctypes.c_int, [_p, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)])
 _snapshot_save = _sig("rlt_snapshot_save", ctypes.c_int,
-                      [_p, ctypes.POINTER(rlt_state), _p, _p, _i32, _p, ctypes.c_size_t, _p])
+                      [_p, ctypes.POINTER(rlt_state), _p, _p, _p, _i32, _p, ctypes.c_size_t, _p])
 _snapshot_restore = _sig("rlt_snapshot_restore", ctypes.c_int,
-                         [_p, _p, ctypes.c_size_t, ctypes.POINTER(rlt_state), _p, _p, _i32, _p])
+                         [_p, _p, ctypes.c_size_t, ctypes.POINTER(rlt_state), _p, _p, _p, _i32, _p])
 _bptt_workspace_size = _sig("rlt_bptt_workspace_size", ctypes.c_int,
                             [_p, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)])
 _bptt = _sig("rlt_bptt", ctypes.c_int,
@@ -114,16 +115,19 @@ _timer_read = _sig("rlt_timer_read", ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_
 _strerror = _sig("rlt_strerror", ctypes.c_char_p, [ctypes.c_int])
 _launch_count = _sig("rlt_launch_count", ctypes.c_uint64, [])
 _abi_version = _sig("rlt_abi_version", ctypes.c_int, [])
+_debug_withhold_copy = _sig("rlt_debug_withhold_copy", ctypes.c_int, [_p, _i32, ctypes.c_int64])
 
 EXPORTED = ["rlt_model_create", "rlt_model_set_version", "rlt_model_destroy", "rlt_workspace_size",
             "rlt_workspace_init", "rlt_state_sizes", "rlt_state_init", "rlt_encode", "rlt_decode_steps",
             "rlt_status", "rlt_strerror", "rlt_launch_count", "rlt_abi_version", "rlt_timer_arm",
             "rlt_timer_read", "rlt_cross_attention", "rlt_cross_attention_noalloc", "rlt_linear",
             "rlt_snapshot_size", "rlt_snapshot_save", "rlt_snapshot_restore", "rlt_encode_kv", "rlt_generate",
-            "rlt_bptt_workspace_size", "rlt_bptt", "rlt_set_decode_path", "rlt_fused_plan"]
+            "rlt_bptt_workspace_size", "rlt_bptt", "rlt_set_decode_path", "rlt_fused_plan",
+            "rlt_debug_withhold_copy", "rlt_cross_attention_noalloc_status"]
 RLT_DECODE_AUTO, RLT_DECODE_GRAPH, RLT_DECODE_FUSED = 0, 1, 2
 DECODE_PATHS = {"auto": RLT_DECODE_AUTO, "graph": RLT_DECODE_GRAPH, "fused": RLT_DECODE_FUSED}
 RLT_TIMER_CLASSES = {"off": 0, "xattn": 1, "swa": 2, "gemm": 3, "head": 4, "step": 5}
+RLT_KERNEL_XATTN, RLT_KERNEL_GEMM = 1, 2
 
 
 class RLTError(RuntimeError):
@@ -236,15 +240,15 @@ def rlt_generate(model: int, st: rlt_state, e, mem, enc_kv, T_max: int, n: int, 
     return rc
 
 
-def rlt_snapshot_size(model: int, B: int, pos: int) -> int:
+def rlt_snapshot_size(model: int, B: int, pos: int, with_enc_kv: bool = False) -> int:
     n = ctypes.c_size_t()
-    _check(_snapshot_size(model, B, pos, ctypes.byref(n)), "rlt_snapshot_size")
+    _check(_snapshot_size(model, B, pos, int(bool(with_enc_kv)), ctypes.byref(n)), "rlt_snapshot_size")
     return n.value
 
 
 def rlt_snapshot_save(model: int, st: rlt_state, e, mem, T_mem: int, snap, snap_bytes: int, stream=None,
-                      check: bool = True) -> int:
-    rc = _snapshot_save(model, ctypes.byref(st), _ptr(e), _ptr(mem), T_mem, _ptr(snap), snap_bytes,
+                      check: bool = True, enc_kv=None) -> int:
+    rc = _snapshot_save(model, ctypes.byref(st), _ptr(e), _ptr(mem), _ptr(enc_kv), T_mem, _ptr(snap), snap_bytes,
                         _stream_ptr(stream))
     if check:
         _check(rc, "rlt_snapshot_save")
@@ -252,8 +256,8 @@ def rlt_snapshot_save(model: int, st: rlt_state, e, mem, T_mem: int, snap, snap_
 
 
 def rlt_snapshot_restore(model: int, snap, snap_bytes: int, st: rlt_state, e, mem, T_mem: int, stream=None,
-                         check: bool = True) -> int:
-    rc = _snapshot_restore(model, _ptr(snap), snap_bytes, ctypes.byref(st), _ptr(e), _ptr(mem), T_mem,
+                         check: bool = True, enc_kv=None) -> int:
+    rc = _snapshot_restore(model, _ptr(snap), snap_bytes, ctypes.byref(st), _ptr(e), _ptr(mem), _ptr(enc_kv), T_mem,
                            _stream_ptr(stream))
     if check:
         _check(rc, "rlt_snapshot_restore")
@@ -278,6 +282,12 @@ def rlt_cross_attention_noalloc(q, mem_k, mem_v, B: int, n_heads: int, head_dim:
     if check:
         _check(rc, "rlt_cross_attention_noalloc")
     return rc
+
+
+def rlt_cross_attention_noalloc_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status of
+    the allocation-free entry point's built-in array."""
+    return int(_cross_attention_noalloc_status(_stream_ptr(stream)))
 
 
 def rlt_linear(model: int, A, lda: int, M: int, K: int, W, W3, ldw: int, N: int, C, ldc: int, ws, ws_bytes: int,
@@ -319,6 +329,15 @@ def rlt_fused_plan(model: int, B: int):
         return None
     _check(rc, "rlt_fused_plan")
     return tuple(x.value for x in out)
+
+
+def rlt_debug_withhold_copy(model: int, kernel: int, budget_cycles: int, check: bool = True) -> int:
+    """Arms the bounded-wait give-up path for the next standalone launch of
+    `kernel` (RLT_KERNEL_XATTN or RLT_KERNEL_GEMM) on this model."""
+    rc = _debug_withhold_copy(model, kernel, budget_cycles)
+    if check:
+        _check(rc, "rlt_debug_withhold_copy")
+    return rc
 
 
 def rlt_timer_arm(model: int, kernel_class: int, max_launches: int):

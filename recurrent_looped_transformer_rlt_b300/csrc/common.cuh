@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace rlt {
 
 using bf16 = __nv_bfloat16;
@@ -50,6 +52,25 @@ __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + __ex
 struct StepCtx {
   int pos;
   int step;
+};
+
+// Host-side set-up that CUDA keeps per device (a kernel's dynamic shared
+// memory limit, occupancy): computed once for each device the process uses,
+// under a lock, on the calling thread's current device.  get() returns the
+// stored value (compute() must return non-zero), or -1 for a device index
+// outside the table.
+struct PerDevice {
+  static constexpr int kMaxDevices = 128;
+  std::mutex mu;
+  int val[kMaxDevices] = {};
+  template <class F>
+  int get(F&& compute) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    std::lock_guard<std::mutex> lk(mu);
+    if (val[dev] == 0) val[dev] = compute();
+    return val[dev];
+  }
 };
 
 }  // namespace rlt

@@ -173,6 +173,9 @@ struct AOperand {
 struct SplitK {
   int splits;        // CTAs along K (= cluster size along z when > 1)
   int kb_per_split;  // k-blocks per CTA
+  long long budget;  // clock cycles a wait may take before it gives up (0: kWaitBudget)
+  int withhold;      // failure injection: CTA (0, 0, 0) never requests its first A tile, so the
+                     // MMA's wait on that stage runs out (tests of the timeout path)
 };
 
 __device__ __forceinline__ void cluster_arrive() {
@@ -361,6 +364,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int kb0 = z * sk.kb_per_split;
   const int nkb = max(0, min(kb_total, kb0 + sk.kb_per_split) - kb0);
   int issued = 0;  // k-blocks whose copies were requested (weights of the first `pre` requested earlier)
+  const long long budget = sk.budget > 0 ? sk.budget : kWaitBudget;
+  const bool withhold = sk.withhold && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -407,14 +412,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int pos = ao.pos3d ? ao.ctx->pos : 0;
       for (int i = 0; i < nkb; ++i) {
         const int s = i % STAGES;
-        if (i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, kWaitBudget)) {
+        if (i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, budget)) {
           atomicExch(&s_fail, 1);
           break;
         }
         unsigned char* sa = smem + s * C::STAGE_BYTES;
         const int kx = (kb0 + i) * BK;
         if (i >= pre) mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-        if (kb0 + i < ao.split_kb) {
+        if (withhold && i == 0) {
+          // (injection: the stage's A bytes are expected, never requested)
+        } else if (kb0 + i < ao.split_kb) {
           if (ao.pos3d)
             tma_load_3d(sa, &tmA, kx, pos, m0, &full[s]);
           else
@@ -439,7 +446,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
       for (int i = 0; i < nkb; ++i) {
         const int s = i % STAGES;
-        if (!mbar_wait(&full[s], (i / STAGES) & 1, kWaitBudget)) {
+        if (!mbar_wait(&full[s], (i / STAGES) & 1, budget)) {
           atomicExch(&s_fail, 1);
           break;
         }
@@ -460,7 +467,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     //    i.e. TMEM lane); the stage ring is free once every MMA has completed.
     const int q = warp & 3;
     const int rl = q * 32 + lane;
-    const bool ok = mbar_wait(accum, 0, kWaitBudget) && (nkb > 0);
+    const bool ok = mbar_wait(accum, 0, budget) && (nkb > 0);
     if (!ok) atomicExch(&s_fail, 1);
     tc_fence_after();
     float* stile = reinterpret_cast<float*>(smem);
@@ -548,7 +555,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (s_fail && threadIdx.x == 0) {
     set_error(status, kErrTimeout);
     // give the copies still in flight a bounded time to land before leaving
-    for (int i = max(0, issued - STAGES); i < issued; ++i) mbar_wait(&full[i % STAGES], (i / STAGES) & 1, kWaitBudget);
+    for (int i = max(0, issued - STAGES); i < issued; ++i) mbar_wait(&full[i % STAGES], (i / STAGES) & 1, budget);
   }
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }

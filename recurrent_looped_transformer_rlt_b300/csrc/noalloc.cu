@@ -13,10 +13,16 @@
 // code the array's name only stands for the symbol; its device address is
 // obtained once per device with cudaGetSymbolAddress (with that device
 // current) on the first call made on that device, which is why that first call
-// should come before any stream capture.  All calls share the array; each call
-// clears the arrival counters it uses (the partials need no clearing: every
-// partial that is read was written by the same call); calls that overlap on the
-// GPU race on it.
+// should come before any stream capture.  The address is kept for the life of
+// the process, so the entry point must not be used on a device after a
+// cudaDeviceReset (or other teardown of the device's primary context) in the
+// same process.  All calls share the array; each call clears the arrival
+// counters it uses (the partials need no clearing: every partial that is read
+// was written by the same call); calls that overlap on the GPU race on it.
+// A bounded wait that gives up inside the kernel records RLT_ETIMEOUT in a
+// status word of the array (the first condition wins); the call itself
+// returns before the kernel runs, so the word is read (and cleared) with
+// rlt_cross_attention_noalloc_status.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -43,6 +49,7 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
 constexpr size_t kCtxBytes = 256;                    // step context + status word at the start of the array
+constexpr size_t kStatusOffset = 128;                // the status word (zero in a freshly loaded module)
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 128;
@@ -76,6 +83,23 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 extern "C" {
 
+int rlt_cross_attention_noalloc_status(rlt_stream_t stream) {
+  void* base = nullptr;
+  int n_sm = 0;
+  int rc = scratch_on_current_device(&base, &n_sm);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RLT_ECUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_noalloc_scratch, sizeof(int), kStatusOffset, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return RLT_ECUDA;
+  if (v != 0) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_noalloc_scratch, &z, sizeof(int), kStatusOffset, cudaMemcpyHostToDevice) != cudaSuccess)
+      return RLT_ECUDA;
+  }
+  return v;
+}
+
 int rlt_cross_attention_noalloc(const float* q, const void* mem_k, const void* mem_v, int32_t B, int32_t n_heads,
                                 int32_t head_dim, int32_t dtype, int32_t T_mem, int32_t t, void* out,
                                 rlt_stream_t stream) {
@@ -94,7 +118,7 @@ int rlt_cross_attention_noalloc(const float* q, const void* mem_k, const void* m
   if (rc) return rc;
   unsigned char* sb = static_cast<unsigned char*>(base);
   StepCtx* ctx = reinterpret_cast<StepCtx*>(sb);
-  int* status = reinterpret_cast<int*>(sb + 128);
+  int* status = reinterpret_cast<int*>(sb + kStatusOffset);
   int* cnt = reinterpret_cast<int*>(sb + kCtxBytes);
   float* part = reinterpret_cast<float*>(sb + kCtxBytes + cnt_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

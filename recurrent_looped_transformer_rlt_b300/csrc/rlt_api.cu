@@ -86,6 +86,11 @@ struct rlt_model {
   // the persistent path (0: chosen per call)
   int decode_path;
   int fused_cs;
+  // one-shot failure injection of rlt_debug_withhold_copy: the kernel class
+  // (RLT_KERNEL_*, 0 none) whose next standalone launch withholds a copy,
+  // and the wait budget of that launch in clock cycles
+  mutable int inject_kernel;
+  mutable long long inject_budget;
 };
 
 // ---------------------------------------------------------------------------
@@ -224,6 +229,8 @@ struct TcScratch {
   int n_sm;
   int* status;
   const int (*maxc)[9];  // rlt_model::gemm_maxc
+  long long budget = 0;  // wait budget of the launch (0: the kernels' default)
+  int withhold = 0;      // failure injection (rlt_debug_withhold_copy)
 };
 
 // The A operand of a projection: A [M][lda] for k < split (all of K when
@@ -243,13 +250,14 @@ template <int BN, int STAGES, bool GLU, class Epi, int BMA = tc::BM>
 int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, const bf16* B3, int ldb, int N,
                    Epi epi, const TcScratch& sc, int split_req = 0) {
   using C = tc::Cfg<BN, STAGES, BMA>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
-      return RLT_ECUDA;
-    attr = true;
-  }
+  static PerDevice attr;  // the shared-memory attribute is per device
+  if (attr.get([] {
+        return cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) == cudaSuccess
+                   ? 1
+                   : -1;
+      }) != 1)
+    return RLT_ECUDA;
   if (M > BMA && BMA != tc::BM) return RLT_EINVAL;
   const int nout = GLU ? BN / 2 : BN;
   const int tiles_n = (N + nout - 1) / nout, tiles_m = (M + tc::BM - 1) / tc::BM;
@@ -285,7 +293,7 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   if ((rc = tmap_bf16(&tb, B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
   if ((rc = tmap_bf16(&tb3, GLU ? B3 : B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
   tc::AOperand ao{a.A2 ? a.split / tc::BK : kb, a.T3 > 0 ? 1 : 0, a.ctx};
-  tc::SplitK sk{splits, kbps};
+  tc::SplitK sk{splits, kbps, sc.budget, sc.withhold};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_m, splits);
   cfg.blockDim = dim3(tc::THREADS);
@@ -468,20 +476,18 @@ const T_* wl(const void* base, int l, size_t per_layer) {
   return static_cast<const T_*>(base) + (size_t)l * per_layer;
 }
 
-bool g_attr_done = false;
-std::mutex g_attr_mu;
-
 template <typename T_>
 void set_attrs() {
   cudaFuncSetAttribute(enc_attn_simt_kernel<T_>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
   cudaFuncSetAttribute(head_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }
-void ensure_attrs() {
-  std::lock_guard<std::mutex> lk(g_attr_mu);
-  if (g_attr_done) return;
-  set_attrs<float>();
-  set_attrs<bf16>();
-  g_attr_done = true;
+void ensure_attrs() {  // once per device: function attributes are per device
+  static PerDevice done;
+  done.get([] {
+    set_attrs<float>();
+    set_attrs<bf16>();
+    return 1;
+  });
 }
 
 // ---------------------------------------------------------------------------
@@ -514,13 +520,14 @@ int norm_rows(cudaStream_t st, const float* h, const float* ss, const float* g, 
 // cores (head_dim 16..128), the CUDA-core kernel below that.
 template <int HD>
 int enc_flash_launch(cudaStream_t st, const bf16* q, const bf16* k, const bf16* v, bf16* o, int B, int T, int H) {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(fa::enc_flash_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)fa::smem_bytes<HD>()) != cudaSuccess)
-      return RLT_ECUDA;
-    attr = true;
-  }
+  static PerDevice attr;  // the shared-memory attribute is per device
+  if (attr.get([] {
+        return cudaFuncSetAttribute(fa::enc_flash_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)fa::smem_bytes<HD>()) == cudaSuccess
+                   ? 1
+                   : -1;
+      }) != 1)
+    return RLT_ECUDA;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   fa::enc_flash_kernel<HD><<<dim3(cdiv(T, fa::BQ), H, B), fa::THREADS, fa::smem_bytes<HD>(), st>>>(q, k, v, o, T, H,
                                                                                                    scale_log2);
@@ -1584,7 +1591,7 @@ int validate_cfg(const rlt_config* c) {
 
 extern "C" {
 
-int rlt_abi_version(void) { return 103; }
+int rlt_abi_version(void) { return 200; }
 
 uint64_t rlt_launch_count(void) { return g_launches.load(); }
 
@@ -1648,23 +1655,26 @@ int rlt_model_create(const rlt_config* cfg, const rlt_weights* w, uint64_t versi
 
 namespace {
 
-// Header at the start of a snapshot (64 bytes), then s, ring K, ring V, e and
-// M, each section starting on a 256-byte boundary.
+// Header at the start of a snapshot (64 bytes), then s, ring K, ring V, e, M
+// and (optional) the encoder's key/value cache, each section starting on a
+// 256-byte boundary.
 struct SnapHeader {
   uint32_t magic, abi;
   uint64_t version;
   int32_t B, pos, d, L, H, hd, W, G, dtype, mem_source;
-  int32_t pad[2];
+  int32_t enc_kv;  // 1: the encoder cache section is present
+  int32_t pad;
 };
 static_assert(sizeof(SnapHeader) == 64, "snapshot header");
 constexpr uint32_t kSnapMagic = 0x534c5452u;  // "RTLS"
 
 struct SnapLayout {
-  size_t s, rk, rv, e, mem, total;
+  size_t s, rk, rv, e, mem, kv, total;
   size_t s_bytes, ring_bytes, e_row, mem_row;  // e_row: pos * d elements, mem_row: pos * hd (bytes)
   size_t mem_rows;                              // G * 2 * B * H
+  size_t kv_rows;                               // L * 2 * B * H (rows of mem_row bytes), 0 without the section
 };
-SnapLayout snap_layout(const rlt_model* m, int B, int pos) {
+SnapLayout snap_layout(const rlt_model* m, int B, int pos, bool with_kv) {
   const rlt_config& c = m->cfg;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   SnapLayout L{};
@@ -1684,6 +1694,9 @@ SnapLayout snap_layout(const rlt_model* m, int B, int pos) {
   off += up(L.e_row * B);
   L.mem = off;
   off += up(L.mem_row * L.mem_rows);
+  L.kv = off;
+  L.kv_rows = with_kv ? (size_t)c.n_layers * 2 * B * c.n_heads : 0;
+  off += up(L.mem_row * L.kv_rows);
   L.total = off;
   return L;
 }
@@ -1692,20 +1705,21 @@ __global__ void snap_header_kernel(SnapHeader* dst, SnapHeader h) { *dst = h; }
 
 }  // namespace
 
-int rlt_snapshot_size(const rlt_model* m, int32_t B, int32_t pos, size_t* bytes) {
-  if (!m || !bytes || B <= 0 || pos < 0) return RLT_EINVAL;
-  *bytes = snap_layout(m, B, pos).total;
+int rlt_snapshot_size(const rlt_model* m, int32_t B, int32_t pos, int32_t with_enc_kv, size_t* bytes) {
+  if (!m || !bytes || B <= 0 || pos < 0 || (with_enc_kv != 0 && with_enc_kv != 1)) return RLT_EINVAL;
+  *bytes = snap_layout(m, B, pos, with_enc_kv != 0).total;
   return RLT_OK;
 }
 
-int rlt_snapshot_save(const rlt_model* m, const rlt_state* st, const void* e, const void* mem, int32_t T_mem,
-                      void* snap, size_t snap_bytes, rlt_stream_t stream) {
+int rlt_snapshot_save(const rlt_model* m, const rlt_state* st, const void* e, const void* mem, const void* enc_kv,
+                      int32_t T_mem, void* snap, size_t snap_bytes, rlt_stream_t stream) {
   if (!m || !st || !snap || !aligned16(snap) || st->batch <= 0 || !st->s || !st->ring_k || !st->ring_v)
     return RLT_EINVAL;
   if (st->version != m->version) return RLT_ESTALE;
   const int B = st->batch, pos = st->pos;
   if (pos < 0 || (pos > 0 && (!e || !mem || T_mem < pos))) return RLT_EINVAL;
-  const SnapLayout L = snap_layout(m, B, pos);
+  const bool with_kv = enc_kv != nullptr;
+  const SnapLayout L = snap_layout(m, B, pos, with_kv);
   if (snap_bytes < L.total) return RLT_EINVAL;
   const rlt_config& c = m->cfg;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1724,6 +1738,7 @@ int rlt_snapshot_save(const rlt_model* m, const rlt_state* st, const void* e, co
   h.G = c.mem_groups;
   h.dtype = c.dtype;
   h.mem_source = c.mem_source;
+  h.enc_kv = with_kv ? 1 : 0;
   snap_header_kernel<<<1, 1, 0, s>>>(reinterpret_cast<SnapHeader*>(base), h);
   g_launches++;
   RLT_CUDA_TRY(cudaGetLastError());
@@ -1736,12 +1751,15 @@ int rlt_snapshot_save(const rlt_model* m, const rlt_state* st, const void* e, co
                                    cudaMemcpyDeviceToDevice, s));
     RLT_CUDA_TRY(cudaMemcpy2DAsync(base + L.mem, L.mem_row, mem, (size_t)T_mem * c.head_dim * m->esz, L.mem_row,
                                    L.mem_rows, cudaMemcpyDeviceToDevice, s));
+    if (with_kv)  // rows 0..pos-1 of every (layer, K/V, sequence, head) plane of the encoder cache
+      RLT_CUDA_TRY(cudaMemcpy2DAsync(base + L.kv, L.mem_row, enc_kv, (size_t)T_mem * c.head_dim * m->esz, L.mem_row,
+                                     L.kv_rows, cudaMemcpyDeviceToDevice, s));
   }
   return RLT_OK;
 }
 
 int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t snap_bytes, rlt_state* st, void* e, void* mem,
-                         int32_t T_mem, rlt_stream_t stream) {
+                         void* enc_kv, int32_t T_mem, rlt_stream_t stream) {
   if (!m || !st || !snap || !aligned16(snap) || st->batch <= 0 || !st->s || !st->ring_k || !st->ring_v ||
       snap_bytes < sizeof(SnapHeader))
     return RLT_EINVAL;
@@ -1754,10 +1772,14 @@ int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t snap_bytes
   if (h.d != c.d_model || h.L != c.n_layers || h.H != c.n_heads || h.hd != c.head_dim || h.W != c.window ||
       h.G != c.mem_groups || h.dtype != c.dtype || h.mem_source != c.mem_source || h.B != st->batch)
     return RLT_EINVAL;
+  if (h.enc_kv != 0 && h.enc_kv != 1) return RLT_EINVAL;
+  // the cache section is restored exactly when the caller asks for it, and
+  // can only be asked for when the snapshot holds it
+  if ((enc_kv != nullptr) != (h.enc_kv == 1)) return RLT_EINVAL;
   if (h.version != m->version) return RLT_ESTALE;
   const int B = h.B, pos = h.pos;
   if (pos < 0 || (pos > 0 && (!e || !mem || T_mem < pos))) return RLT_EINVAL;
-  const SnapLayout L = snap_layout(m, B, pos);
+  const SnapLayout L = snap_layout(m, B, pos, h.enc_kv == 1);
   if (snap_bytes < L.total) return RLT_EINVAL;
   const char* base = static_cast<const char*>(snap);
   RLT_CUDA_TRY(cudaMemcpyAsync(st->s, base + L.s, L.s_bytes, cudaMemcpyDeviceToDevice, s));
@@ -1768,6 +1790,9 @@ int rlt_snapshot_restore(const rlt_model* m, const void* snap, size_t snap_bytes
                                    cudaMemcpyDeviceToDevice, s));
     RLT_CUDA_TRY(cudaMemcpy2DAsync(mem, (size_t)T_mem * c.head_dim * m->esz, base + L.mem, L.mem_row, L.mem_row,
                                    L.mem_rows, cudaMemcpyDeviceToDevice, s));
+    if (enc_kv)
+      RLT_CUDA_TRY(cudaMemcpy2DAsync(enc_kv, (size_t)T_mem * c.head_dim * m->esz, base + L.kv, L.mem_row, L.mem_row,
+                                     L.kv_rows, cudaMemcpyDeviceToDevice, s));
   }
   st->pos = pos;
   st->version = h.version;
@@ -2007,6 +2032,11 @@ int rlt_cross_attention(const rlt_model* m, const float* q, const void* mem_k, c
   xa.scale = 1.0f / sqrtf((float)hd);
   xa.ctx = ctx;
   xa.status = at<int>(ws, Lw.status);
+  if (m->inject_kernel == RLT_KERNEL_XATTN) {  // one-shot (rlt_debug_withhold_copy)
+    xa.budget = m->inject_budget;
+    xa.withhold = 1;
+    m->inject_kernel = 0;
+  }
   set_ctx_kernel<<<1, 1, 0, s>>>(ctx, t - 1);
   RLT_CUDA_TRY(cudaMemsetAsync(xa.cnt, 0, sizeof(int) * (size_t)B * H, s));
   cudaError_t ce = (c.dtype == RLT_BF16) ? launch_xattn<bf16>(xa, hd, m->n_sm, s) : launch_xattn<float>(xa, hd, m->n_sm, s);
@@ -2024,7 +2054,12 @@ int rlt_linear(const rlt_model* m, const void* A, int32_t lda, int32_t M, int32_
   WsLayout Lw = layout(m, 1, 1);
   if (ws_bytes < Lw.total) return RLT_EWORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const TcScratch sc = tc_scratch(m, ws, Lw);
+  TcScratch sc = tc_scratch(m, ws, Lw);
+  if (m->inject_kernel == RLT_KERNEL_GEMM) {  // one-shot (rlt_debug_withhold_copy)
+    sc.budget = m->inject_budget;
+    sc.withhold = 1;
+    m->inject_kernel = 0;
+  }
   AArg a;
   a.A = static_cast<const bf16*>(A);
   a.lda = lda;
@@ -2032,6 +2067,16 @@ int rlt_linear(const rlt_model* m, const void* A, int32_t lda, int32_t M, int32_
   if (W3)
     return proj_bf16<true>(s, a, M, K, w, static_cast<const bf16*>(W3), ldw, N, EpiStoreF32{C, ldc}, sc);
   return proj_bf16<false>(s, a, M, K, w, nullptr, ldw, N, EpiStoreF32{C, ldc}, sc);
+}
+
+int rlt_debug_withhold_copy(rlt_model* m, int32_t kernel, int64_t budget_cycles) {
+  if (!m || (kernel != RLT_KERNEL_XATTN && kernel != RLT_KERNEL_GEMM) || budget_cycles < 1000 ||
+      budget_cycles > 4000000000LL)
+    return RLT_EINVAL;
+  if (kernel == RLT_KERNEL_GEMM && m->cfg.dtype != RLT_BF16) return RLT_EUNSUPPORTED;
+  m->inject_budget = budget_cycles;
+  m->inject_kernel = kernel;
+  return RLT_OK;
 }
 
 int rlt_status(void* ws, rlt_stream_t stream) {

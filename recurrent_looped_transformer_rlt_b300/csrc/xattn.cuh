@@ -80,6 +80,9 @@ struct XattnArgs {
   float scale;
   const StepCtx* ctx;
   int* status;
+  long long budget;   // clock cycles a wait may take before it gives up (0: kWaitBudget)
+  int withhold;       // failure injection: global warp 0 never requests its first value chunk,
+                      // so its wait on it runs out (tests of the timeout path)
 };
 
 template <typename T_, int EPL>
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
 #pragma unroll
   for (int lv = 0; lv < LV; ++lv) idx = (idx << 1) | ((lane & (LPR >> (lv + 1))) ? 1 : 0);
   const bool rep0 = (lane & (REP - 1)) == 0;
+  const long long budget = a.budget > 0 ? a.budget : kWaitBudget;
   const int t = min(a.t_cap, a.ctx->pos + 1);
   const int nch = (t + CH - 1) / CH;
   const int pairs = a.B * a.H;
@@ -175,7 +179,8 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
     mbar_arrive_expect_tx(&bar[stage], bytes);
     bulk_g2s(sbuf + (stage * 2) * CHE, mk + off, bytes, &bar[stage]);
     mbar_arrive_expect_tx(&bar[ST + stage], bytes);
-    bulk_g2s(sbuf + (stage * 2 + 1) * CHE, mv + off, bytes, &bar[ST + stage]);
+    if (!(a.withhold && gw == 0 && iu == u_beg))  // (injection: the bytes are expected, never sent)
+      bulk_g2s(sbuf + (stage * 2 + 1) * CHE, mv + off, bytes, &bar[ST + stage]);
     ++iu;
   };
   // copies that may start before the previous kernel has finished: all of the
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
       const int nj = min(CH, t - c0);
       const int st = used % ST;
       const unsigned par = (phase >> st) & 1u;
-      if (!mbar_wait(&bar[st], par, kWaitBudget)) goto fail;
+      if (!mbar_wait(&bar[st], par, budget)) goto fail;
       // ---- scores: pass p covers rows p*RPW + rg; partial dots of the lane's
       //      EPL dimensions, then a transposed reduction over the row group
       //      (LV halving steps leave NV full dots per lane: passes idx*NV + j)
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(kXThreads, xattn_blocks_per_sm(ST)) dec_xattn_
       l = l * corr + (rep0 ? ls : 0.f);  // each row counted by one lane
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] *= corr;
-      if (!mbar_wait(&bar[ST + st], par, kWaitBudget)) goto fail;
+      if (!mbar_wait(&bar[ST + st], par, budget)) goto fail;
       const T_* Vs = sbuf + (st * 2 + 1) * CHE;
 #pragma unroll
       for (int p = 0; p < PASSES; ++p) {
@@ -349,8 +354,8 @@ fail:
     set_error(a.status, kErrTimeout);
     for (int s2 = 0; s2 < ST; ++s2) {
       const unsigned p2 = (phase >> s2) & 1u;
-      mbar_wait(&bar[s2], p2, kWaitBudget);
-      mbar_wait(&bar[ST + s2], p2, kWaitBudget);
+      mbar_wait(&bar[s2], p2, budget);
+      mbar_wait(&bar[ST + s2], p2, budget);
     }
   }
   __syncwarp();
@@ -360,17 +365,19 @@ fail:
 template <typename T_, int HD, int ST>
 inline cudaError_t launch_xattn_st(const XattnArgs& a, int n_sm, cudaStream_t st) {
   using S = XShape<T_, HD, ST>;
-  static int occ = 0;
-  if (occ == 0) {
-    cudaFuncSetAttribute(dec_xattn_kernel<T_, HD, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)S::smem_bytes());
+  static PerDevice occ_of;  // the shared-memory attribute and the occupancy are per device
+  const int occ = occ_of.get([] {
+    if (cudaFuncSetAttribute(dec_xattn_kernel<T_, HD, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)S::smem_bytes()) != cudaSuccess)
+      return -1;
     int o = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, dec_xattn_kernel<T_, HD, ST>, kXThreads, S::smem_bytes()) !=
             cudaSuccess ||
         o < 1)
       o = 1;
-    occ = o;
-  }
+    return o;
+  });
+  if (occ < 1) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_sm * occ);
   cfg.blockDim = dim3(kXThreads);

@@ -27,6 +27,11 @@ struct dim3 {
 typedef struct CUstream_st* cudaStream_t;
 typedef int cudaError_t;
 constexpr int cudaSuccess = 0;
+// host set-up calls of the library's headers: one device, index 0
+inline cudaError_t cudaGetDevice(int* dev) {
+  *dev = 0;
+  return cudaSuccess;
+}
 
 inline thread_local dim3 threadIdx, blockIdx;
 inline dim3 blockDim, gridDim;

@@ -125,3 +125,85 @@ def test_snapshot_rejected_after_weight_update_and_on_mismatch():
     assert rlt.rlt_snapshot_restore(model.handle, snap, n, st2.c, buf.e, buf.mem, 12, check=False) == rlt.RLT_ESTALE
     assert rlt.rlt_snapshot_save(model.handle, st.c, buf.e, buf.mem, 12, snap, n, check=False) == rlt.RLT_ESTALE
     model.close()
+
+
+@pytest.mark.parametrize("p", [0, 9, 23])
+def test_snapshot_continuation_matches_the_oracle(p):
+    """A continuation restored from a snapshot, into fresh buffers, against
+    the oracle's uninterrupted run (fp32 model: absolute 1e-4 on every
+    scored log-probability, the logits of every step and the final state)."""
+    from oracle import rlt_oracle as O
+    rlt, runner, wl, model, tok = _setup("tiny", 3, 30)
+    B, T = 3, 30
+    acts = ri.teacher_actions(tok, 0, T)
+    buf = runner.alloc_buffers(model, B, T)
+    runner.encode(model, torch.from_numpy(tok).cuda(), buf)
+    st = runner.new_state(model, B)
+    if p:
+        _decode(runner, model, st, buf, acts, 0, p)
+    n = rlt.rlt_snapshot_size(model.handle, B, p)
+    snap = torch.empty(n, dtype=torch.uint8, device="cuda")
+    rlt.rlt_snapshot_save(model.handle, st.c, buf.e, buf.mem, T, snap, n)
+    buf2 = runner.alloc_buffers(model, B, T)   # fresh: the prefix comes from the snapshot,
+    runner.encode(model, torch.from_numpy(tok).cuda(), buf2)   # the suffix from this request's encode
+    if p:
+        buf2.e[:, :p] = float("nan")
+        buf2.mem[:, :, :, :, :p] = float("nan")
+    st2 = rlt.State(model, B)
+    rlt.rlt_snapshot_restore(model.handle, snap, n, st2.c, buf2.e, buf2.mem, T)
+    out = runner.decode(model, st2, buf2, T - p, torch.from_numpy(acts[:, p:]).cuda().contiguous(),
+                        emit_steps=list(range(T - p)))
+    _, _, ost, oout = O.run_sequence(O.Cfg.of(wl.cfg), ri.make_weights(wl.cfg, wl.seed, norm_jitter=0.1), tok, acts,
+                                     emit=list(range(T)))
+    assert np.abs(st2.s.cpu().numpy() - ost.s).max() <= 1e-4
+    for i in range(T - p):
+        assert np.abs(out.logits[i].cpu().numpy() - oout.logits[p + i]).max() <= 1e-4
+    lp, olp = out.logp.cpu().numpy(), oout.logp[:, p:]
+    m = ~np.isnan(olp)
+    assert np.array_equal(np.isnan(lp), ~m) and np.abs(lp[m] - olp[m]).max() <= 1e-4
+    model.close()
+
+
+def test_snapshot_with_the_encoder_cache_resumes_generation_bitwise():
+    """A snapshot that carries the encoder's key/value cache: generation
+    restored from it (into buffers whose prefix rows are garbage) draws the
+    same tokens with the same log-probabilities, and leaves the same state,
+    encoder rows, memory rows and cache rows, as generation that never
+    stopped."""
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from tests.test_gpu_generate import Gen
+    g = Gen(B=3, T0=16, T_max=64)
+    st = g.prefill()
+    g.generate(st, 10, 77, 0.9, 7)
+    p = st.c.pos
+    n = rlt.rlt_snapshot_size(g.model.handle, g.B, p, with_enc_kv=True)
+    assert n > rlt.rlt_snapshot_size(g.model.handle, g.B, p)
+    snap = torch.empty(n, dtype=torch.uint8, device="cuda")
+    rlt.rlt_snapshot_save(g.model.handle, st.c, g.e, g.mem, g.T_max, snap, n, enc_kv=g.kv)
+    _, ta, la = g.generate(st, 20, 77, 0.9, 7)
+    ref = dict(s=st.s.clone(), e=g.e.clone(), mem=g.mem.clone(), kv=g.kv.clone())
+    # restore: garbage everywhere the snapshot must bring back, a fresh state
+    g.e.fill_(float("nan"))
+    g.mem.fill_(float("nan"))
+    g.kv.fill_(float("nan"))
+    st2 = rlt.State(g.model, g.B)
+    st2.s.fill_(float("nan"))
+    # the cache section is restored exactly when asked for
+    assert rlt.rlt_snapshot_restore(g.model.handle, snap, n, st2.c, g.e, g.mem, g.T_max, check=False) == rlt.RLT_EINVAL
+    rlt.rlt_snapshot_restore(g.model.handle, snap, n, st2.c, g.e, g.mem, g.T_max, enc_kv=g.kv)
+    assert st2.c.pos == p
+    _, tb, lb = g.generate(st2, 20, 77, 0.9, 7)
+    assert np.array_equal(ta, tb) and np.array_equal(la, lb, equal_nan=True)
+    T = p + 20
+    assert torch.equal(st2.s, ref["s"])
+    assert torch.equal(g.e[:, :T], ref["e"][:, :T]) and torch.equal(g.mem[..., :T, :], ref["mem"][..., :T, :])
+    assert torch.equal(g.kv[..., :T, :], ref["kv"][..., :T, :])
+    # a snapshot without the section cannot restore a cache
+    n0 = rlt.rlt_snapshot_size(g.model.handle, g.B, p)
+    snap0 = torch.empty(n0, dtype=torch.uint8, device="cuda")
+    st3 = g.runner.new_state(g.model, g.B)
+    g.runner.decode(g.model, st3, g.runner.Buffers(g.e, g.mem, g.ws, g.B, g.T_max), p)
+    rlt.rlt_snapshot_save(g.model.handle, st3.c, g.e, g.mem, g.T_max, snap0, n0)
+    assert rlt.rlt_snapshot_restore(g.model.handle, snap0, n0, st2.c, g.e, g.mem, g.T_max, check=False,
+                                    enc_kv=g.kv) == rlt.RLT_EINVAL
+    g.model.close()

@@ -44,7 +44,7 @@ def test_library_is_built_for_sm_103a():
 
 def test_abi_version_and_strerror():
     import recurrent_looped_transformer_rlt_b300 as rlt
-    assert rlt.rlt_abi_version() == 103
+    assert rlt.rlt_abi_version() == 200
     assert rlt.rlt_strerror(rlt.RLT_ESTALE).startswith("state built")
     assert rlt.rlt_strerror(12345) == "unknown error"
 
@@ -107,3 +107,15 @@ def test_decode_path_calls_reject_bad_arguments_without_gpu():
     assert rlt._set_decode_path(fake, rlt.RLT_DECODE_FUSED, 3) == rlt.RLT_EINVAL
     assert rlt._set_decode_path(fake, rlt.RLT_DECODE_FUSED, 32) == rlt.RLT_EINVAL
     assert rlt._fused_plan(fake, 0, *[ctypes.byref(x) for x in out]) == rlt.RLT_EINVAL
+
+
+def test_withhold_copy_rejects_bad_arguments_without_gpu():
+    """rlt_debug_withhold_copy validates before touching the model: a null
+    model, an unknown kernel class, a wait budget outside 1e3 .. 4e9 cycles."""
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    assert rlt.rlt_debug_withhold_copy(None, rlt.RLT_KERNEL_XATTN, 10 ** 6, check=False) == rlt.RLT_EINVAL
+    fake = ctypes.c_void_p(16)
+    assert rlt._debug_withhold_copy(fake, 0, 10 ** 6) == rlt.RLT_EINVAL
+    assert rlt._debug_withhold_copy(fake, 3, 10 ** 6) == rlt.RLT_EINVAL
+    assert rlt._debug_withhold_copy(fake, rlt.RLT_KERNEL_XATTN, 999) == rlt.RLT_EINVAL
+    assert rlt._debug_withhold_copy(fake, rlt.RLT_KERNEL_GEMM, 4 * 10 ** 9 + 1) == rlt.RLT_EINVAL
