@@ -799,34 +799,35 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   for (int k = 0; k < PPS; ++k) PSS += nparts_of(phase_at(a, k, r, wk, scorer));
   const Ph ph_tail = phase_at(a, 1, r, wk, scorer);  // the head (phase 1 of a step when it is the tail)
   const int NQ = a.n * PSS + (tail ? nparts_of(ph_tail) : 0);
-  auto issue_step = [&](int qq, unsigned char* stg) {  // weights of pipeline step qq
-    Ph ph;
-    int pt;
-    if (qq >= a.n * PSS) {
-      ph = ph_tail;
-      pt = qq - a.n * PSS;
-    } else {
-      int j = qq % PSS;
-      for (int k = 0;; ++k) {
-        ph = phase_at(a, k, r, wk, scorer);
-        const int np = nparts_of(ph);
-        if (j < np) break;
-        j -= np;
-      }
-      pt = j;
-    }
+  // Pipeline steps are requested strictly in order (0, 1, 2, ...), so a
+  // cursor over (phase of the step, part of the phase) names the next one:
+  // one phase_at per phase instead of a search from the step's first phase.
+  int ic_q = 0, ic_k = 0, ic_pt = 0;  // next pipeline step; its phase and part
+  Ph ic_ph = phase_at(a, 0, r, wk, scorer);
+  int ic_np = nparts_of(ic_ph);
+  auto issue_next = [&](unsigned char* stg) {  // weights of pipeline step ic_q
+    const bool in_tail = ic_q >= a.n * PSS;
+    const Ph ph = in_tail ? ph_tail : ic_ph;
+    const int pt = in_tail ? ic_q - a.n * PSS : ic_pt;
     const int tpp = tpp_of(ph), t0 = pt * tpp;
     issue(a, ph, r, wk, stg, min(t0, ph.nt), min(ph.nt, t0 + tpp));
+    ++ic_q;
+    if (!in_tail && ++ic_pt == ic_np) {  // the next phase (the next step's first after the last)
+      ic_pt = 0;
+      ic_k = ic_k + 1 == PPS ? 0 : ic_k + 1;
+      ic_ph = phase_at(a, ic_k, r, wk, scorer);
+      ic_np = nparts_of(ic_ph);
+    }
   };
   auto stage_of = [&](int q) { return stage + (size_t)(q & 1) * P.stage_units * kUnitBytes; };
   // step q's weights go to stage q mod 2; they are requested right after
   // step q - 2's projection has read that half (one cp.async group per
   // step), so each copy has most of two steps to land
   int qc = 0;  // the pipeline step being computed
-  issue_step(0, stage_of(0));
+  issue_next(stage_of(0));
   issue_e(0);
   cp_async_commit();
-  if (NQ > 1) issue_step(1, stage_of(1));
+  if (NQ > 1) issue_next(stage_of(1));
   cp_async_commit();
   prefetch_mem(0, a.p0);
 
@@ -856,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
           const int t0 = min(pt * tpp, ph.nt);
           sub.nt = min(ph.nt, t0 + tpp) - t0;
           y = proj(sub, cols, stg, X, ldX, out, part, reduce || np > 1, t0);
-          if (qc + 2 < NQ) issue_step(qc + 2, stg);
+          if (qc + 2 < NQ) issue_next(stg);  // pipeline step qc + 2 (= ic_q)
           if (k == 0 && pt == 0 && i + 1 < a.n) issue_e(i + 1);  // the next step's e, landed long before it is read
           cp_async_commit();
           ++qc;
@@ -1089,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
       const int t0 = min(pt * tpp, ph_tail.nt);
       sub.nt = min(ph_tail.nt, t0 + tpp) - t0;
       proj(sub, cols, stage_of(qc), xb, P.ldx, out, part, true, t0);
-      if (qc + 2 < NQ) issue_step(qc + 2, stage_of(qc));
+      if (qc + 2 < NQ) issue_next(stage_of(qc));  // pipeline step qc + 2 (= ic_q)
       cp_async_commit();
       ++qc;
     }

@@ -116,6 +116,8 @@ def _check_bf16(g, o, emit, top_k=0, acts=None, temperature=1.0):
     Ol = np.concatenate([o["logits"][i] for i in emit])
     ga = np.concatenate([g["argmax"][:, i] for i in emit])
     raw = check_argmax(ga, G, Ol)
+    print(f"bf16 parity over {len(ga)} scored rows: max rel logit err {rel.max():.2e}, raw argmax agreement "
+          f"{raw:.4f} (bar 0.999 on rows whose top-2 gap exceeds twice the error)")
     assert raw >= 0.99, raw
     srel = np.abs(g["s"] - o["s"]).max() / np.abs(o["s"]).max()
     assert srel <= BF16_REL_LOGIT, srel
@@ -187,25 +189,35 @@ def test_small_bf16_full_size_sampled_rows():
 # tolerances; the encoder is checked on a prefix of the sequences (causal, so
 # the prefix depends on its own tokens only).
 
-@pytest.mark.parametrize("name,B,T,t0s,kw", [
-    ("medium", 4, 300, [0, 5, 127, 128, 299], {}),                          # ring of 128 wraps
-    ("rlreplay", 4, 120, [0, 63, 64, 119], dict(temperature=0.7, top_k=50)),  # G = L, tempered top-k
+@pytest.mark.parametrize("name,B,T,t0s,kw,rows", [
+    ("medium", 4, 300, [0, 5, 127, 128, 299], {}, None),                          # ring of 128 wraps
+    ("rlreplay", 4, 120, [0, 63, 64, 119], dict(temperature=0.7, top_k=50), None),  # G = L, tempered top-k
+    # the reference-depth model (48 layers, d = 2048, hd = 128, V = 32000): the
+    # ring of 256 slots fills (t0 = 255), wraps (256) and is four times over (1023)
+    ("refdep", 2, 1025, [0, 255, 256, 1023], {}, None),
+    # the replay shape at its full batch (M = 1024 rows per projection: the
+    # tensor-core-bound plan), the oracle on four sampled sequences
+    ("rlreplay", 1024, 72, [0, 63, 64, 71], dict(temperature=0.7, top_k=50), [0, 341, 682, 1023]),
 ])
-def test_large_configs_transition_parity(name, B, T, t0s, kw):
+def test_large_configs_transition_parity(name, B, T, t0s, kw, rows):
     wl, W, tok, acts = _inputs(name, B=B, T=T, jitter=0.0)
-    rows = list(range(B))
+    rows = list(range(B)) if rows is None else rows
     e, mem, snaps = gpu_transition_snapshots(wl, W, tok, acts, t0s, rows, **kw)
+    tok, acts = tok[rows], acts[rows]
+    agree = []
     for snap in snaps:
         t0 = snap["pos"]
         o = oracle_transition(wl, W, e, mem, snap, acts[:, t0:t0 + 1], **kw)
         rel = rel_logit_err(snap["logits"], o["logits"])
         assert rel.max() <= BF16_REL_LOGIT, (t0, rel.max())
-        check_argmax(snap["argmax"], snap["logits"], o["logits"])
+        agree.append(check_argmax(snap["argmax"], snap["logits"], o["logits"]))
         srel = np.abs(snap["s_next"] - o["s_next"]).max() / np.abs(o["s_next"]).max()
         assert srel <= BF16_REL_LOGIT, (t0, srel)
+        print(f"{name} B={B} t0={t0}: max rel logit err {rel.max():.2e}, |ds|/|s| {srel:.2e}, "
+              f"raw argmax agreement {agree[-1]:.4f} (bar 0.999 on rows whose top-2 gap exceeds twice the error)")
         m = np.isfinite(o["logp"])
         assert np.array_equal(np.isfinite(snap["logp"]), m)
-        lim = 2 * BF16_REL_LOGIT * np.abs(o["logits"]).max() + 1e-3
+        lim = (2 * BF16_REL_LOGIT * np.abs(o["logits"]).max() + 1e-3) / kw.get("temperature", 1.0)
         if m.any():
             assert np.abs(snap["logp"][m] - o["logp"][m]).max() <= lim
         mf = np.isfinite(o["logp_full"])   # the last position has no next token to score
