@@ -655,31 +655,45 @@ def run_profile_case(args):
 
 
 def run_fused_case(args):
-    """One rlt_decode_steps call of the persistent cluster decoder over n =
-    --bptt-steps (default 32) steps from the middle of the workload's
-    sequences (the state is brought to position T/2 - n/2 first and restored
-    before each timed call), timed with CUDA events over --steps calls after
-    --warmup; one JSON line with the call's algorithmic bytes and its
-    fraction of HBM bandwidth.  A short single launch for ncu captures."""
+    """One rlt_decode_steps call over n = --bptt-steps (default 32) steps from
+    the middle of the workload's sequences (the state is brought to position
+    --case-pos, default T/2 - n/2, first and restored before each timed
+    call), timed with CUDA events over --steps calls after --warmup; one JSON
+    line with the call's algorithmic bytes and its fraction of HBM
+    bandwidth.  Case "fused": the persistent cluster decoder (one launch, for
+    ncu captures); case "decode": the path --decode-path names."""
     import torch
     import recurrent_looped_transformer_rlt_b300 as rlt
     from recurrent_looped_transformer_rlt_b300 import runner
     wl = ri.preset(args.workload)
     c, B, T = wl.cfg, wl.B, wl.T
     n = args.bptt_steps or 32
-    p0 = max(0, T // 2 - n // 2)
+    p0 = args.case_pos if args.case_pos >= 0 else max(0, T // 2 - n // 2)
+    if p0 + n > T:
+        raise SystemExit("--case-pos + steps beyond T")
+    path = "fused" if args.profile_case == "fused" else args.decode_path
     W = ri.make_weights(c, wl.seed)
     tok = ri.make_tokens(wl)
     model = rlt.Model(c, W)
-    model.set_decode_path("fused")
-    plan = model.fused_plan(B)
-    if plan is None:
+    del W
+    model.set_decode_path(path)
+    plan = model.fused_plan(B) if path == "fused" else None
+    if path == "fused" and plan is None:
         raise SystemExit(f"the fused decoder does not take the {wl.name} model")
     buf = runner.alloc_buffers(model, B, T)
     runner.encode(model, torch.from_numpy(tok).cuda(), buf)
     acts = torch.from_numpy(ri.teacher_actions(tok, 0, T)).cuda()
     st = runner.new_state(model, B)
-    if p0 > 0:
+    if p0 > 0 and args.case_synthetic_state:
+        # timing only: a seeded random state at position p0 (s ~ N(0, 1),
+        # window entries ~ N(0, 1) in storage precision) instead of p0 decoded
+        # steps; no kernel's work depends on the values
+        g = torch.Generator(device="cuda").manual_seed(p0)
+        st.s.copy_(torch.randn(st.s.shape, device="cuda", generator=g))
+        st.ring_k.copy_(torch.randn(st.ring_k.shape, device="cuda", generator=g).to(st.ring_k.dtype))
+        st.ring_v.copy_(torch.randn(st.ring_v.shape, device="cuda", generator=g).to(st.ring_v.dtype))
+        st.c.pos = p0
+    elif p0 > 0:
         runner.decode(model, st, buf, p0, acts[:, :p0].contiguous())
     saved = (st.s.clone(), st.ring_k.clone(), st.ring_v.clone())
     a_n = acts[:, p0:p0 + n].contiguous()
@@ -706,9 +720,11 @@ def run_fused_case(args):
     bw, _, src = load_peaks()
     t = float(np.mean(ts))
     nbytes = sum(step_bytes(c, B, p + 1) for p in range(p0, p0 + n))
-    print(json.dumps({"case": "fused", "workload": wl.name, "kernel": "dec_fused_kernel", "B": B, "p0": p0,
-                      "steps": n, "plan": {"cluster": plan[0], "seqs_per_cluster": plan[1], "clusters": plan[2],
-                                           "smem_bytes": plan[3]},
+    print(json.dumps({"case": args.profile_case, "workload": wl.name, "decode_path": path,
+                      "kernel": "dec_fused_kernel" if path == "fused" else "decoder step graph", "B": B, "p0": p0,
+                      "steps": n, "plan": (None if plan is None else
+                                           {"cluster": plan[0], "seqs_per_cluster": plan[1], "clusters": plan[2],
+                                            "smem_bytes": plan[3]}),
                       "us_per_call": round(1e6 * t, 2), "us_per_step": round(1e6 * t / n, 2),
                       "bytes_per_call": nbytes, "achieved_gbs": round(nbytes / t / 1e9, 1),
                       "peak_gbs": round(bw / 1e9, 1), "frac": round(nbytes / t / bw, 4), "peak_source": src,
@@ -848,12 +864,17 @@ def main():
     ap.add_argument("--decode-path", default="graph", choices=["graph", "fused"],
                     help="decoder path of rlt_decode_steps: the per-step graph or the persistent cluster kernel")
     ap.add_argument("--profile-case", default="",
-                    choices=["", "xattn", "swa", "proj", "glu", "generate", "bptt", "fused"],
+                    choices=["", "xattn", "swa", "proj", "glu", "generate", "bptt", "fused", "decode"],
                     help="time one kernel of the workload (profiler captures), generation, the decoder's "
                          "backpropagation through time, or one call of the persistent decoder, instead of the "
                          "bench step")
     ap.add_argument("--bptt-steps", type=int, default=0,
-                    help="steps of the bptt case (default: T / 4) and of the fused case (default: 32)")
+                    help="steps of the bptt case (default: T / 4) and of the fused / decode cases (default: 32)")
+    ap.add_argument("--case-pos", type=int, default=-1,
+                    help="first position of the fused / decode cases (default: T/2 - steps/2)")
+    ap.add_argument("--case-synthetic-state", action="store_true",
+                    help="fused / decode cases: start from a seeded random state at --case-pos instead of "
+                         "decoding up to it (timing and profiler captures only)")
     args = ap.parse_args()
     if args.profile_case == "generate":
         run_generate_case(args)
@@ -861,7 +882,7 @@ def main():
     if args.profile_case == "bptt":
         run_bptt_case(args)
         return
-    if args.profile_case == "fused":
+    if args.profile_case in ("fused", "decode"):
         run_fused_case(args)
         return
     if args.profile_case:
