@@ -82,10 +82,16 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, const bf16* __res
 // left per 128-column block (ss[p][r], p < d/128):
 //   x[r] = bf16(h[r] / sqrt(sum_p ss[p][r] / d + eps) * g).
 // Block = one row, d/4 threads (4 columns each).
+// The kernel lets its dependent start before waiting on its own predecessor:
+// what follows a norm (a projection, a row copy) does nothing but request
+// weights before its own wait, which ends only after this kernel - and so the
+// projection before it - has completed.  A projection after a norm thereby
+// streams its first weights while the projection before the norm drains and
+// the norm runs (its CTAs take the SMs the earlier projection frees).
 __global__ void norm_rows_kernel(const float* __restrict__ h, const float* __restrict__ ss, const float* __restrict__ g,
                                  bf16* __restrict__ xo, int rows, int d, float eps) {
-  pdl_wait();
   if (threadIdx.x == 0) pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, c = threadIdx.x * 4;
   if (r >= rows) return;
   float tot = 0.f;

@@ -56,9 +56,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
 // Programmatic dependent launch.  pdl_wait: block until the previous kernel of
 // the stream has completed and its memory is visible (immediately when the
 // kernel was launched without the programmatic attribute); pdl_trigger: allow
-// the next kernel to be scheduled.  Kernels here trigger only after their own
+// the next kernel to be scheduled.  Kernels here trigger after their own
 // wait, so at most one kernel runs ahead: before its wait a kernel may read
 // only data produced two or more kernels earlier (weights, encoder memory).
+// The one exception is the RMSNorm kernel (norm_rows_kernel), which triggers
+// first: every kernel that follows it reads nothing but weights before its
+// wait.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
