@@ -421,8 +421,7 @@ def run_gpu(args, rank, world, local_rank):
 # algorithmic bytes of that launch).  The bench reports traffic per launch as
 # its average algorithmic bytes times this ratio.
 XATTN_TRAFFIC = {
-    "small": (16892672 + 0, 16875520),              # t = 256, ring depth 3
-    "refdep": (1075558656 + 3819776, 1074528256),   # t = 2048, ring depth 2
+    "refdep": (1075496192 + 3594496, 1074528256),   # t = 2048, ring depth 2
 }
 
 
