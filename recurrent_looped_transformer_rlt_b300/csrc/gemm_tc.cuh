@@ -341,8 +341,13 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
 // rows of W_3 in its second half, so that the epilogue sees gate and linear
 // values of one output column in the same thread and writes
 // silu(gate) * linear.
-template <int BN, int STAGES, bool GLU, class Epi, int BMA = BM>
-__global__ void __launch_bounds__(THREADS, 1)
+// MINB: CTAs per SM the instantiation is built for.  With MINB = 2 (a ring of
+// at most ~100 KB) two CTAs share an SM, so one CTA's epilogue overlaps the
+// other's main loop; such instantiations take no K split (their launches
+// must pass splits = 1) and leave the split reduction out, which keeps them
+// within the register budget of two CTAs.
+template <int BN, int STAGES, bool GLU, class Epi, int BMA = BM, int MINB = 1>
+__global__ void __launch_bounds__(THREADS, MINB)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3, int M, int N,
                    int K, AOperand ao, SplitK sk, Epi epi, int* status) {
@@ -494,7 +499,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- all threads: split-K reduction through distributed shared memory
   const int rows = min(BM, M - m0);
   int r0 = 0, r1 = rows;
-  if (sk.splits > 1) {
+  if (MINB == 1 && sk.splits > 1) {
     cluster_sync_all();  // every split's tile is staged
     r0 = (int)(((long long)rows * z) / sk.splits);
     r1 = (int)(((long long)rows * (z + 1)) / sk.splits);
@@ -549,7 +554,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     epi_bar();
     if (!s_fail) epilogue_tile<BN, GLU>(stile, r0, r1, m0, nb0, N, epi, et);
   }
-  if (sk.splits > 1) cluster_wait();  // peers are done reading this CTA's tile before it exits
+  if (MINB == 1 && sk.splits > 1) cluster_wait();  // peers are done reading this CTA's tile before it exits
   tc_fence_before();
   __syncthreads();
   if (s_fail && threadIdx.x == 0) {

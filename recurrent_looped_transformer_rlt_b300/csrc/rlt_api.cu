@@ -21,6 +21,7 @@
 #include "gemm_tc.cuh"
 #include "kernels.cuh"
 #include "attn_enc.cuh"
+#include "attn_enc_tc.cuh"
 #include "xattn.cuh"
 #include "dec_fused.cuh"
 
@@ -224,6 +225,22 @@ int tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t T, u
   return r == CUDA_SUCCESS ? RLT_OK : RLT_ECUDA;
 }
 
+// 3-D map of a bf16 tensor [d2][d1][d0] (d0 contiguous), box = 64 x box1 x 1
+// (128-byte swizzle): a [box1][64] tile of one d2 slice.
+int tmap_bf16_3d_tile(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box1) {
+  auto fn = tmap_encoder();
+  if (!fn) return RLT_ECUDA;
+  if (((uintptr_t)base & 15u) || (d0 * 2) % 16) return RLT_EINVAL;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d1 * d0 * 2};
+  cuuint32_t box[3] = {64, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RLT_OK : RLT_ECUDA;
+}
+
 // Launch context of the tensor-core GEMMs.
 struct TcScratch {
   int n_sm;
@@ -246,13 +263,14 @@ struct AArg {
   const StepCtx* ctx = nullptr;
 };
 
-template <int BN, int STAGES, bool GLU, class Epi, int BMA = tc::BM>
+template <int BN, int STAGES, bool GLU, class Epi, int BMA = tc::BM, int MINB = 1>
 int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, const bf16* B3, int ldb, int N,
                    Epi epi, const TcScratch& sc, int split_req = 0) {
   using C = tc::Cfg<BN, STAGES, BMA>;
+  static_assert(MINB == 1 || MINB * (C::SMEM + 1024) <= 228 * 1024, "CTAs per SM");
   static PerDevice attr;  // the shared-memory attribute is per device
   if (attr.get([] {
-        return cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA>,
+        return cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA, MINB>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) == cudaSuccess
                    ? 1
                    : -1;
@@ -278,6 +296,7 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   else if (tiles < 128)
     splits = 2;
   splits = std::max(1, std::min(splits, kb));
+  if (MINB > 1) splits = 1;  // (instantiations for two CTAs per SM have no split reduction)
   const int kbps = (kb + splits - 1) / splits;
   splits = (kb + kbps - 1) / kbps;
   if (a.A2 && (a.split % tc::BK)) return RLT_EINVAL;
@@ -308,7 +327,7 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   at[1].val.clusterDim.z = splits;
   cfg.attrs = at;
   cfg.numAttrs = splits > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA>, ta, ta2, tb, tb3, M, N, K, ao, sk,
+  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA, MINB>, ta, ta2, tb, tb3, M, N, K, ao, sk,
                          epi, sc.status) != cudaSuccess)
     return RLT_ECUDA;
   g_launches++;
@@ -321,7 +340,7 @@ int gemm_bf16_tc(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, in
                  const TcScratch& sc) {
   if (M <= 0 || N <= 0) return RLT_OK;
   if (M <= tc::BM) return gemm_tc_launch<128, 3, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc);
-  return gemm_tc_launch<256, 4, false>(st, a, M, K, B, nullptr, ldb, N, epi, sc);
+  return gemm_tc_launch<128, 3, false, Epi, tc::BM, 2>(st, a, M, K, B, nullptr, ldb, N, epi, sc);
 }
 template <class Epi>
 int gemm_bf16_tc(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf16* B, int ldb, int N, Epi epi,
@@ -355,17 +374,18 @@ DeepPlan deep_plan(const TcScratch& sc, int M, int N, int K, bool glu) {
   DeepPlan best{base + 1, 1};
   int best_ctas = 0, best_s = 0;
   for (int j = 0; j < 2; ++j) {
+    const int cfg = base + j;
     const int bn = j ? 256 : 128, nout = glu ? bn / 2 : bn;
     const long long tiles = (N + nout - 1) / nout;
     // (256, 128) tiles have no split (their partial tiles are the largest)
-    const int smax = (base + j == 3) ? 1 : std::min(8, kb);
+    const int smax = (cfg == 3) ? 1 : std::min(8, kb);
     for (int s = 1; s <= smax; ++s) {
       const int kbps = (kb + s - 1) / s;
       if ((kb + kbps - 1) / kbps != s) continue;  // every split non-empty
       const long long ctas = tiles * s;
-      if (ctas > (long long)sc.maxc[base + j][s] * s) continue;
+      if (ctas > (long long)sc.maxc[cfg][s] * s) continue;
       if (ctas > best_ctas || (ctas == best_ctas && s < best_s)) {
-        best = {base + j, s};
+        best = {cfg, s};
         best_ctas = (int)ctas;
         best_s = s;
       }
@@ -431,7 +451,7 @@ int proj_bf16(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const
               const TcScratch& sc) {
   if (M <= 0 || N <= 0) return RLT_OK;
   if (M <= tc::BM) return proj_deep<GLU>(st, x, M, K, W, W3, ldw, N, epi, sc);
-  return gemm_tc_launch<256, 4, GLU>(st, x, M, K, W, W3, ldw, N, epi, sc);
+  return gemm_tc_launch<128, 3, GLU, Epi, tc::BM, 2>(st, x, M, K, W, W3, ldw, N, epi, sc);
 }
 
 // out[m][j] = silu(A W_1^T)[m][j] * (A W_3^T)[m][j], j < N (= d_ffn).
@@ -443,7 +463,7 @@ int gemm_bf16_tc_glu(cudaStream_t st, const bf16* A, int lda, int M, int K, cons
   a.A = A;
   a.lda = lda;
   if (M <= tc::BM) return gemm_tc_launch<128, 3, true>(st, a, M, K, W1, W3, ldb, N, epi, sc);
-  return gemm_tc_launch<256, 4, true>(st, a, M, K, W1, W3, ldb, N, epi, sc);
+  return gemm_tc_launch<128, 3, true, Epi, tc::BM, 2>(st, a, M, K, W1, W3, ldb, N, epi, sc);
 }
 
 TcScratch tc_scratch(const rlt_model* m, void* ws, const WsLayout& Lw) {
@@ -534,8 +554,46 @@ int enc_flash_launch(cudaStream_t st, const bf16* q, const bf16* k, const bf16* 
   g_launches++;
   return launch_ok();
 }
+// The tcgen05 encoder attention (attn_enc_tc.cuh): V transposed into vt
+// (B*H*hd*T elements of scratch), then one launch.
+template <int HD>
+int enc_attn_tc_launch(cudaStream_t st, const bf16* q, const bf16* k, const bf16* v, bf16* vt, bf16* o, int B,
+                       int T, int H, int* status) {
+  using Lo = fat::Lay<HD>;
+  static PerDevice attr;  // the shared-memory attribute is per device
+  if (attr.get([] {
+        return cudaFuncSetAttribute(fat::enc_attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)Lo::SMEM) == cudaSuccess
+                   ? 1
+                   : -1;
+      }) != 1)
+    return RLT_ECUDA;
+  const uint64_t BH = (uint64_t)B * H;
+  fat::vt_transpose_kernel<<<dim3(cdiv(T, 32), HD / 32, (unsigned)BH), dim3(32, 8), 0, st>>>(v, vt, T, HD);
+  g_launches++;
+  int rc;
+  if ((rc = launch_ok())) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = tmap_bf16_3d_tile(&tq, q, HD, T, BH, fat::BQ)) || (rc = tmap_bf16_3d_tile(&tk, k, HD, T, BH, fat::BKV)) ||
+      (rc = tmap_bf16_3d_tile(&tv, vt, T, HD, BH, HD)))
+    return rc;
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  fat::enc_attn_tc_kernel<HD><<<dim3(cdiv(T, fat::BQ), H, B), fat::THREADS, Lo::SMEM, st>>>(tq, tk, tv, o, T, H,
+                                                                                             scale_log2, status);
+  g_launches++;
+  return launch_ok();
+}
+
+// Causal self-attention of the bf16 encoder.  Head widths 64 and 128 with T a
+// multiple of 8 (the transposed V's rows must be 16-byte multiples for the
+// tensor maps) run on the tcgen05 kernel, which takes vt (B*H*hd*T elements
+// of scratch); the others on the warp-level MMA kernel.
 int enc_attention_bf16(cudaStream_t st, const bf16* q, const bf16* k, const bf16* v, bf16* o, int B, int T, int H,
-                       int hd) {
+                       int hd, bf16* vt, int* status) {
+  if (vt && T % 8 == 0) {
+    if (hd == 128) return enc_attn_tc_launch<128>(st, q, k, v, vt, o, B, T, H, status);
+    if (hd == 64) return enc_attn_tc_launch<64>(st, q, k, v, vt, o, B, T, H, status);
+  }
   switch (hd) {
     case 16: return enc_flash_launch<16>(st, q, k, v, o, B, T, H);
     case 32: return enc_flash_launch<32>(st, q, k, v, o, B, T, H);
@@ -610,7 +668,9 @@ int encode_bf16(const rlt_model* m, const int32_t* tok, int B, int T, bf16* e, b
       RLT_CUDA_TRY(cudaMemcpy2DAsync(enc_kv + (2 * l + 1) * kvp, (size_t)T_stride * hd * 2, v, row, row,
                                      (size_t)B * H, cudaMemcpyDeviceToDevice, st));
     }
-    if ((rc = enc_attention_bf16(st, q, k, v, o, B, T, H, hd))) return rc;
+    // V transposed into the SwiGLU buffer (free until this layer's W_1/W_3;
+    // it holds R x f >= R x d elements when f >= d)
+    if ((rc = enc_attention_bf16(st, q, k, v, o, B, T, H, hd, f >= d ? xm : nullptr, sc.status))) return rc;
     const bf16* WO = wl<bf16>(w.W_O, l, (size_t)d * d);
     if ((rc = gemm_bf16_tc(st, o, d, R, d, WO, d, d, EpiResidual{HOut{h, d, nullptr, nullptr, ss, R}}, sc))) return rc;
     if ((rc = norm_rows(st, h, ss, w.enc_ffn_norm + (size_t)l * d, x, R, d, c.rms_eps))) return rc;

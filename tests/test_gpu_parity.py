@@ -341,3 +341,32 @@ def test_cross_attention_entry_point(name, B, T_mem, ts):
         else:
             assert np.abs(got - ref).max() <= F32_ABS
     model.close()
+
+
+# ---------------------------------------------------------------------------
+# the encoder's causal attention on the tensor cores (head widths 64 and 128,
+# T a multiple of 8): e and the memory against the oracle's encoder
+
+@pytest.mark.parametrize("name,B,T,over", [
+    ("refdep", 2, 264, dict(n_layers=1, vocab=256)),     # hd 128: three query blocks, the last ragged
+    ("refdep", 1, 128, dict(n_layers=2, vocab=256)),     # hd 128: one block, two layers
+    ("medium", 3, 136, dict(n_layers=2, vocab=512)),     # hd 64, a ragged second block
+    ("medium", 2, 520, dict(n_layers=1, vocab=512)),     # hd 64: five query blocks
+])
+def test_encoder_on_tensor_core_attention_widths(name, B, T, over):
+    import torch
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from recurrent_looped_transformer_rlt_b300 import runner
+    wl, W, tok, _ = _inputs(name, B=B, T=T, **over)
+    model = rlt.Model(wl.cfg, W)
+    buf = runner.alloc_buffers(model, B, T)
+    runner.encode(model, torch.from_numpy(tok).cuda(), buf)
+    torch.cuda.synchronize()
+    assert runner.status(buf) == 0
+    ge, gm = buf.e.float().cpu().numpy(), buf.mem.float().cpu().numpy()
+    oe, om = O.encode(O.Cfg.of(wl.cfg), W, tok)
+    erel = np.abs(ge - oe).max() / np.abs(oe).max()
+    mrel = np.abs(gm - om).max() / np.abs(om).max()
+    print(f"encoder {name} hd={wl.cfg.head_dim} B={B} T={T}: |de|/|e| {erel:.2e}, |dM|/|M| {mrel:.2e}")
+    assert erel <= BF16_REL_LOGIT and mrel <= BF16_REL_LOGIT
+    model.close()
