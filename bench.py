@@ -731,6 +731,50 @@ def run_fused_case(args):
     model.close()
 
 
+def run_encode_case(args):
+    """The token-parallel encoder alone (rlt_encode of B sequences of T
+    positions) on a model of the workload's widths with --case-layers layers
+    (default 1), timed with CUDA events over --steps calls after --warmup;
+    --case-batch overrides B (smaller captures).  One JSON line with the
+    algorithmic flops per layer (projections and causal attention) and the
+    rate."""
+    import torch
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from recurrent_looped_transformer_rlt_b300 import runner
+    L = args.case_layers or 1
+    wl = ri.preset(args.workload, n_layers=L, mem_groups=1, vocab=256)
+    c = wl.cfg
+    B = args.case_batch or wl.B
+    T = wl.T
+    W = ri.make_weights(c, wl.seed)
+    tok = torch.from_numpy(ri.make_tokens(wl, B=B, T=T)).cuda()
+    model = rlt.Model(c, W)
+    buf = runner.alloc_buffers(model, B, T)
+    stream = torch.cuda.current_stream()
+    ts = []
+    for it in range(args.warmup + args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        runner.encode(model, tok, buf)
+        e1.record(stream)
+        e1.synchronize()
+        if it >= args.warmup:
+            ts.append(e0.elapsed_time(e1) / 1e3)
+    if runner.status(buf) != 0:
+        raise RuntimeError("device status flag set")
+    t = float(np.mean(ts))
+    d, f, H, hd = c.d, c.d_ffn, c.n_heads, c.head_dim
+    R = B * T
+    gemm = 2 * R * (6 * d * d + 3 * d * f) * L + 2 * R * 2 * d * d  # layers + the memory projection
+    attn = 4 * B * H * T * T * hd // 2 * L                          # causal: half of Q K^T and P V
+    _, peak, src = load_peaks()
+    print(json.dumps({"case": "encode", "workload": wl.name, "layers": L, "B": B, "T": T, "head_dim": hd,
+                      "ms_per_call": round(1e3 * t, 3), "gemm_flops": gemm, "attn_flops": attn,
+                      "tflops": round((gemm + attn) / t / 1e12, 1), "peak_tflops": round(peak / 1e12, 1),
+                      "peak_source": src, "calls": len(ts)}), flush=True)
+    model.close()
+
+
 def run_bptt_case(args):
     """Backpropagation through time (rlt_bptt) over the first --bptt-steps
     positions of the workload's sequences (encoded on the GPU), full BPTT with
@@ -863,7 +907,7 @@ def main():
     ap.add_argument("--decode-path", default="graph", choices=["graph", "fused"],
                     help="decoder path of rlt_decode_steps: the per-step graph or the persistent cluster kernel")
     ap.add_argument("--profile-case", default="",
-                    choices=["", "xattn", "swa", "proj", "glu", "generate", "bptt", "fused", "decode"],
+                    choices=["", "xattn", "swa", "proj", "glu", "generate", "bptt", "fused", "decode", "encode"],
                     help="time one kernel of the workload (profiler captures), generation, the decoder's "
                          "backpropagation through time, or one call of the persistent decoder, instead of the "
                          "bench step")
@@ -871,6 +915,8 @@ def main():
                     help="steps of the bptt case (default: T / 4) and of the fused / decode cases (default: 32)")
     ap.add_argument("--case-pos", type=int, default=-1,
                     help="first position of the fused / decode cases (default: T/2 - steps/2)")
+    ap.add_argument("--case-layers", type=int, default=0, help="layers of the encode case (default 1)")
+    ap.add_argument("--case-batch", type=int, default=0, help="sequences of the encode case (default: the workload's)")
     ap.add_argument("--case-synthetic-state", action="store_true",
                     help="fused / decode cases: start from a seeded random state at --case-pos instead of "
                          "decoding up to it (timing and profiler captures only)")
@@ -883,6 +929,9 @@ def main():
         return
     if args.profile_case in ("fused", "decode"):
         run_fused_case(args)
+        return
+    if args.profile_case == "encode":
+        run_encode_case(args)
         return
     if args.profile_case:
         run_profile_case(args)
