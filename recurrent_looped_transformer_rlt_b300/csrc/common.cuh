@@ -30,6 +30,17 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+// Sum over each half-warp (lanes 0-15 and 16-31 separately), butterfly
+// order.  Each half-warp synchronises only its own 16 lanes, so a caller may
+// have one half of a warp take a different path than the other (each half
+// must be converged in itself).  1-D blocks: the half is bit 4 of the thread
+// index.
+__device__ __forceinline__ float half_warp_sum(float v) {
+  const unsigned mask = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(mask, v, o);
+  return v;
+}
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -124,6 +124,7 @@ __device__ __forceinline__ Work work_of(const Plan& P, int r, int nbv) {
 
 struct Ph {
   int kind, l, nt, K, U;
+  int lo;  // first tile of the row-split phases (gate, O, Ox, W_1/W_3, W_2)
 };
 struct Tile {
   const bf16* W;
@@ -184,18 +185,18 @@ __device__ __forceinline__ Ph phase_at(const Args& a, int k, int r, const Work& 
   int lo, hi;
   const int th = wk.npairs > 0 ? wk.hpc * (s.hd / 16) : 0;
   switch (ph.kind) {
-    case kGate: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = 2 * s.d; break;
+    case kGate: part_range(s.d / 16, CS, r, &lo, &hi); ph.lo = lo; ph.nt = hi - lo; ph.K = 2 * s.d; break;
     case kQKV:
     case kEQKV: ph.nt = 3 * th; ph.K = s.d; break;
     case kQx: ph.nt = th; ph.K = s.d; break;
     case kMem: ph.nt = 2 * th; ph.K = s.d; break;
     case kO:
     case kOx:
-    case kEO: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = s.d; break;
+    case kEO: part_range(s.d / 16, CS, r, &lo, &hi); ph.lo = lo; ph.nt = hi - lo; ph.K = s.d; break;
     case kW13:
-    case kEW13: part_range(cdivi(s.f, 16), CS, r, &lo, &hi); ph.nt = 2 * (hi - lo); ph.K = s.d; break;
+    case kEW13: part_range(cdivi(s.f, 16), CS, r, &lo, &hi); ph.lo = lo; ph.nt = 2 * (hi - lo); ph.K = s.d; break;
     case kW2:
-    case kEW2: part_range(s.d / 16, CS, r, &lo, &hi); ph.nt = hi - lo; ph.K = s.f; break;
+    case kEW2: part_range(s.d / 16, CS, r, &lo, &hi); ph.lo = lo; ph.nt = hi - lo; ph.K = s.f; break;
     case kTok: ph.nt = scorer ? cdivi(s.V, 16) : 0; ph.K = s.d; break;
     default: ph.nt = cdivi(s.V, 16); ph.K = s.d; break;
   }
@@ -203,16 +204,16 @@ __device__ __forceinline__ Ph phase_at(const Args& a, int k, int r, const Work& 
   return ph;
 }
 
-// Weight rows of tile t of phase ph on CTA r.
-__device__ __forceinline__ Tile tile_at(const Args& a, const Ph& ph, int t, int r, const Work& wk) {
+// Weight rows of tile t of phase ph (ph.lo: the CTA's first tile of the
+// row-split phases).
+__device__ __forceinline__ Tile tile_at(const Args& a, const Ph& ph, int t, int, const Work& wk) {
   const Shape& s = a.sh;
-  const int d = s.d, hd = s.hd, nh = hd / 16, CS = a.P.CS;
+  const int d = s.d, hd = s.hd, nh = hd / 16;
   const size_t dd = (size_t)d * d, fd = (size_t)s.f * d;
+  const int lo = ph.lo;
   Tile T;
-  int lo, hi;
   switch (ph.kind) {
     case kGate:
-      part_range(d / 16, CS, r, &lo, &hi);
       T = Tile{a.W_g, (lo + t) * 16, d};
       break;
     case kQKV:
@@ -234,17 +235,14 @@ __device__ __forceinline__ Tile tile_at(const Args& a, const Ph& ph, int t, int 
     case kO:
     case kOx:
     case kEO:
-      part_range(d / 16, CS, r, &lo, &hi);
       T = Tile{(ph.kind == kOx ? a.W_Ox : a.W_O) + (size_t)ph.l * dd, (lo + t) * 16, d};
       break;
     case kW13:
     case kEW13:
-      part_range(cdivi(s.f, 16), CS, r, &lo, &hi);
       T = Tile{((t & 1) ? a.W_3 : a.W_1) + (size_t)ph.l * fd, (lo + (t >> 1)) * 16, s.f};
       break;
     case kW2:
     case kEW2:
-      part_range(d / 16, CS, r, &lo, &hi);
       T = Tile{a.W_2 + (size_t)ph.l * fd, (lo + t) * 16, d};
       break;
     default:
@@ -604,14 +602,30 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
                   bytes);
     }
   };
-  auto rmsnorm_x = [&](const float* h, const float* g) {  // xb = bf16(RMSNorm(h) g)
+  // xb = bf16(RMSNorm(h) g) (h in shared memory): lane j takes columns
+  // 8j .. 8j + 7 of each 256-column group, 16-byte accesses; the row is read
+  // twice (sum of squares, then the scaled values) so that nothing is held in
+  // registers across the groups
+  auto rmsnorm_x = [&](const float* h, const float* g) {
     for (int b = warp; b < nbv; b += kWarps) {
       const float* hr = h + (size_t)b * d;
       float ss = 0.f;
-      for (int j = lane; j < d; j += 32) ss = fmaf(hr[j], hr[j], ss);
+      for (int c = 8 * lane; c < d; c += 256) {
+        const float4 u0 = *reinterpret_cast<const float4*>(hr + c);
+        const float4 u1 = *reinterpret_cast<const float4*>(hr + c + 4);
+        ss = fmaf(u0.x, u0.x, fmaf(u0.y, u0.y, fmaf(u0.z, u0.z, fmaf(u0.w, u0.w, ss))));
+        ss = fmaf(u1.x, u1.x, fmaf(u1.y, u1.y, fmaf(u1.z, u1.z, fmaf(u1.w, u1.w, ss))));
+      }
       ss = warp_sum(ss);
       const float rv = 1.0f / sqrtf(ss / (float)d + a.eps);
-      for (int j = lane; j < d; j += 32) xb[(size_t)b * P.ldx + j] = __float2bfloat16_rn(hr[j] * rv * g[j]);
+      for (int c = 8 * lane; c < d; c += 256) {
+        const float4 u0 = *reinterpret_cast<const float4*>(hr + c);
+        const float4 u1 = *reinterpret_cast<const float4*>(hr + c + 4);
+        const float4 g0 = ld_nc_f4(g + c), g1 = ld_nc_f4(g + c + 4);
+        const float v8[8] = {u0.x * rv * g0.x, u0.y * rv * g0.y, u0.z * rv * g0.z, u0.w * rv * g0.w,
+                             u1.x * rv * g1.x, u1.y * rv * g1.y, u1.z * rv * g1.z, u1.w * rv * g1.w};
+        *reinterpret_cast<uint4*>(xb + (size_t)b * P.ldx + c) = pack8(v8);
+      }
     }
     __syncthreads();
   };
@@ -701,10 +715,17 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
   // Kb(pi), Vb(pi) ([nk][hd] bf16): each pair's keys split over ns warps,
   // partials combined in split order, the result pushed to ob.  coherent:
   // rows written during this launch, read through L2.
+  // Segments: one per pair when the pairs fill the warps; otherwise the kWarps
+  // warps split the pairs' keys, pair pi owning segments
+  // [ceil(pi kWarps / np), ceil((pi + 1) kWarps / np)) (every warp busy).
   auto pair_attention = [&](auto Kb, auto Vb, int nk, bool coherent) {
-    const int ns = wk.npairs >= kWarps ? 1 : kWarps / max(wk.npairs, 1);
-    for (int w0 = warp; w0 < wk.npairs * ns; w0 += kWarps) {
-      const int pi = w0 / ns, sp = w0 - pi * ns;
+    const int np = wk.npairs;
+    const bool split = np > 0 && np < kWarps;
+    const int nseg = split ? kWarps : np;
+    auto seg_lo = [&](int pi) { return split ? (pi * kWarps + np - 1) / np : pi; };
+    for (int w0 = warp; w0 < nseg; w0 += kWarps) {
+      const int pi = split ? (w0 * np) / kWarps : w0;
+      const int s0 = seg_lo(pi), ns = seg_lo(pi + 1) - s0, sp = w0 - s0;
       const bf16* Kp = Kb(pi) + 8 * cc;
       const bf16* Vp = Vb(pi) + 8 * cc;
       float qv[8];
@@ -727,14 +748,15 @@ __global__ void __launch_bounds__(kThreads, 1) dec_fused_kernel(const __grid_con
     __syncthreads();
     for (int i2 = tid; i2 < wk.npairs * hd8; i2 += kThreads) {
       const int pi = i2 / hd8, c8 = i2 - pi * hd8;
+      const int s0 = seg_lo(pi), s1 = seg_lo(pi + 1);
       float M = -INFINITY;
-      for (int sp = 0; sp < ns; ++sp) {
-        const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
+      for (int sg = s0; sg < s1; ++sg) {
+        const float* xw = xp + (size_t)sg * (hd + 2);
         if (xw[hd + 1] > 0.f) M = fmaxf(M, xw[hd]);
       }
       float num[8] = {}, den = 0.f;
-      for (int sp = 0; sp < ns; ++sp) {
-        const float* xw = xp + (size_t)(pi * ns + sp) * (hd + 2);
+      for (int sg = s0; sg < s1; ++sg) {
+        const float* xw = xp + (size_t)sg * (hd + 2);
         if (xw[hd + 1] > 0.f) {
           const float cf = exp2f(xw[hd] - M);
 #pragma unroll

@@ -30,6 +30,7 @@ namespace fused {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCols = 16;          // sequences per cluster: two 8-column MMA tiles
+constexpr int kMaxD = 1024;           // model width the kernel's row norms keep in registers
 constexpr int kUnitBytes = 1024;      // one staged weight unit: 16 rows x 32 columns, bf16
 constexpr size_t kMaxSmem = 232448;   // dynamic shared memory per CTA (227 KB)
 
@@ -62,10 +63,12 @@ RLT_HD inline int cdivi(int a, int b) { return (a + b - 1) / b; }
 RLT_HD inline int round32(int k) { return (k + 31) / 32 * 32; }
 inline size_t al128(size_t x) { return (x + 127) / 128 * 128; }
 
-// Rows of a d- or f-row projection taken by CTA r: tiles [lo, hi) of nt.
+// Rows of a d- or f-row projection taken by CTA r: tiles [lo, hi) of nt
+// (r <= 16 and nt < 2^26, so 32-bit products; a 64-bit division costs the
+// device ~100 instructions, and the kernel asks for these ranges per tile).
 RLT_HD inline void part_range(int nt, int CS, int r, int* lo, int* hi) {
-  *lo = (int)((long long)r * nt / CS);
-  *hi = (int)((long long)(r + 1) * nt / CS);
+  *lo = r * nt / CS;
+  *hi = (r + 1) * nt / CS;
 }
 inline int part_max(int nt, int CS) { return cdivi(nt, CS); }
 
@@ -73,7 +76,8 @@ inline int part_max(int nt, int CS) { return cdivi(nt, CS); }
 // cluster and Bc sequences per cluster, -1 otherwise.
 inline int make_plan(const Shape& s, int B, int CS, int Bc, Plan* P) {
   if (CS < 1 || CS > 16 || Bc < 1 || Bc > kMaxCols || B < 1) return -1;
-  if (s.d % 32 || s.hd % 16 || s.hd > 128 || s.f % 8 || s.H * s.hd != s.d || s.W < 1 || s.V < 1 || s.L < 1)
+  if (s.d % 32 || s.d > kMaxD || s.hd % 16 || s.hd > 128 || s.f % 8 || s.H * s.hd != s.d || s.W < 1 || s.V < 1 ||
+      s.L < 1)
     return -1;
   if (!(s.hd == 16 || s.hd == 32 || s.hd == 64 || s.hd == 128)) return -1;  // lanes per key row: hd / 8
   if (!(CS % s.H == 0 || s.H % CS == 0)) return -1;

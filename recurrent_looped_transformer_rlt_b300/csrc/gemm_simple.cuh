@@ -150,7 +150,7 @@ struct EpiEncQKVRope {
 // Epilogues that produce the residual stream h (fp32 [M][ldh]) declare kHOut,
 // load(m, n) of what they combine with and combine(aux, acc4, n) -> the new
 // h[m][n..n+3].  The kernel then writes h, optional copies s (fp32) and s16
-// (bf16), and per row and 128-column block the sum of squares ss[n / 128][m]
+// (bf16), and per row and 64-column block the sum of squares ss[n / 64][m]
 // (the next RMSNorm reads these instead of reducing the row again).
 struct HOut {
   float* h;

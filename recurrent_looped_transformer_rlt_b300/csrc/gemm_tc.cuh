@@ -254,7 +254,8 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
     }
   } else if constexpr (IsHOutEpi<Epi>::value) {
     // the residual stream: N a multiple of BN and rows 16-byte aligned
-    // (checked by the host); a warp covers 128 consecutive columns of one row
+    // (checked by the host); a half-warp covers 64 consecutive columns of one
+    // row (the row sums of squares are kept per 64-column group)
     constexpr int V4 = BN / 4;
     const int n = (r1 - r0) * V4;
     const HOut& o = epi.o;
@@ -268,7 +269,7 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * 128;
-        if (i >= n) continue;  // warp-uniform: n is a multiple of 32
+        if (i >= n) continue;  // uniform per half-warp: n is a multiple of 16 (the sums are per half-warp)
         const int r = r0 + i / V4, c = (i % V4) * 4;
         const int m = m0 + r, col = nb0 + c;
         const float4 hv = epi.combine(aux[u], *reinterpret_cast<const float4*>(stile + r * LDT + c), col);
@@ -283,8 +284,8 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
           sp.y = *reinterpret_cast<unsigned*>(&s23);
           *reinterpret_cast<uint2*>(o.s16 + off) = sp;
         }
-        const float q2 = warp_sum(hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w);
-        if ((et & 31) == 0) o.ss[(size_t)(col >> 7) * o.M + m] = q2;
+        const float q2 = half_warp_sum(hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w);
+        if ((et & 15) == 0) o.ss[(size_t)(col >> 6) * o.M + m] = q2;
       }
     }
   } else if constexpr (IsStore4Epi<Epi>::value || IsAdd4Epi<Epi>::value) {

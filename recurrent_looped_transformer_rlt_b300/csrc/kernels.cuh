@@ -79,7 +79,7 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, const bf16* __res
 }
 
 // RMSNorm of bf16 models from the row sums of squares the producing GEMM
-// left per 128-column block (ss[p][r], p < d/128):
+// left per 64-column block (ss[p][r], p < d/64):
 //   x[r] = bf16(h[r] / sqrt(sum_p ss[p][r] / d + eps) * g).
 // Block = one row, d/4 threads (4 columns each).
 // The kernel lets its dependent start before waiting on its own predecessor:
@@ -95,7 +95,7 @@ __global__ void norm_rows_kernel(const float* __restrict__ h, const float* __res
   const int r = blockIdx.x, c = threadIdx.x * 4;
   if (r >= rows) return;
   float tot = 0.f;
-  for (int p = 0; p < d / 128; ++p) tot += ss[(size_t)p * rows + r];
+  for (int p = 0; p < d / 64; ++p) tot += ss[(size_t)p * rows + r];
   const float rs = rsqrtf(tot / (float)d + eps);
   const float4 v = *reinterpret_cast<const float4*>(h + (size_t)r * d + c);
   const float4 gg = *reinterpret_cast<const float4*>(g + c);
@@ -552,19 +552,19 @@ __global__ void __launch_bounds__(1024) head_reduce_kernel(HeadArgs a, const Ste
   }
 }
 
-// Per-row sums of squares of h [rows][d] in 128-column groups, ss[g][r], with
-// the same lane mapping and warp reduction as the residual epilogue of the
-// projections (so that an RMSNorm from them is bitwise the in-step one).
-// One warp per (row, group); blockDim 128.
+// Per-row sums of squares of h [rows][d] in 64-column groups, ss[g][r], with
+// the same lane mapping and half-warp reduction as the residual epilogue of
+// the projections (so that an RMSNorm from them is bitwise the in-step one).
+// One warp per (row, pair of groups); blockDim 128.
 __global__ void row_ss_kernel(const float* __restrict__ h, float* __restrict__ ss, int rows, int d) {
   const int lane = threadIdx.x & 31;
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int groups = d / 128;
-  if (wid >= rows * groups) return;
-  const int r = wid / groups, g = wid - r * groups;
-  const float4 v = *reinterpret_cast<const float4*>(h + (size_t)r * d + g * 128 + lane * 4);
-  const float q2 = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
-  if (lane == 0) ss[(size_t)g * rows + r] = q2;
+  const int pairs = d / 128;
+  if (wid >= rows * pairs) return;  // warp-uniform
+  const int r = wid / pairs, g2 = wid - r * pairs;
+  const float4 v = *reinterpret_cast<const float4*>(h + (size_t)r * d + g2 * 128 + lane * 4);
+  const float q2 = half_warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+  if ((lane & 15) == 0) ss[(size_t)(2 * g2 + (lane >> 4)) * rows + r] = q2;
 }
 
 // e[b][pos][:] = x[b][:] (bf16 rows, pos = ctx->pos), pos < T.

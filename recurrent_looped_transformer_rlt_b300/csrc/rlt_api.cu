@@ -82,7 +82,7 @@ struct rlt_model {
   KernelTimer* timer;
   // co-resident clusters of the deep projection kernels, [config][cluster
   // size] (size 1: CTAs), measured on the device at creation
-  int gemm_maxc[4][9];
+  int gemm_maxc[5][9];
   // decoder path of rlt_decode_steps (RLT_DECODE_*) and the cluster size of
   // the persistent path (0: chosen per call)
   int decode_path;
@@ -137,7 +137,7 @@ WsLayout layout(const rlt_model* m, int B, int T) {
   L.d_o = take(es * (size_t)B * d);
   L.d_part = take(4 * (size_t)B * H * kXMaxSplits * (hd + 2));
   L.d_cnt = take(sizeof(int) * (size_t)B * H);
-  L.d_ss = take(4 * (size_t)B * ((d + 127) / 128));
+  L.d_ss = take(4 * (size_t)B * ((d + 63) / 64));
   L.d_s16 = take(es * (size_t)B * d);
   L.d_tok = take(sizeof(int) * (size_t)B);
   const size_t dec_end = off;
@@ -152,7 +152,7 @@ WsLayout layout(const rlt_model* m, int B, int T) {
   L.e_k = take(es * R * d);
   L.e_v = take(es * R * d);
   L.e_o = take(es * R * d);
-  L.e_ss = take(4 * R * ((d + 127) / 128));
+  L.e_ss = take(4 * R * ((d + 63) / 64));
   const size_t enc_end = off;
   L.total = std::max(dec_end, enc_end);
   return L;
@@ -355,6 +355,7 @@ int gemm_bf16_tc(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf
 // 100-160 KB of weights in flight.  Configurations (BN, rows of A per copy):
 //   0: (128, 64)  8 stages   1: (256, 64)  5 stages
 //   2: (128, 128) 6 stages   3: (256, 128) 4 stages
+//   4: (64, 64)   8 stages (not for RoPE tiles of heads wider than 64)
 template <int BN, int BMA>
 constexpr int deep_stages() {
   return std::min(8, (200 * 1024) / ((BMA + BN) * tc::BK * 2));
@@ -368,14 +369,20 @@ struct DeepPlan {
 // once and share the epilogue; a split's partial sums cost a cluster barrier
 // and a pull through distributed shared memory (~2-3 us, measured), which
 // fewer, longer CTAs lose more than that to streaming and epilogue time.
-DeepPlan deep_plan(const TcScratch& sc, int M, int N, int K, bool glu) {
+// 64-wide tiles are considered only when the wider ones leave more than half
+// of the SMs idle (narrow projections of small models: measured 11 % faster
+// per step at d = 256; at d = 2048, where 128-wide tiles already take 96 or
+// more CTAs, they were 2-3 % slower).
+DeepPlan deep_plan(const TcScratch& sc, int M, int N, int K, bool glu, bool allow64) {
   const int base = (M <= 64) ? 0 : 2;
   const int kb = (K + tc::BK - 1) / tc::BK;
   DeepPlan best{base + 1, 1};
   int best_ctas = 0, best_s = 0;
-  for (int j = 0; j < 2; ++j) {
-    const int cfg = base + j;
-    const int bn = j ? 256 : 128, nout = glu ? bn / 2 : bn;
+  const int order[3] = {0, 1, -1};  // 128 wide, 256 wide, then 64 wide
+  for (const int j : order) {
+    if (j < 0 && !(base == 0 && allow64 && 2 * best_ctas < sc.n_sm)) break;
+    const int cfg = j < 0 ? 4 : base + j;
+    const int bn = j < 0 ? 64 : j ? 256 : 128, nout = glu ? bn / 2 : bn;
     const long long tiles = (N + nout - 1) / nout;
     // (256, 128) tiles have no split (their partial tiles are the largest)
     const int smax = (cfg == 3) ? 1 : std::min(8, kb);
@@ -396,8 +403,12 @@ DeepPlan deep_plan(const TcScratch& sc, int M, int N, int K, bool glu) {
 template <bool GLU, class Epi>
 int proj_deep(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const bf16* W3, int ldw, int N, Epi epi,
               const TcScratch& sc) {
-  const DeepPlan p = deep_plan(sc, M, N, K, GLU);
+  bool allow64 = true;  // RoPE pair tiles start on head boundaries: 64-wide tiles only for heads of <= 64
+  if constexpr (tc::IsPairEpi<Epi>::value) allow64 = epi.hd <= 64;
+  const DeepPlan p = deep_plan(sc, M, N, K, GLU, allow64);
   switch (p.cfg) {
+    case 4:
+      return gemm_tc_launch<64, deep_stages<64, 64>(), GLU, Epi, 64>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
     case 0:
       return gemm_tc_launch<128, deep_stages<128, 64>(), GLU, Epi, 64>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
     case 1:
@@ -442,7 +453,8 @@ int deep_occupancy_all(rlt_model* m) {
   if ((rc = deep_occupancy<128, 64>(m->n_sm, m->gemm_maxc[0]))) return rc;
   if ((rc = deep_occupancy<256, 64>(m->n_sm, m->gemm_maxc[1]))) return rc;
   if ((rc = deep_occupancy<128, 128>(m->n_sm, m->gemm_maxc[2]))) return rc;
-  return deep_occupancy<256, 128>(m->n_sm, m->gemm_maxc[3]);
+  if ((rc = deep_occupancy<256, 128>(m->n_sm, m->gemm_maxc[3]))) return rc;
+  return deep_occupancy<64, 64>(m->n_sm, m->gemm_maxc[4]);
 }
 // Projection of a batch of sequences (decoder step, rlt_linear): the deep
 // weight-streaming kernels up to 128 rows, 4 stages of 256-wide tiles beyond.
@@ -529,7 +541,7 @@ int swiglu_proj(cudaStream_t st, const T_* A, int lda, int M, int K, const T_* W
   }
 }
 
-// x = bf16(RMSNorm(h) * g) for bf16 models, from the producer's per-128-column
+// x = bf16(RMSNorm(h) * g) for bf16 models, from the producer's per-64-column
 // sums of squares.
 int norm_rows(cudaStream_t st, const float* h, const float* ss, const float* g, bf16* x, int rows, int d, float eps) {
   g_launches++;

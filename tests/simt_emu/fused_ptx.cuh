@@ -75,6 +75,11 @@ inline uint4 ld_nc16(const void* p) {
   return v;
 }
 inline uint4 ld_cg16(const void* p) { return ld_nc16(p); }
+inline float4 ld_nc_f4(const float* p) {
+  float4 v;
+  std::memcpy(&v, p, 16);
+  return v;
+}
 inline bf16 ld_cg_bf16(const bf16* p) { return *p; }
 
 }  // namespace fused
