@@ -463,6 +463,12 @@ int proj_bf16(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const
               const TcScratch& sc) {
   if (M <= 0 || N <= 0) return RLT_OK;
   if (M <= tc::BM) return proj_deep<GLU>(st, x, M, K, W, W3, ldw, N, epi, sc);
+  // hundreds of sequences (tensor-core bound): 128 x 128 tiles two per SM, or
+  // 128 x 64 tiles where the wider ones would leave SMs without a tile
+  // (d-wide outputs of d = 1024 at M = 1024: 64 tiles of 128 columns)
+  bool narrow = (long long)((M + tc::BM - 1) / tc::BM) * ((N + (GLU ? 63 : 127)) / (GLU ? 64 : 128)) < sc.n_sm;
+  if constexpr (tc::IsPairEpi<Epi>::value) narrow = narrow && epi.hd <= 64;  // RoPE tiles start on head boundaries
+  if (narrow) return gemm_tc_launch<64, 4, GLU, Epi, tc::BM, 2>(st, x, M, K, W, W3, ldw, N, epi, sc);
   return gemm_tc_launch<128, 3, GLU, Epi, tc::BM, 2>(st, x, M, K, W, W3, ldw, N, epi, sc);
 }
 
