@@ -478,9 +478,19 @@ __global__ void __launch_bounds__(1024) head_reduce_kernel(HeadArgs a, const Ste
       __syncthreads();
       const unsigned pref = s_prefix;
       const unsigned hmask = (pass == 0) ? 0u : (0xffffffffu << (shift + 8));
-      for (int v = tid; v < a.V; v += nthr) {
-        unsigned kk = f2key(sx[v]);
-        if ((kk & hmask) == pref) atomicAdd(&hist[(kk >> shift) & 255u], 1u);
+      // the keys of a row are mostly alike in their high bytes, so the lanes
+      // of a warp that fall into the same bin are counted with one add (the
+      // same-address adds would otherwise serialise); every warp runs the
+      // same number of iterations so that all its lanes take part
+      for (int v0 = 0; v0 < a.V; v0 += nthr) {
+        const int v = v0 + tid;
+        int bin = -1;
+        if (v < a.V) {
+          const unsigned kk = f2key(sx[v]);
+          if ((kk & hmask) == pref) bin = (int)((kk >> shift) & 255u);
+        }
+        const unsigned grp = __match_any_sync(0xffffffffu, bin);
+        if (bin >= 0 && lane == __ffs(grp) - 1) atomicAdd(&hist[bin], (unsigned)__popc(grp));
       }
       __syncthreads();
       if (tid == 0) {

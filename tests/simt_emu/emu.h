@@ -120,6 +120,19 @@ inline int __shfl_sync(unsigned, int v, int src) {
   w.bar->arrive_and_wait();
   return r;
 }
+// lanes of the warp holding the same value (full warps only)
+inline unsigned __match_any_sync(unsigned, int v) {
+  auto& w = (*emu_warps)[emu_warp];
+  w.i[emu_lane] = v;
+  w.bar->arrive_and_wait();
+  unsigned m = 0;
+  for (int l = 0; l < 32; ++l)
+    if (w.i[l] == v) m |= 1u << l;
+  w.bar->arrive_and_wait();
+  return m;
+}
+inline int __ffs(unsigned x) { return x ? __builtin_ctz(x) + 1 : 0; }
+inline int __popc(unsigned x) { return __builtin_popcount(x); }
 inline unsigned atomicAdd(unsigned* p, unsigned v) { return std::atomic_ref<unsigned>(*p).fetch_add(v); }
 inline int atomicCAS(int* p, int cmp, int val) {
   std::atomic_ref<int> a(*p);
