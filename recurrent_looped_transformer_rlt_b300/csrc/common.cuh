@@ -20,6 +20,17 @@ template <> __device__ __forceinline__ float from_f32<float>(float x) { return x
 template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
 // Round an fp32 value through the storage type (identity for fp32).
 template <typename T> __device__ __forceinline__ float round_st(float x) { return to_f32(from_f32<T>(x)); }
+// Four consecutive values rounded to the storage type and written with one
+// store (p aligned to 4 elements: 8 bytes for bf16, 16 for fp32).
+template <typename T> __device__ __forceinline__ void store4_st(T* p, float4 v);
+template <> __device__ __forceinline__ void store4_st<float>(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+template <> __device__ __forceinline__ void store4_st<bf16>(bf16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<unsigned*>(&a);
+  u.y = *reinterpret_cast<unsigned*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
 
 template <typename T> __device__ __forceinline__ T nan_of();
 template <> __device__ __forceinline__ float nan_of<float>() { return __int_as_float(0x7fc00000); }

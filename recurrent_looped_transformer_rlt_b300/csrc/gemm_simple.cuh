@@ -20,11 +20,26 @@ struct EpiStoreF32 {
   int ldc;
   __device__ __forceinline__ void operator()(int m, int n, float v) const { C[(size_t)m * ldc + n] = v; }
 };
+// Epilogues that declare kVec4 also take four consecutive columns n .. n + 3
+// of one row at once (store4; n a multiple of 4, all four inside N), with the
+// same values as four calls of operator().
 template <typename T>
 struct EpiStoreT {  // store rounded to the storage type
+  static constexpr bool kVec4 = true;
   T* C;
   int ldc;
   __device__ __forceinline__ void operator()(int m, int n, float v) const { C[(size_t)m * ldc + n] = from_f32<T>(v); }
+  __device__ __forceinline__ void store4(int m, int n, float4 v) const {
+    T* p = C + (size_t)m * ldc + n;
+    if ((reinterpret_cast<uintptr_t>(p) & (4 * sizeof(T) - 1)) == 0) {
+      store4_st<T>(p, v);
+    } else {
+      p[0] = from_f32<T>(v.x);
+      p[1] = from_f32<T>(v.y);
+      p[2] = from_f32<T>(v.z);
+      p[3] = from_f32<T>(v.w);
+    }
+  }
 };
 struct EpiAddF32 {  // residual stream update h += acc
   static constexpr bool kAdd4 = true;
@@ -36,6 +51,7 @@ struct EpiAddF32 {  // residual stream update h += acc
 // dst[b][h][t][i] (dst already offset to the group and key/value plane).
 template <typename T>
 struct EpiMemScatter {
+  static constexpr bool kVec4 = true;
   T* dst;
   int T_len, H, hd;
   int T_stride = 0;  // positions per (b, h) plane row of dst; 0: T_len
@@ -44,6 +60,19 @@ struct EpiMemScatter {
     int h = n / hd, i = n - h * hd;
     const int ts = T_stride ? T_stride : T_len;
     dst[(((size_t)b * H + h) * ts + t) * hd + i] = from_f32<T>(v);
+  }
+  __device__ __forceinline__ void store4(int m, int n, float4 v) const {
+    if (hd & 3) {  // four columns may cross a head: one at a time
+      (*this)(m, n, v.x);
+      (*this)(m, n + 1, v.y);
+      (*this)(m, n + 2, v.z);
+      (*this)(m, n + 3, v.w);
+      return;
+    }
+    const int b = m / T_len, t = m - b * T_len;
+    const int h = n / hd, i = n - h * hd;
+    const int ts = T_stride ? T_stride : T_len;
+    store4_st<T>(dst + (((size_t)b * H + h) * ts + t) * hd + i, v);
   }
 };
 
@@ -144,6 +173,27 @@ struct EpiEncQKVRope {
     T* dst = (c.which == 0) ? q : k;
     dst[o] = from_f32<T>(x1 * cs.x - x2 * cs.y);
     dst[o + half] = from_f32<T>(x2 * cs.x + x1 * cs.y);
+  }
+  // pairs i .. i + 3 of column n = which*d + head*hd + i (i a multiple of 4,
+  // hd a multiple of 8): the same values as four calls of pair()
+  static constexpr bool kPair4 = true;
+  __device__ __forceinline__ void pair4(int m, int n, float4 x1, float4 x2) const {
+    const int half = hd >> 1;
+    const int which = n / d, r = n - which * d, head = r / hd, i = r - head * hd;
+    const int b = m / T_len, t = m - b * T_len;
+    const size_t o = (((size_t)b * H + head) * T_len + t) * hd + i;
+    if (which == 2) {
+      store4_st<T>(v + o, x1);
+      store4_st<T>(v + o + half, x2);
+      return;
+    }
+    const float4 c01 = *reinterpret_cast<const float4*>(tab + (size_t)t * half + i);  // (cos, sin) of i, i + 1
+    const float4 c23 = *reinterpret_cast<const float4*>(tab + (size_t)t * half + i + 2);
+    T* dst = (which == 0) ? q : k;
+    store4_st<T>(dst + o, make_float4(x1.x * c01.x - x2.x * c01.y, x1.y * c01.z - x2.y * c01.w,
+                                      x1.z * c23.x - x2.z * c23.y, x1.w * c23.z - x2.w * c23.w));
+    store4_st<T>(dst + o + half, make_float4(x2.x * c01.x + x1.x * c01.y, x2.y * c01.z + x1.y * c01.w,
+                                             x2.z * c23.x + x1.z * c23.y, x2.w * c23.z + x1.w * c23.w));
   }
 };
 

@@ -159,6 +159,17 @@ template <class E, class = void>
 struct IsAdd4Epi : std::false_type {};
 template <class E>
 struct IsAdd4Epi<E, std::void_t<decltype(E::kAdd4)>> : std::true_type {};
+// kVec4: store4(m, n, float4) takes columns n .. n + 3; kPair4: pair4(m, n,
+// x1, x2) takes the pairs (n + j, n + j + hd/2), j < 4 (functors in
+// gemm_simple.cuh)
+template <class E, class = void>
+struct IsVec4Epi : std::false_type {};
+template <class E>
+struct IsVec4Epi<E, std::void_t<decltype(E::kVec4)>> : std::true_type {};
+template <class E, class = void>
+struct IsPair4Epi : std::false_type {};
+template <class E>
+struct IsPair4Epi<E, std::void_t<decltype(E::kPair4)>> : std::true_type {};
 
 // Where the A tiles come from.  k-blocks below split_kb are read through tmA
 // (a 2-D map [M][K], or with pos3d a 3-D map [M][T][K] at position
@@ -222,16 +233,55 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
   constexpr int LDT = BN + 4;
   if constexpr (GLU) {
     constexpr int HB = BN / 2;
-    const int n = (r1 - r0) * HB;
+    if constexpr (IsVec4Epi<Epi>::value) {
+      // four consecutive outputs per thread (the values of the scalar path)
+      constexpr int G4 = HB / 4;
+      const int n = (r1 - r0) * G4;
+#pragma unroll 2
+      for (int i = et; i < n; i += 128) {
+        const int r = r0 + i / G4, j = (i % G4) * 4;
+        const float4 g = *reinterpret_cast<const float4*>(stile + r * LDT + j);
+        const float4 u = *reinterpret_cast<const float4*>(stile + r * LDT + j + HB);
+        const float4 o = make_float4(silu_f(g.x) * u.x, silu_f(g.y) * u.y, silu_f(g.z) * u.z, silu_f(g.w) * u.w);
+        if (nb0 + j + 3 < N) {
+          epi.store4(m0 + r, nb0 + j, o);
+        } else {
+          const float ov[4] = {o.x, o.y, o.z, o.w};
+          for (int q = 0; q < 4 && nb0 + j + q < N; ++q) epi(m0 + r, nb0 + j + q, ov[q]);
+        }
+      }
+    } else {
+      const int n = (r1 - r0) * HB;
 #pragma unroll 4
-    for (int i = et; i < n; i += 128) {
-      const int r = r0 + i / HB, j = i % HB;
-      if (nb0 + j < N) epi(m0 + r, nb0 + j, silu_f(stile[r * LDT + j]) * stile[r * LDT + j + HB]);
+      for (int i = et; i < n; i += 128) {
+        const int r = r0 + i / HB, j = i % HB;
+        if (nb0 + j < N) epi(m0 + r, nb0 + j, silu_f(stile[r * LDT + j]) * stile[r * LDT + j + HB]);
+      }
     }
   } else if constexpr (IsPairEpi<Epi>::value) {
     const int half = epi.hd >> 1;
     constexpr int HB = BN / 2;  // pairs per tile row
-    if constexpr (128 % HB == 0) {
+    bool done = false;
+    if constexpr (IsPair4Epi<Epi>::value) {
+      if ((half & 3) == 0) {
+        // four consecutive pairs of one head per thread (tiles start on head
+        // boundaries and N is a multiple of hd: a group inside N is whole)
+        constexpr int G4 = HB / 4;
+        const int n = (r1 - r0) * G4;
+#pragma unroll 2
+        for (int i = et; i < n; i += 128) {
+          const int r = r0 + i / G4, pi = (i % G4) * 4;
+          const int hb = pi / half, ii = pi - hb * half;
+          const int c = hb * 2 * half + ii;
+          if (nb0 + c < N)
+            epi.pair4(m0 + r, nb0 + c, *reinterpret_cast<const float4*>(stile + r * LDT + c),
+                      *reinterpret_cast<const float4*>(stile + r * LDT + c + half));
+        }
+        done = true;
+      }
+    }
+    if (done) {
+    } else if constexpr (128 % HB == 0) {
       // a thread keeps one pair of columns for all its rows: its per-column
       // context (position, rotation) is read once
       const int pi = et % HB, hb = pi / half, ii = pi - hb * half;
@@ -325,6 +375,21 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
       for (int i = et; i < (r1 - r0) * w; i += 128) {
         const int r = r0 + i / w, c = c_beg + i % w;
         epi(m0 + r, nb0 + c, stile[r * LDT + c]);
+      }
+    }
+  } else if constexpr (IsVec4Epi<Epi>::value) {
+    // four consecutive columns per thread; the ragged end of N one at a time
+    constexpr int G4 = BN / 4;
+    const int n = (r1 - r0) * G4;
+#pragma unroll 2
+    for (int i = et; i < n; i += 128) {
+      const int r = r0 + i / G4, c = (i % G4) * 4;
+      const float4 x = *reinterpret_cast<const float4*>(stile + r * LDT + c);
+      if (nb0 + c + 3 < N) {
+        epi.store4(m0 + r, nb0 + c, x);
+      } else {
+        const float xv[4] = {x.x, x.y, x.z, x.w};
+        for (int q = 0; q < 4 && nb0 + c + q < N; ++q) epi(m0 + r, nb0 + c + q, xv[q]);
       }
     }
   } else {
