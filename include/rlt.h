@@ -423,15 +423,21 @@ RLT_API int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t
  *   RLT_KERNEL_GEMM   rlt_linear (bf16 models): the first CTA never requests
  *                     its first A tile (its split-K cluster peers then wait on
  *                     it at the cluster barrier until it gives up and arrives);
+ *   RLT_KERNEL_NORM_PROJ  rlt_decode_steps (bf16 models, batches of up to 128
+ *                     sequences, whose projections build their RMSNorm input
+ *                     in the kernel): in the layer-0 QKV projection the first
+ *                     CTA never requests the fp32 rows of its first k-block,
+ *                     so the group converting them and then the MMA give up;
+ *                     every step of that call repeats it (call with n = 1);
  * and gives every wait of that launch budget_cycles clock cycles (1e3 ..
  * 4e9) instead of the default.  The launch's output is then unspecified and
  * rlt_status() of its workspace returns RLT_ETIMEOUT; later launches are not
  * affected (one-shot; the attention's arrival counters are cleared by every
  * rlt_cross_attention call).  Host-side setting, not thread-safe with
  * concurrent calls on the same model.  Errors: RLT_EINVAL (null model,
- * unknown kernel, budget out of range), RLT_EUNSUPPORTED (RLT_KERNEL_GEMM on
- * an fp32 model). */
-enum { RLT_KERNEL_XATTN = 1, RLT_KERNEL_GEMM = 2 };
+ * unknown kernel, budget out of range), RLT_EUNSUPPORTED (RLT_KERNEL_GEMM or
+ * RLT_KERNEL_NORM_PROJ on an fp32 model). */
+enum { RLT_KERNEL_XATTN = 1, RLT_KERNEL_GEMM = 2, RLT_KERNEL_NORM_PROJ = 3 };
 RLT_API int rlt_debug_withhold_copy(rlt_model* m, int32_t kernel, int64_t budget_cycles);
 
 /* Synchronises the stream, returns the device status recorded in the workspace

@@ -127,7 +127,7 @@ EXPORTED = ["rlt_model_create", "rlt_model_set_version", "rlt_model_destroy", "r
 RLT_DECODE_AUTO, RLT_DECODE_GRAPH, RLT_DECODE_FUSED = 0, 1, 2
 DECODE_PATHS = {"auto": RLT_DECODE_AUTO, "graph": RLT_DECODE_GRAPH, "fused": RLT_DECODE_FUSED}
 RLT_TIMER_CLASSES = {"off": 0, "xattn": 1, "swa": 2, "gemm": 3, "head": 4, "step": 5}
-RLT_KERNEL_XATTN, RLT_KERNEL_GEMM = 1, 2
+RLT_KERNEL_XATTN, RLT_KERNEL_GEMM, RLT_KERNEL_NORM_PROJ = 1, 2, 3
 
 
 class RLTError(RuntimeError):
@@ -332,8 +332,10 @@ def rlt_fused_plan(model: int, B: int):
 
 
 def rlt_debug_withhold_copy(model: int, kernel: int, budget_cycles: int, check: bool = True) -> int:
-    """Arms the bounded-wait give-up path for the next standalone launch of
-    `kernel` (RLT_KERNEL_XATTN or RLT_KERNEL_GEMM) on this model."""
+    """Arms the bounded-wait give-up path for the next launch of `kernel` on
+    this model: RLT_KERNEL_XATTN (rlt_cross_attention), RLT_KERNEL_GEMM
+    (rlt_linear) or RLT_KERNEL_NORM_PROJ (the layer-0 QKV projection of the
+    next rlt_decode_steps call)."""
     rc = _debug_withhold_copy(model, kernel, budget_cycles)
     if check:
         _check(rc, "rlt_debug_withhold_copy")

@@ -63,7 +63,7 @@ struct Lay {
   static constexpr int TMEM_COLS = 512;                   // S0 [0,128), S1 [128,256), O [256, 256 + HD)
 };
 
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+using tc::fence_async_smem;
 
 // q, k: [B*H][T][HD] (maps tm_q, tm_k: dims {HD, T, B*H}, box {64, 128, 1});
 // vt: [B*H][HD][T] (map tm_v: dims {T, HD, B*H}, box {64, HD, 1});

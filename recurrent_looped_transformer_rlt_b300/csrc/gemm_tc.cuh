@@ -41,11 +41,13 @@ constexpr int THREADS = 192;
 // always reads 128 rows; with BMA = 64 rows 64..127 of its A operand fall on
 // the B tile of the same stage, and the accumulator rows they produce are
 // never read.
-template <int BN, int STAGES, int BMA = BM>
+// NORMA: the A area of a stage holds the fp32 rows of the k-block (4 bytes
+// per element), converted in place to the bf16 operand (its first half).
+template <int BN, int STAGES, int BMA = BM, bool NORMA = false>
 struct Cfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN");
   static_assert(BMA == BM || (BMA == 64 && BN >= 64), "A rows 64..127 must stay inside the stage");
-  static constexpr int A_BYTES = BMA * BK * 2;
+  static constexpr int A_BYTES = BMA * BK * (NORMA ? 4 : 2);
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = BN;  // fp32 accumulator: one column per output column
@@ -138,6 +140,11 @@ __device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+// Named barriers of 64 threads (ids 2, 3: the two halves of the epilogue warps).
+__device__ __forceinline__ void half_bar(int id) { asm volatile("bar.sync %0, 64;\n" ::"r"(id) : "memory"); }
+// Makes this thread's shared-memory stores visible to the tensor cores (the
+// asynchronous proxy) once the synchronisation that follows is passed.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 // ---------------------------------------------------------------------------
 
 // Epilogues that consume column pairs (i, i + hd/2) of each head block of hd
@@ -179,6 +186,15 @@ struct AOperand {
   int split_kb;
   int pos3d;
   const StepCtx* ctx;
+  // RMSNorm operand (kernels built with NORMA; tmA then maps the fp32 matrix
+  // h [M][K]): A[m][k] = bf16(h[m][k] rs[m] g[k]), rs[m] = 1 / sqrt(sum_p
+  // ss[p][m] / K + eps), ss[p][m] the sum of squares of h[m] over columns
+  // 64p .. 64p + 63 (row stride ss_ld) left by the kernel that produced h;
+  // K a multiple of 64
+  const float* nss;
+  const float* ng;
+  float neps;
+  int nss_ld;
 };
 
 struct SplitK {
@@ -412,21 +428,33 @@ __device__ __forceinline__ void epilogue_tile(const float* stile, int r0, int r1
 // other's main loop; such instantiations take no K split (their launches
 // must pass splits = 1) and leave the split reduction out, which keeps them
 // within the register budget of two CTAs.
-template <int BN, int STAGES, bool GLU, class Epi, int BMA = BM, int MINB = 1>
+// NORMA: A is the RMSNorm of an fp32 matrix (AOperand): the producer copies
+// each k-block's fp32 rows into the stage's A area (signalled on hfull, a
+// ring ahead like any A tile), the epilogue warps - idle until the
+// accumulator is ready - convert them in place into the bf16 operand with
+// the scaling and rounding of the stand-alone RMSNorm kernel (two groups of
+// 64 threads on alternate k-blocks), and the stage's full barrier then takes
+// the weight bytes from the TMA plus one arrival from the group.  The
+// normalised matrix is never written to global memory.
+template <int BN, int STAGES, bool GLU, class Epi, int BMA = BM, int MINB = 1, bool NORMA = false>
 __global__ void __launch_bounds__(THREADS, MINB)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3, int M, int N,
                    int K, AOperand ao, SplitK sk, Epi epi, int* status) {
-  using C = Cfg<BN, STAGES, BMA>;
+  using C = Cfg<BN, STAGES, BMA, NORMA>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* accum = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* hfull = accum + 1;  // NORMA: the fp32 rows of a stage have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(hfull + STAGES);
   constexpr int LDT = BN + 4;
   __shared__ int s_fail;
+  __shared__ float s_rs[NORMA ? BMA : 1];  // NORMA: 1 / RMS of each row of the tile
+  __shared__ int s_built[2];               // NORMA: k-blocks each converting group delivered
+  __shared__ int s_ok[2];                  // NORMA: a group's wait for its stage's rows succeeded
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, z = blockIdx.z;
@@ -438,10 +466,13 @@ __global__ void __launch_bounds__(THREADS, MINB)
   const long long budget = sk.budget > 0 ? sk.budget : kWaitBudget;
   const bool withhold = sk.withhold && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 
+  // bytes of a stage the full barrier counts (the weights only with NORMA)
+  constexpr unsigned kTx = NORMA ? C::B_BYTES : C::STAGE_BYTES;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], NORMA ? 2 : 1);
       mbar_init(&empty[s], 1);
+      if (NORMA) mbar_init(&hfull[s], 1);
     }
     mbar_init(accum, 1);
     s_fail = 0;
@@ -466,7 +497,7 @@ __global__ void __launch_bounds__(THREADS, MINB)
     for (int i = 0; i < pre; ++i) {
       unsigned char* sa = smem + i * C::STAGE_BYTES;
       const int kx = (kb0 + i) * BK;
-      mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+      mbar_arrive_expect_tx(&full[i], kTx);
       if (GLU) {
         tma_load_2d(sa + C::A_BYTES, &tmB, kx, nb0, &full[i]);
         tma_load_2d(sa + C::A_BYTES + C::B_BYTES / 2, &tmB3, kx, nb0, &full[i]);
@@ -489,8 +520,11 @@ __global__ void __launch_bounds__(THREADS, MINB)
         }
         unsigned char* sa = smem + s * C::STAGE_BYTES;
         const int kx = (kb0 + i) * BK;
-        if (i >= pre) mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-        if (withhold && i == 0) {
+        if (i >= pre) mbar_arrive_expect_tx(&full[s], kTx);
+        if (NORMA) {
+          mbar_arrive_expect_tx(&hfull[s], C::A_BYTES);
+          if (!(withhold && i == 0)) tma_load_2d(sa, &tmA, kx, m0, &hfull[s]);  // (injection: never sent)
+        } else if (withhold && i == 0) {
           // (injection: the stage's A bytes are expected, never requested)
         } else if (kb0 + i < ao.split_kb) {
           if (ao.pos3d)
@@ -534,6 +568,73 @@ __global__ void __launch_bounds__(THREADS, MINB)
     __syncwarp();
   } else {
     // ---- epilogue warps (128 threads)
+    if constexpr (NORMA) {
+      // 0. the A operand: 1 / RMS of the tile's rows, then the k-blocks
+      const int et = threadIdx.x - 64;
+      if (et < BMA) {
+        const int m = m0 + et;
+        float rs = 0.f;  // rows past M: zero rows
+        if (m < M) {
+          float tot = 0.f;
+          for (int p = 0; p < K / 64; ++p) tot += ao.nss[(size_t)p * ao.nss_ld + m];
+          rs = rsqrtf(tot / (float)K + ao.neps);
+        }
+        s_rs[et] = rs;
+      }
+      epi_bar();
+      // group grp converts k-blocks grp, grp + 2, ...: the stage's fp32 rows
+      // [BMA][64] (256 bytes each) become bf16 rows of 128 bytes, 16-byte
+      // chunks permuted by row % 8 (the layout a 128-byte-swizzled TMA copy
+      // writes), in place: 64 rows at a time, all of them read before any is
+      // written (row r's output lies over input rows r/2, read already)
+      const int grp = et >> 6, gt = et & 63, c16 = gt & 7;
+      int built = 0;
+      for (int i = grp; i < nkb; i += 2) {
+        const int s = i % STAGES;
+        if (gt == 0) s_ok[grp] = mbar_wait(&hfull[s], (i / STAGES) & 1, budget) ? 1 : 0;
+        half_bar(2 + grp);
+        if (!s_ok[grp]) {  // (the same for the whole group)
+          atomicExch(&s_fail, 1);
+          break;
+        }
+        const int col = (kb0 + i) * BK + c16 * 8;
+        const float4 g0 = *reinterpret_cast<const float4*>(ao.ng + col);
+        const float4 g1 = *reinterpret_cast<const float4*>(ao.ng + col + 4);
+        unsigned char* sa = smem + s * C::STAGE_BYTES;
+#pragma unroll 1
+        for (int rb = 0; rb < BMA; rb += 64) {
+          float4 hv[8][2];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = rb + (gt >> 3) + 8 * j;
+            const float* src = reinterpret_cast<const float*>(sa + r * 256 + c16 * 32);
+            hv[j][0] = *reinterpret_cast<const float4*>(src);
+            hv[j][1] = *reinterpret_cast<const float4*>(src + 4);
+          }
+          half_bar(2 + grp);  // the group's reads of these rows are done
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = rb + (gt >> 3) + 8 * j;
+            const float rs = s_rs[r];
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(hv[j][0].x * rs * g0.x, hv[j][0].y * rs * g0.y);
+            __nv_bfloat162 p1 = __floats2bfloat162_rn(hv[j][0].z * rs * g0.z, hv[j][0].w * rs * g0.w);
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(hv[j][1].x * rs * g1.x, hv[j][1].y * rs * g1.y);
+            __nv_bfloat162 p3 = __floats2bfloat162_rn(hv[j][1].z * rs * g1.z, hv[j][1].w * rs * g1.w);
+            uint4 pk;
+            pk.x = *reinterpret_cast<unsigned*>(&p0);
+            pk.y = *reinterpret_cast<unsigned*>(&p1);
+            pk.z = *reinterpret_cast<unsigned*>(&p2);
+            pk.w = *reinterpret_cast<unsigned*>(&p3);
+            *reinterpret_cast<uint4*>(sa + r * 128 + ((c16 ^ (r & 7)) << 4)) = pk;
+          }
+        }
+        fence_async_smem();
+        half_bar(2 + grp);
+        if (gt == 0) mbar_arrive(&full[s]);
+        ++built;
+      }
+      if (gt == 0) s_built[grp] = built;
+    }
     // 1. TMEM -> shared staging tile [BM][BN + 4] fp32 (thread <-> tile row,
     //    i.e. TMEM lane); the stage ring is free once every MMA has completed.
     const int q = warp & 3;
@@ -626,7 +727,16 @@ __global__ void __launch_bounds__(THREADS, MINB)
   if (s_fail && threadIdx.x == 0) {
     set_error(status, kErrTimeout);
     // give the copies still in flight a bounded time to land before leaving
-    for (int i = max(0, issued - STAGES); i < issued; ++i) mbar_wait(&full[i % STAGES], (i / STAGES) & 1, budget);
+    // (NORMA: the fp32 rows too, and the converting group's arrival on
+    // stages it never delivered is added, so that each such phase completes
+    // once its weight bytes land)
+    for (int i = max(0, issued - STAGES); i < issued; ++i) {
+      if (NORMA) {
+        mbar_wait(&hfull[i % STAGES], (i / STAGES) & 1, budget);
+        if ((i >> 1) >= s_built[i & 1]) mbar_arrive(&full[i % STAGES]);
+      }
+      mbar_wait(&full[i % STAGES], (i / STAGES) & 1, budget);
+    }
   }
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }

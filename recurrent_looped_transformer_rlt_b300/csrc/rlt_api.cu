@@ -209,6 +209,21 @@ int tmap_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, u
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? RLT_OK : RLT_ECUDA;
 }
+// 2-D map of an fp32 matrix [rows][cols] (row stride ld elements), box = 64
+// columns x box_rows rows, no swizzle (rows of 256 bytes in shared memory).
+int tmap_f32(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows) {
+  auto fn = tmap_encoder();
+  if (!fn) return RLT_ECUDA;
+  if (((uintptr_t)base & 15u) || (ld * 4) % 16) return RLT_EINVAL;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 4};
+  cuuint32_t box[2] = {(cuuint32_t)tc::BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RLT_OK : RLT_ECUDA;
+}
 // 3-D map of a bf16 tensor [rows][T][cols] (rows of T positions), box = 64
 // columns x 1 position x box_rows rows: one position of every row.
 int tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t T, uint64_t cols, uint32_t box_rows) {
@@ -261,22 +276,30 @@ struct AArg {
   int split = 0;
   int T3 = 0;
   const StepCtx* ctx = nullptr;
+  // A = bf16(RMSNorm(nh) * ng) built inside the projection (nh [M][K] fp32,
+  // nss its per-64-column sums of squares [K/64][M]); A above is then unused
+  const float* nh = nullptr;
+  const float* nss = nullptr;
+  const float* ng = nullptr;
+  float neps = 0.f;
 };
 
-template <int BN, int STAGES, bool GLU, class Epi, int BMA = tc::BM, int MINB = 1>
+template <int BN, int STAGES, bool GLU, class Epi, int BMA = tc::BM, int MINB = 1, bool NORMA = false>
 int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, const bf16* B3, int ldb, int N,
                    Epi epi, const TcScratch& sc, int split_req = 0) {
-  using C = tc::Cfg<BN, STAGES, BMA>;
+  using C = tc::Cfg<BN, STAGES, BMA, NORMA>;
   static_assert(MINB == 1 || MINB * (C::SMEM + 1024) <= 228 * 1024, "CTAs per SM");
+  static_assert(!NORMA || MINB == 1, "the RMSNorm operand is built in single-CTA instantiations");
   static PerDevice attr;  // the shared-memory attribute is per device
   if (attr.get([] {
-        return cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA, MINB>,
+        return cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA, MINB, NORMA>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) == cudaSuccess
                    ? 1
                    : -1;
       }) != 1)
     return RLT_ECUDA;
   if (M > BMA && BMA != tc::BM) return RLT_EINVAL;
+  if (NORMA != (a.nh != nullptr) || (NORMA && (M > BMA || K % 64 || a.A2 || a.T3 > 0))) return RLT_EINVAL;
   const int nout = GLU ? BN / 2 : BN;
   const int tiles_n = (N + nout - 1) / nout, tiles_m = (M + tc::BM - 1) / tc::BM;
   const int kb = (K + tc::BK - 1) / tc::BK;
@@ -303,7 +326,9 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   CUtensorMap ta, ta2, tb, tb3;
   int rc;
   const int k1 = a.A2 ? a.split : K;
-  if (a.T3 > 0) {
+  if (NORMA) {
+    if ((rc = tmap_f32(&ta, a.nh, M, K, K, BMA))) return rc;
+  } else if (a.T3 > 0) {
     if ((rc = tmap_bf16_3d(&ta, a.A, M, a.T3, a.lda, BMA))) return rc;
   } else if ((rc = tmap_bf16(&ta, a.A, M, k1, a.lda, BMA))) {
     return rc;
@@ -311,7 +336,7 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   if ((rc = tmap_bf16(&ta2, a.A2 ? a.A2 : a.A, M, a.A2 ? K - a.split : k1, a.A2 ? a.lda2 : a.lda, BMA))) return rc;
   if ((rc = tmap_bf16(&tb, B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
   if ((rc = tmap_bf16(&tb3, GLU ? B3 : B, N, K, ldb, GLU ? BN / 2 : BN))) return rc;
-  tc::AOperand ao{a.A2 ? a.split / tc::BK : kb, a.T3 > 0 ? 1 : 0, a.ctx};
+  tc::AOperand ao{a.A2 ? a.split / tc::BK : kb, a.T3 > 0 ? 1 : 0, a.ctx, a.nss, a.ng, a.neps, M};
   tc::SplitK sk{splits, kbps, sc.budget, sc.withhold};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_m, splits);
@@ -327,7 +352,7 @@ int gemm_tc_launch(cudaStream_t st, const AArg& a, int M, int K, const bf16* B, 
   at[1].val.clusterDim.z = splits;
   cfg.attrs = at;
   cfg.numAttrs = splits > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA, MINB>, ta, ta2, tb, tb3, M, N, K, ao, sk,
+  if (cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, STAGES, GLU, Epi, BMA, MINB, NORMA>, ta, ta2, tb, tb3, M, N, K, ao, sk,
                          epi, sc.status) != cudaSuccess)
     return RLT_ECUDA;
   g_launches++;
@@ -356,13 +381,18 @@ int gemm_bf16_tc(cudaStream_t st, const bf16* A, int lda, int M, int K, const bf
 //   0: (128, 64)  8 stages   1: (256, 64)  5 stages
 //   2: (128, 128) 6 stages   3: (256, 128) 4 stages
 //   4: (64, 64)   8 stages (not for RoPE tiles of heads wider than 64)
-template <int BN, int BMA>
+// (NORMA: the A area of a stage holds fp32 rows, twice the bf16 bytes)
+template <int BN, int BMA, bool NORMA = false>
 constexpr int deep_stages() {
-  return std::min(8, (200 * 1024) / ((BMA + BN) * tc::BK * 2));
+  return std::min(8, (200 * 1024) / (((NORMA ? 2 : 1) * BMA + BN) * tc::BK * 2));
 }
 struct DeepPlan {
   int cfg, splits;
 };
+// Whether a projection of M rows can take its RMSNorm operand from the fp32
+// rows directly (AArg::nh): the deep kernels (M <= 128), K in whole
+// 64-column sum-of-squares groups.
+inline bool norm_fusable(int M, int K) { return M > 0 && M <= tc::BM && K % 64 == 0; }
 // The tile width and K split with the most CTAs that are all resident at
 // once (one wave), fewer splits on ties; the widest tiles without a split
 // when no choice fits in one wave.  More CTAs stream more weight bytes at
@@ -400,23 +430,24 @@ DeepPlan deep_plan(const TcScratch& sc, int M, int N, int K, bool glu, bool allo
   }
   return best;
 }
-template <bool GLU, class Epi>
+template <int BN, int BMA, bool GLU, bool NORMA, class Epi>
+int deep_launch(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const bf16* W3, int ldw, int N, Epi epi,
+                const TcScratch& sc, int splits) {
+  return gemm_tc_launch<BN, deep_stages<BN, BMA, NORMA>(), GLU, Epi, BMA, 1, NORMA>(st, x, M, K, W, W3, ldw, N, epi,
+                                                                                     sc, splits);
+}
+template <bool GLU, class Epi, bool NORMA = false>
 int proj_deep(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const bf16* W3, int ldw, int N, Epi epi,
               const TcScratch& sc) {
   bool allow64 = true;  // RoPE pair tiles start on head boundaries: 64-wide tiles only for heads of <= 64
   if constexpr (tc::IsPairEpi<Epi>::value) allow64 = epi.hd <= 64;
   const DeepPlan p = deep_plan(sc, M, N, K, GLU, allow64);
   switch (p.cfg) {
-    case 4:
-      return gemm_tc_launch<64, deep_stages<64, 64>(), GLU, Epi, 64>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
-    case 0:
-      return gemm_tc_launch<128, deep_stages<128, 64>(), GLU, Epi, 64>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
-    case 1:
-      return gemm_tc_launch<256, deep_stages<256, 64>(), GLU, Epi, 64>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
-    case 2:
-      return gemm_tc_launch<128, deep_stages<128, 128>(), GLU, Epi>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
-    default:
-      return gemm_tc_launch<256, deep_stages<256, 128>(), GLU, Epi>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
+    case 4: return deep_launch<64, 64, GLU, NORMA>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
+    case 0: return deep_launch<128, 64, GLU, NORMA>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
+    case 1: return deep_launch<256, 64, GLU, NORMA>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
+    case 2: return deep_launch<128, 128, GLU, NORMA>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
+    default: return deep_launch<256, 128, GLU, NORMA>(st, x, M, K, W, W3, ldw, N, epi, sc, p.splits);
   }
 }
 // Co-resident clusters of each deep configuration for cluster sizes 1..8.
@@ -458,10 +489,15 @@ int deep_occupancy_all(rlt_model* m) {
 }
 // Projection of a batch of sequences (decoder step, rlt_linear): the deep
 // weight-streaming kernels up to 128 rows, 4 stages of 256-wide tiles beyond.
+// An RMSNorm operand (x.nh) is built inside the deep kernels (norm_fusable).
 template <bool GLU, class Epi>
 int proj_bf16(cudaStream_t st, const AArg& x, int M, int K, const bf16* W, const bf16* W3, int ldw, int N, Epi epi,
               const TcScratch& sc) {
   if (M <= 0 || N <= 0) return RLT_OK;
+  if (x.nh) {
+    if (!norm_fusable(M, K)) return RLT_EINVAL;
+    return proj_deep<GLU, Epi, true>(st, x, M, K, W, W3, ldw, N, epi, sc);
+  }
   if (M <= tc::BM) return proj_deep<GLU>(st, x, M, K, W, W3, ldw, N, epi, sc);
   // hundreds of sequences (tensor-core bound): 128 x 128 tiles two per SM, or
   // 128 x 64 tiles where the wider ones would leave SMs without a tile
@@ -551,7 +587,9 @@ int swiglu_proj(cudaStream_t st, const T_* A, int lda, int M, int K, const T_* W
 // sums of squares.
 int norm_rows(cudaStream_t st, const float* h, const float* ss, const float* g, bf16* x, int rows, int d, float eps) {
   g_launches++;
-  return launch_pdl(norm_rows_kernel, dim3(rows), dim3(d / 4), 0, st, h, ss, g, x, rows, d, eps);
+  if (rows > 1024)
+    return launch_pdl(norm_rows_kernel<true>, dim3(rows), dim3(d / 4), 0, st, h, ss, g, x, rows, d, eps);
+  return launch_pdl(norm_rows_kernel<false>, dim3(rows), dim3(d / 4), 0, st, h, ss, g, x, rows, d, eps);
 }
 
 // Causal self-attention of the bf16 encoder: the flash kernel on the tensor
@@ -1071,12 +1109,23 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, a, B, 2 * d, static_cast<const bf16*>(w.W_g), nullptr, 2 * d, d, em, sc)))) return rc;
   }
-  auto norm = [&](const float* g) -> int {  // x = bf16(RMSNorm(h) * g)
-    int r = norm_rows(st, h, ss, g, x, B, d, c.rms_eps);
+  // x = bf16(RMSNorm(h) * g) as the input of the next projection: built
+  // inside that projection's kernel where it can (the same values, one
+  // launch fewer), else by the RMSNorm kernel into x
+  const bool fuse_norm = norm_fusable(B, d);
+  auto normed = [&](const float* g, AArg* a) -> int {
+    *a = act(x, d);
+    if (fuse_norm) {
+      a->nh = h;
+      a->nss = ss;
+      a->ng = g;
+      a->neps = c.rms_eps;
+      return RLT_OK;
+    }
     nk++;
-    return r;
+    return norm_rows(st, h, ss, g, x, B, d, c.rms_eps);
   };
-  if ((rc = norm(w.dec_attn_norm))) return rc;
+  AArg xn;
   const size_t ring_layer = (size_t)B * H * Wn * hd;
   const size_t plane = (size_t)B * H * A.T_mem * hd;
   bf16* rk = static_cast<bf16*>(sst->ring_k);
@@ -1096,8 +1145,15 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     // self-attention over the window
     const bf16* Wqkv = wl<bf16>(w.W_qkv, l, (size_t)3 * d * d);
     EpiQKVRope<bf16> eq{C, rk + l * ring_layer, rv + l * ring_layer, tab, ctx, d, H, hd, Wn};
+    if ((rc = normed(w.dec_attn_norm + ld, &xn))) return rc;
+    TcScratch sq = sc;
+    if (l == 0 && fuse_norm && m->inject_kernel == RLT_KERNEL_NORM_PROJ) {  // one-shot (rlt_debug_withhold_copy)
+      sq.budget = m->inject_budget;
+      sq.withhold = 1;
+      m->inject_kernel = 0;
+    }
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, Wqkv, nullptr, d, 3 * d, eq, sc)))) return rc;
+    if ((rc = gemm_done(proj_bf16<false>(st, xn, B, d, Wqkv, nullptr, d, 3 * d, eq, sq)))) return rc;
     if ((rc = mark(RLT_TIMER_SWA))) return rc;
     {
       XattnArgs sa = xa;
@@ -1114,10 +1170,10 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     if ((rc = gemm_done(proj_bf16<false>(st, act(o, d), B, d, wl<bf16>(w.W_O, l, (size_t)d * d), nullptr, d, d,
                                          EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc))))
       return rc;
-    if ((rc = norm(w.dec_xattn_norm + ld))) return rc;
     // cross-attention to memory positions 0..p
+    if ((rc = normed(w.dec_xattn_norm + ld, &xn))) return rc;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, wl<bf16>(w.W_Qx, l, (size_t)d * d), nullptr, d, d,
+    if ((rc = gemm_done(proj_bf16<false>(st, xn, B, d, wl<bf16>(w.W_Qx, l, (size_t)d * d), nullptr, d, d,
                                          EpiStoreF32{C, d}, sc))))
       return rc;
     const int g = (c.mem_groups == 1) ? 0 : l;
@@ -1137,10 +1193,10 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     if ((rc = gemm_done(proj_bf16<false>(st, act(o, d), B, d, wl<bf16>(w.W_Ox, l, (size_t)d * d), nullptr, d, d,
                                          EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc))))
       return rc;
-    if ((rc = norm(w.dec_ffn_norm + ld))) return rc;
     // SwiGLU FFN
+    if ((rc = normed(w.dec_ffn_norm + ld, &xn))) return rc;
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-    if ((rc = gemm_done(proj_bf16<true>(st, act(x, d), B, d, wl<bf16>(w.W_1, l, (size_t)f * d),
+    if ((rc = gemm_done(proj_bf16<true>(st, xn, B, d, wl<bf16>(w.W_1, l, (size_t)f * d),
                                         wl<bf16>(w.W_3, l, (size_t)f * d), d, f, EpiStoreT<bf16>{xm, f}, sc))))
       return rc;
     const bool last = (l + 1 == L);
@@ -1148,12 +1204,12 @@ int enqueue_step_bf16(const rlt_model* m, rlt_state* sst, const DecodeArgs& A, v
     if ((rc = mark(RLT_TIMER_GEMM))) return rc;
     if ((rc = gemm_done(proj_bf16<false>(st, act(xm, f), B, f, wl<bf16>(w.W_2, l, (size_t)d * f), nullptr, f, d, EpiResidual{ho}, sc))))
       return rc;
-    if ((rc = norm(last ? w.head_norm : w.dec_attn_norm + ld + d))) return rc;
   }
   // head: logits = W_o x with x = bf16(RMSNorm_o(s_t))
   if ((rc = mark(RLT_TIMER_HEAD))) return rc;
+  if ((rc = normed(w.head_norm, &xn))) return rc;
   if ((rc = mark(RLT_TIMER_GEMM))) return rc;
-  if ((rc = gemm_done(proj_bf16<false>(st, act(x, d), B, d, static_cast<const bf16*>(w.W_o), nullptr, d, V, EpiStoreF32{C, V}, sc))))
+  if ((rc = gemm_done(proj_bf16<false>(st, xn, B, d, static_cast<const bf16*>(w.W_o), nullptr, d, V, EpiStoreF32{C, V}, sc))))
     return rc;
   HeadArgs ha;
   ha.logits = C;
@@ -2148,10 +2204,10 @@ int rlt_linear(const rlt_model* m, const void* A, int32_t lda, int32_t M, int32_
 }
 
 int rlt_debug_withhold_copy(rlt_model* m, int32_t kernel, int64_t budget_cycles) {
-  if (!m || (kernel != RLT_KERNEL_XATTN && kernel != RLT_KERNEL_GEMM) || budget_cycles < 1000 ||
-      budget_cycles > 4000000000LL)
+  if (!m || (kernel != RLT_KERNEL_XATTN && kernel != RLT_KERNEL_GEMM && kernel != RLT_KERNEL_NORM_PROJ) ||
+      budget_cycles < 1000 || budget_cycles > 4000000000LL)
     return RLT_EINVAL;
-  if (kernel == RLT_KERNEL_GEMM && m->cfg.dtype != RLT_BF16) return RLT_EUNSUPPORTED;
+  if (kernel != RLT_KERNEL_XATTN && m->cfg.dtype != RLT_BF16) return RLT_EUNSUPPORTED;
   m->inject_budget = budget_cycles;
   m->inject_kernel = kernel;
   return RLT_OK;

@@ -119,3 +119,44 @@ def test_injection_arms_only_the_named_kernel():
     rlt.rlt_cross_attention(model.handle, q, mk, mv, B, T_mem, T_mem, out, ws, ws.numel())
     assert rlt.rlt_status(ws) == rlt.RLT_ETIMEOUT
     model.close()
+
+
+def test_decoder_norm_projection_wait_gives_up_and_reports_a_timeout():
+    """The decoder's projections build their RMSNorm input in the kernel: the
+    fp32 rows of a k-block land on their own barrier, a group of the
+    epilogue warps converts them and adds its arrival to the stage.  With
+    those rows never requested (layer-0 QKV projection of one step), the
+    group and then the MMA give up, the launch drains and frees its tensor
+    memory, the step reports RLT_ETIMEOUT, and the next call from the same
+    starting state is bitwise the uninjected one."""
+    import recurrent_looped_transformer_rlt_b300 as rlt
+    from recurrent_looped_transformer_rlt_b300 import runner
+    wl = ri.preset("small", n_layers=2, mem_groups=2)
+    c = wl.cfg
+    model = rlt.Model(c, ri.make_weights(c, wl.seed))
+    B, T = 8, 16
+    tok = ri.make_tokens(wl, B=B, T=T)
+    buf = runner.alloc_buffers(model, B, T)
+    runner.encode(model, torch.from_numpy(tok).cuda(), buf)
+    acts = torch.from_numpy(ri.teacher_actions(tok, 0, T)).cuda()
+    st0 = runner.new_state(model, B)
+    runner.decode(model, st0, buf, 3, acts[:, :3].contiguous())
+    assert runner.status(buf) == rlt.RLT_OK
+
+    def step(st):
+        return runner.decode(model, st, buf, 1, acts[:, 3:4].contiguous())
+
+    st_ref = st0.clone()
+    ref = step(st_ref)
+    assert runner.status(buf) == rlt.RLT_OK
+    rlt.rlt_debug_withhold_copy(model.handle, rlt.RLT_KERNEL_NORM_PROJ, BUDGET)
+    t0 = time.perf_counter()
+    step(st0.clone())
+    assert runner.status(buf) == rlt.RLT_ETIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    assert runner.status(buf) == rlt.RLT_OK        # reading clears it
+    st1 = st0.clone()
+    again = step(st1)                              # one-shot: the next call is whole again
+    assert runner.status(buf) == rlt.RLT_OK
+    assert torch.equal(again.logp, ref.logp) and torch.equal(st1.s, st_ref.s)
+    model.close()

@@ -116,6 +116,7 @@ def test_withhold_copy_rejects_bad_arguments_without_gpu():
     assert rlt.rlt_debug_withhold_copy(None, rlt.RLT_KERNEL_XATTN, 10 ** 6, check=False) == rlt.RLT_EINVAL
     fake = ctypes.c_void_p(16)
     assert rlt._debug_withhold_copy(fake, 0, 10 ** 6) == rlt.RLT_EINVAL
-    assert rlt._debug_withhold_copy(fake, 3, 10 ** 6) == rlt.RLT_EINVAL
+    assert rlt._debug_withhold_copy(fake, 4, 10 ** 6) == rlt.RLT_EINVAL
+    assert rlt._debug_withhold_copy(fake, rlt.RLT_KERNEL_NORM_PROJ, 999) == rlt.RLT_EINVAL
     assert rlt._debug_withhold_copy(fake, rlt.RLT_KERNEL_XATTN, 999) == rlt.RLT_EINVAL
     assert rlt._debug_withhold_copy(fake, rlt.RLT_KERNEL_GEMM, 4 * 10 ** 9 + 1) == rlt.RLT_EINVAL
