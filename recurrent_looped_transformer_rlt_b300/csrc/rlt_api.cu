@@ -1290,6 +1290,19 @@ int enqueue_enc_step_bf16(const rlt_model* m, int B, int T_max, bf16* e, bf16* m
     nk++;
     return norm_rows(st, h, ss, g, out, B, d, c.rms_eps);
   };
+  // the input of the next projection: bf16(RMSNorm(h) * g) built inside it
+  // where it can (as in the decoder step), else by the RMSNorm kernel into x
+  const bool fuse_norm = norm_fusable(B, d);
+  auto normed = [&](const float* g, AArg* a) -> int {
+    *a = act(x, d);
+    if (!fuse_norm) return norm(g, x);
+    a->nh = h;
+    a->nss = ss;
+    a->ng = g;
+    a->neps = c.rms_eps;
+    return RLT_OK;
+  };
+  AArg xn = act(x, d);  // layer 0: the embedding kernel's normalised rows
   embed_norm_kernel<<<B, d / 4, 0, st>>>(tok, static_cast<const bf16*>(w.tok_emb), h, x, w.enc_attn_norm, B, d,
                                          c.vocab, c.rms_eps, status);
   g_launches++;
@@ -1310,8 +1323,7 @@ int enqueue_enc_step_bf16(const rlt_model* m, int B, int T_max, bf16* e, bf16* m
     bf16* vc = enc_kv + (2 * l + 1) * kvp;
     // q, k with RoPE at p; k, v appended at cache slot p
     EpiQKVRope<bf16> eq{C, kc, vc, tab, ctx, d, H, hd, T_max};
-    if ((rc = proj_bf16<false>(st, act(x, d), B, d, wl<bf16>(w.W_qkv, l, (size_t)3 * d * d), nullptr, d, 3 * d, eq,
-                               sc)))
+    if ((rc = proj_bf16<false>(st, xn, B, d, wl<bf16>(w.W_qkv, l, (size_t)3 * d * d), nullptr, d, 3 * d, eq, sc)))
       return rc;
     nk++;
     XattnArgs sa = xa;
@@ -1328,9 +1340,9 @@ int enqueue_enc_step_bf16(const rlt_model* m, int B, int T_max, bf16* e, bf16* m
                                EpiResidual{HOut{h, d, nullptr, nullptr, ss, B}}, sc)))
       return rc;
     nk++;
-    if ((rc = norm(w.enc_ffn_norm + (size_t)l * d, x))) return rc;
-    if ((rc = proj_bf16<true>(st, act(x, d), B, d, wl<bf16>(w.W_1, l, (size_t)f * d), wl<bf16>(w.W_3, l, (size_t)f * d),
-                              d, f, EpiStoreT<bf16>{xm, f}, sc)))
+    if ((rc = normed(w.enc_ffn_norm + (size_t)l * d, &xn))) return rc;
+    if ((rc = proj_bf16<true>(st, xn, B, d, wl<bf16>(w.W_1, l, (size_t)f * d), wl<bf16>(w.W_3, l, (size_t)f * d), d, f,
+                              EpiStoreT<bf16>{xm, f}, sc)))
       return rc;
     nk++;
     if ((rc = proj_bf16<false>(st, act(xm, f), B, f, wl<bf16>(w.W_2, l, (size_t)d * f), nullptr, f, d,
@@ -1341,7 +1353,7 @@ int enqueue_enc_step_bf16(const rlt_model* m, int B, int T_max, bf16* e, bf16* m
       if ((rc = norm(w.enc_norm, o))) return rc;
       if ((rc = mem_rows(o, l))) return rc;
     }
-    if (l + 1 < L && (rc = norm(w.enc_attn_norm + (size_t)(l + 1) * d, x))) return rc;
+    if (l + 1 < L && (rc = normed(w.enc_attn_norm + (size_t)(l + 1) * d, &xn))) return rc;
   }
   // e_p = RMSNorm_e(h), then the memory rows of p
   if ((rc = norm(w.enc_norm, x))) return rc;
