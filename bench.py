@@ -660,11 +660,19 @@ def run_fused_case(args):
     call), timed with CUDA events over --steps calls after --warmup; one JSON
     line with the call's algorithmic bytes and its fraction of HBM
     bandwidth.  Case "fused": the persistent cluster decoder (one launch, for
-    ncu captures); case "decode": the path --decode-path names."""
+    ncu captures); case "decode": the path --decode-path names.  For small
+    profiler captures of one kernel at the workload's widths, --case-layers
+    L and --case-T T build an L-layer model (one memory group) over T
+    positions instead of the workload's."""
     import torch
     import recurrent_looped_transformer_rlt_b300 as rlt
     from recurrent_looped_transformer_rlt_b300 import runner
-    wl = ri.preset(args.workload)
+    over = {}
+    if args.case_layers:
+        over.update(n_layers=args.case_layers, mem_groups=1)
+    if args.case_T:
+        over.update(T=args.case_T)
+    wl = ri.preset(args.workload, **over)
     c, B, T = wl.cfg, wl.B, wl.T
     n = args.bptt_steps or 32
     p0 = args.case_pos if args.case_pos >= 0 else max(0, T // 2 - n // 2)
@@ -915,7 +923,9 @@ def main():
                     help="steps of the bptt case (default: T / 4) and of the fused / decode cases (default: 32)")
     ap.add_argument("--case-pos", type=int, default=-1,
                     help="first position of the fused / decode cases (default: T/2 - steps/2)")
-    ap.add_argument("--case-layers", type=int, default=0, help="layers of the encode case (default 1)")
+    ap.add_argument("--case-layers", type=int, default=0,
+                    help="layers of the encode case (default 1), or of the decode case (default: the workload's)")
+    ap.add_argument("--case-T", type=int, default=0, help="positions of the decode case (default: the workload's)")
     ap.add_argument("--case-batch", type=int, default=0, help="sequences of the encode case (default: the workload's)")
     ap.add_argument("--case-synthetic-state", action="store_true",
                     help="fused / decode cases: start from a seeded random state at --case-pos instead of "

@@ -88,35 +88,20 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, const bf16* __res
 // projection before it - has completed.  A projection after a norm thereby
 // streams its first weights while the projection before the norm drains and
 // the norm runs (its CTAs take the SMs the earlier projection frees).
-// SHARED: one thread sums the row's partials and shares the scale (many
-// rows: the encoder, where every thread reading all partials costs more
-// than the barrier); otherwise every thread sums them itself (a decoder
-// step's few rows, where the barrier would lengthen a latency chain).  The
-// partials are summed in the same order either way.
-template <bool SHARED>
 __global__ void norm_rows_kernel(const float* __restrict__ h, const float* __restrict__ ss, const float* __restrict__ g,
                                  bf16* __restrict__ xo, int rows, int d, float eps) {
   if (threadIdx.x == 0) pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x, c = threadIdx.x * 4;
-  if (r >= rows) return;  // (uniform per block)
+  if (r >= rows) return;
+  // every thread sums the row's partials itself (L1 hits after the first;
+  // one thread summing them for the block behind a barrier was measured
+  // slower: 1.25 -> 2.0 ms per launch at 262144 rows)
+  float tot = 0.f;
+  for (int p = 0; p < d / 64; ++p) tot += ss[(size_t)p * rows + r];
+  const float rs = rsqrtf(tot / (float)d + eps);
   const float4 v = *reinterpret_cast<const float4*>(h + (size_t)r * d + c);
   const float4 gg = *reinterpret_cast<const float4*>(g + c);
-  float rs;
-  if constexpr (SHARED) {
-    __shared__ float s_rs;
-    if (threadIdx.x == 0) {  // while the other threads' loads land
-      float tot = 0.f;
-      for (int p = 0; p < d / 64; ++p) tot += ss[(size_t)p * rows + r];
-      s_rs = rsqrtf(tot / (float)d + eps);
-    }
-    __syncthreads();
-    rs = s_rs;
-  } else {
-    float tot = 0.f;
-    for (int p = 0; p < d / 64; ++p) tot += ss[(size_t)p * rows + r];
-    rs = rsqrtf(tot / (float)d + eps);
-  }
   __nv_bfloat162 x01 = __floats2bfloat162_rn(v.x * rs * gg.x, v.y * rs * gg.y);
   __nv_bfloat162 x23 = __floats2bfloat162_rn(v.z * rs * gg.z, v.w * rs * gg.w);
   uint2 xp;

@@ -587,9 +587,7 @@ int swiglu_proj(cudaStream_t st, const T_* A, int lda, int M, int K, const T_* W
 // sums of squares.
 int norm_rows(cudaStream_t st, const float* h, const float* ss, const float* g, bf16* x, int rows, int d, float eps) {
   g_launches++;
-  if (rows > 1024)
-    return launch_pdl(norm_rows_kernel<true>, dim3(rows), dim3(d / 4), 0, st, h, ss, g, x, rows, d, eps);
-  return launch_pdl(norm_rows_kernel<false>, dim3(rows), dim3(d / 4), 0, st, h, ss, g, x, rows, d, eps);
+  return launch_pdl(norm_rows_kernel, dim3(rows), dim3(d / 4), 0, st, h, ss, g, x, rows, d, eps);
 }
 
 // Causal self-attention of the bf16 encoder: the flash kernel on the tensor
