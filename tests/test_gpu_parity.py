@@ -198,6 +198,9 @@ def test_small_bf16_full_size_sampled_rows():
     # the replay shape at its full batch (M = 1024 rows per projection: the
     # tensor-core-bound plan), the oracle on four sampled sequences
     ("rlreplay", 1024, 72, [0, 63, 64, 71], dict(temperature=0.7, top_k=50), [0, 341, 682, 1023]),
+    # 100 sequences: 128-row A tiles of which 28 rows are past the batch, the
+    # RMSNorm operand built in the projections over both 64-row halves
+    ("medium", 100, 40, [0, 39], {}, [0, 63, 64, 99]),
 ])
 def test_large_configs_transition_parity(name, B, T, t0s, kw, rows):
     wl, W, tok, acts = _inputs(name, B=B, T=T, jitter=0.0)
