@@ -429,6 +429,8 @@ RLT_API int rlt_bptt(const rlt_model* m, const void* e, const void* mem, int32_t
  *                     CTA never requests the fp32 rows of its first k-block,
  *                     so the group converting them and then the MMA give up;
  *                     every step of that call repeats it (call with n = 1);
+ *                     calls that build no such projection (fp32 models,
+ *                     more than 128 sequences) leave it armed;
  * and gives every wait of that launch budget_cycles clock cycles (1e3 ..
  * 4e9) instead of the default.  The launch's output is then unspecified and
  * rlt_status() of its workspace returns RLT_ETIMEOUT; later launches are not
