@@ -1720,8 +1720,8 @@ int validate_cfg(const rlt_config* c) {
   if (c->head_dim % 8 != 0 || 128 % c->head_dim != 0) return RLT_EUNSUPPORTED;
   // bf16 rows are moved in 16-byte pieces
   if (c->dtype == RLT_BF16 && (c->d_model % 8 != 0 || c->d_ffn % 8 != 0)) return RLT_EUNSUPPORTED;
-  // bf16 models: the residual stream is produced in 256-column tiles and the
-  // deferred RMSNorm keeps one sum of squares per 128 columns
+  // bf16 models: the residual stream is produced in tiles of up to 256
+  // columns and the deferred RMSNorm keeps one sum of squares per 64 columns
   if (c->dtype == RLT_BF16 && c->d_model % 256 != 0) return RLT_EUNSUPPORTED;
   if (c->vocab > 49152) return RLT_EUNSUPPORTED;
   if (c->window > 4096) return RLT_EUNSUPPORTED;
